@@ -1,0 +1,378 @@
+#!/usr/bin/env python
+"""Benchmark of one training step of the group-shared fixed fan-in sparse
+output layer (forward Z_k = H_k W_k^T, fused BCE gradient, dW_k and the
+Split-K feature gradient dh) on synthetic data shaped like the Amazon-3M tail.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` = label-logits per second (B*L per s,
+summed over ranks) with inputs resident in HBM; `e2e` = the same through the
+public API from pinned host buffers (h and positives copied in, loss copied out
+every step); `roofline` = the dominant kernel's algorithmic bytes / its mean
+launch time (CUDA events on its own stream) against the measured HBM peak;
+`cpu_baseline` = the CPU oracle on a bounded sample of the same workload.
+`--impl reference` times that oracle alone (there is no other implementation
+of the method to run).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from workloads import CONFIGS, generate  # noqa: E402
+
+METRIC = "fwd+bwd label-logits/s (B·L per s) and % of BF16/HBM roofline on 1 GB300"
+UNIT = "label-logits/s"
+DEFAULT_WORKLOAD = "amazon3m_tail"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ------------------------------------------------------------------ work model
+def algorithmic(w, B, kind):
+    """(bytes, flops) one launch of `kind` must move / do at minimum.
+    bf16 W, dW, Z, dZ, h; uint16 idx; fp32 dh; positives as int32."""
+    L, K, F, H = w.L, w.K, w.F, w.H
+    W_b = L * F * 2
+    idx_b = K * F * 2
+    h_b = B * H * 2
+    dh_b = B * H * 4
+    z_b = B * L * 2
+    nnz_b = B * w.pos * 4 * 2
+    flops_gemm = 2 * B * L * F
+    if kind == "step":
+        return W_b + W_b + idx_b + h_b + dh_b + nnz_b, 3 * flops_gemm
+    if kind == "fwd":      # fused BCE: writes dZ
+        return W_b + idx_b + h_b + z_b + nnz_b, flops_gemm
+    if kind == "bce":
+        return z_b + z_b + nnz_b, 0
+    if kind == "dW":
+        return z_b + h_b + idx_b + W_b, flops_gemm
+    if kind == "dh":
+        return z_b + W_b + idx_b + dh_b, flops_gemm
+    return 0, 0
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in Path(self.path).read_text().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+            os.unlink(self.path)
+        except Exception:
+            return None
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample_step(p, ids, sol, n_groups):
+    """The CPU oracle's step (positives, forward, BCE, dW, dh) on the slots of
+    the first n_groups groups and every sample; returns seconds taken."""
+    import oracle
+    w = p.w
+    Ls = n_groups * w.G
+    t0 = time.perf_counter()
+    st, srp, ssl = oracle.pos_slots(p.pos_rowptr, p.pos_label, w.L, sol)
+    keep = ssl < Ls
+    srp2 = np.zeros_like(srp)
+    for b in range(len(srp) - 1):
+        srp2[b + 1] = srp2[b] + int(keep[srp[b]:srp[b + 1]].sum())
+    ssl2 = ssl[keep]
+    Z = oracle.forward(p.h, p.W[:Ls], ids[:n_groups], w.G)
+    dZ, loss = oracle.bce(Z, srp2, ssl2)
+    oracle.weight_grad(p.h, dZ, ids[:n_groups], w.G, w.F)
+    oracle.feature_grad(p.W[:Ls], dZ, ids[:n_groups], w.G, w.H)
+    return time.perf_counter() - t0
+
+
+def oracle_baseline(p, target_s: float):
+    """Time the oracle on a bounded sample sized to about target_s seconds."""
+    import oracle
+    w = p.w
+    st, sol, los, ids = oracle.layout_build(p.groups, p.idx, w.L, w.G, w.F, w.H)
+    if st != 0:
+        raise RuntimeError("oracle rejected the layout")
+    n = max(1, min(w.K, 4096 // max(1, w.G)))
+    t = oracle_sample_step(p, ids, sol, n)
+    n2 = int(min(w.K, max(1, n * target_s / max(t, 1e-3))))
+    if n2 > n:
+        n = n2
+        t = oracle_sample_step(p, ids, sol, n)
+    return dict(value=p.h.shape[0] * n * w.G / t, seconds=t, n_groups=n,
+                cores=oracle.num_threads(), ids=ids, sol=sol)
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = CONFIGS[args.workload]
+    p = generate(w)
+    calib = oracle_baseline(p, args.ref_step_seconds)
+    n = calib["n_groups"]
+    for _ in range(args.warmup):
+        oracle_sample_step(p, calib["ids"], calib["sol"], n)
+    times = [oracle_sample_step(p, calib["ids"], calib["sol"], n) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    value = w.B * n * w.G / t
+    sample = (f"first {n} of {w.K} groups ({n * w.G} of {w.L} labels), all {w.B} samples; "
+              "step = positives + forward + BCE + dW + dh in double")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "G": w.G, "F": w.F, "H": w.H},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": calib["cores"],
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import extreme_label_sparse_gb300 as sg
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    sg.build()
+    sg.load()
+    w = CONFIGS[args.workload]
+    # weak scaling: every rank owns one shard of w.L labels (its own groups,
+    # W rows and positives); dh and the loss are summed over the shards
+    p = generate(w.with_(seed=w.seed + rank))
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    h, W = bf(p.h), bf(p.W)
+    rowptr, labels = i32(p.pos_rowptr), i32(p.pos_label)
+    lay = sg.sg_layout_build(i32(p.groups), w.L, w.G, i32(p.idx.reshape(-1)), w.F, w.H,
+                             w.B, max(p.nnz, 1))
+    engine = {"auto": sg.SG_ENGINE_AUTO, "simt": sg.SG_ENGINE_SIMT, "tc": sg.SG_ENGINE_TC}[args.engine]
+    sg.sg_layout_set_engine(lay, engine)
+    dW = torch.empty((w.L, w.F), dtype=torch.int16, device=dev)
+    dh = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    loss = torch.zeros(1, dtype=torch.float64, device=dev)
+
+    def step(h_, rp_, lb_):
+        sg.sg_step(lay, h_, W, rp_, lb_, p.nnz, dW, dh, loss)
+        if world > 1:
+            dist.all_reduce(dh)
+            dist.all_reduce(loss)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step(h, rowptr, labels)
+    torch.cuda.synchronize()
+    if sg.sg_layout_status(lay) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---- device-timed region: inputs resident in HBM
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    sg.sg_timing_start(lay, 64 * args.steps)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(h, rowptr, labels)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    kinds = sg.sg_timing_stop(lay)
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * w.B * w.L / (ms * 1e-3)
+
+    # ---- end to end through the public API: host buffers, copies timed
+    h_host = torch.from_numpy(np.ascontiguousarray(p.h).view(np.int16)).pin_memory()
+    rp_host = torch.from_numpy(p.pos_rowptr.astype(np.int32)).pin_memory()
+    lb_host = torch.from_numpy(p.pos_label.astype(np.int32)).pin_memory()
+    loss_host = torch.zeros(1, dtype=torch.float64).pin_memory()
+    h_d, rp_d, lb_d = torch.empty_like(h), torch.empty_like(rowptr), torch.empty_like(labels)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        h_d.copy_(h_host, non_blocking=True)
+        rp_d.copy_(rp_host, non_blocking=True)
+        lb_d.copy_(lb_host, non_blocking=True)
+        step(h_d, rp_d, lb_d)
+        loss_host.copy_(loss, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    h2d = h_host.numel() * 2 + rp_host.numel() * 4 + lb_host.numel() * 4
+    if sg.sg_layout_status(lay) != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    # ---- roofline of the dominant kernel
+    hbm, tflops, peak_src = _peaks()
+    dom = max((k for k in kinds if kinds[k][1] > 0), key=lambda k: kinds[k][0])
+    dom_ms, dom_n = kinds[dom]
+    bytes_, flops = algorithmic(w, w.B, dom)
+    per_launch_s = dom_ms * 1e-3 / dom_n
+    achieved = bytes_ / per_launch_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None, "kernel": dom,
+                "peak_source": peak_src,
+                "launch_ms": per_launch_s * 1e3,
+                "tensor_tflops": flops / per_launch_s / 1e12 if flops else 0.0,
+                "tensor_frac_of_bf16_peak": (flops / per_launch_s / 1e12) / tflops if flops else 0.0,
+                "per_kind_ms_per_step": {k: v[0] / args.steps for k, v in kinds.items() if v[1]}}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        b = oracle_baseline(p, args.cpu_seconds)
+        cpu = {"value": b["value"], "unit": UNIT, "cores": b["cores"], "kind": "oracle",
+               "sample": (f"first {b['n_groups']} of {w.K} groups ({b['n_groups'] * w.G} labels), "
+                          f"all {w.B} samples; positives + forward + BCE + dW + dh in double, "
+                          f"{b['seconds']:.1f} s")}
+
+    launches = sum(v[1] for v in kinds.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "G": w.G, "F": w.F, "H": w.H,
+                   "nnz": p.nnz, "engine": args.engine,
+                   "l2": f"inputs larger than L2 (W {w.L * w.F * 2 / 1e6:.0f} MB read, dW written each step)",
+                   "parallelism": "single GPU" if world == 1 else f"{world} label shards, dh all-reduce"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * w.B * w.L / (ms_e2e * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 8},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    lay.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
+    ap.add_argument("--engine", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,556 @@
+// C-ABI entry points of the sg library: argument validation, the layout
+// handle, and dispatch to the tensor-core or CUDA-core engine.  The operations
+// themselves are defined in include/sg.h.
+#include "sg_internal.cuh"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+namespace {
+
+thread_local char g_err[512];
+
+// Makes the layout's device current for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess)
+            ok = false;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev)
+            cudaSetDevice(prev);
+    }
+};
+
+#define FAIL(code, ...)               \
+    do {                              \
+        sg_set_error(__VA_ARGS__);    \
+        return code;                  \
+    } while (0)
+
+sg_status check_call(const sg_layout *lo, int32_t B, const char *fn)
+{
+    if (!lo)
+        FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
+    if (B < 1)
+        FAIL(SG_ERR_INVALID, "%s: B must be >= 1 (got %d)", fn, B);
+    if (B > lo->max_B)
+        FAIL(SG_ERR_INVALID, "%s: B=%d exceeds the layout's max_B=%d", fn, B,
+             lo->max_B);
+    return SG_OK;
+}
+
+sg_status check_pos(const sg_layout *lo, const int32_t *rowptr,
+                    const int32_t *labels, int64_t nnz, const char *fn)
+{
+    if (!rowptr)
+        FAIL(SG_ERR_INVALID, "%s: pos_rowptr is NULL", fn);
+    if (nnz < 0)
+        FAIL(SG_ERR_INVALID, "%s: nnz must be >= 0", fn);
+    if (nnz > 0 && !labels)
+        FAIL(SG_ERR_INVALID, "%s: pos_label is NULL", fn);
+    if (nnz > lo->max_nnz)
+        FAIL(SG_ERR_INVALID, "%s: nnz=%lld exceeds the layout's max_nnz=%lld",
+             fn, (long long)nnz, (long long)lo->max_nnz);
+    return SG_OK;
+}
+
+#define REQUIRE(ptr, fn)                                                   \
+    do {                                                                   \
+        if (!(ptr))                                                        \
+            FAIL(SG_ERR_INVALID, "%s: %s is NULL", fn, #ptr);              \
+    } while (0)
+
+#define TRY(expr)                  \
+    do {                           \
+        sg_status rc_ = (expr);    \
+        if (rc_ != SG_OK)          \
+            return rc_;            \
+    } while (0)
+
+bool use_tc(const sg_layout *lo)
+{
+    if (lo->engine == SG_ENGINE_SIMT)
+        return false;
+    return lo->tc_ok;
+}
+
+void timer_release(sg_layout::Timer &t)
+{
+    if (t.ev) {
+        for (int i = 0; i < 2 * t.cap; ++i)
+            cudaEventDestroy(t.ev[i]);
+        delete[] t.ev;
+    }
+    delete[] t.kind;
+    t = sg_layout::Timer();
+}
+
+void free_layout(sg_layout *lo)
+{
+    if (!lo)
+        return;
+    timer_release(lo->timer);
+    void *bufs[] = {lo->slot_of_label, lo->label_of_slot, lo->idx_s, lo->hT,
+                    lo->gcount, lo->gptr, lo->gent, lo->tsorted, lo->tslots,
+                    lo->rowcnt, lo->loss_part, lo->status, lo->dZ_ws};
+    for (void *p : bufs)
+        if (p)
+            cudaFree(p);
+    delete lo;
+}
+
+template <typename T>
+sg_status dev_alloc(T **p, size_t n, const char *what)
+{
+    size_t bytes = n * sizeof(T);
+    if (bytes == 0)
+        bytes = sizeof(T);
+    if (cudaMalloc((void **)p, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        FAIL(SG_ERR_OOM, "sg_layout_build: cudaMalloc of %zu bytes for %s failed",
+             bytes, what);
+    }
+    return SG_OK;
+}
+
+sg_status ensure_dz_ws(sg_layout *lo)
+{
+    size_t need = (size_t)lo->max_B * (size_t)lo->L;
+    if (lo->dZ_ws && lo->dZ_ws_elems >= need)
+        return SG_OK;
+    if (lo->dZ_ws)
+        cudaFree(lo->dZ_ws);
+    lo->dZ_ws = nullptr;
+    if (cudaMalloc((void **)&lo->dZ_ws, need * 2) != cudaSuccess) {
+        cudaGetLastError();
+        FAIL(SG_ERR_OOM, "sg_step: cudaMalloc of %zu bytes of dZ scratch failed",
+             need * 2);
+    }
+    lo->dZ_ws_elems = need;
+    return SG_OK;
+}
+
+}  // namespace
+
+void sg_set_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+}
+
+extern "C" {
+
+const char *sg_last_error(void) { return g_err; }
+
+int32_t sg_abi_version(void) { return SG_ABI_VERSION; }
+
+const char *sg_status_string(int32_t s)
+{
+    switch (s) {
+    case SG_OK: return "SG_OK";
+    case SG_ERR_INVALID: return "SG_ERR_INVALID";
+    case SG_ERR_UNSUPPORTED: return "SG_ERR_UNSUPPORTED";
+    case SG_ERR_CUDA: return "SG_ERR_CUDA";
+    case SG_ERR_OOM: return "SG_ERR_OOM";
+    case SG_ERR_TIMEOUT: return "SG_ERR_TIMEOUT";
+    case SG_ERR_DATA: return "SG_ERR_DATA";
+    default: return "SG_ERR_UNKNOWN";
+    }
+}
+
+// ---------------------------------------------------------------- layout
+sg_status sg_layout_build(const int32_t *groups, int64_t L, int32_t G,
+                          const int32_t *idx, int32_t F, int32_t H,
+                          int32_t max_B, int64_t max_nnz, void *stream,
+                          sg_layout **out)
+{
+    const char *fn = "sg_layout_build";
+    if (!out)
+        FAIL(SG_ERR_INVALID, "%s: out is NULL", fn);
+    *out = nullptr;
+    REQUIRE(groups, fn);
+    REQUIRE(idx, fn);
+    if (L < 1 || G < 1 || F < 1 || H < 1 || max_B < 1 || max_nnz < 0)
+        FAIL(SG_ERR_INVALID, "%s: sizes must be positive (L=%lld G=%d F=%d H=%d "
+             "max_B=%d max_nnz=%lld)", fn, (long long)L, G, F, H, max_B,
+             (long long)max_nnz);
+    if (L % G != 0)
+        FAIL(SG_ERR_INVALID, "%s: L=%lld is not a multiple of G=%d", fn,
+             (long long)L, G);
+    if (F > H)
+        FAIL(SG_ERR_INVALID, "%s: F=%d exceeds H=%d", fn, F, H);
+    if (G > SG_MAX_G || F > SG_MAX_F || H > SG_MAX_H || max_B > SG_MAX_B)
+        FAIL(SG_ERR_UNSUPPORTED, "%s: outside the supported range (G<=%d, F<=%d, "
+             "H<=%d, max_B<=%d)", fn, SG_MAX_G, SG_MAX_F, SG_MAX_H, SG_MAX_B);
+    if (L > (int64_t)INT32_MAX || max_nnz > (int64_t)INT32_MAX)
+        FAIL(SG_ERR_UNSUPPORTED, "%s: L and max_nnz must fit in int32", fn);
+
+    sg_layout *lo = new (std::nothrow) sg_layout();
+    if (!lo)
+        FAIL(SG_ERR_OOM, "%s: host allocation failed", fn);
+    lo->L = L;
+    lo->G = G;
+    lo->K = L / G;
+    lo->F = F;
+    lo->H = H;
+    lo->max_B = max_B;
+    lo->max_nnz = max_nnz;
+    lo->ldB = (int32_t)(ceil_div(max_B, 8) * 8);
+    cudaStream_t st = (cudaStream_t)stream;
+
+    sg_status rc = SG_OK;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&lo->device) != cudaSuccess ||
+        cudaGetDeviceProperties(&prop, lo->device) != cudaSuccess) {
+        sg_set_error("%s: no usable CUDA device (%s)", fn,
+                     cudaGetErrorString(cudaGetLastError()));
+        delete lo;
+        return SG_ERR_CUDA;
+    }
+    lo->num_sms = prop.multiProcessorCount;
+    lo->loss_part_n = 8192;
+
+#define ALLOC(field, n)                                                    \
+    do {                                                                   \
+        rc = dev_alloc(&lo->field, (size_t)(n), #field);                   \
+        if (rc != SG_OK) {                                                 \
+            free_layout(lo);                                               \
+            return rc;                                                     \
+        }                                                                  \
+    } while (0)
+    ALLOC(slot_of_label, L);
+    ALLOC(label_of_slot, L);
+    ALLOC(idx_s, lo->K * F);
+    ALLOC(hT, (size_t)H * lo->ldB);
+    ALLOC(gcount, lo->K + 1);
+    ALLOC(gptr, lo->K + 1);
+    ALLOC(gent, max_nnz);
+    ALLOC(tsorted, max_nnz);
+    ALLOC(tslots, max_nnz);
+    ALLOC(rowcnt, max_B);
+    ALLOC(loss_part, lo->loss_part_n);
+    ALLOC(status, 1);
+#undef ALLOC
+    if (cudaMemsetAsync(lo->gcount, 0, sizeof(int32_t) * (lo->K + 1), st) != cudaSuccess ||
+        cudaMemsetAsync(lo->status, 0, sizeof(int32_t), st) != cudaSuccess ||
+        cudaMemsetAsync(lo->hT, 0, (size_t)H * lo->ldB * 2, st) != cudaSuccess) {
+        sg_set_error("%s: %s", fn, cudaGetErrorString(cudaGetLastError()));
+        free_layout(lo);
+        return SG_ERR_CUDA;
+    }
+    rc = sg_layout_kernels(lo, groups, idx, st);
+    if (rc != SG_OK) {
+        free_layout(lo);
+        return rc;
+    }
+    lo->tc_ok = tc_supported(lo);
+    *out = lo;
+    return SG_OK;
+}
+
+sg_status sg_layout_export(const sg_layout *lo, int32_t *slot_of_label,
+                           int32_t *label_of_slot, uint16_t *idx_sorted,
+                           void *stream)
+{
+    const char *fn = "sg_layout_export";
+    if (!lo)
+        FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
+    DeviceGuard dg(lo->device);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (slot_of_label)
+        SG_TRY_CUDA(cudaMemcpyAsync(slot_of_label, lo->slot_of_label, 4 * lo->L,
+                                    cudaMemcpyDeviceToDevice, st));
+    if (label_of_slot)
+        SG_TRY_CUDA(cudaMemcpyAsync(label_of_slot, lo->label_of_slot, 4 * lo->L,
+                                    cudaMemcpyDeviceToDevice, st));
+    if (idx_sorted)
+        SG_TRY_CUDA(cudaMemcpyAsync(idx_sorted, lo->idx_s, 2 * lo->K * lo->F,
+                                    cudaMemcpyDeviceToDevice, st));
+    SG_TRY_CUDA(cudaStreamSynchronize(st));
+    return SG_OK;
+}
+
+void sg_layout_free(sg_layout *lo)
+{
+    if (!lo)
+        return;
+    DeviceGuard dg(lo->device);
+    cudaDeviceSynchronize();
+    free_layout(lo);
+}
+
+sg_status sg_layout_set_engine(sg_layout *lo, int32_t engine)
+{
+    const char *fn = "sg_layout_set_engine";
+    if (!lo)
+        FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
+    if (engine != SG_ENGINE_AUTO && engine != SG_ENGINE_SIMT && engine != SG_ENGINE_TC)
+        FAIL(SG_ERR_INVALID, "%s: unknown engine %d", fn, engine);
+    if (engine == SG_ENGINE_TC && !lo->tc_ok)
+        FAIL(SG_ERR_UNSUPPORTED, "%s: the tensor-core engine needs G %% 16 == 0 and "
+             "F %% 16 == 0 (G=%d, F=%d)", fn, lo->G, lo->F);
+    lo->engine = engine;
+    return SG_OK;
+}
+
+sg_status sg_layout_info(const sg_layout *lo, int64_t *L, int32_t *G,
+                         int32_t *F, int32_t *H, int64_t *K)
+{
+    if (!lo)
+        FAIL(SG_ERR_INVALID, "sg_layout_info: layout is NULL");
+    if (L) *L = lo->L;
+    if (G) *G = lo->G;
+    if (F) *F = lo->F;
+    if (H) *H = lo->H;
+    if (K) *K = lo->K;
+    return SG_OK;
+}
+
+sg_status sg_layout_status(sg_layout *lo, int32_t *code, int32_t clear)
+{
+    const char *fn = "sg_layout_status";
+    if (!lo)
+        FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
+    REQUIRE(code, fn);
+    DeviceGuard dg(lo->device);
+    SG_TRY_CUDA(cudaDeviceSynchronize());
+    SG_TRY_CUDA(cudaMemcpy(code, lo->status, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    if (clear)
+        SG_TRY_CUDA(cudaMemset(lo->status, 0, sizeof(int32_t)));
+    SG_TRY_CUDA(cudaDeviceSynchronize());
+    return SG_OK;
+}
+
+// ---------------------------------------------------------------- positives
+sg_status sg_pos_export(sg_layout *lo, int32_t B, const int32_t *pos_rowptr,
+                        const int32_t *pos_label, int64_t nnz,
+                        int32_t *out_rowptr, int32_t *out_slots,
+                        int32_t *out_gptr, int32_t *out_gentry, void *stream)
+{
+    const char *fn = "sg_pos_export";
+    TRY(check_call(lo, B, fn));
+    TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
+    DeviceGuard dg(lo->device);
+    cudaStream_t st = (cudaStream_t)stream;
+    TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+    if (out_rowptr || out_slots) {
+        int32_t *orp = out_rowptr;
+        if (!orp)
+            FAIL(SG_ERR_INVALID, "%s: out_slots needs out_rowptr", fn);
+        TRY(sg_pos_compact(lo, B, pos_rowptr, orp, out_slots, st));
+    }
+    if (out_gptr)
+        SG_TRY_CUDA(cudaMemcpyAsync(out_gptr, lo->gptr, 4 * (lo->K + 1),
+                                    cudaMemcpyDeviceToDevice, st));
+    if (out_gentry && nnz > 0)
+        SG_TRY_CUDA(cudaMemcpyAsync(out_gentry, lo->gent, 4 * nnz,
+                                    cudaMemcpyDeviceToDevice, st));
+    return SG_OK;
+}
+
+// ---------------------------------------------------------------- forward
+sg_status sg_fwd(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
+                 sg_bf16 *Z, void *stream)
+{
+    const char *fn = "sg_fwd";
+    TRY(check_call(lo, B, fn));
+    REQUIRE(h, fn);
+    REQUIRE(W, fn);
+    REQUIRE(Z, fn);
+    DeviceGuard dg(lo->device);
+    cudaStream_t st = (cudaStream_t)stream;
+    TRY(simt_transpose_h(lo, h, B, st));
+    if (use_tc(lo))
+        return tc_fwd(lo, B, W, Z, nullptr, nullptr, st);
+    return simt_fwd(lo, B, W, Z, nullptr, nullptr, st);
+}
+
+sg_status sg_bce_grad(sg_layout *lo, const sg_bf16 *Z, int32_t B,
+                      const int32_t *pos_rowptr, const int32_t *pos_label,
+                      int64_t nnz, sg_bf16 *dZ, double *loss, void *stream)
+{
+    const char *fn = "sg_bce_grad";
+    TRY(check_call(lo, B, fn));
+    TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
+    REQUIRE(Z, fn);
+    REQUIRE(dZ, fn);
+    REQUIRE(loss, fn);
+    DeviceGuard dg(lo->device);
+    cudaStream_t st = (cudaStream_t)stream;
+    TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+    return simt_bce(lo, Z, B, dZ, loss, st);
+}
+
+sg_status sg_fwd_bce(sg_layout *lo, const sg_bf16 *h, int32_t B,
+                     const sg_bf16 *W, const int32_t *pos_rowptr,
+                     const int32_t *pos_label, int64_t nnz, sg_bf16 *dZ,
+                     double *loss, sg_bf16 *Z_or_null, void *stream)
+{
+    const char *fn = "sg_fwd_bce";
+    TRY(check_call(lo, B, fn));
+    TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
+    REQUIRE(h, fn);
+    REQUIRE(W, fn);
+    REQUIRE(dZ, fn);
+    REQUIRE(loss, fn);
+    DeviceGuard dg(lo->device);
+    cudaStream_t st = (cudaStream_t)stream;
+    TRY(simt_transpose_h(lo, h, B, st));
+    TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+    if (use_tc(lo))
+        return tc_fwd(lo, B, W, Z_or_null, dZ, loss, st);
+    return simt_fwd(lo, B, W, Z_or_null, dZ, loss, st);
+}
+
+// ---------------------------------------------------------------- backward
+sg_status sg_bwd_dW(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h,
+                    int32_t B, sg_bf16 *dW, void *stream)
+{
+    const char *fn = "sg_bwd_dW";
+    TRY(check_call(lo, B, fn));
+    REQUIRE(dZ, fn);
+    REQUIRE(h, fn);
+    REQUIRE(dW, fn);
+    DeviceGuard dg(lo->device);
+    cudaStream_t st = (cudaStream_t)stream;
+    TRY(simt_transpose_h(lo, h, B, st));
+    if (use_tc(lo))
+        return tc_dW(lo, dZ, B, dW, st);
+    return simt_dW(lo, dZ, B, dW, st);
+}
+
+sg_status sg_bwd_dh(sg_layout *lo, const sg_bf16 *dZ, int32_t B,
+                    const sg_bf16 *W, float *dh, void *stream)
+{
+    const char *fn = "sg_bwd_dh";
+    TRY(check_call(lo, B, fn));
+    REQUIRE(dZ, fn);
+    REQUIRE(W, fn);
+    REQUIRE(dh, fn);
+    DeviceGuard dg(lo->device);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (use_tc(lo))
+        return tc_dh(lo, dZ, B, W, dh, st);
+    return simt_dh(lo, dZ, B, W, dh, st);
+}
+
+sg_status sg_bwd(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h, int32_t B,
+                 const sg_bf16 *W, sg_bf16 *dW, float *dh, void *stream)
+{
+    const char *fn = "sg_bwd";
+    TRY(check_call(lo, B, fn));
+    REQUIRE(dZ, fn);
+    REQUIRE(h, fn);
+    REQUIRE(W, fn);
+    REQUIRE(dW, fn);
+    REQUIRE(dh, fn);
+    TRY(sg_bwd_dW(lo, dZ, h, B, dW, stream));
+    return sg_bwd_dh(lo, dZ, B, W, dh, stream);
+}
+
+// ---------------------------------------------------------------- step
+sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
+                  const int32_t *pos_rowptr, const int32_t *pos_label,
+                  int64_t nnz, sg_bf16 *dW, float *dh, double *loss,
+                  void *stream)
+{
+    const char *fn = "sg_step";
+    TRY(check_call(lo, B, fn));
+    TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
+    REQUIRE(h, fn);
+    REQUIRE(W, fn);
+    REQUIRE(dW, fn);
+    REQUIRE(dh, fn);
+    REQUIRE(loss, fn);
+    DeviceGuard dg(lo->device);
+    cudaStream_t st = (cudaStream_t)stream;
+    TRY(simt_transpose_h(lo, h, B, st));
+    TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+    if (use_tc(lo))
+        return tc_step(lo, B, W, dW, dh, loss, st);
+    // CUDA-core engine: forward + BCE into dZ scratch, then dW and dh
+    TRY(ensure_dz_ws(lo));
+    TRY(simt_fwd(lo, B, W, nullptr, lo->dZ_ws, loss, st));
+    TRY(simt_dW(lo, lo->dZ_ws, B, dW, st));
+    return simt_dh(lo, lo->dZ_ws, B, W, dh, st);
+}
+
+// ---------------------------------------------------------------- timing
+sg_status sg_timing_start(sg_layout *lo, int32_t capacity)
+{
+    const char *fn = "sg_timing_start";
+    if (!lo)
+        FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
+    if (capacity < 0 || capacity > (1 << 20))
+        FAIL(SG_ERR_INVALID, "%s: capacity %d out of range", fn, capacity);
+    DeviceGuard dg(lo->device);
+    sg_layout::Timer &t = lo->timer;
+    if (t.cap < capacity) {
+        timer_release(t);
+        t.ev = new (std::nothrow) cudaEvent_t[2 * (size_t)capacity];
+        t.kind = new (std::nothrow) int[capacity];
+        if (!t.ev || !t.kind) {
+            timer_release(t);
+            FAIL(SG_ERR_OOM, "%s: host allocation failed", fn);
+        }
+        for (int i = 0; i < 2 * capacity; ++i) {
+            if (cudaEventCreate(&t.ev[i]) != cudaSuccess) {
+                t.cap = i / 2;
+                for (int j = 2 * t.cap; j < i; ++j)
+                    cudaEventDestroy(t.ev[j]);
+                timer_release(t);
+                FAIL(SG_ERR_CUDA, "%s: cudaEventCreate failed", fn);
+            }
+        }
+        t.cap = capacity;
+    }
+    t.n = 0;
+    t.pending = false;
+    for (int i = 0; i < SG_KIND_COUNT; ++i)
+        t.counts[i] = 0;
+    t.on = true;
+    return SG_OK;
+}
+
+sg_status sg_timing_stop(sg_layout *lo, double *ms_per_kind,
+                         int32_t *launches_per_kind)
+{
+    const char *fn = "sg_timing_stop";
+    if (!lo)
+        FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
+    DeviceGuard dg(lo->device);
+    sg_layout::Timer &t = lo->timer;
+    t.on = false;
+    double ms[SG_KIND_COUNT] = {};
+    if (t.n > 0)
+        SG_TRY_CUDA(cudaEventSynchronize(t.ev[2 * t.n - 1]));
+    for (int i = 0; i < t.n; ++i) {
+        float e = 0.f;
+        SG_TRY_CUDA(cudaEventElapsedTime(&e, t.ev[2 * i], t.ev[2 * i + 1]));
+        ms[t.kind[i]] += e;
+    }
+    for (int k = 0; k < SG_KIND_COUNT; ++k) {
+        if (ms_per_kind)
+            ms_per_kind[k] = ms[k];
+        if (launches_per_kind)
+            launches_per_kind[k] = t.counts[k];
+    }
+    return SG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,221 @@
+// Positive-label preparation for one call: Y of the BCE objective (HASTE, key
+// design "head-tail split": sum of per-label BCE terms) as per-group lists, so
+// the forward epilogue of group k can read its few positives directly.
+//
+//   1. k_pos_rows  : one warp per sample: labels -> slots, sort, drop
+//                    duplicates (Y is binary), count positives per group.
+//   2. k_scan      : exclusive scan of the per-group counts -> gptr[K+1].
+//   3. k_pos_place : bucket the entries by group: gent[] = (b << 16) | j.
+//                    Placement counts the group counters back down to zero,
+//                    so they are ready for the next call without a memset.
+#include "sg_internal.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void k_pos_rows(int32_t B, const int32_t *__restrict__ rowptr,
+                           const int32_t *__restrict__ labels, int64_t nnz,
+                           int64_t L, int32_t G,
+                           const int32_t *__restrict__ slot_of_label,
+                           int32_t *tsorted, int32_t *tslots, int32_t *rowcnt,
+                           int32_t *gcount, int32_t *status)
+{
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (b >= B)
+        return;
+    if (b == 0 && lane == 0 && (rowptr[0] != 0 || (int64_t)rowptr[B] != nnz))
+        sg_flag(status, SG_ERR_DATA);
+    const int64_t r0 = rowptr[b], r1 = rowptr[b + 1];
+    if (r0 < 0 || r1 < r0 || r1 > nnz) {
+        if (lane == 0) {
+            sg_flag(status, SG_ERR_DATA);
+            rowcnt[b] = 0;
+        }
+        return;
+    }
+    const int n = (int)(r1 - r0);
+    // pass 1: stable rank sort of the row's slots (invalid labels -> -1 first)
+    for (int i = lane; i < n; i += 32) {
+        int32_t lab = labels[r0 + i];
+        int32_t v;
+        if (lab < 0 || lab >= L) {
+            sg_flag(status, SG_ERR_DATA);
+            v = -1;
+        } else {
+            v = slot_of_label[lab];
+        }
+        int rank = 0;
+        for (int q = 0; q < n; ++q) {
+            int32_t lq = labels[r0 + q];
+            int32_t u = (lq < 0 || lq >= L) ? -1 : slot_of_label[lq];
+            rank += (u < v) | ((u == v) & (q < i));
+        }
+        tsorted[r0 + rank] = v;
+    }
+    __syncwarp();
+    __threadfence_block();
+    // pass 2: keep the first of each run of equal values, compact in order
+    int kept = 0;
+    for (int base = 0; base < n; base += 32) {
+        int p = base + lane;
+        int32_t v = p < n ? tsorted[r0 + p] : -1;
+        int32_t prev = (p > 0 && p <= n) ? tsorted[r0 + p - 1] : -1;
+        bool keep = p < n && v >= 0 && (p == 0 || v != prev);
+        unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+            int at = kept + __popc(m & ((1u << lane) - 1u));
+            tslots[r0 + at] = v;
+            atomicAdd(&gcount[v / G], 1);
+        }
+        kept += __popc(m);
+    }
+    if (lane == 0)
+        rowcnt[b] = kept;
+}
+
+// Single-block exclusive scan: out[i] = sum_{j<i} in[j], out[n] = total.
+__global__ void __launch_bounds__(1024) k_scan(const int32_t *__restrict__ in,
+                                               int64_t n, int32_t *out)
+{
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0)
+        carry_s = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < n; base += 1024) {
+        int64_t i = base + tid;
+        int32_t v = i < n ? in[i] : 0;
+        int32_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
+        }
+        if (lane == 31)
+            warp_sums[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int32_t w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o)
+                    w += y;
+            }
+            warp_sums[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        int32_t carry = carry_s;
+        int32_t excl = carry + (wid ? warp_sums[wid - 1] : 0) + x - v;
+        if (i < n)
+            out[i] = excl;
+        __syncthreads();
+        if (tid == 1023)
+            carry_s = excl + v;
+        __syncthreads();
+    }
+    if (tid == 0)
+        out[n] = carry_s;
+}
+
+__global__ void k_pos_place(int32_t B, const int32_t *__restrict__ rowptr,
+                            const int32_t *__restrict__ tslots,
+                            const int32_t *__restrict__ rowcnt, int32_t G,
+                            const int32_t *__restrict__ gptr, int32_t *gcount,
+                            int32_t *gent)
+{
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (b >= B)
+        return;
+    const int64_t r0 = rowptr[b];
+    const int n = rowcnt[b];
+    for (int c = lane; c < n; c += 32) {
+        int32_t v = tslots[r0 + c];
+        int32_t k = v / G;
+        int32_t pos = atomicSub(&gcount[k], 1) - 1;
+        gent[gptr[k] + pos] = (b << 16) | (v - k * G);
+    }
+}
+
+// canonical slot-CSR: compacted rows
+__global__ void k_pos_compact(int32_t B, const int32_t *__restrict__ rowptr,
+                              const int32_t *__restrict__ tslots,
+                              const int32_t *__restrict__ rowcnt,
+                              const int32_t *__restrict__ out_rowptr,
+                              int32_t *out_slots)
+{
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (b >= B)
+        return;
+    const int64_t r0 = rowptr[b];
+    const int n = rowcnt[b];
+    for (int c = lane; c < n; c += 32)
+        out_slots[out_rowptr[b] + c] = tslots[r0 + c];
+}
+
+__global__ void __launch_bounds__(1024) k_loss_finalize(const double *__restrict__ part,
+                                                        int n, double *loss)
+{
+    __shared__ double s[1024];
+    double acc = 0.0;
+    for (int i = threadIdx.x; i < n; i += 1024)
+        acc += part[i];
+    s[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 512; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w)
+            s[threadIdx.x] += s[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        *loss = s[0];
+}
+
+}  // namespace
+
+sg_status sg_pos_prepare(sg_layout *lo, int32_t B, const int32_t *rowptr,
+                         const int32_t *labels, int64_t nnz, cudaStream_t st)
+{
+    const int wpb = kThreads / 32;
+    const int rows_grid = (int)ceil_div(B, wpb);
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_pos_rows<<<rows_grid, kThreads, 0, st>>>(B, rowptr, labels, nnz, lo->L,
+                                               lo->G, lo->slot_of_label,
+                                               lo->tsorted, lo->tslots,
+                                               lo->rowcnt, lo->gcount,
+                                               lo->status));
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_scan<<<1, 1024, 0, st>>>(lo->gcount, lo->K, lo->gptr));
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_pos_place<<<rows_grid, kThreads, 0, st>>>(B, rowptr, lo->tslots,
+                                                lo->rowcnt, lo->G, lo->gptr,
+                                                lo->gcount, lo->gent));
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+sg_status sg_pos_compact(sg_layout *lo, int32_t B, const int32_t *rowptr,
+                         int32_t *out_rowptr, int32_t *out_slots,
+                         cudaStream_t st)
+{
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_scan<<<1, 1024, 0, st>>>(lo->rowcnt, B, out_rowptr));
+    if (out_slots) {
+        const int wpb = kThreads / 32;
+        SG_LAUNCH(lo, SG_KIND_PREP, st,
+                  k_pos_compact<<<(int)ceil_div(B, wpb), kThreads, 0, st>>>(
+                      B, rowptr, lo->tslots, lo->rowcnt, out_rowptr, out_slots));
+    }
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+sg_status sg_loss_finalize(sg_layout *lo, int32_t nparts, double *loss,
+                           cudaStream_t st)
+{
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_loss_finalize<<<1, 1024, 0, st>>>(lo->loss_part, nparts, loss));
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}

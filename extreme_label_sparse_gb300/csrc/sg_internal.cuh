@@ -1,0 +1,169 @@
+// Internal declarations of the sg library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sg.h"
+
+// ----------------------------------------------------------------- limits
+constexpr int SG_MAX_B = 256;
+constexpr int SG_MAX_F = 256;
+constexpr int SG_MAX_H = 1024;
+constexpr int SG_MAX_G = 256;
+
+// ----------------------------------------------------------------- layout
+struct sg_layout {
+    int64_t L = 0, K = 0;
+    int32_t G = 0, F = 0, H = 0, max_B = 0;
+    int64_t max_nnz = 0;
+    int32_t engine = SG_ENGINE_AUTO;
+    int32_t device = 0;
+    int32_t num_sms = 0;
+    bool tc_ok = false;  // the tensor-core engine can run this layout
+
+    // canonical layout (device)
+    int32_t *slot_of_label = nullptr;  // [L]
+    int32_t *label_of_slot = nullptr;  // [L]
+    uint16_t *idx_s = nullptr;         // [K][F] ascending
+
+    // per-call scratch (device)
+    uint16_t *hT = nullptr;  // [H][ldB] bf16, transposed h, zero padded
+    int32_t ldB = 0;         // roundup(max_B, 8)
+    int32_t *gcount = nullptr;  // [K+1], all zero between calls
+    int32_t *gptr = nullptr;    // [K+1]
+    int32_t *gent = nullptr;    // [max_nnz]  (b << 16) | j
+    int32_t *tsorted = nullptr; // [max_nnz]  per-row slots, sorted (with dups)
+    int32_t *tslots = nullptr;  // [max_nnz]  per-row slots, sorted, deduplicated
+    int32_t *rowcnt = nullptr;  // [max_B]    kept entries per row
+    double *loss_part = nullptr;
+    int32_t loss_part_n = 0;
+    int32_t *status = nullptr;  // sticky device status word
+
+    // dZ scratch of the composed step, allocated on first use
+    uint16_t *dZ_ws = nullptr;
+    size_t dZ_ws_elems = 0;
+
+    // per-kernel event timing (sg_timing_start / sg_timing_stop)
+    struct Timer {
+        bool on = false;
+        bool pending = false;
+        int cap = 0, n = 0;
+        cudaEvent_t *ev = nullptr;  // [2 * cap]
+        int *kind = nullptr;        // [cap]
+        int32_t counts[SG_KIND_COUNT] = {};
+    } timer;
+};
+
+// Bracket one kernel launch with timing events (no-op unless enabled).
+inline void sg_tick(sg_layout *lo, int kind, cudaStream_t st)
+{
+    sg_layout::Timer &t = lo->timer;
+    if (!t.on)
+        return;
+    t.counts[kind] += 1;
+    t.pending = t.n < t.cap;
+    if (t.pending) {
+        t.kind[t.n] = kind;
+        cudaEventRecord(t.ev[2 * t.n], st);
+    }
+}
+
+inline void sg_tock(sg_layout *lo, cudaStream_t st)
+{
+    sg_layout::Timer &t = lo->timer;
+    if (!t.on || !t.pending)
+        return;
+    cudaEventRecord(t.ev[2 * t.n + 1], st);
+    t.n += 1;
+    t.pending = false;
+}
+
+#define SG_LAUNCH(lo, kind, st, ...)   \
+    do {                               \
+        sg_tick((lo), (kind), (st));   \
+        __VA_ARGS__;                   \
+        sg_tock((lo), (st));           \
+    } while (0)
+
+// ----------------------------------------------------------------- errors
+void sg_set_error(const char *fmt, ...);
+#define SG_TRY_CUDA(expr)                                                   \
+    do {                                                                    \
+        cudaError_t e_ = (expr);                                            \
+        if (e_ != cudaSuccess) {                                            \
+            sg_set_error("%s failed: %s (%s:%d)", #expr,                    \
+                         cudaGetErrorString(e_), __FILE__, __LINE__);       \
+            return SG_ERR_CUDA;                                             \
+        }                                                                   \
+    } while (0)
+
+// First error wins: a later error never overwrites an earlier one.
+__device__ __forceinline__ void sg_flag(int32_t *status, int32_t code)
+{
+    atomicCAS(status, 0, code);
+}
+
+// ----------------------------------------------------------------- bf16
+__device__ __forceinline__ float bf2f(uint16_t v)
+{
+    return __uint_as_float(((uint32_t)v) << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs; NaN kept quiet)
+__device__ __forceinline__ uint16_t f2bf(float x)
+{
+    uint32_t u = __float_as_uint(x);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu))
+        return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+// ----------------------------------------------------------------- BCE
+// loss term max(z,0) - y z + log(1 + e^-|z|) and gradient sigmoid(z) - y,
+// in fp32 with CUDA's expf/log1pf.
+__device__ __forceinline__ float bce_grad_loss(float z, int y, float *loss)
+{
+    float e = expf(-fabsf(z));
+    float r = 1.0f / (1.0f + e);
+    float sig = z >= 0.f ? r : e * r;
+    *loss = fmaxf(z, 0.f) - (y ? z : 0.f) + log1pf(e);
+    return sig - (float)y;
+}
+
+// ----------------------------------------------------------------- launchers
+// layout.cu
+sg_status sg_layout_kernels(sg_layout *lo, const int32_t *groups,
+                            const int32_t *idx, cudaStream_t st);
+// pos.cu: build the per-group positive lists (gptr/gent) for one call
+sg_status sg_pos_prepare(sg_layout *lo, int32_t B, const int32_t *rowptr,
+                         const int32_t *labels, int64_t nnz, cudaStream_t st);
+sg_status sg_pos_compact(sg_layout *lo, int32_t B, const int32_t *rowptr,
+                         int32_t *out_rowptr, int32_t *out_slots,
+                         cudaStream_t st);
+sg_status sg_loss_finalize(sg_layout *lo, int32_t nparts, double *loss,
+                           cudaStream_t st);
+// simt.cu
+sg_status simt_transpose_h(sg_layout *lo, const uint16_t *h, int32_t B,
+                           cudaStream_t st);
+sg_status simt_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
+                   uint16_t *dZ, double *loss, cudaStream_t st);
+sg_status simt_bce(sg_layout *lo, const uint16_t *Z, int32_t B, uint16_t *dZ,
+                   double *loss, cudaStream_t st);
+sg_status simt_dW(sg_layout *lo, const uint16_t *dZ, int32_t B, uint16_t *dW,
+                  cudaStream_t st);
+sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, int32_t B,
+                  const uint16_t *W, float *dh, cudaStream_t st);
+// tc.cu
+bool tc_supported(const sg_layout *lo);
+sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
+                 uint16_t *dZ, double *loss, cudaStream_t st);
+sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, int32_t B, uint16_t *dW,
+                cudaStream_t st);
+sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, int32_t B,
+                const uint16_t *W, float *dh, cudaStream_t st);
+sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW,
+                  float *dh, double *loss, cudaStream_t st);
+
+static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

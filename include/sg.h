@@ -1,0 +1,230 @@
+/*
+ * sg.h -- C ABI of the group-shared fixed fan-in sparse output layer, one
+ * training step, on one GB300 (sm_103a).
+ *
+ * The layer (HASTE: Hardware-Aware Dynamic Sparse Training for Large Output
+ * Spaces -- "Method / overall framework" and key design "group-shared fixed
+ * fan-in sparsity"): L labels are split into K = L/G groups of G labels.  All
+ * labels of group k share one fan-in index set I_k of F feature dims; every
+ * label keeps its own F weights.  The logit of label l in group k is
+ *     z_l = < w_l , h[I_k] >                       (no bias)
+ * Per group this is the dense product Z_k = H_k W_k^T with H_k = h[:, I_k]
+ * (key design "gather-once + dense MMA kernel"), trained with BCE
+ * (key design "head-tail split"; section "loss / training strategy").
+ *
+ * Conventions used by every call
+ *   - bf16 tensors are passed as sg_bf16 (the raw bit pattern, RNE-rounded).
+ *   - A "slot" is a label's position after grouping: slot s = k*G + j is the
+ *     j-th smallest label id of group k.  W, dW are [L][F] row-major in slot
+ *     order; Z, dZ are [B][L] row-major in slot order; h is [B][H] row-major;
+ *     dh is [B][H] row-major fp32.
+ *   - Positives are given per sample as CSR over LABEL ids:
+ *     pos_rowptr[B+1] (pos_rowptr[0] = 0, non-decreasing, pos_rowptr[B] = nnz)
+ *     and pos_label[nnz] in [0, L), any order, duplicates allowed (a sample's
+ *     label is positive once: Y is binary).
+ *   - The loss written is the SUM over all (sample, label) of
+ *     max(z,0) - y z + log(1 + exp(-|z|)); dZ = sigmoid(Z) - Y is its exact
+ *     gradient.  The page's per-sample mean is that sum divided by B.
+ *   - All pointers to tensors are DEVICE pointers to caller-owned memory; the
+ *     library never frees or keeps them.  Outputs are overwritten, never
+ *     accumulated into.  `stream` is a cudaStream_t (NULL = legacy default).
+ *   - Every call except sg_layout_build, sg_layout_export and
+ *     sg_layout_status is asynchronous on `stream`.  Argument/shape errors are
+ *     returned before anything is launched.  Data errors found on the device
+ *     (a label id out of range, a malformed CSR, a bounded wait that gave up)
+ *     set the layout's sticky status word, read with sg_layout_status.
+ *   - A layout holds scratch memory, so one layout must not be used by two
+ *     streams at the same time.
+ *   - Thread safety: calls on different layouts may run from different host
+ *     threads; sg_last_error is per host thread.
+ *
+ * Supported range (anything else returns SG_ERR_UNSUPPORTED)
+ *   1 <= B <= 256, 1 <= F <= 256, F <= H <= 1024, 1 <= G <= 256, L = K*G
+ *   < 2^31.  Tensor-core engine (used when possible): G % 16 == 0 and
+ *   F % 16 == 0.  Every other G (including G = 1, per-label fixed fan-in) runs
+ *   on the CUDA-core engine.
+ */
+#ifndef SG_H
+#define SG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* exported symbols keep default visibility even when the library is built
+ * with -fvisibility=hidden */
+#if defined(__GNUC__)
+#define SG_API __attribute__((visibility("default")))
+#else
+#define SG_API
+#endif
+
+typedef uint16_t sg_bf16;
+
+typedef enum sg_status {
+    SG_OK = 0,
+    SG_ERR_INVALID = -1,     /* bad argument (null pointer, negative size, ...) */
+    SG_ERR_UNSUPPORTED = -2, /* outside the supported range above */
+    SG_ERR_CUDA = -3,        /* a CUDA runtime call failed */
+    SG_ERR_OOM = -4,         /* device allocation failed */
+    SG_ERR_TIMEOUT = -5,     /* a bounded device wait gave up */
+    SG_ERR_DATA = -6         /* the data breaks the layer's rules */
+} sg_status;
+
+typedef enum sg_engine {
+    SG_ENGINE_AUTO = 0, /* tensor-core engine where supported, else CUDA cores */
+    SG_ENGINE_SIMT = 1, /* CUDA-core engine for every call */
+    SG_ENGINE_TC = 2    /* tensor-core engine; calls it cannot run fail */
+} sg_engine;
+
+/* Opaque, library-owned: the canonical layout plus per-layout scratch. */
+typedef struct sg_layout sg_layout;
+
+/* ---------------------------------------------------------------- layout
+ * sg_layout_build -- group the labels and fix each group's fan-in set
+ * (key design "group-shared fixed fan-in sparsity": K groups of exactly G
+ * labels, shared I_k with |I_k| = F, index memory (L/G)*F).
+ *   groups[L]   device int32, group id of every label, each id in [0, K) used
+ *               by exactly G labels.
+ *   idx[K*F]    device int32, row k = I_k in any order; entries distinct and
+ *               in [0, H).
+ *   max_B       largest batch the layout's scratch will serve (<= 256).
+ *   max_nnz     largest positive count (nnz) a call will pass.
+ * Result: slots in ascending label id within each group, I_k sorted ascending
+ * and stored as uint16.  Synchronous (waits for `stream`) because data errors
+ * are returned: SG_ERR_DATA for a bad group id, a group of size != G, a
+ * duplicate or out-of-range index.  On success *out owns about
+ * 2*K*F + 8*L + 2*H*max_B + 8*K + 12*max_nnz bytes of device memory; free
+ * it with sg_layout_free.  On error *out is set to NULL.                    */
+SG_API sg_status sg_layout_build(const int32_t *groups, int64_t L, int32_t G,
+                          const int32_t *idx, int32_t F, int32_t H,
+                          int32_t max_B, int64_t max_nnz, void *stream,
+                          sg_layout **out);
+
+/* Copy the canonical layout out (device outputs, any may be NULL):
+ * slot_of_label[L], label_of_slot[L], idx_sorted[K*F] (uint16). Synchronous. */
+SG_API sg_status sg_layout_export(const sg_layout *layout, int32_t *slot_of_label,
+                           int32_t *label_of_slot, uint16_t *idx_sorted,
+                           void *stream);
+
+/* Release the layout and its scratch (NULL is a no-op).  Waits for the
+ * device to finish work that uses it. */
+SG_API void sg_layout_free(sg_layout *layout);
+
+/* Pick the engine for later calls on this layout (sg_engine value).
+ * SG_ENGINE_TC on a layout the tensor-core engine cannot run returns
+ * SG_ERR_UNSUPPORTED and leaves the engine unchanged. */
+SG_API sg_status sg_layout_set_engine(sg_layout *layout, int32_t engine);
+
+/* Sizes of a layout (any pointer may be NULL). */
+SG_API sg_status sg_layout_info(const sg_layout *layout, int64_t *L, int32_t *G,
+                         int32_t *F, int32_t *H, int64_t *K);
+
+/* Read (and if `clear`, reset) the layout's sticky device status word.
+ * Synchronous (waits for the device).  *code is an sg_status value. */
+SG_API sg_status sg_layout_status(sg_layout *layout, int32_t *code, int32_t clear);
+
+/* ---------------------------------------------------------------- positives
+ * sg_pos_export -- the positive lists as the step uses them (Y of the BCE in
+ * key design "head-tail split"): labels mapped to slots, sorted ascending and
+ * deduplicated per sample (out_rowptr[B+1], out_slots[<= nnz]); and the same
+ * entries bucketed by group (out_gptr[K+1]; out_gentry[] = (b << 16) | j for
+ * slot k*G + j; order inside one group unspecified).  Any output may be NULL.
+ * Asynchronous; a label id out of range sets the status word (SG_ERR_DATA)
+ * and that entry is dropped. */
+SG_API sg_status sg_pos_export(sg_layout *layout, int32_t B, const int32_t *pos_rowptr,
+                        const int32_t *pos_label, int64_t nnz,
+                        int32_t *out_rowptr, int32_t *out_slots,
+                        int32_t *out_gptr, int32_t *out_gentry, void *stream);
+
+/* ---------------------------------------------------------------- forward
+ * sg_fwd -- Z_k = H_k W_k^T for every group (key design "gather-once + dense
+ * MMA kernel"), i.e. Z[b][s] = sum_f W[s][f] h[b][I_k[f]], k = s / G.
+ * FP32 accumulation, Z rounded to bf16 (RNE).
+ *   h[B][H] bf16, W[L][F] bf16 (slot order), Z[B][L] bf16 (slot order).     */
+SG_API sg_status sg_fwd(sg_layout *layout, const sg_bf16 *h, int32_t B,
+                 const sg_bf16 *W, sg_bf16 *Z, void *stream);
+
+/* sg_bce_grad -- dZ = sigmoid(Z) - Y (bf16) and loss = sum of the BCE terms
+ * (double, device scalar), from a stored Z[B][L].                         */
+SG_API sg_status sg_bce_grad(sg_layout *layout, const sg_bf16 *Z, int32_t B,
+                      const int32_t *pos_rowptr, const int32_t *pos_label,
+                      int64_t nnz, sg_bf16 *dZ, double *loss, void *stream);
+
+/* sg_fwd_bce -- sg_fwd with the BCE step fused into its epilogue: Z stays in
+ * FP32 on chip; writes dZ (bf16), the loss, and Z (bf16) only if Z_or_null is
+ * not NULL.                                                              */
+SG_API sg_status sg_fwd_bce(sg_layout *layout, const sg_bf16 *h, int32_t B,
+                     const sg_bf16 *W, const int32_t *pos_rowptr,
+                     const int32_t *pos_label, int64_t nnz, sg_bf16 *dZ,
+                     double *loss, sg_bf16 *Z_or_null, void *stream);
+
+/* ---------------------------------------------------------------- backward
+ * sg_bwd_dW -- dW_k = dZ_k^T H_k (key design "gather-once + dense MMA
+ * kernel": the weight gradient is the symmetric dense GEMM), i.e.
+ * dW[s][f] = sum_b dZ[b][s] h[b][I_k[f]].  FP32 accumulation, bf16 output.
+ *   dZ[B][L] bf16, h[B][H] bf16, dW[L][F] bf16.                            */
+SG_API sg_status sg_bwd_dW(sg_layout *layout, const sg_bf16 *dZ, const sg_bf16 *h,
+                    int32_t B, sg_bf16 *dW, void *stream);
+
+/* sg_bwd_dh -- the feature gradient, summed over groups whose I_k overlap
+ * (same key design: Split-K along the label dimension), i.e.
+ * dh[b][i] = sum_s sum_f [I_k(s)[f] = i] dZ[b][s] W[s][f].  FP32 output;
+ * partial sums are added with atomics, so the last bits are not reproducible
+ * run to run.   dZ[B][L] bf16, W[L][F] bf16, dh[B][H] fp32.                */
+SG_API sg_status sg_bwd_dh(sg_layout *layout, const sg_bf16 *dZ, int32_t B,
+                    const sg_bf16 *W, float *dh, void *stream);
+
+/* sg_bwd -- sg_bwd_dW and sg_bwd_dh in one call. */
+SG_API sg_status sg_bwd(sg_layout *layout, const sg_bf16 *dZ, const sg_bf16 *h,
+                 int32_t B, const sg_bf16 *W, sg_bf16 *dW, float *dh,
+                 void *stream);
+
+/* ---------------------------------------------------------------- step
+ * sg_step -- the whole training step of the layer: forward, BCE gradient,
+ * dW and dh, from h, W and the positives.  Writes dW[L][F] bf16, dh[B][H]
+ * fp32 and the loss (double).  dZ is never returned.                       */
+SG_API sg_status sg_step(sg_layout *layout, const sg_bf16 *h, int32_t B,
+                  const sg_bf16 *W, const int32_t *pos_rowptr,
+                  const int32_t *pos_label, int64_t nnz, sg_bf16 *dW,
+                  float *dh, double *loss, void *stream);
+
+/* ---------------------------------------------------------------- timing
+ * Per-kernel device timing for benchmarks: while enabled, every kernel the
+ * library launches for this layout is bracketed by a pair of CUDA events
+ * recorded on the stream of the call, tagged by its kind (sg_kernel_kind).
+ * sg_timing_start(capacity) clears the record and keeps room for `capacity`
+ * launches (later ones are counted but not timed); sg_timing_stop waits for
+ * the device, writes per-kind total milliseconds and launch counts
+ * (arrays of SG_KIND_COUNT), and disables the record.                       */
+typedef enum sg_kernel_kind {
+    SG_KIND_PREP = 0,    /* h transpose, positive lists, loss reduction */
+    SG_KIND_FWD = 1,     /* forward (with or without the fused BCE)     */
+    SG_KIND_BCE = 2,     /* BCE from a stored Z                          */
+    SG_KIND_DW = 3,      /* weight gradient                              */
+    SG_KIND_DH = 4,      /* feature gradient                             */
+    SG_KIND_STEP = 5,    /* fused whole step                             */
+    SG_KIND_COUNT = 6
+} sg_kernel_kind;
+
+SG_API sg_status sg_timing_start(sg_layout *layout, int32_t capacity);
+SG_API sg_status sg_timing_stop(sg_layout *layout, double *ms_per_kind,
+                                int32_t *launches_per_kind);
+
+/* ---------------------------------------------------------------- misc */
+/* Message of the last failing call on this host thread ("" if none). */
+SG_API const char *sg_last_error(void);
+/* Constant name of a status value. */
+SG_API const char *sg_status_string(int32_t status);
+/* ABI version of this header (bumped on incompatible change). */
+SG_API int32_t sg_abi_version(void);
+
+#define SG_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SG_H */

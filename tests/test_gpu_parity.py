@@ -1,0 +1,294 @@
+"""GPU parity: every entry point of the C ABI against the CPU oracle on the
+same seeded inputs, element by element (small and ragged sizes), for both
+engines where they apply.  Bit-exact for the layout and the positive lists;
+max |gpu - ref| <= 2e-2 (1 + |ref|) for Z, dZ, dW, dh; loss within 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import extreme_label_sparse_gb300 as sg
+from workloads import CONFIGS, Workload, draw_bf16_matrix, generate
+
+from gpu_common import (LOSS_RTOL, assert_close, build_layout, dev_bf16, dev_i32,
+                        dev_problem, host_bf16_to_f64)
+
+pytestmark = pytest.mark.gpu
+
+SIMT, TC = sg.SG_ENGINE_SIMT, sg.SG_ENGINE_TC
+
+
+def _w(name, B, H, L, G, F, pos=3, idx_mode="uniform", dist="uniform", seed=0):
+    return Workload(name, B=B, H=H, L=L, G=G, F=F, pos=pos, pos_dist=dist, zipf_s=1.1,
+                    idx_mode=idx_mode, seed=seed)
+
+
+# (workload, engines): shapes spanning several tiles, ragged tails and the
+# degenerate cases (B = 1, G = 1, F = H, odd G / F)
+CASES = [
+    (CONFIGS["tiny"], (SIMT, TC)),
+    (_w("g1", B=37, H=96, L=300, G=1, F=24), (SIMT,)),
+    (_w("g3_oddF", B=5, H=50, L=99, G=3, F=7), (SIMT,)),
+    (_w("b1", B=1, H=64, L=512, G=16, F=16), (SIMT, TC)),
+    (_w("g32_b100", B=100, H=200, L=32 * 70, G=32, F=48, dist="zipf"), (SIMT, TC)),
+    (_w("g64_b200", B=200, H=768, L=64 * 40, G=64, F=128, pos=8, dist="zipf"), (SIMT, TC)),
+    (_w("dense_F_eq_H", B=16, H=32, L=16 * 12, G=16, F=32), (SIMT, TC)),
+    (_w("clustered", B=64, H=768, L=16 * 100, G=16, F=128, idx_mode="clustered"), (SIMT, TC)),
+    (_w("b256_f256", B=256, H=512, L=32 * 20, G=32, F=256, pos=4), (SIMT, TC)),
+]
+
+
+def _ids(case):
+    return case[0].name
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    sg.build()
+    sg.load()
+
+
+@pytest.fixture(scope="module", params=CASES, ids=[c[0].name for c in CASES])
+def case(request, oracle_mod):
+    w, engines = request.param
+    p = generate(w)
+    ref = oracle_mod.step(p, want_Z=True)
+    return w, engines, p, ref
+
+
+def _engines(case_):
+    w, engines, p, ref = case_
+    return engines
+
+
+def _layout(p, engine):
+    lay = build_layout(p)
+    if engine == TC:
+        try:
+            sg.sg_layout_set_engine(lay, TC)
+        except sg.SGError as e:
+            pytest.skip(f"tensor-core engine unavailable: {e}")
+    else:
+        sg.sg_layout_set_engine(lay, engine)
+    return lay
+
+
+def _status_ok(lay):
+    assert sg.sg_layout_status(lay) == 0
+
+
+@pytest.mark.parametrize("engine", [SIMT, TC], ids=["simt", "tc"])
+def test_layout_and_positives_bit_exact(case, engine):
+    w, engines, p, ref = case
+    if engine not in engines:
+        pytest.skip("engine not used for this shape")
+    lay = _layout(p, engine)
+    sol, los, ids = sg.sg_layout_export(lay)
+    assert np.array_equal(sol.cpu().numpy(), ref["slot_of_label"])
+    assert np.array_equal(los.cpu().numpy(), ref["label_of_slot"])
+    assert np.array_equal(ids.cpu().numpy().view(np.uint16), ref["idx_sorted"])
+    d = dev_problem(p)
+    orp, osl, ogp, oge = sg.sg_pos_export(lay, w.B, d["rowptr"], d["labels"], p.nnz)
+    orp = orp.cpu().numpy()
+    assert np.array_equal(orp, ref["srowptr"])
+    assert np.array_equal(osl.cpu().numpy()[:orp[-1]], ref["sslots"])
+    # per-group lists: the oracle's canonical slot lists regrouped by group
+    want = [[] for _ in range(w.K)]
+    for b in range(w.B):
+        for s in ref["sslots"][ref["srowptr"][b]:ref["srowptr"][b + 1]]:
+            want[s // w.G].append((b << 16) | (s % w.G))
+    gp = ogp.cpu().numpy()
+    ge = oge.cpu().numpy()
+    assert gp[0] == 0 and gp[-1] == len(ref["sslots"])
+    for k in range(w.K):
+        assert sorted(ge[gp[k]:gp[k + 1]].tolist()) == sorted(want[k]), k
+    _status_ok(lay)
+
+
+@pytest.mark.parametrize("engine", [SIMT, TC], ids=["simt", "tc"])
+def test_fwd(case, engine):
+    w, engines, p, ref = case
+    if engine not in engines:
+        pytest.skip("engine not used for this shape")
+    lay = _layout(p, engine)
+    d = dev_problem(p)
+    Z = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
+    sg.sg_fwd(lay, d["h"], d["W"], Z)
+    assert_close(host_bf16_to_f64(Z), ref["Z"], what="Z")
+    _status_ok(lay)
+
+
+@pytest.mark.parametrize("engine", [SIMT, TC], ids=["simt", "tc"])
+def test_fwd_bce(case, engine, oracle_mod):
+    w, engines, p, ref = case
+    if engine not in engines:
+        pytest.skip("engine not used for this shape")
+    lay = _layout(p, engine)
+    d = dev_problem(p)
+    dZ = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
+    Z = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    for with_z in (False, True):
+        sg.sg_fwd_bce(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dZ, loss,
+                      Z if with_z else None)
+        assert_close(host_bf16_to_f64(dZ), ref["dZ"], what="dZ")
+        assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
+        if with_z:
+            assert_close(host_bf16_to_f64(Z), ref["Z"], what="Z")
+    _status_ok(lay)
+
+
+def test_bce_grad_stage(case, oracle_mod):
+    """sg_bce_grad on a Z drawn by the generator (not produced by the GPU)."""
+    w, engines, p, ref = case
+    lay = _layout(p, SIMT)
+    zbits = draw_bf16_matrix(1234, w.B, w.L, 3.0)
+    want_dZ, want_loss = oracle_mod.bce(zbits, ref["srowptr"], ref["sslots"])
+    d = dev_problem(p)
+    dZ = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sg.sg_bce_grad(lay, dev_bf16(zbits), w.B, d["rowptr"], d["labels"], p.nnz, dZ, loss)
+    assert_close(host_bf16_to_f64(dZ), want_dZ, what="dZ")
+    assert float(loss.item()) == pytest.approx(want_loss, rel=LOSS_RTOL)
+    _status_ok(lay)
+
+
+@pytest.mark.parametrize("engine", [SIMT, TC], ids=["simt", "tc"])
+def test_bwd_stage(case, engine, oracle_mod):
+    """sg_bwd / sg_bwd_dW / sg_bwd_dh on a dZ drawn by the generator."""
+    w, engines, p, ref = case
+    if engine not in engines:
+        pytest.skip("engine not used for this shape")
+    lay = _layout(p, engine)
+    dzbits = draw_bf16_matrix(99, w.B, w.L, 0.5)
+    want_dW = oracle_mod.weight_grad(p.h, dzbits, ref["idx_sorted"], w.G, w.F)
+    want_dh = oracle_mod.feature_grad(p.W, dzbits, ref["idx_sorted"], w.G, w.H)
+    d = dev_problem(p)
+    dZ = dev_bf16(dzbits)
+    dW = torch.empty((w.L, w.F), dtype=torch.int16, device="cuda")
+    dh = torch.full((w.B, w.H), float("nan"), dtype=torch.float32, device="cuda")
+    sg.sg_bwd(lay, dZ, d["h"], d["W"], dW, dh)
+    assert_close(host_bf16_to_f64(dW), want_dW, what="dW")
+    assert_close(dh.cpu().numpy(), want_dh, what="dh")
+    dW.zero_()
+    dh.fill_(7.0)
+    sg.sg_bwd_dW(lay, dZ, d["h"], dW)
+    sg.sg_bwd_dh(lay, dZ, w.B, d["W"], dh)
+    assert_close(host_bf16_to_f64(dW), want_dW, what="dW")
+    assert_close(dh.cpu().numpy(), want_dh, what="dh")
+    _status_ok(lay)
+
+
+@pytest.mark.parametrize("engine", [SIMT, TC], ids=["simt", "tc"])
+def test_step_chain(case, engine):
+    """The whole step from h, W and the positives."""
+    w, engines, p, ref = case
+    if engine not in engines:
+        pytest.skip("engine not used for this shape")
+    lay = _layout(p, engine)
+    d = dev_problem(p)
+    dW = torch.empty((w.L, w.F), dtype=torch.int16, device="cuda")
+    dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    for _ in range(2):  # a second call must give the same answer (scratch reuse)
+        sg.sg_step(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dW, dh, loss)
+        assert_close(host_bf16_to_f64(dW), ref["dW"], what="dW")
+        assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+        assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
+    _status_ok(lay)
+
+
+# ------------------------------------------------------------------ edge cases
+def test_empty_positive_lists(oracle_mod):
+    w = _w("nopos", B=8, H=64, L=256, G=16, F=16, pos=0)
+    p = generate(w)
+    ref = oracle_mod.step(p)
+    lay = build_layout(p, max_nnz=1)
+    d = dev_problem(p)
+    dW = torch.empty((w.L, w.F), dtype=torch.int16, device="cuda")
+    dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sg.sg_step(lay, d["h"], d["W"], d["rowptr"], d["labels"], 0, dW, dh, loss)
+    assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
+    assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+
+
+def test_duplicate_positives_count_once(oracle_mod):
+    w = CONFIGS["tiny"]
+    p = generate(w)
+    # repeat every positive of sample 0 three times
+    row0 = p.pos_label[p.pos_rowptr[0]:p.pos_rowptr[1]]
+    labels = np.concatenate([np.repeat(row0, 3), p.pos_label[p.pos_rowptr[1]:]]).astype(np.int32)
+    rowptr = p.pos_rowptr.copy()
+    rowptr[1:] += 2 * len(row0)
+    p.pos_rowptr, p.pos_label = rowptr, labels
+    ref = oracle_mod.step(p)
+    lay = build_layout(p)
+    d = dev_problem(p)
+    dZ = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sg.sg_fwd_bce(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dZ, loss)
+    assert_close(host_bf16_to_f64(dZ), ref["dZ"], what="dZ")
+    assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
+
+
+def test_layout_rejects_bad_data():
+    w = CONFIGS["tiny"]
+    p = generate(w)
+    bad = p.groups.copy()
+    bad[3] = w.K  # group id out of range
+    with pytest.raises(sg.SGError) as e:
+        sg.sg_layout_build(dev_i32(bad), w.L, w.G, dev_i32(p.idx.reshape(-1)), w.F, w.H, 4, 4)
+    assert e.value.status == sg.SG_ERR_DATA
+    bad = p.groups.copy()
+    bad[0], bad[1] = bad[1], bad[1]  # one group too big, another too small
+    if bad[0] != p.groups[0]:
+        with pytest.raises(sg.SGError) as e:
+            sg.sg_layout_build(dev_i32(bad), w.L, w.G, dev_i32(p.idx.reshape(-1)), w.F, w.H, 4, 4)
+        assert e.value.status == sg.SG_ERR_DATA
+    bidx = p.idx.copy()
+    bidx[7, 3] = bidx[7, 4]  # duplicate index
+    with pytest.raises(sg.SGError) as e:
+        sg.sg_layout_build(dev_i32(p.groups), w.L, w.G, dev_i32(bidx.reshape(-1)), w.F, w.H, 4, 4)
+    assert e.value.status == sg.SG_ERR_DATA
+    bidx = p.idx.copy()
+    bidx[9, 0] = w.H  # index out of range
+    with pytest.raises(sg.SGError) as e:
+        sg.sg_layout_build(dev_i32(p.groups), w.L, w.G, dev_i32(bidx.reshape(-1)), w.F, w.H, 4, 4)
+    assert e.value.status == sg.SG_ERR_DATA
+
+
+def test_bad_positive_label_sets_status():
+    w = CONFIGS["tiny"]
+    p = generate(w)
+    lay = build_layout(p)
+    d = dev_problem(p)
+    labels = p.pos_label.copy()
+    labels[2] = w.L + 5
+    dZ = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sg.sg_fwd_bce(lay, d["h"], d["W"], d["rowptr"], dev_i32(labels), p.nnz, dZ, loss)
+    assert sg.sg_layout_status(lay) == sg.SG_ERR_DATA
+    assert sg.sg_layout_status(lay) == 0  # cleared by the first read
+    rp = p.pos_rowptr.copy()
+    rp[3] = rp[4] + 1  # non-monotone row pointers
+    sg.sg_fwd_bce(lay, d["h"], d["W"], dev_i32(rp), d["labels"], p.nnz, dZ, loss)
+    assert sg.sg_layout_status(lay) == sg.SG_ERR_DATA
+
+
+def test_call_argument_errors():
+    w = CONFIGS["tiny"]
+    p = generate(w)
+    lay = build_layout(p, max_B=8, max_nnz=8)
+    d = dev_problem(p)
+    Z = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
+    with pytest.raises(sg.SGError) as e:  # B above max_B
+        sg.sg_fwd(lay, d["h"], d["W"], Z)
+    assert e.value.status == sg.SG_ERR_INVALID
+    with pytest.raises(sg.SGError) as e:  # nnz above max_nnz
+        sg.sg_bce_grad(lay, Z[:8].contiguous(), 8, d["rowptr"][:9].contiguous(),
+                       d["labels"][:16].contiguous(), 16, Z[:8].contiguous(),
+                       torch.zeros(1, dtype=torch.float64, device="cuda"))
+    assert e.value.status == sg.SG_ERR_INVALID
+    with pytest.raises(sg.SGError) as e:
+        sg.sg_layout_set_engine(build_layout(generate(_w("g3", 4, 30, 30, 3, 5))), TC)
+    assert e.value.status == sg.SG_ERR_UNSUPPORTED
