@@ -79,11 +79,20 @@ sg_status check_pos(const sg_layout *lo, const int32_t *rowptr,
             return rc_;            \
     } while (0)
 
-bool use_tc(const sg_layout *lo)
+// Which engine runs `stage` for a batch of B: the tensor-core engine unless the
+// layout is pinned to CUDA cores or the shape is outside what it supports.  A
+// layout pinned to the tensor-core engine fails instead of switching.
+sg_status pick_tc(const sg_layout *lo, int stage, int32_t B, bool *tc, const char *fn)
 {
+    *tc = false;
     if (lo->engine == SG_ENGINE_SIMT)
-        return false;
-    return lo->tc_ok;
+        return SG_OK;
+    const bool ok = lo->tc_ok && tc_stage_ok(lo, stage, B);
+    if (!ok && lo->engine == SG_ENGINE_TC)
+        FAIL(SG_ERR_UNSUPPORTED, "%s: this shape (B=%d G=%d F=%d H=%d) is outside the "
+             "tensor-core engine", fn, B, lo->G, lo->F, lo->H);
+    *tc = ok;
+    return SG_OK;
 }
 
 void timer_release(sg_layout::Timer &t)
@@ -128,7 +137,7 @@ sg_status dev_alloc(T **p, size_t n, const char *what)
 
 sg_status ensure_dz_ws(sg_layout *lo)
 {
-    size_t need = (size_t)lo->max_B * (size_t)lo->L;
+    size_t need = 2 * (size_t)lo->max_B * (size_t)lo->L;
     if (lo->dZ_ws && lo->dZ_ws_elems >= need)
         return SG_OK;
     if (lo->dZ_ws)
@@ -210,7 +219,7 @@ sg_status sg_layout_build(const int32_t *groups, int64_t L, int32_t G,
     lo->H = H;
     lo->max_B = max_B;
     lo->max_nnz = max_nnz;
-    lo->ldB = (int32_t)(ceil_div(max_B, 8) * 8);
+    lo->ldB = (int32_t)(ceil_div(max_B, 128) * 128);
     cudaStream_t st = (cudaStream_t)stream;
 
     sg_status rc = SG_OK;
@@ -374,10 +383,12 @@ sg_status sg_fwd(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
     REQUIRE(Z, fn);
     DeviceGuard dg(lo->device);
     cudaStream_t st = (cudaStream_t)stream;
+    bool tc = false;
+    TRY(pick_tc(lo, SG_KIND_FWD, B, &tc, fn));
     TRY(simt_transpose_h(lo, h, B, st));
-    if (use_tc(lo))
-        return tc_fwd(lo, B, W, Z, nullptr, nullptr, st);
-    return simt_fwd(lo, B, W, Z, nullptr, nullptr, st);
+    if (tc)
+        return tc_fwd(lo, B, W, Z, nullptr, nullptr, nullptr, st);
+    return simt_fwd(lo, B, W, Z, nullptr, nullptr, nullptr, st);
 }
 
 sg_status sg_bce_grad(sg_layout *lo, const sg_bf16 *Z, int32_t B,
@@ -410,11 +421,13 @@ sg_status sg_fwd_bce(sg_layout *lo, const sg_bf16 *h, int32_t B,
     REQUIRE(loss, fn);
     DeviceGuard dg(lo->device);
     cudaStream_t st = (cudaStream_t)stream;
+    bool tc = false;
+    TRY(pick_tc(lo, SG_KIND_FWD, B, &tc, fn));
     TRY(simt_transpose_h(lo, h, B, st));
     TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
-    if (use_tc(lo))
-        return tc_fwd(lo, B, W, Z_or_null, dZ, loss, st);
-    return simt_fwd(lo, B, W, Z_or_null, dZ, loss, st);
+    if (tc)
+        return tc_fwd(lo, B, W, Z_or_null, dZ, nullptr, loss, st);
+    return simt_fwd(lo, B, W, Z_or_null, dZ, nullptr, loss, st);
 }
 
 // ---------------------------------------------------------------- backward
@@ -428,10 +441,12 @@ sg_status sg_bwd_dW(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h,
     REQUIRE(dW, fn);
     DeviceGuard dg(lo->device);
     cudaStream_t st = (cudaStream_t)stream;
+    bool tc = false;
+    TRY(pick_tc(lo, SG_KIND_DW, B, &tc, fn));
     TRY(simt_transpose_h(lo, h, B, st));
-    if (use_tc(lo))
-        return tc_dW(lo, dZ, B, dW, st);
-    return simt_dW(lo, dZ, B, dW, st);
+    if (tc)
+        return tc_dW(lo, dZ, nullptr, B, dW, st);
+    return simt_dW(lo, dZ, nullptr, B, dW, st);
 }
 
 sg_status sg_bwd_dh(sg_layout *lo, const sg_bf16 *dZ, int32_t B,
@@ -444,9 +459,11 @@ sg_status sg_bwd_dh(sg_layout *lo, const sg_bf16 *dZ, int32_t B,
     REQUIRE(dh, fn);
     DeviceGuard dg(lo->device);
     cudaStream_t st = (cudaStream_t)stream;
-    if (use_tc(lo))
-        return tc_dh(lo, dZ, B, W, dh, st);
-    return simt_dh(lo, dZ, B, W, dh, st);
+    bool tc = false;
+    TRY(pick_tc(lo, SG_KIND_DH, B, &tc, fn));
+    if (tc)
+        return tc_dh(lo, dZ, nullptr, B, W, dh, st);
+    return simt_dh(lo, dZ, nullptr, B, W, dh, st);
 }
 
 sg_status sg_bwd(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h, int32_t B,
@@ -479,15 +496,23 @@ sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
     REQUIRE(loss, fn);
     DeviceGuard dg(lo->device);
     cudaStream_t st = (cudaStream_t)stream;
+    bool tc_f = false, tc_w = false, tc_h = false;
+    TRY(pick_tc(lo, SG_KIND_FWD, B, &tc_f, fn));
+    TRY(pick_tc(lo, SG_KIND_DW, B, &tc_w, fn));
+    TRY(pick_tc(lo, SG_KIND_DH, B, &tc_h, fn));
     TRY(simt_transpose_h(lo, h, B, st));
     TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
-    if (use_tc(lo))
-        return tc_step(lo, B, W, dW, dh, loss, st);
-    // CUDA-core engine: forward + BCE into dZ scratch, then dW and dh
+    // forward + BCE into dZ scratch, then dW and dh from it.  dZ is kept as
+    // two bf16 planes (hi + lo): a single bf16 rounding of dZ, summed over B
+    // samples (dW) or over every label (dh), would move results by more than
+    // 2e-2 (1 + |ref|) against the exact gradient.
     TRY(ensure_dz_ws(lo));
-    TRY(simt_fwd(lo, B, W, nullptr, lo->dZ_ws, loss, st));
-    TRY(simt_dW(lo, lo->dZ_ws, B, dW, st));
-    return simt_dh(lo, lo->dZ_ws, B, W, dh, st);
+    uint16_t *dZ = lo->dZ_ws;
+    uint16_t *dZlo = lo->dZ_ws + (size_t)B * lo->L;
+    TRY(tc_f ? tc_fwd(lo, B, W, nullptr, dZ, dZlo, loss, st)
+             : simt_fwd(lo, B, W, nullptr, dZ, dZlo, loss, st));
+    TRY(tc_w ? tc_dW(lo, dZ, dZlo, B, dW, st) : simt_dW(lo, dZ, dZlo, B, dW, st));
+    return tc_h ? tc_dh(lo, dZ, dZlo, B, W, dh, st) : simt_dh(lo, dZ, dZlo, B, W, dh, st);
 }
 
 // ---------------------------------------------------------------- timing
@@ -510,9 +535,10 @@ sg_status sg_timing_start(sg_layout *lo, int32_t capacity)
         }
         for (int i = 0; i < 2 * capacity; ++i) {
             if (cudaEventCreate(&t.ev[i]) != cudaSuccess) {
-                t.cap = i / 2;
-                for (int j = 2 * t.cap; j < i; ++j)
+                for (int j = 0; j < i; ++j)
                     cudaEventDestroy(t.ev[j]);
+                delete[] t.ev;
+                t.ev = nullptr;
                 timer_release(t);
                 FAIL(SG_ERR_CUDA, "%s: cudaEventCreate failed", fn);
             }

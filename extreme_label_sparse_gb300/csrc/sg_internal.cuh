@@ -29,7 +29,7 @@ struct sg_layout {
 
     // per-call scratch (device)
     uint16_t *hT = nullptr;  // [H][ldB] bf16, transposed h, zero padded
-    int32_t ldB = 0;         // roundup(max_B, 8)
+    int32_t ldB = 0;         // roundup(max_B, 128)
     int32_t *gcount = nullptr;  // [K+1], all zero between calls
     int32_t *gptr = nullptr;    // [K+1]
     int32_t *gent = nullptr;    // [max_nnz]  (b << 16) | j
@@ -40,7 +40,8 @@ struct sg_layout {
     int32_t loss_part_n = 0;
     int32_t *status = nullptr;  // sticky device status word
 
-    // dZ scratch of the composed step, allocated on first use
+    // dZ scratch of the composed step (hi and lo bf16 planes of max_B x L),
+    // allocated on first use
     uint16_t *dZ_ws = nullptr;
     size_t dZ_ws_elems = 0;
 
@@ -147,21 +148,24 @@ sg_status sg_loss_finalize(sg_layout *lo, int32_t nparts, double *loss,
 // simt.cu
 sg_status simt_transpose_h(sg_layout *lo, const uint16_t *h, int32_t B,
                            cudaStream_t st);
+// dZ_lo (optional): second bf16 plane with dZ - bf16(dZ), so that hi + lo
+// carries dZ to about 16 significant bits between the forward and backward
 sg_status simt_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
-                   uint16_t *dZ, double *loss, cudaStream_t st);
+                   uint16_t *dZ, uint16_t *dZ_lo, double *loss, cudaStream_t st);
 sg_status simt_bce(sg_layout *lo, const uint16_t *Z, int32_t B, uint16_t *dZ,
                    double *loss, cudaStream_t st);
-sg_status simt_dW(sg_layout *lo, const uint16_t *dZ, int32_t B, uint16_t *dW,
-                  cudaStream_t st);
-sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, int32_t B,
-                  const uint16_t *W, float *dh, cudaStream_t st);
+sg_status simt_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
+                  int32_t B, uint16_t *dW, cudaStream_t st);
+sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
+                  int32_t B, const uint16_t *W, float *dh, cudaStream_t st);
 // tc.cu
 bool tc_supported(const sg_layout *lo);
+bool tc_stage_ok(const sg_layout *lo, int stage, int B);
 sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
-                 uint16_t *dZ, double *loss, cudaStream_t st);
-sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, int32_t B, uint16_t *dW,
-                cudaStream_t st);
-sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, int32_t B,
+                 uint16_t *dZ, uint16_t *dZ_lo, double *loss, cudaStream_t st);
+sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B,
+                uint16_t *dW, cudaStream_t st);
+sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B,
                 const uint16_t *W, float *dh, cudaStream_t st);
 sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW,
                   float *dh, double *loss, cudaStream_t st);

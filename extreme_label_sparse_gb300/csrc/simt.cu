@@ -87,7 +87,7 @@ __device__ __forceinline__ void gather_rows(const uint16_t *__restrict__ hT,
 // ------------------------------------------------------------ forward
 struct FwdArgs {
     const uint16_t *hT, *W, *idx_s;
-    uint16_t *Z, *dZ;
+    uint16_t *Z, *dZ, *dZ_lo;
     const int32_t *gptr, *gent;
     double *loss_part;
     int64_t K, L;
@@ -149,7 +149,10 @@ __global__ void __launch_bounds__(kThreads) k_simt_fwd(FwdArgs a)
                         float lt;
                         float d = bce_grad_loss(acc[u], (y >> u) & 1u, &lt);
                         l += lt;
-                        dr[u] = f2bf(d);
+                        const uint16_t hi = f2bf(d);
+                        dr[u] = hi;
+                        if (a.dZ_lo)
+                            a.dZ_lo[(int64_t)b * a.L + s0 + u] = f2bf(d - bf2f(hi));
                     }
                     lacc += l;
                 }
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kThreads)
 
 // ------------------------------------------------------------ dW
 struct DWArgs {
-    const uint16_t *hT, *dZ, *idx_s;
+    const uint16_t *hT, *dZ, *dZ_lo, *idx_s;
     uint16_t *dW;
     int64_t K, L;
     int32_t B, ldB, G, F;
@@ -225,7 +228,8 @@ __global__ void __launch_bounds__(kThreads) k_simt_dW(DWArgs a)
             const int gc = min(GC, G - j0);
             for (int e = tid; e < B * gc; e += kThreads) {
                 int b = e / gc, j = e - b * gc;
-                dZs[b * 32 + j] = bf2f(a.dZ[(int64_t)b * a.L + k * G + j0 + j]);
+                const int64_t at = (int64_t)b * a.L + k * G + j0 + j;
+                dZs[b * 32 + j] = bf2f(a.dZ[at]) + (a.dZ_lo ? bf2f(a.dZ_lo[at]) : 0.f);
             }
             __syncthreads();
             const int ntask = F * (gc / JT);
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_dW(DWArgs a)
 // part[b][I_k[f]] (shared-memory atomics; groups overlap).  The partial is
 // added to dh once at the end.
 struct DhArgs {
-    const uint16_t *dZ, *W, *idx_s;
+    const uint16_t *dZ, *dZ_lo, *W, *idx_s;
     float *dh;
     int64_t K, L;
     int32_t B, G, F, H;
@@ -298,7 +302,12 @@ __global__ void __launch_bounds__(kThreads) k_simt_dh(DhArgs a)
         for (int e = tid; e < kBT * 32; e += kThreads) {
             int b = e >> 5, s = e & 31;
             int row = brow0 + b;
-            dZs[b * 33 + s] = (s < ns && row < a.B) ? bf2f(a.dZ[(int64_t)row * a.L + s0 + s]) : 0.f;
+            float v = 0.f;
+            if (s < ns && row < a.B) {
+                const int64_t at = (int64_t)row * a.L + s0 + s;
+                v = bf2f(a.dZ[at]) + (a.dZ_lo ? bf2f(a.dZ_lo[at]) : 0.f);
+            }
+            dZs[b * 33 + s] = v;
         }
         for (int e = tid; e < ng * F; e += kThreads)
             idxc[e] = a.idx_s[kfirst * F + e];
@@ -364,7 +373,7 @@ sg_status simt_transpose_h(sg_layout *lo, const uint16_t *h, int32_t B,
                                      (int)(bytes)))
 
 sg_status simt_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
-                   uint16_t *dZ, double *loss, cudaStream_t st)
+                   uint16_t *dZ, uint16_t *dZ_lo, double *loss, cudaStream_t st)
 {
     FwdArgs a;
     a.hT = lo->hT;
@@ -372,6 +381,7 @@ sg_status simt_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
     a.idx_s = lo->idx_s;
     a.Z = Z;
     a.dZ = dZ;
+    a.dZ_lo = dZ_lo;
     a.gptr = lo->gptr;
     a.gent = lo->gent;
     a.loss_part = lo->loss_part;
@@ -411,12 +421,13 @@ sg_status simt_bce(sg_layout *lo, const uint16_t *Z, int32_t B, uint16_t *dZ,
     return sg_loss_finalize(lo, grid, loss, st);
 }
 
-sg_status simt_dW(sg_layout *lo, const uint16_t *dZ, int32_t B, uint16_t *dW,
-                  cudaStream_t st)
+sg_status simt_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
+                  int32_t B, uint16_t *dW, cudaStream_t st)
 {
     DWArgs a;
     a.hT = lo->hT;
     a.dZ = dZ;
+    a.dZ_lo = dZ_lo;
     a.idx_s = lo->idx_s;
     a.dW = dW;
     a.K = lo->K;
@@ -440,11 +451,12 @@ sg_status simt_dW(sg_layout *lo, const uint16_t *dZ, int32_t B, uint16_t *dW,
     return SG_OK;
 }
 
-sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, int32_t B,
-                  const uint16_t *W, float *dh, cudaStream_t st)
+sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
+                  int32_t B, const uint16_t *W, float *dh, cudaStream_t st)
 {
     DhArgs a;
     a.dZ = dZ;
+    a.dZ_lo = dZ_lo;
     a.W = W;
     a.idx_s = lo->idx_s;
     a.dh = dh;

@@ -1,30 +1,1034 @@
-// Tensor-core engine (tcgen05 / TMEM / TMA, sm_103a).
+// Tensor-core engine (sm_103a): tcgen05 MMA with TMEM accumulators, operands
+// staged in shared memory by TMA (tile loads for W_k and dZ_k, gather4 loads
+// for H_k).  HASTE, key design "gather-once + dense MMA kernel":
+//   forward   Z_k    = H_k W_k^T          M = samples, N = G, K = F
+//   weights   dW_k^T = H_k^T dZ_k         M = F,       N = G, K = samples
+//   features  dH_k   = dZ_k W_k, scattered into the columns I_k of dh
+//             (Split-K over groups: each CTA keeps a partial of one band of
+//             dh columns in TMEM and adds it to dh once at the end).
+//
+// Shared-memory operand layouts (all 1024-byte aligned):
+//   H_k  : gathered rows hT[I_k[f]] -> [b-chunk of 64][f][64 b], 128-byte
+//          swizzle.  Read as MN-major A (M = b) by the forward and as K-major A
+//          (M = f, K = b) by the weight gradient.
+//   W_k  : TMA box {64 f, G rows} per 64-wide f chunk, 128-byte swizzle:
+//          K-major B (N = j, K = f) of the forward, MN-major B (N = f, K = j)
+//          of the feature gradient.
+//   dZ_k : TMA box {min(G,64) j, rows b}, swizzle = row width: MN-major B
+//          (N = j, K = b) of the weight gradient, K-major A (M = b, K = j) of
+//          the feature gradient.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "sg_internal.cuh"
+#include "tc_ptx.cuh"
 
-bool tc_supported(const sg_layout *) { return false; }
+using namespace tc;
 
-static sg_status tc_unavailable(const char *fn)
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 220 * 1024;  // dynamic shared memory we plan with
+constexpr int kFwdThreads = 192;         // producer, MMA, 4 epilogue warps
+constexpr int kDhThreads = 192;
+
+// ------------------------------------------------------------------ plans
+struct FwdPlan {
+    bool ok = false;
+    int MT = 0, nk = 0, S = 0;
+    uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, tmem_cols = 0;
+};
+
+struct DWPlan {
+    bool ok = false;
+    int MT = 0, FT = 0, S = 0, nzc = 0, zsw = 0;
+    uint32_t a_bytes = 0, z_bytes = 0, stage_bytes = 0, tmem_cols = 0;
+};
+
+struct DhPlan {
+    bool ok = false;
+    int MT = 0, nk = 0, S = 0, nzc = 0, zsw = 0, nbands = 0, band_w = 0;
+    uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, tmem_cols = 0;
+};
+
+uint32_t pow2_cols(int n)
 {
-    sg_set_error("%s: the tensor-core engine is not available in this build", fn);
+    uint32_t c = 32;
+    while ((int)c < n)
+        c <<= 1;
+    return c;
+}
+
+bool shape_ok(const sg_layout *lo)
+{
+    return lo->G % 16 == 0 && lo->G <= 256 && lo->F % 64 == 0 && lo->F <= 256 &&
+           lo->L % 8 == 0 && lo->ldB % 64 == 0;
+}
+
+FwdPlan plan_fwd(const sg_layout *lo, int B)
+{
+    FwdPlan p;
+    if (!shape_ok(lo) || B < 1 || B > 256)
+        return p;
+    p.MT = (B + 127) / 128;
+    if (p.MT * 128 > lo->ldB)
+        return p;
+    p.nk = lo->F / 64;
+    p.a_bytes = (uint32_t)p.MT * 2 * lo->F * 128;
+    p.w_bytes = (uint32_t)p.nk * lo->G * 128;
+    p.stage_bytes = p.a_bytes + p.w_bytes;
+    p.S = (int)(kSmemBudget / p.stage_bytes);
+    if (p.S > 6)
+        p.S = 6;
+    if (p.S < 2)
+        return p;
+    if (2 * p.MT * lo->G > 512)
+        return p;
+    p.tmem_cols = pow2_cols(2 * p.MT * lo->G);
+    p.ok = true;
+    return p;
+}
+
+int dz_swizzle(int G) { return G * 2 >= 128 ? 128 : G * 2; }
+
+DWPlan plan_dW(const sg_layout *lo, int B, bool split)
+{
+    DWPlan p;
+    if (!shape_ok(lo) || lo->F % 128 != 0 || B < 1 || B > 256)
+        return p;
+    p.MT = (B + 127) / 128;
+    if (p.MT * 128 > lo->ldB)
+        return p;
+    p.FT = lo->F / 128;
+    p.zsw = dz_swizzle(lo->G);
+    p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
+    p.a_bytes = (uint32_t)p.MT * 2 * lo->F * 128;
+    p.z_bytes = (uint32_t)(split ? 2 : 1) * p.nzc * p.MT * 128 * p.zsw;
+    p.stage_bytes = p.a_bytes + p.z_bytes;
+    p.S = (int)(kSmemBudget / p.stage_bytes);
+    if (p.S > 6)
+        p.S = 6;
+    if (p.S < 2)
+        return p;
+    if (2 * p.FT * lo->G > 512)
+        return p;
+    p.tmem_cols = pow2_cols(2 * p.FT * lo->G);
+    p.ok = true;
+    return p;
+}
+
+DhPlan plan_dh(const sg_layout *lo, int B, bool split)
+{
+    DhPlan p;
+    if (!shape_ok(lo) || B < 1 || B > 256)
+        return p;
+    p.MT = (B + 127) / 128;
+    p.nk = lo->F / 64;
+    p.zsw = dz_swizzle(lo->G);
+    p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
+    const int wmax = 512 - lo->F;  // TMEM columns left for the dh partial
+    p.nbands = (lo->H + wmax - 1) / wmax;
+    p.band_w = (lo->H + p.nbands - 1) / p.nbands;
+    p.band_w = (p.band_w + 31) / 32 * 32;
+    if (p.band_w + lo->F > 512)
+        return p;
+    p.z_bytes = (uint32_t)(split ? 2 : 1) * p.nzc * 128 * p.zsw;
+    p.w_bytes = (uint32_t)p.nk * lo->G * 128;
+    p.i_bytes = (uint32_t)((lo->F * 2 + 1023) / 1024 * 1024);
+    p.stage_bytes = p.z_bytes + p.w_bytes + p.i_bytes;
+    p.S = (int)(kSmemBudget / p.stage_bytes);
+    if (p.S > 6)
+        p.S = 6;
+    if (p.S < 2)
+        return p;
+    p.tmem_cols = 512;
+    p.ok = true;
+    return p;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+sg_status get_encode()
+{
+    if (g_encode)
+        return SG_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        sg_set_error("cuTensorMapEncodeTiled is not available from the driver");
+        return SG_ERR_CUDA;
+    }
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    return SG_OK;
+}
+
+sg_status make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                      uint32_t box_inner, uint32_t box_outer, int swizzle_bytes,
+                      const char *what)
+{
+    sg_status rc = get_encode();
+    if (rc != SG_OK)
+        return rc;
+    if (((uintptr_t)base & 15) != 0) {
+        sg_set_error("%s: device pointer must be 16-byte aligned", what);
+        return SG_ERR_INVALID;
+    }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                            : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                            : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                  : CU_TENSOR_MAP_SWIZZLE_NONE;
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        sg_set_error("%s: cuTensorMapEncodeTiled failed (%d)", what, (int)r);
+        return SG_ERR_CUDA;
+    }
+    return SG_OK;
+}
+
+// ------------------------------------------------------------------ common
+struct Ctl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem;
+    int abort_flag;
+    double red[8];
+};
+
+__device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_u32(&b); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
+}
+
+// store n (multiple of 8) floats as bf16 to 16-byte aligned global memory
+template <int N>
+__device__ __forceinline__ void store_bf16_row(uint16_t *dst, const float (&v)[N])
+{
+#pragma unroll
+    for (int i = 0; i < N; i += 8) {
+        uint4 q;
+        q.x = pack_bf16x2(v[i + 0], v[i + 1]);
+        q.y = pack_bf16x2(v[i + 2], v[i + 3]);
+        q.z = pack_bf16x2(v[i + 4], v[i + 5]);
+        q.w = pack_bf16x2(v[i + 6], v[i + 7]);
+        *reinterpret_cast<uint4 *>(dst + i) = q;
+    }
+}
+
+template <int CH>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, float (&v)[CH])
+{
+    if constexpr (CH == 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            v[i] = __uint_as_float(r[i]);
+    } else {
+        uint32_t r[16];
+        tmem_ld16(taddr, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            v[i] = __uint_as_float(r[i]);
+    }
+}
+
+// positives of sample b among columns c0 .. c0+CH-1 of group k
+__device__ __forceinline__ uint32_t group_pos_mask(const int32_t *__restrict__ gptr,
+                                                   const int32_t *__restrict__ gent, int64_t k,
+                                                   int b, int c0, int n)
+{
+    uint32_t y = 0;
+    const int e1 = __ldg(gptr + k + 1);
+    for (int e = __ldg(gptr + k); e < e1; ++e) {
+        const int v = __ldg(gent + e);
+        const int jj = (v & 0xffff) - c0;
+        if ((v >> 16) == b && jj >= 0 && jj < n)
+            y |= 1u << jj;
+    }
+    return y;
+}
+
+// After an abort, wait (bounded) until the loads of the last stages issued
+// have landed, so no TMA write is still in flight when the CTA exits.  In a
+// normal run every one of these phases has already completed.
+__device__ __forceinline__ void drain_loads(Ctl &c, int issued, int S)
+{
+    if (!c.abort_flag)
+        return;
+    for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i)
+        mbar_wait_drain(bar_addr(c.full[i % S]), (uint32_t)(i / S) & 1u);
+}
+
+// sum of one double per thread over the 128 epilogue threads (warps 2..5)
+__device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst)
+{
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_down_sync(0xffffffffu, v, o);
+    const int ew = threadIdx.x / 32 - 2;
+    if ((threadIdx.x & 31) == 0)
+        c.red[ew] = v;
+    named_bar(1, 128);
+    if (ew == 0 && (threadIdx.x & 31) == 0)
+        *dst = c.red[0] + c.red[1] + c.red[2] + c.red[3];
+}
+
+// ================================================================== forward
+struct FwdArgs {
+    const uint16_t *idx_s;
+    uint16_t *Z, *dZ, *dZ_lo;
+    const int32_t *gptr, *gent;
+    double *loss_part;
+    int32_t *status;
+    int64_t K, L;
+    int32_t B, G, F, MT, nk, S;
+    uint32_t a_bytes, w_bytes, stage_bytes, tmem_cols;
+};
+
+template <bool BCE, int CH>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    k_tc_fwd(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+             const FwdArgs a)
+{
+    __shared__ Ctl c;
+    extern __shared__ uint8_t dsm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
+    const int G = a.G, F = a.F, S = a.S;
+
+    if (threadIdx.x == 0) {
+        c.abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_addr(c.full[s]), 1);
+            mbar_init(bar_addr(c.empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_addr(c.tfull[i]), 1);
+            mbar_init(bar_addr(c.tempty[i]), 128);
+        }
+        mbar_init(bar_addr(c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = c.tmem;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
+                break;
+            const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
+            const uint32_t Wt = A + a.a_bytes;
+            const uint32_t fb = bar_addr(c.full[s]);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(fb, a.a_bytes + a.w_bytes);
+                for (int kc = 0; kc < a.nk; ++kc)
+                    tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
+            }
+            __syncwarp();
+            const uint16_t *I = a.idx_s + k * F;
+            const int ng = F / 4;
+            for (int q = lane; q < a.MT * 2 * ng; q += 32) {
+                const int g = q % ng, tcn = q / ng;
+                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(I + 4 * g));
+                tma_gather4(A + (uint32_t)tcn * F * 128 + (uint32_t)g * 512, &tm_h, tcn * 64,
+                            (int)(v.x & 0xffff), (int)(v.x >> 16), (int)(v.y & 0xffff),
+                            (int)(v.y >> 16), fb);
+            }
+        }
+        drain_loads(c, it, S);
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
+        const uint32_t idesc = idesc_bf16(128, G, 1, 0);
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(bar_addr(c.tempty[acc]), aph ^ 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
+                const uint32_t Wt = A + a.a_bytes;
+                for (int t = 0; t < a.MT; ++t) {
+                    const uint32_t d = tbase + (uint32_t)(acc * a.MT * G + t * G);
+                    for (int st = 0; st < F / 16; ++st) {
+                        // A: H_k, MN-major; 8 f-rows per 1024-byte atom, b chunks F*128 apart
+                        const uint64_t ad = sdesc(A + (uint32_t)t * 2 * F * 128 + (uint32_t)st * 2048,
+                                                  (uint32_t)F * 128, 1024, kLayoutSW128);
+                        // B: W_k, K-major; 32 bytes per 16 f inside a 128-byte row
+                        const uint64_t bd = sdesc(Wt + (uint32_t)(st / 4) * G * 128 + (uint32_t)(st % 4) * 32,
+                                                  16, 1024, kLayoutSW128);
+                        mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar_addr(c.empty[s]));
+                mma_commit(bar_addr(c.tfull[acc]));
+            }
+            __syncwarp();
+        }
+        if (lane == 0)
+            mma_commit(bar_addr(c.drain));
+        __syncwarp();
+        mbar_wait_drain(bar_addr(c.drain), 0);
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        double lacc = 0.0;
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(bar_addr(c.tfull[acc]), aph, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            for (int t = 0; t < a.MT; ++t) {
+                const int b = t * 128 + q * 32 + lane;
+                const bool valid = b < a.B;
+                for (int c0 = 0; c0 < G; c0 += CH) {
+                    float v[CH];
+                    tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) +
+                                          (uint32_t)(acc * a.MT * G + t * G + c0),
+                                      v);
+                    if (!valid)
+                        continue;
+                    const int64_t off = (int64_t)b * a.L + k * G + c0;
+                    if (a.Z)
+                        store_bf16_row<CH>(a.Z + off, v);
+                    if (BCE) {
+                        const uint32_t y = group_pos_mask(a.gptr, a.gent, k, b, c0, CH);
+                        float l = 0.f;
+#pragma unroll
+                        for (int i = 0; i < CH; ++i) {
+                            float lt;
+                            v[i] = bce_grad_loss(v[i], (int)((y >> i) & 1u), &lt);
+                            l += lt;
+                        }
+                        lacc += l;
+                        store_bf16_row<CH>(a.dZ + off, v);
+                        if (a.dZ_lo) {
+#pragma unroll
+                            for (int i = 0; i < CH; ++i)
+                                v[i] -= bf2f(f2bf(v[i]));
+                            store_bf16_row<CH>(a.dZ_lo + off, v);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(c.tempty[acc]));
+        }
+        if (BCE)
+            epi_sum_to(lacc, c, a.loss_part + blockIdx.x);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, a.tmem_cols);
+    }
+}
+
+// ================================================================== dW
+struct DWArgs {
+    const uint16_t *idx_s;
+    uint16_t *dW;
+    int32_t *status;
+    int64_t K, L;
+    int32_t B, G, F, MT, FT, S, nzc, zsw, npass;
+    uint32_t a_bytes, z_bytes, stage_bytes, tmem_cols;
+};
+
+template <int CH>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    k_tc_dW(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_z,
+            const __grid_constant__ CUtensorMap tm_zl, const DWArgs a)
+{
+    __shared__ Ctl c;
+    extern __shared__ uint8_t dsm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
+    const int G = a.G, F = a.F, S = a.S;
+    const uint32_t zrows = (uint32_t)a.MT * 128;
+
+    if (threadIdx.x == 0) {
+        c.abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_addr(c.full[s]), 1);
+            mbar_init(bar_addr(c.empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_addr(c.tfull[i]), 1);
+            mbar_init(bar_addr(c.tempty[i]), 128);
+        }
+        mbar_init(bar_addr(c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = c.tmem;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp == 0) {
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
+                break;
+            const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
+            const uint32_t Zs = A + a.a_bytes;
+            const uint32_t fb = bar_addr(c.full[s]);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(fb, a.a_bytes + a.z_bytes);
+                const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
+                for (int cj = 0; cj < a.nzc; ++cj) {
+                    tma_load_2d(Zs + (uint32_t)cj * zrows * a.zsw, &tm_z, (int)(k * G + cj * 64), 0, fb);
+                    if (a.npass > 1)
+                        tma_load_2d(Zs + zplane + (uint32_t)cj * zrows * a.zsw, &tm_zl,
+                                    (int)(k * G + cj * 64), 0, fb);
+                }
+            }
+            __syncwarp();
+            const uint16_t *I = a.idx_s + k * F;
+            const int ng = F / 4;
+            for (int q = lane; q < a.MT * 2 * ng; q += 32) {
+                const int g = q % ng, tcn = q / ng;
+                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(I + 4 * g));
+                tma_gather4(A + (uint32_t)tcn * F * 128 + (uint32_t)g * 512, &tm_h, tcn * 64,
+                            (int)(v.x & 0xffff), (int)(v.x >> 16), (int)(v.y & 0xffff),
+                            (int)(v.y >> 16), fb);
+            }
+        }
+        drain_loads(c, it, S);
+    } else if (warp == 1) {
+        const uint32_t idesc = idesc_bf16(128, G, 0, 1);
+        const uint32_t zlayout = layout_for_swizzle(a.zsw);
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(bar_addr(c.tempty[acc]), aph ^ 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
+                const uint32_t Zs = A + a.a_bytes;
+                const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
+                for (int tf = 0; tf < a.FT; ++tf) {
+                    const uint32_t d = tbase + (uint32_t)(acc * a.FT * G + tf * G);
+                    for (int ps = 0; ps < a.npass; ++ps) {      // dZ hi, then dZ lo
+                        for (int st = 0; st < a.MT * 8; ++st) {
+                            // A: H_k^T, K-major (rows f, K = b): b chunk st/4, 32 B per 16 b
+                            const uint64_t ad = sdesc(A + (uint32_t)(st / 4) * F * 128 +
+                                                          (uint32_t)tf * 128 * 128 + (uint32_t)(st % 4) * 32,
+                                                      16, 1024, kLayoutSW128);
+                            // B: dZ_k, MN-major (N = j, K = b): 16 b rows per step
+                            const uint64_t bd = sdesc(Zs + (uint32_t)ps * zplane + (uint32_t)st * 16 * a.zsw,
+                                                      zrows * a.zsw, 8 * a.zsw, zlayout);
+                            mma_bf16(d, ad, bd, idesc, (ps > 0 || st > 0) ? 1u : 0u);
+                        }
+                    }
+                }
+                mma_commit(bar_addr(c.empty[s]));
+                mma_commit(bar_addr(c.tfull[acc]));
+            }
+            __syncwarp();
+        }
+        if (lane == 0)
+            mma_commit(bar_addr(c.drain));
+        __syncwarp();
+        mbar_wait_drain(bar_addr(c.drain), 0);
+    } else {
+        const int q = warp & 3;
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(bar_addr(c.tfull[acc]), aph, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            for (int tf = 0; tf < a.FT; ++tf) {
+                const int f = tf * 128 + q * 32 + lane;
+                for (int c0 = 0; c0 < G; c0 += CH) {
+                    float v[CH];
+                    tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) +
+                                          (uint32_t)(acc * a.FT * G + tf * G + c0),
+                                      v);
+                    uint16_t *dst = a.dW + (k * G + c0) * F + f;
+#pragma unroll
+                    for (int i = 0; i < CH; ++i)
+                        dst[(int64_t)i * F] = f2bf(v[i]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(c.tempty[acc]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, a.tmem_cols);
+    }
+}
+
+// ================================================================== dh
+struct DhArgs {
+    const uint16_t *idx_s;
+    float *dh;
+    int32_t *status;
+    int64_t K, L;
+    int32_t B, G, F, H, MT, nk, S, nzc, zsw, nbands, band_w, parts, npass;
+    uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, tmem_cols;
+};
+
+// CTA (band, mtile, part): dh columns [i0, i1) of the band, samples
+// [128 mt, 128 mt + 128), groups k = part, part + parts, ...  TMEM columns
+// [0, band_w) hold the CTA's fp32 partial of dh, [band_w, band_w + F) the
+// dH_k pieces of the current group.
+__global__ void __launch_bounds__(kDhThreads, 1)
+    k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
+            const __grid_constant__ CUtensorMap tm_w, const DhArgs a)
+{
+    __shared__ Ctl c;
+    extern __shared__ uint8_t dsm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
+    uint8_t *stage0_ptr = dsm + (stage0 - smem_u32(dsm));
+    const int G = a.G, F = a.F, S = a.S;
+    const int band = blockIdx.x % a.nbands;
+    const int mt = (blockIdx.x / a.nbands) % a.MT;
+    const int part = blockIdx.x / (a.nbands * a.MT);
+    const int i0 = band * a.band_w;
+    const int i1 = min(a.H, i0 + a.band_w);
+    const uint32_t zrows = 128;
+
+    if (threadIdx.x == 0) {
+        c.abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_addr(c.full[s]), 1);
+            mbar_init(bar_addr(c.empty[s]), 128);  // released by the epilogue
+        }
+        mbar_init(bar_addr(c.tfull[0]), 1);
+        mbar_init(bar_addr(c.tempty[0]), 128);
+        mbar_init(bar_addr(c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = c.tmem;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp == 0) {
+        int it = 0;
+        for (int64_t k = part; k < a.K; k += a.parts, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
+                break;
+            const uint32_t Zs = stage0 + (uint32_t)s * a.stage_bytes;
+            const uint32_t Wt = Zs + a.z_bytes;
+            const uint32_t Is = Wt + a.w_bytes;
+            const uint32_t fb = bar_addr(c.full[s]);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(fb, a.z_bytes + a.w_bytes + (uint32_t)F * 2);
+                const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
+                for (int cj = 0; cj < a.nzc; ++cj) {
+                    tma_load_2d(Zs + (uint32_t)cj * zrows * a.zsw, &tm_z, (int)(k * G + cj * 64),
+                                mt * 128, fb);
+                    if (a.npass > 1)
+                        tma_load_2d(Zs + zplane + (uint32_t)cj * zrows * a.zsw, &tm_zl,
+                                    (int)(k * G + cj * 64), mt * 128, fb);
+                }
+                for (int kc = 0; kc < a.nk; ++kc)
+                    tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
+                bulk_load(Is, a.idx_s + k * F, (uint32_t)F * 2, fb);
+            }
+            __syncwarp();
+        }
+        drain_loads(c, it, S);
+    } else if (warp == 1) {
+        const uint32_t idesc = idesc_bf16(128, 16, 0, 1);
+        const uint32_t zlayout = layout_for_swizzle(a.zsw);
+        int it = 0;
+        for (int64_t k = part; k < a.K; k += a.parts, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            if (!mbar_wait(bar_addr(c.tempty[0]), ((uint32_t)it & 1u) ^ 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t Zs = stage0 + (uint32_t)s * a.stage_bytes;
+                const uint32_t Wt = Zs + a.z_bytes;
+                const uint16_t *I = reinterpret_cast<const uint16_t *>(
+                    stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes + a.w_bytes);
+                // f range whose index falls in [i0, i1): I_k is ascending
+                int fa = 0, fbnd = 0;
+                for (int f = 0; f < F; ++f) {
+                    const int v = I[f];
+                    fa += v < i0;
+                    fbnd += v < i1;
+                }
+                const int p0 = fa / 16, p1 = (fbnd + 15) / 16;
+                const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
+                const int nks = G / 16;
+                for (int p = p0; p < p1; ++p) {
+                    const int f0 = p * 16;
+                    const uint32_t d = tbase + (uint32_t)(a.band_w + (p - p0) * 16);
+                    // K runs over j twice: dZ hi against W_k, then dZ lo against W_k
+                    for (int ks2 = 0; ks2 < a.npass * nks; ++ks2) {
+                        const int ks = ks2 % nks;
+                        // A: dZ_k, K-major (rows b, K = j)
+                        const uint32_t za = Zs + (uint32_t)(ks2 / nks) * zplane +
+                                            (uint32_t)(ks / 4) * zrows * 128 + (uint32_t)(ks % 4) * 32;
+                        const uint64_t ad = sdesc(za, 16, 8 * a.zsw, zlayout);
+                        // B: W_k, MN-major (N = f, K = j): 16 j rows = 2 atoms
+                        const uint64_t bd = sdesc(Wt + (uint32_t)(f0 / 64) * G * 128 +
+                                                      (uint32_t)(f0 % 64) * 2 + (uint32_t)ks * 2048,
+                                                  (uint32_t)G * 128, 1024, kLayoutSW128);
+                        mma_bf16(d, ad, bd, idesc, ks2 > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar_addr(c.tfull[0]));
+            }
+            __syncwarp();
+        }
+        if (lane == 0)
+            mma_commit(bar_addr(c.drain));
+        __syncwarp();
+        mbar_wait_drain(bar_addr(c.drain), 0);
+    } else {
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        // zero the partial
+        for (int col = 0; col < a.band_w; ++col)
+            tmem_st1(tbase + lane_off + (uint32_t)col, 0u);
+        tmem_st_wait();
+        int it = 0;
+        for (int64_t k = part; k < a.K; k += a.parts, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
+                break;
+            if (!mbar_wait(bar_addr(c.tfull[0]), (uint32_t)it & 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            const uint16_t *I = reinterpret_cast<const uint16_t *>(
+                stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes + a.w_bytes);
+            int fa = 0, fbnd = 0;
+            for (int f = 0; f < F; ++f) {
+                const int v = I[f];
+                fa += v < i0;
+                fbnd += v < i1;
+            }
+            const int p0 = fa / 16, p1 = (fbnd + 15) / 16;
+            for (int p = p0; p < p1; ++p) {
+                uint32_t r[16];
+                tmem_ld16(tbase + lane_off + (uint32_t)(a.band_w + (p - p0) * 16), r);
+                uint32_t old[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int f = p * 16 + u;
+                    old[u] = 0u;
+                    if (f >= fa && f < fbnd)
+                        old[u] = tmem_ld1(tbase + lane_off + (uint32_t)(I[f] - i0));
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int f = p * 16 + u;
+                    if (f >= fa && f < fbnd)
+                        tmem_st1(tbase + lane_off + (uint32_t)(I[f] - i0),
+                                 __float_as_uint(__uint_as_float(old[u]) + __uint_as_float(r[u])));
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_addr(c.tempty[0]));
+            mbar_arrive(bar_addr(c.empty[s]));
+        }
+        // add the partial into dh
+        const int b = mt * 128 + q * 32 + lane;
+        for (int c0 = 0; c0 < a.band_w; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + lane_off + (uint32_t)c0, r);
+            tmem_ld_wait();
+            if (b < a.B) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = i0 + c0 + i;
+                    if (col < i1)
+                        atomicAdd(a.dh + (int64_t)b * a.H + col, __uint_as_float(r[i]));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, a.tmem_cols);
+    }
+}
+
+template <typename K>
+sg_status set_smem(K kern, size_t bytes)
+{
+    SG_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+    return SG_OK;
+}
+
+int persistent_grid(const sg_layout *lo, int64_t work)
+{
+    int64_t g = lo->num_sms;
+    if (g > work)
+        g = work;
+    if (g < 1)
+        g = 1;
+    return (int)g;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host side
+bool tc_supported(const sg_layout *lo) { return plan_fwd(lo, lo->max_B).ok; }
+
+bool tc_stage_ok(const sg_layout *lo, int stage, int B)
+{
+    switch (stage) {
+    case SG_KIND_FWD: return plan_fwd(lo, B).ok;
+    case SG_KIND_DW: return plan_dW(lo, B, true).ok;
+    case SG_KIND_DH: return plan_dh(lo, B, true).ok;
+    default: return false;
+    }
+}
+
+sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint16_t *dZ,
+                 uint16_t *dZ_lo, double *loss, cudaStream_t st)
+{
+    const FwdPlan p = plan_fwd(lo, B);
+    if (!p.ok) {
+        sg_set_error("tc_fwd: shape not supported by the tensor-core engine");
+        return SG_ERR_UNSUPPORTED;
+    }
+    CUtensorMap tm_h, tm_w;
+    sg_status rc = make_map_2d(&tm_h, lo->hT, (uint64_t)lo->ldB, (uint64_t)lo->H, 64, 1, 128, "hT");
+    if (rc != SG_OK)
+        return rc;
+    rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)lo->G, 128, "W");
+    if (rc != SG_OK)
+        return rc;
+    FwdArgs a;
+    a.idx_s = lo->idx_s;
+    a.Z = Z;
+    a.dZ = dZ;
+    a.dZ_lo = dZ_lo;
+    a.gptr = lo->gptr;
+    a.gent = lo->gent;
+    a.loss_part = lo->loss_part;
+    a.status = lo->status;
+    a.K = lo->K;
+    a.L = lo->L;
+    a.B = B;
+    a.G = lo->G;
+    a.F = lo->F;
+    a.MT = p.MT;
+    a.nk = p.nk;
+    a.S = p.S;
+    a.a_bytes = p.a_bytes;
+    a.w_bytes = p.w_bytes;
+    a.stage_bytes = p.stage_bytes;
+    a.tmem_cols = p.tmem_cols;
+    const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
+    const int grid = persistent_grid(lo, lo->K);
+    const bool bce = dZ != nullptr;
+    void (*kern)(CUtensorMap, CUtensorMap, FwdArgs);
+    if (lo->G % 32 == 0)
+        kern = bce ? k_tc_fwd<true, 32> : k_tc_fwd<false, 32>;
+    else
+        kern = bce ? k_tc_fwd<true, 16> : k_tc_fwd<false, 16>;
+    rc = set_smem(kern, smem);
+    if (rc != SG_OK)
+        return rc;
+    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, kFwdThreads, smem, st>>>(tm_h, tm_w, a));
+    SG_TRY_CUDA(cudaGetLastError());
+    if (bce)
+        return sg_loss_finalize(lo, grid, loss, st);
+    return SG_OK;
+}
+
+sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B,
+                uint16_t *dW, cudaStream_t st)
+{
+    const DWPlan p = plan_dW(lo, B, dZ_lo != nullptr);
+    if (!p.ok) {
+        sg_set_error("tc_dW: shape not supported by the tensor-core engine");
+        return SG_ERR_UNSUPPORTED;
+    }
+    CUtensorMap tm_h, tm_z;
+    sg_status rc = make_map_2d(&tm_h, lo->hT, (uint64_t)lo->ldB, (uint64_t)lo->H, 64, 1, 128, "hT");
+    if (rc != SG_OK)
+        return rc;
+    const int zbox = lo->G < 64 ? lo->G : 64;
+    rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
+                     (uint32_t)(p.MT * 128), p.zsw, "dZ");
+    if (rc != SG_OK)
+        return rc;
+    CUtensorMap tm_zl = tm_z;
+    if (dZ_lo) {
+        rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
+                         (uint32_t)(p.MT * 128), p.zsw, "dZ_lo");
+        if (rc != SG_OK)
+            return rc;
+    }
+    DWArgs a;
+    a.idx_s = lo->idx_s;
+    a.dW = dW;
+    a.status = lo->status;
+    a.K = lo->K;
+    a.L = lo->L;
+    a.B = B;
+    a.G = lo->G;
+    a.F = lo->F;
+    a.MT = p.MT;
+    a.FT = p.FT;
+    a.S = p.S;
+    a.nzc = p.nzc;
+    a.zsw = p.zsw;
+    a.npass = dZ_lo ? 2 : 1;
+    a.a_bytes = p.a_bytes;
+    a.z_bytes = p.z_bytes;
+    a.stage_bytes = p.stage_bytes;
+    a.tmem_cols = p.tmem_cols;
+    const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
+    const int grid = persistent_grid(lo, lo->K);
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, DWArgs) =
+        lo->G % 32 == 0 ? k_tc_dW<32> : k_tc_dW<16>;
+    rc = set_smem(kern, smem);
+    if (rc != SG_OK)
+        return rc;
+    SG_LAUNCH(lo, SG_KIND_DW, st, kern<<<grid, kFwdThreads, smem, st>>>(tm_h, tm_z, tm_zl, a));
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B,
+                const uint16_t *W, float *dh, cudaStream_t st)
+{
+    const DhPlan p = plan_dh(lo, B, dZ_lo != nullptr);
+    if (!p.ok) {
+        sg_set_error("tc_dh: shape not supported by the tensor-core engine");
+        return SG_ERR_UNSUPPORTED;
+    }
+    CUtensorMap tm_z, tm_w;
+    const int zbox = lo->G < 64 ? lo->G : 64;
+    sg_status rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox, 128,
+                               p.zsw, "dZ");
+    if (rc != SG_OK)
+        return rc;
+    CUtensorMap tm_zl = tm_z;
+    if (dZ_lo) {
+        rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox, 128, p.zsw,
+                         "dZ_lo");
+        if (rc != SG_OK)
+            return rc;
+    }
+    rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)lo->G, 128, "W");
+    if (rc != SG_OK)
+        return rc;
+    DhArgs a;
+    a.idx_s = lo->idx_s;
+    a.dh = dh;
+    a.status = lo->status;
+    a.K = lo->K;
+    a.L = lo->L;
+    a.B = B;
+    a.G = lo->G;
+    a.F = lo->F;
+    a.H = lo->H;
+    a.MT = p.MT;
+    a.nk = p.nk;
+    a.S = p.S;
+    a.nzc = p.nzc;
+    a.zsw = p.zsw;
+    a.nbands = p.nbands;
+    a.band_w = p.band_w;
+    a.npass = dZ_lo ? 2 : 1;
+    int parts = lo->num_sms / (p.nbands * p.MT);
+    if (parts < 1)
+        parts = 1;
+    if (parts > lo->K)
+        parts = (int)lo->K;
+    a.parts = parts;
+    a.z_bytes = p.z_bytes;
+    a.w_bytes = p.w_bytes;
+    a.i_bytes = p.i_bytes;
+    a.stage_bytes = p.stage_bytes;
+    a.tmem_cols = p.tmem_cols;
+    const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
+    rc = set_smem(k_tc_dh, smem);
+    if (rc != SG_OK)
+        return rc;
+    SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
+    SG_LAUNCH(lo, SG_KIND_DH, st,
+              k_tc_dh<<<p.nbands * p.MT * parts, kDhThreads, smem, st>>>(tm_z, tm_zl, tm_w, a));
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW, float *dh,
+                  double *loss, cudaStream_t st)
+{
+    (void)lo; (void)B; (void)W; (void)dW; (void)dh; (void)loss; (void)st;
+    sg_set_error("tc_step: the fused step kernel is not built yet");
     return SG_ERR_UNSUPPORTED;
-}
-
-sg_status tc_fwd(sg_layout *, int32_t, const uint16_t *, uint16_t *, uint16_t *,
-                 double *, cudaStream_t)
-{
-    return tc_unavailable("tc_fwd");
-}
-sg_status tc_dW(sg_layout *, const uint16_t *, int32_t, uint16_t *, cudaStream_t)
-{
-    return tc_unavailable("tc_dW");
-}
-sg_status tc_dh(sg_layout *, const uint16_t *, int32_t, const uint16_t *, float *,
-                cudaStream_t)
-{
-    return tc_unavailable("tc_dh");
-}
-sg_status tc_step(sg_layout *, int32_t, const uint16_t *, uint16_t *, float *,
-                  double *, cudaStream_t)
-{
-    return tc_unavailable("tc_step");
 }

@@ -34,7 +34,25 @@ CASES = [
     (_w("dense_F_eq_H", B=16, H=32, L=16 * 12, G=16, F=32), (SIMT, TC)),
     (_w("clustered", B=64, H=768, L=16 * 100, G=16, F=128, idx_mode="clustered"), (SIMT, TC)),
     (_w("b256_f256", B=256, H=512, L=32 * 20, G=32, F=256, pos=4), (SIMT, TC)),
+    # shapes of the three label-space workloads, fewer groups
+    (_w("like3m", B=128, H=768, L=32 * 300, G=32, F=128, pos=36, dist="zipf"), (SIMT, TC)),
+    (_w("like670k", B=256, H=768, L=16 * 400, G=16, F=128, pos=5, dist="zipf"), (SIMT, TC)),
+    (_w("like8p6m", B=64, H=768, L=32 * 500, G=32, F=64, pos=10, dist="zipf"), (SIMT, TC)),
+    # ragged batch, one dh band; G above one 64-wide swizzle row; three bands
+    (_w("tc_b37_h320", B=37, H=320, L=16 * 64, G=16, F=128, pos=4), (SIMT, TC)),
+    (_w("tc_g128", B=100, H=768, L=128 * 20, G=128, F=128, pos=6, dist="zipf"), (SIMT, TC)),
+    (_w("tc_h1000", B=130, H=1000, L=32 * 40, G=32, F=128, pos=6), (SIMT, TC)),
 ]
+
+
+def _run(fn, *args, **kw):
+    """Call an entry point; a shape the pinned engine cannot run skips the test."""
+    try:
+        return fn(*args, **kw)
+    except sg.SGError as e:
+        if e.status == sg.SG_ERR_UNSUPPORTED:
+            pytest.skip(f"engine does not run this shape: {e}")
+        raise
 
 
 def _ids(case):
@@ -112,7 +130,7 @@ def test_fwd(case, engine):
     lay = _layout(p, engine)
     d = dev_problem(p)
     Z = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
-    sg.sg_fwd(lay, d["h"], d["W"], Z)
+    _run(sg.sg_fwd, lay, d["h"], d["W"], Z)
     assert_close(host_bf16_to_f64(Z), ref["Z"], what="Z")
     _status_ok(lay)
 
@@ -128,8 +146,8 @@ def test_fwd_bce(case, engine, oracle_mod):
     Z = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
     loss = torch.zeros(1, dtype=torch.float64, device="cuda")
     for with_z in (False, True):
-        sg.sg_fwd_bce(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dZ, loss,
-                      Z if with_z else None)
+        _run(sg.sg_fwd_bce, lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dZ, loss,
+             Z if with_z else None)
         assert_close(host_bf16_to_f64(dZ), ref["dZ"], what="dZ")
         assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
         if with_z:
@@ -166,13 +184,13 @@ def test_bwd_stage(case, engine, oracle_mod):
     dZ = dev_bf16(dzbits)
     dW = torch.empty((w.L, w.F), dtype=torch.int16, device="cuda")
     dh = torch.full((w.B, w.H), float("nan"), dtype=torch.float32, device="cuda")
-    sg.sg_bwd(lay, dZ, d["h"], d["W"], dW, dh)
+    _run(sg.sg_bwd_dW, lay, dZ, d["h"], dW)
     assert_close(host_bf16_to_f64(dW), want_dW, what="dW")
+    _run(sg.sg_bwd_dh, lay, dZ, w.B, d["W"], dh)
     assert_close(dh.cpu().numpy(), want_dh, what="dh")
     dW.zero_()
     dh.fill_(7.0)
-    sg.sg_bwd_dW(lay, dZ, d["h"], dW)
-    sg.sg_bwd_dh(lay, dZ, w.B, d["W"], dh)
+    _run(sg.sg_bwd, lay, dZ, d["h"], d["W"], dW, dh)
     assert_close(host_bf16_to_f64(dW), want_dW, what="dW")
     assert_close(dh.cpu().numpy(), want_dh, what="dh")
     _status_ok(lay)
@@ -190,7 +208,7 @@ def test_step_chain(case, engine):
     dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
     loss = torch.zeros(1, dtype=torch.float64, device="cuda")
     for _ in range(2):  # a second call must give the same answer (scratch reuse)
-        sg.sg_step(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dW, dh, loss)
+        _run(sg.sg_step, lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dW, dh, loss)
         assert_close(host_bf16_to_f64(dW), ref["dW"], what="dW")
         assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
         assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
