@@ -220,9 +220,12 @@ def run_ours(args):
     sg.build()
     sg.load()
     w = CONFIGS[args.workload]
+    if args.labels:
+        w = w.with_(L=args.labels, name=f"{w.name}_L{args.labels}")
     # weak scaling: every rank owns one shard of w.L labels (its own groups,
-    # W rows and positives); dh and the loss are summed over the shards
-    p = generate(w.with_(seed=w.seed + rank))
+    # W rows and positives; h is shared); dh and the loss are summed over the
+    # shards with one all-reduce each
+    p = generate(w, shard=rank)
 
     def i32(a):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
@@ -365,6 +368,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
     ap.add_argument("--engine", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--labels", type=int, default=0,
+                    help="override L (a multiple of G) for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)

@@ -19,6 +19,7 @@
 //          the feature gradient.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 
 #include "sg_internal.cuh"
 #include "tc_ptx.cuh"
@@ -29,8 +30,9 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 220 * 1024;  // dynamic shared memory we plan with
-constexpr int kFwdThreads = 192;         // producer, MMA, 4 epilogue warps
-constexpr int kDhThreads = 192;
+constexpr int kEpiWarps = 8;             // two per TMEM lane quarter
+constexpr int kFwdThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue warps
+constexpr int kDhThreads = 64 + 32 * kEpiWarps;
 
 // ------------------------------------------------------------------ plans
 struct FwdPlan {
@@ -203,28 +205,42 @@ struct Ctl {
     uint64_t drain;
     uint32_t tmem;
     int abort_flag;
-    double red[8];
+    double red[kEpiWarps];
 };
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_u32(&b); }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+// two floats -> packed bf16x2 (a in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack2(float a, float b)
 {
-    return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// store n (multiple of 8) floats as bf16 to 16-byte aligned global memory
+__device__ __forceinline__ float lo_half(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_half(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// store N (multiple of 8) floats as bf16 to 16-byte aligned global memory;
+// with `lo`, also store the rounding residual v - bf16(v) as a second plane
 template <int N>
-__device__ __forceinline__ void store_bf16_row(uint16_t *dst, const float (&v)[N])
+__device__ __forceinline__ void store_bf16_row(uint16_t *dst, uint16_t *lo, const float (&v)[N])
 {
 #pragma unroll
     for (int i = 0; i < N; i += 8) {
         uint4 q;
-        q.x = pack_bf16x2(v[i + 0], v[i + 1]);
-        q.y = pack_bf16x2(v[i + 2], v[i + 3]);
-        q.z = pack_bf16x2(v[i + 4], v[i + 5]);
-        q.w = pack_bf16x2(v[i + 6], v[i + 7]);
+        q.x = pack2(v[i + 0], v[i + 1]);
+        q.y = pack2(v[i + 2], v[i + 3]);
+        q.z = pack2(v[i + 4], v[i + 5]);
+        q.w = pack2(v[i + 6], v[i + 7]);
         *reinterpret_cast<uint4 *>(dst + i) = q;
+        if (lo) {
+            uint4 r;
+            r.x = pack2(v[i + 0] - lo_half(q.x), v[i + 1] - hi_half(q.x));
+            r.y = pack2(v[i + 2] - lo_half(q.y), v[i + 3] - hi_half(q.y));
+            r.z = pack2(v[i + 4] - lo_half(q.z), v[i + 5] - hi_half(q.z));
+            r.w = pack2(v[i + 6] - lo_half(q.w), v[i + 7] - hi_half(q.w));
+            *reinterpret_cast<uint4 *>(lo + i) = r;
+        }
     }
 }
 
@@ -248,20 +264,42 @@ __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, float (&v)[CH])
     }
 }
 
-// positives of sample b among columns c0 .. c0+CH-1 of group k
-__device__ __forceinline__ uint32_t group_pos_mask(const int32_t *__restrict__ gptr,
-                                                   const int32_t *__restrict__ gent, int64_t k,
-                                                   int b, int c0, int n)
+// positives of sample b among columns c0 .. c0+n-1 of a group whose entries
+// are gent[e0 .. e1)
+__device__ __forceinline__ uint32_t group_pos_mask(const int32_t *__restrict__ gent, int e0,
+                                                   int e1, int b, int c0, int n)
 {
     uint32_t y = 0;
-    const int e1 = __ldg(gptr + k + 1);
-    for (int e = __ldg(gptr + k); e < e1; ++e) {
+    for (int e = e0; e < e1; ++e) {
         const int v = __ldg(gent + e);
         const int jj = (v & 0xffff) - c0;
         if ((v >> 16) == b && jj >= 0 && jj < n)
             y |= 1u << jj;
     }
     return y;
+}
+
+// BCE on a chunk of logits in place: v[i] <- sigmoid(v[i]) - y_i; returns the
+// chunk's loss sum(max(z,0) - y z + log(1 + e^-|z|)).  The log of the product
+// of the (1 + e^-|z|) factors (each in (1, 2], so at most 2^32 for 32 of
+// them) replaces one log per element.
+template <int CH>
+__device__ __forceinline__ float bce_chunk(float (&v)[CH], uint32_t y)
+{
+    float prod = 1.f, lin = 0.f;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const float z = v[i];
+        const float e = __expf(-fabsf(z));
+        const float one_e = 1.f + e;
+        const float r = __fdividef(1.f, one_e);
+        const float sig = z >= 0.f ? r : e * r;
+        const bool yi = (y >> i) & 1u;
+        lin += fmaxf(z, 0.f) - (yi ? z : 0.f);
+        prod *= one_e;
+        v[i] = sig - (yi ? 1.f : 0.f);
+    }
+    return lin + __logf(prod);
 }
 
 // After an abort, wait (bounded) until the loads of the last stages issued
@@ -275,7 +313,7 @@ __device__ __forceinline__ void drain_loads(Ctl &c, int issued, int S)
         mbar_wait_drain(bar_addr(c.full[i % S]), (uint32_t)(i / S) & 1u);
 }
 
-// sum of one double per thread over the 128 epilogue threads (warps 2..5)
+// sum of one double per thread over the epilogue threads (warps 2 .. 2+kEpiWarps)
 __device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst)
 {
     for (int o = 16; o > 0; o >>= 1)
@@ -283,9 +321,44 @@ __device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst)
     const int ew = threadIdx.x / 32 - 2;
     if ((threadIdx.x & 31) == 0)
         c.red[ew] = v;
-    named_bar(1, 128);
-    if (ew == 0 && (threadIdx.x & 31) == 0)
-        *dst = c.red[0] + c.red[1] + c.red[2] + c.red[3];
+    named_bar(1, kEpiWarps * 32);
+    if (ew == 0 && (threadIdx.x & 31) == 0) {
+        double s = 0.0;
+        for (int i = 0; i < kEpiWarps; ++i)
+            s += c.red[i];
+        *dst = s;
+    }
+}
+
+// Producer side of the H_k gather: lane l issues the gather4 loads q = l,
+// l + 32, ... of the MT*2 b-chunks x F/4 row quads; its row indices come from
+// at most two quads (g = l mod F/4 and (l + 32) mod F/4), loaded one group
+// ahead so the TMA issue never waits on them.
+struct IdxQuads {
+    uint2 a, b;
+};
+
+__device__ __forceinline__ IdxQuads load_quads(const uint16_t *idx_s, int64_t k, int F, int lane)
+{
+    const int ng = F / 4;
+    const uint16_t *I = idx_s + k * F;
+    IdxQuads r;
+    r.a = __ldg(reinterpret_cast<const uint2 *>(I + 4 * (lane % ng)));
+    r.b = __ldg(reinterpret_cast<const uint2 *>(I + 4 * ((lane + 32) % ng)));
+    return r;
+}
+
+__device__ __forceinline__ void issue_gathers(const CUtensorMap *tm_h, uint32_t A, int F, int MT,
+                                              const IdxQuads &iq, int lane, uint32_t fb)
+{
+    const int ng = F / 4;
+    for (int q = lane; q < MT * 2 * ng; q += 32) {
+        const int g = q % ng, tcn = q / ng;
+        const uint2 v = (g == lane % ng) ? iq.a : iq.b;
+        tma_gather4(A + (uint32_t)tcn * F * 128 + (uint32_t)g * 512, tm_h, tcn * 64,
+                    (int)(v.x & 0xffff), (int)(v.x >> 16), (int)(v.y & 0xffff),
+                    (int)(v.y >> 16), fb);
+    }
 }
 
 // ================================================================== forward
@@ -319,7 +392,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c.tfull[i]), 1);
-            mbar_init(bar_addr(c.tempty[i]), 128);
+            mbar_init(bar_addr(c.tempty[i]), kEpiWarps * 32);
         }
         mbar_init(bar_addr(c.drain), 1);
         fence_mbar_init();
@@ -337,9 +410,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         int it = 0;
+        IdxQuads cur = {};
+        if (blockIdx.x < a.K)
+            cur = load_quads(a.idx_s, blockIdx.x, F, lane);
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
             const int s = it % S;
             const uint32_t ph = (uint32_t)(it / S) & 1u;
+            IdxQuads nxt = cur;
+            if (k + gridDim.x < a.K)
+                nxt = load_quads(a.idx_s, k + gridDim.x, F, lane);
             if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
                 break;
             const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
@@ -351,15 +430,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
             }
             __syncwarp();
-            const uint16_t *I = a.idx_s + k * F;
-            const int ng = F / 4;
-            for (int q = lane; q < a.MT * 2 * ng; q += 32) {
-                const int g = q % ng, tcn = q / ng;
-                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(I + 4 * g));
-                tma_gather4(A + (uint32_t)tcn * F * 128 + (uint32_t)g * 512, &tm_h, tcn * 64,
-                            (int)(v.x & 0xffff), (int)(v.x >> 16), (int)(v.y & 0xffff),
-                            (int)(v.y >> 16), fb);
-            }
+            issue_gathers(&tm_h, A, F, a.MT, cur, lane, fb);
+            cur = nxt;
         }
         drain_loads(c, it, S);
     } else if (warp == 1) {
@@ -403,46 +475,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_wait_drain(bar_addr(c.drain), 0);
     } else {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // two warps per TMEM lane quarter; they split the (tile, chunk) units
+        const int q = warp & 3;
+        const int sub = (warp - 2) / 4;
+        const int units = a.MT * (G / CH);
         double lacc = 0.0;
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            int e0 = 0, e1 = 0;
+            if (BCE) {
+                e0 = __ldg(a.gptr + k);
+                e1 = __ldg(a.gptr + k + 1);
+            }
             if (!mbar_wait(bar_addr(c.tfull[acc]), aph, abort_flag, a.status))
                 break;
             tc_fence_after();
-            for (int t = 0; t < a.MT; ++t) {
+            for (int u = sub; u < units; u += 2) {
+                const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
                 const int b = t * 128 + q * 32 + lane;
-                const bool valid = b < a.B;
-                for (int c0 = 0; c0 < G; c0 += CH) {
-                    float v[CH];
-                    tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) +
-                                          (uint32_t)(acc * a.MT * G + t * G + c0),
-                                      v);
-                    if (!valid)
-                        continue;
-                    const int64_t off = (int64_t)b * a.L + k * G + c0;
-                    if (a.Z)
-                        store_bf16_row<CH>(a.Z + off, v);
-                    if (BCE) {
-                        const uint32_t y = group_pos_mask(a.gptr, a.gent, k, b, c0, CH);
-                        float l = 0.f;
-#pragma unroll
-                        for (int i = 0; i < CH; ++i) {
-                            float lt;
-                            v[i] = bce_grad_loss(v[i], (int)((y >> i) & 1u), &lt);
-                            l += lt;
-                        }
-                        lacc += l;
-                        store_bf16_row<CH>(a.dZ + off, v);
-                        if (a.dZ_lo) {
-#pragma unroll
-                            for (int i = 0; i < CH; ++i)
-                                v[i] -= bf2f(f2bf(v[i]));
-                            store_bf16_row<CH>(a.dZ_lo + off, v);
-                        }
-                    }
+                float v[CH];
+                tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) +
+                                      (uint32_t)(acc * a.MT * G + t * G + c0),
+                                  v);
+                if (b >= a.B)
+                    continue;
+                const int64_t off = (int64_t)b * a.L + k * G + c0;
+                if (a.Z)
+                    store_bf16_row<CH>(a.Z + off, nullptr, v);
+                if (BCE) {
+                    const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
+                    lacc += bce_chunk<CH>(v, y);
+                    store_bf16_row<CH>(a.dZ + off, a.dZ_lo ? a.dZ_lo + off : nullptr, v);
                 }
             }
             tc_fence_before();
@@ -489,7 +554,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c.tfull[i]), 1);
-            mbar_init(bar_addr(c.tempty[i]), 128);
+            mbar_init(bar_addr(c.tempty[i]), kEpiWarps * 32);
         }
         mbar_init(bar_addr(c.drain), 1);
         fence_mbar_init();
@@ -506,9 +571,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
     if (warp == 0) {
         int it = 0;
+        IdxQuads cur = {};
+        if (blockIdx.x < a.K)
+            cur = load_quads(a.idx_s, blockIdx.x, F, lane);
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
             const int s = it % S;
             const uint32_t ph = (uint32_t)(it / S) & 1u;
+            IdxQuads nxt = cur;
+            if (k + gridDim.x < a.K)
+                nxt = load_quads(a.idx_s, k + gridDim.x, F, lane);
             if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
                 break;
             const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
@@ -525,15 +596,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
             __syncwarp();
-            const uint16_t *I = a.idx_s + k * F;
-            const int ng = F / 4;
-            for (int q = lane; q < a.MT * 2 * ng; q += 32) {
-                const int g = q % ng, tcn = q / ng;
-                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(I + 4 * g));
-                tma_gather4(A + (uint32_t)tcn * F * 128 + (uint32_t)g * 512, &tm_h, tcn * 64,
-                            (int)(v.x & 0xffff), (int)(v.x >> 16), (int)(v.y & 0xffff),
-                            (int)(v.y >> 16), fb);
-            }
+            issue_gathers(&tm_h, A, F, a.MT, cur, lane, fb);
+            cur = nxt;
         }
         drain_loads(c, it, S);
     } else if (warp == 1) {
@@ -581,6 +645,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_wait_drain(bar_addr(c.drain), 0);
     } else {
         const int q = warp & 3;
+        const int sub = (warp - 2) / 4;
+        const int units = a.FT * (G / CH);
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
             const int acc = it & 1;
@@ -588,18 +654,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!mbar_wait(bar_addr(c.tfull[acc]), aph, abort_flag, a.status))
                 break;
             tc_fence_after();
-            for (int tf = 0; tf < a.FT; ++tf) {
+            for (int u = sub; u < units; u += 2) {
+                const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
                 const int f = tf * 128 + q * 32 + lane;
-                for (int c0 = 0; c0 < G; c0 += CH) {
-                    float v[CH];
-                    tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) +
-                                          (uint32_t)(acc * a.FT * G + tf * G + c0),
-                                      v);
-                    uint16_t *dst = a.dW + (k * G + c0) * F + f;
+                float v[CH];
+                tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) +
+                                      (uint32_t)(acc * a.FT * G + tf * G + c0),
+                                  v);
+                uint16_t *dst = a.dW + (k * G + c0) * F + f;
 #pragma unroll
-                    for (int i = 0; i < CH; ++i)
-                        dst[(int64_t)i * F] = f2bf(v[i]);
-                }
+                for (int i = 0; i < CH; ++i)
+                    dst[(int64_t)i * F] = f2bf(v[i]);
             }
             tc_fence_before();
             mbar_arrive(bar_addr(c.tempty[acc]));
@@ -622,6 +687,20 @@ struct DhArgs {
     int32_t B, G, F, H, MT, nk, S, nzc, zsw, nbands, band_w, parts, npass;
     uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, tmem_cols;
 };
+
+// first f with I[f] >= v (I ascending, n entries)
+__device__ __forceinline__ int lower_bound_u16(const uint16_t *I, int n, int v)
+{
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((int)I[mid] < v)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
+}
 
 // CTA (band, mtile, part): dh columns [i0, i1) of the band, samples
 // [128 mt, 128 mt + 128), groups k = part, part + parts, ...  TMEM columns
@@ -648,10 +727,10 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         c.abort_flag = 0;
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_addr(c.full[s]), 1);
-            mbar_init(bar_addr(c.empty[s]), 128);  // released by the epilogue
+            mbar_init(bar_addr(c.empty[s]), kEpiWarps * 32);  // released by the epilogue
         }
         mbar_init(bar_addr(c.tfull[0]), 1);
-        mbar_init(bar_addr(c.tempty[0]), 128);
+        mbar_init(bar_addr(c.tempty[0]), kEpiWarps * 32);
         mbar_init(bar_addr(c.drain), 1);
         fence_mbar_init();
     }
@@ -712,12 +791,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 const uint16_t *I = reinterpret_cast<const uint16_t *>(
                     stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes + a.w_bytes);
                 // f range whose index falls in [i0, i1): I_k is ascending
-                int fa = 0, fbnd = 0;
-                for (int f = 0; f < F; ++f) {
-                    const int v = I[f];
-                    fa += v < i0;
-                    fbnd += v < i1;
-                }
+                const int fa = lower_bound_u16(I, F, i0), fbnd = lower_bound_u16(I, F, i1);
                 const int p0 = fa / 16, p1 = (fbnd + 15) / 16;
                 const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
                 const int nks = G / 16;
@@ -747,10 +821,11 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         __syncwarp();
         mbar_wait_drain(bar_addr(c.drain), 0);
     } else {
+        // two warps per TMEM lane quarter; pieces alternate between them
         const int q = warp & 3;
+        const int sub = (warp - 2) / 4;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        // zero the partial
-        for (int col = 0; col < a.band_w; ++col)
+        for (int col = sub; col < a.band_w; col += 2)
             tmem_st1(tbase + lane_off + (uint32_t)col, 0u);
         tmem_st_wait();
         int it = 0;
@@ -764,32 +839,26 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             tc_fence_after();
             const uint16_t *I = reinterpret_cast<const uint16_t *>(
                 stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes + a.w_bytes);
-            int fa = 0, fbnd = 0;
-            for (int f = 0; f < F; ++f) {
-                const int v = I[f];
-                fa += v < i0;
-                fbnd += v < i1;
-            }
+            const int fa = lower_bound_u16(I, F, i0), fbnd = lower_bound_u16(I, F, i1);
             const int p0 = fa / 16, p1 = (fbnd + 15) / 16;
-            for (int p = p0; p < p1; ++p) {
+            for (int p = p0 + sub; p < p1; p += 2) {
                 uint32_t r[16];
                 tmem_ld16(tbase + lane_off + (uint32_t)(a.band_w + (p - p0) * 16), r);
-                uint32_t old[16];
+                uint32_t col[16], old[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int f = p * 16 + u;
+                    col[u] = (f >= fa && f < fbnd) ? (uint32_t)(I[f] - i0) : 0xffffffffu;
                     old[u] = 0u;
-                    if (f >= fa && f < fbnd)
-                        old[u] = tmem_ld1(tbase + lane_off + (uint32_t)(I[f] - i0));
+                    if (col[u] != 0xffffffffu)
+                        old[u] = tmem_ld1(tbase + lane_off + col[u]);
                 }
                 tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int f = p * 16 + u;
-                    if (f >= fa && f < fbnd)
-                        tmem_st1(tbase + lane_off + (uint32_t)(I[f] - i0),
+                for (int u = 0; u < 16; ++u)
+                    if (col[u] != 0xffffffffu)
+                        tmem_st1(tbase + lane_off + col[u],
                                  __float_as_uint(__uint_as_float(old[u]) + __uint_as_float(r[u])));
-                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -798,16 +867,16 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         }
         // add the partial into dh
         const int b = mt * 128 + q * 32 + lane;
-        for (int c0 = 0; c0 < a.band_w; c0 += 32) {
+        for (int c0 = sub * 32; c0 < a.band_w; c0 += 64) {
             uint32_t r[32];
             tmem_ld32(tbase + lane_off + (uint32_t)c0, r);
             tmem_ld_wait();
             if (b < a.B) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int col = i0 + c0 + i;
-                    if (col < i1)
-                        atomicAdd(a.dh + (int64_t)b * a.H + col, __uint_as_float(r[i]));
+                    const int colg = i0 + c0 + i;
+                    if (colg < i1)
+                        atomicAdd(a.dh + (int64_t)b * a.H + colg, __uint_as_float(r[i]));
                 }
             }
         }
@@ -892,7 +961,7 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     const int grid = persistent_grid(lo, lo->K);
     const bool bce = dZ != nullptr;
     void (*kern)(CUtensorMap, CUtensorMap, FwdArgs);
-    if (lo->G % 32 == 0)
+    if (lo->G >= 64)
         kern = bce ? k_tc_fwd<true, 32> : k_tc_fwd<false, 32>;
     else
         kern = bce ? k_tc_fwd<true, 16> : k_tc_fwd<false, 16>;
@@ -952,7 +1021,7 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, DWArgs) =
-        lo->G % 32 == 0 ? k_tc_dW<32> : k_tc_dW<16>;
+        lo->G >= 64 ? k_tc_dW<32> : k_tc_dW<16>;
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;

@@ -200,15 +200,19 @@ def _draw_positives(rng, B: int, L: int, n: int, dist: str, s: float):
     return rowptr, labels
 
 
-def generate(w: Workload, *, B: Optional[int] = None) -> Problem:
+def generate(w: Workload, *, B: Optional[int] = None, shard: int = 0) -> Problem:
     """Draw one problem instance for workload `w` (deterministic in w.seed).
 
     `B` overrides the batch size (used for bounded samples); the other draws do
-    not depend on it except h and the positives."""
+    not depend on it except h and the positives.  `shard` > 0 draws another
+    label shard of the same batch: groups, idx, W and positives come from their
+    own streams, h is the shard-0 h (the samples are shared)."""
     if w.L % w.G:
         raise ValueError("L must be a multiple of G")
     B = w.B if B is None else B
     s_groups, s_idx, s_h, s_W, s_pos = np.random.SeedSequence(w.seed).spawn(5)
+    if shard:
+        s_groups, s_idx, _, s_W, s_pos = np.random.SeedSequence([w.seed, shard]).spawn(5)
     groups = _draw_groups(_rng(s_groups), w.L, w.G)
     idx = _draw_idx(_rng(s_idx), w.K, w.F, w.H, w.idx_mode)
     h = _draw_normal_bf16(_rng(s_h), B, w.H, 1.0)
