@@ -61,6 +61,7 @@ def load():
             "sg_bwd_dW": ([P, P, P, i32, P, P], C.c_int),
             "sg_bwd_dh": ([P, P, i32, P, P, P], C.c_int),
             "sg_step": ([P, P, i32, P, P, P, i64, P, P, P, P], C.c_int),
+            "sg_bce_grad_noalloc": ([P, i32, i64, i32, P, P, i64, P, P, P], C.c_int),
             "sg_timing_start": ([P, i32], C.c_int),
             "sg_timing_stop": ([P, P, P], C.c_int),
             "sg_last_error": ([], C.c_char_p),
@@ -273,3 +274,15 @@ def sg_timing_stop(layout: Layout):
     n = (C.c_int32 * len(KIND_NAMES))()
     _check(load().sg_timing_stop(layout, C.cast(ms, C.c_void_p), C.cast(n, C.c_void_p)))
     return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KIND_NAMES)}
+
+
+# ---------------------------------------------------------------- no allocation
+def sg_bce_grad_noalloc(Z, B: int, L: int, G: int, pos_rowptr, pos_slot, nnz: int, dZ, loss):
+    """sg_bce_grad without a layout and without any device allocation: for
+    callers whose device memory is owned by someone else.  Positives are slot
+    ids.  Calls share one fixed working array: do not overlap them."""
+    ps = _dev(pos_slot, "pos_slot", _I32, nnz) if nnz else C.c_void_p(0)
+    _check(load().sg_bce_grad_noalloc(_dev(Z, "Z", _BF16, B * L), B, L, G,
+                                      _dev(pos_rowptr, "pos_rowptr", _I32, B + 1), ps, nnz,
+                                      _dev(dZ, "dZ", _BF16, B * L),
+                                      _dev(loss, "loss", (torch.float64,), 1), _stream(Z.device)))

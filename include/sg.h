@@ -213,6 +213,31 @@ SG_API sg_status sg_timing_start(sg_layout *layout, int32_t capacity);
 SG_API sg_status sg_timing_stop(sg_layout *layout, double *ms_per_kind,
                                 int32_t *launches_per_kind);
 
+/* ---------------------------------------------------------------- no allocation
+ * sg_bce_grad_noalloc -- the same BCE step as sg_bce_grad (dZ = sigmoid(Z) - Y,
+ * bf16, and the summed loss, double), for callers that cannot allocate device
+ * memory: processes whose framework's caching allocator already holds the
+ * device memory, or deployments that allow no allocation after start-up.  It
+ * needs no layout and calls no allocator (cudaMalloc, cudaFree or any library
+ * routine that allocates).  The paper has no counterpart: this is a service
+ * of the library, not part of the method.
+ *   Z[B][L], dZ[B][L] bf16, slot order; L = K*G.
+ *   pos_rowptr[B+1], pos_slot[nnz]: each sample's positives as SLOT ids in
+ *   [0, L) (any order, duplicates count once); out-of-range slots and
+ *   malformed rows are dropped, since there is no layout status word.
+ * Working memory is one device array built into the library (about 3.2 MB,
+ * held by every GPU that loads the library until the process exits), so the
+ * sizes are capped: B <= 256, L/G <= 300000, nnz <= 65536; larger calls
+ * return SG_ERR_UNSUPPORTED before launching anything.  Every call uses that
+ * same array (it clears what must start at zero), so calls that overlap on
+ * the GPU -- from two streams or two host threads -- race; serialize them.
+ * The first call on a device looks up the array's device address (a runtime
+ * query, no allocation); make that first call before any stream capture.
+ * Asynchronous on `stream` otherwise.                                       */
+SG_API sg_status sg_bce_grad_noalloc(const sg_bf16 *Z, int32_t B, int64_t L, int32_t G,
+                                     const int32_t *pos_rowptr, const int32_t *pos_slot,
+                                     int64_t nnz, sg_bf16 *dZ, double *loss, void *stream);
+
 /* ---------------------------------------------------------------- misc */
 /* Message of the last failing call on this host thread ("" if none). */
 SG_API const char *sg_last_error(void);
