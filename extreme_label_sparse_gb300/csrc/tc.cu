@@ -30,26 +30,33 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 220 * 1024;  // dynamic shared memory we plan with
-constexpr int kEpiWarps = 8;             // two per TMEM lane quarter
-constexpr int kFwdThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue warps
-constexpr int kDhThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiWarps = 8;   // two per TMEM lane quarter
+constexpr int kProdWarps = 4;  // cp.async gather + TMA issue
+// forward / dW: producers, two MMA-issuing warps, epilogue
+constexpr int kFwdThreads = 32 * (kProdWarps + 2 + kEpiWarps);
+constexpr int kFirstEpi = kProdWarps + 2;
+// dh: one TMA producer, one MMA warp, epilogue
+constexpr int kDhThreads = 32 * (2 + kEpiWarps);
 
 // ------------------------------------------------------------------ plans
 struct FwdPlan {
     bool ok = false;
-    int MT = 0, nk = 0, S = 0;
+    int MT = 0, nk = 0, S = 0, issuers = 0;
     uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, tmem_cols = 0;
 };
 
 struct DWPlan {
     bool ok = false;
-    int MT = 0, FT = 0, S = 0, nzc = 0, zsw = 0;
+    int MT = 0, FT = 0, S = 0, nzc = 0, zsw = 0, issuers = 0;
+    int planes = 0;   // dZ planes in smem (2 with the lo residual)
+    int ncat = 0;     // 1: the planes are concatenated along N in one pass
+    int Nacc = 0;     // accumulator columns per (f tile, group)
     uint32_t a_bytes = 0, z_bytes = 0, stage_bytes = 0, tmem_cols = 0;
 };
 
 struct DhPlan {
     bool ok = false;
-    int MT = 0, nk = 0, S = 0, nzc = 0, zsw = 0, nbands = 0, band_w = 0;
+    int MT = 0, nk = 0, S = 0, nzc = 0, zsw = 0, nbands = 0, band_w = 0, win = 0;
     uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, tmem_cols = 0;
 };
 
@@ -64,7 +71,13 @@ uint32_t pow2_cols(int n)
 bool shape_ok(const sg_layout *lo)
 {
     return lo->G % 16 == 0 && lo->G <= 256 && lo->F % 64 == 0 && lo->F <= 256 &&
-           lo->L % 8 == 0 && lo->ldB % 64 == 0;
+           lo->L % 8 == 0 && lo->ldB % 128 == 0;
+}
+
+int stages_for(uint32_t stage_bytes)
+{
+    int S = (int)(kSmemBudget / stage_bytes);
+    return S > 6 ? 6 : S;
 }
 
 FwdPlan plan_fwd(const sg_layout *lo, int B)
@@ -79,14 +92,14 @@ FwdPlan plan_fwd(const sg_layout *lo, int B)
     p.a_bytes = (uint32_t)p.MT * 2 * lo->F * 128;
     p.w_bytes = (uint32_t)p.nk * lo->G * 128;
     p.stage_bytes = p.a_bytes + p.w_bytes;
-    p.S = (int)(kSmemBudget / p.stage_bytes);
-    if (p.S > 6)
-        p.S = 6;
-    if (p.S < 2)
+    p.S = stages_for(p.stage_bytes);
+    if (p.S < 3)
         return p;
-    if (2 * p.MT * lo->G > 512)
+    const int per = p.MT * lo->G;  // accumulator columns of one group
+    p.issuers = 4 * per <= 512 ? 2 : 1;
+    if (2 * p.issuers * per > 512)
         return p;
-    p.tmem_cols = pow2_cols(2 * p.MT * lo->G);
+    p.tmem_cols = pow2_cols(2 * p.issuers * per);
     p.ok = true;
     return p;
 }
@@ -104,17 +117,20 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
     p.FT = lo->F / 128;
     p.zsw = dz_swizzle(lo->G);
     p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
+    p.planes = split ? 2 : 1;
+    p.ncat = (split && 2 * lo->G <= 256) ? 1 : 0;
+    p.Nacc = p.ncat ? 2 * lo->G : lo->G;
     p.a_bytes = (uint32_t)p.MT * 2 * lo->F * 128;
-    p.z_bytes = (uint32_t)(split ? 2 : 1) * p.nzc * p.MT * 128 * p.zsw;
+    p.z_bytes = (uint32_t)p.planes * p.nzc * p.MT * 128 * p.zsw;
     p.stage_bytes = p.a_bytes + p.z_bytes;
-    p.S = (int)(kSmemBudget / p.stage_bytes);
-    if (p.S > 6)
-        p.S = 6;
-    if (p.S < 2)
+    p.S = stages_for(p.stage_bytes);
+    if (p.S < 3)
         return p;
-    if (2 * p.FT * lo->G > 512)
+    const int per = p.FT * p.Nacc;
+    p.issuers = 4 * per <= 512 ? 2 : 1;
+    if (2 * p.issuers * per > 512)
         return p;
-    p.tmem_cols = pow2_cols(2 * p.FT * lo->G);
+    p.tmem_cols = pow2_cols(2 * p.issuers * per);
     p.ok = true;
     return p;
 }
@@ -122,25 +138,25 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 DhPlan plan_dh(const sg_layout *lo, int B, bool split)
 {
     DhPlan p;
-    if (!shape_ok(lo) || B < 1 || B > 256)
+    if (!shape_ok(lo) || lo->F > 128 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     p.nk = lo->F / 64;
     p.zsw = dz_swizzle(lo->G);
     p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
-    const int wmax = 512 - lo->F;  // TMEM columns left for the dh partial
+    // TMEM: [0, band_w) partial, then two dH windows of F columns
+    p.win = lo->F;
+    const int wmax = 512 - 2 * p.win;
     p.nbands = (lo->H + wmax - 1) / wmax;
     p.band_w = (lo->H + p.nbands - 1) / p.nbands;
     p.band_w = (p.band_w + 31) / 32 * 32;
-    if (p.band_w + lo->F > 512)
+    if (p.band_w + 2 * p.win > 512)
         return p;
     p.z_bytes = (uint32_t)(split ? 2 : 1) * p.nzc * 128 * p.zsw;
     p.w_bytes = (uint32_t)p.nk * lo->G * 128;
     p.i_bytes = (uint32_t)((lo->F * 2 + 1023) / 1024 * 1024);
     p.stage_bytes = p.z_bytes + p.w_bytes + p.i_bytes;
-    p.S = (int)(kSmemBudget / p.stage_bytes);
-    if (p.S > 6)
-        p.S = 6;
+    p.S = stages_for(p.stage_bytes);
     if (p.S < 2)
         return p;
     p.tmem_cols = 512;
@@ -197,12 +213,14 @@ sg_status make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t
 }
 
 // ------------------------------------------------------------------ common
+constexpr int kMaxAcc = 4;  // accumulator slots: two per MMA-issuing warp
+
 struct Ctl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t drain;
+    uint64_t tfull[kMaxAcc];
+    uint64_t tempty[kMaxAcc];
+    uint64_t drain[2];  // one per MMA-issuing warp
     uint32_t tmem;
     int abort_flag;
     double red[kEpiWarps];
@@ -313,12 +331,12 @@ __device__ __forceinline__ void drain_loads(Ctl &c, int issued, int S)
         mbar_wait_drain(bar_addr(c.full[i % S]), (uint32_t)(i / S) & 1u);
 }
 
-// sum of one double per thread over the epilogue threads (warps 2 .. 2+kEpiWarps)
-__device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst)
+// sum of one double per thread over the epilogue threads (warps first_epi ..)
+__device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst, int first_epi)
 {
     for (int o = 16; o > 0; o >>= 1)
         v += __shfl_down_sync(0xffffffffu, v, o);
-    const int ew = threadIdx.x / 32 - 2;
+    const int ew = threadIdx.x / 32 - first_epi;
     if ((threadIdx.x & 31) == 0)
         c.red[ew] = v;
     named_bar(1, kEpiWarps * 32);
@@ -330,74 +348,161 @@ __device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst)
     }
 }
 
-// Producer side of the H_k gather: lane l issues the gather4 loads q = l,
-// l + 32, ... of the MT*2 b-chunks x F/4 row quads; its row indices come from
-// at most two quads (g = l mod F/4 and (l + 32) mod F/4), loaded one group
-// ahead so the TMA issue never waits on them.
-struct IdxQuads {
-    uint2 a, b;
+// ------------------------------------------------------------------ gather
+// H_k = rows I_k[f] of hT, copied with 16-byte cp.async by the producer
+// threads into the 128-byte-swizzled layout [b-chunk of 64][f][64 b]: unit u
+// (16 B) of row f lands at chunk(u/8) * F*128 + f*128 + ((u%8) ^ (f%8))*16.
+// Thread t copies the units u of rows f = t mod F (every unit of its row when
+// F = 128); its row indices are loaded one group ahead.
+struct GatherRows {
+    int f0, f1;   // rows of this thread (f1 = -1 if one row)
+    int i0, i1;   // their indices in hT
 };
 
-__device__ __forceinline__ IdxQuads load_quads(const uint16_t *idx_s, int64_t k, int F, int lane)
+__device__ __forceinline__ GatherRows gather_rows_of(const uint16_t *idx_s, int64_t k, int F, int t)
 {
-    const int ng = F / 4;
+    GatherRows g;
+    g.f0 = t % F;
+    g.f1 = F > kProdWarps * 32 ? t + kProdWarps * 32 : -1;
     const uint16_t *I = idx_s + k * F;
-    IdxQuads r;
-    r.a = __ldg(reinterpret_cast<const uint2 *>(I + 4 * (lane % ng)));
-    r.b = __ldg(reinterpret_cast<const uint2 *>(I + 4 * ((lane + 32) % ng)));
-    return r;
+    g.i0 = __ldg(I + g.f0);
+    g.i1 = g.f1 >= 0 ? __ldg(I + g.f1) : 0;
+    return g;
 }
 
-__device__ __forceinline__ void issue_gathers(const CUtensorMap *tm_h, uint32_t A, int F, int MT,
-                                              const IdxQuads &iq, int lane, uint32_t fb)
+__device__ __forceinline__ void issue_gather(const uint16_t *hT, int ldB, uint32_t A, int F,
+                                             int units, const GatherRows &g, int t)
 {
-    const int ng = F / 4;
-    for (int q = lane; q < MT * 2 * ng; q += 32) {
-        const int g = q % ng, tcn = q / ng;
-        const uint2 v = (g == lane % ng) ? iq.a : iq.b;
-        tma_gather4(A + (uint32_t)tcn * F * 128 + (uint32_t)g * 512, tm_h, tcn * 64,
-                    (int)(v.x & 0xffff), (int)(v.x >> 16), (int)(v.y & 0xffff),
-                    (int)(v.y >> 16), fb);
+    // units = MT * 16 16-byte units per row; rows f0 (and f1) of this thread
+    const int nthr = kProdWarps * 32;
+    const int rows_per_pass = nthr < F ? nthr : F;     // threads sharing the rows
+    const int u_step = nthr / rows_per_pass;           // threads per row
+    const int u_first = t / rows_per_pass;
+    for (int r = 0; r < 2; ++r) {
+        const int f = r == 0 ? g.f0 : g.f1;
+        if (f < 0)
+            break;
+        const uint16_t *src = hT + (size_t)(r == 0 ? g.i0 : g.i1) * ldB;
+        const uint32_t rowbase = A + (uint32_t)f * 128;
+        for (int u = u_first; u < units; u += u_step) {
+            const int cch = u >> 3, w = u & 7;
+            cp_async16(rowbase + (uint32_t)cch * F * 128 + (uint32_t)((w ^ (f & 7)) << 4), src + u * 8);
+        }
     }
+}
+
+// Producer loop shared by the forward and the weight gradient: per group, one
+// thread arms the stage barrier with the TMA bytes (`tma_bytes`, issued by
+// `issue_tma`), every producer thread copies its share of H_k, and a copy
+// group is signalled complete two groups later (wait_group, proxy fence,
+// arrive) so each thread keeps three groups of copies in flight.
+template <typename IssueTma>
+__device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t stage_bytes, int S,
+                                              int64_t K, const uint16_t *idx_s, const uint16_t *hT,
+                                              int ldB, int F, int MT, uint32_t tma_bytes,
+                                              volatile int *abort_flag, int32_t *status,
+                                              IssueTma issue_tma)
+{
+    constexpr int kLag = 2;
+    const int t = threadIdx.x;  // producer threads are 0 .. kProdWarps*32-1
+    const int units = MT * 16;
+    int it = 0;
+    GatherRows cur = {0, -1, 0, 0};
+    if (blockIdx.x < K)
+        cur = gather_rows_of(idx_s, blockIdx.x, F, t);
+    for (int64_t k = blockIdx.x; k < K; k += gridDim.x, ++it) {
+        const int s = it % S;
+        const uint32_t ph = (uint32_t)(it / S) & 1u;
+        GatherRows nxt = cur;
+        if (k + gridDim.x < K)
+            nxt = gather_rows_of(idx_s, k + gridDim.x, F, t);
+        if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status))
+            break;
+        const uint32_t A = stage0 + (uint32_t)s * stage_bytes;
+        if (t == 0) {
+            mbar_arrive_expect_tx(bar_addr(c.full[s]), tma_bytes);
+            issue_tma(k, A, bar_addr(c.full[s]));
+        }
+        issue_gather(hT, ldB, A, F, units, cur, t);
+        cp_async_commit();
+        if (it >= kLag) {
+            cp_async_wait<kLag>();
+            fence_proxy_async();
+            mbar_arrive(bar_addr(c.full[(it - kLag) % S]));
+        }
+        cur = nxt;
+    }
+    cp_async_wait<0>();
+    fence_proxy_async();
+    for (int j = it - kLag < 0 ? 0 : it - kLag; j < it; ++j)
+        mbar_arrive(bar_addr(c.full[j % S]));
+    if (*abort_flag) {
+        // wait (bounded) for the TMA bytes of the stages still in flight
+        for (int j = it - S < 0 ? 0 : it - S; j < it; ++j)
+            mbar_wait_drain(bar_addr(c.full[j % S]), (uint32_t)(j / S) & 1u);
+    }
+}
+
+__device__ __forceinline__ void setup_ctl(Ctl &c, int S, int nacc, uint32_t full_count,
+                                          uint32_t empty_count)
+{
+    // the plans keep S <= kMaxStages and nacc <= kMaxAcc; never index past them
+    if (S > kMaxStages)
+        S = kMaxStages;
+    if (nacc > kMaxAcc)
+        nacc = kMaxAcc;
+    c.abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+        mbar_init(bar_addr(c.full[s]), full_count);
+        mbar_init(bar_addr(c.empty[s]), empty_count);
+    }
+    for (int i = 0; i < nacc; ++i) {
+        mbar_init(bar_addr(c.tfull[i]), 1);
+        mbar_init(bar_addr(c.tempty[i]), kEpiWarps * 32);
+    }
+    mbar_init(bar_addr(c.drain[0]), 1);
+    mbar_init(bar_addr(c.drain[1]), 1);
+    fence_mbar_init();
+}
+
+// Accumulator slot of the it-th group: the issuer is it mod `issuers`, each
+// issuer owns two slots used alternately.
+__device__ __forceinline__ int acc_slot(int it, int issuers)
+{
+    return issuers == 2 ? 2 * (it & 1) + ((it >> 1) & 1) : (it & 1);
+}
+__device__ __forceinline__ uint32_t acc_phase(int it, int issuers)
+{
+    return issuers == 2 ? (uint32_t)(it >> 2) & 1u : (uint32_t)(it >> 1) & 1u;
 }
 
 // ================================================================== forward
 struct FwdArgs {
-    const uint16_t *idx_s;
+    const uint16_t *idx_s, *hT;
     uint16_t *Z, *dZ, *dZ_lo;
     const int32_t *gptr, *gent;
     double *loss_part;
     int32_t *status;
     int64_t K, L;
-    int32_t B, G, F, MT, nk, S;
+    int32_t B, G, F, MT, nk, S, issuers, ldB;
     uint32_t a_bytes, w_bytes, stage_bytes, tmem_cols;
 };
 
 template <bool BCE, int CH>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    k_tc_fwd(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
-             const FwdArgs a)
+    k_tc_fwd(const __grid_constant__ CUtensorMap tm_w, const FwdArgs a)
 {
     __shared__ Ctl c;
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
     const int G = a.G, F = a.F, S = a.S;
+    const int nacc = 2 * a.issuers;
+    const int per = a.MT * G;  // accumulator columns per group
 
-    if (threadIdx.x == 0) {
-        c.abort_flag = 0;
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar_addr(c.full[s]), 1);
-            mbar_init(bar_addr(c.empty[s]), 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(c.tfull[i]), 1);
-            mbar_init(bar_addr(c.tempty[i]), kEpiWarps * 32);
-        }
-        mbar_init(bar_addr(c.drain), 1);
-        fence_mbar_init();
-    }
-    if (warp == 1) {
+    if (threadIdx.x == 0)
+        setup_ctl(c, S, nacc, kProdWarps * 32 + 1, 1);
+    if (warp == kProdWarps) {
         tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
         tmem_relinquish();
     }
@@ -407,43 +512,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
-        int it = 0;
-        IdxQuads cur = {};
-        if (blockIdx.x < a.K)
-            cur = load_quads(a.idx_s, blockIdx.x, F, lane);
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
-            IdxQuads nxt = cur;
-            if (k + gridDim.x < a.K)
-                nxt = load_quads(a.idx_s, k + gridDim.x, F, lane);
-            if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
-                break;
-            const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
-            const uint32_t Wt = A + a.a_bytes;
-            const uint32_t fb = bar_addr(c.full[s]);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(fb, a.a_bytes + a.w_bytes);
-                for (int kc = 0; kc < a.nk; ++kc)
-                    tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
-            }
-            __syncwarp();
-            issue_gathers(&tm_h, A, F, a.MT, cur, lane, fb);
-            cur = nxt;
-        }
-        drain_loads(c, it, S);
-    } else if (warp == 1) {
+    if (warp < kProdWarps) {
+        // ---------------------------------------------------------- producers
+        producer_loop(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes,
+                      abort_flag, a.status, [&](int64_t k, uint32_t A, uint32_t fb) {
+                          const uint32_t Wt = A + a.a_bytes;
+                          for (int kc = 0; kc < a.nk; ++kc)
+                              tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
+                      });
+    } else if (warp < kFirstEpi) {
         // ---------------------------------------------------------- MMA issue
+        const int me = warp - kProdWarps;
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            if (it % a.issuers != me)
+                continue;
             const int s = it % S;
             const uint32_t ph = (uint32_t)(it / S) & 1u;
-            const int acc = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait(bar_addr(c.tempty[acc]), aph ^ 1u, abort_flag, a.status))
+            const int acc = acc_slot(it, a.issuers);
+            if (!mbar_wait(bar_addr(c.tempty[acc]), acc_phase(it, a.issuers) ^ 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
             if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
@@ -453,7 +541,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
                 const uint32_t Wt = A + a.a_bytes;
                 for (int t = 0; t < a.MT; ++t) {
-                    const uint32_t d = tbase + (uint32_t)(acc * a.MT * G + t * G);
+                    const uint32_t d = tbase + (uint32_t)(acc * per + t * G);
                     for (int st = 0; st < F / 16; ++st) {
                         // A: H_k, MN-major; 8 f-rows per 1024-byte atom, b chunks F*128 apart
                         const uint64_t ad = sdesc(A + (uint32_t)t * 2 * F * 128 + (uint32_t)st * 2048,
@@ -469,36 +557,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             }
             __syncwarp();
         }
+        // every MMA this warp issued has completed once its drain barrier flips
         if (lane == 0)
-            mma_commit(bar_addr(c.drain));
+            mma_commit(bar_addr(c.drain[me]));
         __syncwarp();
-        mbar_wait_drain(bar_addr(c.drain), 0);
+        mbar_wait_drain(bar_addr(c.drain[me]), 0);
     } else {
         // ---------------------------------------------------------- epilogue
         // two warps per TMEM lane quarter; they split the (tile, chunk) units
         const int q = warp & 3;
-        const int sub = (warp - 2) / 4;
+        const int sub = (warp - kFirstEpi) / 4;
         const int units = a.MT * (G / CH);
         double lacc = 0.0;
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            const int acc = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            const int acc = acc_slot(it, a.issuers);
             int e0 = 0, e1 = 0;
             if (BCE) {
                 e0 = __ldg(a.gptr + k);
                 e1 = __ldg(a.gptr + k + 1);
             }
-            if (!mbar_wait(bar_addr(c.tfull[acc]), aph, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.tfull[acc]), acc_phase(it, a.issuers), abort_flag, a.status))
                 break;
             tc_fence_after();
             for (int u = sub; u < units; u += 2) {
                 const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
                 const int b = t * 128 + q * 32 + lane;
                 float v[CH];
-                tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) +
-                                      (uint32_t)(acc * a.MT * G + t * G + c0),
-                                  v);
+                tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * per + t * G + c0), v);
                 if (b >= a.B)
                     continue;
                 const int64_t off = (int64_t)b * a.L + k * G + c0;
@@ -514,11 +600,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_arrive(bar_addr(c.tempty[acc]));
         }
         if (BCE)
-            epi_sum_to(lacc, c, a.loss_part + blockIdx.x);
+            epi_sum_to(lacc, c, a.loss_part + blockIdx.x, kFirstEpi);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kProdWarps) {
         tc_fence_after();
         tmem_dealloc(tbase, a.tmem_cols);
     }
@@ -526,18 +612,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 // ================================================================== dW
 struct DWArgs {
-    const uint16_t *idx_s;
+    const uint16_t *idx_s, *hT;
     uint16_t *dW;
     int32_t *status;
     int64_t K, L;
-    int32_t B, G, F, MT, FT, S, nzc, zsw, npass;
+    int32_t B, G, F, MT, FT, S, nzc, zsw, planes, ncat, Nacc, issuers, ldB;
     uint32_t a_bytes, z_bytes, stage_bytes, tmem_cols;
 };
 
 template <int CH>
 __global__ void __launch_bounds__(kFwdThreads, 1)
-    k_tc_dW(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_z,
-            const __grid_constant__ CUtensorMap tm_zl, const DWArgs a)
+    k_tc_dW(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
+            const DWArgs a)
 {
     __shared__ Ctl c;
     extern __shared__ uint8_t dsm[];
@@ -545,21 +631,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
     const int G = a.G, F = a.F, S = a.S;
     const uint32_t zrows = (uint32_t)a.MT * 128;
+    const uint32_t zchunk = zrows * (uint32_t)a.zsw;          // one dZ chunk (<= 64 j)
+    const uint32_t zplane = (uint32_t)a.nzc * zchunk;         // all of G for hi or lo
+    const int nacc = 2 * a.issuers;
+    const int per = a.FT * a.Nacc;
 
-    if (threadIdx.x == 0) {
-        c.abort_flag = 0;
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar_addr(c.full[s]), 1);
-            mbar_init(bar_addr(c.empty[s]), 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(c.tfull[i]), 1);
-            mbar_init(bar_addr(c.tempty[i]), kEpiWarps * 32);
-        }
-        mbar_init(bar_addr(c.drain), 1);
-        fence_mbar_init();
-    }
-    if (warp == 1) {
+    if (threadIdx.x == 0)
+        setup_ctl(c, S, nacc, kProdWarps * 32 + 1, 1);
+    if (warp == kProdWarps) {
         tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
         tmem_relinquish();
     }
@@ -569,47 +648,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
 
-    if (warp == 0) {
-        int it = 0;
-        IdxQuads cur = {};
-        if (blockIdx.x < a.K)
-            cur = load_quads(a.idx_s, blockIdx.x, F, lane);
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
-            IdxQuads nxt = cur;
-            if (k + gridDim.x < a.K)
-                nxt = load_quads(a.idx_s, k + gridDim.x, F, lane);
-            if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
-                break;
-            const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
-            const uint32_t Zs = A + a.a_bytes;
-            const uint32_t fb = bar_addr(c.full[s]);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(fb, a.a_bytes + a.z_bytes);
-                const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
-                for (int cj = 0; cj < a.nzc; ++cj) {
-                    tma_load_2d(Zs + (uint32_t)cj * zrows * a.zsw, &tm_z, (int)(k * G + cj * 64), 0, fb);
-                    if (a.npass > 1)
-                        tma_load_2d(Zs + zplane + (uint32_t)cj * zrows * a.zsw, &tm_zl,
-                                    (int)(k * G + cj * 64), 0, fb);
-                }
-            }
-            __syncwarp();
-            issue_gathers(&tm_h, A, F, a.MT, cur, lane, fb);
-            cur = nxt;
-        }
-        drain_loads(c, it, S);
-    } else if (warp == 1) {
-        const uint32_t idesc = idesc_bf16(128, G, 0, 1);
+    if (warp < kProdWarps) {
+        producer_loop(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.z_bytes,
+                      abort_flag, a.status, [&](int64_t k, uint32_t A, uint32_t fb) {
+                          const uint32_t Zs = A + a.a_bytes;
+                          for (int cj = 0; cj < a.nzc; ++cj) {
+                              tma_load_2d(Zs + (uint32_t)cj * zchunk, &tm_z, (int)(k * G + cj * 64), 0, fb);
+                              if (a.planes > 1)
+                                  tma_load_2d(Zs + zplane + (uint32_t)cj * zchunk, &tm_zl,
+                                              (int)(k * G + cj * 64), 0, fb);
+                          }
+                      });
+    } else if (warp < kFirstEpi) {
+        const int me = warp - kProdWarps;
         const uint32_t zlayout = layout_for_swizzle(a.zsw);
+        // N = Nacc columns: [hi | lo] along N when concatenated (chunks of
+        // <= 64 j at a uniform stride zchunk), else G columns per pass
+        const uint32_t idesc = idesc_bf16(128, a.Nacc, 0, 1);
+        const int passes = a.ncat ? 1 : a.planes;
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            if (it % a.issuers != me)
+                continue;
             const int s = it % S;
             const uint32_t ph = (uint32_t)(it / S) & 1u;
-            const int acc = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait(bar_addr(c.tempty[acc]), aph ^ 1u, abort_flag, a.status))
+            const int acc = acc_slot(it, a.issuers);
+            if (!mbar_wait(bar_addr(c.tempty[acc]), acc_phase(it, a.issuers) ^ 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
             if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
@@ -618,10 +682,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (lane == 0) {
                 const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
                 const uint32_t Zs = A + a.a_bytes;
-                const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
                 for (int tf = 0; tf < a.FT; ++tf) {
-                    const uint32_t d = tbase + (uint32_t)(acc * a.FT * G + tf * G);
-                    for (int ps = 0; ps < a.npass; ++ps) {      // dZ hi, then dZ lo
+                    const uint32_t d = tbase + (uint32_t)(acc * per + tf * a.Nacc);
+                    for (int ps = 0; ps < passes; ++ps) {
                         for (int st = 0; st < a.MT * 8; ++st) {
                             // A: H_k^T, K-major (rows f, K = b): b chunk st/4, 32 B per 16 b
                             const uint64_t ad = sdesc(A + (uint32_t)(st / 4) * F * 128 +
@@ -629,7 +692,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                                       16, 1024, kLayoutSW128);
                             // B: dZ_k, MN-major (N = j, K = b): 16 b rows per step
                             const uint64_t bd = sdesc(Zs + (uint32_t)ps * zplane + (uint32_t)st * 16 * a.zsw,
-                                                      zrows * a.zsw, 8 * a.zsw, zlayout);
+                                                      zchunk, 8 * a.zsw, zlayout);
                             mma_bf16(d, ad, bd, idesc, (ps > 0 || st > 0) ? 1u : 0u);
                         }
                     }
@@ -640,27 +703,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             __syncwarp();
         }
         if (lane == 0)
-            mma_commit(bar_addr(c.drain));
+            mma_commit(bar_addr(c.drain[me]));
         __syncwarp();
-        mbar_wait_drain(bar_addr(c.drain), 0);
+        mbar_wait_drain(bar_addr(c.drain[me]), 0);
     } else {
         const int q = warp & 3;
-        const int sub = (warp - 2) / 4;
+        const int sub = (warp - kFirstEpi) / 4;
         const int units = a.FT * (G / CH);
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            const int acc = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait(bar_addr(c.tfull[acc]), aph, abort_flag, a.status))
+            const int acc = acc_slot(it, a.issuers);
+            if (!mbar_wait(bar_addr(c.tfull[acc]), acc_phase(it, a.issuers), abort_flag, a.status))
                 break;
             tc_fence_after();
             for (int u = sub; u < units; u += 2) {
                 const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
                 const int f = tf * 128 + q * 32 + lane;
+                const uint32_t col = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * per + tf * a.Nacc + c0);
                 float v[CH];
-                tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) +
-                                      (uint32_t)(acc * a.FT * G + tf * G + c0),
-                                  v);
+                tmem_ld_chunk<CH>(col, v);
+                if (a.ncat) {  // add the lo half, G columns further on
+                    float w[CH];
+                    tmem_ld_chunk<CH>(col + (uint32_t)G, w);
+#pragma unroll
+                    for (int i = 0; i < CH; ++i)
+                        v[i] += w[i];
+                }
                 uint16_t *dst = a.dW + (k * G + c0) * F + f;
 #pragma unroll
                 for (int i = 0; i < CH; ++i)
@@ -672,7 +740,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kProdWarps) {
         tc_fence_after();
         tmem_dealloc(tbase, a.tmem_cols);
     }
@@ -684,7 +752,7 @@ struct DhArgs {
     float *dh;
     int32_t *status;
     int64_t K, L;
-    int32_t B, G, F, H, MT, nk, S, nzc, zsw, nbands, band_w, parts, npass;
+    int32_t B, G, F, H, MT, nk, S, nzc, zsw, nbands, band_w, win, parts, npass;
     uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, tmem_cols;
 };
 
@@ -704,8 +772,9 @@ __device__ __forceinline__ int lower_bound_u16(const uint16_t *I, int n, int v)
 
 // CTA (band, mtile, part): dh columns [i0, i1) of the band, samples
 // [128 mt, 128 mt + 128), groups k = part, part + parts, ...  TMEM columns
-// [0, band_w) hold the CTA's fp32 partial of dh, [band_w, band_w + F) the
-// dH_k pieces of the current group.
+// [0, band_w) hold the CTA's fp32 partial of dh; two windows of `win` columns
+// after it receive dH_k = dZ_k W_k for the f range of the band (alternately,
+// so the MMA of the next group overlaps the scatter of this one).
 __global__ void __launch_bounds__(kDhThreads, 1)
     k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
             const __grid_constant__ CUtensorMap tm_w, const DhArgs a)
@@ -722,18 +791,11 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     const int i0 = band * a.band_w;
     const int i1 = min(a.H, i0 + a.band_w);
     const uint32_t zrows = 128;
+    const uint32_t zchunk = zrows * (uint32_t)a.zsw;
+    const uint32_t zplane = (uint32_t)a.nzc * zchunk;
 
-    if (threadIdx.x == 0) {
-        c.abort_flag = 0;
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar_addr(c.full[s]), 1);
-            mbar_init(bar_addr(c.empty[s]), kEpiWarps * 32);  // released by the epilogue
-        }
-        mbar_init(bar_addr(c.tfull[0]), 1);
-        mbar_init(bar_addr(c.tempty[0]), kEpiWarps * 32);
-        mbar_init(bar_addr(c.drain), 1);
-        fence_mbar_init();
-    }
+    if (threadIdx.x == 0)
+        setup_ctl(c, S, 2, 1, kEpiWarps * 32);  // stages released by the epilogue
     if (warp == 1) {
         tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
         tmem_relinquish();
@@ -757,13 +819,11 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             const uint32_t fb = bar_addr(c.full[s]);
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, a.z_bytes + a.w_bytes + (uint32_t)F * 2);
-                const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
                 for (int cj = 0; cj < a.nzc; ++cj) {
-                    tma_load_2d(Zs + (uint32_t)cj * zrows * a.zsw, &tm_z, (int)(k * G + cj * 64),
-                                mt * 128, fb);
+                    tma_load_2d(Zs + (uint32_t)cj * zchunk, &tm_z, (int)(k * G + cj * 64), mt * 128, fb);
                     if (a.npass > 1)
-                        tma_load_2d(Zs + zplane + (uint32_t)cj * zrows * a.zsw, &tm_zl,
-                                    (int)(k * G + cj * 64), mt * 128, fb);
+                        tma_load_2d(Zs + zplane + (uint32_t)cj * zchunk, &tm_zl, (int)(k * G + cj * 64),
+                                    mt * 128, fb);
                 }
                 for (int kc = 0; kc < a.nk; ++kc)
                     tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
@@ -773,13 +833,14 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         }
         drain_loads(c, it, S);
     } else if (warp == 1) {
-        const uint32_t idesc = idesc_bf16(128, 16, 0, 1);
         const uint32_t zlayout = layout_for_swizzle(a.zsw);
+        const int nks = G / 16;
         int it = 0;
         for (int64_t k = part; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
             const uint32_t ph = (uint32_t)(it / S) & 1u;
-            if (!mbar_wait(bar_addr(c.tempty[0]), ((uint32_t)it & 1u) ^ 1u, abort_flag, a.status))
+            const int wb = it & 1;
+            if (!mbar_wait(bar_addr(c.tempty[wb]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
             if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
@@ -792,36 +853,39 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                     stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes + a.w_bytes);
                 // f range whose index falls in [i0, i1): I_k is ascending
                 const int fa = lower_bound_u16(I, F, i0), fbnd = lower_bound_u16(I, F, i1);
-                const int p0 = fa / 16, p1 = (fbnd + 15) / 16;
-                const uint32_t zplane = (uint32_t)a.nzc * zrows * a.zsw;
-                const int nks = G / 16;
-                for (int p = p0; p < p1; ++p) {
-                    const int f0 = p * 16;
-                    const uint32_t d = tbase + (uint32_t)(a.band_w + (p - p0) * 16);
-                    // K runs over j twice: dZ hi against W_k, then dZ lo against W_k
-                    for (int ks2 = 0; ks2 < a.npass * nks; ++ks2) {
-                        const int ks = ks2 % nks;
-                        // A: dZ_k, K-major (rows b, K = j)
-                        const uint32_t za = Zs + (uint32_t)(ks2 / nks) * zplane +
-                                            (uint32_t)(ks / 4) * zrows * 128 + (uint32_t)(ks % 4) * 32;
-                        const uint64_t ad = sdesc(za, 16, 8 * a.zsw, zlayout);
-                        // B: W_k, MN-major (N = f, K = j): 16 j rows = 2 atoms
-                        const uint64_t bd = sdesc(Wt + (uint32_t)(f0 / 64) * G * 128 +
-                                                      (uint32_t)(f0 % 64) * 2 + (uint32_t)ks * 2048,
-                                                  (uint32_t)G * 128, 1024, kLayoutSW128);
-                        mma_bf16(d, ad, bd, idesc, ks2 > 0 ? 1u : 0u);
+                // whole 64-f chunks of W_k that hold part of the f range:
+                // every window starts on a swizzle-atom boundary of the tile
+                const uint32_t dbase = tbase + (uint32_t)(a.band_w + wb * a.win);
+                if (fa < fbnd) {
+                    const int c_first = fa / 64, c_last = (fbnd - 1) / 64;
+                    const uint32_t idesc = idesc_bf16(128, 64, 0, 1);
+                    for (int cc = c_first; cc <= c_last; ++cc) {
+                        const uint32_t d = dbase + (uint32_t)((cc - c_first) * 64);
+                        // K runs over j for dZ hi (and again for dZ lo) against W_k
+                        for (int ks2 = 0; ks2 < a.npass * nks; ++ks2) {
+                            const int ks = ks2 % nks;
+                            const uint32_t za = Zs + (uint32_t)(ks2 / nks) * zplane +
+                                                (uint32_t)(ks / 4) * zchunk + (uint32_t)(ks % 4) * 32;
+                            const uint64_t ad = sdesc(za, 16, 8 * a.zsw, zlayout);
+                            const uint64_t bd = sdesc(Wt + (uint32_t)cc * G * 128 + (uint32_t)ks * 2048,
+                                                      (uint32_t)G * 128, 1024, kLayoutSW128);
+                            mma_bf16(d, ad, bd, idesc, ks2 > 0 ? 1u : 0u);
+                        }
                     }
                 }
-                mma_commit(bar_addr(c.tfull[0]));
+                mma_commit(bar_addr(c.tfull[wb]));
             }
             __syncwarp();
         }
         if (lane == 0)
-            mma_commit(bar_addr(c.drain));
+            mma_commit(bar_addr(c.drain[0]));
         __syncwarp();
-        mbar_wait_drain(bar_addr(c.drain), 0);
+        mbar_wait_drain(bar_addr(c.drain[0]), 0);
     } else {
-        // two warps per TMEM lane quarter; pieces alternate between them
+        // two warps per TMEM lane quarter.  They may be working on different
+        // groups at the same time (the dH windows are double buffered), so
+        // they own disjoint partial columns (column parity) rather than
+        // disjoint pieces: no column is ever updated by both.
         const int q = warp & 3;
         const int sub = (warp - 2) / 4;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
@@ -832,23 +896,26 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         for (int64_t k = part; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
             const uint32_t ph = (uint32_t)(it / S) & 1u;
+            const int wb = it & 1;
             if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
                 break;
-            if (!mbar_wait(bar_addr(c.tfull[0]), (uint32_t)it & 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.tfull[wb]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
             const uint16_t *I = reinterpret_cast<const uint16_t *>(
                 stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes + a.w_bytes);
             const int fa = lower_bound_u16(I, F, i0), fbnd = lower_bound_u16(I, F, i1);
-            const int p0 = fa / 16, p1 = (fbnd + 15) / 16;
-            for (int p = p0 + sub; p < p1; p += 2) {
+            const int fbase = (fa / 64) * 64;  // first f of the first window
+            const uint32_t dbase = tbase + lane_off + (uint32_t)(a.band_w + wb * a.win);
+            for (int p = fa / 16; p * 16 < fbnd; ++p) {
                 uint32_t r[16];
-                tmem_ld16(tbase + lane_off + (uint32_t)(a.band_w + (p - p0) * 16), r);
+                tmem_ld16(dbase + (uint32_t)(p * 16 - fbase), r);
                 uint32_t col[16], old[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int f = p * 16 + u;
-                    col[u] = (f >= fa && f < fbnd) ? (uint32_t)(I[f] - i0) : 0xffffffffu;
+                    const uint32_t cf = (f >= fa && f < fbnd) ? (uint32_t)(I[f] - i0) : 0xffffffffu;
+                    col[u] = (cf != 0xffffffffu && (int)(cf & 1u) == sub) ? cf : 0xffffffffu;
                     old[u] = 0u;
                     if (col[u] != 0xffffffffu)
                         old[u] = tmem_ld1(tbase + lane_off + col[u]);
@@ -862,10 +929,11 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar_addr(c.tempty[0]));
+            mbar_arrive(bar_addr(c.tempty[wb]));
             mbar_arrive(bar_addr(c.empty[s]));
         }
-        // add the partial into dh
+        // add the partial into dh, once both warps of every quarter are done
+        named_bar(1, kEpiWarps * 32);
         const int b = mt * 128 + q * 32 + lane;
         for (int c0 = sub * 32; c0 < a.band_w; c0 += 64) {
             uint32_t r[32];
@@ -929,15 +997,13 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
         sg_set_error("tc_fwd: shape not supported by the tensor-core engine");
         return SG_ERR_UNSUPPORTED;
     }
-    CUtensorMap tm_h, tm_w;
-    sg_status rc = make_map_2d(&tm_h, lo->hT, (uint64_t)lo->ldB, (uint64_t)lo->H, 64, 1, 128, "hT");
-    if (rc != SG_OK)
-        return rc;
-    rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)lo->G, 128, "W");
+    CUtensorMap tm_w;
+    sg_status rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)lo->G, 128, "W");
     if (rc != SG_OK)
         return rc;
     FwdArgs a;
     a.idx_s = lo->idx_s;
+    a.hT = lo->hT;
     a.Z = Z;
     a.dZ = dZ;
     a.dZ_lo = dZ_lo;
@@ -953,6 +1019,8 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     a.MT = p.MT;
     a.nk = p.nk;
     a.S = p.S;
+    a.issuers = p.issuers;
+    a.ldB = lo->ldB;
     a.a_bytes = p.a_bytes;
     a.w_bytes = p.w_bytes;
     a.stage_bytes = p.stage_bytes;
@@ -960,7 +1028,7 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
     const bool bce = dZ != nullptr;
-    void (*kern)(CUtensorMap, CUtensorMap, FwdArgs);
+    void (*kern)(CUtensorMap, FwdArgs);
     if (lo->G >= 64)
         kern = bce ? k_tc_fwd<true, 32> : k_tc_fwd<false, 32>;
     else
@@ -968,7 +1036,7 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
-    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, kFwdThreads, smem, st>>>(tm_h, tm_w, a));
+    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, kFwdThreads, smem, st>>>(tm_w, a));
     SG_TRY_CUDA(cudaGetLastError());
     if (bce)
         return sg_loss_finalize(lo, grid, loss, st);
@@ -983,16 +1051,13 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
         sg_set_error("tc_dW: shape not supported by the tensor-core engine");
         return SG_ERR_UNSUPPORTED;
     }
-    CUtensorMap tm_h, tm_z;
-    sg_status rc = make_map_2d(&tm_h, lo->hT, (uint64_t)lo->ldB, (uint64_t)lo->H, 64, 1, 128, "hT");
-    if (rc != SG_OK)
-        return rc;
+    CUtensorMap tm_z, tm_zl;
     const int zbox = lo->G < 64 ? lo->G : 64;
-    rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
-                     (uint32_t)(p.MT * 128), p.zsw, "dZ");
+    sg_status rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
+                               (uint32_t)(p.MT * 128), p.zsw, "dZ");
     if (rc != SG_OK)
         return rc;
-    CUtensorMap tm_zl = tm_z;
+    tm_zl = tm_z;
     if (dZ_lo) {
         rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
                          (uint32_t)(p.MT * 128), p.zsw, "dZ_lo");
@@ -1001,6 +1066,7 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     }
     DWArgs a;
     a.idx_s = lo->idx_s;
+    a.hT = lo->hT;
     a.dW = dW;
     a.status = lo->status;
     a.K = lo->K;
@@ -1013,19 +1079,22 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     a.S = p.S;
     a.nzc = p.nzc;
     a.zsw = p.zsw;
-    a.npass = dZ_lo ? 2 : 1;
+    a.planes = p.planes;
+    a.ncat = p.ncat;
+    a.Nacc = p.Nacc;
+    a.issuers = p.issuers;
+    a.ldB = lo->ldB;
     a.a_bytes = p.a_bytes;
     a.z_bytes = p.z_bytes;
     a.stage_bytes = p.stage_bytes;
     a.tmem_cols = p.tmem_cols;
     const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
-    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, DWArgs) =
-        lo->G >= 64 ? k_tc_dW<32> : k_tc_dW<16>;
+    void (*kern)(CUtensorMap, CUtensorMap, DWArgs) = lo->G >= 64 ? k_tc_dW<32> : k_tc_dW<16>;
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
-    SG_LAUNCH(lo, SG_KIND_DW, st, kern<<<grid, kFwdThreads, smem, st>>>(tm_h, tm_z, tm_zl, a));
+    SG_LAUNCH(lo, SG_KIND_DW, st, kern<<<grid, kFwdThreads, smem, st>>>(tm_z, tm_zl, a));
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }
@@ -1038,13 +1107,13 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
         sg_set_error("tc_dh: shape not supported by the tensor-core engine");
         return SG_ERR_UNSUPPORTED;
     }
-    CUtensorMap tm_z, tm_w;
+    CUtensorMap tm_z, tm_zl, tm_w;
     const int zbox = lo->G < 64 ? lo->G : 64;
     sg_status rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox, 128,
                                p.zsw, "dZ");
     if (rc != SG_OK)
         return rc;
-    CUtensorMap tm_zl = tm_z;
+    tm_zl = tm_z;
     if (dZ_lo) {
         rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox, 128, p.zsw,
                          "dZ_lo");
@@ -1071,6 +1140,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     a.zsw = p.zsw;
     a.nbands = p.nbands;
     a.band_w = p.band_w;
+    a.win = p.win;
     a.npass = dZ_lo ? 2 : 1;
     int parts = lo->num_sms / (p.nbands * p.MT);
     if (parts < 1)
