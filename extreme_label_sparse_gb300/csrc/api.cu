@@ -137,7 +137,8 @@ sg_status dev_alloc(T **p, size_t n, const char *what)
 
 sg_status ensure_dz_ws(sg_layout *lo)
 {
-    size_t need = 2 * (size_t)lo->max_B * (size_t)lo->L;
+    // two planes of [B][L], or K group tiles of 2 x roundup(B, 128) x G
+    size_t need = 2 * (size_t)lo->ldB * (size_t)lo->L;
     if (lo->dZ_ws && lo->dZ_ws_elems >= need)
         return SG_OK;
     if (lo->dZ_ws)
@@ -387,7 +388,7 @@ sg_status sg_fwd(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
     TRY(pick_tc(lo, SG_KIND_FWD, B, &tc, fn));
     TRY(simt_transpose_h(lo, h, B, st));
     if (tc)
-        return tc_fwd(lo, B, W, Z, nullptr, nullptr, nullptr, st);
+        return tc_fwd(lo, B, W, Z, nullptr, nullptr, nullptr, nullptr, st);
     return simt_fwd(lo, B, W, Z, nullptr, nullptr, nullptr, st);
 }
 
@@ -426,7 +427,7 @@ sg_status sg_fwd_bce(sg_layout *lo, const sg_bf16 *h, int32_t B,
     TRY(simt_transpose_h(lo, h, B, st));
     TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
     if (tc)
-        return tc_fwd(lo, B, W, Z_or_null, dZ, nullptr, loss, st);
+        return tc_fwd(lo, B, W, Z_or_null, dZ, nullptr, nullptr, loss, st);
     return simt_fwd(lo, B, W, Z_or_null, dZ, nullptr, loss, st);
 }
 
@@ -445,7 +446,7 @@ sg_status sg_bwd_dW(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h,
     TRY(pick_tc(lo, SG_KIND_DW, B, &tc, fn));
     TRY(simt_transpose_h(lo, h, B, st));
     if (tc)
-        return tc_dW(lo, dZ, nullptr, B, dW, st);
+        return tc_dW(lo, dZ, nullptr, nullptr, B, dW, st);
     return simt_dW(lo, dZ, nullptr, B, dW, st);
 }
 
@@ -462,7 +463,7 @@ sg_status sg_bwd_dh(sg_layout *lo, const sg_bf16 *dZ, int32_t B,
     bool tc = false;
     TRY(pick_tc(lo, SG_KIND_DH, B, &tc, fn));
     if (tc)
-        return tc_dh(lo, dZ, nullptr, B, W, dh, st);
+        return tc_dh(lo, dZ, nullptr, nullptr, B, W, dh, st);
     return simt_dh(lo, dZ, nullptr, B, W, dh, st);
 }
 
@@ -507,12 +508,23 @@ sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
     // samples (dW) or over every label (dh), would move results by more than
     // 2e-2 (1 + |ref|) against the exact gradient.
     TRY(ensure_dz_ws(lo));
+    if (tc_f && tc_w && tc_h && tc_tiled_ok(lo, B)) {
+        // all three on the tensor cores: dZ in the group-tiled workspace
+        uint8_t *dZt = reinterpret_cast<uint8_t *>(lo->dZ_ws);
+        if (tc_fwdw_ok(lo, B)) {
+            TRY(tc_fwdw(lo, B, W, dZt, dW, loss, st));
+        } else {
+            TRY(tc_fwd(lo, B, W, nullptr, nullptr, nullptr, dZt, loss, st));
+            TRY(tc_dW(lo, nullptr, nullptr, dZt, B, dW, st));
+        }
+        return tc_dh(lo, nullptr, nullptr, dZt, B, W, dh, st);
+    }
     uint16_t *dZ = lo->dZ_ws;
     uint16_t *dZlo = lo->dZ_ws + (size_t)B * lo->L;
-    TRY(tc_f ? tc_fwd(lo, B, W, nullptr, dZ, dZlo, loss, st)
+    TRY(tc_f ? tc_fwd(lo, B, W, nullptr, dZ, dZlo, nullptr, loss, st)
              : simt_fwd(lo, B, W, nullptr, dZ, dZlo, loss, st));
-    TRY(tc_w ? tc_dW(lo, dZ, dZlo, B, dW, st) : simt_dW(lo, dZ, dZlo, B, dW, st));
-    return tc_h ? tc_dh(lo, dZ, dZlo, B, W, dh, st) : simt_dh(lo, dZ, dZlo, B, W, dh, st);
+    TRY(tc_w ? tc_dW(lo, dZ, dZlo, nullptr, B, dW, st) : simt_dW(lo, dZ, dZlo, B, dW, st));
+    return tc_h ? tc_dh(lo, dZ, dZlo, nullptr, B, W, dh, st) : simt_dh(lo, dZ, dZlo, B, W, dh, st);
 }
 
 // ---------------------------------------------------------------- timing

@@ -161,12 +161,22 @@ sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
 // tc.cu
 bool tc_supported(const sg_layout *lo);
 bool tc_stage_ok(const sg_layout *lo, int stage, int B);
+// dZ is either caller-layout [B][L] (dZ, optional residual plane dZ_lo) or
+// the step's group-tiled workspace dZt (both planes; see tc.cu)
 sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
-                 uint16_t *dZ, uint16_t *dZ_lo, double *loss, cudaStream_t st);
-sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B,
-                uint16_t *dW, cudaStream_t st);
-sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B,
-                const uint16_t *W, float *dh, cudaStream_t st);
+                 uint16_t *dZ, uint16_t *dZ_lo, uint8_t *dZt, double *loss, cudaStream_t st);
+sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
+                int32_t B, uint16_t *dW, cudaStream_t st);
+sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
+                int32_t B, const uint16_t *W, float *dh, cudaStream_t st);
+// bytes of one group's dZ tile, and whether fwd, dW and dh all run on the
+// tensor cores with the tiled workspace for this batch size
+uint64_t tc_dz_tile_bytes(const sg_layout *lo, int32_t B);
+bool tc_tiled_ok(const sg_layout *lo, int32_t B);
+// fused forward + BCE + dW into the tiled workspace (one pass over the groups)
+bool tc_fwdw_ok(const sg_layout *lo, int32_t B);
+sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
+                  double *loss, cudaStream_t st);
 sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW,
                   float *dh, double *loss, cudaStream_t st);
 

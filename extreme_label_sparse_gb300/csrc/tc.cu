@@ -14,9 +14,21 @@
 //   W_k  : TMA box {64 f, G rows} per 64-wide f chunk, 128-byte swizzle:
 //          K-major B (N = j, K = f) of the forward, MN-major B (N = f, K = j)
 //          of the feature gradient.
-//   dZ_k : TMA box {min(G,64) j, rows b}, swizzle = row width: MN-major B
-//          (N = j, K = b) of the weight gradient, K-major A (M = b, K = j) of
-//          the feature gradient.
+//   dZ_k : rows b of min(G,64) j (one chunk per 64 j), swizzle = row width:
+//          MN-major B (N = j, K = b) of the weight gradient, K-major A
+//          (M = b, K = j) of the feature gradient.  From a caller's row-major
+//          [B][L] dZ it is a TMA box; inside the training step dZ lives in a
+//          group-tiled workspace whose tiles already hold these bytes, so one
+//          bulk copy brings a group's tile in.
+//
+// Group-tiled dZ workspace (training step only).  Tile k holds, for plane p
+// (0: bf16(dZ), 1: the residual dZ - bf16(dZ)), chunk cj of 64 columns and
+// row r < Bp = 128 ceil(B/128) (rows >= B are zero), the 16-byte unit u of
+// columns 8u .. 8u+7 of that chunk at byte
+//     ((p * nzc + cj) * Bp + r) * zsw + ((u ^ swz(r)) * 16),
+// zsw = min(2G, 128) the row width and swz the TMA swizzle of that width.
+// A tile is contiguous (2 Bp G bf16 values per plane pair), so writing it
+// touches one or two pages instead of one page per sample row.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -35,7 +47,7 @@ constexpr int kProdWarps = 4;  // cp.async gather + TMA issue
 // forward / dW: producers, two MMA-issuing warps, epilogue
 constexpr int kFwdThreads = 32 * (kProdWarps + 2 + kEpiWarps);
 constexpr int kFirstEpi = kProdWarps + 2;
-// dh: one TMA producer, one MMA warp, epilogue
+// dh: one load warp, one MMA warp, eight builder warps
 constexpr int kDhThreads = 32 * (2 + kEpiWarps);
 
 // ------------------------------------------------------------------ plans
@@ -56,8 +68,8 @@ struct DWPlan {
 
 struct DhPlan {
     bool ok = false;
-    int MT = 0, nk = 0, S = 0, nzc = 0, zsw = 0, nbands = 0, band_w = 0, win = 0;
-    uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, tmem_cols = 0;
+    int MT = 0, nk = 0, S = 0, zsw = 0, nbands = 0, band_w = 0;
+    uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, ws_bytes = 0, tmem_cols = 0;
 };
 
 uint32_t pow2_cols(int n)
@@ -73,6 +85,10 @@ bool shape_ok(const sg_layout *lo)
     return lo->G % 16 == 0 && lo->G <= 256 && lo->F % 64 == 0 && lo->F <= 256 &&
            lo->L % 8 == 0 && lo->ldB % 128 == 0;
 }
+
+// dZ rows of a group must fill whole swizzle rows: 16 or 32 columns, or
+// whole chunks of 64
+bool dz_ok(int G) { return G == 16 || G == 32 || G % 64 == 0; }
 
 int stages_for(uint32_t stage_bytes)
 {
@@ -109,7 +125,7 @@ int dz_swizzle(int G) { return G * 2 >= 128 ? 128 : G * 2; }
 DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 {
     DWPlan p;
-    if (!shape_ok(lo) || lo->F % 128 != 0 || B < 1 || B > 256)
+    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->F % 128 != 0 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
@@ -138,29 +154,28 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 DhPlan plan_dh(const sg_layout *lo, int B, bool split)
 {
     DhPlan p;
-    if (!shape_ok(lo) || lo->F > 128 || B < 1 || B > 256)
+    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->G > 64 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
+    if (p.MT * 128 > lo->ldB)
+        return p;
     p.nk = lo->F / 64;
     p.zsw = dz_swizzle(lo->G);
-    p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
-    // TMEM: [0, band_w) partial, then two dH windows of F columns
-    p.win = lo->F;
-    const int wmax = 512 - 2 * p.win;
-    p.nbands = (lo->H + wmax - 1) / wmax;
-    p.band_w = (lo->H + p.nbands - 1) / p.nbands;
-    p.band_w = (p.band_w + 31) / 32 * 32;
-    if (p.band_w + 2 * p.win > 512)
-        return p;
-    p.z_bytes = (uint32_t)(split ? 2 : 1) * p.nzc * 128 * p.zsw;
+    p.z_bytes = (uint32_t)(split ? 2 : 1) * 128 * p.zsw;
     p.w_bytes = (uint32_t)p.nk * lo->G * 128;
     p.i_bytes = (uint32_t)((lo->F * 2 + 1023) / 1024 * 1024);
     p.stage_bytes = p.z_bytes + p.w_bytes + p.i_bytes;
-    p.S = stages_for(p.stage_bytes);
-    if (p.S < 2)
-        return p;
-    p.tmem_cols = 512;
-    p.ok = true;
+    // bands of at most 256 dh columns (one MMA of N <= 256 per K step), in
+    // whole 64-column chunks of the scattered W_k
+    p.nbands = (lo->H + 255) / 256;
+    p.band_w = ((lo->H + p.nbands - 1) / p.nbands + 63) / 64 * 64;
+    p.ws_bytes = (uint32_t)(p.band_w / 64) * lo->G * 128;
+    p.tmem_cols = pow2_cols(p.band_w);
+    const long room = (long)kSmemBudget - 2l * p.ws_bytes;
+    p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
+    if (p.S > 6)
+        p.S = 6;
+    p.ok = p.S >= 2;
     return p;
 }
 
@@ -259,6 +274,41 @@ __device__ __forceinline__ void store_bf16_row(uint16_t *dst, uint16_t *lo, cons
             r.w = pack2(v[i + 6] - lo_half(q.w), v[i + 7] - hi_half(q.w));
             *reinterpret_cast<uint4 *>(lo + i) = r;
         }
+    }
+}
+
+// 16-byte unit that unit u of row r lands on under the TMA swizzle of a
+// zsw-byte row (the XOR of the unit index with address bits 7.. of the row)
+__device__ __forceinline__ int swz_of(int r, int zsw)
+{
+    return zsw == 128 ? (r & 7) : zsw == 64 ? ((r >> 1) & 3) : ((r >> 2) & 1);
+}
+
+// CH values (columns c0 .. c0+CH-1, sample row r) into a group's dZ tile:
+// bf16 values into plane 0, their rounding residuals into plane 1
+template <int CH>
+__device__ __forceinline__ void store_dz_tile(uint8_t *tile, int r, int c0, const float (&v)[CH],
+                                              int zsw, int nzc, int Bp)
+{
+    const int sw = swz_of(r, zsw);
+    const int u0 = (c0 & 63) >> 3;
+    uint8_t *hi = tile + ((size_t)(c0 >> 6) * Bp + r) * zsw;
+    uint8_t *lo = hi + (size_t)nzc * Bp * zsw;
+#pragma unroll
+    for (int i = 0; i < CH / 8; ++i) {
+        const float *x = v + 8 * i;
+        uint4 q, e;
+        q.x = pack2(x[0], x[1]);
+        q.y = pack2(x[2], x[3]);
+        q.z = pack2(x[4], x[5]);
+        q.w = pack2(x[6], x[7]);
+        e.x = pack2(x[0] - lo_half(q.x), x[1] - hi_half(q.x));
+        e.y = pack2(x[2] - lo_half(q.y), x[3] - hi_half(q.y));
+        e.z = pack2(x[4] - lo_half(q.z), x[5] - hi_half(q.z));
+        e.w = pack2(x[6] - lo_half(q.w), x[7] - hi_half(q.w));
+        const int off = ((u0 + i) ^ sw) << 4;
+        *reinterpret_cast<uint4 *>(hi + off) = q;
+        *reinterpret_cast<uint4 *>(lo + off) = e;
     }
 }
 
@@ -480,6 +530,9 @@ __device__ __forceinline__ uint32_t acc_phase(int it, int issuers)
 struct FwdArgs {
     const uint16_t *idx_s, *hT;
     uint16_t *Z, *dZ, *dZ_lo;
+    uint8_t *dZt;          // group-tiled dZ output (instead of dZ / dZ_lo)
+    uint64_t tile_bytes;
+    int32_t zsw, nzc, Bp;
     const int32_t *gptr, *gent;
     double *loss_part;
     int32_t *status;
@@ -585,6 +638,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const int b = t * 128 + q * 32 + lane;
                 float v[CH];
                 tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * per + t * G + c0), v);
+                if (BCE && a.dZt) {
+                    // every row of the tile is written; rows >= B hold zeros
+                    if (b < a.B) {
+                        const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
+                        lacc += bce_chunk<CH>(v, y);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < CH; ++i)
+                            v[i] = 0.f;
+                    }
+                    store_dz_tile<CH>(a.dZt + (size_t)k * a.tile_bytes, b, c0, v, a.zsw, a.nzc, a.Bp);
+                    continue;
+                }
                 if (b >= a.B)
                     continue;
                 const int64_t off = (int64_t)b * a.L + k * G + c0;
@@ -613,6 +679,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // ================================================================== dW
 struct DWArgs {
     const uint16_t *idx_s, *hT;
+    const uint8_t *dZt;    // group-tiled dZ input (else the tensor maps)
+    uint64_t tile_bytes;
     uint16_t *dW;
     int32_t *status;
     int64_t K, L;
@@ -652,6 +720,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         producer_loop(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.z_bytes,
                       abort_flag, a.status, [&](int64_t k, uint32_t A, uint32_t fb) {
                           const uint32_t Zs = A + a.a_bytes;
+                          if (a.dZt) {  // the tile is the stage image of both planes
+                              bulk_load(Zs, a.dZt + (size_t)k * a.tile_bytes, a.z_bytes, fb);
+                              return;
+                          }
                           for (int cj = 0; cj < a.nzc; ++cj) {
                               tma_load_2d(Zs + (uint32_t)cj * zchunk, &tm_z, (int)(k * G + cj * 64), 0, fb);
                               if (a.planes > 1)
@@ -746,35 +818,314 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
 }
 
+// ================================================================== fused forward + BCE + dW
+// One pass over the groups for the training step: per group the producers
+// gather H_k and load W_k, one MMA warp computes Z_k = H_k W_k^T, the epilogue
+// turns it into dZ_k (BCE), writes dZ_k to the group-tiled workspace (for dh)
+// and into shared memory, and a second MMA warp computes dW_k^T = H_k^T dZ_k
+// from the same shared-memory H_k, so H_k is gathered once and dZ_k is never
+// read back for dW.  Warps: 4 producers, 2 forward MMA warps, 2 dW MMA warps
+// (each pair alternates groups), 8 epilogue warps.
+constexpr int kFWThreads = 32 * (kProdWarps + 4 + kEpiWarps);
+constexpr int kFWFirstEpi = kProdWarps + 4;
+
+struct FWPlan {
+    bool ok = false;
+    int MT = 0, FT = 0, nk = 0, S = 0, zsw = 0, nzc = 0, nslot = 0;
+    uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, dz_bytes = 0, zcols = 0, wcols = 0,
+             tmem_cols = 0;
+};
+
+FWPlan plan_fwdw(const sg_layout *lo, int B)
+{
+    FWPlan p;
+    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->F % 128 != 0 || 2 * lo->G > 256 || B < 1 || B > 256)
+        return p;
+    p.MT = (B + 127) / 128;
+    if (p.MT * 128 > lo->ldB)
+        return p;
+    p.FT = lo->F / 128;
+    p.nk = lo->F / 64;
+    p.zsw = dz_swizzle(lo->G);
+    p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
+    p.a_bytes = (uint32_t)p.MT * 2 * lo->F * 128;
+    p.w_bytes = (uint32_t)p.nk * lo->G * 128;
+    p.stage_bytes = p.a_bytes + p.w_bytes;
+    p.dz_bytes = 2u * (uint32_t)p.nzc * p.MT * 128 * p.zsw;  // both planes, all rows
+    p.zcols = (uint32_t)p.MT * lo->G;
+    p.wcols = (uint32_t)p.FT * 2 * lo->G;
+    p.nslot = 4 * (p.zcols + p.wcols) <= 512 ? 4 : 2;
+    if (p.nslot * (p.zcols + p.wcols) > 512)
+        return p;
+    p.tmem_cols = pow2_cols(p.nslot * (p.zcols + p.wcols));
+    const long room = (long)kSmemBudget - 2l * p.dz_bytes;
+    p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
+    if (p.S > 6)
+        p.S = 6;
+    p.ok = p.S >= 3;
+    return p;
+}
+
+struct FWArgs {
+    const uint16_t *idx_s, *hT;
+    uint8_t *dZt;
+    uint64_t tile_bytes;
+    uint16_t *dW;
+    const int32_t *gptr, *gent;
+    double *loss_part;
+    int32_t *status;
+    int64_t K, L;
+    int32_t B, G, F, MT, FT, nk, S, zsw, nzc, nslot, Bp, ldB;
+    uint32_t a_bytes, w_bytes, stage_bytes, dz_bytes, zcols, wcols, tmem_cols;
+};
+
+// the common control block (stages; tfull/tempty = Z accumulators; drain of
+// the forward MMA warps) plus the barriers of the dW half
+struct CtlFW {
+    Ctl c;
+    uint64_t wfull[4], wempty[4];    // dW accumulators
+    uint64_t dzfull[2], dzempty[2];  // dZ_k in shared memory
+    uint64_t wdrain[2];              // drain of the dW MMA warps
+};
+
+template <int CH>
+__global__ void __launch_bounds__(kFWThreads, 1)
+    k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
+{
+    __shared__ CtlFW cf;
+    Ctl &c = cf.c;
+    extern __shared__ uint8_t dsm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+    uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
+    // [dZ_k buffer 0][dZ_k buffer 1][stages]
+    const uint32_t stage0 = base + 2 * a.dz_bytes;
+    const int G = a.G, F = a.F, S = a.S, NS = a.nslot;
+    const uint32_t zrows = (uint32_t)a.MT * 128;
+    const uint32_t zchunk = zrows * (uint32_t)a.zsw;
+    const uint32_t wbase = (uint32_t)NS * a.zcols;  // first dW accumulator column
+
+    if (threadIdx.x == 0) {
+        setup_ctl(c, S, NS, kProdWarps * 32 + 1, 1);
+        for (int i = 0; i < NS && i < 4; ++i) {
+            mbar_init(bar_addr(cf.wfull[i]), 1);
+            mbar_init(bar_addr(cf.wempty[i]), kEpiWarps * 32);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_addr(cf.dzfull[i]), kEpiWarps * 32);
+            mbar_init(bar_addr(cf.dzempty[i]), 1);
+            mbar_init(bar_addr(cf.wdrain[i]), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == kProdWarps) {
+        tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = c.tmem;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp < kProdWarps) {
+        // ---------------------------------------------------------- producers
+        producer_loop(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes,
+                      abort_flag, a.status, [&](int64_t k, uint32_t A, uint32_t fb) {
+                          const uint32_t Wt = A + a.a_bytes;
+                          for (int kc = 0; kc < a.nk; ++kc)
+                              tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
+                      });
+    } else if (warp < kProdWarps + 2) {
+        // ---------------------------------------------------------- forward MMA
+        const int me = warp - kProdWarps;
+        const uint32_t idesc = idesc_bf16(128, G, 1, 0);
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            if ((it & 1) != me)
+                continue;
+            const int s = it % S;
+            const int zs = it % NS;
+            if (!mbar_wait(bar_addr(c.tempty[zs]), ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
+                const uint32_t Wt = A + a.a_bytes;
+                for (int t = 0; t < a.MT; ++t) {
+                    const uint32_t d = tbase + (uint32_t)(zs * a.zcols + t * G);
+                    for (int st = 0; st < F / 16; ++st) {
+                        const uint64_t ad = sdesc(A + (uint32_t)t * 2 * F * 128 + (uint32_t)st * 2048,
+                                                  (uint32_t)F * 128, 1024, kLayoutSW128);
+                        const uint64_t bd = sdesc(Wt + (uint32_t)(st / 4) * G * 128 + (uint32_t)(st % 4) * 32,
+                                                  16, 1024, kLayoutSW128);
+                        mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar_addr(c.tfull[zs]));
+            }
+            __syncwarp();
+        }
+        if (lane == 0)
+            mma_commit(bar_addr(c.drain[me]));
+        __syncwarp();
+        mbar_wait_drain(bar_addr(c.drain[me]), 0);
+    } else if (warp < kFWFirstEpi) {
+        // ---------------------------------------------------------- dW MMA
+        const int me = warp - kProdWarps - 2;
+        const uint32_t zlayout = layout_for_swizzle(a.zsw);
+        const uint32_t idesc = idesc_bf16(128, 2 * G, 0, 1);  // N = [hi | lo] along j
+        int it = 0;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            if ((it & 1) != me)
+                continue;
+            const int s = it % S;
+            const int ws = it % NS;
+            const int db = it & 1;
+            if (!mbar_wait(bar_addr(cf.wempty[ws]), ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (!mbar_wait(bar_addr(cf.dzfull[db]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
+                const uint32_t Zs = base + (uint32_t)db * a.dz_bytes;
+                for (int tf = 0; tf < a.FT; ++tf) {
+                    const uint32_t d = tbase + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G);
+                    for (int st = 0; st < a.MT * 8; ++st) {
+                        const uint64_t ad = sdesc(A + (uint32_t)(st / 4) * F * 128 + (uint32_t)tf * 128 * 128 +
+                                                      (uint32_t)(st % 4) * 32,
+                                                  16, 1024, kLayoutSW128);
+                        const uint64_t bd = sdesc(Zs + (uint32_t)st * 16 * a.zsw, zchunk, 8 * a.zsw, zlayout);
+                        mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar_addr(cf.wfull[ws]));
+                mma_commit(bar_addr(cf.dzempty[db]));
+                mma_commit(bar_addr(c.empty[s]));  // last reader of the stage's H_k
+            }
+            __syncwarp();
+        }
+        if (lane == 0)
+            mma_commit(bar_addr(cf.wdrain[me]));
+        __syncwarp();
+        mbar_wait_drain(bar_addr(cf.wdrain[me]), 0);
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int sub = (warp - kFWFirstEpi) / 4;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int zunits = a.MT * (G / CH);
+        const int wunits = a.FT * (G / CH);
+        double lacc = 0.0;
+        bool ok = true;
+        // dW of the group `it` (written one group late, so its MMA has the
+        // BCE of the next group to complete in)
+        auto store_dW = [&](int64_t k, int it) -> bool {
+            const int ws = it % NS;
+            if (!mbar_wait(bar_addr(cf.wfull[ws]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
+                return false;
+            tc_fence_after();
+            for (int u = sub; u < wunits; u += 2) {
+                const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
+                const int f = tf * 128 + q * 32 + lane;
+                const uint32_t col = tbase + lane_off + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G + c0);
+                float v[CH], w[CH];
+                tmem_ld_chunk<CH>(col, v);
+                tmem_ld_chunk<CH>(col + (uint32_t)G, w);
+                uint16_t *dst = a.dW + (k * G + c0) * F + f;
+#pragma unroll
+                for (int i = 0; i < CH; ++i)
+                    dst[(int64_t)i * F] = f2bf(v[i] + w[i]);
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(cf.wempty[ws]));
+            return true;
+        };
+        int it = 0;
+        int64_t kprev = -1;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+            const int zs = it % NS;
+            const int db = it & 1;
+            const int e0 = __ldg(a.gptr + k), e1 = __ldg(a.gptr + k + 1);
+            if (!mbar_wait(bar_addr(c.tfull[zs]), (uint32_t)(it / NS) & 1u, abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            // the dZ buffer of two groups ago must have been consumed by its dW MMA
+            if (!mbar_wait(bar_addr(cf.dzempty[db]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint8_t *tile = a.dZt + (size_t)k * a.tile_bytes;
+            uint8_t *zs_smem = base_ptr + (size_t)db * a.dz_bytes;
+            for (int u = sub; u < zunits; u += 2) {
+                const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
+                const int b = t * 128 + q * 32 + lane;
+                float v[CH];
+                tmem_ld_chunk<CH>(tbase + lane_off + (uint32_t)(zs * a.zcols + t * G + c0), v);
+                if (b < a.B) {
+                    const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
+                    lacc += bce_chunk<CH>(v, y);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < CH; ++i)
+                        v[i] = 0.f;
+                }
+                store_dz_tile<CH>(tile, b, c0, v, a.zsw, a.nzc, a.Bp);
+                store_dz_tile<CH>(zs_smem, b, c0, v, a.zsw, a.nzc, a.Bp);
+            }
+            tc_fence_before();
+            mbar_arrive(bar_addr(c.tempty[zs]));
+            fence_proxy_async();  // dZ_k in shared memory -> the dW MMA (async proxy)
+            mbar_arrive(bar_addr(cf.dzfull[db]));
+            if (kprev >= 0 && !store_dW(kprev, it - 1)) {
+                ok = false;
+                break;
+            }
+            kprev = k;
+        }
+        if (ok && kprev >= 0)
+            store_dW(kprev, it - 1);
+        epi_sum_to(lacc, c, a.loss_part + blockIdx.x, kFWFirstEpi);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProdWarps) {
+        tc_fence_after();
+        tmem_dealloc(tbase, a.tmem_cols);
+    }
+}
+
 // ================================================================== dh
 struct DhArgs {
     const uint16_t *idx_s;
+    const uint8_t *dZt;    // group-tiled dZ input (else the tensor maps)
+    uint64_t tile_bytes;
     float *dh;
     int32_t *status;
     int64_t K, L;
-    int32_t B, G, F, H, MT, nk, S, nzc, zsw, nbands, band_w, win, parts, npass;
-    uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, tmem_cols;
+    int32_t B, G, F, H, MT, nk, S, zsw, nbands, band_w, parts, npass, Bp, vec4;
+    uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, ws_bytes, tmem_cols;
 };
 
-// first f with I[f] >= v (I ascending, n entries)
-__device__ __forceinline__ int lower_bound_u16(const uint16_t *I, int n, int v)
-{
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if ((int)I[mid] < v)
-            lo = mid + 1;
-        else
-            hi = mid;
-    }
-    return lo;
-}
+constexpr int kDhFirstEpi = 2;  // warp 0: loads, warp 1: MMA, then the builders
 
-// CTA (band, mtile, part): dh columns [i0, i1) of the band, samples
-// [128 mt, 128 mt + 128), groups k = part, part + parts, ...  TMEM columns
-// [0, band_w) hold the CTA's fp32 partial of dh; two windows of `win` columns
-// after it receive dH_k = dZ_k W_k for the f range of the band (alternately,
-// so the MMA of the next group overlaps the scatter of this one).
+// CTA (band, mtile, part): dh columns [i0, i0 + band_w) of the band, samples
+// [128 mt, 128 mt + 128), groups k = part, part + parts, ...
+//
+// The scatter-add of dH_k = dZ_k W_k into the columns I_k of dh is itself a
+// product: dh[:, band] += dZ_k Ws_k with Ws_k[j][i - i0] = W_k[j][f] where
+// I_k[f] = i (zero in every other column).  Eight builder warps write Ws_k for
+// the band into shared memory (MN-major, 128-byte swizzle, like W_k itself);
+// one MMA warp accumulates dZ_k Ws_k over all the CTA's groups into one TMEM
+// accumulator of 128 samples x band_w columns, so the partial of dh never
+// leaves TMEM until it is added into dh at the end.
 __global__ void __launch_bounds__(kDhThreads, 1)
     k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
             const __grid_constant__ CUtensorMap tm_w, const DhArgs a)
@@ -782,20 +1133,28 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     __shared__ Ctl c;
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
-    uint8_t *stage0_ptr = dsm + (stage0 - smem_u32(dsm));
+    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+    uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
+    // [Ws buffer 0][Ws buffer 1][stages]
+    const uint32_t stage0 = base + 2 * a.ws_bytes;
+    uint8_t *stage0_ptr = base_ptr + 2 * (size_t)a.ws_bytes;
     const int G = a.G, F = a.F, S = a.S;
     const int band = blockIdx.x % a.nbands;
     const int mt = (blockIdx.x / a.nbands) % a.MT;
-    const int part = blockIdx.x / (a.nbands * a.MT);
+    const int part_id = blockIdx.x / (a.nbands * a.MT);
     const int i0 = band * a.band_w;
-    const int i1 = min(a.H, i0 + a.band_w);
-    const uint32_t zrows = 128;
-    const uint32_t zchunk = zrows * (uint32_t)a.zsw;
-    const uint32_t zplane = (uint32_t)a.nzc * zchunk;
+    const uint32_t zchunk = 128u * (uint32_t)a.zsw;  // one plane of the stage (G <= 64)
 
-    if (threadIdx.x == 0)
-        setup_ctl(c, S, 2, 1, kEpiWarps * 32);  // stages released by the epilogue
+    // stages: full = loads landed; empty = the MMAs that read them are done.
+    // tfull/tempty[0..1] = Ws buffer written / consumed; drain[0] = last MMA.
+    if (threadIdx.x == 0) {
+        setup_ctl(c, S, 0, 1, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_addr(c.tfull[i]), kEpiWarps * 32);
+            mbar_init(bar_addr(c.tempty[i]), 1);
+        }
+        fence_mbar_init();
+    }
     if (warp == 1) {
         tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
         tmem_relinquish();
@@ -807,8 +1166,9 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     volatile int *abort_flag = &c.abort_flag;
 
     if (warp == 0) {
+        // ---------------------------------------------------------- producer
         int it = 0;
-        for (int64_t k = part; k < a.K; k += a.parts, ++it) {
+        for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
             const uint32_t ph = (uint32_t)(it / S) & 1u;
             if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
@@ -819,11 +1179,15 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             const uint32_t fb = bar_addr(c.full[s]);
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, a.z_bytes + a.w_bytes + (uint32_t)F * 2);
-                for (int cj = 0; cj < a.nzc; ++cj) {
-                    tma_load_2d(Zs + (uint32_t)cj * zchunk, &tm_z, (int)(k * G + cj * 64), mt * 128, fb);
+                if (a.dZt) {
+                    // rows [128 mt, 128 mt + 128) of each plane of the tile
+                    const uint8_t *t = a.dZt + (size_t)k * a.tile_bytes + (size_t)mt * zchunk;
+                    for (int pl = 0; pl < a.npass; ++pl)
+                        bulk_load(Zs + (uint32_t)pl * zchunk, t + (size_t)pl * a.Bp * a.zsw, zchunk, fb);
+                } else {
+                    tma_load_2d(Zs, &tm_z, (int)(k * G), mt * 128, fb);
                     if (a.npass > 1)
-                        tma_load_2d(Zs + zplane + (uint32_t)cj * zchunk, &tm_zl, (int)(k * G + cj * 64),
-                                    mt * 128, fb);
+                        tma_load_2d(Zs + zchunk, &tm_zl, (int)(k * G), mt * 128, fb);
                 }
                 for (int kc = 0; kc < a.nk; ++kc)
                     tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
@@ -833,118 +1197,112 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         }
         drain_loads(c, it, S);
     } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issue
         const uint32_t zlayout = layout_for_swizzle(a.zsw);
         const int nks = G / 16;
         int it = 0;
-        for (int64_t k = part; k < a.K; k += a.parts, ++it) {
+        for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
-            const int wb = it & 1;
-            if (!mbar_wait(bar_addr(c.tempty[wb]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
+            const int nb = it & 1;
+            if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
-            tc_fence_after();
-            if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.tfull[nb]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t Zs = stage0 + (uint32_t)s * a.stage_bytes;
-                const uint32_t Wt = Zs + a.z_bytes;
-                const uint16_t *I = reinterpret_cast<const uint16_t *>(
-                    stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes + a.w_bytes);
-                // f range whose index falls in [i0, i1): I_k is ascending
-                const int fa = lower_bound_u16(I, F, i0), fbnd = lower_bound_u16(I, F, i1);
-                // whole 64-f chunks of W_k that hold part of the f range:
-                // every window starts on a swizzle-atom boundary of the tile
-                const uint32_t dbase = tbase + (uint32_t)(a.band_w + wb * a.win);
-                if (fa < fbnd) {
-                    const int c_first = fa / 64, c_last = (fbnd - 1) / 64;
-                    const uint32_t idesc = idesc_bf16(128, 64, 0, 1);
-                    for (int cc = c_first; cc <= c_last; ++cc) {
-                        const uint32_t d = dbase + (uint32_t)((cc - c_first) * 64);
-                        // K runs over j for dZ hi (and again for dZ lo) against W_k
-                        for (int ks2 = 0; ks2 < a.npass * nks; ++ks2) {
-                            const int ks = ks2 % nks;
-                            const uint32_t za = Zs + (uint32_t)(ks2 / nks) * zplane +
-                                                (uint32_t)(ks / 4) * zchunk + (uint32_t)(ks % 4) * 32;
-                            const uint64_t ad = sdesc(za, 16, 8 * a.zsw, zlayout);
-                            const uint64_t bd = sdesc(Wt + (uint32_t)cc * G * 128 + (uint32_t)ks * 2048,
-                                                      (uint32_t)G * 128, 1024, kLayoutSW128);
-                            mma_bf16(d, ad, bd, idesc, ks2 > 0 ? 1u : 0u);
-                        }
+                const uint32_t Ws = base + (uint32_t)nb * a.ws_bytes;
+                // K runs over j for dZ hi (and again for dZ lo) against Ws_k;
+                // N over the band in pieces of at most 256 columns
+                for (int ks2 = 0; ks2 < a.npass * nks; ++ks2) {
+                    const int ks = ks2 % nks;
+                    const uint32_t za = Zs + (uint32_t)(ks2 / nks) * zchunk + (uint32_t)ks * 32;
+                    const uint64_t ad = sdesc(za, 16, 8 * a.zsw, zlayout);
+                    for (int n0 = 0; n0 < a.band_w; n0 += 256) {
+                        const int nn = a.band_w - n0 < 256 ? a.band_w - n0 : 256;
+                        const uint64_t bd = sdesc(Ws + (uint32_t)(n0 / 64) * G * 128 + (uint32_t)ks * 2048,
+                                                  (uint32_t)G * 128, 1024, kLayoutSW128);
+                        mma_bf16(tbase + (uint32_t)n0, ad, bd, idesc_bf16(128, nn, 0, 1),
+                                 (it > 0 || ks2 > 0) ? 1u : 0u);
                     }
                 }
-                mma_commit(bar_addr(c.tfull[wb]));
+                mma_commit(bar_addr(c.tempty[nb]));
+                mma_commit(bar_addr(c.empty[s]));
             }
             __syncwarp();
         }
         if (lane == 0)
             mma_commit(bar_addr(c.drain[0]));
         __syncwarp();
-        mbar_wait_drain(bar_addr(c.drain[0]), 0);
+        mbar_wait_drain(bar_addr(c.drain[0]), 0);  // no MMA in flight at the dealloc
     } else {
-        // two warps per TMEM lane quarter.  They may be working on different
-        // groups at the same time (the dH windows are double buffered), so
-        // they own disjoint partial columns (column parity) rather than
-        // disjoint pieces: no column is ever updated by both.
-        const int q = warp & 3;
-        const int sub = (warp - 2) / 4;
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        for (int col = sub; col < a.band_w; col += 2)
-            tmem_st1(tbase + lane_off + (uint32_t)col, 0u);
-        tmem_st_wait();
+        // ---------------------------------------------------------- builders
+        const int ew = warp - kDhFirstEpi;  // 0 .. 7
+        const int t = ew * 32 + lane;
         int it = 0;
-        for (int64_t k = part; k < a.K; k += a.parts, ++it) {
+        for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
-            const int wb = it & 1;
-            if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
+            const int nb = it & 1;
+            if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
-            if (!mbar_wait(bar_addr(c.tfull[wb]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.tempty[nb]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
                 break;
-            tc_fence_after();
-            const uint16_t *I = reinterpret_cast<const uint16_t *>(
-                stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes + a.w_bytes);
-            const int fa = lower_bound_u16(I, F, i0), fbnd = lower_bound_u16(I, F, i1);
-            const int fbase = (fa / 64) * 64;  // first f of the first window
-            const uint32_t dbase = tbase + lane_off + (uint32_t)(a.band_w + wb * a.win);
-            for (int p = fa / 16; p * 16 < fbnd; ++p) {
-                uint32_t r[16];
-                tmem_ld16(dbase + (uint32_t)(p * 16 - fbase), r);
-                uint32_t col[16], old[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int f = p * 16 + u;
-                    const uint32_t cf = (f >= fa && f < fbnd) ? (uint32_t)(I[f] - i0) : 0xffffffffu;
-                    col[u] = (cf != 0xffffffffu && (int)(cf & 1u) == sub) ? cf : 0xffffffffu;
-                    old[u] = 0u;
-                    if (col[u] != 0xffffffffu)
-                        old[u] = tmem_ld1(tbase + lane_off + col[u]);
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (col[u] != 0xffffffffu)
-                        tmem_st1(tbase + lane_off + col[u],
-                                 __float_as_uint(__uint_as_float(old[u]) + __uint_as_float(r[u])));
+            uint8_t *Ws = base_ptr + (size_t)nb * a.ws_bytes;
+            const uint8_t *Wt = stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes;
+            const uint16_t *I = reinterpret_cast<const uint16_t *>(Wt + a.w_bytes);
+            // clear the buffer (its last use held another group's columns)
+            for (uint32_t o = (uint32_t)t * 16; o < a.ws_bytes; o += kEpiWarps * 32 * 16)
+                *reinterpret_cast<uint4 *>(Ws + o) = make_uint4(0, 0, 0, 0);
+            // f range of the band: I_k ascending, so count entries below each end
+            int na = 0, ne = 0;
+            for (int f = lane; f < F; f += 32) {
+                const int v = I[f];
+                na += v < i0;
+                ne += v < i0 + a.band_w;
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar_addr(c.tempty[wb]));
-            mbar_arrive(bar_addr(c.empty[s]));
+            const int fa = __reduce_add_sync(0xffffffffu, na);
+            const int fe = __reduce_add_sync(0xffffffffu, ne);
+            named_bar(1, kEpiWarps * 32);  // every clear lands before any write
+            // warp ew writes rows j = ew, ew + 8, ...; lanes run along f
+            for (int f = fa + lane; f < fe; f += 32) {
+                const int i = (int)I[f] - i0;
+                const uint32_t wsrc = (uint32_t)(f >> 6) * G * 128 + (uint32_t)(((f & 63) >> 3) << 4) +
+                                      (uint32_t)(f & 7) * 2;
+                const uint32_t wdst = (uint32_t)(i >> 6) * G * 128 + (uint32_t)(((i & 63) >> 3) << 4) +
+                                      (uint32_t)(i & 7) * 2;
+                for (int j = ew; j < G; j += kEpiWarps) {
+                    const uint32_t row = (uint32_t)j * 128, sw = (uint32_t)(j & 7) << 4;
+                    const uint16_t w = *reinterpret_cast<const uint16_t *>(Wt + ((wsrc + row) ^ sw));
+                    *reinterpret_cast<uint16_t *>(Ws + ((wdst + row) ^ sw)) = w;
+                }
+            }
+            fence_proxy_async();  // Ws_k (generic writes) -> the MMA (async proxy)
+            mbar_arrive(bar_addr(c.tfull[nb]));
         }
-        // add the partial into dh, once both warps of every quarter are done
-        named_bar(1, kEpiWarps * 32);
-        const int b = mt * 128 + q * 32 + lane;
-        for (int c0 = sub * 32; c0 < a.band_w; c0 += 64) {
-            uint32_t r[32];
-            tmem_ld32(tbase + lane_off + (uint32_t)c0, r);
-            tmem_ld_wait();
-            if (b < a.B) {
+        // the accumulator holds this CTA's partial of dh[:, band]: add it in
+        if (mbar_wait(bar_addr(c.drain[0]), 0, abort_flag, a.status) && !*abort_flag && it > 0) {
+            tc_fence_after();
+            const int q = warp & 3, sub = ew / 4;
+            const int b = mt * 128 + q * 32 + lane;
+            const int i_end = a.H - i0 < a.band_w ? a.H - i0 : a.band_w;
+            for (int c0 = sub * 32; c0 < a.band_w; c0 += 64) {
+                uint32_t r[32];
+                tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+                tmem_ld_wait();
+                if (b < a.B) {
+                    float *dst = a.dh + (int64_t)b * a.H + i0 + c0;
+                    if (a.vec4 && c0 + 32 <= i_end) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int colg = i0 + c0 + i;
-                    if (colg < i1)
-                        atomicAdd(a.dh + (int64_t)b * a.H + colg, __uint_as_float(r[i]));
+                        for (int i = 0; i < 32; i += 4)
+                            atomicAdd(reinterpret_cast<float4 *>(dst + i),
+                                      make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                                  __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c0 + i < i_end)
+                                atomicAdd(dst + i, __uint_as_float(r[i]));
+                    }
                 }
             }
         }
@@ -989,10 +1347,25 @@ bool tc_stage_ok(const sg_layout *lo, int stage, int B)
     }
 }
 
+uint64_t tc_dz_tile_bytes(const sg_layout *lo, int32_t B)
+{
+    const int Bp = (B + 127) / 128 * 128;
+    return 2ull * (uint64_t)Bp * (uint64_t)lo->G * 2ull;
+}
+
+bool tc_tiled_ok(const sg_layout *lo, int32_t B)
+{
+    return dz_ok(lo->G) && plan_fwd(lo, B).ok && plan_dW(lo, B, true).ok && plan_dh(lo, B, true).ok;
+}
+
 sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint16_t *dZ,
-                 uint16_t *dZ_lo, double *loss, cudaStream_t st)
+                 uint16_t *dZ_lo, uint8_t *dZt, double *loss, cudaStream_t st)
 {
     const FwdPlan p = plan_fwd(lo, B);
+    if (dZt && !dz_ok(lo->G)) {
+        sg_set_error("tc_fwd: group size %d has no tiled dZ layout", lo->G);
+        return SG_ERR_UNSUPPORTED;
+    }
     if (!p.ok) {
         sg_set_error("tc_fwd: shape not supported by the tensor-core engine");
         return SG_ERR_UNSUPPORTED;
@@ -1007,6 +1380,11 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     a.Z = Z;
     a.dZ = dZ;
     a.dZ_lo = dZ_lo;
+    a.dZt = dZt;
+    a.tile_bytes = tc_dz_tile_bytes(lo, B);
+    a.zsw = dz_swizzle(lo->G);
+    a.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
+    a.Bp = p.MT * 128;
     a.gptr = lo->gptr;
     a.gent = lo->gent;
     a.loss_part = lo->loss_part;
@@ -1027,7 +1405,7 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     a.tmem_cols = p.tmem_cols;
     const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
-    const bool bce = dZ != nullptr;
+    const bool bce = dZ != nullptr || dZt != nullptr;
     void (*kern)(CUtensorMap, FwdArgs);
     if (lo->G >= 64)
         kern = bce ? k_tc_fwd<true, 32> : k_tc_fwd<false, 32>;
@@ -1043,22 +1421,82 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     return SG_OK;
 }
 
-sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B,
-                uint16_t *dW, cudaStream_t st)
+bool tc_fwdw_ok(const sg_layout *lo, int32_t B) { return plan_fwdw(lo, B).ok; }
+
+sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
+                  double *loss, cudaStream_t st)
 {
-    const DWPlan p = plan_dW(lo, B, dZ_lo != nullptr);
+    const FWPlan p = plan_fwdw(lo, B);
+    if (!p.ok) {
+        sg_set_error("tc_fwdw: shape not supported by the fused forward + dW kernel");
+        return SG_ERR_UNSUPPORTED;
+    }
+    CUtensorMap tm_w;
+    sg_status rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)lo->G, 128, "W");
+    if (rc != SG_OK)
+        return rc;
+    FWArgs a;
+    a.idx_s = lo->idx_s;
+    a.hT = lo->hT;
+    a.dZt = dZt;
+    a.tile_bytes = tc_dz_tile_bytes(lo, B);
+    a.dW = dW;
+    a.gptr = lo->gptr;
+    a.gent = lo->gent;
+    a.loss_part = lo->loss_part;
+    a.status = lo->status;
+    a.K = lo->K;
+    a.L = lo->L;
+    a.B = B;
+    a.G = lo->G;
+    a.F = lo->F;
+    a.MT = p.MT;
+    a.FT = p.FT;
+    a.nk = p.nk;
+    a.S = p.S;
+    a.zsw = p.zsw;
+    a.nzc = p.nzc;
+    a.nslot = p.nslot;
+    a.Bp = p.MT * 128;
+    a.ldB = lo->ldB;
+    a.a_bytes = p.a_bytes;
+    a.w_bytes = p.w_bytes;
+    a.stage_bytes = p.stage_bytes;
+    a.dz_bytes = p.dz_bytes;
+    a.zcols = p.zcols;
+    a.wcols = p.wcols;
+    a.tmem_cols = p.tmem_cols;
+    const size_t smem = 2 * (size_t)p.dz_bytes + (size_t)p.S * p.stage_bytes + 1024;
+    const int grid = persistent_grid(lo, lo->K);
+    void (*kern)(CUtensorMap, FWArgs) = lo->G >= 64 ? k_tc_fwdw<32> : k_tc_fwdw<16>;
+    rc = set_smem(kern, smem);
+    if (rc != SG_OK)
+        return rc;
+    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, kFWThreads, smem, st>>>(tm_w, a));
+    SG_TRY_CUDA(cudaGetLastError());
+    return sg_loss_finalize(lo, grid, loss, st);
+}
+
+sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
+                int32_t B, uint16_t *dW, cudaStream_t st)
+{
+    const DWPlan p = plan_dW(lo, B, dZ_lo != nullptr || dZt != nullptr);
     if (!p.ok) {
         sg_set_error("tc_dW: shape not supported by the tensor-core engine");
         return SG_ERR_UNSUPPORTED;
     }
     CUtensorMap tm_z, tm_zl;
     const int zbox = lo->G < 64 ? lo->G : 64;
-    sg_status rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
-                               (uint32_t)(p.MT * 128), p.zsw, "dZ");
-    if (rc != SG_OK)
-        return rc;
+    sg_status rc = SG_OK;
+    memset(&tm_z, 0, sizeof(tm_z));
+    if (!dZt) {
+        rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
+                         (uint32_t)(p.MT * 128), p.zsw, "dZ");
+        if (rc != SG_OK)
+            return rc;
+    }
     tm_zl = tm_z;
-    if (dZ_lo) {
+    if (dZ_lo && !dZt) {
         rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
                          (uint32_t)(p.MT * 128), p.zsw, "dZ_lo");
         if (rc != SG_OK)
@@ -1067,6 +1505,8 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     DWArgs a;
     a.idx_s = lo->idx_s;
     a.hT = lo->hT;
+    a.dZt = dZt;
+    a.tile_bytes = tc_dz_tile_bytes(lo, B);
     a.dW = dW;
     a.status = lo->status;
     a.K = lo->K;
@@ -1099,23 +1539,26 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     return SG_OK;
 }
 
-sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B,
-                const uint16_t *W, float *dh, cudaStream_t st)
+sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
+                int32_t B, const uint16_t *W, float *dh, cudaStream_t st)
 {
-    const DhPlan p = plan_dh(lo, B, dZ_lo != nullptr);
+    const bool split = dZ_lo != nullptr || dZt != nullptr;
+    const DhPlan p = plan_dh(lo, B, split);
     if (!p.ok) {
         sg_set_error("tc_dh: shape not supported by the tensor-core engine");
         return SG_ERR_UNSUPPORTED;
     }
     CUtensorMap tm_z, tm_zl, tm_w;
-    const int zbox = lo->G < 64 ? lo->G : 64;
-    sg_status rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox, 128,
-                               p.zsw, "dZ");
-    if (rc != SG_OK)
-        return rc;
+    sg_status rc = SG_OK;
+    memset(&tm_z, 0, sizeof(tm_z));
+    if (!dZt) {
+        rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)lo->G, 128, p.zsw, "dZ");
+        if (rc != SG_OK)
+            return rc;
+    }
     tm_zl = tm_z;
-    if (dZ_lo) {
-        rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox, 128, p.zsw,
+    if (dZ_lo && !dZt) {
+        rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)lo->G, 128, p.zsw,
                          "dZ_lo");
         if (rc != SG_OK)
             return rc;
@@ -1125,6 +1568,8 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
         return rc;
     DhArgs a;
     a.idx_s = lo->idx_s;
+    a.dZt = dZt;
+    a.tile_bytes = tc_dz_tile_bytes(lo, B);
     a.dh = dh;
     a.status = lo->status;
     a.K = lo->K;
@@ -1136,12 +1581,12 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     a.MT = p.MT;
     a.nk = p.nk;
     a.S = p.S;
-    a.nzc = p.nzc;
     a.zsw = p.zsw;
     a.nbands = p.nbands;
     a.band_w = p.band_w;
-    a.win = p.win;
-    a.npass = dZ_lo ? 2 : 1;
+    a.npass = split ? 2 : 1;
+    a.Bp = p.MT * 128;
+    a.vec4 = (lo->H % 4 == 0 && ((uintptr_t)dh & 15) == 0) ? 1 : 0;
     int parts = lo->num_sms / (p.nbands * p.MT);
     if (parts < 1)
         parts = 1;
@@ -1152,8 +1597,9 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     a.w_bytes = p.w_bytes;
     a.i_bytes = p.i_bytes;
     a.stage_bytes = p.stage_bytes;
+    a.ws_bytes = p.ws_bytes;
     a.tmem_cols = p.tmem_cols;
-    const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
+    const size_t smem = 2 * (size_t)p.ws_bytes + (size_t)p.S * p.stage_bytes + 1024;
     rc = set_smem(k_tc_dh, smem);
     if (rc != SG_OK)
         return rc;
