@@ -288,12 +288,14 @@ __device__ __forceinline__ int swz_of(int r, int zsw)
 // bf16 values into plane 0, their rounding residuals into plane 1
 template <int CH>
 __device__ __forceinline__ void store_dz_tile(uint8_t *tile, int r, int c0, const float (&v)[CH],
-                                              int zsw, int nzc, int Bp)
+                                              int zsw, int nzc, int Bp, uint8_t *tile2 = nullptr)
 {
     const int sw = swz_of(r, zsw);
     const int u0 = (c0 & 63) >> 3;
-    uint8_t *hi = tile + ((size_t)(c0 >> 6) * Bp + r) * zsw;
-    uint8_t *lo = hi + (size_t)nzc * Bp * zsw;
+    const size_t row = ((size_t)(c0 >> 6) * Bp + r) * zsw;
+    const size_t plane = (size_t)nzc * Bp * zsw;
+    uint8_t *hi = tile + row;
+    uint8_t *lo = hi + plane;
 #pragma unroll
     for (int i = 0; i < CH / 8; ++i) {
         const float *x = v + 8 * i;
@@ -309,6 +311,10 @@ __device__ __forceinline__ void store_dz_tile(uint8_t *tile, int r, int c0, cons
         const int off = ((u0 + i) ^ sw) << 4;
         *reinterpret_cast<uint4 *>(hi + off) = q;
         *reinterpret_cast<uint4 *>(lo + off) = e;
+        if (tile2) {  // the same bytes into a second copy of the tile
+            *reinterpret_cast<uint4 *>(tile2 + row + off) = q;
+            *reinterpret_cast<uint4 *>(tile2 + row + plane + off) = e;
+        }
     }
 }
 
@@ -354,20 +360,36 @@ __device__ __forceinline__ uint32_t group_pos_mask(const int32_t *__restrict__ g
 template <int CH>
 __device__ __forceinline__ float bce_chunk(float (&v)[CH], uint32_t y)
 {
-    float prod = 1.f, lin = 0.f;
+    float prod = 1.f, lin = 0.f, zpos = 0.f;
+    if (y) {  // positives are rare: their terms are applied separately
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+            if ((y >> i) & 1u)
+                zpos += v[i];
+    }
 #pragma unroll
     for (int i = 0; i < CH; ++i) {
         const float z = v[i];
         const float e = __expf(-fabsf(z));
         const float one_e = 1.f + e;
         const float r = __fdividef(1.f, one_e);
-        const float sig = z >= 0.f ? r : e * r;
-        const bool yi = (y >> i) & 1u;
-        lin += fmaxf(z, 0.f) - (yi ? z : 0.f);
+        v[i] = z >= 0.f ? r : e * r;
+        lin += fmaxf(z, 0.f);
         prod *= one_e;
-        v[i] = sig - (yi ? 1.f : 0.f);
     }
-    return lin + __logf(prod);
+    if (y) {
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+            if ((y >> i) & 1u)
+                v[i] -= 1.f;
+    }
+    return lin - zpos + __logf(prod);
+}
+
+// fp32 -> bf16 bits, round to nearest even (the hardware conversion)
+__device__ __forceinline__ uint16_t bf16_rn(float x)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
 // After an abort, wait (bounded) until the loads of the last stages issued
@@ -399,44 +421,44 @@ __device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst, int fi
 }
 
 // ------------------------------------------------------------------ gather
-// H_k = rows I_k[f] of hT, copied with 16-byte cp.async by the producer
-// threads into the 128-byte-swizzled layout [b-chunk of 64][f][64 b]: unit u
+// H_k = rows I_k[f] of hT, copied with 16-byte cp.async by the four producer
+// warps into the 128-byte-swizzled layout [b-chunk of 64][f][64 b]: unit u
 // (16 B) of row f lands at chunk(u/8) * F*128 + f*128 + ((u%8) ^ (f%8))*16.
-// Thread t copies the units u of rows f = t mod F (every unit of its row when
-// F = 128); its row indices are loaded one group ahead.
-struct GatherRows {
-    int f0, f1;   // rows of this thread (f1 = -1 if one row)
-    int i0, i1;   // their indices in hT
+// Producer warp pw copies rows f in [pw*RW, pw*RW + RW), RW = F/4.  The lanes
+// of one cp.async instruction cover whole rows (16 lanes per 256-byte row when
+// B <= 128, all 32 when B <= 256), so every 32-byte sector fetched from L2 is
+// used in full.  A lane holds the hT row index of rows pw*RW + lane (+ 32),
+// loaded one group ahead; the copy loop broadcasts them with shuffles.
+struct GatherIdx {
+    uint32_t i[2];
 };
 
-__device__ __forceinline__ GatherRows gather_rows_of(const uint16_t *idx_s, int64_t k, int F, int t)
+__device__ __forceinline__ GatherIdx gather_idx_of(const uint16_t *idx_s, int64_t k, int F, int lane)
 {
-    GatherRows g;
-    g.f0 = t % F;
-    g.f1 = F > kProdWarps * 32 ? t + kProdWarps * 32 : -1;
-    const uint16_t *I = idx_s + k * F;
-    g.i0 = __ldg(I + g.f0);
-    g.i1 = g.f1 >= 0 ? __ldg(I + g.f1) : 0;
+    const int RW = F / kProdWarps;
+    const int pw = threadIdx.x / 32;
+    const uint16_t *I = idx_s + k * F + pw * RW;
+    GatherIdx g;
+    g.i[0] = lane < RW ? __ldg(I + lane) : 0u;
+    g.i[1] = lane + 32 < RW ? __ldg(I + lane + 32) : 0u;
     return g;
 }
 
 __device__ __forceinline__ void issue_gather(const uint16_t *hT, int ldB, uint32_t A, int F,
-                                             int units, const GatherRows &g, int t)
+                                             int units, const GatherIdx &g, int lane)
 {
-    // units = MT * 16 16-byte units per row; rows f0 (and f1) of this thread
-    const int nthr = kProdWarps * 32;
-    const int rows_per_pass = nthr < F ? nthr : F;     // threads sharing the rows
-    const int u_step = nthr / rows_per_pass;           // threads per row
-    const int u_first = t / rows_per_pass;
-    for (int r = 0; r < 2; ++r) {
-        const int f = r == 0 ? g.f0 : g.f1;
-        if (f < 0)
-            break;
-        const uint16_t *src = hT + (size_t)(r == 0 ? g.i0 : g.i1) * ldB;
-        const uint32_t rowbase = A + (uint32_t)f * 128;
-        for (int u = u_first; u < units; u += u_step) {
-            const int cch = u >> 3, w = u & 7;
-            cp_async16(rowbase + (uint32_t)cch * F * 128 + (uint32_t)((w ^ (f & 7)) << 4), src + u * 8);
+    const int RW = F / kProdWarps;
+    const int pw = threadIdx.x / 32;
+    const int lpr = units < 32 ? units : 32;  // lanes per row
+    const int rpi = 32 / lpr;                 // rows per instruction
+    const int u = lane % lpr, rsub = lane / lpr;
+    for (int r0 = 0; r0 < RW; r0 += rpi) {
+        const int r = r0 + rsub;
+        const uint32_t row = __shfl_sync(0xffffffffu, r0 < 32 ? g.i[0] : g.i[1], r & 31);
+        if (r < RW) {
+            const int f = pw * RW + r;
+            cp_async16(A + (uint32_t)(u >> 3) * F * 128 + (uint32_t)f * 128 + (uint32_t)(((u & 7) ^ (f & 7)) << 4),
+                       hT + (size_t)row * ldB + u * 8);
         }
     }
 }
@@ -455,17 +477,18 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
 {
     constexpr int kLag = 2;
     const int t = threadIdx.x;  // producer threads are 0 .. kProdWarps*32-1
+    const int lane = t & 31;
     const int units = MT * 16;
     int it = 0;
-    GatherRows cur = {0, -1, 0, 0};
+    GatherIdx cur = {{0u, 0u}};
     if (blockIdx.x < K)
-        cur = gather_rows_of(idx_s, blockIdx.x, F, t);
+        cur = gather_idx_of(idx_s, blockIdx.x, F, lane);
     for (int64_t k = blockIdx.x; k < K; k += gridDim.x, ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
-        GatherRows nxt = cur;
+        GatherIdx nxt = cur;
         if (k + gridDim.x < K)
-            nxt = gather_rows_of(idx_s, k + gridDim.x, F, t);
+            nxt = gather_idx_of(idx_s, k + gridDim.x, F, lane);
         if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status))
             break;
         const uint32_t A = stage0 + (uint32_t)s * stage_bytes;
@@ -473,7 +496,7 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
             mbar_arrive_expect_tx(bar_addr(c.full[s]), tma_bytes);
             issue_tma(k, A, bar_addr(c.full[s]));
         }
-        issue_gather(hT, ldB, A, F, units, cur, t);
+        issue_gather(hT, ldB, A, F, units, cur, lane);
         cp_async_commit();
         if (it >= kLag) {
             cp_async_wait<kLag>();
@@ -623,12 +646,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int units = a.MT * (G / CH);
         double lacc = 0.0;
         int it = 0;
+        // positive-list bounds of the group, loaded one group ahead
+        int e0n = 0, e1n = 0;
+        if (BCE && blockIdx.x < a.K) {
+            e0n = __ldg(a.gptr + blockIdx.x);
+            e1n = __ldg(a.gptr + blockIdx.x + 1);
+        }
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
             const int acc = acc_slot(it, a.issuers);
-            int e0 = 0, e1 = 0;
-            if (BCE) {
-                e0 = __ldg(a.gptr + k);
-                e1 = __ldg(a.gptr + k + 1);
+            const int e0 = e0n, e1 = e1n;
+            if (BCE && k + gridDim.x < a.K) {
+                e0n = __ldg(a.gptr + k + gridDim.x);
+                e1n = __ldg(a.gptr + k + gridDim.x + 1);
             }
             if (!mbar_wait(bar_addr(c.tfull[acc]), acc_phase(it, a.issuers), abort_flag, a.status))
                 break;
@@ -804,7 +833,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 uint16_t *dst = a.dW + (k * G + c0) * F + f;
 #pragma unroll
                 for (int i = 0; i < CH; ++i)
-                    dst[(int64_t)i * F] = f2bf(v[i]);
+                    dst[(int64_t)i * F] = bf16_rn(v[i]);
             }
             tc_fence_before();
             mbar_arrive(bar_addr(c.tempty[acc]));
@@ -1040,7 +1069,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 uint16_t *dst = a.dW + (k * G + c0) * F + f;
 #pragma unroll
                 for (int i = 0; i < CH; ++i)
-                    dst[(int64_t)i * F] = f2bf(v[i] + w[i]);
+                    dst[(int64_t)i * F] = bf16_rn(v[i] + w[i]);
             }
             tc_fence_before();
             mbar_arrive(bar_addr(cf.wempty[ws]));
@@ -1048,10 +1077,20 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         };
         int it = 0;
         int64_t kprev = -1;
+        // positive-list bounds of the group, loaded one group ahead
+        int e0n = 0, e1n = 0;
+        if (blockIdx.x < a.K) {
+            e0n = __ldg(a.gptr + blockIdx.x);
+            e1n = __ldg(a.gptr + blockIdx.x + 1);
+        }
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
             const int zs = it % NS;
             const int db = it & 1;
-            const int e0 = __ldg(a.gptr + k), e1 = __ldg(a.gptr + k + 1);
+            const int e0 = e0n, e1 = e1n;
+            if (k + gridDim.x < a.K) {
+                e0n = __ldg(a.gptr + k + gridDim.x);
+                e1n = __ldg(a.gptr + k + gridDim.x + 1);
+            }
             if (!mbar_wait(bar_addr(c.tfull[zs]), (uint32_t)(it / NS) & 1u, abort_flag, a.status)) {
                 ok = false;
                 break;
@@ -1077,8 +1116,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     for (int i = 0; i < CH; ++i)
                         v[i] = 0.f;
                 }
-                store_dz_tile<CH>(tile, b, c0, v, a.zsw, a.nzc, a.Bp);
-                store_dz_tile<CH>(zs_smem, b, c0, v, a.zsw, a.nzc, a.Bp);
+                store_dz_tile<CH>(tile, b, c0, v, a.zsw, a.nzc, a.Bp, zs_smem);
             }
             tc_fence_before();
             mbar_arrive(bar_addr(c.tempty[zs]));
@@ -1111,13 +1149,23 @@ struct DhArgs {
     int32_t *status;
     int64_t K, L;
     int32_t B, G, F, H, MT, nk, S, zsw, nbands, band_w, parts, npass, Bp, vec4;
+    int32_t csize;  // CTAs per cluster: the bands of one (mtile, part), or 1
     uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, ws_bytes, tmem_cols;
 };
 
 constexpr int kDhFirstEpi = 2;  // warp 0: loads, warp 1: MMA, then the builders
+// Multicast the band CTAs' common loads across a cluster (off: measured
+// slower than independent loads that hit in L2, the cluster-wide stage
+// release costing more than the L2 traffic it saves)
+constexpr bool kDhMulticast = false;
 
 // CTA (band, mtile, part): dh columns [i0, i0 + band_w) of the band, samples
-// [128 mt, 128 mt + 128), groups k = part, part + parts, ...
+// [128 mt, 128 mt + 128), groups k = part, part + parts, ...  The band CTAs of
+// one (mtile, part) form a cluster and read the same tiles: each loads a share
+// of a stage's pieces and multicasts it to all of them, so a tile crosses from
+// L2 once per cluster rather than once per band.  A CTA's stage is refilled
+// once every CTA of the cluster has released it (a cluster-wide barrier per
+// stage, `cempty`).
 //
 // The scatter-add of dH_k = dZ_k W_k into the columns I_k of dh is itself a
 // product: dh[:, band] += dZ_k Ws_k with Ws_k[j][i - i0] = W_k[j][f] where
@@ -1131,10 +1179,12 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             const __grid_constant__ CUtensorMap tm_w, const DhArgs a)
 {
     __shared__ Ctl c;
+    __shared__ uint64_t cempty[kMaxStages];
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
+    const int C = a.csize;
     // [Ws buffer 0][Ws buffer 1][stages]
     const uint32_t stage0 = base + 2 * a.ws_bytes;
     uint8_t *stage0_ptr = base_ptr + 2 * (size_t)a.ws_bytes;
@@ -1153,6 +1203,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             mbar_init(bar_addr(c.tfull[i]), kEpiWarps * 32);
             mbar_init(bar_addr(c.tempty[i]), 1);
         }
+        for (int s = 0; s < S && s < kMaxStages; ++s)
+            mbar_init(bar_addr(cempty[s]), (uint32_t)C);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -1161,6 +1213,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (C > 1)
+        cluster_sync();  // every CTA's barriers exist before any remote use
     tc_fence_after();
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
@@ -1173,25 +1227,55 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             const uint32_t ph = (uint32_t)(it / S) & 1u;
             if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
                 break;
+            if (C > 1) {
+                // stage s is free here; load into it once it is free everywhere
+                if (lane == 0)
+                    for (int r = 0; r < C; ++r)
+                        mbar_arrive_cluster(mapa_shared(bar_addr(cempty[s]), (uint32_t)r));
+                __syncwarp();
+                if (!mbar_wait(bar_addr(cempty[s]), ph, abort_flag, a.status))
+                    break;
+            }
             const uint32_t Zs = stage0 + (uint32_t)s * a.stage_bytes;
             const uint32_t Wt = Zs + a.z_bytes;
             const uint32_t Is = Wt + a.w_bytes;
             const uint32_t fb = bar_addr(c.full[s]);
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, a.z_bytes + a.w_bytes + (uint32_t)F * 2);
+                // pieces of the stage, dealt round-robin over the cluster
+                const uint16_t mask = (uint16_t)((1u << C) - 1u);
+                int piece = 0;
+                const int rank = C > 1 ? band : 0;  // this CTA's rank in its cluster
+                auto mine = [&]() { return (piece++ % C) == rank; };
+                auto bulk = [&](uint32_t dst, const void *src, uint32_t bytes) {
+                    if (mine()) {
+                        if (C > 1)
+                            bulk_load_mc(dst, src, bytes, fb, mask);
+                        else
+                            bulk_load(dst, src, bytes, fb);
+                    }
+                };
+                auto tile = [&](uint32_t dst, const CUtensorMap *m, int x, int y) {
+                    if (mine()) {
+                        if (C > 1)
+                            tma_load_2d_mc(dst, m, x, y, fb, mask);
+                        else
+                            tma_load_2d(dst, m, x, y, fb);
+                    }
+                };
                 if (a.dZt) {
                     // rows [128 mt, 128 mt + 128) of each plane of the tile
                     const uint8_t *t = a.dZt + (size_t)k * a.tile_bytes + (size_t)mt * zchunk;
                     for (int pl = 0; pl < a.npass; ++pl)
-                        bulk_load(Zs + (uint32_t)pl * zchunk, t + (size_t)pl * a.Bp * a.zsw, zchunk, fb);
+                        bulk(Zs + (uint32_t)pl * zchunk, t + (size_t)pl * a.Bp * a.zsw, zchunk);
                 } else {
-                    tma_load_2d(Zs, &tm_z, (int)(k * G), mt * 128, fb);
+                    tile(Zs, &tm_z, (int)(k * G), mt * 128);
                     if (a.npass > 1)
-                        tma_load_2d(Zs + zchunk, &tm_zl, (int)(k * G), mt * 128, fb);
+                        tile(Zs + zchunk, &tm_zl, (int)(k * G), mt * 128);
                 }
                 for (int kc = 0; kc < a.nk; ++kc)
-                    tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
-                bulk_load(Is, a.idx_s + k * F, (uint32_t)F * 2, fb);
+                    tile(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G));
+                bulk(Is, a.idx_s + k * F, (uint32_t)F * 2);
             }
             __syncwarp();
         }
@@ -1309,6 +1393,9 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // no CTA leaves while another may still multicast into it or arrive on it
+    if (C > 1)
+        cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, a.tmem_cols);
@@ -1587,25 +1674,53 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.npass = split ? 2 : 1;
     a.Bp = p.MT * 128;
     a.vec4 = (lo->H % 4 == 0 && ((uintptr_t)dh & 15) == 0) ? 1 : 0;
-    int parts = lo->num_sms / (p.nbands * p.MT);
+    const size_t smem = 2 * (size_t)p.ws_bytes + (size_t)p.S * p.stage_bytes + 1024;
+    rc = set_smem(k_tc_dh, smem);
+    if (rc != SG_OK)
+        return rc;
+    // one cluster per (mtile, part) holding its bands when the loads are
+    // multicast; as many parts as clusters fit on the GPU at once
+    a.csize = kDhMulticast ? p.nbands : 1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kDhThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = lo->num_sms / p.nbands;
+    if (a.csize > 1) {
+        cfg.gridDim = dim3((unsigned)(p.nbands * p.MT * clusters), 1, 1);
+        int n = 0;
+        SG_TRY_CUDA(cudaOccupancyMaxActiveClusters(&n, k_tc_dh, &cfg));
+        if (n < 1) {
+            sg_set_error("tc_dh: no cluster of %d CTAs fits on the device", p.nbands);
+            return SG_ERR_UNSUPPORTED;
+        }
+        clusters = n;
+    }
+    int parts = clusters / p.MT;
     if (parts < 1)
         parts = 1;
     if (parts > lo->K)
         parts = (int)lo->K;
     a.parts = parts;
+    cfg.gridDim = dim3((unsigned)(p.nbands * p.MT * parts), 1, 1);
     a.z_bytes = p.z_bytes;
     a.w_bytes = p.w_bytes;
     a.i_bytes = p.i_bytes;
     a.stage_bytes = p.stage_bytes;
     a.ws_bytes = p.ws_bytes;
     a.tmem_cols = p.tmem_cols;
-    const size_t smem = 2 * (size_t)p.ws_bytes + (size_t)p.S * p.stage_bytes + 1024;
-    rc = set_smem(k_tc_dh, smem);
-    if (rc != SG_OK)
-        return rc;
     SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
-    SG_LAUNCH(lo, SG_KIND_DH, st,
-              k_tc_dh<<<p.nbands * p.MT * parts, kDhThreads, smem, st>>>(tm_z, tm_zl, tm_w, a));
+    cudaError_t le = cudaSuccess;
+    SG_LAUNCH(lo, SG_KIND_DH, st, le = cudaLaunchKernelEx(&cfg, k_tc_dh, tm_z, tm_zl, tm_w, a));
+    SG_TRY_CUDA(le);
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }
