@@ -43,12 +43,13 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 220 * 1024;  // dynamic shared memory we plan with
 constexpr int kEpiWarps = 8;   // two per TMEM lane quarter
-constexpr int kProdWarps = 4;  // cp.async gather + TMA issue
+constexpr int kProdWarps = 8;  // cp.async gather + TMA issue (8: measured ~2x the copy rate of 4)
 // forward / dW: producers, two MMA-issuing warps, epilogue
 constexpr int kFwdThreads = 32 * (kProdWarps + 2 + kEpiWarps);
 constexpr int kFirstEpi = kProdWarps + 2;
 // dh: one load warp, one MMA warp, eight builder warps
 constexpr int kDhThreads = 32 * (2 + kEpiWarps);
+constexpr int kDhWs = 3;  // scattered-W buffers (builders run up to 2 groups ahead)
 
 // ------------------------------------------------------------------ plans
 struct FwdPlan {
@@ -165,17 +166,22 @@ DhPlan plan_dh(const sg_layout *lo, int B, bool split)
     p.w_bytes = (uint32_t)p.nk * lo->G * 128;
     p.i_bytes = (uint32_t)((lo->F * 2 + 1023) / 1024 * 1024);
     p.stage_bytes = p.z_bytes + p.w_bytes + p.i_bytes;
-    // bands of at most 256 dh columns (one MMA of N <= 256 per K step), in
-    // whole 64-column chunks of the scattered W_k
-    p.nbands = (lo->H + 255) / 256;
-    p.band_w = ((lo->H + p.nbands - 1) / p.nbands + 63) / 64 * 64;
-    p.ws_bytes = (uint32_t)(p.band_w / 64) * lo->G * 128;
-    p.tmem_cols = pow2_cols(p.band_w);
-    const long room = (long)kSmemBudget - 2l * p.ws_bytes;
-    p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
+    // bands of at most 512 dh columns (the accumulator fills at most all of
+    // TMEM; MMAs of N <= 256 per K step), in whole 64-column chunks of the
+    // scattered W_k.  Each band re-reads a group's tiles, so fewer, wider
+    // bands cost fewer loads for the same tensor work.
+    for (p.nbands = (lo->H + 511) / 512; p.nbands * 64 < lo->H + 64; ++p.nbands) {
+        p.band_w = ((lo->H + p.nbands - 1) / p.nbands + 63) / 64 * 64;
+        p.ws_bytes = (uint32_t)(p.band_w / 64) * lo->G * 128;
+        const long room = (long)kSmemBudget - (long)kDhWs * p.ws_bytes;
+        p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
+        if (p.S >= 3)
+            break;
+    }
     if (p.S > 6)
         p.S = 6;
-    p.ok = p.S >= 2;
+    p.tmem_cols = pow2_cols(p.band_w);
+    p.ok = p.S >= 3 && p.band_w <= 512;
     return p;
 }
 
@@ -338,6 +344,26 @@ __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, float (&v)[CH])
     }
 }
 
+// two chunks (e.g. the hi and lo halves of an accumulator) with one wait
+template <int CH>
+__device__ __forceinline__ void tmem_ld_chunk2(uint32_t ta, uint32_t tb, float (&v)[CH], float (&w)[CH])
+{
+    uint32_t r[CH], u[CH];
+    if constexpr (CH == 32) {
+        tmem_ld32(ta, r);
+        tmem_ld32(tb, u);
+    } else {
+        tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tmem_ld16(tb, *reinterpret_cast<uint32_t(*)[16]>(u));
+    }
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        v[i] = __uint_as_float(r[i]);
+        w[i] = __uint_as_float(u[i]);
+    }
+}
+
 // positives of sample b among columns c0 .. c0+n-1 of a group whose entries
 // are gent[e0 .. e1)
 __device__ __forceinline__ uint32_t group_pos_mask(const int32_t *__restrict__ gent, int e0,
@@ -421,10 +447,10 @@ __device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst, int fi
 }
 
 // ------------------------------------------------------------------ gather
-// H_k = rows I_k[f] of hT, copied with 16-byte cp.async by the four producer
+// H_k = rows I_k[f] of hT, copied with 16-byte cp.async by the producer
 // warps into the 128-byte-swizzled layout [b-chunk of 64][f][64 b]: unit u
 // (16 B) of row f lands at chunk(u/8) * F*128 + f*128 + ((u%8) ^ (f%8))*16.
-// Producer warp pw copies rows f in [pw*RW, pw*RW + RW), RW = F/4.  The lanes
+// Producer warp pw copies rows f in [pw*RW, pw*RW + RW), RW = F/kProdWarps.  The lanes
 // of one cp.async instruction cover whole rows (16 lanes per 256-byte row when
 // B <= 128, all 32 when B <= 256), so every 32-byte sector fetched from L2 is
 // used in full.  A lane holds the hT row index of rows pw*RW + lane (+ 32),
@@ -465,9 +491,11 @@ __device__ __forceinline__ void issue_gather(const uint16_t *hT, int ldB, uint32
 
 // Producer loop shared by the forward and the weight gradient: per group, one
 // thread arms the stage barrier with the TMA bytes (`tma_bytes`, issued by
-// `issue_tma`), every producer thread copies its share of H_k, and a copy
-// group is signalled complete two groups later (wait_group, proxy fence,
-// arrive) so each thread keeps three groups of copies in flight.
+// `issue_tma`), every producer thread copies its share of H_k and has the
+// copy hardware arrive on the stage barrier once its copies land, so the
+// producers run ahead as far as free stages allow.  The cp.async writes are
+// generic-proxy writes: every MMA warp fences (proxy.async) after it has seen
+// the stage barrier and before its MMAs read the stage.
 template <typename IssueTma>
 __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t stage_bytes, int S,
                                               int64_t K, const uint16_t *idx_s, const uint16_t *hT,
@@ -475,7 +503,6 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
                                               volatile int *abort_flag, int32_t *status,
                                               IssueTma issue_tma)
 {
-    constexpr int kLag = 2;
     const int t = threadIdx.x;  // producer threads are 0 .. kProdWarps*32-1
     const int lane = t & 31;
     const int units = MT * 16;
@@ -497,18 +524,10 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
             issue_tma(k, A, bar_addr(c.full[s]));
         }
         issue_gather(hT, ldB, A, F, units, cur, lane);
-        cp_async_commit();
-        if (it >= kLag) {
-            cp_async_wait<kLag>();
-            fence_proxy_async();
-            mbar_arrive(bar_addr(c.full[(it - kLag) % S]));
-        }
+        cp_async_arrive_noinc(bar_addr(c.full[s]));
         cur = nxt;
     }
-    cp_async_wait<0>();
-    fence_proxy_async();
-    for (int j = it - kLag < 0 ? 0 : it - kLag; j < it; ++j)
-        mbar_arrive(bar_addr(c.full[j % S]));
+    cp_async_wait_all();
     if (*abort_flag) {
         // wait (bounded) for the TMA bytes of the stages still in flight
         for (int j = it - S < 0 ? 0 : it - S; j < it; ++j)
@@ -613,6 +632,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
                 break;
             tc_fence_after();
+            fence_proxy_async();  // cp.async-written H_k -> the MMA (async proxy)
             if (lane == 0) {
                 const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
                 const uint32_t Wt = A + a.a_bytes;
@@ -780,6 +800,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
                 break;
             tc_fence_after();
+            fence_proxy_async();  // cp.async-written H_k -> the MMA (async proxy)
             if (lane == 0) {
                 const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
                 const uint32_t Zs = A + a.a_bytes;
@@ -853,22 +874,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // turns it into dZ_k (BCE), writes dZ_k to the group-tiled workspace (for dh)
 // and into shared memory, and a second MMA warp computes dW_k^T = H_k^T dZ_k
 // from the same shared-memory H_k, so H_k is gathered once and dZ_k is never
-// read back for dW.  Warps: 4 producers, 2 forward MMA warps, 2 dW MMA warps
-// (each pair alternates groups), 8 epilogue warps.
-constexpr int kFWThreads = 32 * (kProdWarps + 4 + kEpiWarps);
-constexpr int kFWFirstEpi = kProdWarps + 4;
+// read back for dW.  Warps: the producers, one forward MMA warp, one dW MMA
+// warp, eight BCE warps and four dW store warps.
+constexpr int kFWBce = 8;  // BCE warps: two per TMEM lane quarter
+constexpr int kFWDw = 4;   // dW store warps: one per lane quarter
+constexpr int kFWThreads = 32 * (kProdWarps + 2 + kFWBce + kFWDw);
+constexpr int kFWFirstEpi = kProdWarps + 2;
 
 struct FWPlan {
     bool ok = false;
     int MT = 0, FT = 0, nk = 0, S = 0, zsw = 0, nzc = 0, nslot = 0;
-    uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, dz_bytes = 0, zcols = 0, wcols = 0,
+    uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, dz_bytes = 0, stg_bytes = 0, zcols = 0, wcols = 0,
              tmem_cols = 0;
 };
 
 FWPlan plan_fwdw(const sg_layout *lo, int B)
 {
     FWPlan p;
-    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->F % 128 != 0 || 2 * lo->G > 256 || B < 1 || B > 256)
+    if (!shape_ok(lo) || !dz_ok(lo->G) || (lo->F != 128 && lo->F != 256) || 2 * lo->G > 256 || B < 1 ||
+        B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
@@ -881,17 +905,18 @@ FWPlan plan_fwdw(const sg_layout *lo, int B)
     p.w_bytes = (uint32_t)p.nk * lo->G * 128;
     p.stage_bytes = p.a_bytes + p.w_bytes;
     p.dz_bytes = 2u * (uint32_t)p.nzc * p.MT * 128 * p.zsw;  // both planes, all rows
+    p.stg_bytes = (uint32_t)lo->G * lo->F * 2;                 // dW_k staged for its store
     p.zcols = (uint32_t)p.MT * lo->G;
     p.wcols = (uint32_t)p.FT * 2 * lo->G;
     p.nslot = 4 * (p.zcols + p.wcols) <= 512 ? 4 : 2;
     if (p.nslot * (p.zcols + p.wcols) > 512)
         return p;
     p.tmem_cols = pow2_cols(p.nslot * (p.zcols + p.wcols));
-    const long room = (long)kSmemBudget - 2l * p.dz_bytes;
+    const long room = (long)kSmemBudget - 2l * p.dz_bytes - 2l * p.stg_bytes;
     p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
     if (p.S > 6)
         p.S = 6;
-    p.ok = p.S >= 3;
+    p.ok = p.S >= 2;
     return p;
 }
 
@@ -905,7 +930,7 @@ struct FWArgs {
     int32_t *status;
     int64_t K, L;
     int32_t B, G, F, MT, FT, nk, S, zsw, nzc, nslot, Bp, ldB;
-    uint32_t a_bytes, w_bytes, stage_bytes, dz_bytes, zcols, wcols, tmem_cols;
+    uint32_t a_bytes, w_bytes, stage_bytes, dz_bytes, stg_bytes, zcols, wcols, tmem_cols;
 };
 
 // the common control block (stages; tfull/tempty = Z accumulators; drain of
@@ -917,7 +942,10 @@ struct CtlFW {
     uint64_t wdrain[2];              // drain of the dW MMA warps
 };
 
-template <int CH>
+// The MMA issue loops have compile-time trip counts (FK = F/16 K steps, MT
+// sample tiles): tcgen05.mma issued from a loop with a run-time trip count
+// measured about 2x slower per instruction than the same MMAs unrolled.
+template <int CH, int FK, int MT>
 __global__ void __launch_bounds__(kFWThreads, 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
 {
@@ -927,22 +955,28 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
-    // [dZ_k buffer 0][dZ_k buffer 1][stages]
-    const uint32_t stage0 = base + 2 * a.dz_bytes;
+    // [dZ_k buffer 0][dZ_k buffer 1][dW_k staging 0][dW_k staging 1][stages]
+    const uint32_t stg0 = base + 2 * a.dz_bytes;
+    const uint32_t stage0 = stg0 + 2 * a.stg_bytes;
     const int G = a.G, F = a.F, S = a.S, NS = a.nslot;
     const uint32_t zrows = (uint32_t)a.MT * 128;
     const uint32_t zchunk = zrows * (uint32_t)a.zsw;
     const uint32_t wbase = (uint32_t)NS * a.zcols;  // first dW accumulator column
 
+    // the epilogue is two teams: the BCE warps turn Z_k into dZ_k, the dW
+    // warps store dW of the group
     if (threadIdx.x == 0) {
-        setup_ctl(c, S, NS, kProdWarps * 32 + 1, 1);
+        setup_ctl(c, S, 0, kProdWarps * 32 + 1, 1);
         for (int i = 0; i < NS && i < 4; ++i) {
+            mbar_init(bar_addr(c.tfull[i]), 1);
+            mbar_init(bar_addr(c.tempty[i]), kFWBce * 32);
             mbar_init(bar_addr(cf.wfull[i]), 1);
-            mbar_init(bar_addr(cf.wempty[i]), kEpiWarps * 32);
+            mbar_init(bar_addr(cf.wempty[i]), kFWDw * 32);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(cf.dzfull[i]), kEpiWarps * 32);
-            mbar_init(bar_addr(cf.dzempty[i]), 1);
+            mbar_init(bar_addr(cf.dzfull[i]), kFWBce * 32);
+            // freed by the dW MMA (commit) and by the end of the tile's store read
+            mbar_init(bar_addr(cf.dzempty[i]), 2);
             mbar_init(bar_addr(cf.wdrain[i]), 1);
         }
         fence_mbar_init();
@@ -965,14 +999,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                           for (int kc = 0; kc < a.nk; ++kc)
                               tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
                       });
-    } else if (warp < kProdWarps + 2) {
+    } else if (warp == kProdWarps) {
         // ---------------------------------------------------------- forward MMA
-        const int me = warp - kProdWarps;
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            if ((it & 1) != me)
-                continue;
             const int s = it % S;
             const int zs = it % NS;
             if (!mbar_wait(bar_addr(c.tempty[zs]), ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, a.status))
@@ -981,14 +1012,17 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
+            fence_proxy_async();  // cp.async-written H_k -> the MMA (async proxy)
             if (lane == 0) {
                 const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
                 const uint32_t Wt = A + a.a_bytes;
-                for (int t = 0; t < a.MT; ++t) {
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
                     const uint32_t d = tbase + (uint32_t)(zs * a.zcols + t * G);
-                    for (int st = 0; st < F / 16; ++st) {
-                        const uint64_t ad = sdesc(A + (uint32_t)t * 2 * F * 128 + (uint32_t)st * 2048,
-                                                  (uint32_t)F * 128, 1024, kLayoutSW128);
+#pragma unroll
+                    for (int st = 0; st < FK; ++st) {
+                        const uint64_t ad = sdesc(A + (uint32_t)t * 2 * FK * 2048 + (uint32_t)st * 2048,
+                                                  (uint32_t)FK * 2048, 1024, kLayoutSW128);
                         const uint64_t bd = sdesc(Wt + (uint32_t)(st / 4) * G * 128 + (uint32_t)(st % 4) * 32,
                                                   16, 1024, kLayoutSW128);
                         mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
@@ -999,18 +1033,15 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             __syncwarp();
         }
         if (lane == 0)
-            mma_commit(bar_addr(c.drain[me]));
+            mma_commit(bar_addr(c.drain[0]));
         __syncwarp();
-        mbar_wait_drain(bar_addr(c.drain[me]), 0);
+        mbar_wait_drain(bar_addr(c.drain[0]), 0);
     } else if (warp < kFWFirstEpi) {
         // ---------------------------------------------------------- dW MMA
-        const int me = warp - kProdWarps - 2;
         const uint32_t zlayout = layout_for_swizzle(a.zsw);
         const uint32_t idesc = idesc_bf16(128, 2 * G, 0, 1);  // N = [hi | lo] along j
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            if ((it & 1) != me)
-                continue;
             const int s = it % S;
             const int ws = it % NS;
             const int db = it & 1;
@@ -1019,14 +1050,30 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             tc_fence_after();
             if (!mbar_wait(bar_addr(cf.dzfull[db]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
                 break;
+            // H_k of this stage landed long ago (the forward MMA used it); this
+            // warp sees the barrier itself before its MMAs read the cp.async data
+            if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
+                break;
             tc_fence_after();
+            fence_proxy_async();
             if (lane == 0) {
                 const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
                 const uint32_t Zs = base + (uint32_t)db * a.dz_bytes;
-                for (int tf = 0; tf < a.FT; ++tf) {
+                // dZ_k goes to the workspace with one bulk store of the shared
+                // tile; the previous group's store has read its buffer once
+                // this returns, which frees that buffer (with its MMA commit)
+                if (it > 0) {
+                    bulk_wait_read<0>();
+                    mbar_arrive(bar_addr(cf.dzempty[db ^ 1]));
+                }
+                bulk_store(a.dZt + (size_t)k * a.tile_bytes, Zs, a.dz_bytes);
+                bulk_commit();
+#pragma unroll
+                for (int tf = 0; tf < FK / 8; ++tf) {
                     const uint32_t d = tbase + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G);
-                    for (int st = 0; st < a.MT * 8; ++st) {
-                        const uint64_t ad = sdesc(A + (uint32_t)(st / 4) * F * 128 + (uint32_t)tf * 128 * 128 +
+#pragma unroll
+                    for (int st = 0; st < MT * 8; ++st) {
+                        const uint64_t ad = sdesc(A + (uint32_t)(st / 4) * FK * 2048 + (uint32_t)tf * 128 * 128 +
                                                       (uint32_t)(st % 4) * 32,
                                                   16, 1024, kLayoutSW128);
                         const uint64_t bd = sdesc(Zs + (uint32_t)st * 16 * a.zsw, zchunk, 8 * a.zsw, zlayout);
@@ -1039,98 +1086,104 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             }
             __syncwarp();
         }
-        if (lane == 0)
-            mma_commit(bar_addr(cf.wdrain[me]));
+        if (lane == 0) {
+            mma_commit(bar_addr(cf.wdrain[0]));
+            bulk_wait<0>();  // every dZ tile store has landed
+        }
         __syncwarp();
-        mbar_wait_drain(bar_addr(cf.wdrain[me]), 0);
+        mbar_wait_drain(bar_addr(cf.wdrain[0]), 0);
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
-        const int sub = (warp - kFWFirstEpi) / 4;
+        const int ew = warp - kFWFirstEpi;  // BCE warps 0 .. kFWBce-1, then the dW warps
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        const int zunits = a.MT * (G / CH);
-        const int wunits = a.FT * (G / CH);
-        double lacc = 0.0;
-        bool ok = true;
-        // dW of the group `it` (written one group late, so its MMA has the
-        // BCE of the next group to complete in)
-        auto store_dW = [&](int64_t k, int it) -> bool {
-            const int ws = it % NS;
-            if (!mbar_wait(bar_addr(cf.wfull[ws]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
-                return false;
-            tc_fence_after();
-            for (int u = sub; u < wunits; u += 2) {
-                const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
-                const int f = tf * 128 + q * 32 + lane;
-                const uint32_t col = tbase + lane_off + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G + c0);
-                float v[CH], w[CH];
-                tmem_ld_chunk<CH>(col, v);
-                tmem_ld_chunk<CH>(col + (uint32_t)G, w);
-                uint16_t *dst = a.dW + (k * G + c0) * F + f;
+        if (ew < kFWBce) {
+            double lacc = 0.0;
+            const int sub = ew / 4;  // two warps per lane quarter split the column units
+            // Z_k -> BCE -> dZ_k (workspace tile and shared memory for the dW MMA)
+            const int zunits = a.MT * (G / CH);
+            // positive-list bounds of the group, loaded one group ahead
+            int e0n = 0, e1n = 0;
+            if (blockIdx.x < a.K) {
+                e0n = __ldg(a.gptr + blockIdx.x);
+                e1n = __ldg(a.gptr + blockIdx.x + 1);
+            }
+            int it = 0;
+            for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+                const int zs = it % NS;
+                const int db = it & 1;
+                const int e0 = e0n, e1 = e1n;
+                if (k + gridDim.x < a.K) {
+                    e0n = __ldg(a.gptr + k + gridDim.x);
+                    e1n = __ldg(a.gptr + k + gridDim.x + 1);
+                }
+                if (!mbar_wait(bar_addr(c.tfull[zs]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
+                    break;
+                // the dZ buffer of two groups ago must have been consumed by its dW MMA
+                if (!mbar_wait(bar_addr(cf.dzempty[db]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
+                    break;
+                tc_fence_after();
+                uint8_t *zs_smem = base_ptr + (size_t)db * a.dz_bytes;
+                for (int u = sub; u < zunits; u += 2) {
+                    const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
+                    const int b = t * 128 + q * 32 + lane;
+                    float v[CH];
+                    tmem_ld_chunk<CH>(tbase + lane_off + (uint32_t)(zs * a.zcols + t * G + c0), v);
+                    if (b < a.B) {
+                        const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
+                        lacc += bce_chunk<CH>(v, y);
+                    } else {
 #pragma unroll
-                for (int i = 0; i < CH; ++i)
-                    dst[(int64_t)i * F] = bf16_rn(v[i] + w[i]);
+                        for (int i = 0; i < CH; ++i)
+                            v[i] = 0.f;
+                    }
+                    store_dz_tile<CH>(zs_smem, b, c0, v, a.zsw, a.nzc, a.Bp);
+                }
+                tc_fence_before();
+                mbar_arrive(bar_addr(c.tempty[zs]));
+                fence_proxy_async();  // dZ_k in shared memory -> the dW MMA (async proxy)
+                mbar_arrive(bar_addr(cf.dzfull[db]));
             }
-            tc_fence_before();
-            mbar_arrive(bar_addr(cf.wempty[ws]));
-            return true;
-        };
-        int it = 0;
-        int64_t kprev = -1;
-        // positive-list bounds of the group, loaded one group ahead
-        int e0n = 0, e1n = 0;
-        if (blockIdx.x < a.K) {
-            e0n = __ldg(a.gptr + blockIdx.x);
-            e1n = __ldg(a.gptr + blockIdx.x + 1);
-        }
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            const int zs = it % NS;
-            const int db = it & 1;
-            const int e0 = e0n, e1 = e1n;
-            if (k + gridDim.x < a.K) {
-                e0n = __ldg(a.gptr + k + gridDim.x);
-                e1n = __ldg(a.gptr + k + gridDim.x + 1);
-            }
-            if (!mbar_wait(bar_addr(c.tfull[zs]), (uint32_t)(it / NS) & 1u, abort_flag, a.status)) {
-                ok = false;
-                break;
-            }
-            // the dZ buffer of two groups ago must have been consumed by its dW MMA
-            if (!mbar_wait(bar_addr(cf.dzempty[db]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint8_t *tile = a.dZt + (size_t)k * a.tile_bytes;
-            uint8_t *zs_smem = base_ptr + (size_t)db * a.dz_bytes;
-            for (int u = sub; u < zunits; u += 2) {
-                const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
-                const int b = t * 128 + q * 32 + lane;
-                float v[CH];
-                tmem_ld_chunk<CH>(tbase + lane_off + (uint32_t)(zs * a.zcols + t * G + c0), v);
-                if (b < a.B) {
-                    const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
-                    lacc += bce_chunk<CH>(v, y);
-                } else {
+            epi_sum_to(lacc, c, a.loss_part + blockIdx.x, kFWFirstEpi);
+        } else {
+            // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
+            // staged in shared memory as [j][f] and stored with one bulk copy
+            const int dw = ew - kFWBce;  // 0 .. kFWDw-1
+            const int wunits = a.FT * (G / CH);
+            int it = 0;
+            for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+                const int ws = it % NS;
+                const int wb = it & 1;
+                uint16_t *stg = reinterpret_cast<uint16_t *>(base_ptr + 2 * (size_t)a.dz_bytes + (size_t)wb * a.stg_bytes);
+                if (!mbar_wait(bar_addr(cf.wfull[ws]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
+                    break;
+                tc_fence_after();
+                // the staging buffer's store of two groups ago has read it
+                if (dw == 0 && lane == 0)
+                    bulk_wait_read<1>();
+                named_bar(2, kFWDw * 32);
+                for (int u = 0; u < wunits; ++u) {
+                    const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
+                    const int f = tf * 128 + q * 32 + lane;
+                    const uint32_t col = tbase + lane_off + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G + c0);
+                    float v[CH], w[CH];
+                    tmem_ld_chunk2<CH>(col, col + (uint32_t)G, v, w);
 #pragma unroll
                     for (int i = 0; i < CH; ++i)
-                        v[i] = 0.f;
+                        stg[(c0 + i) * F + f] = bf16_rn(v[i] + w[i]);
                 }
-                store_dz_tile<CH>(tile, b, c0, v, a.zsw, a.nzc, a.Bp, zs_smem);
+                tc_fence_before();
+                mbar_arrive(bar_addr(cf.wempty[ws]));
+                fence_proxy_async();  // staged dW_k -> the bulk store (async proxy)
+                named_bar(2, kFWDw * 32);
+                if (dw == 0 && lane == 0) {
+                    bulk_store(a.dW + k * G * F, stg0 + (uint32_t)wb * a.stg_bytes, a.stg_bytes);
+                    bulk_commit();
+                }
             }
-            tc_fence_before();
-            mbar_arrive(bar_addr(c.tempty[zs]));
-            fence_proxy_async();  // dZ_k in shared memory -> the dW MMA (async proxy)
-            mbar_arrive(bar_addr(cf.dzfull[db]));
-            if (kprev >= 0 && !store_dW(kprev, it - 1)) {
-                ok = false;
-                break;
-            }
-            kprev = k;
+            if (dw == 0 && lane == 0)
+                bulk_wait<0>();  // every dW store has landed
         }
-        if (ok && kprev >= 0)
-            store_dW(kprev, it - 1);
-        epi_sum_to(lacc, c, a.loss_part + blockIdx.x, kFWFirstEpi);
     }
     tc_fence_before();
     __syncthreads();
@@ -1143,6 +1196,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
 // ================================================================== dh
 struct DhArgs {
     const uint16_t *idx_s;
+    const uint16_t *W;     // [L][F] in slot order
     const uint8_t *dZt;    // group-tiled dZ input (else the tensor maps)
     uint64_t tile_bytes;
     float *dh;
@@ -1174,9 +1228,13 @@ constexpr bool kDhMulticast = false;
 // one MMA warp accumulates dZ_k Ws_k over all the CTA's groups into one TMEM
 // accumulator of 128 samples x band_w columns, so the partial of dh never
 // leaves TMEM until it is added into dh at the end.
+//
+// Compile-time shape: NPASS dZ planes, NKS = G/16 K steps per plane, NP
+// pieces of at most 256 columns per band (fully unrolled MMA issue).
+template <int NPASS, int NKS, int NP>
 __global__ void __launch_bounds__(kDhThreads, 1)
     k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
-            const __grid_constant__ CUtensorMap tm_w, const DhArgs a)
+            const DhArgs a)
 {
     __shared__ Ctl c;
     __shared__ uint64_t cempty[kMaxStages];
@@ -1185,9 +1243,9 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
     const int C = a.csize;
-    // [Ws buffer 0][Ws buffer 1][stages]
-    const uint32_t stage0 = base + 2 * a.ws_bytes;
-    uint8_t *stage0_ptr = base_ptr + 2 * (size_t)a.ws_bytes;
+    // [Ws buffers 0 .. kDhWs-1][stages]
+    const uint32_t stage0 = base + kDhWs * a.ws_bytes;
+    uint8_t *stage0_ptr = base_ptr + kDhWs * (size_t)a.ws_bytes;
     const int G = a.G, F = a.F, S = a.S;
     const int band = blockIdx.x % a.nbands;
     const int mt = (blockIdx.x / a.nbands) % a.MT;
@@ -1196,10 +1254,10 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     const uint32_t zchunk = 128u * (uint32_t)a.zsw;  // one plane of the stage (G <= 64)
 
     // stages: full = loads landed; empty = the MMAs that read them are done.
-    // tfull/tempty[0..1] = Ws buffer written / consumed; drain[0] = last MMA.
+    // tfull/tempty[nb] = Ws buffer nb written / consumed; drain[0] = last MMA.
     if (threadIdx.x == 0) {
         setup_ctl(c, S, 0, 1, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kDhWs; ++i) {
             mbar_init(bar_addr(c.tfull[i]), kEpiWarps * 32);
             mbar_init(bar_addr(c.tempty[i]), 1);
         }
@@ -1273,8 +1331,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                     if (a.npass > 1)
                         tile(Zs + zchunk, &tm_zl, (int)(k * G), mt * 128);
                 }
-                for (int kc = 0; kc < a.nk; ++kc)
-                    tile(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G));
+                // W_k: G contiguous rows of F, read row-major by the builders
+                bulk(Wt, a.W + k * G * F, a.w_bytes);
                 bulk(Is, a.idx_s + k * F, (uint32_t)F * 2);
             }
             __syncwarp();
@@ -1283,14 +1341,13 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         const uint32_t zlayout = layout_for_swizzle(a.zsw);
-        const int nks = G / 16;
         int it = 0;
         for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
-            const int nb = it & 1;
+            const int nb = it % kDhWs;
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
-            if (!mbar_wait(bar_addr(c.tfull[nb]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.tfull[nb]), (uint32_t)(it / kDhWs) & 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
             if (lane == 0) {
@@ -1298,11 +1355,14 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 const uint32_t Ws = base + (uint32_t)nb * a.ws_bytes;
                 // K runs over j for dZ hi (and again for dZ lo) against Ws_k;
                 // N over the band in pieces of at most 256 columns
-                for (int ks2 = 0; ks2 < a.npass * nks; ++ks2) {
-                    const int ks = ks2 % nks;
-                    const uint32_t za = Zs + (uint32_t)(ks2 / nks) * zchunk + (uint32_t)ks * 32;
+#pragma unroll
+                for (int ks2 = 0; ks2 < NPASS * NKS; ++ks2) {
+                    const int ks = ks2 % NKS;
+                    const uint32_t za = Zs + (uint32_t)(ks2 / NKS) * zchunk + (uint32_t)ks * 32;
                     const uint64_t ad = sdesc(za, 16, 8 * a.zsw, zlayout);
-                    for (int n0 = 0; n0 < a.band_w; n0 += 256) {
+#pragma unroll
+                    for (int pc = 0; pc < NP; ++pc) {
+                        const int n0 = pc * 256;
                         const int nn = a.band_w - n0 < 256 ? a.band_w - n0 : 256;
                         const uint64_t bd = sdesc(Ws + (uint32_t)(n0 / 64) * G * 128 + (uint32_t)ks * 2048,
                                                   (uint32_t)G * 128, 1024, kLayoutSW128);
@@ -1321,22 +1381,30 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         mbar_wait_drain(bar_addr(c.drain[0]), 0);  // no MMA in flight at the dealloc
     } else {
         // ---------------------------------------------------------- builders
+        // Warp ew owns rows j = ew, ew + 8, ... of every Ws buffer: it clears
+        // them and writes them, so the warps never touch each other's rows and
+        // need no barrier between them.
         const int ew = warp - kDhFirstEpi;  // 0 .. 7
-        const int t = ew * 32 + lane;
+        const int nrows = (G - ew + kEpiWarps - 1) / kEpiWarps;
+        const uint32_t chunk_bytes = (uint32_t)G * 128;  // one 64-column chunk of Ws
+        const int nchunks = a.band_w / 64;
+        // every buffer starts zero
+        for (int nb = 0; nb < kDhWs; ++nb)
+            for (int r = 0; r < nrows; ++r)
+                for (int cch = lane / 8; cch < nchunks; cch += 4)
+                    *reinterpret_cast<uint4 *>(base_ptr + (size_t)nb * a.ws_bytes + cch * chunk_bytes +
+                                               (uint32_t)(ew + r * kEpiWarps) * 128 + (lane & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+        __syncwarp();
         int it = 0;
         for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
-            const int nb = it & 1;
+            const int nb = it % kDhWs;
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
-                break;
-            if (!mbar_wait(bar_addr(c.tempty[nb]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
                 break;
             uint8_t *Ws = base_ptr + (size_t)nb * a.ws_bytes;
             const uint8_t *Wt = stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes;
             const uint16_t *I = reinterpret_cast<const uint16_t *>(Wt + a.w_bytes);
-            // clear the buffer (its last use held another group's columns)
-            for (uint32_t o = (uint32_t)t * 16; o < a.ws_bytes; o += kEpiWarps * 32 * 16)
-                *reinterpret_cast<uint4 *>(Ws + o) = make_uint4(0, 0, 0, 0);
             // f range of the band: I_k ascending, so count entries below each end
             int na = 0, ne = 0;
             for (int f = lane; f < F; f += 32) {
@@ -1346,18 +1414,32 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             }
             const int fa = __reduce_add_sync(0xffffffffu, na);
             const int fe = __reduce_add_sync(0xffffffffu, ne);
-            named_bar(1, kEpiWarps * 32);  // every clear lands before any write
-            // warp ew writes rows j = ew, ew + 8, ...; lanes run along f
+            // the buffer's last group must be through its MMA before it is reused
+            if (!mbar_wait(bar_addr(c.tempty[nb]), ((uint32_t)(it / kDhWs) & 1u) ^ 1u, abort_flag, a.status))
+                break;
+            for (int r = 0; r < nrows; ++r)
+                for (int cch = lane / 8; cch < nchunks; cch += 4)
+                    *reinterpret_cast<uint4 *>(Ws + cch * chunk_bytes + (uint32_t)(ew + r * kEpiWarps) * 128 +
+                                               (lane & 7) * 16) = make_uint4(0, 0, 0, 0);
+            __syncwarp();
+            // lanes run along f; each lane moves W_k[j][f] to Ws[j][I_k[f] - i0]
+            const uint16_t *Wrow = reinterpret_cast<const uint16_t *>(Wt);  // [G][F], row-major
             for (int f = fa + lane; f < fe; f += 32) {
                 const int i = (int)I[f] - i0;
-                const uint32_t wsrc = (uint32_t)(f >> 6) * G * 128 + (uint32_t)(((f & 63) >> 3) << 4) +
-                                      (uint32_t)(f & 7) * 2;
-                const uint32_t wdst = (uint32_t)(i >> 6) * G * 128 + (uint32_t)(((i & 63) >> 3) << 4) +
+                const uint32_t wdst = (uint32_t)(i >> 6) * chunk_bytes + (uint32_t)(((i & 63) >> 3) << 4) +
                                       (uint32_t)(i & 7) * 2;
-                for (int j = ew; j < G; j += kEpiWarps) {
-                    const uint32_t row = (uint32_t)j * 128, sw = (uint32_t)(j & 7) << 4;
-                    const uint16_t w = *reinterpret_cast<const uint16_t *>(Wt + ((wsrc + row) ^ sw));
-                    *reinterpret_cast<uint16_t *>(Ws + ((wdst + row) ^ sw)) = w;
+                uint16_t w[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int j = ew + r * kEpiWarps;
+                    if (r < nrows)
+                        w[r] = Wrow[j * F + f];
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const uint32_t j = (uint32_t)(ew + r * kEpiWarps);
+                    if (r < nrows)
+                        *reinterpret_cast<uint16_t *>(Ws + ((wdst + j * 128) ^ ((j & 7) << 4))) = w[r];
                 }
             }
             fence_proxy_async();  // Ws_k (generic writes) -> the MMA (async proxy)
@@ -1550,12 +1632,24 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.w_bytes = p.w_bytes;
     a.stage_bytes = p.stage_bytes;
     a.dz_bytes = p.dz_bytes;
+    a.stg_bytes = p.stg_bytes;
     a.zcols = p.zcols;
     a.wcols = p.wcols;
     a.tmem_cols = p.tmem_cols;
-    const size_t smem = 2 * (size_t)p.dz_bytes + (size_t)p.S * p.stage_bytes + 1024;
+    const size_t smem = 2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
-    void (*kern)(CUtensorMap, FWArgs) = lo->G >= 64 ? k_tc_fwdw<32> : k_tc_fwdw<16>;
+    void (*kern)(CUtensorMap, FWArgs) = nullptr;
+    const bool c32 = lo->G >= 64;
+    if (lo->F == 128)
+        kern = p.MT == 1 ? (c32 ? k_tc_fwdw<32, 8, 1> : k_tc_fwdw<16, 8, 1>)
+                         : (c32 ? k_tc_fwdw<32, 8, 2> : k_tc_fwdw<16, 8, 2>);
+    else if (lo->F == 256)
+        kern = p.MT == 1 ? (c32 ? k_tc_fwdw<32, 16, 1> : k_tc_fwdw<16, 16, 1>)
+                         : (c32 ? k_tc_fwdw<32, 16, 2> : k_tc_fwdw<16, 16, 2>);
+    if (!kern) {
+        sg_set_error("tc_fwdw: F = %d has no fused kernel", lo->F);
+        return SG_ERR_UNSUPPORTED;
+    }
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
@@ -1635,7 +1729,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
         sg_set_error("tc_dh: shape not supported by the tensor-core engine");
         return SG_ERR_UNSUPPORTED;
     }
-    CUtensorMap tm_z, tm_zl, tm_w;
+    CUtensorMap tm_z, tm_zl;
     sg_status rc = SG_OK;
     memset(&tm_z, 0, sizeof(tm_z));
     if (!dZt) {
@@ -1650,11 +1744,13 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
         if (rc != SG_OK)
             return rc;
     }
-    rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)lo->G, 128, "W");
-    if (rc != SG_OK)
-        return rc;
+    if (((uintptr_t)W & 15) != 0) {
+        sg_set_error("W: device pointer must be 16-byte aligned");
+        return SG_ERR_INVALID;
+    }
     DhArgs a;
     a.idx_s = lo->idx_s;
+    a.W = W;
     a.dZt = dZt;
     a.tile_bytes = tc_dz_tile_bytes(lo, B);
     a.dh = dh;
@@ -1674,8 +1770,22 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.npass = split ? 2 : 1;
     a.Bp = p.MT * 128;
     a.vec4 = (lo->H % 4 == 0 && ((uintptr_t)dh & 15) == 0) ? 1 : 0;
-    const size_t smem = 2 * (size_t)p.ws_bytes + (size_t)p.S * p.stage_bytes + 1024;
-    rc = set_smem(k_tc_dh, smem);
+    const size_t smem = kDhWs * (size_t)p.ws_bytes + (size_t)p.S * p.stage_bytes + 1024;
+    // kernel instance for (planes, K steps per plane, N pieces)
+    void (*kern)(CUtensorMap, CUtensorMap, DhArgs) = nullptr;
+    const int nks = lo->G / 16, np = (p.band_w + 255) / 256;
+#define SG_DH_PICK(P, K, N)                          \
+    if (a.npass == P && nks == K && np == N)         \
+        kern = k_tc_dh<P, K, N>;
+    SG_DH_PICK(1, 1, 1) SG_DH_PICK(1, 1, 2) SG_DH_PICK(1, 2, 1) SG_DH_PICK(1, 2, 2)
+    SG_DH_PICK(1, 4, 1) SG_DH_PICK(1, 4, 2) SG_DH_PICK(2, 1, 1) SG_DH_PICK(2, 1, 2)
+    SG_DH_PICK(2, 2, 1) SG_DH_PICK(2, 2, 2) SG_DH_PICK(2, 4, 1) SG_DH_PICK(2, 4, 2)
+#undef SG_DH_PICK
+    if (!kern) {
+        sg_set_error("tc_dh: no kernel for G = %d, band %d", lo->G, p.band_w);
+        return SG_ERR_UNSUPPORTED;
+    }
+    rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
     // one cluster per (mtile, part) holding its bands when the loads are
@@ -1697,7 +1807,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     if (a.csize > 1) {
         cfg.gridDim = dim3((unsigned)(p.nbands * p.MT * clusters), 1, 1);
         int n = 0;
-        SG_TRY_CUDA(cudaOccupancyMaxActiveClusters(&n, k_tc_dh, &cfg));
+        SG_TRY_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
         if (n < 1) {
             sg_set_error("tc_dh: no cluster of %d CTAs fits on the device", p.nbands);
             return SG_ERR_UNSUPPORTED;
@@ -1719,7 +1829,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.tmem_cols = p.tmem_cols;
     SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
     cudaError_t le = cudaSuccess;
-    SG_LAUNCH(lo, SG_KIND_DH, st, le = cudaLaunchKernelEx(&cfg, k_tc_dh, tm_z, tm_zl, tm_w, a));
+    SG_LAUNCH(lo, SG_KIND_DH, st, le = cudaLaunchKernelEx(&cfg, kern, tm_z, tm_zl, a));
     SG_TRY_CUDA(le);
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
