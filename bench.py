@@ -52,27 +52,38 @@ def _peaks():
 
 
 # ------------------------------------------------------------------ work model
-def algorithmic(w, B, kind):
-    """(bytes, flops) one launch of `kind` must move / do at minimum.
-    bf16 W, dW, Z, dZ, h; uint16 idx; fp32 dh; positives as int32."""
+# DRAM bytes per group measured by ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum of one launch / its groups) on the 3M shape at
+# L = 524,288; profiles/k_tc_fwdw_k_tc_dh_amazon3m_L524288.md.  Scaled to a
+# launch by the groups it processes; None for other shapes.
+MEASURED_TRAFFIC_PER_GROUP = {
+    ("amazon3m_tail", "fwd"): (138.781440e6 + 341.582592e6) / 16384,
+    ("amazon3m_tail", "dh"): (407.305984e6 + 3.266048e6) / 16384,
+}
+
+
+def algorithmic(w, B, kind, fused_dW=False):
+    """(bytes, flops) one launch of `kind` must move / do at minimum inside the
+    training step.  bf16 W, dW, h; uint16 idx; fp32 dh; positives as int32.
+    dZ is internal to the step (no call outputs it), so it is not counted;
+    `fused_dW`: the forward launch also computes and writes dW."""
     L, K, F, H = w.L, w.K, w.F, w.H
     W_b = L * F * 2
     idx_b = K * F * 2
     h_b = B * H * 2
     dh_b = B * H * 4
-    z_b = B * L * 2
     nnz_b = B * w.pos * 4 * 2
     flops_gemm = 2 * B * L * F
     if kind == "step":
         return W_b + W_b + idx_b + h_b + dh_b + nnz_b, 3 * flops_gemm
-    if kind == "fwd":      # fused BCE: writes dZ
-        return W_b + idx_b + h_b + z_b + nnz_b, flops_gemm
-    if kind == "bce":
-        return z_b + z_b + nnz_b, 0
+    if kind == "fwd":      # forward + fused BCE (+ dW when fused)
+        if fused_dW:
+            return W_b + W_b + idx_b + h_b + nnz_b, 2 * flops_gemm
+        return W_b + idx_b + h_b + nnz_b, flops_gemm
     if kind == "dW":
-        return z_b + h_b + idx_b + W_b, flops_gemm
+        return W_b + idx_b + h_b, flops_gemm
     if kind == "dh":
-        return z_b + W_b + idx_b + dh_b, flops_gemm
+        return W_b + idx_b + dh_b, flops_gemm
     return 0, 0
 
 
@@ -314,11 +325,14 @@ def run_ours(args):
     hbm, tflops, peak_src = _peaks()
     dom = max((k for k in kinds if kinds[k][1] > 0), key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
-    bytes_, flops = algorithmic(w, w.B, dom)
+    fused = kinds.get("dW", (0.0, 0))[1] == 0
+    bytes_, flops = algorithmic(w, w.B, dom, fused_dW=fused)
     per_launch_s = dom_ms * 1e-3 / dom_n
     achieved = bytes_ / per_launch_s / 1e9
+    per_group = MEASURED_TRAFFIC_PER_GROUP.get((w.name.split("_L")[0], dom))
+    traffic = per_group * w.K if per_group is not None and dom_n else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None, "kernel": dom,
+                "frac": achieved / hbm, "traffic": traffic, "kernel": dom,
                 "peak_source": peak_src,
                 "launch_ms": per_launch_s * 1e3,
                 "tensor_tflops": flops / per_launch_s / 1e12 if flops else 0.0,
