@@ -113,7 +113,7 @@ void free_layout(sg_layout *lo)
     timer_release(lo->timer);
     void *bufs[] = {lo->slot_of_label, lo->label_of_slot, lo->idx_s, lo->hT,
                     lo->gcount, lo->gptr, lo->gent, lo->tsorted, lo->tslots,
-                    lo->rowcnt, lo->loss_part, lo->status, lo->dZ_ws};
+                    lo->rowcnt, lo->loss_part, lo->status, lo->dZ_ws, lo->scan_part};
     for (void *p : bufs)
         if (p)
             cudaFree(p);
@@ -249,6 +249,7 @@ sg_status sg_layout_build(const int32_t *groups, int64_t L, int32_t G,
     ALLOC(hT, (size_t)H * lo->ldB);
     ALLOC(gcount, lo->K + 1);
     ALLOC(gptr, lo->K + 1);
+    ALLOC(scan_part, (lo->K + 4095) / 4096 + 1);
     ALLOC(gent, max_nnz);
     ALLOC(tsorted, max_nnz);
     ALLOC(tslots, max_nnz);

@@ -4,7 +4,7 @@
 //
 //   1. k_pos_rows  : one warp per sample: labels -> slots, sort, drop
 //                    duplicates (Y is binary), count positives per group.
-//   2. k_scan      : exclusive scan of the per-group counts -> gptr[K+1].
+//   2. k_scan_*    : exclusive scan of the per-group counts -> gptr[K+1].
 //   3. k_pos_place : bucket the entries by group: gent[] = (b << 16) | j.
 //                    Placement counts the group counters back down to zero,
 //                    so they are ready for the next call without a memset.
@@ -75,51 +75,75 @@ __global__ void k_pos_rows(int32_t B, const int32_t *__restrict__ rowptr,
         rowcnt[b] = kept;
 }
 
-// Single-block exclusive scan: out[i] = sum_{j<i} in[j], out[n] = total.
-__global__ void __launch_bounds__(1024) k_scan(const int32_t *__restrict__ in,
-                                               int64_t n, int32_t *out)
+// Exclusive scan out[i] = sum_{j<i} in[j], out[n] = total, in two passes over
+// tiles of kScanTile entries: k_scan_tiles scans each tile on its own and
+// records the tile's total; k_scan_add adds the totals of the tiles before it.
+constexpr int kScanTile = 4096;  // 1024 threads x 4 entries
+
+__global__ void __launch_bounds__(1024) k_scan_tiles(const int32_t *__restrict__ in, int64_t n,
+                                                     int32_t *out, int32_t *tile_sum)
 {
     __shared__ int32_t warp_sums[32];
-    __shared__ int32_t carry_s;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    if (tid == 0)
-        carry_s = 0;
+    const int64_t base = (int64_t)blockIdx.x * kScanTile + (int64_t)tid * 4;
+    int32_t v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        v[e] = base + e < n ? in[base + e] : 0;
+    const int32_t own = v[0] + v[1] + v[2] + v[3];
+    int32_t x = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        warp_sums[wid] = x;
     __syncthreads();
-    for (int64_t base = 0; base < n; base += 1024) {
-        int64_t i = base + tid;
-        int32_t v = i < n ? in[i] : 0;
-        int32_t x = v;
+    if (wid == 0) {
+        int32_t w = warp_sums[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o)
-                x += y;
+                w += y;
         }
-        if (lane == 31)
-            warp_sums[wid] = x;
-        __syncthreads();
-        if (wid == 0) {
-            int32_t w = warp_sums[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int32_t y = __shfl_up_sync(0xffffffffu, w, o);
-                if (lane >= o)
-                    w += y;
-            }
-            warp_sums[lane] = w;  // inclusive over warps
-        }
-        __syncthreads();
-        int32_t carry = carry_s;
-        int32_t excl = carry + (wid ? warp_sums[wid - 1] : 0) + x - v;
-        if (i < n)
-            out[i] = excl;
-        __syncthreads();
-        if (tid == 1023)
-            carry_s = excl + v;
-        __syncthreads();
+        warp_sums[lane] = w;
     }
-    if (tid == 0)
-        out[n] = carry_s;
+    __syncthreads();
+    int32_t run = (wid ? warp_sums[wid - 1] : 0) + x - own;  // exclusive prefix in the tile
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if (base + e < n)
+            out[base + e] = run;
+        run += v[e];
+    }
+    if (tid == 1023)
+        tile_sum[blockIdx.x] = warp_sums[31];
+}
+
+__global__ void __launch_bounds__(1024) k_scan_add(int64_t n, int32_t *out, const int32_t *tile_sum)
+{
+    __shared__ int32_t off_s;
+    if (threadIdx.x < 32) {
+        int32_t s = 0;
+        for (int t = threadIdx.x; t < (int)blockIdx.x; t += 32)
+            s += tile_sum[t];
+        for (int o = 16; o > 0; o >>= 1)
+            s += __shfl_down_sync(0xffffffffu, s, o);
+        if (threadIdx.x == 0)
+            off_s = s;
+    }
+    __syncthreads();
+    const int32_t off = off_s;
+    const int64_t base = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * 4;
+    if (off)
+        for (int e = 0; e < 4; ++e)
+            if (base + e < n)
+                out[base + e] += off;
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0)
+        out[n] = off + tile_sum[blockIdx.x];
 }
 
 __global__ void k_pos_place(int32_t B, const int32_t *__restrict__ rowptr,
@@ -189,7 +213,10 @@ sg_status sg_pos_prepare(sg_layout *lo, int32_t B, const int32_t *rowptr,
                                                lo->tsorted, lo->tslots,
                                                lo->rowcnt, lo->gcount,
                                                lo->status));
-    SG_LAUNCH(lo, SG_KIND_PREP, st, k_scan<<<1, 1024, 0, st>>>(lo->gcount, lo->K, lo->gptr));
+    const int tiles = (int)((lo->K + kScanTile - 1) / kScanTile);
+    SG_LAUNCH(lo, SG_KIND_PREP, st,
+              k_scan_tiles<<<tiles, 1024, 0, st>>>(lo->gcount, lo->K, lo->gptr, lo->scan_part));
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_scan_add<<<tiles, 1024, 0, st>>>(lo->K, lo->gptr, lo->scan_part));
     SG_LAUNCH(lo, SG_KIND_PREP, st, k_pos_place<<<rows_grid, kThreads, 0, st>>>(B, rowptr, lo->tslots,
                                                 lo->rowcnt, lo->G, lo->gptr,
                                                 lo->gcount, lo->gent));
@@ -201,7 +228,8 @@ sg_status sg_pos_compact(sg_layout *lo, int32_t B, const int32_t *rowptr,
                          int32_t *out_rowptr, int32_t *out_slots,
                          cudaStream_t st)
 {
-    SG_LAUNCH(lo, SG_KIND_PREP, st, k_scan<<<1, 1024, 0, st>>>(lo->rowcnt, B, out_rowptr));
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_scan_tiles<<<1, 1024, 0, st>>>(lo->rowcnt, B, out_rowptr, lo->scan_part));
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_scan_add<<<1, 1024, 0, st>>>(B, out_rowptr, lo->scan_part));
     if (out_slots) {
         const int wpb = kThreads / 32;
         SG_LAUNCH(lo, SG_KIND_PREP, st,

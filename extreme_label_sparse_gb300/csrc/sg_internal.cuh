@@ -32,6 +32,7 @@ struct sg_layout {
     int32_t ldB = 0;         // roundup(max_B, 128)
     int32_t *gcount = nullptr;  // [K+1], all zero between calls
     int32_t *gptr = nullptr;    // [K+1]
+    int32_t *scan_part = nullptr;  // per-tile sums of the group-count scan
     int32_t *gent = nullptr;    // [max_nnz]  (b << 16) | j
     int32_t *tsorted = nullptr; // [max_nnz]  per-row slots, sorted (with dups)
     int32_t *tslots = nullptr;  // [max_nnz]  per-row slots, sorted, deduplicated

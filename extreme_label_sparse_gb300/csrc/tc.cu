@@ -49,7 +49,6 @@ constexpr int kFwdThreads = 32 * (kProdWarps + 2 + kEpiWarps);
 constexpr int kFirstEpi = kProdWarps + 2;
 // dh: one load warp, one MMA warp, eight builder warps
 constexpr int kDhThreads = 32 * (2 + kEpiWarps);
-constexpr int kDhWs = 3;  // scattered-W buffers (builders run up to 2 groups ahead)
 
 // ------------------------------------------------------------------ plans
 struct FwdPlan {
@@ -69,8 +68,8 @@ struct DWPlan {
 
 struct DhPlan {
     bool ok = false;
-    int MT = 0, nk = 0, S = 0, zsw = 0, nbands = 0, band_w = 0;
-    uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, ws_bytes = 0, tmem_cols = 0;
+    int MT = 0, S = 0, zsw = 0, nbands = 0, band_w = 0, nmt = 0;
+    uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, tmem_cols = 0;
 };
 
 uint32_t pow2_cols(int n)
@@ -160,28 +159,24 @@ DhPlan plan_dh(const sg_layout *lo, int B, bool split)
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
         return p;
-    p.nk = lo->F / 64;
     p.zsw = dz_swizzle(lo->G);
     p.z_bytes = (uint32_t)(split ? 2 : 1) * 128 * p.zsw;
-    p.w_bytes = (uint32_t)p.nk * lo->G * 128;
+    p.w_bytes = (uint32_t)lo->G * lo->F * 2;
     p.i_bytes = (uint32_t)((lo->F * 2 + 1023) / 1024 * 1024);
     p.stage_bytes = p.z_bytes + p.w_bytes + p.i_bytes;
-    // bands of at most 512 dh columns (the accumulator fills at most all of
-    // TMEM; MMAs of N <= 256 per K step), in whole 64-column chunks of the
-    // scattered W_k.  Each band re-reads a group's tiles, so fewer, wider
-    // bands cost fewer loads for the same tensor work.
-    for (p.nbands = (lo->H + 511) / 512; p.nbands * 64 < lo->H + 64; ++p.nbands) {
-        p.band_w = ((lo->H + p.nbands - 1) / p.nbands + 63) / 64 * 64;
-        p.ws_bytes = (uint32_t)(p.band_w / 64) * lo->G * 128;
-        const long room = (long)kSmemBudget - (long)kDhWs * p.ws_bytes;
-        p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
-        if (p.S >= 3)
-            break;
-    }
-    if (p.S > 6)
-        p.S = 6;
-    p.tmem_cols = pow2_cols(p.band_w);
-    p.ok = p.S >= 3 && p.band_w <= 512;
+    // TMEM: NMT accumulator tiles of 128 columns plus two A buffers of NMT
+    // tiles of G/2 columns; as many tiles per band as fit (at most 3)
+    int nmt_max = 512 / (128 + lo->G);
+    if (nmt_max > 3)
+        nmt_max = 3;
+    p.nbands = (lo->H + nmt_max * 128 - 1) / (nmt_max * 128);
+    p.nmt = ((lo->H + p.nbands - 1) / p.nbands + 127) / 128;
+    p.band_w = p.nmt * 128;
+    p.tmem_cols = 512;
+    p.S = (int)(kSmemBudget / p.stage_bytes);
+    if (p.S > kMaxStages)
+        p.S = kMaxStages;
+    p.ok = p.S >= 3;
     return p;
 }
 
@@ -1202,50 +1197,40 @@ struct DhArgs {
     float *dh;
     int32_t *status;
     int64_t K, L;
-    int32_t B, G, F, H, MT, nk, S, zsw, nbands, band_w, parts, npass, Bp, vec4;
-    int32_t csize;  // CTAs per cluster: the bands of one (mtile, part), or 1
-    uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, ws_bytes, tmem_cols;
+    int32_t B, G, F, H, MT, S, zsw, nbands, band_w, parts, npass, Bp;
+    uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, tmem_cols;
 };
 
 constexpr int kDhFirstEpi = 2;  // warp 0: loads, warp 1: MMA, then the builders
-// Multicast the band CTAs' common loads across a cluster (off: measured
-// slower than independent loads that hit in L2, the cluster-wide stage
-// release costing more than the L2 traffic it saves)
-constexpr bool kDhMulticast = false;
 
-// CTA (band, mtile, part): dh columns [i0, i0 + band_w) of the band, samples
-// [128 mt, 128 mt + 128), groups k = part, part + parts, ...  The band CTAs of
-// one (mtile, part) form a cluster and read the same tiles: each loads a share
-// of a stage's pieces and multicasts it to all of them, so a tile crosses from
-// L2 once per cluster rather than once per band.  A CTA's stage is refilled
-// once every CTA of the cluster has released it (a cluster-wide barrier per
-// stage, `cempty`).
+// CTA (band, mtile, part): dh columns [i0, i0 + 128 NMT) of the band, samples
+// [128 mt, 128 mt + 128), groups k = part, part + parts, ...
 //
 // The scatter-add of dH_k = dZ_k W_k into the columns I_k of dh is itself a
-// product: dh[:, band] += dZ_k Ws_k with Ws_k[j][i - i0] = W_k[j][f] where
-// I_k[f] = i (zero in every other column).  Eight builder warps write Ws_k for
-// the band into shared memory (MN-major, 128-byte swizzle, like W_k itself);
-// one MMA warp accumulates dZ_k Ws_k over all the CTA's groups into one TMEM
-// accumulator of 128 samples x band_w columns, so the partial of dh never
-// leaves TMEM until it is added into dh at the end.
+// product, taken transposed:
+//     dh[:, band]^T += Ws_k^T dZ_k^T,   Ws_k^T[i - i0][j] = W_k[j][f] where I_k[f] = i
+// (zero rows elsewhere).  The accumulator (M = 128 dh columns per tile, N = 128
+// samples) stays in TMEM over all the CTA's groups.  Ws_k^T is the MMA's A
+// operand and lives in TMEM too: eight builder warps write every one of its
+// rows each group (W_k's column f, or zeros) with tcgen05.st, so nothing has
+// to be cleared and no shared memory is spent on it; B is the group's dZ tile
+// (K-major, rows = samples) as it arrives in shared memory.
 //
-// Compile-time shape: NPASS dZ planes, NKS = G/16 K steps per plane, NP
-// pieces of at most 256 columns per band (fully unrolled MMA issue).
-template <int NPASS, int NKS, int NP>
+// Compile-time shape: NPASS dZ planes, NKS = G/16 K steps per plane, NMT
+// tiles of 128 dh columns per band (fully unrolled MMA issue).
+template <int NPASS, int NKS, int NMT>
 __global__ void __launch_bounds__(kDhThreads, 1)
     k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
             const DhArgs a)
 {
+    constexpr int ACOLS = NKS * 8;  // 32-bit TMEM columns of one A tile (G bf16 per row)
+    constexpr uint32_t kA = NMT * 128;  // first A column; D occupies [0, 128 NMT)
     __shared__ Ctl c;
-    __shared__ uint64_t cempty[kMaxStages];
+    __shared__ uint16_t inv_s[kEpiWarps][32];  // per builder warp: f of each row of its block
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
-    uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
-    const int C = a.csize;
-    // [Ws buffers 0 .. kDhWs-1][stages]
-    const uint32_t stage0 = base + kDhWs * a.ws_bytes;
-    uint8_t *stage0_ptr = base_ptr + kDhWs * (size_t)a.ws_bytes;
+    const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
+    uint8_t *stage0_ptr = dsm + (stage0 - smem_u32(dsm));
     const int G = a.G, F = a.F, S = a.S;
     const int band = blockIdx.x % a.nbands;
     const int mt = (blockIdx.x / a.nbands) % a.MT;
@@ -1253,16 +1238,14 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     const int i0 = band * a.band_w;
     const uint32_t zchunk = 128u * (uint32_t)a.zsw;  // one plane of the stage (G <= 64)
 
-    // stages: full = loads landed; empty = the MMAs that read them are done.
-    // tfull/tempty[nb] = Ws buffer nb written / consumed; drain[0] = last MMA.
+    // stages: full = loads landed; empty = the MMAs (and builders) are done
+    // with them.  tfull/tempty[0..1] = A buffer written / consumed.
     if (threadIdx.x == 0) {
         setup_ctl(c, S, 0, 1, 1);
-        for (int i = 0; i < kDhWs; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c.tfull[i]), kEpiWarps * 32);
             mbar_init(bar_addr(c.tempty[i]), 1);
         }
-        for (int s = 0; s < S && s < kMaxStages; ++s)
-            mbar_init(bar_addr(cempty[s]), (uint32_t)C);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -1271,8 +1254,6 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (C > 1)
-        cluster_sync();  // every CTA's barriers exist before any remote use
     tc_fence_after();
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
@@ -1285,55 +1266,25 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             const uint32_t ph = (uint32_t)(it / S) & 1u;
             if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
                 break;
-            if (C > 1) {
-                // stage s is free here; load into it once it is free everywhere
-                if (lane == 0)
-                    for (int r = 0; r < C; ++r)
-                        mbar_arrive_cluster(mapa_shared(bar_addr(cempty[s]), (uint32_t)r));
-                __syncwarp();
-                if (!mbar_wait(bar_addr(cempty[s]), ph, abort_flag, a.status))
-                    break;
-            }
             const uint32_t Zs = stage0 + (uint32_t)s * a.stage_bytes;
             const uint32_t Wt = Zs + a.z_bytes;
             const uint32_t Is = Wt + a.w_bytes;
             const uint32_t fb = bar_addr(c.full[s]);
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, a.z_bytes + a.w_bytes + (uint32_t)F * 2);
-                // pieces of the stage, dealt round-robin over the cluster
-                const uint16_t mask = (uint16_t)((1u << C) - 1u);
-                int piece = 0;
-                const int rank = C > 1 ? band : 0;  // this CTA's rank in its cluster
-                auto mine = [&]() { return (piece++ % C) == rank; };
-                auto bulk = [&](uint32_t dst, const void *src, uint32_t bytes) {
-                    if (mine()) {
-                        if (C > 1)
-                            bulk_load_mc(dst, src, bytes, fb, mask);
-                        else
-                            bulk_load(dst, src, bytes, fb);
-                    }
-                };
-                auto tile = [&](uint32_t dst, const CUtensorMap *m, int x, int y) {
-                    if (mine()) {
-                        if (C > 1)
-                            tma_load_2d_mc(dst, m, x, y, fb, mask);
-                        else
-                            tma_load_2d(dst, m, x, y, fb);
-                    }
-                };
                 if (a.dZt) {
                     // rows [128 mt, 128 mt + 128) of each plane of the tile
                     const uint8_t *t = a.dZt + (size_t)k * a.tile_bytes + (size_t)mt * zchunk;
-                    for (int pl = 0; pl < a.npass; ++pl)
-                        bulk(Zs + (uint32_t)pl * zchunk, t + (size_t)pl * a.Bp * a.zsw, zchunk);
+                    for (int pl = 0; pl < NPASS; ++pl)
+                        bulk_load(Zs + (uint32_t)pl * zchunk, t + (size_t)pl * a.Bp * a.zsw, zchunk, fb);
                 } else {
-                    tile(Zs, &tm_z, (int)(k * G), mt * 128);
-                    if (a.npass > 1)
-                        tile(Zs + zchunk, &tm_zl, (int)(k * G), mt * 128);
+                    tma_load_2d(Zs, &tm_z, (int)(k * G), mt * 128, fb);
+                    if (NPASS > 1)
+                        tma_load_2d(Zs + zchunk, &tm_zl, (int)(k * G), mt * 128, fb);
                 }
                 // W_k: G contiguous rows of F, read row-major by the builders
-                bulk(Wt, a.W + k * G * F, a.w_bytes);
-                bulk(Is, a.idx_s + k * F, (uint32_t)F * 2);
+                bulk_load(Wt, a.W + k * G * F, a.w_bytes, fb);
+                bulk_load(Is, a.idx_s + k * F, (uint32_t)F * 2, fb);
             }
             __syncwarp();
         }
@@ -1341,36 +1292,31 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         const uint32_t zlayout = layout_for_swizzle(a.zsw);
+        const uint32_t idesc = idesc_bf16(128, 128, 0, 0);  // M = 128 dh columns, N = 128 samples
         int it = 0;
         for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
-            const int nb = it % kDhWs;
+            const int buf = it & 1;
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
-            if (!mbar_wait(bar_addr(c.tfull[nb]), (uint32_t)(it / kDhWs) & 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.tfull[buf]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t Zs = stage0 + (uint32_t)s * a.stage_bytes;
-                const uint32_t Ws = base + (uint32_t)nb * a.ws_bytes;
-                // K runs over j for dZ hi (and again for dZ lo) against Ws_k;
-                // N over the band in pieces of at most 256 columns
 #pragma unroll
-                for (int ks2 = 0; ks2 < NPASS * NKS; ++ks2) {
-                    const int ks = ks2 % NKS;
-                    const uint32_t za = Zs + (uint32_t)(ks2 / NKS) * zchunk + (uint32_t)ks * 32;
-                    const uint64_t ad = sdesc(za, 16, 8 * a.zsw, zlayout);
+                for (int mi = 0; mi < NMT; ++mi) {
 #pragma unroll
-                    for (int pc = 0; pc < NP; ++pc) {
-                        const int n0 = pc * 256;
-                        const int nn = a.band_w - n0 < 256 ? a.band_w - n0 : 256;
-                        const uint64_t bd = sdesc(Ws + (uint32_t)(n0 / 64) * G * 128 + (uint32_t)ks * 2048,
-                                                  (uint32_t)G * 128, 1024, kLayoutSW128);
-                        mma_bf16(tbase + (uint32_t)n0, ad, bd, idesc_bf16(128, nn, 0, 1),
-                                 (it > 0 || ks2 > 0) ? 1u : 0u);
+                    for (int ks2 = 0; ks2 < NPASS * NKS; ++ks2) {
+                        const int ks = ks2 % NKS;
+                        // B: dZ plane ks2 / NKS, K-major (rows = samples), 16 j per step
+                        const uint64_t bd = sdesc(Zs + (uint32_t)(ks2 / NKS) * zchunk + (uint32_t)ks * 32, 16,
+                                                  8 * a.zsw, zlayout);
+                        const uint32_t at = tbase + kA + (uint32_t)((buf * NMT + mi) * ACOLS + ks * 8);
+                        mma_bf16_ta(tbase + (uint32_t)(mi * 128), at, bd, idesc, (it > 0 || ks2 > 0) ? 1u : 0u);
                     }
                 }
-                mma_commit(bar_addr(c.tempty[nb]));
+                mma_commit(bar_addr(c.tempty[buf]));
                 mma_commit(bar_addr(c.empty[s]));
             }
             __syncwarp();
@@ -1381,93 +1327,68 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         mbar_wait_drain(bar_addr(c.drain[0]), 0);  // no MMA in flight at the dealloc
     } else {
         // ---------------------------------------------------------- builders
-        // Warp ew owns rows j = ew, ew + 8, ... of every Ws buffer: it clears
-        // them and writes them, so the warps never touch each other's rows and
-        // need no barrier between them.
+        // warp (q, sub) writes the A rows of lane quarter q of tiles sub, sub + 2
         const int ew = warp - kDhFirstEpi;  // 0 .. 7
-        const int nrows = (G - ew + kEpiWarps - 1) / kEpiWarps;
-        const uint32_t chunk_bytes = (uint32_t)G * 128;  // one 64-column chunk of Ws
-        const int nchunks = a.band_w / 64;
-        // every buffer starts zero
-        for (int nb = 0; nb < kDhWs; ++nb)
-            for (int r = 0; r < nrows; ++r)
-                for (int cch = lane / 8; cch < nchunks; cch += 4)
-                    *reinterpret_cast<uint4 *>(base_ptr + (size_t)nb * a.ws_bytes + cch * chunk_bytes +
-                                               (uint32_t)(ew + r * kEpiWarps) * 128 + (lane & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-        __syncwarp();
+        const int q = warp & 3, sub = ew / 4;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         int it = 0;
         for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
             const int s = it % S;
-            const int nb = it % kDhWs;
+            const int buf = it & 1;
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
-            uint8_t *Ws = base_ptr + (size_t)nb * a.ws_bytes;
             const uint8_t *Wt = stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes;
-            const uint16_t *I = reinterpret_cast<const uint16_t *>(Wt + a.w_bytes);
-            // f range of the band: I_k ascending, so count entries below each end
-            int na = 0, ne = 0;
-            for (int f = lane; f < F; f += 32) {
-                const int v = I[f];
-                na += v < i0;
-                ne += v < i0 + a.band_w;
-            }
-            const int fa = __reduce_add_sync(0xffffffffu, na);
-            const int fe = __reduce_add_sync(0xffffffffu, ne);
-            // the buffer's last group must be through its MMA before it is reused
-            if (!mbar_wait(bar_addr(c.tempty[nb]), ((uint32_t)(it / kDhWs) & 1u) ^ 1u, abort_flag, a.status))
-                break;
-            for (int r = 0; r < nrows; ++r)
-                for (int cch = lane / 8; cch < nchunks; cch += 4)
-                    *reinterpret_cast<uint4 *>(Ws + cch * chunk_bytes + (uint32_t)(ew + r * kEpiWarps) * 128 +
-                                               (lane & 7) * 16) = make_uint4(0, 0, 0, 0);
-            __syncwarp();
-            // lanes run along f; each lane moves W_k[j][f] to Ws[j][I_k[f] - i0]
             const uint16_t *Wrow = reinterpret_cast<const uint16_t *>(Wt);  // [G][F], row-major
-            for (int f = fa + lane; f < fe; f += 32) {
-                const int i = (int)I[f] - i0;
-                const uint32_t wdst = (uint32_t)(i >> 6) * chunk_bytes + (uint32_t)(((i & 63) >> 3) << 4) +
-                                      (uint32_t)(i & 7) * 2;
-                uint16_t w[8];
+            const uint16_t *I = reinterpret_cast<const uint16_t *>(Wt + a.w_bytes);
+            // the A buffer's last group must be through its MMA before it is rewritten
+            if (!mbar_wait(bar_addr(c.tempty[buf]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
+                break;
+            tc_fence_after();
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int j = ew + r * kEpiWarps;
-                    if (r < nrows)
-                        w[r] = Wrow[j * F + f];
+            for (int mi = sub; mi < NMT; mi += 2) {
+                const int R0 = i0 + mi * 128 + q * 32;  // dh column of this block's lane 0
+                // which f (if any) lands on each of the block's 32 columns
+                inv_s[ew][lane] = 0xffffu;
+                __syncwarp();
+                for (int f = lane; f < F; f += 32) {
+                    const int v = (int)I[f] - R0;
+                    if (v >= 0 && v < 32)
+                        inv_s[ew][v] = (uint16_t)f;
                 }
+                __syncwarp();
+                const uint32_t f = inv_s[ew][lane];
+                __syncwarp();
+                uint32_t av[ACOLS];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const uint32_t j = (uint32_t)(ew + r * kEpiWarps);
-                    if (r < nrows)
-                        *reinterpret_cast<uint16_t *>(Ws + ((wdst + j * 128) ^ ((j & 7) << 4))) = w[r];
+                for (int cc = 0; cc < ACOLS; ++cc)
+                    av[cc] = 0u;
+                if (f != 0xffffu) {
+#pragma unroll
+                    for (int cc = 0; cc < ACOLS; ++cc)
+                        av[cc] = (uint32_t)Wrow[(2 * cc) * F + f] | ((uint32_t)Wrow[(2 * cc + 1) * F + f] << 16);
                 }
+                tmem_st<ACOLS>(tbase + lane_off + kA + (uint32_t)((buf * NMT + mi) * ACOLS), av);
             }
-            fence_proxy_async();  // Ws_k (generic writes) -> the MMA (async proxy)
-            mbar_arrive(bar_addr(c.tfull[nb]));
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_addr(c.tfull[buf]));
         }
-        // the accumulator holds this CTA's partial of dh[:, band]: add it in
+        // the accumulator holds this CTA's partial of dh[:, band]^T: add it in
         if (mbar_wait(bar_addr(c.drain[0]), 0, abort_flag, a.status) && !*abort_flag && it > 0) {
             tc_fence_after();
-            const int q = warp & 3, sub = ew / 4;
-            const int b = mt * 128 + q * 32 + lane;
-            const int i_end = a.H - i0 < a.band_w ? a.H - i0 : a.band_w;
-            for (int c0 = sub * 32; c0 < a.band_w; c0 += 64) {
-                uint32_t r[32];
-                tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
-                tmem_ld_wait();
-                if (b < a.B) {
-                    float *dst = a.dh + (int64_t)b * a.H + i0 + c0;
-                    if (a.vec4 && c0 + 32 <= i_end) {
+            for (int mi = sub; mi < NMT; mi += 2) {
+                const int i = i0 + mi * 128 + q * 32 + lane;  // this lane's dh column
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + (uint32_t)(mi * 128 + c0), r);
+                    tmem_ld_wait();
+                    if (i < a.H) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            atomicAdd(reinterpret_cast<float4 *>(dst + i),
-                                      make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                                  __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (c0 + i < i_end)
-                                atomicAdd(dst + i, __uint_as_float(r[i]));
+                        for (int x = 0; x < 32; ++x) {
+                            const int b = mt * 128 + c0 + x;
+                            if (b < a.B)
+                                atomicAdd(a.dh + (int64_t)b * a.H + i, __uint_as_float(r[x]));
+                        }
                     }
                 }
             }
@@ -1475,9 +1396,6 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    // no CTA leaves while another may still multicast into it or arrive on it
-    if (C > 1)
-        cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, a.tmem_cols);
@@ -1762,75 +1680,47 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.F = lo->F;
     a.H = lo->H;
     a.MT = p.MT;
-    a.nk = p.nk;
     a.S = p.S;
     a.zsw = p.zsw;
     a.nbands = p.nbands;
     a.band_w = p.band_w;
     a.npass = split ? 2 : 1;
     a.Bp = p.MT * 128;
-    a.vec4 = (lo->H % 4 == 0 && ((uintptr_t)dh & 15) == 0) ? 1 : 0;
-    const size_t smem = kDhWs * (size_t)p.ws_bytes + (size_t)p.S * p.stage_bytes + 1024;
-    // kernel instance for (planes, K steps per plane, N pieces)
-    void (*kern)(CUtensorMap, CUtensorMap, DhArgs) = nullptr;
-    const int nks = lo->G / 16, np = (p.band_w + 255) / 256;
-#define SG_DH_PICK(P, K, N)                          \
-    if (a.npass == P && nks == K && np == N)         \
-        kern = k_tc_dh<P, K, N>;
-    SG_DH_PICK(1, 1, 1) SG_DH_PICK(1, 1, 2) SG_DH_PICK(1, 2, 1) SG_DH_PICK(1, 2, 2)
-    SG_DH_PICK(1, 4, 1) SG_DH_PICK(1, 4, 2) SG_DH_PICK(2, 1, 1) SG_DH_PICK(2, 1, 2)
-    SG_DH_PICK(2, 2, 1) SG_DH_PICK(2, 2, 2) SG_DH_PICK(2, 4, 1) SG_DH_PICK(2, 4, 2)
-#undef SG_DH_PICK
-    if (!kern) {
-        sg_set_error("tc_dh: no kernel for G = %d, band %d", lo->G, p.band_w);
-        return SG_ERR_UNSUPPORTED;
-    }
-    rc = set_smem(kern, smem);
-    if (rc != SG_OK)
-        return rc;
-    // one cluster per (mtile, part) holding its bands when the loads are
-    // multicast; as many parts as clusters fit on the GPU at once
-    a.csize = kDhMulticast ? p.nbands : 1;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)a.csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kDhThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = lo->num_sms / p.nbands;
-    if (a.csize > 1) {
-        cfg.gridDim = dim3((unsigned)(p.nbands * p.MT * clusters), 1, 1);
-        int n = 0;
-        SG_TRY_CUDA(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
-        if (n < 1) {
-            sg_set_error("tc_dh: no cluster of %d CTAs fits on the device", p.nbands);
-            return SG_ERR_UNSUPPORTED;
-        }
-        clusters = n;
-    }
-    int parts = clusters / p.MT;
+    int parts = lo->num_sms / (p.nbands * p.MT);
     if (parts < 1)
         parts = 1;
     if (parts > lo->K)
         parts = (int)lo->K;
     a.parts = parts;
-    cfg.gridDim = dim3((unsigned)(p.nbands * p.MT * parts), 1, 1);
     a.z_bytes = p.z_bytes;
     a.w_bytes = p.w_bytes;
     a.i_bytes = p.i_bytes;
     a.stage_bytes = p.stage_bytes;
-    a.ws_bytes = p.ws_bytes;
     a.tmem_cols = p.tmem_cols;
+    // kernel instance for (planes, K steps per plane, tiles per band)
+    void (*kern)(CUtensorMap, CUtensorMap, DhArgs) = nullptr;
+    const int nks = lo->G / 16;
+#define SG_DH_PICK(P, K, N)                                   \
+    if (a.npass == P && nks == K && p.nmt == N)               \
+        kern = k_tc_dh<P, K, N>;
+    SG_DH_PICK(1, 1, 1) SG_DH_PICK(1, 1, 2) SG_DH_PICK(1, 1, 3)
+    SG_DH_PICK(1, 2, 1) SG_DH_PICK(1, 2, 2) SG_DH_PICK(1, 2, 3)
+    SG_DH_PICK(1, 4, 1) SG_DH_PICK(1, 4, 2)
+    SG_DH_PICK(2, 1, 1) SG_DH_PICK(2, 1, 2) SG_DH_PICK(2, 1, 3)
+    SG_DH_PICK(2, 2, 1) SG_DH_PICK(2, 2, 2) SG_DH_PICK(2, 2, 3)
+    SG_DH_PICK(2, 4, 1) SG_DH_PICK(2, 4, 2)
+#undef SG_DH_PICK
+    if (!kern) {
+        sg_set_error("tc_dh: no kernel for G = %d, %d tiles per band", lo->G, p.nmt);
+        return SG_ERR_UNSUPPORTED;
+    }
+    const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
+    rc = set_smem(kern, smem);
+    if (rc != SG_OK)
+        return rc;
     SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
-    cudaError_t le = cudaSuccess;
-    SG_LAUNCH(lo, SG_KIND_DH, st, le = cudaLaunchKernelEx(&cfg, kern, tm_z, tm_zl, a));
-    SG_TRY_CUDA(le);
+    SG_LAUNCH(lo, SG_KIND_DH, st,
+              kern<<<p.nbands * p.MT * parts, kDhThreads, smem, st>>>(tm_z, tm_zl, a));
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }
