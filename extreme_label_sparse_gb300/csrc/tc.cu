@@ -47,8 +47,10 @@ constexpr int kProdWarps = 8;  // cp.async gather + TMA issue (8: measured ~2x t
 // forward / dW: producers, two MMA-issuing warps, epilogue
 constexpr int kFwdThreads = 32 * (kProdWarps + 2 + kEpiWarps);
 constexpr int kFirstEpi = kProdWarps + 2;
-// dh: one load warp, one MMA warp, eight builder warps
-constexpr int kDhThreads = 32 * (2 + kEpiWarps);
+// dh: one load warp, one MMA warp, twelve builder warps (one per lane
+// quarter of each of up to three 128-column tiles)
+constexpr int kDhBuilders = 12;
+constexpr int kDhThreads = 32 * (2 + kDhBuilders);
 
 // ------------------------------------------------------------------ plans
 struct FwdPlan {
@@ -1226,7 +1228,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     constexpr int ACOLS = NKS * 8;  // 32-bit TMEM columns of one A tile (G bf16 per row)
     constexpr uint32_t kA = NMT * 128;  // first A column; D occupies [0, 128 NMT)
     __shared__ Ctl c;
-    __shared__ uint16_t inv_s[kEpiWarps][32];  // per builder warp: f of each row of its block
+    __shared__ uint16_t inv_s[kDhBuilders][32];  // per builder warp: f of each row of its block
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
@@ -1243,7 +1245,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     if (threadIdx.x == 0) {
         setup_ctl(c, S, 0, 1, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(c.tfull[i]), kEpiWarps * 32);
+            mbar_init(bar_addr(c.tfull[i]), kDhBuilders * 32);
             mbar_init(bar_addr(c.tempty[i]), 1);
         }
         fence_mbar_init();
@@ -1327,8 +1329,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         mbar_wait_drain(bar_addr(c.drain[0]), 0);  // no MMA in flight at the dealloc
     } else {
         // ---------------------------------------------------------- builders
-        // warp (q, sub) writes the A rows of lane quarter q of tiles sub, sub + 2
-        const int ew = warp - kDhFirstEpi;  // 0 .. 7
+        // warp (q, sub) writes the A rows of lane quarter q of tile sub
+        const int ew = warp - kDhFirstEpi;  // 0 .. kDhBuilders-1
         const int q = warp & 3, sub = ew / 4;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         int it = 0;
@@ -1344,8 +1346,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             if (!mbar_wait(bar_addr(c.tempty[buf]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
-#pragma unroll
-            for (int mi = sub; mi < NMT; mi += 2) {
+            for (int mi = sub; mi < NMT; mi += kDhBuilders / 4) {
                 const int R0 = i0 + mi * 128 + q * 32;  // dh column of this block's lane 0
                 // which f (if any) lands on each of the block's 32 columns
                 inv_s[ew][lane] = 0xffffu;
@@ -1376,7 +1377,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         // the accumulator holds this CTA's partial of dh[:, band]^T: add it in
         if (mbar_wait(bar_addr(c.drain[0]), 0, abort_flag, a.status) && !*abort_flag && it > 0) {
             tc_fence_after();
-            for (int mi = sub; mi < NMT; mi += 2) {
+            for (int mi = sub; mi < NMT; mi += kDhBuilders / 4) {
                 const int i = i0 + mi * 128 + q * 32 + lane;  // this lane's dh column
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t r[32];
