@@ -45,6 +45,10 @@ struct sg_layout {
     // allocated on first use
     uint16_t *dZ_ws = nullptr;
     size_t dZ_ws_elems = 0;
+    // dh: per group, for each dh column i (row stride Hp = H rounded up to 16)
+    // the f with I_k[f] = i, 0xff where none (lazily built, needs F < 255)
+    uint8_t *invmap = nullptr;
+    int32_t invmap_hp = 0;
 
     // per-kernel event timing (sg_timing_start / sg_timing_stop)
     struct Timer {

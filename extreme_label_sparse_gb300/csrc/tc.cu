@@ -156,7 +156,7 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 DhPlan plan_dh(const sg_layout *lo, int B, bool split)
 {
     DhPlan p;
-    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->G > 64 || B < 1 || B > 256)
+    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->G > 64 || lo->F >= 255 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
@@ -164,8 +164,6 @@ DhPlan plan_dh(const sg_layout *lo, int B, bool split)
     p.zsw = dz_swizzle(lo->G);
     p.z_bytes = (uint32_t)(split ? 2 : 1) * 128 * p.zsw;
     p.w_bytes = (uint32_t)lo->G * lo->F * 2;
-    p.i_bytes = (uint32_t)((lo->F * 2 + 1023) / 1024 * 1024);
-    p.stage_bytes = p.z_bytes + p.w_bytes + p.i_bytes;
     // TMEM: NMT accumulator tiles of 128 columns plus two A buffers of NMT
     // tiles of G/2 columns; as many tiles per band as fit (at most 3)
     int nmt_max = 512 / (128 + lo->G);
@@ -174,6 +172,9 @@ DhPlan plan_dh(const sg_layout *lo, int B, bool split)
     p.nbands = (lo->H + nmt_max * 128 - 1) / (nmt_max * 128);
     p.nmt = ((lo->H + p.nbands - 1) / p.nbands + 127) / 128;
     p.band_w = p.nmt * 128;
+    // the band's slice of the group's inverse map (u8 per dh column)
+    p.i_bytes = (uint32_t)((p.band_w + 1023) / 1024 * 1024);
+    p.stage_bytes = p.z_bytes + p.w_bytes + p.i_bytes;
     p.tmem_cols = 512;
     p.S = (int)(kSmemBudget / p.stage_bytes);
     if (p.S > kMaxStages)
@@ -1192,7 +1193,8 @@ __global__ void __launch_bounds__(kFWThreads, 1)
 
 // ================================================================== dh
 struct DhArgs {
-    const uint16_t *idx_s;
+    const uint8_t *invmap;  // [K][Hp]: f with I_k[f] = i, 0xff where none
+    int64_t Hp;
     const uint16_t *W;     // [L][F] in slot order
     const uint8_t *dZt;    // group-tiled dZ input (else the tensor maps)
     uint64_t tile_bytes;
@@ -1228,7 +1230,6 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     constexpr int ACOLS = NKS * 8;  // 32-bit TMEM columns of one A tile (G bf16 per row)
     constexpr uint32_t kA = NMT * 128;  // first A column; D occupies [0, 128 NMT)
     __shared__ Ctl c;
-    __shared__ uint16_t inv_s[kDhBuilders][32];  // per builder warp: f of each row of its block
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
@@ -1273,7 +1274,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             const uint32_t Is = Wt + a.w_bytes;
             const uint32_t fb = bar_addr(c.full[s]);
             if (lane == 0) {
-                mbar_arrive_expect_tx(fb, a.z_bytes + a.w_bytes + (uint32_t)F * 2);
+                mbar_arrive_expect_tx(fb, a.z_bytes + a.w_bytes + (uint32_t)a.band_w);
                 if (a.dZt) {
                     // rows [128 mt, 128 mt + 128) of each plane of the tile
                     const uint8_t *t = a.dZt + (size_t)k * a.tile_bytes + (size_t)mt * zchunk;
@@ -1286,7 +1287,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 }
                 // W_k: G contiguous rows of F, read row-major by the builders
                 bulk_load(Wt, a.W + k * G * F, a.w_bytes, fb);
-                bulk_load(Is, a.idx_s + k * F, (uint32_t)F * 2, fb);
+                // which f lands on each dh column of the band
+                bulk_load(Is, a.invmap + k * a.Hp + i0, (uint32_t)a.band_w, fb);
             }
             __syncwarp();
         }
@@ -1341,29 +1343,19 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 break;
             const uint8_t *Wt = stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes;
             const uint16_t *Wrow = reinterpret_cast<const uint16_t *>(Wt);  // [G][F], row-major
-            const uint16_t *I = reinterpret_cast<const uint16_t *>(Wt + a.w_bytes);
+            const uint8_t *inv = Wt + a.w_bytes;  // band's inverse map
             // the A buffer's last group must be through its MMA before it is rewritten
             if (!mbar_wait(bar_addr(c.tempty[buf]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
             for (int mi = sub; mi < NMT; mi += kDhBuilders / 4) {
-                const int R0 = i0 + mi * 128 + q * 32;  // dh column of this block's lane 0
-                // which f (if any) lands on each of the block's 32 columns
-                inv_s[ew][lane] = 0xffffu;
-                __syncwarp();
-                for (int f = lane; f < F; f += 32) {
-                    const int v = (int)I[f] - R0;
-                    if (v >= 0 && v < 32)
-                        inv_s[ew][v] = (uint16_t)f;
-                }
-                __syncwarp();
-                const uint32_t f = inv_s[ew][lane];
-                __syncwarp();
+                // the f (if any) that lands on this lane's dh column
+                const uint32_t f = inv[mi * 128 + q * 32 + lane];
                 uint32_t av[ACOLS];
 #pragma unroll
                 for (int cc = 0; cc < ACOLS; ++cc)
                     av[cc] = 0u;
-                if (f != 0xffffu) {
+                if (f != 0xffu) {
 #pragma unroll
                     for (int cc = 0; cc < ACOLS; ++cc)
                         av[cc] = (uint32_t)Wrow[(2 * cc) * F + f] | ((uint32_t)Wrow[(2 * cc + 1) * F + f] << 16);
@@ -1639,6 +1631,34 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     return SG_OK;
 }
 
+// inverse of I_k per group: map[k][I_k[f]] = f
+__global__ void k_invmap(const uint16_t *__restrict__ idx_s, int64_t K, int F, int64_t Hp, uint8_t *map)
+{
+    const int64_t k = blockIdx.x;
+    for (int f = threadIdx.x; f < F; f += blockDim.x)
+        map[k * Hp + idx_s[k * F + f]] = (uint8_t)f;
+}
+
+sg_status ensure_invmap(sg_layout *lo, int band_w, cudaStream_t st)
+{
+    if (lo->invmap)
+        return SG_OK;
+    const int64_t Hp = (lo->H + 15) / 16 * 16;
+    // the last band may read up to band_w past the last row's start
+    const size_t bytes = (size_t)lo->K * Hp + (size_t)band_w + 16;
+    if (cudaMalloc((void **)&lo->invmap, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        lo->invmap = nullptr;
+        sg_set_error("tc_dh: cudaMalloc of %zu bytes for the inverse map failed", bytes);
+        return SG_ERR_OOM;
+    }
+    lo->invmap_hp = (int32_t)Hp;
+    SG_TRY_CUDA(cudaMemsetAsync(lo->invmap, 0xff, bytes, st));
+    k_invmap<<<(unsigned)lo->K, 128, 0, st>>>(lo->idx_s, lo->K, lo->F, Hp, lo->invmap);
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
 sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
                 int32_t B, const uint16_t *W, float *dh, cudaStream_t st)
 {
@@ -1667,8 +1687,12 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
         sg_set_error("W: device pointer must be 16-byte aligned");
         return SG_ERR_INVALID;
     }
+    rc = ensure_invmap(lo, p.band_w, st);
+    if (rc != SG_OK)
+        return rc;
     DhArgs a;
-    a.idx_s = lo->idx_s;
+    a.invmap = lo->invmap;
+    a.Hp = lo->invmap_hp;
     a.W = W;
     a.dZt = dZt;
     a.tile_bytes = tc_dz_tile_bytes(lo, B);

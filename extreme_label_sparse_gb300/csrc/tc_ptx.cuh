@@ -337,11 +337,15 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
                  : "memory");
 }
 
-// 32 lanes x N consecutive 32-bit columns (N = 8, 16 or 32)
+// 32 lanes x N consecutive 32-bit columns (N = 4, 8, 16 or 32)
 template <int N>
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&v)[N])
 {
-    if constexpr (N == 8) {
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]),
+                     "r"(v[1]), "r"(v[2]), "r"(v[3])
+                     : "memory");
+    } else if constexpr (N == 8) {
         asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                      : "memory");
@@ -352,7 +356,7 @@ __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&v)[N])
             "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
             : "memory");
     } else {
-        static_assert(N == 32, "x8, x16 or x32");
+        static_assert(N == 32, "x4, x8, x16 or x32");
         asm volatile(
             "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
             "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
