@@ -487,6 +487,30 @@ __device__ __forceinline__ void issue_gather(const uint16_t *hT, int ldB, uint32
     }
 }
 
+// The same copy with the shape known at compile time (F rows, U 16-byte units
+// per row): the loop unrolls, the per-lane offsets are computed once, and an
+// instruction costs a shuffle, a 32-bit multiply-add and the copy.
+template <int F_, int U_>
+__device__ __forceinline__ void issue_gather_t(const uint16_t *hT, int ldB, uint32_t A, const GatherIdx &g,
+                                               int lane)
+{
+    constexpr int RW = F_ / kProdWarps;
+    constexpr int LPR = U_ < 32 ? U_ : 32;  // lanes per row
+    constexpr int RPI = 32 / LPR;           // rows per instruction
+    static_assert(RW % RPI == 0 && RW <= 64, "rows per producer warp");
+    const int pw = threadIdx.x / 32;
+    const int u = lane % LPR, rsub = lane / LPR;
+    const uint32_t dst0 = A + (uint32_t)(u >> 3) * F_ * 128 + (uint32_t)(pw * RW + rsub) * 128;
+    const uint16_t *src0 = hT + u * 8;
+#pragma unroll
+    for (int t = 0; t < RW / RPI; ++t) {
+        const int r = t * RPI + rsub;  // row within the warp's RW rows (RW is a multiple of 8)
+        const uint32_t row = __shfl_sync(0xffffffffu, t * RPI < 32 ? g.i[0] : g.i[1], r & 31);
+        cp_async16(dst0 + (uint32_t)(t * RPI) * 128 + (uint32_t)(((u & 7) ^ (r & 7)) << 4),
+                   src0 + row * (uint32_t)ldB);
+    }
+}
+
 // Producer loop shared by the forward and the weight gradient: per group, one
 // thread arms the stage barrier with the TMA bytes (`tma_bytes`, issued by
 // `issue_tma`), every producer thread copies its share of H_k and has the
@@ -494,7 +518,7 @@ __device__ __forceinline__ void issue_gather(const uint16_t *hT, int ldB, uint32
 // producers run ahead as far as free stages allow.  The cp.async writes are
 // generic-proxy writes: every MMA warp fences (proxy.async) after it has seen
 // the stage barrier and before its MMAs read the stage.
-template <typename IssueTma>
+template <int F_ = 0, int U_ = 0, typename IssueTma>
 __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t stage_bytes, int S,
                                               int64_t K, const uint16_t *idx_s, const uint16_t *hT,
                                               int ldB, int F, int MT, uint32_t tma_bytes,
@@ -521,7 +545,10 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
             mbar_arrive_expect_tx(bar_addr(c.full[s]), tma_bytes);
             issue_tma(k, A, bar_addr(c.full[s]));
         }
-        issue_gather(hT, ldB, A, F, units, cur, lane);
+        if constexpr (F_ > 0)
+            issue_gather_t<F_, U_>(hT, ldB, A, cur, lane);
+        else
+            issue_gather(hT, ldB, A, F, units, cur, lane);
         cp_async_arrive_noinc(bar_addr(c.full[s]));
         cur = nxt;
     }
@@ -991,7 +1018,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
 
     if (warp < kProdWarps) {
         // ---------------------------------------------------------- producers
-        producer_loop(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes,
+        producer_loop<FK * 16, MT * 16>(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes,
                       abort_flag, a.status, [&](int64_t k, uint32_t A, uint32_t fb) {
                           const uint32_t Wt = A + a.a_bytes;
                           for (int kc = 0; kc < a.nk; ++kc)
