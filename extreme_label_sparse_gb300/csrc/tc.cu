@@ -970,10 +970,15 @@ struct CtlFW {
 // The MMA issue loops have compile-time trip counts (FK = F/16 K steps, MT
 // sample tiles): tcgen05.mma issued from a loop with a run-time trip count
 // measured about 2x slower per instruction than the same MMAs unrolled.
-template <int CH, int FK, int MT>
+template <int G_, int FK, int MT>
 __global__ void __launch_bounds__(kFWThreads, 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
 {
+    // compile-time group width: column chunk of the epilogue, dZ row width
+    // (swizzle) and 64-column chunks of the dZ tile
+    constexpr int CH = G_ >= 64 ? 32 : 16;
+    constexpr int ZSW = G_ * 2 >= 128 ? 128 : G_ * 2;
+    constexpr int NZC = G_ * 2 > 128 ? G_ / 64 : 1;
     __shared__ CtlFW cf;
     Ctl &c = cf.c;
     extern __shared__ uint8_t dsm[];
@@ -983,9 +988,10 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     // [dZ_k buffer 0][dZ_k buffer 1][dW_k staging 0][dW_k staging 1][stages]
     const uint32_t stg0 = base + 2 * a.dz_bytes;
     const uint32_t stage0 = stg0 + 2 * a.stg_bytes;
-    const int G = a.G, F = a.F, S = a.S, NS = a.nslot;
-    const uint32_t zrows = (uint32_t)a.MT * 128;
-    const uint32_t zchunk = zrows * (uint32_t)a.zsw;
+    constexpr int G = G_;
+    const int F = a.F, S = a.S, NS = a.nslot;
+    constexpr uint32_t zrows = (uint32_t)MT * 128;
+    constexpr uint32_t zchunk = zrows * (uint32_t)ZSW;
     const uint32_t wbase = (uint32_t)NS * a.zcols;  // first dW accumulator column
 
     // the epilogue is two teams: the BCE warps turn Z_k into dZ_k, the dW
@@ -1063,7 +1069,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         mbar_wait_drain(bar_addr(c.drain[0]), 0);
     } else if (warp < kFWFirstEpi) {
         // ---------------------------------------------------------- dW MMA
-        const uint32_t zlayout = layout_for_swizzle(a.zsw);
+        const uint32_t zlayout = layout_for_swizzle(ZSW);
         const uint32_t idesc = idesc_bf16(128, 2 * G, 0, 1);  // N = [hi | lo] along j
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
@@ -1101,7 +1107,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                         const uint64_t ad = sdesc(A + (uint32_t)(st / 4) * FK * 2048 + (uint32_t)tf * 128 * 128 +
                                                       (uint32_t)(st % 4) * 32,
                                                   16, 1024, kLayoutSW128);
-                        const uint64_t bd = sdesc(Zs + (uint32_t)st * 16 * a.zsw, zchunk, 8 * a.zsw, zlayout);
+                        const uint64_t bd = sdesc(Zs + (uint32_t)st * 16 * ZSW, zchunk, 8 * ZSW, zlayout);
                         mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
                     }
                 }
@@ -1126,7 +1132,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             double lacc = 0.0;
             const int sub = ew / 4;  // two warps per lane quarter split the column units
             // Z_k -> BCE -> dZ_k (workspace tile and shared memory for the dW MMA)
-            const int zunits = a.MT * (G / CH);
+            constexpr int zunits = MT * (G / CH);
             // positive-list bounds of the group, loaded one group ahead
             int e0n = 0, e1n = 0;
             if (blockIdx.x < a.K) {
@@ -1149,6 +1155,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     break;
                 tc_fence_after();
                 uint8_t *zs_smem = base_ptr + (size_t)db * a.dz_bytes;
+#pragma unroll
                 for (int u = sub; u < zunits; u += 2) {
                     const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
                     const int b = t * 128 + q * 32 + lane;
@@ -1162,7 +1169,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                         for (int i = 0; i < CH; ++i)
                             v[i] = 0.f;
                     }
-                    store_dz_tile<CH>(zs_smem, b, c0, v, a.zsw, a.nzc, a.Bp);
+                    store_dz_tile<CH>(zs_smem, b, c0, v, ZSW, NZC, MT * 128);
                 }
                 tc_fence_before();
                 mbar_arrive(bar_addr(c.tempty[zs]));
@@ -1174,7 +1181,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
             // staged in shared memory as [j][f] and stored with one bulk copy
             const int dw = ew - kFWBce;  // 0 .. kFWDw-1
-            const int wunits = a.FT * (G / CH);
+            constexpr int wunits = (FK / 8) * (G / CH);
             int it = 0;
             for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
                 const int ws = it % NS;
@@ -1187,6 +1194,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 if (dw == 0 && lane == 0)
                     bulk_wait_read<1>();
                 named_bar(2, kFWDw * 32);
+#pragma unroll 1
                 for (int u = 0; u < wunits; ++u) {
                     const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
                     const int f = tf * 128 + q * 32 + lane;
@@ -1577,15 +1585,15 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     const size_t smem = 2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
-    const bool c32 = lo->G >= 64;
-    if (lo->F == 128)
-        kern = p.MT == 1 ? (c32 ? k_tc_fwdw<32, 8, 1> : k_tc_fwdw<16, 8, 1>)
-                         : (c32 ? k_tc_fwdw<32, 8, 2> : k_tc_fwdw<16, 8, 2>);
-    else if (lo->F == 256)
-        kern = p.MT == 1 ? (c32 ? k_tc_fwdw<32, 16, 1> : k_tc_fwdw<16, 16, 1>)
-                         : (c32 ? k_tc_fwdw<32, 16, 2> : k_tc_fwdw<16, 16, 2>);
+#define SG_FW_PICK(GG, KK, MM)                                           \
+    if (lo->G == GG && lo->F == KK * 16 && p.MT == MM)                   \
+        kern = k_tc_fwdw<GG, KK, MM>;
+    SG_FW_PICK(16, 8, 1) SG_FW_PICK(16, 8, 2) SG_FW_PICK(16, 16, 1) SG_FW_PICK(16, 16, 2)
+    SG_FW_PICK(32, 8, 1) SG_FW_PICK(32, 8, 2) SG_FW_PICK(32, 16, 1) SG_FW_PICK(32, 16, 2)
+    SG_FW_PICK(64, 8, 1) SG_FW_PICK(64, 8, 2) SG_FW_PICK(64, 16, 1) SG_FW_PICK(64, 16, 2)
+#undef SG_FW_PICK
     if (!kern) {
-        sg_set_error("tc_fwdw: F = %d has no fused kernel", lo->F);
+        sg_set_error("tc_fwdw: G = %d, F = %d has no fused kernel", lo->G, lo->F);
         return SG_ERR_UNSUPPORTED;
     }
     rc = set_smem(kern, smem);
