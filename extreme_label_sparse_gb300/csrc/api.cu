@@ -498,10 +498,16 @@ sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
     REQUIRE(loss, fn);
     DeviceGuard dg(lo->device);
     cudaStream_t st = (cudaStream_t)stream;
-    bool tc_f = false, tc_w = false, tc_h = false;
-    TRY(pick_tc(lo, SG_KIND_FWD, B, &tc_f, fn));
-    TRY(pick_tc(lo, SG_KIND_DW, B, &tc_w, fn));
-    TRY(pick_tc(lo, SG_KIND_DH, B, &tc_h, fn));
+    // the fused forward + BCE + dW kernel and the tensor-core dh, with dZ in
+    // the group-tiled workspace, whenever the shape fits them
+    const bool fused = lo->engine != SG_ENGINE_SIMT && lo->tc_ok && tc_fwdw_ok(lo, B) &&
+                       tc_stage_ok(lo, SG_KIND_DH, B);
+    bool tc_f = fused, tc_w = fused, tc_h = fused;
+    if (!fused) {
+        TRY(pick_tc(lo, SG_KIND_FWD, B, &tc_f, fn));
+        TRY(pick_tc(lo, SG_KIND_DW, B, &tc_w, fn));
+        TRY(pick_tc(lo, SG_KIND_DH, B, &tc_h, fn));
+    }
     TRY(simt_transpose_h(lo, h, B, st));
     TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
     // forward + BCE into dZ scratch, then dW and dh from it.  dZ is kept as
@@ -509,10 +515,10 @@ sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
     // samples (dW) or over every label (dh), would move results by more than
     // 2e-2 (1 + |ref|) against the exact gradient.
     TRY(ensure_dz_ws(lo));
-    if (tc_f && tc_w && tc_h && tc_tiled_ok(lo, B)) {
+    if (fused || (tc_f && tc_w && tc_h && tc_tiled_ok(lo, B))) {
         // all three on the tensor cores: dZ in the group-tiled workspace
         uint8_t *dZt = reinterpret_cast<uint8_t *>(lo->dZ_ws);
-        if (tc_fwdw_ok(lo, B)) {
+        if (fused) {
             TRY(tc_fwdw(lo, B, W, dZt, dW, loss, st));
         } else {
             TRY(tc_fwd(lo, B, W, nullptr, nullptr, nullptr, dZt, loss, st));

@@ -910,19 +910,21 @@ struct FWPlan {
     bool ok = false;
     int MT = 0, FT = 0, nk = 0, S = 0, zsw = 0, nzc = 0, nslot = 0;
     uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, dz_bytes = 0, stg_bytes = 0, zcols = 0, wcols = 0,
-             tmem_cols = 0;
+             tmem_cols = 0, pad_bytes = 0;
 };
 
 FWPlan plan_fwdw(const sg_layout *lo, int B)
 {
     FWPlan p;
-    if (!shape_ok(lo) || !dz_ok(lo->G) || (lo->F != 128 && lo->F != 256) || 2 * lo->G > 256 || B < 1 ||
-        B > 256)
+    if (!shape_ok(lo) || !dz_ok(lo->G) || (lo->F != 64 && lo->F != 128 && lo->F != 256) ||
+        2 * lo->G > 256 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
         return p;
-    p.FT = lo->F / 128;
+    // dW tiles of M = 128 rows of f; with F = 64 the upper 64 accumulator
+    // lanes read the next 64 rows of shared memory and are never stored
+    p.FT = (lo->F + 127) / 128;
     p.nk = lo->F / 64;
     p.zsw = dz_swizzle(lo->G);
     p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
@@ -937,7 +939,9 @@ FWPlan plan_fwdw(const sg_layout *lo, int B)
     if (p.nslot * (p.zcols + p.wcols) > 512)
         return p;
     p.tmem_cols = pow2_cols(p.nslot * (p.zcols + p.wcols));
-    const long room = (long)kSmemBudget - 2l * p.dz_bytes - 2l * p.stg_bytes;
+    // F = 64: the last stage's dW MMA reads up to 8 KB past it
+    p.pad_bytes = lo->F < 128 ? 8192u : 0u;
+    const long room = (long)kSmemBudget - 2l * p.dz_bytes - 2l * p.stg_bytes - (long)p.pad_bytes;
     p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
     if (p.S > 6)
         p.S = 6;
@@ -1100,7 +1104,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 bulk_store(a.dZt + (size_t)k * a.tile_bytes, Zs, a.dz_bytes);
                 bulk_commit();
 #pragma unroll
-                for (int tf = 0; tf < FK / 8; ++tf) {
+                for (int tf = 0; tf < (FK + 7) / 8; ++tf) {
                     const uint32_t d = tbase + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G);
 #pragma unroll
                     for (int st = 0; st < MT * 8; ++st) {
@@ -1181,7 +1185,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
             // staged in shared memory as [j][f] and stored with one bulk copy
             const int dw = ew - kFWBce;  // 0 .. kFWDw-1
-            constexpr int wunits = (FK / 8) * (G / CH);
+            constexpr int wunits = ((FK + 7) / 8) * (G / CH);
             int it = 0;
             for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
                 const int ws = it % NS;
@@ -1201,9 +1205,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     const uint32_t col = tbase + lane_off + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G + c0);
                     float v[CH], w[CH];
                     tmem_ld_chunk2<CH>(col, col + (uint32_t)G, v, w);
+                    if (f < F) {
 #pragma unroll
-                    for (int i = 0; i < CH; ++i)
-                        stg[(c0 + i) * F + f] = bf16_rn(v[i] + w[i]);
+                        for (int i = 0; i < CH; ++i)
+                            stg[(c0 + i) * F + f] = bf16_rn(v[i] + w[i]);
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(bar_addr(cf.wempty[ws]));
@@ -1582,12 +1588,15 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.zcols = p.zcols;
     a.wcols = p.wcols;
     a.tmem_cols = p.tmem_cols;
-    const size_t smem = 2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + 1024;
+    const size_t smem =
+        2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
 #define SG_FW_PICK(GG, KK, MM)                                           \
     if (lo->G == GG && lo->F == KK * 16 && p.MT == MM)                   \
         kern = k_tc_fwdw<GG, KK, MM>;
+    SG_FW_PICK(16, 4, 1) SG_FW_PICK(16, 4, 2) SG_FW_PICK(32, 4, 1) SG_FW_PICK(32, 4, 2)
+    SG_FW_PICK(64, 4, 1) SG_FW_PICK(64, 4, 2)
     SG_FW_PICK(16, 8, 1) SG_FW_PICK(16, 8, 2) SG_FW_PICK(16, 16, 1) SG_FW_PICK(16, 16, 2)
     SG_FW_PICK(32, 8, 1) SG_FW_PICK(32, 8, 2) SG_FW_PICK(32, 16, 1) SG_FW_PICK(32, 16, 2)
     SG_FW_PICK(64, 8, 1) SG_FW_PICK(64, 8, 2) SG_FW_PICK(64, 16, 1) SG_FW_PICK(64, 16, 2)
