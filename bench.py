@@ -57,8 +57,8 @@ def _peaks():
 # L = 524,288; profiles/k_tc_fwdw_k_tc_dh_amazon3m_L524288.md.  Scaled to a
 # launch by the groups it processes; None for other shapes.
 MEASURED_TRAFFIC_PER_GROUP = {
-    ("amazon3m_tail", "fwd"): (138.781440e6 + 341.582592e6) / 16384,
-    ("amazon3m_tail", "dh"): (407.305984e6 + 3.266048e6) / 16384,
+    ("amazon3m_tail", "fwd"): (138.778368e6 + 341.185024e6) / 16384,
+    ("amazon3m_tail", "dh"): (415.697408e6 + 3.247616e6) / 16384,
 }
 
 
