@@ -54,12 +54,10 @@ def _peaks():
 # ------------------------------------------------------------------ work model
 # DRAM bytes per group measured by ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum of one launch / its groups) on the 3M shape at
-# L = 524,288; profiles/k_tc_fwdw_k_tc_dh_amazon3m_L524288.md.  Scaled to a
-# launch by the groups it processes; None for other shapes.
-MEASURED_TRAFFIC_PER_GROUP = {
-    ("amazon3m_tail", "fwd"): (138.778368e6 + 341.185024e6) / 16384,
-    ("amazon3m_tail", "dh"): (415.697408e6 + 3.247616e6) / 16384,
-}
+# L = 524,288 for the kernels as they stand (empty until a capture of the
+# current kernels is taken).  Scaled to a launch by the groups it processes;
+# None for other shapes.
+MEASURED_TRAFFIC_PER_GROUP = {}
 
 
 def algorithmic(w, B, kind, fused_dW=False):

@@ -29,9 +29,17 @@
 // zsw = min(2G, 128) the row width and swz the TMA swizzle of that width.
 // A tile is contiguous (2 Bp G bf16 values per plane pair), so writing it
 // touches one or two pages instead of one page per sample row.
+//
+// Transposed-W workspace (training step only).  Tile k (G F bf16 values at
+// element k G F) holds W_k^T: row f is the G values W_k[0..G)[f], the 16-byte
+// unit of columns 8u .. 8u+7 at logical byte o = 2 G f + 16 u, stored at
+// wt_swz(o) (the 128-byte swizzle over the tile's bytes).  The fused forward
+// kernel writes it from the W_k it already holds in shared memory; the feature
+// gradient then reads each row of its A operand with G/8 16-byte loads.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "sg_internal.cuh"
 #include "tc_ptx.cuh"
@@ -47,9 +55,14 @@ constexpr int kProdWarps = 8;  // cp.async gather + TMA issue (8: measured ~2x t
 // forward / dW: producers, two MMA-issuing warps, epilogue
 constexpr int kFwdThreads = 32 * (kProdWarps + 2 + kEpiWarps);
 constexpr int kFirstEpi = kProdWarps + 2;
-// dh: one load warp, one MMA warp, twelve builder warps (one per lane
-// quarter of each of up to three 128-column tiles)
+// dh: one load warp, one MMA warp, twelve builder warps (one thread per
+// dh column of a band of up to 384)
 constexpr int kDhBuilders = 12;
+constexpr int kDhMaxBuf = 4;  // scattered-W buffers in shared memory
+// groups per pipeline unit (one stage, one scattered-W buffer): a stage's
+// round trip costs about the same from 2 KB to 32 KB of loads, so each stage
+// carries the loads of several groups
+constexpr int kDhP = 2;
 constexpr int kDhThreads = 32 * (2 + kDhBuilders);
 
 // ------------------------------------------------------------------ plans
@@ -70,8 +83,8 @@ struct DWPlan {
 
 struct DhPlan {
     bool ok = false;
-    int MT = 0, S = 0, zsw = 0, nbands = 0, band_w = 0, nmt = 0;
-    uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, tmem_cols = 0;
+    int MT = 0, S = 0, zsw = 0, nbands = 0, band_w = 0, bwt = 0, nbuf = 0;
+    uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, ws_bytes = 0, tmem_cols = 0;
 };
 
 uint32_t pow2_cols(int n)
@@ -91,6 +104,12 @@ bool shape_ok(const sg_layout *lo)
 // dZ rows of a group must fill whole swizzle rows: 16 or 32 columns, or
 // whole chunks of 64
 bool dz_ok(int G) { return G == 16 || G == 32 || G % 64 == 0; }
+
+// 128-byte swizzle of a byte offset inside a transposed-W tile: the 16-byte
+// unit index (bits 4-6) is XORed with the 128-byte line index (bits 7-9), so
+// eight consecutive rows f at the same unit land in eight different bank
+// groups for both the writer (stmatrix) and the reader (dh builders)
+__host__ __device__ __forceinline__ uint32_t wt_swz(uint32_t o) { return o ^ (((o >> 7) & 7u) << 4); }
 
 int stages_for(uint32_t stage_bytes)
 {
@@ -164,22 +183,24 @@ DhPlan plan_dh(const sg_layout *lo, int B, bool split)
     p.zsw = dz_swizzle(lo->G);
     p.z_bytes = (uint32_t)(split ? 2 : 1) * 128 * p.zsw;
     p.w_bytes = (uint32_t)lo->G * lo->F * 2;
-    // TMEM: NMT accumulator tiles of 128 columns plus two A buffers of NMT
-    // tiles of G/2 columns; as many tiles per band as fit (at most 3)
-    int nmt_max = 512 / (128 + lo->G);
-    if (nmt_max > 3)
-        nmt_max = 3;
-    p.nbands = (lo->H + nmt_max * 128 - 1) / (nmt_max * 128);
-    p.nmt = ((lo->H + p.nbands - 1) / p.nbands + 127) / 128;
-    p.band_w = p.nmt * 128;
+    // bands of at most 384 dh columns (TMEM accumulator: 128 samples x band)
+    p.nbands = (lo->H + 383) / 384;
+    p.bwt = ((lo->H + p.nbands - 1) / p.nbands + 127) / 128;
+    p.band_w = p.bwt * 128;
     // the band's slice of the group's inverse map (u8 per dh column)
-    p.i_bytes = (uint32_t)((p.band_w + 1023) / 1024 * 1024);
-    p.stage_bytes = p.z_bytes + p.w_bytes + p.i_bytes;
-    p.tmem_cols = 512;
-    p.S = (int)(kSmemBudget / p.stage_bytes);
+    p.i_bytes = (uint32_t)((p.band_w + 127) / 128 * 128);
+    // one unit = kDhP groups: [dZ x P][W^T x P][inverse-map slices x P]
+    // (whole KB, so that every stage's dZ tiles sit on swizzle-atom boundaries)
+    p.stage_bytes = (kDhP * (p.z_bytes + p.w_bytes + p.i_bytes) + 1023u) & ~1023u;
+    p.ws_bytes = kDhP * (uint32_t)p.band_w * 2 * lo->G;  // one row of G values per dh column
+    p.tmem_cols = pow2_cols(p.band_w);
+    p.nbuf = 2;
+    const long room = (long)kSmemBudget - (long)p.nbuf * p.ws_bytes;
+    p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
     if (p.S > kMaxStages)
         p.S = kMaxStages;
-    p.ok = p.S >= 3;
+    // the flush transposes through 12 x 33 x 32 floats of shared memory
+    p.ok = p.S >= 2 && (long)p.nbuf * p.ws_bytes + (long)p.S * p.stage_bytes >= 12l * 33 * 32 * 4;
     return p;
 }
 
@@ -254,6 +275,12 @@ __device__ __forceinline__ uint32_t pack2(float a, float b)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack2_f16(float a, float b)
+{
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
 __device__ __forceinline__ float lo_half(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_half(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -286,6 +313,27 @@ __device__ __forceinline__ void store_bf16_row(uint16_t *dst, uint16_t *lo, cons
 __device__ __forceinline__ int swz_of(int r, int zsw)
 {
     return zsw == 128 ? (r & 7) : zsw == 64 ? ((r >> 1) & 3) : ((r >> 2) & 1);
+}
+
+// CH values (columns c0 .. c0+CH-1, sample row r) into a group's fp16 dZ
+// tile in global memory (one plane, same unit layout as the bf16 plane 0)
+template <int CH>
+__device__ __forceinline__ void store_dz_tile_f16(uint8_t *tile, int r, int c0, const float (&v)[CH],
+                                                  int zsw, int Bp)
+{
+    const int sw = swz_of(r, zsw);
+    const int u0 = (c0 & 63) >> 3;
+    uint8_t *row = tile + ((size_t)(c0 >> 6) * Bp + r) * zsw;
+#pragma unroll
+    for (int i = 0; i < CH / 8; ++i) {
+        const float *x = v + 8 * i;
+        uint4 q;
+        q.x = pack2_f16(x[0], x[1]);
+        q.y = pack2_f16(x[2], x[3]);
+        q.z = pack2_f16(x[4], x[5]);
+        q.w = pack2_f16(x[6], x[7]);
+        *reinterpret_cast<uint4 *>(row + (((u0 + i) ^ sw) << 4)) = q;
+    }
 }
 
 // CH values (columns c0 .. c0+CH-1, sample row r) into a group's dZ tile:
@@ -905,6 +953,8 @@ constexpr int kFWBce = 8;  // BCE warps: two per TMEM lane quarter
 constexpr int kFWDw = 4;   // dW store warps: one per lane quarter
 constexpr int kFWThreads = 32 * (kProdWarps + 2 + kFWBce + kFWDw);
 constexpr int kFWFirstEpi = kProdWarps + 2;
+// dynamic shared memory the fused plan may use (the opt-in maximum is 227 KB)
+constexpr int kFWBudget = 224 * 1024;
 
 struct FWPlan {
     bool ok = false;
@@ -941,7 +991,8 @@ FWPlan plan_fwdw(const sg_layout *lo, int B)
     p.tmem_cols = pow2_cols(p.nslot * (p.zcols + p.wcols));
     // F = 64: the last stage's dW MMA reads up to 8 KB past it
     p.pad_bytes = lo->F < 128 ? 8192u : 0u;
-    const long room = (long)kSmemBudget - 2l * p.dz_bytes - 2l * p.stg_bytes - (long)p.pad_bytes;
+    // two dW_k staging buffers and two W_k^T staging buffers (same size)
+    const long room = (long)kFWBudget - 2l * p.dz_bytes - 4l * p.stg_bytes - (long)p.pad_bytes;
     p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
     if (p.S > 6)
         p.S = 6;
@@ -954,6 +1005,8 @@ struct FWArgs {
     uint8_t *dZt;
     uint64_t tile_bytes;
     uint16_t *dW;
+    uint16_t *Wt;     // transposed-W workspace
+    uint32_t *wmax;   // max |W| (bf16 magnitude bits) over the step, for dh
     const int32_t *gptr, *gent;
     double *loss_part;
     int32_t *status;
@@ -989,9 +1042,10 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
-    // [dZ_k buffer 0][dZ_k buffer 1][dW_k staging 0][dW_k staging 1][stages]
+    // [dZ_k buffer 0][dZ_k buffer 1][dW_k staging 0, 1][W_k^T staging 0, 1][stages]
     const uint32_t stg0 = base + 2 * a.dz_bytes;
-    const uint32_t stage0 = stg0 + 2 * a.stg_bytes;
+    const uint32_t wtstg0 = stg0 + 2 * a.stg_bytes;
+    const uint32_t stage0 = wtstg0 + 2 * a.stg_bytes;
     constexpr int G = G_;
     const int F = a.F, S = a.S, NS = a.nslot;
     constexpr uint32_t zrows = (uint32_t)MT * 128;
@@ -999,9 +1053,10 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     const uint32_t wbase = (uint32_t)NS * a.zcols;  // first dW accumulator column
 
     // the epilogue is two teams: the BCE warps turn Z_k into dZ_k, the dW
-    // warps store dW of the group
+    // warps store dW of the group and W_k^T.  A stage is freed by the dW MMA
+    // (last reader of H_k) and by the dW warps (last readers of W_k).
     if (threadIdx.x == 0) {
-        setup_ctl(c, S, 0, kProdWarps * 32 + 1, 1);
+        setup_ctl(c, S, 0, kProdWarps * 32 + 1, 2);
         for (int i = 0; i < NS && i < 4; ++i) {
             mbar_init(bar_addr(c.tfull[i]), 1);
             mbar_init(bar_addr(c.tempty[i]), kFWBce * 32);
@@ -1010,8 +1065,8 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(cf.dzfull[i]), kFWBce * 32);
-            // freed by the dW MMA (commit) and by the end of the tile's store read
-            mbar_init(bar_addr(cf.dzempty[i]), 2);
+            // freed by the dW MMA (commit)
+            mbar_init(bar_addr(cf.dzempty[i]), 1);
             mbar_init(bar_addr(cf.wdrain[i]), 1);
         }
         fence_mbar_init();
@@ -1094,15 +1149,6 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             if (lane == 0) {
                 const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
                 const uint32_t Zs = base + (uint32_t)db * a.dz_bytes;
-                // dZ_k goes to the workspace with one bulk store of the shared
-                // tile; the previous group's store has read its buffer once
-                // this returns, which frees that buffer (with its MMA commit)
-                if (it > 0) {
-                    bulk_wait_read<0>();
-                    mbar_arrive(bar_addr(cf.dzempty[db ^ 1]));
-                }
-                bulk_store(a.dZt + (size_t)k * a.tile_bytes, Zs, a.dz_bytes);
-                bulk_commit();
 #pragma unroll
                 for (int tf = 0; tf < (FK + 7) / 8; ++tf) {
                     const uint32_t d = tbase + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G);
@@ -1121,10 +1167,8 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             }
             __syncwarp();
         }
-        if (lane == 0) {
+        if (lane == 0)
             mma_commit(bar_addr(cf.wdrain[0]));
-            bulk_wait<0>();  // every dZ tile store has landed
-        }
         __syncwarp();
         mbar_wait_drain(bar_addr(cf.wdrain[0]), 0);
     } else {
@@ -1173,7 +1217,10 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                         for (int i = 0; i < CH; ++i)
                             v[i] = 0.f;
                     }
+                    // bf16 value + residual planes for the dW MMA; the fp16
+                    // tile for the feature gradient straight to the workspace
                     store_dz_tile<CH>(zs_smem, b, c0, v, ZSW, NZC, MT * 128);
+                    store_dz_tile_f16<CH>(a.dZt + (size_t)k * a.tile_bytes, b, c0, v, ZSW, MT * 128);
                 }
                 tc_fence_before();
                 mbar_arrive(bar_addr(c.tempty[zs]));
@@ -1183,20 +1230,61 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             epi_sum_to(lacc, c, a.loss_part + blockIdx.x, kFWFirstEpi);
         } else {
             // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
-            // staged in shared memory as [j][f] and stored with one bulk copy
+            // staged in shared memory as [j][f] and stored with one bulk copy.
+            // Before that, W_k of the stage is transposed into the W^T tile
+            // (8x8 blocks: ldmatrix.trans from the TMA layout, stmatrix into
+            // the swizzled [f][j] rows) and stored the same way.  The elected
+            // thread's bulk groups alternate W^T, dW: a staging buffer of two
+            // groups ago has been read once at most three groups are pending.
             const int dw = ew - kFWBce;  // 0 .. kFWDw-1
             constexpr int wunits = ((FK + 7) / 8) * (G / CH);
+            constexpr int JB = G / 8;                // 8-row blocks of j
+            constexpr int XPW = (JB * 2 * FK) / 16;  // ldmatrix.x4 per warp (4 blocks each)
+            uint32_t wmag = 0;  // running max of |W| bits, two bf16 lanes
             int it = 0;
             for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+                const int s = it % S;
                 const int ws = it % NS;
                 const int wb = it & 1;
                 uint16_t *stg = reinterpret_cast<uint16_t *>(base_ptr + 2 * (size_t)a.dz_bytes + (size_t)wb * a.stg_bytes);
+                // ---- W_k -> W_k^T
+                if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
+                    break;
+                if (dw == 0 && lane == 0)
+                    bulk_wait_read<3>();
+                named_bar(2, kFWDw * 32);
+                const uint32_t Ws = stage0 + (uint32_t)s * a.stage_bytes + a.a_bytes;
+                const uint32_t T = wtstg0 + (uint32_t)wb * a.stg_bytes;
+#pragma unroll
+                for (int x = 0; x < XPW; ++x) {
+                    const int blk = 4 * (x * kFWDw + dw) + (lane >> 3), r = lane & 7;
+                    const int jb = blk % JB, fb = blk / JB;
+                    const int j = jb * 8 + r;
+                    // row j of the 8x8 block: 8 f of the 64-f TMA box fb / 8
+                    const uint32_t src = Ws + (uint32_t)(fb >> 3) * G * 128 + (uint32_t)j * 128 +
+                                         ((uint32_t)((fb & 7) ^ (j & 7)) << 4);
+                    // row f = 8 fb + r of the block: its 8 j at unit jb
+                    const uint32_t o = (uint32_t)(fb * 8 + r) * (2 * G) + (uint32_t)jb * 16;
+                    uint32_t v[4];
+                    ldmatrix_x4_trans(src, v);
+                    stmatrix_x4(T + wt_swz(o), v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        wmag = __vmaxu2(wmag, v[e] & 0x7fff7fffu);
+                }
+                fence_proxy_async();  // staged W_k^T -> the bulk store (async proxy)
+                named_bar(2, kFWDw * 32);
+                if (dw == 0 && lane == 0) {
+                    mbar_arrive(bar_addr(c.empty[s]));  // done with the stage's W_k
+                    bulk_store(a.Wt + k * G * F, T, a.stg_bytes);
+                    bulk_commit();
+                }
+                // ---- dW_k
                 if (!mbar_wait(bar_addr(cf.wfull[ws]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
                     break;
                 tc_fence_after();
-                // the staging buffer's store of two groups ago has read it
                 if (dw == 0 && lane == 0)
-                    bulk_wait_read<1>();
+                    bulk_wait_read<3>();
                 named_bar(2, kFWDw * 32);
 #pragma unroll 1
                 for (int u = 0; u < wunits; ++u) {
@@ -1220,8 +1308,13 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     bulk_commit();
                 }
             }
+            wmag = max(wmag & 0xffffu, wmag >> 16);
+            for (int o = 16; o > 0; o >>= 1)
+                wmag = max(wmag, __shfl_xor_sync(0xffffffffu, wmag, o));
+            if (lane == 0)
+                atomicMax(a.wmax, wmag);
             if (dw == 0 && lane == 0)
-                bulk_wait<0>();  // every dW store has landed
+                bulk_wait<0>();  // every dW and W^T store has landed
         }
     }
     tc_fence_before();
@@ -1236,59 +1329,84 @@ __global__ void __launch_bounds__(kFWThreads, 1)
 struct DhArgs {
     const uint8_t *invmap;  // [K][Hp]: f with I_k[f] = i, 0xff where none
     int64_t Hp;
-    const uint16_t *W;     // [L][F] in slot order
+    const uint16_t *Wt;    // transposed-W workspace (tile k = W_k^T, swizzled)
+    const uint32_t *wmax;  // max |W| bits of the step (fp16 operands only)
     const uint8_t *dZt;    // group-tiled dZ input (else the tensor maps)
     uint64_t tile_bytes;
     float *dh;
     int32_t *status;
-    int64_t K, L;
-    int32_t B, G, F, H, MT, S, zsw, nbands, band_w, parts, npass, Bp;
-    uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, tmem_cols;
+    int64_t K, L, Kc;      // Kc: groups per CTA (a contiguous range)
+    int32_t B, G, F, H, MT, S, zsw, nbands, band_w, parts, npass, Bp, nbuf;
+    uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, ws_bytes, tmem_cols;
 };
 
 constexpr int kDhFirstEpi = 2;  // warp 0: loads, warp 1: MMA, then the builders
 
-// CTA (band, mtile, part): dh columns [i0, i0 + 128 NMT) of the band, samples
-// [128 mt, 128 mt + 128), groups k = part, part + parts, ...
+struct CtlDh {
+    Ctl c;                                           // stages, drain
+    uint64_t wfull[kDhMaxBuf], wempty[kDhMaxBuf];    // scattered-W buffers
+};
+
+// CTA (band, mtile, part): dh columns [i0, i0 + BW) of the band (BW = 128 BWT),
+// samples [128 mt, 128 mt + 128), the contiguous groups [Kc part, Kc part + Kc).
 //
 // The scatter-add of dH_k = dZ_k W_k into the columns I_k of dh is itself a
-// product, taken transposed:
-//     dh[:, band]^T += Ws_k^T dZ_k^T,   Ws_k^T[i - i0][j] = W_k[j][f] where I_k[f] = i
-// (zero rows elsewhere).  The accumulator (M = 128 dh columns per tile, N = 128
-// samples) stays in TMEM over all the CTA's groups.  Ws_k^T is the MMA's A
-// operand and lives in TMEM too: eight builder warps write every one of its
-// rows each group (W_k's column f, or zeros) with tcgen05.st, so nothing has
-// to be cleared and no shared memory is spent on it; B is the group's dZ tile
-// (K-major, rows = samples) as it arrives in shared memory.
+// product:
+//     dh[:, band] += dZ_k Ws_k,   Ws_k[j][i - i0] = W_k[j][f] where I_k[f] = i
+// (zero columns elsewhere).  The accumulator (M = 128 samples, N = BW dh
+// columns: one MMA of N = 256 and one of N = 128 per K step at BW = 384) stays
+// in TMEM over all the CTA's groups and is added to dh once at the end.  A is
+// the group's dZ tile (K-major, rows = samples) as it arrives in shared
+// memory; B = Ws_k^T (K-major, one 2G-byte row per dh column) is written into
+// shared memory by the builder warps -- every row, row f of the staged W_k^T
+// tile or zeros.  Loads, builders and MMAs move in units of kDhP groups: one
+// stage and one Ws buffer per unit.
 //
-// Compile-time shape: NPASS dZ planes, NKS = G/16 K steps per plane, NMT
-// tiles of 128 dh columns per band (fully unrolled MMA issue).
-template <int NPASS, int NKS, int NMT>
+// Compile-time shape: NPASS dZ planes, NKS = G/16 K steps per plane, BWT
+// 128-column blocks per band.  F16: dZ is one fp16 plane (the training step's
+// workspace) and the builders write W_k as fp16, scaled by 2^-s so that the
+// step's largest |W| stays finite (s = 0 unless |W| >= 2^15); the flush
+// scales the sums back by 2^s.
+template <int NPASS, int NKS, int BWT, bool F16>
 __global__ void __launch_bounds__(kDhThreads, 1)
     k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
             const DhArgs a)
 {
-    constexpr int ACOLS = NKS * 8;  // 32-bit TMEM columns of one A tile (G bf16 per row)
-    constexpr uint32_t kA = NMT * 128;  // first A column; D occupies [0, 128 NMT)
-    __shared__ Ctl c;
+    static_assert(!F16 || NPASS == 1, "the fp16 dZ workspace has one plane");
+    constexpr int G = NKS * 16;
+    constexpr int RB = 2 * G;         // bytes of one Ws row (one dh column)
+    constexpr int BW = BWT * 128;     // dh columns of the band
+    constexpr int N0 = BW > 256 ? 256 : BW;
+    constexpr int N1 = BW - N0;       // 0 or 128
+    constexpr int NCW = G / 8;        // 16-byte units of a row
+    constexpr int P = kDhP;
+    static_assert(BW <= kDhBuilders * 32, "one builder thread per dh column");
+    __shared__ CtlDh cd;
+    Ctl &c = cd.c;
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-    const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
-    uint8_t *stage0_ptr = dsm + (stage0 - smem_u32(dsm));
-    const int G = a.G, F = a.F, S = a.S;
+    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+    uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
+    // [Ws buffers][stages]; a stage: [dZ x P][W^T x P][inverse-map slices x P]
+    const uint32_t stage0 = base + (uint32_t)a.nbuf * a.ws_bytes;
+    uint8_t *stage0_ptr = base_ptr + (size_t)a.nbuf * a.ws_bytes;
+    const int F = a.F, S = a.S, NB = a.nbuf;
+    const uint32_t zoff = 0, woff = P * a.z_bytes, ioff = P * (a.z_bytes + a.w_bytes);
     const int band = blockIdx.x % a.nbands;
     const int mt = (blockIdx.x / a.nbands) % a.MT;
     const int part_id = blockIdx.x / (a.nbands * a.MT);
-    const int i0 = band * a.band_w;
-    const uint32_t zchunk = 128u * (uint32_t)a.zsw;  // one plane of the stage (G <= 64)
+    const int i0 = band * BW;
+    const uint32_t zchunk = 128u * (uint32_t)a.zsw;  // one plane of one group (G <= 64)
+    const int64_t kbeg = (int64_t)part_id * a.Kc;
+    const int64_t kend = kbeg + a.Kc < a.K ? kbeg + a.Kc : a.K;
 
     // stages: full = loads landed; empty = the MMAs (and builders) are done
-    // with them.  tfull/tempty[0..1] = A buffer written / consumed.
+    // with them.  wfull/wempty: Ws buffer written / consumed.
     if (threadIdx.x == 0) {
         setup_ctl(c, S, 0, 1, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(c.tfull[i]), kDhBuilders * 32);
-            mbar_init(bar_addr(c.tempty[i]), 1);
+        for (int i = 0; i < NB && i < kDhMaxBuf; ++i) {
+            mbar_init(bar_addr(cd.wfull[i]), kDhBuilders);  // one arrival per builder warp
+            mbar_init(bar_addr(cd.wempty[i]), 1);
         }
         fence_mbar_init();
     }
@@ -1305,31 +1423,34 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         int it = 0;
-        for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
+        for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it) {
             const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
-            if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
+            const int np = kend - k0 < P ? (int)(kend - k0) : P;
+            if (!mbar_wait(bar_addr(c.empty[s]), ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, a.status))
                 break;
-            const uint32_t Zs = stage0 + (uint32_t)s * a.stage_bytes;
-            const uint32_t Wt = Zs + a.z_bytes;
-            const uint32_t Is = Wt + a.w_bytes;
+            const uint32_t st = stage0 + (uint32_t)s * a.stage_bytes;
             const uint32_t fb = bar_addr(c.full[s]);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(fb, a.z_bytes + a.w_bytes + (uint32_t)a.band_w);
+            if (lane == 0)
+                mbar_arrive_expect_tx(fb, (uint32_t)np * (a.z_bytes + a.w_bytes + (uint32_t)BW));
+            __syncwarp();
+            if (lane < np) {
+                // lane g loads group k0 + g
+                const int64_t k = k0 + lane;
+                const uint32_t Zs = st + zoff + (uint32_t)lane * a.z_bytes;
                 if (a.dZt) {
                     // rows [128 mt, 128 mt + 128) of each plane of the tile
-                    const uint8_t *t = a.dZt + (size_t)k * a.tile_bytes + (size_t)mt * zchunk;
+                    const uint8_t *tz = a.dZt + (size_t)k * a.tile_bytes + (size_t)mt * zchunk;
                     for (int pl = 0; pl < NPASS; ++pl)
-                        bulk_load(Zs + (uint32_t)pl * zchunk, t + (size_t)pl * a.Bp * a.zsw, zchunk, fb);
+                        bulk_load(Zs + (uint32_t)pl * zchunk, tz + (size_t)pl * a.Bp * a.zsw, zchunk, fb);
                 } else {
                     tma_load_2d(Zs, &tm_z, (int)(k * G), mt * 128, fb);
                     if (NPASS > 1)
                         tma_load_2d(Zs + zchunk, &tm_zl, (int)(k * G), mt * 128, fb);
                 }
-                // W_k: G contiguous rows of F, read row-major by the builders
-                bulk_load(Wt, a.W + k * G * F, a.w_bytes, fb);
+                // W_k^T: F swizzled rows of G, one per f
+                bulk_load(st + woff + (uint32_t)lane * a.w_bytes, a.Wt + k * G * F, a.w_bytes, fb);
                 // which f lands on each dh column of the band
-                bulk_load(Is, a.invmap + k * a.Hp + i0, (uint32_t)a.band_w, fb);
+                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.invmap + k * a.Hp + i0, (uint32_t)BW, fb);
             }
             __syncwarp();
         }
@@ -1337,34 +1458,52 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
         const uint32_t zlayout = layout_for_swizzle(a.zsw);
-        const uint32_t idesc = idesc_bf16(128, 128, 0, 0);  // M = 128 dh columns, N = 128 samples
-        int it = 0;
-        for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
+        constexpr uint32_t wlayout = layout_for_swizzle(RB);
+        constexpr uint32_t id0 = F16 ? idesc_f16(128, N0, 0, 0) : idesc_bf16(128, N0, 0, 0);
+        constexpr uint32_t id1 = N1 == 0 ? 0u : F16 ? idesc_f16(128, N1 > 0 ? N1 : 16, 0, 0)
+                                                     : idesc_bf16(128, N1 > 0 ? N1 : 16, 0, 0);
+        int it = 0, buf = 0;
+        uint32_t wph = 0;
+        for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it) {
             const int s = it % S;
-            const int buf = it & 1;
+            const int np = kend - k0 < P ? (int)(kend - k0) : P;
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
-            if (!mbar_wait(bar_addr(c.tfull[buf]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(cd.wfull[buf]), wph, abort_flag, a.status))
                 break;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t Zs = stage0 + (uint32_t)s * a.stage_bytes;
+                const uint32_t st = stage0 + (uint32_t)s * a.stage_bytes;
+                const uint32_t Wb = base + (uint32_t)buf * a.ws_bytes;
 #pragma unroll
-                for (int mi = 0; mi < NMT; ++mi) {
+                for (int g = 0; g < P; ++g) {
+                    if (g < np) {
+                        const uint32_t Zs = st + zoff + (uint32_t)g * a.z_bytes;
+                        const uint32_t Ws = Wb + (uint32_t)(g * BW * RB);
 #pragma unroll
-                    for (int ks2 = 0; ks2 < NPASS * NKS; ++ks2) {
-                        const int ks = ks2 % NKS;
-                        // B: dZ plane ks2 / NKS, K-major (rows = samples), 16 j per step
-                        const uint64_t bd = sdesc(Zs + (uint32_t)(ks2 / NKS) * zchunk + (uint32_t)ks * 32, 16,
-                                                  8 * a.zsw, zlayout);
-                        const uint32_t at = tbase + kA + (uint32_t)((buf * NMT + mi) * ACOLS + ks * 8);
-                        mma_bf16_ta(tbase + (uint32_t)(mi * 128), at, bd, idesc, (it > 0 || ks2 > 0) ? 1u : 0u);
+                        for (int ks2 = 0; ks2 < NPASS * NKS; ++ks2) {
+                            const int ks = ks2 % NKS;
+                            const uint32_t acc = (it > 0 || g > 0 || ks2 > 0) ? 1u : 0u;
+                            // A: dZ plane ks2 / NKS (rows = samples), 16 j per step
+                            const uint64_t ad = sdesc(Zs + (uint32_t)(ks2 / NKS) * zchunk + (uint32_t)ks * 32, 16,
+                                                      8 * a.zsw, zlayout);
+                            // B: Ws rows (dh columns), the same 16 j
+                            mma_bf16(tbase, ad, sdesc(Ws + (uint32_t)ks * 32, 16, 8 * RB, wlayout), id0, acc);
+                            if (N1 > 0)
+                                mma_bf16(tbase + (uint32_t)N0, ad,
+                                         sdesc(Ws + (uint32_t)(N0 * RB) + (uint32_t)ks * 32, 16, 8 * RB, wlayout),
+                                         id1, acc);
+                        }
                     }
                 }
-                mma_commit(bar_addr(c.tempty[buf]));
+                mma_commit(bar_addr(cd.wempty[buf]));
                 mma_commit(bar_addr(c.empty[s]));
             }
             __syncwarp();
+            if (++buf == NB) {
+                buf = 0;
+                wph ^= 1u;
+            }
         }
         if (lane == 0)
             mma_commit(bar_addr(c.drain[0]));
@@ -1372,58 +1511,98 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         mbar_wait_drain(bar_addr(c.drain[0]), 0);  // no MMA in flight at the dealloc
     } else {
         // ---------------------------------------------------------- builders
-        // warp (q, sub) writes the A rows of lane quarter q of tile sub
-        const int ew = warp - kDhFirstEpi;  // 0 .. kDhBuilders-1
-        const int q = warp & 3, sub = ew / 4;
-        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        int it = 0;
-        for (int64_t k = part_id; k < a.K; k += a.parts, ++it) {
+        // thread t writes the Ws rows of dh column i0 + t (one per group)
+        const int tb = threadIdx.x - kDhFirstEpi * 32;  // 0 .. 383
+        const int q = warp & 3, sub = (warp - kDhFirstEpi) / 4;
+        float down = 1.f, up = 1.f;  // 2^-s, 2^s (fp16 operands)
+        if (F16) {
+            const uint32_t m = __ldg(a.wmax);
+            const int e = (int)(m >> 7) - 127;  // exponent of the largest |W|
+            const int sh = (m < 0x7f80u && e > 14) ? e - 14 : 0;
+            down = __uint_as_float((uint32_t)(127 - sh) << 23);
+            up = __uint_as_float((uint32_t)(127 + sh) << 23);
+        }
+        const int sw = swz_of(tb, RB);
+        int it = 0, buf = 0;
+        uint32_t wph = 0;
+        for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it) {
             const int s = it % S;
-            const int buf = it & 1;
+            const int np = kend - k0 < P ? (int)(kend - k0) : P;
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
-            const uint8_t *Wt = stage0_ptr + (size_t)s * a.stage_bytes + a.z_bytes;
-            const uint16_t *Wrow = reinterpret_cast<const uint16_t *>(Wt);  // [G][F], row-major
-            const uint8_t *inv = Wt + a.w_bytes;  // band's inverse map
-            // the A buffer's last group must be through its MMA before it is rewritten
-            if (!mbar_wait(bar_addr(c.tempty[buf]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
-                break;
-            tc_fence_after();
-            for (int mi = sub; mi < NMT; mi += kDhBuilders / 4) {
-                // the f (if any) that lands on this lane's dh column
-                const uint32_t f = inv[mi * 128 + q * 32 + lane];
-                uint32_t av[ACOLS];
+            const uint8_t *st = stage0_ptr + (size_t)s * a.stage_bytes;
+            // the rows are read from the stage before waiting for the buffer
+            uint4 row[P][NCW];
 #pragma unroll
-                for (int cc = 0; cc < ACOLS; ++cc)
-                    av[cc] = 0u;
-                if (f != 0xffu) {
+            for (int g = 0; g < P; ++g) {
 #pragma unroll
-                    for (int cc = 0; cc < ACOLS; ++cc)
-                        av[cc] = (uint32_t)Wrow[(2 * cc) * F + f] | ((uint32_t)Wrow[(2 * cc + 1) * F + f] << 16);
-                }
-                tmem_st<ACOLS>(tbase + lane_off + kA + (uint32_t)((buf * NMT + mi) * ACOLS), av);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar_addr(c.tfull[buf]));
-        }
-        // the accumulator holds this CTA's partial of dh[:, band]^T: add it in
-        if (mbar_wait(bar_addr(c.drain[0]), 0, abort_flag, a.status) && !*abort_flag && it > 0) {
-            tc_fence_after();
-            for (int mi = sub; mi < NMT; mi += kDhBuilders / 4) {
-                const int i = i0 + mi * 128 + q * 32 + lane;  // this lane's dh column
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tbase + lane_off + (uint32_t)(mi * 128 + c0), r);
-                    tmem_ld_wait();
-                    if (i < a.H) {
+                for (int u = 0; u < NCW; ++u)
+                    row[g][u] = make_uint4(0u, 0u, 0u, 0u);
+                if (tb < BW && g < np) {
+                    const uint8_t *Wt = st + woff + (size_t)g * a.w_bytes;  // W_k^T tile
+                    const uint32_t f = st[ioff + (size_t)g * a.i_bytes + tb];  // f (if any) of this dh column
+                    if (f != 0xffu) {
 #pragma unroll
-                        for (int x = 0; x < 32; ++x) {
-                            const int b = mt * 128 + c0 + x;
-                            if (b < a.B)
-                                atomicAdd(a.dh + (int64_t)b * a.H + i, __uint_as_float(r[x]));
+                        for (int u = 0; u < NCW; ++u) {
+                            uint4 w = *reinterpret_cast<const uint4 *>(Wt + wt_swz(f * (uint32_t)RB + 16u * u));
+                            if (F16) {
+                                w.x = pack2_f16(lo_half(w.x) * down, hi_half(w.x) * down);
+                                w.y = pack2_f16(lo_half(w.y) * down, hi_half(w.y) * down);
+                                w.z = pack2_f16(lo_half(w.z) * down, hi_half(w.z) * down);
+                                w.w = pack2_f16(lo_half(w.w) * down, hi_half(w.w) * down);
+                            }
+                            row[g][u] = w;
                         }
                     }
+                }
+            }
+            // the buffer's last unit must be through its MMAs before it is rewritten
+            if (!mbar_wait(bar_addr(cd.wempty[buf]), wph ^ 1u, abort_flag, a.status))
+                break;
+            if (tb < BW) {
+#pragma unroll
+                for (int g = 0; g < P; ++g) {
+                    uint8_t *dst = base_ptr + (size_t)buf * a.ws_bytes + (size_t)(g * BW + tb) * RB;
+#pragma unroll
+                    for (int u = 0; u < NCW; ++u)
+                        *reinterpret_cast<uint4 *>(dst + ((u ^ sw) << 4)) = row[g][u];
+                }
+            }
+            fence_proxy_async();  // Ws rows (generic writes) -> the MMA (async proxy)
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_addr(cd.wfull[buf]));
+            if (++buf == NB) {
+                buf = 0;
+                wph ^= 1u;
+            }
+        }
+        // the accumulator (lanes = samples, columns = the band's dh columns)
+        // holds this CTA's partial: add it in, transposed through shared memory
+        // (free once every MMA is done) so that the atomics run along dh rows
+        if (mbar_wait(bar_addr(c.drain[0]), 0, abort_flag, a.status) && !*abort_flag && it > 0) {
+            tc_fence_after();
+            float *tr = reinterpret_cast<float *>(base_ptr) + (size_t)(warp - kDhFirstEpi) * 33 * 32;
+            const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+            for (int cs = sub; cs < BWT; cs += kDhBuilders / 4) {
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + lane_off + (uint32_t)(cs * 128 + c0), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        tr[lane * 33 + x] = __uint_as_float(r[x]);
+                    __syncwarp();
+                    const int i = i0 + cs * 128 + c0 + lane;  // this lane's dh column
+                    if (i < a.H) {
+                        for (int y = 0; y < 32; ++y) {
+                            const int b = mt * 128 + q * 32 + y;
+                            if (b < a.B)
+                                atomicAdd(a.dh + (int64_t)b * a.H + i, F16 ? tr[y * 33 + lane] * up
+                                                                           : tr[y * 33 + lane]);
+                        }
+                    }
+                    __syncwarp();
                 }
             }
         }
@@ -1545,7 +1724,7 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
 bool tc_fwdw_ok(const sg_layout *lo, int32_t B) { return plan_fwdw(lo, B).ok; }
 
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
-                  double *loss, cudaStream_t st)
+                  uint16_t *Wt, double *loss, cudaStream_t st)
 {
     const FWPlan p = plan_fwdw(lo, B);
     if (!p.ok) {
@@ -1559,9 +1738,15 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     FWArgs a;
     a.idx_s = lo->idx_s;
     a.hT = lo->hT;
+    if (!Wt || !lo->wmax) {
+        sg_set_error("tc_fwdw: the transposed-W workspace is not allocated");
+        return SG_ERR_INVALID;
+    }
     a.dZt = dZt;
-    a.tile_bytes = tc_dz_tile_bytes(lo, B);
+    a.tile_bytes = tc_dz_tile_bytes(lo, B) / 2;  // one fp16 plane
     a.dW = dW;
+    a.Wt = Wt;
+    a.wmax = lo->wmax;
     a.gptr = lo->gptr;
     a.gent = lo->gent;
     a.loss_part = lo->loss_part;
@@ -1589,7 +1774,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.wcols = p.wcols;
     a.tmem_cols = p.tmem_cols;
     const size_t smem =
-        2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
+        2 * (size_t)p.dz_bytes + 4 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
 #define SG_FW_PICK(GG, KK, MM)                                           \
@@ -1608,6 +1793,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
+    SG_TRY_CUDA(cudaMemsetAsync(lo->wmax, 0, sizeof(uint32_t), st));
     SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, kFWThreads, smem, st>>>(tm_w, a));
     SG_TRY_CUDA(cudaGetLastError());
     return sg_loss_finalize(lo, grid, loss, st);
@@ -1683,6 +1869,22 @@ __global__ void k_invmap(const uint16_t *__restrict__ idx_s, int64_t K, int F, i
         map[k * Hp + idx_s[k * F + f]] = (uint8_t)f;
 }
 
+sg_status tc_ensure_wt(sg_layout *lo)
+{
+    if (lo->wt_ws)
+        return SG_OK;
+    // the W^T tiles, then one word: max |W| bits of the step
+    const size_t bytes = (size_t)lo->L * lo->F * 2;
+    if (cudaMalloc((void **)&lo->wt_ws, bytes + 16) != cudaSuccess) {
+        cudaGetLastError();
+        lo->wt_ws = nullptr;
+        sg_set_error("cudaMalloc of %zu bytes for the transposed-W workspace failed", bytes + 16);
+        return SG_ERR_OOM;
+    }
+    lo->wmax = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(lo->wt_ws) + bytes);
+    return SG_OK;
+}
+
 sg_status ensure_invmap(sg_layout *lo, int band_w, cudaStream_t st)
 {
     if (lo->invmap)
@@ -1703,10 +1905,31 @@ sg_status ensure_invmap(sg_layout *lo, int band_w, cudaStream_t st)
     return SG_OK;
 }
 
-sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
-                int32_t B, const uint16_t *W, float *dh, cudaStream_t st)
+// W_k^T tiles from W for the callers whose step did not write them
+__global__ void k_wt_transpose(const uint16_t *__restrict__ W, int64_t K, int G, int F, uint16_t *__restrict__ Wt)
 {
-    const bool split = dZ_lo != nullptr || dZt != nullptr;
+    const int units = F * G / 8;  // 16-byte units of a tile
+    for (int64_t k = blockIdx.x; k < K; k += gridDim.x) {
+        const uint16_t *Wk = W + k * G * F;
+        uint8_t *T = reinterpret_cast<uint8_t *>(Wt + k * G * F);
+        for (int e = threadIdx.x; e < units; e += blockDim.x) {
+            const int f = e % F, u = e / F;  // consecutive threads: consecutive f
+            uint32_t w[4];
+            for (int x = 0; x < 4; ++x)
+                w[x] = (uint32_t)Wk[(8 * u + 2 * x) * F + f] | ((uint32_t)Wk[(8 * u + 2 * x + 1) * F + f] << 16);
+            *reinterpret_cast<uint4 *>(T + wt_swz((uint32_t)(f * 2 * G + 16 * u))) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
+                bool dzt_f16, int32_t B, const uint16_t *W, const uint16_t *Wt, float *dh, cudaStream_t st)
+{
+    if (dzt_f16 && (!dZt || !Wt)) {
+        sg_set_error("tc_dh: the fp16 dZ workspace comes with the step's W^T tiles");
+        return SG_ERR_INVALID;
+    }
+    const bool split = dZ_lo != nullptr || (dZt != nullptr && !dzt_f16);
     const DhPlan p = plan_dh(lo, B, split);
     if (!p.ok) {
         sg_set_error("tc_dh: shape not supported by the tensor-core engine");
@@ -1734,12 +1957,21 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     rc = ensure_invmap(lo, p.band_w, st);
     if (rc != SG_OK)
         return rc;
+    if (!Wt) {
+        rc = tc_ensure_wt(lo);
+        if (rc != SG_OK)
+            return rc;
+        k_wt_transpose<<<persistent_grid(lo, lo->K) * 4, 256, 0, st>>>(W, lo->K, lo->G, lo->F, lo->wt_ws);
+        SG_TRY_CUDA(cudaGetLastError());
+        Wt = lo->wt_ws;
+    }
     DhArgs a;
     a.invmap = lo->invmap;
     a.Hp = lo->invmap_hp;
-    a.W = W;
+    a.Wt = Wt;
+    a.wmax = lo->wmax;
     a.dZt = dZt;
-    a.tile_bytes = tc_dz_tile_bytes(lo, B);
+    a.tile_bytes = dzt_f16 ? tc_dz_tile_bytes(lo, B) / 2 : tc_dz_tile_bytes(lo, B);
     a.dh = dh;
     a.status = lo->status;
     a.K = lo->K;
@@ -1758,32 +1990,40 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     int parts = lo->num_sms / (p.nbands * p.MT);
     if (parts < 1)
         parts = 1;
-    if (parts > lo->K)
-        parts = (int)lo->K;
+    // contiguous ranges of whole units of groups
+    int64_t kc = (lo->K + parts - 1) / parts;
+    kc = (kc + kDhP - 1) / kDhP * kDhP;
+    parts = (int)((lo->K + kc - 1) / kc);
     a.parts = parts;
+    a.Kc = kc;
     a.z_bytes = p.z_bytes;
     a.w_bytes = p.w_bytes;
     a.i_bytes = p.i_bytes;
     a.stage_bytes = p.stage_bytes;
+    a.ws_bytes = p.ws_bytes;
+    a.nbuf = p.nbuf;
     a.tmem_cols = p.tmem_cols;
-    // kernel instance for (planes, K steps per plane, tiles per band)
+    // kernel instance for (planes, K steps per plane, 128-column blocks per band)
     void (*kern)(CUtensorMap, CUtensorMap, DhArgs) = nullptr;
     const int nks = lo->G / 16;
-#define SG_DH_PICK(P, K, N)                                   \
-    if (a.npass == P && nks == K && p.nmt == N)               \
-        kern = k_tc_dh<P, K, N>;
-    SG_DH_PICK(1, 1, 1) SG_DH_PICK(1, 1, 2) SG_DH_PICK(1, 1, 3)
-    SG_DH_PICK(1, 2, 1) SG_DH_PICK(1, 2, 2) SG_DH_PICK(1, 2, 3)
-    SG_DH_PICK(1, 4, 1) SG_DH_PICK(1, 4, 2)
-    SG_DH_PICK(2, 1, 1) SG_DH_PICK(2, 1, 2) SG_DH_PICK(2, 1, 3)
-    SG_DH_PICK(2, 2, 1) SG_DH_PICK(2, 2, 2) SG_DH_PICK(2, 2, 3)
-    SG_DH_PICK(2, 4, 1) SG_DH_PICK(2, 4, 2)
+#define SG_DH_PICK(P, K, N, H16)                                          \
+    if (a.npass == P && nks == K && p.bwt == N && dzt_f16 == H16)         \
+        kern = k_tc_dh<P, K, N, H16>;
+    SG_DH_PICK(1, 1, 1, false) SG_DH_PICK(1, 1, 2, false) SG_DH_PICK(1, 1, 3, false)
+    SG_DH_PICK(1, 2, 1, false) SG_DH_PICK(1, 2, 2, false) SG_DH_PICK(1, 2, 3, false)
+    SG_DH_PICK(1, 4, 1, false) SG_DH_PICK(1, 4, 2, false) SG_DH_PICK(1, 4, 3, false)
+    SG_DH_PICK(2, 1, 1, false) SG_DH_PICK(2, 1, 2, false) SG_DH_PICK(2, 1, 3, false)
+    SG_DH_PICK(2, 2, 1, false) SG_DH_PICK(2, 2, 2, false) SG_DH_PICK(2, 2, 3, false)
+    SG_DH_PICK(2, 4, 1, false) SG_DH_PICK(2, 4, 2, false) SG_DH_PICK(2, 4, 3, false)
+    SG_DH_PICK(1, 1, 1, true) SG_DH_PICK(1, 1, 2, true) SG_DH_PICK(1, 1, 3, true)
+    SG_DH_PICK(1, 2, 1, true) SG_DH_PICK(1, 2, 2, true) SG_DH_PICK(1, 2, 3, true)
+    SG_DH_PICK(1, 4, 1, true) SG_DH_PICK(1, 4, 2, true) SG_DH_PICK(1, 4, 3, true)
 #undef SG_DH_PICK
     if (!kern) {
-        sg_set_error("tc_dh: no kernel for G = %d, %d tiles per band", lo->G, p.nmt);
+        sg_set_error("tc_dh: no kernel for G = %d, band of %d columns", lo->G, p.band_w);
         return SG_ERR_UNSUPPORTED;
     }
-    const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
+    const size_t smem = (size_t)p.nbuf * p.ws_bytes + (size_t)p.S * p.stage_bytes + 1024;
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;

@@ -103,6 +103,27 @@ __device__ __forceinline__ void named_bar(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// four 8x8 b16 matrices, transposed on the way in: lane l gives the address of
+// row l % 8 of matrix l / 8 (16 bytes); r[m] then holds, for lane t, column
+// t / 4 of matrix m at rows 2 (t % 4) and 2 (t % 4) + 1 (low half first)
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// the inverse fragment order of ldmatrix: r[m] of lane t goes to row t / 4,
+// columns 2 (t % 4) and 2 (t % 4) + 1 of matrix m, whose row l % 8 is at the
+// address lane l = 8 m + l % 8 gives
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, const uint32_t (&r)[4])
+{
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t bar)
@@ -289,6 +310,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
         : "memory");
 }
 
+// the same, arriving on the mbarrier at this offset in every CTA of `mask`
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -402,6 +432,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) |
            ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// the same for fp16 A and B (A/B format fields 0)
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn)
+{
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 
 // layout code of a TMA swizzle width (bytes of one swizzled row)
