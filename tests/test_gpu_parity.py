@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import extreme_label_sparse_gb300 as sg
-from workloads import CONFIGS, Workload, draw_bf16_matrix, generate
+from workloads import CONFIGS, Workload, bf16_bits_to_f32, draw_bf16_matrix, generate
 
 from gpu_common import (LOSS_RTOL, assert_close, build_layout, dev_bf16, dev_i32,
                         dev_problem, host_bf16_to_f64)
@@ -228,6 +228,30 @@ def test_empty_positive_lists(oracle_mod):
     sg.sg_step(lay, d["h"], d["W"], d["rowptr"], d["labels"], 0, dW, dh, loss)
     assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
     assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+
+
+def test_step_large_weights(oracle_mod):
+    """|W| far above the fp16 range (W x 2^20, exact in bf16): inside the step
+    dh multiplies fp16 copies of dZ and of W scaled by 2^-s, and scales the
+    sums back by 2^s; the result must match the oracle as for ordinary W."""
+    w = _w("bigw", B=128, H=768, L=32 * 40, G=32, F=128, pos=36, dist="zipf")
+    p = generate(w)
+    bits = p.W.astype(np.uint32)
+    expo = (bits >> 7) & 0xFF
+    scale = (expo > 0) & (expo < 0xFF - 20)
+    p.W = np.where(scale, bits + (20 << 7), bits).astype(np.uint16)
+    assert np.abs(bf16_bits_to_f32(p.W)).max() > 2.0 ** 16
+    ref = oracle_mod.step(p)
+    lay = build_layout(p)
+    d = dev_problem(p)
+    dW = torch.empty((w.L, w.F), dtype=torch.int16, device="cuda")
+    dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sg.sg_step(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dW, dh, loss)
+    _status_ok(lay)
+    assert_close(host_bf16_to_f64(dW), ref["dW"], what="dW")
+    assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+    assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
 
 
 def test_duplicate_positives_count_once(oracle_mod):
