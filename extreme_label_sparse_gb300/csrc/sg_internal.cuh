@@ -45,10 +45,6 @@ struct sg_layout {
     // allocated on first use
     uint16_t *dZ_ws = nullptr;
     size_t dZ_ws_elems = 0;
-    // dh: per group, for each dh column i (row stride Hp = H rounded up to 16)
-    // the f with I_k[f] = i, 0xff where none (lazily built, needs F < 255)
-    uint8_t *invmap = nullptr;
-    int32_t invmap_hp = 0;
     // W transposed per group ([k][f][j], bf16), written during a step for dh,
     // followed by one word: the step's max |W| as bf16 magnitude bits
     uint16_t *wt_ws = nullptr;

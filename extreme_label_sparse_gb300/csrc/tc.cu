@@ -58,11 +58,12 @@ constexpr int kFirstEpi = kProdWarps + 2;
 // dh: one load warp, one MMA warp, twelve builder warps (one thread per
 // dh column of a band of up to 384)
 constexpr int kDhBuilders = 12;
-constexpr int kDhMaxBuf = 4;  // scattered-W buffers in shared memory
+constexpr int kDhMaxBuf = 3;  // scattered-W buffers in shared memory (one per builder team)
 // groups per pipeline unit (one stage, one scattered-W buffer): a stage's
 // round trip costs about the same from 2 KB to 32 KB of loads, so each stage
-// carries the loads of several groups
-constexpr int kDhP = 2;
+// carries the loads of several groups -- two while their W rows fit twice in
+// shared memory (G <= 32), else one
+__host__ __device__ constexpr int dh_units(int G) { return G <= 32 ? 2 : 1; }
 constexpr int kDhThreads = 32 * (2 + kDhBuilders);
 
 // ------------------------------------------------------------------ plans
@@ -175,7 +176,7 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 DhPlan plan_dh(const sg_layout *lo, int B, bool split)
 {
     DhPlan p;
-    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->G > 64 || lo->F >= 255 || B < 1 || B > 256)
+    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->G > 64 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
@@ -187,13 +188,16 @@ DhPlan plan_dh(const sg_layout *lo, int B, bool split)
     p.nbands = (lo->H + 383) / 384;
     p.bwt = ((lo->H + p.nbands - 1) / p.nbands + 127) / 128;
     p.band_w = p.bwt * 128;
-    // the band's slice of the group's inverse map (u8 per dh column)
-    p.i_bytes = (uint32_t)((p.band_w + 127) / 128 * 128);
-    // one unit = kDhP groups: [dZ x P][W^T x P][inverse-map slices x P]
+    // the group's sorted index row I_k (u16)
+    p.i_bytes = (uint32_t)((lo->F * 2 + 127) / 128 * 128);
+    // one unit = P groups: [dZ x P][W^T x P][I_k x P]
     // (whole KB, so that every stage's dZ tiles sit on swizzle-atom boundaries)
-    p.stage_bytes = (kDhP * (p.z_bytes + p.w_bytes + p.i_bytes) + 1023u) & ~1023u;
-    p.ws_bytes = kDhP * (uint32_t)p.band_w * 2 * lo->G;  // one row of G values per dh column
+    const uint32_t P = (uint32_t)dh_units(lo->G);
+    p.stage_bytes = (P * (p.z_bytes + p.w_bytes + p.i_bytes) + 1023u) & ~1023u;
+    p.ws_bytes = P * (uint32_t)p.band_w * 2 * lo->G;  // one row of G values per dh column
     p.tmem_cols = pow2_cols(p.band_w);
+    // two builder teams, one buffer each (a third team and buffer cost a
+    // stage, and measured slower)
     p.nbuf = 2;
     const long room = (long)kSmemBudget - (long)p.nbuf * p.ws_bytes;
     p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
@@ -1327,8 +1331,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
 
 // ================================================================== dh
 struct DhArgs {
-    const uint8_t *invmap;  // [K][Hp]: f with I_k[f] = i, 0xff where none
-    int64_t Hp;
+    const uint16_t *idx_s;  // [K][F] sorted index rows I_k
     const uint16_t *Wt;    // transposed-W workspace (tile k = W_k^T, swizzled)
     const uint32_t *wmax;  // max |W| bits of the step (fp16 operands only)
     const uint8_t *dZt;    // group-tiled dZ input (else the tensor maps)
@@ -1357,10 +1360,12 @@ struct CtlDh {
 // columns: one MMA of N = 256 and one of N = 128 per K step at BW = 384) stays
 // in TMEM over all the CTA's groups and is added to dh once at the end.  A is
 // the group's dZ tile (K-major, rows = samples) as it arrives in shared
-// memory; B = Ws_k^T (K-major, one 2G-byte row per dh column) is written into
-// shared memory by the builder warps -- every row, row f of the staged W_k^T
-// tile or zeros.  Loads, builders and MMAs move in units of kDhP groups: one
-// stage and one Ws buffer per unit.
+// memory; B = Ws_k^T (K-major, one 2G-byte row per dh column) lives in
+// shared memory, zero except for the rows of the band's I_k: builder thread
+// (g, f) copies row f of the staged W_k^T tile to row I_k[f] - i0 when that
+// falls in the band, after zeroing the row it wrote the last time the buffer
+// was used (the buffers start zeroed).  Loads, builders and MMAs move in
+// units of P groups: one stage and one Ws buffer per unit.
 //
 // Compile-time shape: NPASS dZ planes, NKS = G/16 K steps per plane, BWT
 // 128-column blocks per band.  F16: dZ is one fp16 plane (the training step's
@@ -1379,15 +1384,14 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     constexpr int N0 = BW > 256 ? 256 : BW;
     constexpr int N1 = BW - N0;       // 0 or 128
     constexpr int NCW = G / 8;        // 16-byte units of a row
-    constexpr int P = kDhP;
-    static_assert(BW <= kDhBuilders * 32, "one builder thread per dh column");
+    constexpr int P = dh_units(G);
     __shared__ CtlDh cd;
     Ctl &c = cd.c;
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
-    // [Ws buffers][stages]; a stage: [dZ x P][W^T x P][inverse-map slices x P]
+    // [Ws buffers][stages]; a stage: [dZ x P][W^T x P][I_k x P]
     const uint32_t stage0 = base + (uint32_t)a.nbuf * a.ws_bytes;
     uint8_t *stage0_ptr = base_ptr + (size_t)a.nbuf * a.ws_bytes;
     const int F = a.F, S = a.S, NB = a.nbuf;
@@ -1405,7 +1409,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     if (threadIdx.x == 0) {
         setup_ctl(c, S, 0, 1, 1);
         for (int i = 0; i < NB && i < kDhMaxBuf; ++i) {
-            mbar_init(bar_addr(cd.wfull[i]), kDhBuilders);  // one arrival per builder warp
+            mbar_init(bar_addr(cd.wfull[i]), kDhBuilders / NB);  // one arrival per warp of its team
             mbar_init(bar_addr(cd.wempty[i]), 1);
         }
         fence_mbar_init();
@@ -1431,7 +1435,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             const uint32_t st = stage0 + (uint32_t)s * a.stage_bytes;
             const uint32_t fb = bar_addr(c.full[s]);
             if (lane == 0)
-                mbar_arrive_expect_tx(fb, (uint32_t)np * (a.z_bytes + a.w_bytes + (uint32_t)BW));
+                mbar_arrive_expect_tx(fb, (uint32_t)np * (a.z_bytes + a.w_bytes + (uint32_t)(2 * F)));
             __syncwarp();
             if (lane < np) {
                 // lane g loads group k0 + g
@@ -1449,16 +1453,21 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 }
                 // W_k^T: F swizzled rows of G, one per f
                 bulk_load(st + woff + (uint32_t)lane * a.w_bytes, a.Wt + k * G * F, a.w_bytes, fb);
-                // which f lands on each dh column of the band
-                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.invmap + k * a.Hp + i0, (uint32_t)BW, fb);
+                // I_k: the dh column of each f
+                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + k * F, (uint32_t)(2 * F), fb);
             }
             __syncwarp();
         }
         drain_loads(c, it, S);
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue
-        const uint32_t zlayout = layout_for_swizzle(a.zsw);
-        constexpr uint32_t wlayout = layout_for_swizzle(RB);
+        // descriptors: everything but the start address is fixed, and within a
+        // unit the start addresses differ by compile-time offsets
+        constexpr int ZSW = 2 * G >= 128 ? 128 : 2 * G;  // dZ row bytes (= a.zsw)
+        constexpr uint32_t ZCH = 128u * ZSW;             // one plane of one group
+        constexpr uint32_t ZB = NPASS * ZCH;             // one group's dZ (= a.z_bytes)
+        const uint64_t adesc0 = sdesc(0, 16, 8 * ZSW, layout_for_swizzle(ZSW));
+        const uint64_t bdesc0 = sdesc(0, 16, 8 * RB, layout_for_swizzle(RB));
         constexpr uint32_t id0 = F16 ? idesc_f16(128, N0, 0, 0) : idesc_bf16(128, N0, 0, 0);
         constexpr uint32_t id1 = N1 == 0 ? 0u : F16 ? idesc_f16(128, N1 > 0 ? N1 : 16, 0, 0)
                                                      : idesc_bf16(128, N1 > 0 ? N1 : 16, 0, 0);
@@ -1473,26 +1482,21 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 break;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t st = stage0 + (uint32_t)s * a.stage_bytes;
-                const uint32_t Wb = base + (uint32_t)buf * a.ws_bytes;
+                // A: dZ (rows = samples), B: Ws rows (dh columns); 16 j per K step
+                const uint64_t au = adesc0 + (uint64_t)((stage0 + (uint32_t)s * a.stage_bytes + zoff) >> 4);
+                const uint64_t bu = bdesc0 + (uint64_t)((base + (uint32_t)buf * a.ws_bytes) >> 4);
 #pragma unroll
                 for (int g = 0; g < P; ++g) {
                     if (g < np) {
-                        const uint32_t Zs = st + zoff + (uint32_t)g * a.z_bytes;
-                        const uint32_t Ws = Wb + (uint32_t)(g * BW * RB);
 #pragma unroll
                         for (int ks2 = 0; ks2 < NPASS * NKS; ++ks2) {
                             const int ks = ks2 % NKS;
                             const uint32_t acc = (it > 0 || g > 0 || ks2 > 0) ? 1u : 0u;
-                            // A: dZ plane ks2 / NKS (rows = samples), 16 j per step
-                            const uint64_t ad = sdesc(Zs + (uint32_t)(ks2 / NKS) * zchunk + (uint32_t)ks * 32, 16,
-                                                      8 * a.zsw, zlayout);
-                            // B: Ws rows (dh columns), the same 16 j
-                            mma_bf16(tbase, ad, sdesc(Ws + (uint32_t)ks * 32, 16, 8 * RB, wlayout), id0, acc);
+                            const uint64_t ad = au + ((g * ZB + (ks2 / NKS) * ZCH + ks * 32) >> 4);
+                            const uint64_t bd = bu + ((g * BW * RB + ks * 32) >> 4);
+                            mma_bf16(tbase, ad, bd, id0, acc);
                             if (N1 > 0)
-                                mma_bf16(tbase + (uint32_t)N0, ad,
-                                         sdesc(Ws + (uint32_t)(N0 * RB) + (uint32_t)ks * 32, 16, 8 * RB, wlayout),
-                                         id1, acc);
+                                mma_bf16(tbase + (uint32_t)N0, ad, bd + ((N0 * RB) >> 4), id1, acc);
                         }
                     }
                 }
@@ -1511,8 +1515,15 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         mbar_wait_drain(bar_addr(c.drain[0]), 0);  // no MMA in flight at the dealloc
     } else {
         // ---------------------------------------------------------- builders
-        // thread t writes the Ws rows of dh column i0 + t (one per group)
+        // NB teams of 12 / NB warps take turns at the units (team t: units t,
+        // t + NB, ..., always Ws buffer t), so the teams build concurrently
+        // while the MMAs consume.  Team thread tt handles the slots e = tt,
+        // tt + NT, ... of the unit's P x F (group g = e / F, feature f = e % F).
+        const int NT = kDhBuilders * 32 / NB;  // threads of a team
+        constexpr int NT_MIN = kDhBuilders * 32 / (P == 2 ? 3 : 2);
+        constexpr int NSLOT = (P * 256 + NT_MIN - 1) / NT_MIN;
         const int tb = threadIdx.x - kDhFirstEpi * 32;  // 0 .. 383
+        const int team = tb / NT, tt = tb - team * NT;
         const int q = warp & 3, sub = (warp - kDhFirstEpi) / 4;
         float down = 1.f, up = 1.f;  // 2^-s, 2^s (fp16 operands)
         if (F16) {
@@ -1522,60 +1533,79 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             down = __uint_as_float((uint32_t)(127 - sh) << 23);
             up = __uint_as_float((uint32_t)(127 + sh) << 23);
         }
-        const int sw = swz_of(tb, RB);
-        int it = 0, buf = 0;
+        // the team's buffer starts zeroed; prev[x]: the row slot x wrote in it
+        uint8_t *Wb = base_ptr + (size_t)team * a.ws_bytes;
+        for (uint32_t o = (uint32_t)tt * 16; o < a.ws_bytes; o += NT * 16)
+            *reinterpret_cast<uint4 *>(Wb + o) = make_uint4(0u, 0u, 0u, 0u);
+        int prev[NSLOT];
+#pragma unroll
+        for (int x = 0; x < NSLOT; ++x)
+            prev[x] = -1;
+        int it = team;
         uint32_t wph = 0;
-        for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it) {
+        for (int64_t k0 = kbeg + (int64_t)team * P; k0 < kend; k0 += (int64_t)NB * P, it += NB) {
             const int s = it % S;
             const int np = kend - k0 < P ? (int)(kend - k0) : P;
-            if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
-                break;
+            bool ok = mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status);
             const uint8_t *st = stage0_ptr + (size_t)s * a.stage_bytes;
-            // the rows are read from the stage before waiting for the buffer
-            uint4 row[P][NCW];
+            // this thread's rows, read from the stage before waiting for the buffer
+            uint4 row[NSLOT][NCW];
+            int dst[NSLOT];
 #pragma unroll
-            for (int g = 0; g < P; ++g) {
-#pragma unroll
-                for (int u = 0; u < NCW; ++u)
-                    row[g][u] = make_uint4(0u, 0u, 0u, 0u);
-                if (tb < BW && g < np) {
-                    const uint8_t *Wt = st + woff + (size_t)g * a.w_bytes;  // W_k^T tile
-                    const uint32_t f = st[ioff + (size_t)g * a.i_bytes + tb];  // f (if any) of this dh column
-                    if (f != 0xffu) {
+            for (int x = 0; x < NSLOT; ++x) {
+                dst[x] = -1;
+                const int e = tt + x * NT;
+                const int g = e / F, f = e - g * F;
+                if (ok && g < np && x * NT < P * F) {
+                    const int i = (int)reinterpret_cast<const uint16_t *>(st + ioff + (size_t)g * a.i_bytes)[f] - i0;
+                    if (i >= 0 && i < BW) {
+                        dst[x] = g * BW + i;
+                        const uint8_t *Wt = st + woff + (size_t)g * a.w_bytes;  // W_k^T tile
 #pragma unroll
                         for (int u = 0; u < NCW; ++u) {
-                            uint4 w = *reinterpret_cast<const uint4 *>(Wt + wt_swz(f * (uint32_t)RB + 16u * u));
+                            uint4 w = *reinterpret_cast<const uint4 *>(Wt + wt_swz((uint32_t)(f * RB + 16 * u)));
                             if (F16) {
                                 w.x = pack2_f16(lo_half(w.x) * down, hi_half(w.x) * down);
                                 w.y = pack2_f16(lo_half(w.y) * down, hi_half(w.y) * down);
                                 w.z = pack2_f16(lo_half(w.z) * down, hi_half(w.z) * down);
                                 w.w = pack2_f16(lo_half(w.w) * down, hi_half(w.w) * down);
                             }
-                            row[g][u] = w;
+                            row[x][u] = w;
                         }
                     }
                 }
             }
             // the buffer's last unit must be through its MMAs before it is rewritten
-            if (!mbar_wait(bar_addr(cd.wempty[buf]), wph ^ 1u, abort_flag, a.status))
-                break;
-            if (tb < BW) {
+            ok = ok && mbar_wait(bar_addr(cd.wempty[team]), wph ^ 1u, abort_flag, a.status);
+            if (named_bar_any(1 + team, NT, !ok))
+                break;  // the whole team leaves together
+            // zero the rows of the buffer's last unit, then write this unit's
 #pragma unroll
-                for (int g = 0; g < P; ++g) {
-                    uint8_t *dst = base_ptr + (size_t)buf * a.ws_bytes + (size_t)(g * BW + tb) * RB;
+            for (int x = 0; x < NSLOT; ++x) {
+                if (prev[x] >= 0) {
+                    uint8_t *d = Wb + (size_t)prev[x] * RB;
 #pragma unroll
                     for (int u = 0; u < NCW; ++u)
-                        *reinterpret_cast<uint4 *>(dst + ((u ^ sw) << 4)) = row[g][u];
+                        *reinterpret_cast<uint4 *>(d + (u << 4)) = make_uint4(0u, 0u, 0u, 0u);
                 }
+            }
+            named_bar(1 + team, NT);
+#pragma unroll
+            for (int x = 0; x < NSLOT; ++x) {
+                if (dst[x] >= 0) {
+                    uint8_t *d = Wb + (size_t)dst[x] * RB;
+                    const int sw = swz_of(dst[x], RB);
+#pragma unroll
+                    for (int u = 0; u < NCW; ++u)
+                        *reinterpret_cast<uint4 *>(d + ((u ^ sw) << 4)) = row[x][u];
+                }
+                prev[x] = dst[x];
             }
             fence_proxy_async();  // Ws rows (generic writes) -> the MMA (async proxy)
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar_addr(cd.wfull[buf]));
-            if (++buf == NB) {
-                buf = 0;
-                wph ^= 1u;
-            }
+                mbar_arrive(bar_addr(cd.wfull[team]));
+            wph ^= 1u;
         }
         // the accumulator (lanes = samples, columns = the band's dh columns)
         // holds this CTA's partial: add it in, transposed through shared memory
@@ -1861,14 +1891,6 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     return SG_OK;
 }
 
-// inverse of I_k per group: map[k][I_k[f]] = f
-__global__ void k_invmap(const uint16_t *__restrict__ idx_s, int64_t K, int F, int64_t Hp, uint8_t *map)
-{
-    const int64_t k = blockIdx.x;
-    for (int f = threadIdx.x; f < F; f += blockDim.x)
-        map[k * Hp + idx_s[k * F + f]] = (uint8_t)f;
-}
-
 sg_status tc_ensure_wt(sg_layout *lo)
 {
     if (lo->wt_ws)
@@ -1882,26 +1904,6 @@ sg_status tc_ensure_wt(sg_layout *lo)
         return SG_ERR_OOM;
     }
     lo->wmax = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(lo->wt_ws) + bytes);
-    return SG_OK;
-}
-
-sg_status ensure_invmap(sg_layout *lo, int band_w, cudaStream_t st)
-{
-    if (lo->invmap)
-        return SG_OK;
-    const int64_t Hp = (lo->H + 15) / 16 * 16;
-    // the last band may read up to band_w past the last row's start
-    const size_t bytes = (size_t)lo->K * Hp + (size_t)band_w + 16;
-    if (cudaMalloc((void **)&lo->invmap, bytes) != cudaSuccess) {
-        cudaGetLastError();
-        lo->invmap = nullptr;
-        sg_set_error("tc_dh: cudaMalloc of %zu bytes for the inverse map failed", bytes);
-        return SG_ERR_OOM;
-    }
-    lo->invmap_hp = (int32_t)Hp;
-    SG_TRY_CUDA(cudaMemsetAsync(lo->invmap, 0xff, bytes, st));
-    k_invmap<<<(unsigned)lo->K, 128, 0, st>>>(lo->idx_s, lo->K, lo->F, Hp, lo->invmap);
-    SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }
 
@@ -1954,9 +1956,6 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
         sg_set_error("W: device pointer must be 16-byte aligned");
         return SG_ERR_INVALID;
     }
-    rc = ensure_invmap(lo, p.band_w, st);
-    if (rc != SG_OK)
-        return rc;
     if (!Wt) {
         rc = tc_ensure_wt(lo);
         if (rc != SG_OK)
@@ -1966,8 +1965,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
         Wt = lo->wt_ws;
     }
     DhArgs a;
-    a.invmap = lo->invmap;
-    a.Hp = lo->invmap_hp;
+    a.idx_s = lo->idx_s;
     a.Wt = Wt;
     a.wmax = lo->wmax;
     a.dZt = dZt;
@@ -1982,7 +1980,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.H = lo->H;
     a.MT = p.MT;
     a.S = p.S;
-    a.zsw = p.zsw;
+    a.zsw = p.zsw;  // = min(2G, 128), which the kernel also derives from G
     a.nbands = p.nbands;
     a.band_w = p.band_w;
     a.npass = split ? 2 : 1;
@@ -1992,7 +1990,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
         parts = 1;
     // contiguous ranges of whole units of groups
     int64_t kc = (lo->K + parts - 1) / parts;
-    kc = (kc + kDhP - 1) / kDhP * kDhP;
+    kc = (kc + dh_units(lo->G) - 1) / dh_units(lo->G) * dh_units(lo->G);
     parts = (int)((lo->K + kc - 1) / kc);
     a.parts = parts;
     a.Kc = kc;

@@ -103,6 +103,22 @@ __device__ __forceinline__ void named_bar(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// barrier over `threads` threads (whole warps) that also ORs a predicate:
+// every participant gets true if any of them passed true
+__device__ __forceinline__ bool named_bar_any(int id, int threads, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 // four 8x8 b16 matrices, transposed on the way in: lane l gives the address of
 // row l % 8 of matrix l / 8 (16 bytes); r[m] then holds, for lane t, column
 // t / 4 of matrix m at rows 2 (t % 4) and 2 (t % 4) + 1 (low half first)
