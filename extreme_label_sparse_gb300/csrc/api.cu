@@ -113,7 +113,7 @@ void free_layout(sg_layout *lo)
     timer_release(lo->timer);
     void *bufs[] = {lo->slot_of_label, lo->label_of_slot, lo->idx_s, lo->hT,
                     lo->gcount, lo->gptr, lo->gent, lo->tsorted, lo->tslots,
-                    lo->rowcnt, lo->loss_part, lo->status, lo->dZ_ws, lo->scan_part, lo->wt_ws};
+                    lo->rowcnt, lo->loss_part, lo->status, lo->dZ_ws, lo->scan_part, lo->wmax};
     for (void *p : bufs)
         if (p)
             cudaFree(p);
@@ -464,7 +464,7 @@ sg_status sg_bwd_dh(sg_layout *lo, const sg_bf16 *dZ, int32_t B,
     bool tc = false;
     TRY(pick_tc(lo, SG_KIND_DH, B, &tc, fn));
     if (tc)
-        return tc_dh(lo, dZ, nullptr, nullptr, false, B, W, nullptr, dh, st);
+        return tc_dh(lo, dZ, nullptr, nullptr, false, B, W, dh, st);
     return simt_dh(lo, dZ, nullptr, B, W, dh, st);
 }
 
@@ -519,21 +519,20 @@ sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
         // all three on the tensor cores: dZ in the group-tiled workspace
         uint8_t *dZt = reinterpret_cast<uint8_t *>(lo->dZ_ws);
         if (fused) {
-            // the fused kernel also leaves W_k transposed for dh
-            TRY(tc_ensure_wt(lo));
-            TRY(tc_fwdw(lo, B, W, dZt, dW, lo->wt_ws, loss, st));
-            return tc_dh(lo, nullptr, nullptr, dZt, true, B, W, lo->wt_ws, dh, st);
+            // the fused kernel leaves dZ as one fp16 plane and max |W| for dh
+            TRY(tc_fwdw(lo, B, W, dZt, dW, loss, st));
+            return tc_dh(lo, nullptr, nullptr, dZt, true, B, W, dh, st);
         }
         TRY(tc_fwd(lo, B, W, nullptr, nullptr, nullptr, dZt, loss, st));
         TRY(tc_dW(lo, nullptr, nullptr, dZt, B, dW, st));
-        return tc_dh(lo, nullptr, nullptr, dZt, false, B, W, nullptr, dh, st);
+        return tc_dh(lo, nullptr, nullptr, dZt, false, B, W, dh, st);
     }
     uint16_t *dZ = lo->dZ_ws;
     uint16_t *dZlo = lo->dZ_ws + (size_t)B * lo->L;
     TRY(tc_f ? tc_fwd(lo, B, W, nullptr, dZ, dZlo, nullptr, loss, st)
              : simt_fwd(lo, B, W, nullptr, dZ, dZlo, loss, st));
     TRY(tc_w ? tc_dW(lo, dZ, dZlo, nullptr, B, dW, st) : simt_dW(lo, dZ, dZlo, B, dW, st));
-    return tc_h ? tc_dh(lo, dZ, dZlo, nullptr, false, B, W, nullptr, dh, st) : simt_dh(lo, dZ, dZlo, B, W, dh, st);
+    return tc_h ? tc_dh(lo, dZ, dZlo, nullptr, false, B, W, dh, st) : simt_dh(lo, dZ, dZlo, B, W, dh, st);
 }
 
 // ---------------------------------------------------------------- timing

@@ -45,10 +45,8 @@ struct sg_layout {
     // allocated on first use
     uint16_t *dZ_ws = nullptr;
     size_t dZ_ws_elems = 0;
-    // W transposed per group ([k][f][j], bf16), written during a step for dh,
-    // followed by one word: the step's max |W| as bf16 magnitude bits
-    uint16_t *wt_ws = nullptr;
-    uint32_t *wmax = nullptr;  // inside the wt_ws allocation
+    // the step's max |W| as bf16 magnitude bits (scale of dh's fp16 operands)
+    uint32_t *wmax = nullptr;
 
     // per-kernel event timing (sg_timing_start / sg_timing_stop)
     struct Timer {
@@ -172,13 +170,11 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
                  uint16_t *dZ, uint16_t *dZ_lo, uint8_t *dZt, double *loss, cudaStream_t st);
 sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
                 int32_t B, uint16_t *dW, cudaStream_t st);
-// dh reads W_k transposed: Wt = lo->wt_ws already filled this step (by the
-// fused kernel), or nullptr to transpose W into it first.  dzt_f16: the tiled
-// dZ is the fused kernel's single fp16 plane (fp16 MMA operands)
+// dzt_f16: the tiled dZ is the fused kernel's single fp16 plane (fp16 MMA
+// operands, W scaled by the step's max |W| that kernel recorded)
 sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
-                bool dzt_f16, int32_t B, const uint16_t *W, const uint16_t *Wt, float *dh,
-                cudaStream_t st);
-sg_status tc_ensure_wt(sg_layout *lo);
+                bool dzt_f16, int32_t B, const uint16_t *W, float *dh, cudaStream_t st);
+sg_status tc_ensure_wmax(sg_layout *lo);
 // bytes of one group's dZ tile, and whether fwd, dW and dh all run on the
 // tensor cores with the tiled workspace for this batch size
 uint64_t tc_dz_tile_bytes(const sg_layout *lo, int32_t B);
@@ -186,7 +182,7 @@ bool tc_tiled_ok(const sg_layout *lo, int32_t B);
 // fused forward + BCE + dW into the tiled workspace (one pass over the groups)
 bool tc_fwdw_ok(const sg_layout *lo, int32_t B);
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
-                  uint16_t *Wt, double *loss, cudaStream_t st);
+                  double *loss, cudaStream_t st);
 sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW,
                   float *dh, double *loss, cudaStream_t st);
 

@@ -29,13 +29,7 @@
 // zsw = min(2G, 128) the row width and swz the TMA swizzle of that width.
 // A tile is contiguous (2 Bp G bf16 values per plane pair), so writing it
 // touches one or two pages instead of one page per sample row.
-//
-// Transposed-W workspace (training step only).  Tile k (G F bf16 values at
-// element k G F) holds W_k^T: row f is the G values W_k[0..G)[f], the 16-byte
-// unit of columns 8u .. 8u+7 at logical byte o = 2 G f + 16 u, stored at
-// wt_swz(o) (the 128-byte swizzle over the tile's bytes).  The fused forward
-// kernel writes it from the W_k it already holds in shared memory; the feature
-// gradient then reads each row of its A operand with G/8 16-byte loads.
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -106,11 +100,6 @@ bool shape_ok(const sg_layout *lo)
 // whole chunks of 64
 bool dz_ok(int G) { return G == 16 || G == 32 || G % 64 == 0; }
 
-// 128-byte swizzle of a byte offset inside a transposed-W tile: the 16-byte
-// unit index (bits 4-6) is XORed with the 128-byte line index (bits 7-9), so
-// eight consecutive rows f at the same unit land in eight different bank
-// groups for both the writer (stmatrix) and the reader (dh builders)
-__host__ __device__ __forceinline__ uint32_t wt_swz(uint32_t o) { return o ^ (((o >> 7) & 7u) << 4); }
 
 int stages_for(uint32_t stage_bytes)
 {
@@ -995,8 +984,8 @@ FWPlan plan_fwdw(const sg_layout *lo, int B)
     p.tmem_cols = pow2_cols(p.nslot * (p.zcols + p.wcols));
     // F = 64: the last stage's dW MMA reads up to 8 KB past it
     p.pad_bytes = lo->F < 128 ? 8192u : 0u;
-    // two dW_k staging buffers and two W_k^T staging buffers (same size)
-    const long room = (long)kFWBudget - 2l * p.dz_bytes - 4l * p.stg_bytes - (long)p.pad_bytes;
+    // two dW_k staging buffers
+    const long room = (long)kFWBudget - 2l * p.dz_bytes - 2l * p.stg_bytes - (long)p.pad_bytes;
     p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
     if (p.S > 6)
         p.S = 6;
@@ -1009,7 +998,6 @@ struct FWArgs {
     uint8_t *dZt;
     uint64_t tile_bytes;
     uint16_t *dW;
-    uint16_t *Wt;     // transposed-W workspace
     uint32_t *wmax;   // max |W| (bf16 magnitude bits) over the step, for dh
     const int32_t *gptr, *gent;
     double *loss_part;
@@ -1046,10 +1034,9 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
-    // [dZ_k buffer 0][dZ_k buffer 1][dW_k staging 0, 1][W_k^T staging 0, 1][stages]
+    // [dZ_k buffer 0][dZ_k buffer 1][dW_k staging 0, 1][stages]
     const uint32_t stg0 = base + 2 * a.dz_bytes;
-    const uint32_t wtstg0 = stg0 + 2 * a.stg_bytes;
-    const uint32_t stage0 = wtstg0 + 2 * a.stg_bytes;
+    const uint32_t stage0 = stg0 + 2 * a.stg_bytes;
     constexpr int G = G_;
     const int F = a.F, S = a.S, NS = a.nslot;
     constexpr uint32_t zrows = (uint32_t)MT * 128;
@@ -1057,8 +1044,8 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     const uint32_t wbase = (uint32_t)NS * a.zcols;  // first dW accumulator column
 
     // the epilogue is two teams: the BCE warps turn Z_k into dZ_k, the dW
-    // warps store dW of the group and W_k^T.  A stage is freed by the dW MMA
-    // (last reader of H_k) and by the dW warps (last readers of W_k).
+    // warps store dW of the group and take max |W_k|.  A stage is freed by the
+    // dW MMA (last reader of H_k) and by the dW warps (last readers of W_k).
     if (threadIdx.x == 0) {
         setup_ctl(c, S, 0, kProdWarps * 32 + 1, 2);
         for (int i = 0; i < NS && i < 4; ++i) {
@@ -1235,15 +1222,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         } else {
             // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
             // staged in shared memory as [j][f] and stored with one bulk copy.
-            // Before that, W_k of the stage is transposed into the W^T tile
-            // (8x8 blocks: ldmatrix.trans from the TMA layout, stmatrix into
-            // the swizzled [f][j] rows) and stored the same way.  The elected
-            // thread's bulk groups alternate W^T, dW: a staging buffer of two
-            // groups ago has been read once at most three groups are pending.
+            // Before that, the warps take max |W| over the stage's W_k (the
+            // scale of the feature gradient's fp16 operands).
             const int dw = ew - kFWBce;  // 0 .. kFWDw-1
             constexpr int wunits = ((FK + 7) / 8) * (G / CH);
-            constexpr int JB = G / 8;                // 8-row blocks of j
-            constexpr int XPW = (JB * 2 * FK) / 16;  // ldmatrix.x4 per warp (4 blocks each)
+            constexpr int WU = G * FK * 2 / kFWDw / 32;  // 16-byte units of W_k per thread
             uint32_t wmag = 0;  // running max of |W| bits, two bf16 lanes
             int it = 0;
             for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
@@ -1251,44 +1234,29 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 const int ws = it % NS;
                 const int wb = it & 1;
                 uint16_t *stg = reinterpret_cast<uint16_t *>(base_ptr + 2 * (size_t)a.dz_bytes + (size_t)wb * a.stg_bytes);
-                // ---- W_k -> W_k^T
+                // ---- max |W_k|
                 if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                     break;
+                const uint4 *Wsm = reinterpret_cast<const uint4 *>(base_ptr + (stage0 - base) +
+                                                                   (size_t)s * a.stage_bytes + a.a_bytes);
+#pragma unroll
+                for (int x = 0; x < WU; ++x) {
+                    const uint4 v = Wsm[(x * kFWDw + dw) * 32 + lane];
+                    wmag = __vmaxu2(wmag, v.x & 0x7fff7fffu);
+                    wmag = __vmaxu2(wmag, v.y & 0x7fff7fffu);
+                    wmag = __vmaxu2(wmag, v.z & 0x7fff7fffu);
+                    wmag = __vmaxu2(wmag, v.w & 0x7fff7fffu);
+                }
+                named_bar(2, kFWDw * 32);
                 if (dw == 0 && lane == 0)
-                    bulk_wait_read<3>();
-                named_bar(2, kFWDw * 32);
-                const uint32_t Ws = stage0 + (uint32_t)s * a.stage_bytes + a.a_bytes;
-                const uint32_t T = wtstg0 + (uint32_t)wb * a.stg_bytes;
-#pragma unroll
-                for (int x = 0; x < XPW; ++x) {
-                    const int blk = 4 * (x * kFWDw + dw) + (lane >> 3), r = lane & 7;
-                    const int jb = blk % JB, fb = blk / JB;
-                    const int j = jb * 8 + r;
-                    // row j of the 8x8 block: 8 f of the 64-f TMA box fb / 8
-                    const uint32_t src = Ws + (uint32_t)(fb >> 3) * G * 128 + (uint32_t)j * 128 +
-                                         ((uint32_t)((fb & 7) ^ (j & 7)) << 4);
-                    // row f = 8 fb + r of the block: its 8 j at unit jb
-                    const uint32_t o = (uint32_t)(fb * 8 + r) * (2 * G) + (uint32_t)jb * 16;
-                    uint32_t v[4];
-                    ldmatrix_x4_trans(src, v);
-                    stmatrix_x4(T + wt_swz(o), v);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        wmag = __vmaxu2(wmag, v[e] & 0x7fff7fffu);
-                }
-                fence_proxy_async();  // staged W_k^T -> the bulk store (async proxy)
-                named_bar(2, kFWDw * 32);
-                if (dw == 0 && lane == 0) {
                     mbar_arrive(bar_addr(c.empty[s]));  // done with the stage's W_k
-                    bulk_store(a.Wt + k * G * F, T, a.stg_bytes);
-                    bulk_commit();
-                }
                 // ---- dW_k
                 if (!mbar_wait(bar_addr(cf.wfull[ws]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
                     break;
                 tc_fence_after();
+                // the staging buffer's store of two groups ago has read it
                 if (dw == 0 && lane == 0)
-                    bulk_wait_read<3>();
+                    bulk_wait_read<1>();
                 named_bar(2, kFWDw * 32);
 #pragma unroll 1
                 for (int u = 0; u < wunits; ++u) {
@@ -1318,7 +1286,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             if (lane == 0)
                 atomicMax(a.wmax, wmag);
             if (dw == 0 && lane == 0)
-                bulk_wait<0>();  // every dW and W^T store has landed
+                bulk_wait<0>();  // every dW store has landed
         }
     }
     tc_fence_before();
@@ -1332,7 +1300,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
 // ================================================================== dh
 struct DhArgs {
     const uint16_t *idx_s;  // [K][F] sorted index rows I_k
-    const uint16_t *Wt;    // transposed-W workspace (tile k = W_k^T, swizzled)
+    const uint16_t *W;     // [L][F] in slot order
     const uint32_t *wmax;  // max |W| bits of the step (fp16 operands only)
     const uint8_t *dZt;    // group-tiled dZ input (else the tensor maps)
     uint64_t tile_bytes;
@@ -1362,9 +1330,9 @@ struct CtlDh {
 // the group's dZ tile (K-major, rows = samples) as it arrives in shared
 // memory; B = Ws_k^T (K-major, one 2G-byte row per dh column) lives in
 // shared memory, zero except for the rows of the band's I_k: builder thread
-// (g, f) copies row f of the staged W_k^T tile to row I_k[f] - i0 when that
-// falls in the band, after zeroing the row it wrote the last time the buffer
-// was used (the buffers start zeroed).  Loads, builders and MMAs move in
+// (g, f) copies column f of the staged W_k to row I_k[f] - i0 when that falls
+// in the band, after zeroing the row it wrote the last time the buffer was
+// used (the buffers start zeroed).  Loads, builders and MMAs move in
 // units of P groups: one stage and one Ws buffer per unit.
 //
 // Compile-time shape: NPASS dZ planes, NKS = G/16 K steps per plane, BWT
@@ -1391,7 +1359,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
-    // [Ws buffers][stages]; a stage: [dZ x P][W^T x P][I_k x P]
+    // [Ws buffers][stages]; a stage: [dZ x P][W_k x P][I_k x P]
     const uint32_t stage0 = base + (uint32_t)a.nbuf * a.ws_bytes;
     uint8_t *stage0_ptr = base_ptr + (size_t)a.nbuf * a.ws_bytes;
     const int F = a.F, S = a.S, NB = a.nbuf;
@@ -1451,8 +1419,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                     if (NPASS > 1)
                         tma_load_2d(Zs + zchunk, &tm_zl, (int)(k * G), mt * 128, fb);
                 }
-                // W_k^T: F swizzled rows of G, one per f
-                bulk_load(st + woff + (uint32_t)lane * a.w_bytes, a.Wt + k * G * F, a.w_bytes, fb);
+                // W_k: G contiguous rows of F
+                bulk_load(st + woff + (uint32_t)lane * a.w_bytes, a.W + k * G * F, a.w_bytes, fb);
                 // I_k: the dh column of each f
                 bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + k * F, (uint32_t)(2 * F), fb);
             }
@@ -1560,17 +1528,19 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                     const int i = (int)reinterpret_cast<const uint16_t *>(st + ioff + (size_t)g * a.i_bytes)[f] - i0;
                     if (i >= 0 && i < BW) {
                         dst[x] = g * BW + i;
-                        const uint8_t *Wt = st + woff + (size_t)g * a.w_bytes;  // W_k^T tile
+                        // column f of W_k ([G][F] row-major): consecutive
+                        // threads read consecutive f
+                        const uint16_t *Wk = reinterpret_cast<const uint16_t *>(st + woff + (size_t)g * a.w_bytes) + f;
 #pragma unroll
                         for (int u = 0; u < NCW; ++u) {
-                            uint4 w = *reinterpret_cast<const uint4 *>(Wt + wt_swz((uint32_t)(f * RB + 16 * u)));
-                            if (F16) {
-                                w.x = pack2_f16(lo_half(w.x) * down, hi_half(w.x) * down);
-                                w.y = pack2_f16(lo_half(w.y) * down, hi_half(w.y) * down);
-                                w.z = pack2_f16(lo_half(w.z) * down, hi_half(w.z) * down);
-                                w.w = pack2_f16(lo_half(w.w) * down, hi_half(w.w) * down);
+                            uint32_t w[4];
+#pragma unroll
+                            for (int c2 = 0; c2 < 4; ++c2) {
+                                const uint32_t lo = Wk[(8 * u + 2 * c2) * F], hi = Wk[(8 * u + 2 * c2 + 1) * F];
+                                w[c2] = F16 ? pack2_f16(__uint_as_float(lo << 16) * down, __uint_as_float(hi << 16) * down)
+                                            : (lo | (hi << 16));
                             }
-                            row[x][u] = w;
+                            row[x][u] = make_uint4(w[0], w[1], w[2], w[3]);
                         }
                     }
                 }
@@ -1754,7 +1724,7 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
 bool tc_fwdw_ok(const sg_layout *lo, int32_t B) { return plan_fwdw(lo, B).ok; }
 
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
-                  uint16_t *Wt, double *loss, cudaStream_t st)
+                  double *loss, cudaStream_t st)
 {
     const FWPlan p = plan_fwdw(lo, B);
     if (!p.ok) {
@@ -1768,14 +1738,12 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     FWArgs a;
     a.idx_s = lo->idx_s;
     a.hT = lo->hT;
-    if (!Wt || !lo->wmax) {
-        sg_set_error("tc_fwdw: the transposed-W workspace is not allocated");
-        return SG_ERR_INVALID;
-    }
+    rc = tc_ensure_wmax(lo);
+    if (rc != SG_OK)
+        return rc;
     a.dZt = dZt;
     a.tile_bytes = tc_dz_tile_bytes(lo, B) / 2;  // one fp16 plane
     a.dW = dW;
-    a.Wt = Wt;
     a.wmax = lo->wmax;
     a.gptr = lo->gptr;
     a.gent = lo->gent;
@@ -1804,7 +1772,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.wcols = p.wcols;
     a.tmem_cols = p.tmem_cols;
     const size_t smem =
-        2 * (size_t)p.dz_bytes + 4 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
+        2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
 #define SG_FW_PICK(GG, KK, MM)                                           \
@@ -1891,44 +1859,24 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     return SG_OK;
 }
 
-sg_status tc_ensure_wt(sg_layout *lo)
+sg_status tc_ensure_wmax(sg_layout *lo)
 {
-    if (lo->wt_ws)
+    if (lo->wmax)
         return SG_OK;
-    // the W^T tiles, then one word: max |W| bits of the step
-    const size_t bytes = (size_t)lo->L * lo->F * 2;
-    if (cudaMalloc((void **)&lo->wt_ws, bytes + 16) != cudaSuccess) {
+    if (cudaMalloc((void **)&lo->wmax, 16) != cudaSuccess) {
         cudaGetLastError();
-        lo->wt_ws = nullptr;
-        sg_set_error("cudaMalloc of %zu bytes for the transposed-W workspace failed", bytes + 16);
+        lo->wmax = nullptr;
+        sg_set_error("cudaMalloc of 16 bytes for the step's max |W| failed");
         return SG_ERR_OOM;
     }
-    lo->wmax = reinterpret_cast<uint32_t *>(reinterpret_cast<uint8_t *>(lo->wt_ws) + bytes);
     return SG_OK;
 }
 
-// W_k^T tiles from W for the callers whose step did not write them
-__global__ void k_wt_transpose(const uint16_t *__restrict__ W, int64_t K, int G, int F, uint16_t *__restrict__ Wt)
-{
-    const int units = F * G / 8;  // 16-byte units of a tile
-    for (int64_t k = blockIdx.x; k < K; k += gridDim.x) {
-        const uint16_t *Wk = W + k * G * F;
-        uint8_t *T = reinterpret_cast<uint8_t *>(Wt + k * G * F);
-        for (int e = threadIdx.x; e < units; e += blockDim.x) {
-            const int f = e % F, u = e / F;  // consecutive threads: consecutive f
-            uint32_t w[4];
-            for (int x = 0; x < 4; ++x)
-                w[x] = (uint32_t)Wk[(8 * u + 2 * x) * F + f] | ((uint32_t)Wk[(8 * u + 2 * x + 1) * F + f] << 16);
-            *reinterpret_cast<uint4 *>(T + wt_swz((uint32_t)(f * 2 * G + 16 * u))) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-}
-
 sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
-                bool dzt_f16, int32_t B, const uint16_t *W, const uint16_t *Wt, float *dh, cudaStream_t st)
+                bool dzt_f16, int32_t B, const uint16_t *W, float *dh, cudaStream_t st)
 {
-    if (dzt_f16 && (!dZt || !Wt)) {
-        sg_set_error("tc_dh: the fp16 dZ workspace comes with the step's W^T tiles");
+    if (dzt_f16 && (!dZt || !lo->wmax)) {
+        sg_set_error("tc_dh: the fp16 dZ workspace comes with the step's max |W|");
         return SG_ERR_INVALID;
     }
     const bool split = dZ_lo != nullptr || (dZt != nullptr && !dzt_f16);
@@ -1956,17 +1904,9 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
         sg_set_error("W: device pointer must be 16-byte aligned");
         return SG_ERR_INVALID;
     }
-    if (!Wt) {
-        rc = tc_ensure_wt(lo);
-        if (rc != SG_OK)
-            return rc;
-        k_wt_transpose<<<persistent_grid(lo, lo->K) * 4, 256, 0, st>>>(W, lo->K, lo->G, lo->F, lo->wt_ws);
-        SG_TRY_CUDA(cudaGetLastError());
-        Wt = lo->wt_ws;
-    }
     DhArgs a;
     a.idx_s = lo->idx_s;
-    a.Wt = Wt;
+    a.W = W;
     a.wmax = lo->wmax;
     a.dZt = dZt;
     a.tile_bytes = dzt_f16 ? tc_dz_tile_bytes(lo, B) / 2 : tc_dz_tile_bytes(lo, B);

@@ -119,27 +119,6 @@ __device__ __forceinline__ bool named_bar_any(int id, int threads, bool pred)
     return r != 0;
 }
 
-// four 8x8 b16 matrices, transposed on the way in: lane l gives the address of
-// row l % 8 of matrix l / 8 (16 bytes); r[m] then holds, for lane t, column
-// t / 4 of matrix m at rows 2 (t % 4) and 2 (t % 4) + 1 (low half first)
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4])
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
-}
-
-// the inverse fragment order of ldmatrix: r[m] of lane t goes to row t / 4,
-// columns 2 (t % 4) and 2 (t % 4) + 1 of matrix m, whose row l % 8 is at the
-// address lane l = 8 m + l % 8 gives
-__device__ __forceinline__ void stmatrix_x4(uint32_t addr, const uint32_t (&r)[4])
-{
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-                 : "memory");
-}
-
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t bar)
