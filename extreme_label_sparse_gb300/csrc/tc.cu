@@ -120,7 +120,7 @@ FwdPlan plan_fwd(const sg_layout *lo, int B)
     p.w_bytes = (uint32_t)p.nk * lo->G * 128;
     p.stage_bytes = p.a_bytes + p.w_bytes;
     p.S = stages_for(p.stage_bytes);
-    if (p.S < 3)
+    if (p.S < 2)  // two stages still overlap loads with MMAs (G = 64, B = 256 has only room for two)
         return p;
     const int per = p.MT * lo->G;  // accumulator columns of one group
     p.issuers = 4 * per <= 512 ? 2 : 1;
@@ -151,7 +151,7 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
     p.z_bytes = (uint32_t)p.planes * p.nzc * p.MT * 128 * p.zsw;
     p.stage_bytes = p.a_bytes + p.z_bytes;
     p.S = stages_for(p.stage_bytes);
-    if (p.S < 3)
+    if (p.S < 2)
         return p;
     const int per = p.FT * p.Nacc;
     p.issuers = 4 * per <= 512 ? 2 : 1;
