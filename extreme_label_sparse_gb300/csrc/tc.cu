@@ -1,6 +1,7 @@
 // Tensor-core engine (sm_103a): tcgen05 MMA with TMEM accumulators, operands
-// staged in shared memory by TMA (tile loads for W_k and dZ_k, gather4 loads
-// for H_k).  HASTE, key design "gather-once + dense MMA kernel":
+// staged in shared memory by TMA (tile loads for W_k and dZ_k, bulk copies of
+// the step's tiles, a cp.async gather for H_k).  HASTE, key design
+// "gather-once + dense MMA kernel":
 //   forward   Z_k    = H_k W_k^T          M = samples, N = G, K = F
 //   weights   dW_k^T = H_k^T dZ_k         M = F,       N = G, K = samples
 //   features  dH_k   = dZ_k W_k, scattered into the columns I_k of dh
@@ -12,8 +13,8 @@
 //          swizzle.  Read as MN-major A (M = b) by the forward and as K-major A
 //          (M = f, K = b) by the weight gradient.
 //   W_k  : TMA box {64 f, G rows} per 64-wide f chunk, 128-byte swizzle:
-//          K-major B (N = j, K = f) of the forward, MN-major B (N = f, K = j)
-//          of the feature gradient.
+//          K-major B (N = j, K = f) of the forward.  The feature gradient
+//          copies W_k row-major ([G][F]) and scatters its columns.
 //   dZ_k : rows b of min(G,64) j (one chunk per 64 j), swizzle = row width:
 //          MN-major B (N = j, K = b) of the weight gradient, K-major A
 //          (M = b, K = j) of the feature gradient.  From a caller's row-major
@@ -21,14 +22,15 @@
 //          group-tiled workspace whose tiles already hold these bytes, so one
 //          bulk copy brings a group's tile in.
 //
-// Group-tiled dZ workspace (training step only).  Tile k holds, for plane p
-// (0: bf16(dZ), 1: the residual dZ - bf16(dZ)), chunk cj of 64 columns and
-// row r < Bp = 128 ceil(B/128) (rows >= B are zero), the 16-byte unit u of
-// columns 8u .. 8u+7 of that chunk at byte
+// Group-tiled dZ workspace (training step only).  Tile k holds, for plane p,
+// chunk cj of 64 columns and row r < Bp = 128 ceil(B/128) (rows >= B are
+// zero), the 16-byte unit u of columns 8u .. 8u+7 of that chunk at byte
 //     ((p * nzc + cj) * Bp + r) * zsw + ((u ^ swz(r)) * 16),
-// zsw = min(2G, 128) the row width and swz the TMA swizzle of that width.
-// A tile is contiguous (2 Bp G bf16 values per plane pair), so writing it
-// touches one or two pages instead of one page per sample row.
+// zsw = min(2G, 128) the row width and swz the TMA swizzle of that width.  The
+// fused step writes one fp16 plane (the feature gradient's operand); the
+// unfused step writes p = 0: bf16(dZ), p = 1: the residual dZ - bf16(dZ).  A
+// tile is contiguous, so writing it touches one or two pages instead of one
+// page per sample row.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
