@@ -230,6 +230,32 @@ def test_empty_positive_lists(oracle_mod):
     assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
 
 
+_BY_NAME = {w.name: w for w, _ in CASES}
+
+
+@pytest.mark.parametrize("name", ["like3m", "like670k", "like8p6m"])
+def test_step_fused_on_tensor_cores(name, oracle_mod):
+    """The shapes of the three label-space workloads run the whole step on
+    the tensor cores (engine pinned: a CUDA-core fallback would raise) and
+    through the fused forward + BCE + dW kernel (no separate dW launch)."""
+    w = _BY_NAME[name]
+    p = generate(w)
+    ref = oracle_mod.step(p)
+    lay = _layout(p, TC)
+    d = dev_problem(p)
+    dW = torch.empty((w.L, w.F), dtype=torch.int16, device="cuda")
+    dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sg.sg_timing_start(lay, 64)
+    sg.sg_step(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dW, dh, loss)
+    rec = sg.sg_timing_stop(lay)
+    _status_ok(lay)
+    launched = {k for k, (ms, n) in rec.items() if n > 0}
+    assert launched == {"prep", "fwd", "dh"}, rec
+    assert_close(host_bf16_to_f64(dW), ref["dW"], what="dW")
+    assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+
+
 def test_step_large_weights(oracle_mod):
     """|W| far above the fp16 range (W x 2^20, exact in bf16): inside the step
     dh multiplies fp16 copies of dZ and of W scaled by 2^-s, and scales the
