@@ -183,7 +183,5 @@ bool tc_tiled_ok(const sg_layout *lo, int32_t B);
 bool tc_fwdw_ok(const sg_layout *lo, int32_t B);
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
                   double *loss, cudaStream_t st);
-sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW,
-                  float *dh, double *loss, cudaStream_t st);
 
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

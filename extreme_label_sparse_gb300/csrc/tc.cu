@@ -1973,11 +1973,3 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }
-
-sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW, float *dh,
-                  double *loss, cudaStream_t st)
-{
-    (void)lo; (void)B; (void)W; (void)dW; (void)dh; (void)loss; (void)st;
-    sg_set_error("tc_step: the fused step kernel is not built yet");
-    return SG_ERR_UNSUPPORTED;
-}
