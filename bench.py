@@ -62,7 +62,10 @@ MEASURED_TRAFFIC_PER_GROUP = {
 }
 
 
-def algorithmic(w, B, kind, fused_dW=False):
+SGD_LR, SGD_MU = 1e-3, 0.9  # momentum SGD of the --sgd step (values do not change the work)
+
+
+def algorithmic(w, B, kind, fused_dW=False, sgd=False):
     """(bytes, flops) one launch of `kind` must move / do at minimum inside the
     training step.  bf16 W, dW, h; uint16 idx; fp32 dh; positives as int32.
     dZ is internal to the step (no call outputs it), so it is not counted;
@@ -77,6 +80,8 @@ def algorithmic(w, B, kind, fused_dW=False):
     if kind == "step":
         return W_b + W_b + idx_b + h_b + dh_b + nnz_b, 3 * flops_gemm
     if kind == "fwd":      # forward + fused BCE (+ dW when fused)
+        if fused_dW and sgd:  # + the momentum-SGD update: W_out written, fp32 momentum read and written
+            return W_b + W_b + 2 * L * F * 4 + idx_b + h_b + nnz_b, 2 * flops_gemm
         if fused_dW:
             return W_b + W_b + idx_b + h_b + nnz_b, 2 * flops_gemm
         return W_b + idx_b + h_b + nnz_b, flops_gemm
@@ -253,9 +258,17 @@ def run_ours(args):
     dW = torch.empty((w.L, w.F), dtype=torch.int16, device=dev)
     dh = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
     loss = torch.zeros(1, dtype=torch.float64, device=dev)
+    # --sgd: the step with the output layer's momentum-SGD update, weights
+    # double-buffered as a training loop keeps them (dW is the second buffer)
+    mom = torch.zeros((w.L, w.F), dtype=torch.float32, device=dev) if args.sgd else None
+    bufs = [W, dW]
 
     def step(h_, rp_, lb_):
-        sg.sg_step(lay, h_, W, rp_, lb_, p.nnz, dW, dh, loss)
+        if args.sgd:
+            sg.sg_step_sgd(lay, h_, bufs[0], rp_, lb_, p.nnz, SGD_LR, SGD_MU, mom, bufs[1], dh, loss)
+            bufs.reverse()
+        else:
+            sg.sg_step(lay, h_, W, rp_, lb_, p.nnz, dW, dh, loss)
         if world > 1:
             dist.all_reduce(dh)
             dist.all_reduce(loss)
@@ -326,10 +339,10 @@ def run_ours(args):
     dom = max((k for k in kinds if kinds[k][1] > 0), key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
     fused = kinds.get("dW", (0.0, 0))[1] == 0
-    bytes_, flops = algorithmic(w, w.B, dom, fused_dW=fused)
+    bytes_, flops = algorithmic(w, w.B, dom, fused_dW=fused, sgd=args.sgd)
     per_launch_s = dom_ms * 1e-3 / dom_n
     achieved = bytes_ / per_launch_s / 1e9
-    per_group = MEASURED_TRAFFIC_PER_GROUP.get((w.name.split("_L")[0], dom))
+    per_group = None if args.sgd else MEASURED_TRAFFIC_PER_GROUP.get((w.name.split("_L")[0], dom))
     traffic = per_group * w.K if per_group is not None and dom_n else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic, "kernel": dom,
@@ -357,6 +370,7 @@ def run_ours(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "L": w.L, "G": w.G, "F": w.F, "H": w.H,
                    "nnz": p.nnz, "engine": args.engine,
+                   **({"optimizer": f"momentum SGD lr {SGD_LR} mu {SGD_MU} (sg_step_sgd)"} if args.sgd else {}),
                    "l2": f"inputs larger than L2 (W {w.L * w.F * 2 / 1e6:.0f} MB read, dW written each step)",
                    "parallelism": "single GPU" if world == 1 else f"{world} label shards, dh all-reduce"},
         "roofline": roofline,
@@ -385,6 +399,8 @@ def main():
     ap.add_argument("--labels", type=int, default=0,
                     help="override L (a multiple of G) for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sgd", action="store_true",
+                    help="time sg_step_sgd (the step plus the momentum-SGD update of W)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     args = ap.parse_args()

@@ -1,6 +1,8 @@
 // C-ABI entry points of the sg library: argument validation, the layout
 // handle, and dispatch to the tensor-core or CUDA-core engine.  The operations
 // themselves are defined in include/sg.h.
+#include <cmath>
+
 #include "sg_internal.cuh"
 
 #include <cstdarg>
@@ -483,6 +485,56 @@ sg_status sg_bwd(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h, int32_t B,
 }
 
 // ---------------------------------------------------------------- step
+namespace {
+
+// the step after argument checks; with sgd, dW receives the updated weights
+sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
+                    const int32_t *pos_rowptr, const int32_t *pos_label, int64_t nnz, sg_bf16 *dW,
+                    float *dh, double *loss, const sg_sgd *sgd, cudaStream_t st, const char *fn)
+{
+    // the fused forward + BCE + dW kernel and the tensor-core dh, with dZ in
+    // the group-tiled workspace, whenever the shape fits them
+    const bool fused = lo->engine != SG_ENGINE_SIMT && lo->tc_ok && tc_fwdw_ok(lo, B) &&
+                       tc_stage_ok(lo, SG_KIND_DH, B);
+    bool tc_f = fused, tc_w = fused, tc_h = fused;
+    if (!fused) {
+        TRY(pick_tc(lo, SG_KIND_FWD, B, &tc_f, fn));
+        TRY(pick_tc(lo, SG_KIND_DW, B, &tc_w, fn));
+        TRY(pick_tc(lo, SG_KIND_DH, B, &tc_h, fn));
+    }
+    TRY(simt_transpose_h(lo, h, B, st));
+    TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+    // forward + BCE into dZ scratch, then dW and dh from it.  Outside the
+    // fused kernel dZ is kept as two bf16 planes (hi + lo): a single bf16
+    // rounding of dZ, summed over B samples (dW) or over every label (dh),
+    // would move results by more than 2e-2 (1 + |ref|) against the exact
+    // gradient.
+    TRY(ensure_dz_ws(lo));
+    if (fused || (tc_f && tc_w && tc_h && tc_tiled_ok(lo, B))) {
+        // all three on the tensor cores: dZ in the group-tiled workspace
+        uint8_t *dZt = reinterpret_cast<uint8_t *>(lo->dZ_ws);
+        if (fused) {
+            // the fused kernel leaves dZ as one fp16 plane and max |W| for dh
+            // (and applies the optimiser step to dW in its epilogue)
+            TRY(tc_fwdw(lo, B, W, dZt, dW, sgd, loss, st));
+            return tc_dh(lo, nullptr, nullptr, dZt, true, B, W, dh, st);
+        }
+        TRY(tc_fwd(lo, B, W, nullptr, nullptr, nullptr, dZt, loss, st));
+        TRY(tc_dW(lo, nullptr, nullptr, dZt, B, dW, st));
+        TRY(tc_dh(lo, nullptr, nullptr, dZt, false, B, W, dh, st));
+        return sgd ? sgd_update(lo, W, dW, *sgd, st) : SG_OK;
+    }
+    uint16_t *dZ = lo->dZ_ws;
+    uint16_t *dZlo = lo->dZ_ws + (size_t)B * lo->L;
+    TRY(tc_f ? tc_fwd(lo, B, W, nullptr, dZ, dZlo, nullptr, loss, st)
+             : simt_fwd(lo, B, W, nullptr, dZ, dZlo, loss, st));
+    TRY(tc_w ? tc_dW(lo, dZ, dZlo, nullptr, B, dW, st) : simt_dW(lo, dZ, dZlo, B, dW, st));
+    TRY(tc_h ? tc_dh(lo, dZ, dZlo, nullptr, false, B, W, dh, st) : simt_dh(lo, dZ, dZlo, B, W, dh, st));
+    return sgd ? sgd_update(lo, W, dW, *sgd, st) : SG_OK;
+}
+
+}  // namespace
+
 sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
                   const int32_t *pos_rowptr, const int32_t *pos_label,
                   int64_t nnz, sg_bf16 *dW, float *dh, double *loss,
@@ -497,42 +549,34 @@ sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
     REQUIRE(dh, fn);
     REQUIRE(loss, fn);
     DeviceGuard dg(lo->device);
-    cudaStream_t st = (cudaStream_t)stream;
-    // the fused forward + BCE + dW kernel and the tensor-core dh, with dZ in
-    // the group-tiled workspace, whenever the shape fits them
-    const bool fused = lo->engine != SG_ENGINE_SIMT && lo->tc_ok && tc_fwdw_ok(lo, B) &&
-                       tc_stage_ok(lo, SG_KIND_DH, B);
-    bool tc_f = fused, tc_w = fused, tc_h = fused;
-    if (!fused) {
-        TRY(pick_tc(lo, SG_KIND_FWD, B, &tc_f, fn));
-        TRY(pick_tc(lo, SG_KIND_DW, B, &tc_w, fn));
-        TRY(pick_tc(lo, SG_KIND_DH, B, &tc_h, fn));
-    }
-    TRY(simt_transpose_h(lo, h, B, st));
-    TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
-    // forward + BCE into dZ scratch, then dW and dh from it.  dZ is kept as
-    // two bf16 planes (hi + lo): a single bf16 rounding of dZ, summed over B
-    // samples (dW) or over every label (dh), would move results by more than
-    // 2e-2 (1 + |ref|) against the exact gradient.
-    TRY(ensure_dz_ws(lo));
-    if (fused || (tc_f && tc_w && tc_h && tc_tiled_ok(lo, B))) {
-        // all three on the tensor cores: dZ in the group-tiled workspace
-        uint8_t *dZt = reinterpret_cast<uint8_t *>(lo->dZ_ws);
-        if (fused) {
-            // the fused kernel leaves dZ as one fp16 plane and max |W| for dh
-            TRY(tc_fwdw(lo, B, W, dZt, dW, loss, st));
-            return tc_dh(lo, nullptr, nullptr, dZt, true, B, W, dh, st);
-        }
-        TRY(tc_fwd(lo, B, W, nullptr, nullptr, nullptr, dZt, loss, st));
-        TRY(tc_dW(lo, nullptr, nullptr, dZt, B, dW, st));
-        return tc_dh(lo, nullptr, nullptr, dZt, false, B, W, dh, st);
-    }
-    uint16_t *dZ = lo->dZ_ws;
-    uint16_t *dZlo = lo->dZ_ws + (size_t)B * lo->L;
-    TRY(tc_f ? tc_fwd(lo, B, W, nullptr, dZ, dZlo, nullptr, loss, st)
-             : simt_fwd(lo, B, W, nullptr, dZ, dZlo, loss, st));
-    TRY(tc_w ? tc_dW(lo, dZ, dZlo, nullptr, B, dW, st) : simt_dW(lo, dZ, dZlo, B, dW, st));
-    return tc_h ? tc_dh(lo, dZ, dZlo, nullptr, false, B, W, dh, st) : simt_dh(lo, dZ, dZlo, B, W, dh, st);
+    return step_impl(lo, h, B, W, pos_rowptr, pos_label, nnz, dW, dh, loss, nullptr,
+                     (cudaStream_t)stream, fn);
+}
+
+sg_status sg_step_sgd(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W_in,
+                      const int32_t *pos_rowptr, const int32_t *pos_label, int64_t nnz, float lr,
+                      float mu, float *mom, sg_bf16 *W_out, float *dh, double *loss, void *stream)
+{
+    const char *fn = "sg_step_sgd";
+    TRY(check_call(lo, B, fn));
+    TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
+    REQUIRE(h, fn);
+    REQUIRE(W_in, fn);
+    REQUIRE(W_out, fn);
+    REQUIRE(mom, fn);
+    REQUIRE(dh, fn);
+    REQUIRE(loss, fn);
+    if (!std::isfinite(lr) || !std::isfinite(mu))
+        FAIL(SG_ERR_INVALID, "%s: lr and mu must be finite", fn);
+    // dh is taken at W_in after the update has started writing W_out
+    const uintptr_t in0 = (uintptr_t)W_in, out0 = (uintptr_t)W_out;
+    const uintptr_t bytes = (uintptr_t)lo->L * (uintptr_t)lo->F * sizeof(sg_bf16);
+    if (in0 < out0 + bytes && out0 < in0 + bytes)
+        FAIL(SG_ERR_INVALID, "%s: W_out overlaps W_in", fn);
+    DeviceGuard dg(lo->device);
+    const sg_sgd sgd{mom, lr, mu};
+    return step_impl(lo, h, B, W_in, pos_rowptr, pos_label, nnz, W_out, dh, loss, &sgd,
+                     (cudaStream_t)stream, fn);
 }
 
 // ---------------------------------------------------------------- timing

@@ -181,7 +181,15 @@ uint64_t tc_dz_tile_bytes(const sg_layout *lo, int32_t B);
 bool tc_tiled_ok(const sg_layout *lo, int32_t B);
 // fused forward + BCE + dW into the tiled workspace (one pass over the groups)
 bool tc_fwdw_ok(const sg_layout *lo, int32_t B);
+// momentum SGD of the output layer: m <- mu m + dW, W_out <- bf16(W - lr m)
+struct sg_sgd {
+    float *mom;  // [L][F] fp32, read and written
+    float lr, mu;
+};
+// with sgd, dW receives the updated weights instead of the gradient
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
-                  double *loss, cudaStream_t st);
+                  const sg_sgd *sgd, double *loss, cudaStream_t st);
+// the same update from a stored bf16 dW (in place: W_out holds dW on entry)
+sg_status sgd_update(sg_layout *lo, const uint16_t *W, uint16_t *W_out, const sg_sgd &sgd, cudaStream_t st);
 
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -482,3 +482,29 @@ sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }
+
+// ---------------------------------------------------------------- optimiser
+// Momentum SGD of the output layer from a stored bf16 dW (the unfused step):
+// W_out holds dW on entry and the updated weights on return,
+//     m <- mu m + dW,   W_out <- bf16(W - lr m).
+__global__ void __launch_bounds__(256) k_sgd_update(const uint16_t *__restrict__ W, uint16_t *W_out,
+                                                    float *mom, float lr, float mu, int64_t n)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float m = fmaf(mu, mom[i], bf2f(W_out[i]));
+        mom[i] = m;
+        W_out[i] = f2bf(bf2f(W[i]) - lr * m);
+    }
+}
+
+sg_status sgd_update(sg_layout *lo, const uint16_t *W, uint16_t *W_out, const sg_sgd &sgd, cudaStream_t st)
+{
+    const int64_t n = lo->L * (int64_t)lo->F;
+    int64_t grid = ceil_div(n, 256);
+    if (grid > (int64_t)lo->num_sms * 8)
+        grid = (int64_t)lo->num_sms * 8;
+    SG_LAUNCH(lo, SG_KIND_DW, st, k_sgd_update<<<(unsigned)grid, 256, 0, st>>>(W, W_out, sgd.mom, sgd.lr, sgd.mu, n));
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}

@@ -999,8 +999,13 @@ struct FWArgs {
     const uint16_t *idx_s, *hT;
     uint8_t *dZt;
     uint64_t tile_bytes;
-    uint16_t *dW;
+    uint16_t *dW;     // dW, or the updated weights when `mom` is set
     uint32_t *wmax;   // max |W| (bf16 magnitude bits) over the step, for dh
+    // momentum SGD in the dW epilogue (mom != nullptr): m <- mu m + dW,
+    // W_out <- bf16(W - lr m), W_out written where dW would be
+    const uint16_t *W;
+    float *mom;
+    float lr, mu;
     const int32_t *gptr, *gent;
     double *loss_part;
     int32_t *status;
@@ -1267,7 +1272,24 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     const uint32_t col = tbase + lane_off + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G + c0);
                     float v[CH], w[CH];
                     tmem_ld_chunk2<CH>(col, col + (uint32_t)G, v, w);
-                    if (f < F) {
+                    if (f < F && a.mom) {
+                        // the optimiser step on dW while it is in registers
+                        // (lanes run along f: coalesced rows of m and W)
+                        const int64_t e0 = (k * G + c0) * (int64_t)F + f;
+                        float mv[CH];
+                        uint16_t wv[CH];
+#pragma unroll
+                        for (int i = 0; i < CH; ++i) {
+                            mv[i] = a.mom[e0 + (int64_t)i * F];
+                            wv[i] = __ldg(a.W + e0 + (int64_t)i * F);
+                        }
+#pragma unroll
+                        for (int i = 0; i < CH; ++i) {
+                            const float m = fmaf(a.mu, mv[i], v[i] + w[i]);
+                            a.mom[e0 + (int64_t)i * F] = m;
+                            stg[(c0 + i) * F + f] = bf16_rn(__uint_as_float((uint32_t)wv[i] << 16) - a.lr * m);
+                        }
+                    } else if (f < F) {
 #pragma unroll
                         for (int i = 0; i < CH; ++i)
                             stg[(c0 + i) * F + f] = bf16_rn(v[i] + w[i]);
@@ -1726,7 +1748,7 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
 bool tc_fwdw_ok(const sg_layout *lo, int32_t B) { return plan_fwdw(lo, B).ok; }
 
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
-                  double *loss, cudaStream_t st)
+                  const sg_sgd *sgd, double *loss, cudaStream_t st)
 {
     const FWPlan p = plan_fwdw(lo, B);
     if (!p.ok) {
@@ -1747,6 +1769,10 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.tile_bytes = tc_dz_tile_bytes(lo, B) / 2;  // one fp16 plane
     a.dW = dW;
     a.wmax = lo->wmax;
+    a.W = W;
+    a.mom = sgd ? sgd->mom : nullptr;
+    a.lr = sgd ? sgd->lr : 0.f;
+    a.mu = sgd ? sgd->mu : 0.f;
     a.gptr = lo->gptr;
     a.gent = lo->gent;
     a.loss_part = lo->loss_part;

@@ -61,6 +61,7 @@ def load():
             "sg_bwd_dW": ([P, P, P, i32, P, P], C.c_int),
             "sg_bwd_dh": ([P, P, i32, P, P, P], C.c_int),
             "sg_step": ([P, P, i32, P, P, P, i64, P, P, P, P], C.c_int),
+            "sg_step_sgd": ([P, P, i32, P, P, P, i64, C.c_float, C.c_float, P, P, P, P, P], C.c_int),
             "sg_bce_grad_noalloc": ([P, i32, i64, i32, P, P, i64, P, P, P], C.c_int),
             "sg_timing_start": ([P, i32], C.c_int),
             "sg_timing_stop": ([P, P, P], C.c_int),
@@ -261,6 +262,21 @@ def sg_step(layout: Layout, h, W, pos_rowptr, pos_label, nnz: int, dW, dh, loss)
                           _dev(dW, "dW", _BF16, layout.L * layout.F),
                           _dev(dh, "dh", (torch.float32,), B * layout.H),
                           _dev(loss, "loss", (torch.float64,), 1), _stream(h.device)))
+
+
+def sg_step_sgd(layout: Layout, h, W_in, pos_rowptr, pos_label, nnz: int, lr: float, mu: float,
+                mom, W_out, dh, loss):
+    """The step, then the output layer's momentum-SGD update: mom <- mu mom + dW,
+    W_out <- bf16(W_in - lr mom).  W_out must not overlap W_in."""
+    B = _B_of(h, layout.H)
+    n = layout.L * layout.F
+    lb = _dev(pos_label, "pos_label", _I32, nnz) if nnz else C.c_void_p(0)
+    _check(load().sg_step_sgd(layout, _dev(h, "h", _BF16), B, _dev(W_in, "W_in", _BF16, n),
+                              _dev(pos_rowptr, "pos_rowptr", _I32, B + 1), lb, nnz,
+                              float(lr), float(mu), _dev(mom, "mom", (torch.float32,), n),
+                              _dev(W_out, "W_out", _BF16, n),
+                              _dev(dh, "dh", (torch.float32,), B * layout.H),
+                              _dev(loss, "loss", (torch.float64,), 1), _stream(h.device)))
 
 
 # ---------------------------------------------------------------- timing

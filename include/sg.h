@@ -191,6 +191,25 @@ SG_API sg_status sg_step(sg_layout *layout, const sg_bf16 *h, int32_t B,
                   const int32_t *pos_label, int64_t nnz, sg_bf16 *dW,
                   float *dh, double *loss, void *stream);
 
+/* sg_step_sgd -- the training step followed by the output layer's optimiser
+ * step (HASTE, Loss and training strategy: the output layer trains with
+ * momentum SGD; the heavy-ball rule without dampening or weight decay is the
+ * reading taken).  The gradients are those of sg_step at W_in; then, for
+ * every weight,
+ *     m <- mu m + dW,      W_out <- bf16(W_in - lr m)    (fp32 arithmetic)
+ * When the step takes the fused forward + BCE + dW kernel the update is
+ * applied to dW while it is still on chip, and dW is never written.
+ *   W_in[L][F] bf16 (read), W_out[L][F] bf16 (written; must not overlap W_in,
+ *   since dh is taken at W_in), mom[L][F] fp32 (read and written), dh[B][H]
+ *   fp32 and the loss as in sg_step.
+ * Errors: as sg_step; SG_ERR_INVALID for NULL mom / W_out, overlapping W_in and
+ * W_out, or a non-finite lr or mu.                                          */
+SG_API sg_status sg_step_sgd(sg_layout *layout, const sg_bf16 *h, int32_t B,
+                      const sg_bf16 *W_in, const int32_t *pos_rowptr,
+                      const int32_t *pos_label, int64_t nnz, float lr, float mu,
+                      float *mom, sg_bf16 *W_out, float *dh, double *loss,
+                      void *stream);
+
 /* ---------------------------------------------------------------- timing
  * Per-kernel device timing for benchmarks: while enabled, every kernel the
  * library launches for this layout is bracketed by a pair of CUDA events

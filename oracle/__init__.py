@@ -59,6 +59,7 @@ def _load():
                                                 P, P, P, i64, P, P]
             lib.or_feature_grad_rows.argtypes = [i32, i32, i64, i32, i32, P, C.c_int, P, C.c_int,
                                                  P, P, P, i64, P, P, P]
+            lib.or_sgd_momentum.argtypes = [i64, P, P, P, C.c_double, C.c_double, P]
             lib.or_sigmoid.argtypes = [C.c_double]
             lib.or_sigmoid.restype = C.c_double
             lib.or_bce_term.argtypes = [C.c_double, C.c_int]
@@ -184,6 +185,19 @@ def feature_grad(W, dZ, idx_sorted, G: int, H: int) -> np.ndarray:
     dh = np.empty((B, H), dtype=np.float64)
     _load().or_feature_grad(B, H, L, G, F, _ptr(W), Wb, _ptr(dZ), db, _ptr(ids), _ptr(dh))
     return dh
+
+
+def sgd_momentum(W_bits, dW, m, lr: float, mu: float):
+    """One momentum-SGD update of the output layer's weights (O7):
+    m <- mu m + dW, W <- bf16(W - lr m).  Returns (new W bits, new m); the
+    inputs are not modified."""
+    W_bits = np.ascontiguousarray(W_bits, dtype=np.uint16)
+    dW = np.ascontiguousarray(dW, dtype=np.float64)
+    m_new = np.array(m, dtype=np.float64, copy=True, order="C")
+    assert W_bits.shape == dW.shape == m_new.shape
+    W_out = np.empty_like(W_bits)
+    _load().or_sgd_momentum(W_bits.size, _ptr(W_bits), _ptr(dW), _ptr(m_new), float(lr), float(mu), _ptr(W_out))
+    return W_out, m_new
 
 
 # ------------------------------------------------------------------ sampled

@@ -319,6 +319,32 @@ void or_feature_grad(int32_t B, int32_t H, int64_t L, int32_t G, int32_t F,
     }
 }
 
+/* ------------------------------------------------------- O7: momentum SGD
+ * The output layer's optimiser ("Loss and training strategy": the output
+ * layer trains with momentum SGD; the pages give no formula, the plain
+ * heavy-ball rule without dampening or weight decay is the reading taken):
+ *     m <- mu * m + dW,        W <- bf16(W - lr * m)
+ * m is kept in double here; the new W is rounded to the layer's bf16 storage
+ * (double -> fp32 -> bf16, both round-to-nearest-even, as the inputs are
+ * made).                                                                     */
+static uint16_t bf16_round(double x)
+{
+    const float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
+void or_sgd_momentum(int64_t n, const uint16_t *W, const double *dW, double *m, double lr, double mu,
+                     uint16_t *W_out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        m[i] = mu * m[i] + dW[i];
+        W_out[i] = bf16_round(bf16_value(W[i]) - lr * m[i]);
+    }
+}
+
 /* ---------------------------------------------- sampled outputs (full size)
  * The same definitions evaluated only at chosen outputs, from h and W, so a
  * multi-GB problem can be checked without materialising Z.                   */

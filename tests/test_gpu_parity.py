@@ -9,7 +9,7 @@ import torch
 import extreme_label_sparse_gb300 as sg
 from workloads import CONFIGS, Workload, bf16_bits_to_f32, draw_bf16_matrix, generate
 
-from gpu_common import (LOSS_RTOL, assert_close, build_layout, dev_bf16, dev_i32,
+from gpu_common import (LOSS_RTOL, ZTOL, assert_close, build_layout, dev_bf16, dev_i32,
                         dev_problem, host_bf16_to_f64)
 
 pytestmark = pytest.mark.gpu
@@ -254,6 +254,57 @@ def test_step_fused_on_tensor_cores(name, oracle_mod):
     assert launched == {"prep", "fwd", "dh"}, rec
     assert_close(host_bf16_to_f64(dW), ref["dW"], what="dW")
     assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+
+
+@pytest.mark.parametrize("name", ["tiny", "like3m", "like670k", "like8p6m", "b256_f256"])
+def test_step_sgd_two_steps(name, oracle_mod):
+    """sg_step_sgd against the oracle's step followed by its momentum-SGD update
+    (Loss and training strategy), twice, each step from the library's own W and
+    momentum of the step before.  The momentum may differ from the exact one by
+    the gradient's tolerance, W by that times lr plus one bf16 rounding.
+    Covers the fused path (dW never leaves the chip) and the unfused ones."""
+    w = CONFIGS["tiny"] if name == "tiny" else _BY_NAME[name]
+    p = generate(w)
+    lay = build_layout(p)
+    d = dev_problem(p)
+    rng = np.random.default_rng(3)
+    lr, mu = 0.05, 0.9
+    m = (rng.standard_normal((w.L, w.F)) * 0.1).astype(np.float32)
+    W_bits = p.W.copy()
+    for step in range(2):
+        p.W = W_bits
+        ref = oracle_mod.step(p)
+        W_ref, m_ref = oracle_mod.sgd_momentum(W_bits, ref["dW"], m.astype(np.float64), lr, mu)
+        W_in = dev_bf16(W_bits)
+        W_out = torch.empty_like(W_in)
+        mom = torch.from_numpy(m.copy()).cuda()
+        dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+        loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+        sg.sg_step_sgd(lay, d["h"], W_in, d["rowptr"], d["labels"], p.nnz, lr, mu, mom, W_out, dh, loss)
+        _status_ok(lay)
+        m_gpu = mom.cpu().numpy().astype(np.float64)
+        W_gpu = W_out.cpu().numpy().view(np.uint16)
+        m_tol = ZTOL * (1.0 + np.abs(ref["dW"])) + 1e-6 * (1.0 + np.abs(m_ref))
+        assert np.all(np.abs(m_gpu - m_ref) <= m_tol), f"step {step}: momentum"
+        Wg = bf16_bits_to_f32(W_gpu).astype(np.float64)
+        Wr = bf16_bits_to_f32(W_ref).astype(np.float64)
+        assert np.all(np.abs(Wg - Wr) <= 2.0 ** -7 * np.abs(Wr) + lr * m_tol), f"step {step}: W"
+        assert_close(dh.cpu().numpy(), ref["dh"], what=f"step {step}: dh")
+        assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
+        W_bits, m = W_gpu.copy(), mom.cpu().numpy()
+
+
+def test_step_sgd_rejects_aliased_weights():
+    w = CONFIGS["tiny"]
+    p = generate(w)
+    lay = build_layout(p)
+    d = dev_problem(p)
+    mom = torch.zeros((w.L, w.F), dtype=torch.float32, device="cuda")
+    dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    with pytest.raises(sg.SGError) as e:
+        sg.sg_step_sgd(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, 0.1, 0.9, mom, d["W"], dh, loss)
+    assert e.value.status == sg.SG_ERR_INVALID
 
 
 def test_step_large_weights(oracle_mod):

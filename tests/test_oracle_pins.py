@@ -334,3 +334,45 @@ def test_bf16_widening_is_exact(oracle_mod):
     bits = to_bf16_bits(vals)
     for b, v in zip(bits, bf16_bits_to_f32(bits)):
         assert oracle_mod.bf16_value(int(b)) == float(v)
+
+
+# ------------------------------------------------------------------ O7: momentum SGD
+def test_sgd_momentum_matches_torch_optimizer(oracle_mod):
+    """The output layer's momentum SGD (Loss and training strategy) against an
+    independent implementation: torch.optim.SGD (heavy ball, no dampening, no
+    weight decay) in double, three steps with the momentum carried.  Each step
+    starts torch from the oracle's bf16 weights, so the double update must
+    round to the same bf16 and the momentum must agree exactly."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(7)
+    shape = (64, 48)
+    W = to_bf16_bits(rng.standard_normal(shape) * 0.1)
+    m = np.zeros(shape)
+    lr, mu = 0.05, 0.9
+    p = torch.nn.Parameter(torch.zeros(shape, dtype=torch.float64))
+    opt = torch.optim.SGD([p], lr=lr, momentum=mu, dampening=0.0, nesterov=False, weight_decay=0.0)
+    for step in range(3):
+        g = rng.standard_normal(shape)
+        with torch.no_grad():
+            p.copy_(torch.from_numpy(bf16_bits_to_f32(W).astype(np.float64)))
+        p.grad = torch.from_numpy(g.copy())
+        opt.step()
+        W, m = oracle_mod.sgd_momentum(W, g, m, lr, mu)
+        buf = opt.state[p]["momentum_buffer"].numpy()
+        np.testing.assert_array_equal(m, buf)
+        assert np.array_equal(W, to_bf16_bits(p.detach().numpy())), step
+
+
+def test_sgd_momentum_special_cases(oracle_mod):
+    """lr = 0 leaves W bit-identical; mu = 0 makes the momentum the gradient
+    itself (plain SGD: W - lr dW, rounded once to bf16)."""
+    rng = np.random.default_rng(11)
+    W = to_bf16_bits(rng.standard_normal((16, 32)))
+    g = rng.standard_normal((16, 32))
+    m0 = rng.standard_normal((16, 32))
+    W1, m1 = oracle_mod.sgd_momentum(W, g, m0, 0.0, 0.5)
+    assert np.array_equal(W1, W)
+    np.testing.assert_array_equal(m1, 0.5 * m0 + g)
+    W2, m2 = oracle_mod.sgd_momentum(W, g, m0, 0.25, 0.0)
+    np.testing.assert_array_equal(m2, g)
+    assert np.array_equal(W2, to_bf16_bits(bf16_bits_to_f32(W).astype(np.float64) - 0.25 * g))
