@@ -1026,7 +1026,10 @@ struct CtlFW {
 // The MMA issue loops have compile-time trip counts (FK = F/16 K steps, MT
 // sample tiles): tcgen05.mma issued from a loop with a run-time trip count
 // measured about 2x slower per instruction than the same MMAs unrolled.
-template <int G_, int FK, int MT>
+//
+// SGD: the dW epilogue applies the momentum-SGD update instead of storing dW
+// (its own instance, so the plain step's kernel carries none of that code).
+template <int G_, int FK, int MT, bool SGD>
 __global__ void __launch_bounds__(kFWThreads, 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
 {
@@ -1258,6 +1261,18 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 if (dw == 0 && lane == 0)
                     mbar_arrive(bar_addr(c.empty[s]));  // done with the stage's W_k
                 // ---- dW_k
+                if (SGD) {
+                    // the optimiser step's rows of m and W into L2 while the
+                    // dW MMA runs (lane r: row k G + r, this warp's 32 f)
+                    for (int r = lane; r < G; r += 32) {
+#pragma unroll
+                        for (int tf = 0; tf < (FK + 7) / 8; ++tf) {
+                            const int64_t e = (k * G + r) * (int64_t)F + tf * 128 + q * 32;
+                            prefetch_l2(a.mom + e);
+                            prefetch_l2(a.W + e);
+                        }
+                    }
+                }
                 if (!mbar_wait(bar_addr(cf.wfull[ws]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
                     break;
                 tc_fence_after();
@@ -1272,7 +1287,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     const uint32_t col = tbase + lane_off + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G + c0);
                     float v[CH], w[CH];
                     tmem_ld_chunk2<CH>(col, col + (uint32_t)G, v, w);
-                    if (f < F && a.mom) {
+                    if (SGD && f < F) {
                         // the optimiser step on dW while it is in registers
                         // (lanes run along f: coalesced rows of m and W)
                         const int64_t e0 = (k * G + c0) * (int64_t)F + f;
@@ -1805,7 +1820,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
 #define SG_FW_PICK(GG, KK, MM)                                           \
     if (lo->G == GG && lo->F == KK * 16 && p.MT == MM)                   \
-        kern = k_tc_fwdw<GG, KK, MM>;
+        kern = sgd ? k_tc_fwdw<GG, KK, MM, true> : k_tc_fwdw<GG, KK, MM, false>;
     SG_FW_PICK(16, 4, 1) SG_FW_PICK(16, 4, 2) SG_FW_PICK(32, 4, 1) SG_FW_PICK(32, 4, 2)
     SG_FW_PICK(64, 4, 1) SG_FW_PICK(64, 4, 2)
     SG_FW_PICK(16, 8, 1) SG_FW_PICK(16, 8, 2) SG_FW_PICK(16, 16, 1) SG_FW_PICK(16, 16, 2)

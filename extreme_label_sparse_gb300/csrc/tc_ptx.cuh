@@ -168,6 +168,12 @@ __device__ __forceinline__ void bulk_wait()
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// bring the line holding p into L2 (no register, no completion to wait for)
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------------ cp.async
 // 16-byte global -> shared copy through L2 (no L1 allocation)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
