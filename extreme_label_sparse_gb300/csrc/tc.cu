@@ -939,11 +939,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // ================================================================== fused forward + BCE + dW
 // One pass over the groups for the training step: per group the producers
 // gather H_k and load W_k, one MMA warp computes Z_k = H_k W_k^T, the epilogue
-// turns it into dZ_k (BCE), writes dZ_k to the group-tiled workspace (for dh)
-// and into shared memory, and a second MMA warp computes dW_k^T = H_k^T dZ_k
-// from the same shared-memory H_k, so H_k is gathered once and dZ_k is never
-// read back for dW.  Warps: the producers, one forward MMA warp, one dW MMA
-// warp, eight BCE warps and four dW store warps.
+// turns it into dZ_k (BCE), writes it to the group-tiled workspace as one fp16
+// plane (for dh) and into shared memory as bf16 value + residual planes, and a
+// second MMA warp computes dW_k^T = H_k^T [dZ_hi | dZ_lo] from the same
+// shared-memory H_k, so H_k is gathered once and dZ_k is never read back for
+// dW.  The dW warps store dW_k (or, in the SGD instance, apply the momentum
+// update to it and store the new W_k) and record max |W| for dh's fp16 scale.
+// Warps: the producers, one forward MMA warp, one dW MMA warp, eight BCE
+// warps and four dW warps.
 constexpr int kFWBce = 8;  // BCE warps: two per TMEM lane quarter
 constexpr int kFWDw = 4;   // dW store warps: one per lane quarter
 constexpr int kFWThreads = 32 * (kProdWarps + 2 + kFWBce + kFWDw);
