@@ -271,7 +271,7 @@ sg_status sg_layout_build(const int32_t *groups, int64_t L, int32_t G,
         free_layout(lo);
         return rc;
     }
-    lo->tc_ok = tc_supported(lo);
+    lo->tc_ok = tc_supported(lo) || tc_step_ok(lo, max_B < 128 ? max_B : 128);
     *out = lo;
     return SG_OK;
 }
@@ -492,6 +492,13 @@ sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W
                     const int32_t *pos_rowptr, const int32_t *pos_label, int64_t nnz, sg_bf16 *dW,
                     float *dh, double *loss, const sg_sgd *sgd, cudaStream_t st, const char *fn)
 {
+    // the whole step in one kernel on CTA clusters (dZ never leaves the chip)
+    // whenever the shape fits it
+    if (!sgd && lo->engine != SG_ENGINE_SIMT && tc_step_ok(lo, B)) {
+        TRY(simt_transpose_h(lo, h, B, st));
+        TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+        return tc_step(lo, B, W, dW, dh, loss, st);
+    }
     // the fused forward + BCE + dW kernel and the tensor-core dh, with dZ in
     // the group-tiled workspace, whenever the shape fits them
     const bool fused = lo->engine != SG_ENGINE_SIMT && lo->tc_ok && tc_fwdw_ok(lo, B) &&

@@ -48,6 +48,10 @@ struct sg_layout {
     // the step's max |W| as bf16 magnitude bits (scale of dh's fp16 operands)
     uint32_t *wmax = nullptr;
 
+    // resident clusters of the fused step kernel for the shape keyed by
+    // step_ncl_key (0 until the first call)
+    int64_t step_ncl = 0, step_ncl_key = 0;
+
     // per-kernel event timing (sg_timing_start / sg_timing_stop)
     struct Timer {
         bool on = false;
@@ -191,5 +195,12 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
                   const sg_sgd *sgd, double *loss, cudaStream_t st);
 // the same update from a stored bf16 dW (in place: W_out holds dW on entry)
 sg_status sgd_update(sg_layout *lo, const uint16_t *W, uint16_t *W_out, const sg_sgd &sgd, cudaStream_t st);
+
+// step.cu: the whole step (forward, BCE, dW, dh) in one kernel on clusters
+// of CTAs that split dh's columns (B <= 128, G in {16, 32, 64}, F % 16 == 0,
+// F <= 128)
+bool tc_step_ok(const sg_layout *lo, int32_t B);
+sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW, float *dh, double *loss,
+                  cudaStream_t st);
 
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

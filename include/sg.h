@@ -224,7 +224,7 @@ typedef enum sg_kernel_kind {
     SG_KIND_BCE = 2,     /* BCE from a stored Z                          */
     SG_KIND_DW = 3,      /* weight gradient                              */
     SG_KIND_DH = 4,      /* feature gradient                             */
-    SG_KIND_STEP = 5,    /* reserved: a single-kernel whole step         */
+    SG_KIND_STEP = 5,    /* the whole step in one kernel (fwd+BCE+dW+dh) */
     SG_KIND_COUNT = 6
 } sg_kernel_kind;
 
