@@ -6,10 +6,15 @@ Split-K feature gradient dh) on synthetic data shaped like the Amazon-3M tail.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  `value` = label-logits per second (B*L per s,
-summed over ranks) with inputs resident in HBM; `e2e` = the same through the
-public API from pinned host buffers (h and positives copied in, loss copied out
-every step); `roofline` = the dominant kernel's algorithmic bytes / its mean
-launch time (CUDA events on its own stream) against the measured HBM peak;
+summed over ranks) with inputs resident in HBM, timed without per-kernel
+instrumentation; `e2e` = the same through the public API from pinned host
+buffers (h and positives copied in, loss copied out every step); `roofline` =
+the dominant kernel's algorithmic bytes / its mean launch time (CUDA events
+around each launch, in a separate loop) against the measured HBM peak;
+`roofline_step` = the whole step's algorithmic bytes and FLOPs over the step
+time against both peaks; `workloads` = step time, per-kernel split and step
+roofline of the other label-space workloads and of the group-size sweep
+(G = 1, 16, 32, 64 with uniform and clustered index sets);
 `cpu_baseline` = the CPU oracle on a bounded sample of the same workload.
 `--impl reference` times that oracle alone (there is no other implementation
 of the method to run).
@@ -219,6 +224,116 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ our arm
+class Runner:
+    """One workload on the device: inputs resident, a layout, and the step
+    through the public API (sg_step, or sg_step_sgd)."""
+
+    def __init__(self, sg, torch, dev, p, engine, sgd=False, world=1, dist=None):
+        import numpy as _np
+        self.sg, self.torch, self.dev, self.p, self.sgd = sg, torch, dev, p, sgd
+        self.world, self.dist = world, dist
+        w = p.w
+
+        def i32(a):
+            return torch.from_numpy(_np.ascontiguousarray(a, dtype=_np.int32)).to(dev)
+
+        def bf(a):
+            return torch.from_numpy(_np.ascontiguousarray(a).view(_np.int16)).to(dev)
+
+        self.h, self.W = bf(p.h), bf(p.W)
+        self.rowptr, self.labels = i32(p.pos_rowptr), i32(p.pos_label if p.nnz else _np.zeros(1))
+        self.lay = sg.sg_layout_build(i32(p.groups), w.L, w.G, i32(p.idx.reshape(-1)), w.F, w.H,
+                                      w.B, max(p.nnz, 1))
+        sg.sg_layout_set_engine(self.lay, engine)
+        self.dW = torch.empty((w.L, w.F), dtype=torch.int16, device=dev)
+        self.dh = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+        self.loss = torch.zeros(1, dtype=torch.float64, device=dev)
+        # --sgd: the step with the output layer's momentum-SGD update, weights
+        # double-buffered as a training loop keeps them (dW is the second buffer)
+        self.mom = torch.zeros((w.L, w.F), dtype=torch.float32, device=dev) if sgd else None
+        self.bufs = [self.W, self.dW]
+
+    def step(self, h=None, rp=None, lb=None):
+        sg, p = self.sg, self.p
+        h = self.h if h is None else h
+        rp = self.rowptr if rp is None else rp
+        lb = self.labels if lb is None else lb
+        if self.sgd:
+            sg.sg_step_sgd(self.lay, h, self.bufs[0], rp, lb, p.nnz, SGD_LR, SGD_MU, self.mom,
+                           self.bufs[1], self.dh, self.loss)
+            self.bufs.reverse()
+        else:
+            sg.sg_step(self.lay, h, self.W, rp, lb, p.nnz, self.dW, self.dh, self.loss)
+        if self.world > 1:
+            self.dist.all_reduce(self.dh)
+            self.dist.all_reduce(self.loss)
+
+    def timed(self, steps, stream, barrier=lambda: None):
+        """ms per step over `steps` steps, CUDA events on `stream`, no
+        per-kernel instrumentation inside the timed loop."""
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            self.step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return e0.elapsed_time(e1) / steps
+
+    def per_kind(self, steps):
+        """{kind: (total ms, launches)} over `steps` steps, every kernel
+        bracketed by CUDA events on the stream it is launched on."""
+        self.sg.sg_timing_start(self.lay, 64 * steps)
+        for _ in range(steps):
+            self.step()
+        self.torch.cuda.synchronize()
+        return self.sg.sg_timing_stop(self.lay)
+
+    def status(self):
+        return self.sg.sg_layout_status(self.lay)
+
+    def close(self):
+        self.lay.close()
+
+
+def step_roofline(w, ms, hbm, tflops):
+    """Whole-step work against the binding roofline: the step's algorithmic
+    bytes (W read, dW written, idx, h, dh, positives) and FLOPs (6 B L F)
+    over the measured step time."""
+    bytes_, flops = algorithmic(w, w.B, "step")
+    s = ms * 1e-3
+    gbs, tfs = bytes_ / s / 1e9, flops / s / 1e12
+    t_hbm, t_tc = bytes_ / (hbm * 1e9), flops / (tflops * 1e12)
+    return {"bound": "hbm" if t_hbm >= t_tc else "tensor", "bytes": bytes_, "flops": flops,
+            "achieved_gbs": gbs, "achieved_tflops": tfs, "frac_hbm": gbs / hbm,
+            "frac_tensor": tfs / tflops, "frac": max(t_hbm, t_tc) / s,
+            "t_bound_us": max(t_hbm, t_tc) * 1e6}
+
+
+def measure_other(sg, torch, dev, p, engine, steps, warmup, stream, hbm, tflops):
+    """Step time, per-kind split and the step roofline of one more workload."""
+    r = Runner(sg, torch, dev, p, engine)
+    try:
+        for _ in range(warmup):
+            r.step()
+        torch.cuda.synchronize()
+        ms = r.timed(steps, stream)
+        kinds = r.per_kind(steps)
+        st = r.status()
+    finally:
+        r.close()
+    w = p.w
+    out = {"ms_per_step": ms, "label_logits_per_s": w.B * w.L / (ms * 1e-3),
+           "per_kind_ms_per_step": {k: v[0] / steps for k, v in kinds.items() if v[1]},
+           "launches_per_step": {k: v[1] / steps for k, v in kinds.items() if v[1]},
+           "roofline_step": step_roofline(w, ms, hbm, tflops), "status": st,
+           "config": {"B": w.B, "L": w.L, "G": w.G, "F": w.F, "H": w.H, "idx": w.idx_mode}}
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -238,81 +353,63 @@ def run_ours(args):
     w = CONFIGS[args.workload]
     if args.labels:
         w = w.with_(L=args.labels, name=f"{w.name}_L{args.labels}")
+    engine = {"auto": sg.SG_ENGINE_AUTO, "simt": sg.SG_ENGINE_SIMT, "tc": sg.SG_ENGINE_TC,
+              "fused": sg.SG_ENGINE_FUSED}[args.engine]
+    hbm, tflops, peak_src = _peaks()
+
+    # the other workloads (label-space shapes and the group-size sweep) are
+    # drawn on host threads while the headline workload is measured
+    others = []
+    if rank == 0 and world == 1 and not args.labels:
+        if not args.no_others:
+            others += [n for n in ("amazon670k_tail", "lf8p6m_tail") if n != w.name]
+        if not args.no_sweep:
+            others += [f"sweep_g{g}_{m}" for g in (1, 16, 32, 64) for m in ("uniform", "clustered")]
+    pool = None
+    futures = []
+    if others:
+        from concurrent.futures import ThreadPoolExecutor
+        pool = ThreadPoolExecutor(max_workers=3)
+        futures = [(n, pool.submit(generate, CONFIGS[n])) for n in others]
+
     # weak scaling: every rank owns one shard of w.L labels (its own groups,
     # W rows and positives; h is shared); dh and the loss are summed over the
     # shards with one all-reduce each
     p = generate(w, shard=rank)
-
-    def i32(a):
-        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
-
-    def bf(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
-
-    h, W = bf(p.h), bf(p.W)
-    rowptr, labels = i32(p.pos_rowptr), i32(p.pos_label)
-    lay = sg.sg_layout_build(i32(p.groups), w.L, w.G, i32(p.idx.reshape(-1)), w.F, w.H,
-                             w.B, max(p.nnz, 1))
-    engine = {"auto": sg.SG_ENGINE_AUTO, "simt": sg.SG_ENGINE_SIMT, "tc": sg.SG_ENGINE_TC}[args.engine]
-    sg.sg_layout_set_engine(lay, engine)
-    dW = torch.empty((w.L, w.F), dtype=torch.int16, device=dev)
-    dh = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
-    loss = torch.zeros(1, dtype=torch.float64, device=dev)
-    # --sgd: the step with the output layer's momentum-SGD update, weights
-    # double-buffered as a training loop keeps them (dW is the second buffer)
-    mom = torch.zeros((w.L, w.F), dtype=torch.float32, device=dev) if args.sgd else None
-    bufs = [W, dW]
-
-    def step(h_, rp_, lb_):
-        if args.sgd:
-            sg.sg_step_sgd(lay, h_, bufs[0], rp_, lb_, p.nnz, SGD_LR, SGD_MU, mom, bufs[1], dh, loss)
-            bufs.reverse()
-        else:
-            sg.sg_step(lay, h_, W, rp_, lb_, p.nnz, dW, dh, loss)
-        if world > 1:
-            dist.all_reduce(dh)
-            dist.all_reduce(loss)
+    r = Runner(sg, torch, dev, p, engine, sgd=args.sgd, world=world, dist=dist)
 
     def barrier():
         if world > 1:
             dist.barrier()
 
     for _ in range(max(args.warmup, 3)):
-        step(h, rowptr, labels)
+        r.step()
     torch.cuda.synchronize()
-    if sg.sg_layout_status(lay) != 0:
+    if r.status() != 0:
         raise RuntimeError("device status set during warm-up")
 
-    # ---- device-timed region: inputs resident in HBM
+    # ---- device-timed region: inputs resident in HBM, no instrumentation
     stream = torch.cuda.current_stream(dev)
     clocks = ClockSampler(local)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    sg.sg_timing_start(lay, 64 * args.steps)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step(h, rowptr, labels)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    kinds = sg.sg_timing_stop(lay)
-    barrier()
+    ms = r.timed(args.steps, stream, barrier)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     value = world * w.B * w.L / (ms * 1e-3)
+    # ---- per-kernel split (a separate loop: every kernel between CUDA events)
+    kinds = r.per_kind(args.steps)
 
     # ---- end to end through the public API: host buffers, copies timed
     h_host = torch.from_numpy(np.ascontiguousarray(p.h).view(np.int16)).pin_memory()
     rp_host = torch.from_numpy(p.pos_rowptr.astype(np.int32)).pin_memory()
     lb_host = torch.from_numpy(p.pos_label.astype(np.int32)).pin_memory()
     loss_host = torch.zeros(1, dtype=torch.float64).pin_memory()
-    h_d, rp_d, lb_d = torch.empty_like(h), torch.empty_like(rowptr), torch.empty_like(labels)
+    h_d, rp_d, lb_d = torch.empty_like(r.h), torch.empty_like(r.rowptr), torch.empty_like(r.labels)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     e0.record(stream)
@@ -320,8 +417,8 @@ def run_ours(args):
         h_d.copy_(h_host, non_blocking=True)
         rp_d.copy_(rp_host, non_blocking=True)
         lb_d.copy_(lb_host, non_blocking=True)
-        step(h_d, rp_d, lb_d)
-        loss_host.copy_(loss, non_blocking=True)
+        r.step(h_d, rp_d, lb_d)
+        loss_host.copy_(r.loss, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -331,11 +428,10 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_e2e = float(t.item())
     h2d = h_host.numel() * 2 + rp_host.numel() * 4 + lb_host.numel() * 4
-    if sg.sg_layout_status(lay) != 0:
+    if r.status() != 0:
         raise RuntimeError("device status set during the timed region")
 
-    # ---- roofline of the dominant kernel
-    hbm, tflops, peak_src = _peaks()
+    # ---- roofline of the dominant kernel (per launch) and of the whole step
     dom = max((k for k in kinds if kinds[k][1] > 0), key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
     fused = kinds.get("dW", (0.0, 0))[1] == 0
@@ -346,6 +442,7 @@ def run_ours(args):
     traffic = per_group * w.K if per_group is not None and dom_n else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "traffic": traffic, "kernel": dom,
+                "scope": "per launch of the dominant kernel",
                 "peak_source": peak_src,
                 "launch_ms": per_launch_s * 1e3,
                 "tensor_tflops": flops / per_launch_s / 1e12 if flops else 0.0,
@@ -361,8 +458,18 @@ def run_ours(args):
                "sample": (f"first {b['n_groups']} of {w.K} groups ({b['n_groups'] * w.G} labels), "
                           f"all {w.B} samples; positives + forward + BCE + dW + dh in double, "
                           f"{b['seconds']:.1f} s")}
-
     launches = sum(v[1] for v in kinds.values())
+    r.close()
+    del r
+
+    workloads = {}
+    for name, fut in futures:
+        po = fut.result()
+        workloads[name] = measure_other(sg, torch, dev, po, engine, args.other_steps, 2, stream, hbm, tflops)
+        del po
+    if pool is not None:
+        pool.shutdown()
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
@@ -374,15 +481,17 @@ def run_ours(args):
                    "l2": f"inputs larger than L2 (W {w.L * w.F * 2 / 1e6:.0f} MB read, dW written each step)",
                    "parallelism": "single GPU" if world == 1 else f"{world} label shards, dh all-reduce"},
         "roofline": roofline,
+        "roofline_step": step_roofline(w, ms, hbm, tflops),
         "cpu_baseline": cpu,
         "e2e": {"value": world * w.B * w.L / (ms_e2e * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 8},
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if workloads:
+        line["workloads"] = workloads
     if rank == 0:
         print(json.dumps(line), flush=True)
-    lay.close()
     if world > 1:
         dist.destroy_process_group()
     return 0
@@ -395,13 +504,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(CONFIGS))
-    ap.add_argument("--engine", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--engine", choices=["auto", "simt", "tc", "fused"], default="auto",
+                    help="fused: the whole step in one cluster kernel wherever it fits")
     ap.add_argument("--labels", type=int, default=0,
                     help="override L (a multiple of G) for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sgd", action="store_true",
                     help="time sg_step_sgd (the step plus the momentum-SGD update of W)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the group-size sweep (G = 1, 16, 32, 64; uniform and clustered idx)")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the other label-space workloads (670K- and 8.6M-shaped tails)")
+    ap.add_argument("--other-steps", type=int, default=5,
+                    help="timed steps of each other workload and sweep point")
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -90,7 +90,7 @@ sg_status pick_tc(const sg_layout *lo, int stage, int32_t B, bool *tc, const cha
     if (lo->engine == SG_ENGINE_SIMT)
         return SG_OK;
     const bool ok = lo->tc_ok && tc_stage_ok(lo, stage, B);
-    if (!ok && lo->engine == SG_ENGINE_TC)
+    if (!ok && (lo->engine == SG_ENGINE_TC || lo->engine == SG_ENGINE_FUSED))
         FAIL(SG_ERR_UNSUPPORTED, "%s: this shape (B=%d G=%d F=%d H=%d) is outside the "
              "tensor-core engine", fn, B, lo->G, lo->F, lo->H);
     *tc = ok;
@@ -312,9 +312,10 @@ sg_status sg_layout_set_engine(sg_layout *lo, int32_t engine)
     const char *fn = "sg_layout_set_engine";
     if (!lo)
         FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
-    if (engine != SG_ENGINE_AUTO && engine != SG_ENGINE_SIMT && engine != SG_ENGINE_TC)
+    if (engine != SG_ENGINE_AUTO && engine != SG_ENGINE_SIMT && engine != SG_ENGINE_TC &&
+        engine != SG_ENGINE_FUSED)
         FAIL(SG_ERR_INVALID, "%s: unknown engine %d", fn, engine);
-    if (engine == SG_ENGINE_TC && !lo->tc_ok)
+    if ((engine == SG_ENGINE_TC || engine == SG_ENGINE_FUSED) && !lo->tc_ok)
         FAIL(SG_ERR_UNSUPPORTED, "%s: the tensor-core engine needs G %% 16 == 0 and "
              "F %% 16 == 0 (G=%d, F=%d)", fn, lo->G, lo->F);
     lo->engine = engine;
@@ -492,9 +493,13 @@ sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W
                     const int32_t *pos_rowptr, const int32_t *pos_label, int64_t nnz, sg_bf16 *dW,
                     float *dh, double *loss, const sg_sgd *sgd, cudaStream_t st, const char *fn)
 {
-    // the whole step in one kernel on CTA clusters (dZ never leaves the chip)
-    // whenever the shape fits it
-    if (!sgd && lo->engine != SG_ENGINE_SIMT && tc_step_ok(lo, B)) {
+    // shapes the fused forward + BCE + dW kernel and the dh kernel cannot run
+    // (e.g. F not a multiple of 64) take the whole step in one kernel on CTA
+    // clusters, where it fits: dZ never leaves the chip there, but on the
+    // shapes both paths run it measures slower than the two-kernel path
+    const bool two_kernel = lo->engine != SG_ENGINE_SIMT && tc_fwdw_ok(lo, B) && tc_stage_ok(lo, SG_KIND_DH, B);
+    if (!sgd && lo->engine != SG_ENGINE_SIMT && (!two_kernel || lo->engine == SG_ENGINE_FUSED) &&
+        tc_step_ok(lo, B)) {
         TRY(simt_transpose_h(lo, h, B, st));
         TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
         return tc_step(lo, B, W, dW, dh, loss, st);

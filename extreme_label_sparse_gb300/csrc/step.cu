@@ -25,13 +25,19 @@
 // contribution with fp32 CUDA-core arithmetic and atomics instead.
 //
 // Shared memory (from a 1024-byte aligned base):
-//   [S stages: H_k (2 sample chunks x F rows x 128 B, 128-byte swizzle),
-//              W of the C groups (TMA boxes of CW columns x G rows),
-//              I of the C groups]
-//   [2 x dZ bf16 value + residual planes (dW operand)]
+//   [SH H slots: the own group's H_k (sample chunks of 64 x F rows x 128 B,
+//                128-byte swizzle)]
+//   [SW W slots: W of the C groups (TMA boxes of CW columns x G rows), then
+//                I of the C groups]
+//   [dZ bf16 value + residual planes (dW operand)]
 //   [2 x C fp16 dZ tiles (dh operand): slot g holds group C*step + g]
 //   [2 x Ws (band rows of 2G bytes)]
 // TMEM: dh band [0, BW), Z slots [BW, BW + 2G), dW slot [BW + 2G, BW + 4G).
+//
+// Warp roles: producers (cp.async gather of H_k; TMA of the W and I rows),
+// one MMA-issuing warp each for the forward, dW and dh, one warp that copies
+// the other CTAs' dZ tiles, the BCE team, the dW-store team and the Ws
+// builders (ldmatrix.trans of W_k's column blocks, fp16, one row per f).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,42 +47,71 @@
 
 using namespace tc;
 
+// Timeline hooks for profiling builds (-DSG_STEP_TRACE): every warp of the
+// first cluster records clock64() at marked points of steps [kTrT0, kTrT0 +
+// kTrN) into the buffer set with sg_step_trace_set.  Compiled out otherwise.
+#ifdef SG_STEP_TRACE
+__device__ unsigned long long *g_step_trace = nullptr;
+constexpr int kTrT0 = 100, kTrN = 64, kTrW = 24, kTrS = 16;
+#define STEP_TRACE(slot, itv)                                                                              \
+    do {                                                                                                   \
+        if (g_step_trace && blockIdx.x < 2 && (itv) >= kTrT0 && (itv) < kTrT0 + kTrN && (threadIdx.x & 31) == 0) \
+            g_step_trace[((((size_t)blockIdx.x * kTrW + (threadIdx.x >> 5)) * kTrN + ((itv) - kTrT0)) * kTrS) + \
+                         (slot)] = clock64();                                                              \
+    } while (0)
+extern "C" __attribute__((visibility("default"))) int sg_step_trace_set(void *p)
+{
+    return (int)cudaMemcpyToSymbol(g_step_trace, &p, sizeof(p));
+}
+#else
+#define STEP_TRACE(slot, itv) \
+    do {                      \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int kP = 4;     // producer warps
 constexpr int kBce = 8;   // BCE warps: two per TMEM lane quarter
-constexpr int kDw = 4;    // dW store + tile copy warps: one per lane quarter
-constexpr int kBld = 4;   // Ws builder warps: one thread per feature f
-constexpr int kWA = kP;   // forward and dW MMA warp
-constexpr int kWB = kP + 1;  // dh MMA warp
-constexpr int kW0Bce = kP + 2;
+constexpr int kDw = 4;    // dW store warps: one per lane quarter
+constexpr int kBld = 4;   // Ws builder warps
+constexpr int kWF = kP;          // forward MMA warp
+constexpr int kWD = kP + 1;      // dW MMA warp
+constexpr int kWH = kP + 2;      // dh MMA warp
+constexpr int kWC = kP + 3;      // copies the other CTAs' dZ tiles
+constexpr int kW0Bce = kP + 4;
 constexpr int kW0Dw = kW0Bce + kBce;
 constexpr int kW0Bld = kW0Dw + kDw;
 constexpr int kWarps = kW0Bld + kBld;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxC = 4;
-constexpr int kMaxS = 4;
+constexpr int kMaxSH = 4, kMaxSW = 4;
 constexpr int kMaxF = 128;
+constexpr int kMaxBlk = kMaxF / 8 / kBld;  // column blocks of W_k per builder warp
 // dynamic shared memory the plan may use (the opt-in maximum is 227 KB,
 // less the static control block)
-constexpr int kSmemBudget = 227 * 1024 - 1024;
+constexpr int kSmemBudget = 227 * 1024 - 3072;
 // named barriers
-constexpr int kBarBce = 1, kBarDw = 2, kBarBld = 3;
+constexpr int kBarBce = 1, kBarBld = 3;
 
 struct StepCtl {
-    uint64_t full[kMaxS], empty[kMaxS];
-    uint64_t zfull[2], zempty[2];      // Z slots
-    uint64_t dzwfull[2], dzwempty[2];  // dZ bf16 planes (dW operand)
-    uint64_t wfull, wempty;            // dW slot
-    uint64_t dzhfull[2];               // the step's fp16 tiles are all in place
-    uint64_t dzhdone[2];               // the local dh MMAs are done with them
-    uint64_t dzready[2];               // the other CTAs wrote their tiles (cluster)
-    uint64_t dzcopied[2];              // the other CTAs copied this CTA's tile (cluster)
-    uint64_t wsfull[2], wsempty[2];    // Ws buffers
-    uint64_t drainA, drainB;
+    uint64_t hfull[kMaxSH], hempty[kMaxSH];  // H ring
+    uint64_t wfull[kMaxSW], wempty[kMaxSW];  // W ring
+    uint64_t zfull[2], zempty[2];            // Z slots
+    uint64_t dzwfull, dzwempty;              // dZ bf16 planes (dW operand)
+    uint64_t dwfull, dwempty;                // dW slot
+    uint64_t dzhfull[2];                     // the step's fp16 tiles are all in place
+    uint64_t dzhdone[2];                     // the local dh MMAs are done with them
+    uint64_t dzready[2];                     // the other CTAs wrote their tiles (cluster)
+    uint64_t dzcopied[2];                    // the other CTAs copied this CTA's tile (cluster)
+    uint64_t wsfull[2], wsempty[2];          // Ws buffers
+    uint64_t drain[3];
     uint32_t tmem;
     int abort_flag;
     double red[kBce];
+    // per builder lane and column block: the Ws row it wrote in buffer 0 / 1
+    // (-1: none), zeroed the next time the buffer is used
+    int16_t rowtab[2][kMaxBlk][kBld * 32];
 };
 
 struct StepArgs {
@@ -87,9 +122,9 @@ struct StepArgs {
     double *loss_part;
     int32_t *status;
     int64_t K, NPS;  // groups; steps of C groups
-    int32_t B, F, H, ldB, C, BW, S, CW, nbc;
-    uint32_t h_bytes, w_bytes, i_bytes, stage_bytes, dzw_bytes, ws_bytes;
-    uint32_t off_dzw, off_dzh, off_ws;
+    int32_t B, F, H, ldB, C, BW, SH, SW, nbc;
+    uint32_t h_bytes, w_bytes, i_bytes, wslot_bytes, ws_bytes;
+    uint32_t off_w, off_dzw, off_dzh, off_ws;
 };
 
 __device__ __forceinline__ uint32_t bar_addr(const uint64_t &b) { return smem_u32(&b); }
@@ -101,7 +136,37 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, status));
 }
 
-template <int G_>
+__device__ __forceinline__ int groups_in_step(const StepArgs &a, int64_t ps)
+{
+    return (int)(a.K - ps * a.C < a.C ? a.K - ps * a.C : a.C);
+}
+
+// The band's part of dh for a group whose W_k holds a magnitude >= 2^15 in
+// the band (beyond fp16's exact range): dh[b][i0 + row] += sum_j dZ[b][j]
+// W[j][f] in fp32 from the fp16 dZ tile (rows of zsw bytes, swizzle of that
+// width) and the bf16 W_k box layout (rows of 2 CW bytes).  Out of line: it
+// runs rarely and stays out of the instruction cache of the common path.
+__device__ __noinline__ void dh_band_fp32(const uint8_t *tile, int zsw, const uint8_t *Wg, int G, int CW, int f,
+                                          int row, int i0, int B, int H, float *dh)
+{
+    const int fc = f % CW;
+    const uint32_t wrow = 2u * CW, wch = (uint32_t)G * wrow;
+    const uint8_t *colp = Wg + (size_t)(f / CW) * wch + (fc & 7) * 2;
+    for (int bb = 0; bb < B; ++bb) {
+        float acc = 0.f;
+        const int zr = swz_of(bb, zsw);
+        for (int j = 0; j < G; ++j) {
+            const uint32_t wbits = *reinterpret_cast<const uint16_t *>(
+                colp + (size_t)j * wrow + ((((fc >> 3) ^ swz_of(j, (int)wrow))) << 4));
+            const __half zh = *reinterpret_cast<const __half *>(tile + (size_t)bb * zsw +
+                                                                 ((((j * 2) >> 4) ^ zr) << 4) + (j & 7) * 2);
+            acc = fmaf(__half2float(zh), __uint_as_float(wbits << 16), acc);
+        }
+        atomicAdd(dh + (size_t)bb * H + i0 + row, acc);
+    }
+}
+
+template <int G_, int CW>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__ CUtensorMap tm_w, const StepArgs a)
 {
     constexpr int G = G_;
@@ -109,14 +174,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
     constexpr uint32_t ZCH = 128u * ZSW;              // one dZ plane (128 sample rows)
     constexpr int RB = 2 * G;                         // bytes of a Ws row
     constexpr int CHB = G / 2;                        // BCE columns per warp
-    constexpr int DCH = G < 32 ? G : 32;              // dW columns per TMEM load
+    constexpr int DCH = G < 16 ? G : 16;              // dW columns per TMEM load
+    constexpr int NI = G / 8;                         // 8-row blocks of W_k (one per Ws 16-byte unit)
+    constexpr uint32_t WROW = 2u * CW;                // bytes of a row of one W box
+    constexpr uint32_t WCH = (uint32_t)G * WROW;      // bytes of one W box
     __shared__ StepCtl c;
     extern __shared__ uint8_t dsm[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *bp = dsm + (base - smem_u32(dsm));
-    const int C = a.C, S = a.S, BW = a.BW, F = a.F, CW = a.CW;
-    const uint32_t WCH = (uint32_t)G * CW * 2;  // bytes of one TMA box of W
+    const int C = a.C, SH = a.SH, SW = a.SW, BW = a.BW, F = a.F;
     const uint32_t rank = cluster_rank();
     const int64_t cl = cluster_index(), ncl = cluster_count();
     const int i0 = (int)rank * BW;  // first dh column of this CTA's band
@@ -124,15 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
 
     if (threadIdx.x == 0) {
         c.abort_flag = 0;
-        for (int s = 0; s < S && s < kMaxS; ++s) {
-            mbar_init(bar_addr(c.full[s]), kP * 32 + 1);
-            mbar_init(bar_addr(c.empty[s]), 2);
+        for (int s = 0; s < SH && s < kMaxSH; ++s) {
+            mbar_init(bar_addr(c.hfull[s]), kP * 32);
+            mbar_init(bar_addr(c.hempty[s]), 1);
+        }
+        for (int s = 0; s < SW && s < kMaxSW; ++s) {
+            mbar_init(bar_addr(c.wfull[s]), 1);
+            mbar_init(bar_addr(c.wempty[s]), 2);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c.zfull[i]), 1);
             mbar_init(bar_addr(c.zempty[i]), kBce * 32);
-            mbar_init(bar_addr(c.dzwfull[i]), kBce * 32);
-            mbar_init(bar_addr(c.dzwempty[i]), 1);
             mbar_init(bar_addr(c.dzhfull[i]), C > 1 ? 2 : 1);
             mbar_init(bar_addr(c.dzhdone[i]), 1);
             mbar_init(bar_addr(c.dzready[i]), C > 1 ? C - 1 : 1);
@@ -140,17 +209,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             mbar_init(bar_addr(c.wsfull[i]), 1);
             mbar_init(bar_addr(c.wsempty[i]), 1);
         }
-        mbar_init(bar_addr(c.wfull), 1);
-        mbar_init(bar_addr(c.wempty), kDw * 32);
-        mbar_init(bar_addr(c.drainA), 1);
-        mbar_init(bar_addr(c.drainB), 1);
+        mbar_init(bar_addr(c.dzwfull), kBce * 32);
+        mbar_init(bar_addr(c.dzwempty), 1);
+        mbar_init(bar_addr(c.dwfull), 1);
+        mbar_init(bar_addr(c.dwempty), kDw * 32);
+        for (int i = 0; i < 3; ++i)
+            mbar_init(bar_addr(c.drain[i]), 1);
         fence_mbar_init();
     }
-    if (warp == kWA) {
+    if (warp == kWF) {
         tmem_alloc(smem_u32(&c.tmem), 512);
         tmem_relinquish();
     }
-    // the Ws buffers start zeroed; the builders rewrite only the rows they use
+    for (int i = threadIdx.x; i < 2 * kMaxBlk * kBld * 32; i += kThreads)
+        (&c.rowtab[0][0][0])[i] = -1;
+    // the Ws buffers start zeroed; the builders rewrite only the words they use
     for (uint32_t o = threadIdx.x * 16u; o < 2 * a.ws_bytes; o += kThreads * 16u)
         *reinterpret_cast<uint4 *>(bp + a.off_ws + o) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async();
@@ -160,145 +233,173 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
     tc_fence_after();
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
-
     if (warp < kP) {
         // ---------------------------------------------------------- producers
-        // per step: W_k and I_k of every group of the step (TMA / bulk copies,
-        // thread 0), and the own group's H_k by cp.async: producer warp pw
-        // copies rows [pw RW, pw RW + RW) of H_k, two 256-byte hT rows per
-        // instruction (16 lanes each; only the first chunk of 64 samples
-        // when B <= 64)
+        // thread 0: W_k and I_k of every group of the step (TMA / bulk copy)
+        // into the W ring.  Every producer thread: its share of the own group's
+        // H_k by cp.async into the H ring -- warp pw copies rows
+        // [pw RW, pw RW + RW), two 256-byte hT rows per instruction (16 lanes
+        // each; only the first 64 samples when B <= 64).  The gather's index
+        // rows are loaded one step ahead.
         const int t = threadIdx.x;
         const int RW = F / kP;
         const int u = lane & 15, rsub = lane >> 4;
-        const int ulim = a.nbc * 8;  // 16-byte units per row that are copied
+        const int ulim = a.nbc * 8;
+        uint32_t nrow = 0;
+        if (cl < a.NPS && (int64_t)cl * C + rank < a.K && lane < RW)
+            nrow = __ldg(a.idx_s + ((int64_t)cl * C + rank) * F + warp * RW + lane);
         int it = 0;
+        bool ok = true;
         for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            const int sh = it % SH, sw = it % SW;
             const int64_t k0 = ps * C;
-            const int ng = (int)(a.K - k0 < C ? a.K - k0 : C);
+            const int ng = groups_in_step(a, ps);
             const bool own = (int)rank < ng;
-            uint32_t myrow = 0;
-            if (own && lane < RW)
-                myrow = __ldg(a.idx_s + (k0 + rank) * F + warp * RW + lane);
-            if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, a.status))
-                break;
-            const uint32_t st = base + (uint32_t)s * a.stage_bytes;
-            const uint32_t fb = bar_addr(c.full[s]);
-            if (t == 0) {
-                mbar_arrive_expect_tx(fb, (uint32_t)ng * (a.w_bytes + 2u * F));
-                for (int g = 0; g < ng; ++g) {
-                    const uint32_t wd = st + a.h_bytes + (uint32_t)g * a.w_bytes;
-                    for (int ch = 0; ch * CW < F; ++ch)
-                        tma_load_2d(wd + (uint32_t)ch * WCH, &tm_w, ch * CW, (int)((k0 + g) * G), fb);
-                    bulk_load(st + a.h_bytes + (uint32_t)C * a.w_bytes + (uint32_t)g * a.i_bytes,
-                              a.idx_s + (k0 + g) * F, 2u * F, fb);
+            STEP_TRACE(0, it);
+            const uint32_t myrow = nrow;
+            const int64_t kn = (ps + ncl) * C + rank;
+            if (ps + ncl < a.NPS && kn < a.K && lane < RW)
+                nrow = __ldg(a.idx_s + kn * F + warp * RW + lane);
+            if (t == 0 && ok) {
+                ok = mbar_wait(bar_addr(c.wempty[sw]), ((uint32_t)(it / SW) & 1u) ^ 1u, abort_flag, a.status);
+                if (ok) {
+                    const uint32_t wfb = bar_addr(c.wfull[sw]);
+                    const uint32_t ws = base + a.off_w + (uint32_t)sw * a.wslot_bytes;
+                    mbar_arrive_expect_tx(wfb, (uint32_t)ng * (a.w_bytes + 2u * F));
+                    for (int g = 0; g < ng; ++g) {
+                        for (int ch = 0; ch * CW < F; ++ch)
+                            tma_load_2d(ws + (uint32_t)g * a.w_bytes + (uint32_t)ch * WCH, &tm_w, ch * CW,
+                                        (int)((k0 + g) * G), wfb);
+                        bulk_load(ws + (uint32_t)C * a.w_bytes + (uint32_t)g * a.i_bytes, a.idx_s + (k0 + g) * F,
+                                  2u * F, wfb);
+                    }
                 }
             }
+            STEP_TRACE(1, it);
+            if (!mbar_wait(bar_addr(c.hempty[sh]), ((uint32_t)(it / SH) & 1u) ^ 1u, abort_flag, a.status))
+                break;
+            STEP_TRACE(2, it);
             if (own) {  // warp-uniform: every lane takes part in the shuffles
+                const uint32_t hs = base + (uint32_t)sh * a.h_bytes;
                 for (int r0 = 0; r0 < RW; r0 += 2) {
                     const int rr = r0 + rsub;
                     const uint32_t row = __shfl_sync(0xffffffffu, myrow, rr & 31);
                     const int f = warp * RW + rr;
                     if (u < ulim)
-                        cp_async16(st + (uint32_t)(u >> 3) * F * 128 + (uint32_t)f * 128 +
+                        cp_async16(hs + (uint32_t)(u >> 3) * F * 128 + (uint32_t)f * 128 +
                                        (uint32_t)(((u & 7) ^ (f & 7)) << 4),
                                    a.hT + (size_t)row * a.ldB + u * 8);
                 }
             }
-            cp_async_arrive_noinc(fb);
+            STEP_TRACE(3, it);
+            cp_async_arrive_noinc(bar_addr(c.hfull[sh]));
         }
         cp_async_wait_all();
-        if (*abort_flag)
-            for (int j = it - S < 0 ? 0 : it - S; j < it; ++j)
-                mbar_wait_drain(bar_addr(c.full[j % S]), (uint32_t)(j / S) & 1u);
-    } else if (warp == kWA) {
-        // ---------------------------------------------------------- forward + dW MMA
-        // the forward of a step's group is issued before the dW of the previous
-        // one, so the BCE warps find the next Z ready when they finish a group
+        if (*abort_flag) {
+            for (int j = it - SH < 0 ? 0 : it - SH; j < it; ++j)
+                mbar_wait_drain(bar_addr(c.hfull[j % SH]), (uint32_t)(j / SH) & 1u);
+            if (t == 0)
+                for (int j = it - SW < 0 ? 0 : it - SW; j < it; ++j)
+                    mbar_wait_drain(bar_addr(c.wfull[j % SW]), (uint32_t)(j / SW) & 1u);
+        }
+    } else if (warp == kWF) {
+        // ---------------------------------------------------------- forward MMA
         const uint32_t idf = idesc_bf16(128, G, 1, 0);
-        const uint32_t idw = idesc_bf16(128, 2 * G, 0, 1);
-        const uint32_t wlay = layout_for_swizzle(2 * CW);
-        const uint32_t zlay = layout_for_swizzle(ZSW);
-        const int kb = a.nbc * 4;  // K steps of 16 samples of the dW MMA
-        int it = 0, io = 0, prev_s = 0;
-        bool ok = true;
-        auto issue_dw = [&](int j, int s) -> bool {
-            const int db = j & 1;
-            if (!warp_wait(bar_addr(c.dzwfull[db]), (uint32_t)(j >> 1) & 1u, abort_flag, a.status))
-                return false;
-            if (!warp_wait(bar_addr(c.wempty), ((uint32_t)j & 1u) ^ 1u, abort_flag, a.status))
-                return false;
-            tc_fence_after();
-            fence_proxy_async();
-            if (lane == 0) {
-                const uint32_t A = base + (uint32_t)s * a.stage_bytes;
-                const uint32_t Zs = base + a.off_dzw + (uint32_t)db * a.dzw_bytes;
-                for (int st = 0; st < kb; ++st) {
-                    // A: H_k^T, K-major (rows f, K = samples): sample chunk st/4, 32 B per 16 samples
-                    const uint64_t ad = sdesc(A + (uint32_t)(st >> 2) * F * 128 + (uint32_t)(st & 3) * 32, 16, 1024,
-                                              kLayoutSW128);
-                    // B: [hi | lo] dZ_k, MN-major (N = j, K = samples), the lo plane ZCH further on
-                    const uint64_t bd = sdesc(Zs + (uint32_t)st * 16 * ZSW, ZCH, 8 * ZSW, zlay);
-                    mma_bf16(tbase + col_w, ad, bd, idw, st > 0 ? 1u : 0u);
-                }
-                mma_commit(bar_addr(c.wfull));
-                mma_commit(bar_addr(c.dzwempty[db]));
-                mma_commit(bar_addr(c.empty[s]));  // last reader of H_k (and, earlier, of W_k)
-            }
-            __syncwarp();
-            return true;
-        };
+        constexpr uint32_t wlay = CW == 64 ? kLayoutSW128 : CW == 32 ? kLayoutSW64 : kLayoutSW32;
+        int it = 0, io = 0;
         for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it) {
-            const int s = it % S;
-            const int ng = (int)(a.K - ps * C < C ? a.K - ps * C : C);
-            if (!warp_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status)) {
-                ok = false;
+            const int sh = it % SH, sw = it % SW;
+            STEP_TRACE(0, it);
+            if (!warp_wait(bar_addr(c.wfull[sw]), (uint32_t)(it / SW) & 1u, abort_flag, a.status))
                 break;
-            }
-            if ((int)rank >= ng) {  // no own group: the stage only carries the others' W_k
+            STEP_TRACE(1, it);
+            if ((int)rank >= groups_in_step(a, ps)) {  // no own group this step
                 if (lane == 0)
-                    mbar_arrive(bar_addr(c.empty[s]));
+                    mbar_arrive(bar_addr(c.wempty[sw]));
                 __syncwarp();
                 continue;
             }
             const int zs = io & 1;
-            if (!warp_wait(bar_addr(c.zempty[zs]), ((uint32_t)(io >> 1) & 1u) ^ 1u, abort_flag, a.status)) {
-                ok = false;
+            if (!warp_wait(bar_addr(c.hfull[sh]), (uint32_t)(it / SH) & 1u, abort_flag, a.status))
                 break;
-            }
+            STEP_TRACE(2, it);
+            if (!warp_wait(bar_addr(c.zempty[zs]), ((uint32_t)(io >> 1) & 1u) ^ 1u, abort_flag, a.status))
+                break;
+            STEP_TRACE(3, it);
             tc_fence_after();
             fence_proxy_async();  // cp.async-written H_k -> the MMA (async proxy)
             if (lane == 0) {
-                const uint32_t A = base + (uint32_t)s * a.stage_bytes;
-                const uint32_t Wt = A + a.h_bytes + rank * a.w_bytes;
+                const uint32_t A = base + (uint32_t)sh * a.h_bytes;
+                const uint32_t Wt = base + a.off_w + (uint32_t)sw * a.wslot_bytes + rank * a.w_bytes;
                 for (int st = 0; st < F / 16; ++st) {
                     // A: H_k, MN-major (M = samples); 8 f rows per 1024-byte atom
                     const uint64_t ad = sdesc(A + (uint32_t)st * 2048, (uint32_t)F * 128, 1024, kLayoutSW128);
-                    // B: W_k, K-major; box st*16/CW, 32 bytes per 16 f inside a 2 CW-byte row
+                    // B: W_k, K-major; box st*16/CW, 32 bytes per 16 f inside a row
                     const int f0 = st * 16;
-                    const uint64_t bd = sdesc(Wt + (uint32_t)(f0 / CW) * WCH + (uint32_t)(f0 % CW) * 2, 16,
-                                              8 * 2 * CW, wlay);
+                    const uint64_t bd =
+                        sdesc(Wt + (uint32_t)(f0 / CW) * WCH + (uint32_t)(f0 % CW) * 2, 16, 8 * WROW, wlay);
                     mma_bf16(tbase + col_z + (uint32_t)(zs * G), ad, bd, idf, st > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_addr(c.zfull[zs]));
+                mma_commit(bar_addr(c.wempty[sw]));  // done with the own W_k
             }
             __syncwarp();
-            if (io > 0 && !issue_dw(io - 1, prev_s)) {
-                ok = false;
-                break;
-            }
-            prev_s = s;
+            STEP_TRACE(4, it);
             ++io;
         }
-        if (ok && io > 0)
-            issue_dw(io - 1, prev_s);
         if (lane == 0)
-            mma_commit(bar_addr(c.drainA));
+            mma_commit(bar_addr(c.drain[0]));
         __syncwarp();
-        mbar_wait_drain(bar_addr(c.drainA), 0);
-    } else if (warp == kWB) {
+        mbar_wait_drain(bar_addr(c.drain[0]), 0);
+    } else if (warp == kWD) {
+        // ---------------------------------------------------------- dW MMA
+        const uint32_t idw = idesc_bf16(128, 2 * G, 0, 1);
+        constexpr uint32_t zlay = ZSW == 128 ? kLayoutSW128 : ZSW == 64 ? kLayoutSW64 : kLayoutSW32;
+        const int kb = a.nbc * 4;  // K steps of 16 samples
+        int it = 0, io = 0;
+        for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it) {
+            const int sh = it % SH;
+            // this warp sees the H barrier itself before its MMAs read the cp.async data
+            if (!warp_wait(bar_addr(c.hfull[sh]), (uint32_t)(it / SH) & 1u, abort_flag, a.status))
+                break;
+            if ((int)rank >= groups_in_step(a, ps)) {
+                if (lane == 0)
+                    mbar_arrive(bar_addr(c.hempty[sh]));
+                __syncwarp();
+                continue;
+            }
+            STEP_TRACE(0, it);
+            if (!warp_wait(bar_addr(c.dzwfull), (uint32_t)io & 1u, abort_flag, a.status))
+                break;
+            STEP_TRACE(1, it);
+            if (!warp_wait(bar_addr(c.dwempty), ((uint32_t)io & 1u) ^ 1u, abort_flag, a.status))
+                break;
+            STEP_TRACE(2, it);
+            tc_fence_after();
+            fence_proxy_async();
+            if (lane == 0) {
+                const uint32_t A = base + (uint32_t)sh * a.h_bytes;
+                const uint32_t Zs = base + a.off_dzw;
+                for (int st = 0; st < kb; ++st) {
+                    // A: H_k^T, K-major (rows f, K = samples): sample chunk st/4, 32 B per 16 samples
+                    const uint64_t ad =
+                        sdesc(A + (uint32_t)(st >> 2) * F * 128 + (uint32_t)(st & 3) * 32, 16, 1024, kLayoutSW128);
+                    // B: [hi | lo] dZ_k, MN-major (N = j, K = samples), the lo plane ZCH further on
+                    const uint64_t bd = sdesc(Zs + (uint32_t)st * 16 * ZSW, ZCH, 8 * ZSW, zlay);
+                    mma_bf16(tbase + col_w, ad, bd, idw, st > 0 ? 1u : 0u);
+                }
+                mma_commit(bar_addr(c.dwfull));
+                mma_commit(bar_addr(c.dzwempty));
+                mma_commit(bar_addr(c.hempty[sh]));  // last reader of H_k
+            }
+            __syncwarp();
+            ++io;
+        }
+        if (lane == 0)
+            mma_commit(bar_addr(c.drain[1]));
+        __syncwarp();
+        mbar_wait_drain(bar_addr(c.drain[1]), 0);
+    } else if (warp == kWH) {
         // ---------------------------------------------------------- dh MMA
         // A: a group's fp16 dZ tile (K-major, rows = samples); B: Ws (K-major,
         // rows = the band's dh columns); accumulated in TMEM over every group
@@ -312,19 +413,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
         bool ok = true;
         for (int64_t ps = cl; ps < a.NPS && ok; ps += ncl, ++it) {
             const int db = it & 1;
-            const int ng = (int)(a.K - ps * C < C ? a.K - ps * C : C);
+            const int ng = groups_in_step(a, ps);
+            STEP_TRACE(0, it);
             if (!warp_wait(bar_addr(c.dzhfull[db]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
                 break;
+            STEP_TRACE(1, it);
             for (int g = 0; g < ng; ++g, ++gi) {
                 const int wb = gi & 1;
                 if (!warp_wait(bar_addr(c.wsfull[wb]), (uint32_t)(gi >> 1) & 1u, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
+                STEP_TRACE(2 + g, it);
                 tc_fence_after();
                 if (lane == 0) {
                     const uint64_t au = adesc0 + (uint64_t)((base + a.off_dzh + (uint32_t)(db * C + g) * ZCH) >> 4);
                     const uint64_t bu = bdesc0 + (uint64_t)((base + a.off_ws + (uint32_t)wb * a.ws_bytes) >> 4);
+#pragma unroll
                     for (int ks = 0; ks < G / 16; ++ks) {
                         mma_bf16(tbase, au + (uint64_t)((ks * 32) >> 4), bu + (uint64_t)((ks * 32) >> 4), id0, accf);
                         if (n1 > 0)
@@ -343,9 +448,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             __syncwarp();
         }
         if (lane == 0)
-            mma_commit(bar_addr(c.drainB));
+            mma_commit(bar_addr(c.drain[2]));
         __syncwarp();
-        mbar_wait_drain(bar_addr(c.drainB), 0);
+        mbar_wait_drain(bar_addr(c.drain[2]), 0);
+    } else if (warp == kWC) {
+        // ---------------------------------------------------------- tile copies
+        // the other CTAs' fp16 dZ tiles of a step, by distributed-shared-memory
+        // loads, into this CTA's buffer for the step
+        constexpr int NV = (int)(ZCH / (32 * 16));  // 16-byte loads per lane per tile
+        constexpr int NB = NV > 8 ? 8 : NV;          // loads in flight per lane
+        int it = 0;
+        for (int64_t ps = cl; ps < a.NPS && C > 1; ps += ncl, ++it) {
+            const int db = it & 1;
+            const uint32_t dph = (uint32_t)(it >> 1) & 1u;
+            const int ng = groups_in_step(a, ps);
+            STEP_TRACE(0, it);
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(c.dzready[db]), dph, abort_flag, a.status)))
+                break;
+            STEP_TRACE(1, it);
+            if (!warp_wait(bar_addr(c.dzhdone[db]), dph ^ 1u, abort_flag, a.status))
+                break;
+            STEP_TRACE(2, it);
+            for (int p = 0; p < ng; ++p) {
+                if (p == (int)rank)
+                    continue;
+                const uint32_t off = a.off_dzh + (uint32_t)(db * C + p) * ZCH;
+                const uint32_t src = mapa(base + off, (uint32_t)p);
+#pragma unroll
+                for (int x0 = 0; x0 < NV; x0 += NB) {
+                    uint4 v[NB];
+#pragma unroll
+                    for (int x = 0; x < NB; ++x)
+                        v[x] = ld_dsmem16(src + (uint32_t)(lane + (x0 + x) * 32) * 16u);
+#pragma unroll
+                    for (int x = 0; x < NB; ++x)
+                        *reinterpret_cast<uint4 *>(bp + off + (uint32_t)(lane + (x0 + x) * 32) * 16u) = v[x];
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            STEP_TRACE(3, it);
+            if (lane == 0) {
+                mbar_arrive(bar_addr(c.dzhfull[db]));
+                // the copied values are in use already: nothing to publish
+                for (int p = 0; p < C; ++p)
+                    if (p != (int)rank)
+                        mbar_arrive_remote_relaxed(mapa(bar_addr(c.dzcopied[db]), (uint32_t)p));
+            }
+            __syncwarp();
+        }
     } else if (warp < kW0Dw) {
         // ---------------------------------------------------------- BCE
         const int q = warp & 3;
@@ -353,44 +504,67 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
         const int b = q * 32 + lane;  // sample row of this thread
         const int c0 = sub * CHB;     // first column of this warp
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        double lacc = 0.0;
+        double lacc = 0.0;  // folded in from lf every 32 groups (fp64 is slow on this part)
+        float lf = 0.f;
         int it = 0, io = 0;
+        // positive-list bounds of the own group, loaded one step ahead
+        int e0n = 0, e1n = 0;
+        if (cl < a.NPS && (int64_t)cl * C + rank < a.K) {
+            e0n = __ldg(a.gptr + (int64_t)cl * C + rank);
+            e1n = __ldg(a.gptr + (int64_t)cl * C + rank + 1);
+        }
         for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it) {
             const int db = it & 1;
             const uint32_t dph = (uint32_t)(it >> 1) & 1u;
             const int64_t k = ps * C + rank;
             const bool own = k < a.K;
+            const int e0 = e0n, e1 = e1n;
+            const int64_t kn = k + ncl * C;
+            if (kn < a.K) {
+                e0n = __ldg(a.gptr + kn);
+                e1n = __ldg(a.gptr + kn + 1);
+            }
             bool ok = true;
+            STEP_TRACE(0, it);
             if (own) {
                 const int zs = io & 1;
-                const int e0 = __ldg(a.gptr + k), e1 = __ldg(a.gptr + k + 1);
                 float v[CHB];
                 ok = warp_wait(bar_addr(c.zfull[zs]), (uint32_t)(io >> 1) & 1u, abort_flag, a.status);
+                STEP_TRACE(1, it);
                 if (ok) {
                     tc_fence_after();
                     tmem_ld_chunk<CHB>(tbase + lane_off + col_z + (uint32_t)(zs * G + c0), v);
+                    STEP_TRACE(2, it);
                     tc_fence_before();
                     mbar_arrive(bar_addr(c.zempty[zs]));
                     if (b < a.B) {
                         const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CHB) : 0u;
-                        lacc += bce_chunk<CHB>(v, y);
+                        lf += bce_chunk_ftz<CHB>(v, y);
+                        if ((io & 31) == 31) {
+                            lacc += (double)lf;
+                            lf = 0.f;
+                        }
                     } else {
 #pragma unroll
                         for (int i = 0; i < CHB; ++i)
                             v[i] = 0.f;
                     }
                 }
-                const int dbw = io & 1;
-                ok = ok && mbar_wait(bar_addr(c.dzwempty[dbw]), ((uint32_t)(io >> 1) & 1u) ^ 1u, abort_flag, a.status);
+                STEP_TRACE(3, it);
+                ok = ok && mbar_wait(bar_addr(c.dzwempty), ((uint32_t)io & 1u) ^ 1u, abort_flag, a.status);
+                STEP_TRACE(4, it);
                 if (ok) {
-                    store_dz_tile<CHB>(bp + a.off_dzw + (size_t)dbw * a.dzw_bytes, b, c0, v, ZSW, 1, 128);
+                    store_dz_tile<CHB>(bp + a.off_dzw, b, c0, v, ZSW, 1, 128);
                     fence_proxy_async();
-                    mbar_arrive(bar_addr(c.dzwfull[dbw]));
+                    mbar_arrive(bar_addr(c.dzwfull));
                 }
+                STEP_TRACE(5, it);
                 // the own fp16 tile: once the local dh MMAs and the other CTAs'
                 // copies of this buffer's previous step are done
                 ok = ok && mbar_wait(bar_addr(c.dzhdone[db]), dph ^ 1u, abort_flag, a.status);
+                STEP_TRACE(6, it);
                 ok = ok && (C == 1 || mbar_wait_cluster(bar_addr(c.dzcopied[db]), dph ^ 1u, abort_flag, a.status));
+                STEP_TRACE(7, it);
                 if (ok) {
                     store_dz_tile_f16<CHB>(bp + a.off_dzh + (size_t)(db * C + (int)rank) * ZCH, b, c0, v, ZSW, 128);
                     fence_proxy_async();
@@ -402,10 +576,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
                 ok = mbar_wait(bar_addr(c.dzhdone[db]), dph ^ 1u, abort_flag, a.status);
                 ok = ok && (C == 1 || mbar_wait_cluster(bar_addr(c.dzcopied[db]), dph ^ 1u, abort_flag, a.status));
             }
+            STEP_TRACE(8, it);
             if (named_bar_any(kBarBce, kBce * 32, !ok))
                 break;
+            STEP_TRACE(9, it);
             if (threadIdx.x == kW0Bce * 32) {
-                fence_acq_rel_cluster();
+                // the team's tile writes precede this release (bar.sync orders them)
                 mbar_arrive(bar_addr(c.dzhfull[db]));
                 for (int p = 0; p < C; ++p)
                     if (p != (int)rank)
@@ -413,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             }
         }
         // loss partial of the CTA (fixed order)
-        double v = lacc;
+        double v = lacc + (double)lf;
         for (int o = 16; o > 0; o >>= 1)
             v += __shfl_down_sync(0xffffffffu, v, o);
         if (lane == 0)
@@ -427,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
         }
         // the band's partial of dh (lanes = samples, columns = dh columns
         // i0 ..) added into dh once, after the last dh MMA
-        if (__all_sync(0xffffffffu, mbar_wait(bar_addr(c.drainB), 0, abort_flag, a.status) && !*abort_flag) &&
+        if (__all_sync(0xffffffffu, mbar_wait(bar_addr(c.drain[2]), 0, abort_flag, a.status) && !*abort_flag) &&
             it > 0) {
             tc_fence_after();
             const int half = BW / 2;
@@ -456,161 +632,182 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             }
         }
     } else if (warp < kW0Bld) {
-        // ---------------------------------------------------------- tile copies + dW
+        // ---------------------------------------------------------- dW stores
         const int q = warp & 3;
         const int f = q * 32 + lane;  // lane of the dW^T accumulator
-        const int tt = threadIdx.x - kW0Dw * 32;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        int it = 0, io = 0;
-        for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it) {
-            const int db = it & 1;
-            const uint32_t dph = (uint32_t)(it >> 1) & 1u;
-            const int64_t k0 = ps * C;
-            const int ng = (int)(a.K - k0 < C ? a.K - k0 : C);
-            bool ok = true;
-            if (C > 1) {
-                // the other CTAs' fp16 tiles of this step into the local buffer
-                ok = mbar_wait_cluster(bar_addr(c.dzready[db]), dph, abort_flag, a.status);
-                ok = ok && mbar_wait(bar_addr(c.dzhdone[db]), dph ^ 1u, abort_flag, a.status);
-                if (ok) {
-                    for (int p = 0; p < ng; ++p) {
-                        if (p == (int)rank)
-                            continue;
-                        const uint32_t off = a.off_dzh + (uint32_t)(db * C + p) * ZCH;
-                        const uint32_t src = mapa(base + off, (uint32_t)p);
-                        for (uint32_t o = (uint32_t)tt * 16u; o < ZCH; o += kDw * 32 * 16u)
-                            *reinterpret_cast<uint4 *>(bp + off + o) = ld_dsmem16(src + o);
-                    }
-                    fence_proxy_async();
+        int io = 0;
+        for (int64_t ps = cl; ps < a.NPS; ps += ncl) {
+            const int64_t k = ps * C + rank;
+            if (k >= a.K)
+                break;  // the own groups are a prefix of the steps
+            // dW_k^T accumulator [f][hi j | lo j] -> dW rows k G + j
+            STEP_TRACE(0, io);
+            if (!warp_wait(bar_addr(c.dwfull), (uint32_t)io & 1u, abort_flag, a.status))
+                break;
+            STEP_TRACE(1, io);
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < G; cc += DCH) {
+                float v[DCH], w[DCH];
+                tmem_ld_chunk2<DCH>(tbase + lane_off + col_w + (uint32_t)cc,
+                                    tbase + lane_off + col_w + (uint32_t)(G + cc), v, w);
+                if (cc + DCH >= G) {
+                    tc_fence_before();
+                    mbar_arrive(bar_addr(c.dwempty));  // the slot is in registers
                 }
-                if (named_bar_any(kBarDw, kDw * 32, !ok))
-                    break;
-                if (tt == 0) {
-                    mbar_arrive(bar_addr(c.dzhfull[db]));
-                    for (int p = 0; p < C; ++p)
-                        if (p != (int)rank)
-                            mbar_arrive_remote(mapa(bar_addr(c.dzcopied[db]), (uint32_t)p));
+                if (f < F) {
+                    uint16_t *dst = a.dW + (k * G + cc) * F + f;
+#pragma unroll
+                    for (int i = 0; i < DCH; ++i)
+                        dst[(int64_t)i * F] = bf16_rn(v[i] + w[i]);
                 }
             }
-            if ((int)rank < ng) {
-                // dW_k^T accumulator [f][hi j | lo j] -> dW rows k G + j
-                const int64_t k = k0 + rank;
-                ok = mbar_wait(bar_addr(c.wfull), (uint32_t)io & 1u, abort_flag, a.status);
-                if (named_bar_any(kBarDw, kDw * 32, !ok))
-                    break;
-                tc_fence_after();
-#pragma unroll
-                for (int cc = 0; cc < G; cc += DCH) {
-                    float v[DCH], w[DCH];
-                    tmem_ld_chunk2<DCH>(tbase + lane_off + col_w + (uint32_t)cc,
-                                        tbase + lane_off + col_w + (uint32_t)(G + cc), v, w);
-                    if (f < F) {
-                        uint16_t *dst = a.dW + (k * G + cc) * F + f;
-#pragma unroll
-                        for (int i = 0; i < DCH; ++i)
-                            dst[(int64_t)i * F] = bf16_rn(v[i] + w[i]);
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(bar_addr(c.wempty));
-                ++io;
-            }
+            STEP_TRACE(2, io);
+            ++io;
         }
     } else {
         // ---------------------------------------------------------- Ws builders
-        // thread f: if I_k[f] falls in the band, column f of W_k (fp16) becomes
-        // row I_k[f] - i0 of the group's Ws buffer; the row it wrote there the
-        // last time is zeroed first.  A group with |W| >= 2^15 in the band adds
-        // its band's part of dh on CUDA cores instead (fp32, atomics).
-        const int t = threadIdx.x - kW0Bld * 32;
-        int prev[2] = {-1, -1};
+        // Column block x of W_k (8 columns f, all G rows) comes in with
+        // ldmatrix.trans: lane l holds rows j = 8i + 2(l%4), +1 of column
+        // f = 8x + l/4 (i = 0 .. G/8-1), which is word l%4 of 16-byte unit i
+        // of Ws row I_k[f] - i0.  Blocks whose columns all fall outside the
+        // band are skipped (I_k is sorted).  The words a lane wrote in a
+        // buffer are zeroed the next time the lane uses that buffer.  A group
+        // with |W| >= 2^15 in the band adds its band's part of dh on CUDA
+        // cores instead (fp32, atomics).
+        const int bw = warp - kW0Bld;
+        const int qd = lane & 3;
+        const int tb = threadIdx.x - kW0Bld * 32;  // lane of the team
+        const int nblk = F / 8;
         int it = 0, gi = 0;
         bool ok = true;
         for (int64_t ps = cl; ps < a.NPS && ok; ps += ncl, ++it) {
-            const int s = it % S;
+            const int sw = it % SW;
             const int db = it & 1;
             const uint32_t dph = (uint32_t)(it >> 1) & 1u;
-            const int64_t k0 = ps * C;
-            const int ng = (int)(a.K - k0 < C ? a.K - k0 : C);
-            ok = mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status);
+            const int ng = groups_in_step(a, ps);
+            STEP_TRACE(0, it);
+            ok = mbar_wait(bar_addr(c.wfull[sw]), (uint32_t)(it / SW) & 1u, abort_flag, a.status);
+            STEP_TRACE(1, it);
             if (named_bar_any(kBarBld, kBld * 32, !ok))
                 break;
-            const uint8_t *st = bp + (size_t)s * a.stage_bytes;
+            STEP_TRACE(2, it);
+            const uint32_t wslot = base + a.off_w + (uint32_t)sw * a.wslot_bytes;
             for (int g = 0; g < ng; ++g, ++gi) {
                 const int wb = gi & 1;
-                const uint8_t *Wg = st + a.h_bytes + (size_t)g * a.w_bytes;
-                const uint16_t *Ig = reinterpret_cast<const uint16_t *>(st + a.h_bytes + (size_t)C * a.w_bytes +
-                                                                         (size_t)g * a.i_bytes);
-                int row = -1;
-                bool big = false;
-                uint32_t pk[G / 2];
-                if (t < F) {
-                    const int i = (int)Ig[t] - i0;
-                    if (i >= 0 && i < BW) {
-                        row = i;
-                        // element (j, f) of the TMA box layout: box f / CW, row j,
-                        // 16-byte unit ((f % CW) / 8) ^ swizzle(j), then f % 8
-                        const int fc = t % CW;
-                        const uint8_t *colp = Wg + (size_t)(t / CW) * WCH + (fc & 7) * 2;
-#pragma unroll
-                        for (int jj = 0; jj < G / 2; ++jj) {
-                            const int j = 2 * jj;
-                            const uint32_t lo = *reinterpret_cast<const uint16_t *>(
-                                colp + (size_t)j * 2 * CW + ((((fc >> 3) ^ swz_of(j, 2 * CW))) << 4));
-                            const uint32_t hi = *reinterpret_cast<const uint16_t *>(
-                                colp + (size_t)(j + 1) * 2 * CW + ((((fc >> 3) ^ swz_of(j + 1, 2 * CW))) << 4));
-                            big |= (lo & 0x7fffu) >= 0x4700u || (hi & 0x7fffu) >= 0x4700u;
-                            pk[jj] = pack2_f16(__uint_as_float(lo << 16), __uint_as_float(hi << 16));
-                        }
-                    }
+                const uint32_t Wg = wslot + (uint32_t)g * a.w_bytes;
+                const uint16_t *Ig =
+                    reinterpret_cast<const uint16_t *>(bp + a.off_w + (size_t)sw * a.wslot_bytes +
+                                                       (size_t)C * a.w_bytes + (size_t)g * a.i_bytes);
+                // the band's columns [fa, fe) of the sorted I_k: one ballot per
+                // 32 columns, no per-block loads
+                int fa = 0, fe = 0;
+                for (int f0 = 0; f0 < F; f0 += 32) {
+                    const int iv = f0 + lane < F ? (int)Ig[f0 + lane] : 0x7fffffff;
+                    fa += __popc(__ballot_sync(0xffffffffu, iv < i0));
+                    fe += __popc(__ballot_sync(0xffffffffu, iv < i0 + BW));
                 }
                 ok = mbar_wait(bar_addr(c.wsempty[wb]), ((uint32_t)(gi >> 1) & 1u) ^ 1u, abort_flag, a.status);
+                STEP_TRACE(3 + 4 * g, it);
                 if (named_bar_any(kBarBld, kBld * 32, !ok)) {
                     ok = false;
                     break;
                 }
                 uint8_t *Wb = bp + a.off_ws + (size_t)wb * a.ws_bytes;
-                if (prev[wb] >= 0) {
+                // the words this lane wrote the last time it used the buffer
+#pragma unroll 1
+                for (int x = 0; x < kMaxBlk; ++x) {
+                    const int pr = c.rowtab[wb][x][tb];
+                    if (pr >= 0) {
+                        const int sw2 = swz_of(pr, RB);
 #pragma unroll
-                    for (int x = 0; x < RB / 16; ++x)
-                        *reinterpret_cast<uint4 *>(Wb + (size_t)prev[wb] * RB + x * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        for (int i2 = 0; i2 < NI; ++i2)
+                            *reinterpret_cast<uint32_t *>(Wb + (size_t)pr * RB + ((i2 ^ sw2) << 4) + qd * 4) = 0u;
+                    }
                 }
-                // zeroing before writing (rows move between threads); the vote
-                // sends the whole group to the CUDA-core path
-                const bool slow = named_bar_any(kBarBld, kBld * 32, big);
-                prev[wb] = -1;
-                if (!slow && row >= 0) {
-                    uint8_t *d = Wb + (size_t)row * RB;
-                    const int sw = swz_of(row, RB);
+                named_bar(kBarBld, kBld * 32);  // zeroing before writing: rows move between lanes
+                STEP_TRACE(4 + 4 * g, it);
+                uint32_t mx = 0;
+#pragma unroll 1
+                for (int x = 0; x < kMaxBlk; ++x) {
+                    int row = -1;
+                    const int blk = bw + x * kBld;
+                    const int fb = blk * 8;
+                    if (blk < nblk && fb + 8 > fa && fb < fe) {  // warp-uniform: some column is in the band
+                        // row address of lane l: W_k row j, 16-byte unit of columns fb..fb+7
+                        const uint32_t ubox = (uint32_t)(fb / CW) * WCH;
+                        const int un = (fb % CW) >> 3;
+                        uint32_t pk[NI];
 #pragma unroll
-                    for (int x = 0; x < RB / 16; ++x)
-                        *reinterpret_cast<uint4 *>(d + ((x ^ sw) << 4)) =
-                            make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
-                    prev[wb] = row;
+                        for (int h = 0; h < (NI + 3) / 4; ++h) {
+                            const int j = h * 32 + lane;
+                            const int jj = j < G ? j : 0;
+                            const uint32_t addr =
+                                Wg + ubox + (uint32_t)jj * WROW + (uint32_t)((un ^ swz_of(jj, (int)WROW)) << 4);
+                            if constexpr (NI >= 4) {
+                                uint32_t r4[4];
+                                ldsm_x4_trans(addr, r4);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    pk[h * 4 + i] = r4[i];
+                            } else {
+                                uint32_t r2[2];
+                                ldsm_x2_trans(addr, r2);
+                                pk[0] = r2[0];
+                                pk[1] = r2[1];
+                            }
+                        }
+                        const int f = fb + (lane >> 2);
+                        if (f >= fa && f < fe)
+                            row = (int)Ig[f] - i0;
+                        if (row >= 0) {
+                            const int sw2 = swz_of(row, RB);
+#pragma unroll
+                            for (int i2 = 0; i2 < NI; ++i2) {
+                                const uint32_t r = pk[i2];
+                                mx = __vmaxu2(mx, r & 0x7fff7fffu);
+                                *reinterpret_cast<uint32_t *>(Wb + (size_t)row * RB + ((i2 ^ sw2) << 4) + qd * 4) =
+                                    pack2_f16(__uint_as_float(r << 16), __uint_as_float(r & 0xffff0000u));
+                            }
+                        }
+                    }
+                    c.rowtab[wb][x][tb] = (int16_t)row;
+                }
+                const bool big = (mx & 0xffffu) >= 0x4700u || (mx >> 16) >= 0x4700u;
+                STEP_TRACE(5 + 4 * g, it);
+                // a group with |W| >= 2^15 in the band takes the CUDA-core path:
+                // its rows go back to zero (the rare case pays for it)
+                const bool slow = named_bar_any(kBarBld, kBld * 32, big);
+                if (slow) {
+#pragma unroll 1
+                    for (int x = 0; x < kMaxBlk; ++x) {
+                        const int pr = c.rowtab[wb][x][tb];
+                        if (pr >= 0) {
+                            const int sw2 = swz_of(pr, RB);
+#pragma unroll
+                            for (int i2 = 0; i2 < NI; ++i2)
+                                *reinterpret_cast<uint32_t *>(Wb + (size_t)pr * RB + ((i2 ^ sw2) << 4) + qd * 4) = 0u;
+                        }
+                    }
                 }
                 fence_proxy_async();
                 named_bar(kBarBld, kBld * 32);
-                if (t == 0)
+                STEP_TRACE(6 + 4 * g, it);
+                if (warp == kW0Bld && lane == 0)
                     mbar_arrive(bar_addr(c.wsfull[wb]));
                 if (slow) {
-                    // dh[b][i0 + row] += sum_j dZ[b][j] W[j][f] from the step's fp16 tile
+                    // one lane per column of the band (lanes with l%4 == 0),
+                    // from the step's fp16 tile of the group
                     ok = mbar_wait(bar_addr(c.dzhfull[db]), dph, abort_flag, a.status);
-                    if (ok && row >= 0) {
-                        const uint8_t *tile = bp + a.off_dzh + (size_t)(db * C + g) * ZCH;
-                        const int fc = t % CW;
-                        const uint8_t *colp = Wg + (size_t)(t / CW) * WCH + (fc & 7) * 2;
-                        for (int bb = 0; bb < a.B; ++bb) {
-                            float acc = 0.f;
-                            const int zsw_r = swz_of(bb, ZSW);
-                            for (int j = 0; j < G; ++j) {
-                                const uint32_t wbits = *reinterpret_cast<const uint16_t *>(
-                                    colp + (size_t)j * 2 * CW + ((((fc >> 3) ^ swz_of(j, 2 * CW))) << 4));
-                                const __half zh = *reinterpret_cast<const __half *>(
-                                    tile + (size_t)bb * ZSW + ((((j * 2) >> 4) ^ zsw_r) << 4) + (j & 7) * 2);
-                                acc = fmaf(__half2float(zh), __uint_as_float(wbits << 16), acc);
-                            }
-                            atomicAdd(a.dh + (size_t)bb * a.H + i0 + row, acc);
-                        }
+                    const uint8_t *tile = bp + a.off_dzh + (size_t)(db * C + g) * ZCH;
+#pragma unroll 1
+                    for (int x = 0; x < kMaxBlk; ++x) {
+                        const int pr = c.rowtab[wb][x][tb];
+                        if (ok && qd == 0 && pr >= 0)
+                            dh_band_fp32(tile, ZSW, bp + (Wg - base), G, CW, (bw + x * kBld) * 8 + (lane >> 2), pr,
+                                         i0, a.B, a.H, a.dh);
+                        c.rowtab[wb][x][tb] = -1;  // nothing to zero next time
                     }
                     if (named_bar_any(kBarBld, kBld * 32, !ok)) {
                         ok = false;
@@ -621,14 +818,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             if (!ok)
                 break;
             named_bar(kBarBld, kBld * 32);
-            if (t == 0)
-                mbar_arrive(bar_addr(c.empty[s]));  // done with the stage's W_k and I_k
+            if (warp == kW0Bld && lane == 0)
+                mbar_arrive(bar_addr(c.wempty[sw]));  // done with the slot's W_k and I_k
         }
     }
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // no CTA leaves while another may still read its shared memory
-    if (warp == kWA) {
+    if (warp == kWF) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
@@ -637,9 +834,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
 // ------------------------------------------------------------------ plan
 struct StepPlan {
     bool ok = false;
-    int C = 0, BW = 0, S = 0, CW = 0, nbc = 0;
-    uint32_t h_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, dzw_bytes = 0, ws_bytes = 0;
-    uint32_t off_dzw = 0, off_dzh = 0, off_ws = 0;
+    int C = 0, BW = 0, SH = 0, SW = 0, CW = 0, nbc = 0;
+    uint32_t h_bytes = 0, w_bytes = 0, i_bytes = 0, wslot_bytes = 0, ws_bytes = 0;
+    uint32_t off_w = 0, off_dzw = 0, off_dzh = 0, off_ws = 0;
     size_t smem = 0;
 };
 
@@ -664,31 +861,41 @@ StepPlan plan_step(const sg_layout *lo, int B)
     p.CW = F % 64 == 0 ? 64 : F % 32 == 0 ? 32 : 16;
     p.nbc = B <= 64 ? 1 : 2;
     const uint32_t zsw = 2 * G >= 128 ? 128u : 2u * G;
-    p.h_bytes = 128u * F * 2u;
+    // one H slot: the sample chunks that are gathered (the forward MMA reads
+    // a second chunk's worth past the first; with one chunk that is the next
+    // buffer's bytes, in bounds, multiplied into accumulator rows >= 64 that
+    // are never used)
+    p.h_bytes = (uint32_t)p.nbc * 64u * F * 2u;
     p.w_bytes = (uint32_t)G * F * 2u;
     p.i_bytes = (uint32_t)((2 * F + 127) / 128 * 128);
-    p.stage_bytes = (p.h_bytes + p.C * (p.w_bytes + p.i_bytes) + 1023u) & ~1023u;
-    p.dzw_bytes = 2u * 128u * zsw;
+    p.wslot_bytes = (p.C * (p.w_bytes + p.i_bytes) + 1023u) & ~1023u;
     p.ws_bytes = (uint32_t)p.BW * 2u * G;
-    const long fixed = 2l * p.dzw_bytes + 2l * p.C * 128 * zsw + 2l * p.ws_bytes + 1024;
-    long S = (kSmemBudget - fixed) / (long)p.stage_bytes;
-    if (S > kMaxS)
-        S = kMaxS;
-    if (S < 2)
+    const long fixed = 2l * 128 * zsw + 2l * p.C * 128 * zsw + 2l * p.ws_bytes + 1024;
+    // deepest H ring first (the gather is the longest latency), then W
+    p.SH = 0;
+    for (int sh = kMaxSH; sh >= 2 && p.SH == 0; --sh)
+        for (int sw = kMaxSW; sw >= 2; --sw)
+            if (fixed + (long)sh * p.h_bytes + (long)sw * p.wslot_bytes <= kSmemBudget) {
+                p.SH = sh;
+                p.SW = sw;
+                break;
+            }
+    if (p.SH == 0)
         return p;
-    p.S = (int)S;
-    p.off_dzw = (uint32_t)p.S * p.stage_bytes;
-    p.off_dzh = p.off_dzw + 2u * p.dzw_bytes;
+    p.off_w = (uint32_t)p.SH * p.h_bytes;
+    p.off_dzw = p.off_w + (uint32_t)p.SW * p.wslot_bytes;
+    p.off_dzh = p.off_dzw + 2u * 128u * zsw;
     p.off_ws = p.off_dzh + 2u * p.C * 128u * zsw;
     p.smem = (size_t)p.off_ws + 2u * p.ws_bytes + 1024;
+    // the MMAs read past the last H slot (the dW MMA up to 128 rows of 128
+    // bytes from a sample chunk, the forward a second chunk): the buffers after
+    // the ring cover that
+    if ((size_t)p.off_w + 2 * (size_t)F * 128 + 128 * 128 > p.smem - 1024)
+        return p;
     // more than half of an SM's shared memory: one CTA per SM, so that no two
     // CTAs ever wait for each other's 512 TMEM columns
     if (p.smem < 120 * 1024)
         p.smem = 120 * 1024;
-    // the dW MMA reads up to 128 rows of 128 bytes from the start of the last
-    // stage's second sample chunk: the buffers after the stages cover that
-    if ((size_t)(p.S - 1) * p.stage_bytes + (size_t)F * 128 + 128 * 128 > p.smem - 1024)
-        return p;
     p.ok = true;
     return p;
 }
@@ -745,7 +952,18 @@ sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW, flo
     sg_status rc = encode_w(&tm_w, W, lo, p.CW);
     if (rc != SG_OK)
         return rc;
-    void (*kern)(CUtensorMap, StepArgs) = lo->G == 16 ? k_tc_step<16> : lo->G == 32 ? k_tc_step<32> : k_tc_step<64>;
+    void (*kern)(CUtensorMap, StepArgs) = nullptr;
+#define SG_STEP_PICK(GG, CC)                  \
+    if (lo->G == GG && p.CW == CC)            \
+        kern = k_tc_step<GG, CC>;
+    SG_STEP_PICK(16, 16) SG_STEP_PICK(16, 32) SG_STEP_PICK(16, 64)
+    SG_STEP_PICK(32, 16) SG_STEP_PICK(32, 32) SG_STEP_PICK(32, 64)
+    SG_STEP_PICK(64, 16) SG_STEP_PICK(64, 32) SG_STEP_PICK(64, 64)
+#undef SG_STEP_PICK
+    if (!kern) {
+        sg_set_error("tc_step: no kernel for G = %d", lo->G);
+        return SG_ERR_UNSUPPORTED;
+    }
     SG_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem));
     if (p.C > 1)
         SG_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
@@ -766,15 +984,15 @@ sg_status tc_step(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *dW, flo
     a.ldB = lo->ldB;
     a.C = p.C;
     a.BW = p.BW;
-    a.S = p.S;
-    a.CW = p.CW;
+    a.SH = p.SH;
+    a.SW = p.SW;
     a.nbc = p.nbc;
     a.h_bytes = p.h_bytes;
     a.w_bytes = p.w_bytes;
     a.i_bytes = p.i_bytes;
-    a.stage_bytes = p.stage_bytes;
-    a.dzw_bytes = p.dzw_bytes;
+    a.wslot_bytes = p.wslot_bytes;
     a.ws_bytes = p.ws_bytes;
+    a.off_w = p.off_w;
     a.off_dzw = p.off_dzw;
     a.off_dzh = p.off_dzh;
     a.off_ws = p.off_ws;

@@ -537,7 +537,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int q = warp & 3;
         const int sub = (warp - kFirstEpi) / 4;
         const int units = a.MT * (G / CH);
-        double lacc = 0.0;
+        double lacc = 0.0;  // folded in from lf every 32 groups (fp64 is slow on this part)
+        float lf = 0.f;
         int it = 0;
         // positive-list bounds of the group, loaded one group ahead
         int e0n = 0, e1n = 0;
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     // every row of the tile is written; rows >= B hold zeros
                     if (b < a.B) {
                         const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
-                        lacc += bce_chunk<CH>(v, y);
+                        lf += bce_chunk_ftz<CH>(v, y);
                     } else {
 #pragma unroll
                         for (int i = 0; i < CH; ++i)
@@ -580,15 +581,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     store_bf16_row<CH>(a.Z + off, nullptr, v);
                 if (BCE) {
                     const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
-                    lacc += bce_chunk<CH>(v, y);
+                    lf += bce_chunk_ftz<CH>(v, y);
                     store_bf16_row<CH>(a.dZ + off, a.dZ_lo ? a.dZ_lo + off : nullptr, v);
                 }
             }
             tc_fence_before();
             mbar_arrive(bar_addr(c.tempty[acc]));
+            if ((it & 31) == 31) {
+                lacc += (double)lf;
+                lf = 0.f;
+            }
         }
         if (BCE)
-            epi_sum_to(lacc, c, a.loss_part + blockIdx.x, kFirstEpi);
+            epi_sum_to(lacc + (double)lf, c, a.loss_part + blockIdx.x, kFirstEpi);
     }
     tc_fence_before();
     __syncthreads();
@@ -986,7 +991,8 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         const int ew = warp - kFWFirstEpi;  // BCE warps 0 .. kFWBce-1, then the dW warps
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         if (ew < kFWBce) {
-            double lacc = 0.0;
+            double lacc = 0.0;  // folded in from lf every 32 groups (fp64 is slow on this part)
+            float lf = 0.f;
             const int sub = ew / 4;  // two warps per lane quarter split the column units
             // Z_k -> BCE -> dZ_k (workspace tile and shared memory for the dW MMA)
             constexpr int zunits = MT * (G / CH);
@@ -1020,7 +1026,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     tmem_ld_chunk<CH>(tbase + lane_off + (uint32_t)(zs * a.zcols + t * G + c0), v);
                     if (b < a.B) {
                         const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
-                        lacc += bce_chunk<CH>(v, y);
+                        lf += bce_chunk_ftz<CH>(v, y);
                     } else {
 #pragma unroll
                         for (int i = 0; i < CH; ++i)
@@ -1035,8 +1041,12 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 mbar_arrive(bar_addr(c.tempty[zs]));
                 fence_proxy_async();  // dZ_k in shared memory -> the dW MMA (async proxy)
                 mbar_arrive(bar_addr(cf.dzfull[db]));
+                if ((it & 31) == 31) {
+                    lacc += (double)lf;
+                    lf = 0.f;
+                }
             }
-            epi_sum_to(lacc, c, a.loss_part + blockIdx.x, kFWFirstEpi);
+            epi_sum_to(lacc + (double)lf, c, a.loss_part + blockIdx.x, kFWFirstEpi);
         } else {
             // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
             // staged in shared memory as [j][f] and stored with one bulk copy.

@@ -201,6 +201,62 @@ __device__ __forceinline__ float bce_chunk(float (&v)[CH], uint32_t y)
     return lin - zpos + __logf(prod);
 }
 
+// 2^x and 1/x on the special-function unit, subnormal inputs and results
+// flushed to zero (no fix-up instructions around the approximation)
+__device__ __forceinline__ float ex2_ftz(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_ftz(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2_ftz(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// bce_chunk with the flushing approximations: e = 2^(-|z| log2 e) is 0 for
+// |z| > 87 (where sigma(-|z|) and log(1 + e^-|z|) are below fp32's normal
+// range), the product of the (1 + e) factors stays in [1, 2^CH]
+template <int CH>
+__device__ __forceinline__ float bce_chunk_ftz(float (&v)[CH], uint32_t y)
+{
+    constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
+    float prod = 1.f, lin = 0.f, zpos = 0.f;
+    if (y) {
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+            if ((y >> i) & 1u)
+                zpos += v[i];
+    }
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const float z = v[i];
+        const float e = ex2_ftz(-fabsf(z) * kLog2e);
+        const float one_e = 1.f + e;
+        const float r = rcp_ftz(one_e);
+        v[i] = z >= 0.f ? r : e * r;
+        lin += fmaxf(z, 0.f);
+        prod *= one_e;
+    }
+    if (y) {
+#pragma unroll
+        for (int i = 0; i < CH; ++i)
+            if ((y >> i) & 1u)
+                v[i] -= 1.f;
+    }
+    return lin - zpos + lg2_ftz(prod) * kLn2;
+}
+
 // fp32 -> bf16 bits, round to nearest even (the hardware conversion)
 __device__ __forceinline__ uint16_t bf16_rn(float x)
 {

@@ -61,16 +61,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete.  Returns false (and leaves the
-// CTA's abort flag set) if another role aborted or the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int *abort_flag, int32_t *status)
+// The spinning part of a bounded wait, out of line: every wait site shares
+// one copy, so kernels with many wait sites stay small in the instruction
+// cache.  `cluster`: acquire at cluster scope (a barrier that other CTAs of
+// the cluster arrive on).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                            int32_t *status, bool cluster)
 {
-    if (mbar_try_wait(bar, parity))
-        return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity))
+        uint32_t ok;
+        if (cluster)
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(bar), "r"(parity)
+                : "memory");
+        else
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(bar), "r"(parity)
+                : "memory");
+        if (ok)
             return true;
         if (*abort_flag)
             return false;
@@ -80,6 +97,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
             return false;
         }
     }
+}
+
+// Wait for the phase of `parity` to complete.  Returns false (and leaves the
+// CTA's abort flag set) if another role aborted or the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int *abort_flag, int32_t *status)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    return mbar_wait_slow(bar, parity, abort_flag, status, false);
 }
 
 // Used while winding down: bounded, ignores the abort flag.
@@ -281,6 +308,24 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
                  : "r"(taddr));
 }
 
+// four 8x8 b16 tiles, transposed: lane l supplies the row address of tile
+// l / 8, row l % 8 (16 bytes); register i gets tile i's elements (row 2(l%4),
+// column l/4) and (row 2(l%4)+1, column l/4) -- the low half is the first
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr));
+}
+
+// the same for two tiles (lanes 0..15 supply the row addresses)
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t saddr, uint32_t (&r)[2])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(saddr));
+}
+
 // ------------------------------------------------------------------ clusters
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -320,6 +365,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
                  : "memory");
 }
 
+// the same with relaxed ordering: for a signal that publishes nothing (e.g.
+// "done reading your buffer" after the loaded values are already in use), so
+// it does not wait for this thread's earlier stores to become visible
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -340,18 +394,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
 {
     if (mbar_try_wait_cluster(bar, parity))
         return true;
-    const uint64_t t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait_cluster(bar, parity))
-            return true;
-        if (*abort_flag)
-            return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            sg_flag(status, SG_ERR_TIMEOUT);
-            return false;
-        }
-    }
+    return mbar_wait_slow(bar, parity, abort_flag, status, true);
 }
 
 __device__ __forceinline__ void fence_acq_rel_cluster()

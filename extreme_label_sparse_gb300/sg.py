@@ -20,7 +20,7 @@ _lib = None
 
 SG_OK, SG_ERR_INVALID, SG_ERR_UNSUPPORTED, SG_ERR_CUDA = 0, -1, -2, -3
 SG_ERR_OOM, SG_ERR_TIMEOUT, SG_ERR_DATA = -4, -5, -6
-SG_ENGINE_AUTO, SG_ENGINE_SIMT, SG_ENGINE_TC = 0, 1, 2
+SG_ENGINE_AUTO, SG_ENGINE_SIMT, SG_ENGINE_TC, SG_ENGINE_FUSED = 0, 1, 2, 3
 KIND_NAMES = ("prep", "fwd", "bce", "dW", "dh", "step")
 
 

@@ -74,9 +74,15 @@ typedef enum sg_status {
 } sg_status;
 
 typedef enum sg_engine {
-    SG_ENGINE_AUTO = 0, /* tensor-core engine where supported, else CUDA cores */
-    SG_ENGINE_SIMT = 1, /* CUDA-core engine for every call */
-    SG_ENGINE_TC = 2    /* tensor-core engine; calls it cannot run fail */
+    SG_ENGINE_AUTO = 0,  /* tensor-core engine where supported, else CUDA cores */
+    SG_ENGINE_SIMT = 1,  /* CUDA-core engine for every call */
+    SG_ENGINE_TC = 2,    /* tensor-core engine; calls it cannot run fail */
+    SG_ENGINE_FUSED = 3  /* as SG_ENGINE_TC, and sg_step runs the whole step in
+                            one kernel on clusters of CTAs wherever that kernel
+                            fits (B <= 128, G in {16, 32, 64}, F % 16 == 0,
+                            F <= 128): W is read once and dZ never leaves the
+                            chip.  SG_ENGINE_AUTO takes that kernel only for
+                            shapes the two-kernel tensor-core step cannot run. */
 } sg_engine;
 
 /* Opaque, library-owned: the canonical layout plus per-layout scratch. */

@@ -233,18 +233,18 @@ def test_empty_positive_lists(oracle_mod):
 _BY_NAME = {w.name: w for w, _ in CASES}
 
 
-# kernels each workload shape launches: the whole step in one cluster kernel
-# (B <= 128), else the fused forward + BCE + dW kernel and the dh kernel
-_FUSED_KINDS = {"like3m": {"prep", "step"}, "like8p6m": {"prep", "step"},
+# kernels each workload shape launches: the fused forward + BCE + dW kernel
+# and the dh kernel
+_FUSED_KINDS = {"like3m": {"prep", "fwd", "dh"}, "like8p6m": {"prep", "fwd", "dh"},
                 "like670k": {"prep", "fwd", "dh"}}
 
 
 @pytest.mark.parametrize("name", ["like3m", "like670k", "like8p6m"])
 def test_step_fused_on_tensor_cores(name, oracle_mod):
     """The shapes of the three label-space workloads run the whole step on
-    the tensor cores (engine pinned: a CUDA-core fallback would raise): in one
-    kernel where the batch fits one 128-sample tile, else through the fused
-    forward + BCE + dW kernel (no separate dW launch) and the dh kernel."""
+    the tensor cores (engine pinned: a CUDA-core fallback would raise) through
+    the fused forward + BCE + dW kernel (no separate dW launch) and the dh
+    kernel."""
     w = _BY_NAME[name]
     p = generate(w)
     ref = oracle_mod.step(p)
@@ -261,6 +261,68 @@ def test_step_fused_on_tensor_cores(name, oracle_mod):
     assert launched == _FUSED_KINDS[name], rec
     assert_close(host_bf16_to_f64(dW), ref["dW"], what="dW")
     assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+
+
+# shapes of the single-kernel step (B <= 128, G in {16, 32, 64}, F % 16 == 0,
+# F <= 128): one CTA per cluster (H within one TMEM band), two or three CTAs,
+# a group count that is not a multiple of the cluster size, B = 1 and B <= 64
+_SINGLE = ["tiny", "like3m", "like3m_oddK", "like8p6m", "g32_b100", "tc_b37_h320", "b1",
+           "dense_F_eq_H", "clustered", "f16_h1000_c3"]
+_BY_NAME["like3m_oddK"] = _w("like3m_oddK", B=128, H=768, L=32 * 301, G=32, F=128, pos=36, dist="zipf")
+_BY_NAME["f16_h1000_c3"] = _w("f16_h1000_c3", B=96, H=1000, L=16 * 90, G=16, F=16, pos=3)
+
+
+@pytest.mark.parametrize("name", _SINGLE)
+def test_step_single_kernel(name, oracle_mod):
+    """The whole step in one kernel on CTA clusters (engine SG_ENGINE_FUSED):
+    dW, dh and the loss against the oracle, twice in a row (the layout's
+    scratch and the kernel's shared-memory state must not leak between
+    calls), and only the preparation kernels besides the step kernel run."""
+    w = CONFIGS["tiny"] if name == "tiny" else _BY_NAME[name]
+    p = generate(w)
+    ref = oracle_mod.step(p)
+    lay = build_layout(p)
+    sg.sg_layout_set_engine(lay, sg.SG_ENGINE_FUSED)
+    d = dev_problem(p)
+    dW = torch.empty((w.L, w.F), dtype=torch.int16, device="cuda")
+    dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    for _ in range(2):
+        sg.sg_timing_start(lay, 64)
+        sg.sg_step(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dW, dh, loss)
+        rec = sg.sg_timing_stop(lay)
+        _status_ok(lay)
+        assert {k for k, (ms, n) in rec.items() if n > 0} == {"prep", "step"}, rec
+        assert_close(host_bf16_to_f64(dW), ref["dW"], what="dW")
+        assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+        assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
+
+
+def test_step_single_kernel_large_weights(oracle_mod):
+    """|W| beyond fp16's range (W x 2^20) through the single-kernel step: the
+    groups whose band holds such weights add their part of dh in fp32 on CUDA
+    cores, the rest on the tensor cores; everything must match the oracle."""
+    w = _w("bigw1", B=128, H=768, L=32 * 40, G=32, F=128, pos=36, dist="zipf")
+    p = generate(w)
+    bits = p.W.astype(np.uint32)
+    expo = (bits >> 7) & 0xFF
+    # scale the weights of every third group only: both paths in one call
+    grp = np.arange(w.L) // w.G
+    scale = (expo > 0) & (expo < 0xFF - 20) & ((grp % 3) == 0)[:, None]
+    p.W = np.where(scale, bits + (20 << 7), bits).astype(np.uint16)
+    assert np.abs(bf16_bits_to_f32(p.W)).max() > 2.0 ** 16
+    ref = oracle_mod.step(p)
+    lay = build_layout(p)
+    sg.sg_layout_set_engine(lay, sg.SG_ENGINE_FUSED)
+    d = dev_problem(p)
+    dW = torch.empty((w.L, w.F), dtype=torch.int16, device="cuda")
+    dh = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sg.sg_step(lay, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dW, dh, loss)
+    _status_ok(lay)
+    assert_close(host_bf16_to_f64(dW), ref["dW"], what="dW")
+    assert_close(dh.cpu().numpy(), ref["dh"], what="dh")
+    assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
 
 
 @pytest.mark.parametrize("name", ["tiny", "like3m", "like670k", "like8p6m", "b256_f256"])
