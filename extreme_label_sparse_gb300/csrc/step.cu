@@ -101,7 +101,7 @@ struct StepCtl {
     uint64_t dzwfull, dzwempty;              // dZ bf16 planes (dW operand)
     uint64_t dwfull, dwempty;                // dW slot
     uint64_t dzhfull[2];                     // the step's fp16 tiles are all in place
-    uint64_t dzhdone[2];                     // the local dh MMAs are done with them
+    uint64_t dzhdone[2];                     // the local dh MMAs and builders are done with them
     uint64_t dzready[2];                     // the other CTAs wrote their tiles (cluster)
     uint64_t dzcopied[2];                    // the other CTAs copied this CTA's tile (cluster)
     uint64_t wsfull[2], wsempty[2];          // Ws buffers
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             mbar_init(bar_addr(c.zfull[i]), 1);
             mbar_init(bar_addr(c.zempty[i]), kBce * 32);
             mbar_init(bar_addr(c.dzhfull[i]), C > 1 ? 2 : 1);
-            mbar_init(bar_addr(c.dzhdone[i]), 1);
+            mbar_init(bar_addr(c.dzhdone[i]), 2);  // dh MMA commit + builders (fp32 path reads)
             mbar_init(bar_addr(c.dzready[i]), C > 1 ? C - 1 : 1);
             mbar_init(bar_addr(c.dzcopied[i]), C > 1 ? C - 1 : 1);
             mbar_init(bar_addr(c.wsfull[i]), 1);
@@ -818,8 +818,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             if (!ok)
                 break;
             named_bar(kBarBld, kBld * 32);
-            if (warp == kW0Bld && lane == 0)
+            if (warp == kW0Bld && lane == 0) {
                 mbar_arrive(bar_addr(c.wempty[sw]));  // done with the slot's W_k and I_k
+                mbar_arrive(bar_addr(c.dzhdone[db]));  // and with the step's dZ tiles (fp32 path)
+            }
         }
     }
     tc_fence_before();
