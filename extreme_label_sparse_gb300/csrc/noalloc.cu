@@ -10,6 +10,9 @@
 // partials.  Every call reuses the same array, so calls that overlap on the
 // GPU (two streams, or two host threads) race and must be serialized by the
 // caller.  The counters are cleared at the start of every call.
+#include <atomic>
+#include <climits>
+
 #include "sg_internal.cuh"
 
 namespace {
@@ -34,9 +37,27 @@ struct NaScratch {
 static __device__ __align__(256) NaScratch g_na_scratch;
 
 // Host-side device addresses of g_na_scratch, looked up once per device (the
-// symbol's host name is only a stand-in, never a device address).
+// symbol's host name is only a stand-in, never a device address).  Two host
+// threads may race on the first lookup: both find the same address, and the
+// atomic store keeps the race benign.  cudaDeviceReset ends the context the
+// address belongs to; this cache does not follow a reset.
 constexpr int kNaMaxDevices = 64;
-NaScratch *g_na_addr[kNaMaxDevices] = {};
+std::atomic<NaScratch *> g_na_addr[kNaMaxDevices];
+
+// Row b of the positives is well formed when 0 <= rowptr[b] <= rowptr[b+1]
+// <= nnz and rowptr[b] is at least every earlier row's start: well-formed rows
+// then never overlap (each starts at or after the end of every earlier one),
+// so their sorted copies below never share scratch entries.
+__device__ __forceinline__ bool na_row_ok(const int32_t *__restrict__ rowptr, int b, int64_t nnz, int lane)
+{
+    const int64_t r0 = rowptr[b], r1 = rowptr[b + 1];
+    int32_t mx = INT32_MIN;
+    for (int c = lane; c < b; c += 32)
+        mx = max(mx, rowptr[c]);
+    for (int o = 16; o > 0; o >>= 1)
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    return r0 >= 0 && r1 >= r0 && r1 <= nnz && r0 >= mx;
+}
 
 // one warp per sample: validate, sort and deduplicate the sample's slots,
 // count them per group; out-of-range slots and malformed rows are dropped
@@ -49,7 +70,7 @@ __global__ void k_na_rows(int32_t B, const int32_t *__restrict__ rowptr,
     if (b >= B)
         return;
     const int64_t r0 = rowptr[b], r1 = rowptr[b + 1];
-    if (r0 < 0 || r1 < r0 || r1 > nnz) {
+    if (!na_row_ok(rowptr, b, nnz, lane)) {
         if (lane == 0)
             sc->rowcnt[b] = 0;
         return;
@@ -232,13 +253,15 @@ extern "C" sg_status sg_bce_grad_noalloc(const sg_bf16 *Z, int32_t B, int64_t L,
     SG_TRY_CUDA(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kNaMaxDevices)
         NA_FAIL(SG_ERR_UNSUPPORTED, "%s: device ordinal %d above %d", fn, dev, kNaMaxDevices);
-    if (!g_na_addr[dev]) {
-        // first call on this device: resolve the array's device address
+    NaScratch *sc = g_na_addr[dev].load(std::memory_order_acquire);
+    if (!sc) {
+        // first call on this device (its device current): resolve the array's
+        // device address, a runtime lookup that allocates nothing
         void *p = nullptr;
         SG_TRY_CUDA(cudaGetSymbolAddress(&p, g_na_scratch));
-        g_na_addr[dev] = static_cast<NaScratch *>(p);
+        sc = static_cast<NaScratch *>(p);
+        g_na_addr[dev].store(sc, std::memory_order_release);
     }
-    NaScratch *sc = g_na_addr[dev];
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t K = L / G;
     SG_TRY_CUDA(cudaMemsetAsync(sc->gcount, 0, sizeof(int32_t) * (K + 1), st));

@@ -63,6 +63,7 @@ def load():
             "sg_step": ([P, P, i32, P, P, P, i64, P, P, P, P], C.c_int),
             "sg_step_sgd": ([P, P, i32, P, P, P, i64, C.c_float, C.c_float, P, P, P, P, P], C.c_int),
             "sg_bce_grad_noalloc": ([P, i32, i64, i32, P, P, i64, P, P, P], C.c_int),
+            "sg_selftest_wait_timeout": ([C.POINTER(i32)], C.c_int),
             "sg_timing_start": ([P, i32], C.c_int),
             "sg_timing_stop": ([P, P, P], C.c_int),
             "sg_last_error": ([], C.c_char_p),
@@ -302,3 +303,12 @@ def sg_bce_grad_noalloc(Z, B: int, L: int, G: int, pos_rowptr, pos_slot, nnz: in
                                       _dev(pos_rowptr, "pos_rowptr", _I32, B + 1), ps, nnz,
                                       _dev(dZ, "dZ", _BF16, B * L),
                                       _dev(loss, "loss", (torch.float64,), 1), _stream(Z.device)))
+
+
+# ---------------------------------------------------------------- self-test
+def sg_selftest_wait_timeout() -> int:
+    """Run the bounded-wait self-test on the current device; returns the
+    status the kernel recorded (SG_ERR_TIMEOUT when failure detection works)."""
+    code = C.c_int32(0)
+    _check(load().sg_selftest_wait_timeout(C.byref(code)))
+    return int(code.value)

@@ -249,7 +249,10 @@ SG_API sg_status sg_timing_stop(sg_layout *layout, double *ms_per_kind,
  *   Z[B][L], dZ[B][L] bf16, slot order; L = K*G.
  *   pos_rowptr[B+1], pos_slot[nnz]: each sample's positives as SLOT ids in
  *   [0, L) (any order, duplicates count once); out-of-range slots and
- *   malformed rows are dropped, since there is no layout status word.
+ *   malformed rows are dropped, since there is no layout status word.  Row b
+ *   is well formed when 0 <= pos_rowptr[b] <= pos_rowptr[b+1] <= nnz and
+ *   pos_rowptr[b] is at least every earlier row's start (pos_rowptr[0] may be
+ *   non-zero).
  * Working memory is one device array built into the library (about 3.2 MB,
  * held by every GPU that loads the library until the process exits), so the
  * sizes are capped: B <= 256, L/G <= 300000, nnz <= 65536; larger calls
@@ -257,11 +260,24 @@ SG_API sg_status sg_timing_stop(sg_layout *layout, double *ms_per_kind,
  * same array (it clears what must start at zero), so calls that overlap on
  * the GPU -- from two streams or two host threads -- race; serialize them.
  * The first call on a device looks up the array's device address (a runtime
- * query, no allocation); make that first call before any stream capture.
+ * query, no allocation) and keeps it for the life of the process; make that
+ * first call before any stream capture.  A cudaDeviceReset invalidates the
+ * kept address: do not call this entry point after resetting the device.
  * Asynchronous on `stream` otherwise.                                       */
 SG_API sg_status sg_bce_grad_noalloc(const sg_bf16 *Z, int32_t B, int64_t L, int32_t G,
                                      const int32_t *pos_rowptr, const int32_t *pos_slot,
                                      int64_t nnz, sg_bf16 *dZ, double *loss, void *stream);
+
+/* ---------------------------------------------------------------- self-test
+ * sg_selftest_wait_timeout -- exercises the library's failure detection on
+ * the current device: a one-CTA kernel that holds TMEM columns waits, through
+ * the same bounded wait every tensor-core kernel uses, on an mbarrier that
+ * nothing ever arrives on.  After the wait limit (about 2 s of %globaltimer
+ * time) the kernel records SG_ERR_TIMEOUT, releases its TMEM and returns, so
+ * the CUDA context stays usable.  *code receives the status the kernel
+ * recorded (SG_ERR_TIMEOUT when the mechanism works).  Synchronous; allocates
+ * and frees 4 bytes of device memory.                                      */
+SG_API sg_status sg_selftest_wait_timeout(int32_t *code);
 
 /* ---------------------------------------------------------------- misc */
 /* Message of the last failing call on this host thread ("" if none). */
