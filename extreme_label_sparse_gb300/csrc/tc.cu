@@ -66,7 +66,7 @@ constexpr int kDhThreads = 32 * (2 + kDhBuilders);
 // ------------------------------------------------------------------ plans
 struct FwdPlan {
     bool ok = false;
-    int MT = 0, nk = 0, S = 0, issuers = 0;
+    int MT = 0, nk = 0, cw = 0, S = 0, issuers = 0;  // nk TMA boxes of cw columns of W_k
     uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, tmem_cols = 0;
 };
 
@@ -77,6 +77,7 @@ struct DWPlan {
     int ncat = 0;     // 1: the planes are concatenated along N in one pass
     int Nacc = 0;     // accumulator columns per (f tile, group)
     uint32_t a_bytes = 0, z_bytes = 0, stage_bytes = 0, tmem_cols = 0;
+    uint32_t pad_bytes = 0;  // the last f tile's MMA reads this far past the last stage
 };
 
 struct DhPlan {
@@ -99,6 +100,17 @@ bool shape_ok(const sg_layout *lo)
            lo->L % 8 == 0 && lo->ldB % 128 == 0;
 }
 
+// the stage kernels (forward, dW, dh) take any F that is a multiple of 16
+bool shape_ok16(const sg_layout *lo)
+{
+    return lo->G % 16 == 0 && lo->G <= 256 && lo->F % 16 == 0 && lo->F <= 256 &&
+           lo->L % 8 == 0 && lo->ldB % 128 == 0;
+}
+
+// width (columns) of the TMA boxes W_k is loaded in: 64 (128-byte rows,
+// 128-byte swizzle) when it divides F, else 32 (64-byte swizzle), else 16
+int w_box_cols(int F) { return F % 64 == 0 ? 64 : F % 32 == 0 ? 32 : 16; }
+
 // dZ rows of a group must fill whole swizzle rows: 16 or 32 columns, or
 // whole chunks of 64
 bool dz_ok(int G) { return G == 16 || G == 32 || G % 64 == 0; }
@@ -113,14 +125,15 @@ int stages_for(uint32_t stage_bytes)
 FwdPlan plan_fwd(const sg_layout *lo, int B)
 {
     FwdPlan p;
-    if (!shape_ok(lo) || B < 1 || B > 256)
+    if (!shape_ok16(lo) || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
         return p;
-    p.nk = lo->F / 64;
+    p.cw = w_box_cols(lo->F);
+    p.nk = lo->F / p.cw;
     p.a_bytes = (uint32_t)p.MT * 2 * lo->F * 128;
-    p.w_bytes = (uint32_t)p.nk * lo->G * 128;
+    p.w_bytes = (uint32_t)lo->G * lo->F * 2;
     p.stage_bytes = p.a_bytes + p.w_bytes;
     p.S = stages_for(p.stage_bytes);
     if (p.S < 2)  // two stages still overlap loads with MMAs (G = 64, B = 256 has only room for two)
@@ -139,12 +152,16 @@ int dz_swizzle(int G) { return G * 2 >= 128 ? 128 : G * 2; }
 DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 {
     DWPlan p;
-    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->F % 128 != 0 || B < 1 || B > 256)
+    if (!shape_ok16(lo) || !dz_ok(lo->G) || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
         return p;
-    p.FT = lo->F / 128;
+    // tiles of M = 128 rows of f; with F % 128 != 0 the last tile's upper
+    // accumulator lanes read rows past F (the next sample chunk, or the pad
+    // after the last stage) and are never stored
+    p.FT = (lo->F + 127) / 128;
+    p.pad_bytes = (uint32_t)(p.FT * 128 - lo->F) * 128u;
     p.zsw = dz_swizzle(lo->G);
     p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
     p.planes = split ? 2 : 1;
@@ -168,7 +185,7 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 DhPlan plan_dh(const sg_layout *lo, int B, bool split)
 {
     DhPlan p;
-    if (!shape_ok(lo) || !dz_ok(lo->G) || lo->G > 64 || B < 1 || B > 256)
+    if (!shape_ok16(lo) || !dz_ok(lo->G) || lo->G > 64 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
@@ -452,7 +469,7 @@ struct FwdArgs {
     double *loss_part;
     int32_t *status;
     int64_t K, L;
-    int32_t B, G, F, MT, nk, S, issuers, ldB;
+    int32_t B, G, F, MT, nk, cw, S, issuers, ldB;
     uint32_t a_bytes, w_bytes, stage_bytes, tmem_cols;
 };
 
@@ -482,16 +499,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
     if (warp < kProdWarps) {
         // ---------------------------------------------------------- producers
+        // W_k: nk boxes of cw columns (rows of 2 cw bytes, swizzle of that width)
         producer_loop(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes,
                       abort_flag, a.status, [&](int64_t k, uint32_t A, uint32_t fb) {
                           const uint32_t Wt = A + a.a_bytes;
                           for (int kc = 0; kc < a.nk; ++kc)
-                              tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
+                              tma_load_2d(Wt + (uint32_t)kc * G * 2 * a.cw, &tm_w, kc * a.cw, (int)(k * G), fb);
                       });
     } else if (warp < kFirstEpi) {
         // ---------------------------------------------------------- MMA issue
         const int me = warp - kProdWarps;
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
+        const uint32_t wlay = layout_for_swizzle(2 * a.cw);
         int it = 0;
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
             if (it % a.issuers != me)
@@ -515,9 +534,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         // A: H_k, MN-major; 8 f-rows per 1024-byte atom, b chunks F*128 apart
                         const uint64_t ad = sdesc(A + (uint32_t)t * 2 * F * 128 + (uint32_t)st * 2048,
                                                   (uint32_t)F * 128, 1024, kLayoutSW128);
-                        // B: W_k, K-major; 32 bytes per 16 f inside a 128-byte row
-                        const uint64_t bd = sdesc(Wt + (uint32_t)(st / 4) * G * 128 + (uint32_t)(st % 4) * 32,
-                                                  16, 1024, kLayoutSW128);
+                        // B: W_k, K-major; box 16 st / cw, 32 bytes per 16 f inside a 2 cw-byte row
+                        const int f0 = st * 16;
+                        const uint64_t bd = sdesc(Wt + (uint32_t)(f0 / a.cw) * G * 2 * a.cw + (uint32_t)(f0 % a.cw) * 2,
+                                                  16, 16 * a.cw, wlay);
                         mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
                     }
                 }
@@ -729,10 +749,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     for (int i = 0; i < CH; ++i)
                         v[i] += w[i];
                 }
-                uint16_t *dst = a.dW + (k * G + c0) * F + f;
+                if (f < F) {  // lanes past F (last f tile) hold nothing to store
+                    uint16_t *dst = a.dW + (k * G + c0) * F + f;
 #pragma unroll
-                for (int i = 0; i < CH; ++i)
-                    dst[(int64_t)i * F] = bf16_rn(v[i]);
+                    for (int i = 0; i < CH; ++i)
+                        dst[(int64_t)i * F] = bf16_rn(v[i]);
+                }
             }
             tc_fence_before();
             mbar_arrive(bar_addr(c.tempty[acc]));
@@ -1532,7 +1554,8 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
         return SG_ERR_UNSUPPORTED;
     }
     CUtensorMap tm_w;
-    sg_status rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)lo->G, 128, "W");
+    sg_status rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, (uint32_t)p.cw, (uint32_t)lo->G,
+                               2 * p.cw, "W");
     if (rc != SG_OK)
         return rc;
     FwdArgs a;
@@ -1557,6 +1580,7 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     a.F = lo->F;
     a.MT = p.MT;
     a.nk = p.nk;
+    a.cw = p.cw;
     a.S = p.S;
     a.issuers = p.issuers;
     a.ldB = lo->ldB;
@@ -1713,7 +1737,7 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.z_bytes = p.z_bytes;
     a.stage_bytes = p.stage_bytes;
     a.tmem_cols = p.tmem_cols;
-    const size_t smem = (size_t)p.S * p.stage_bytes + 1024;
+    const size_t smem = (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
     const int grid = persistent_grid(lo, lo->K);
     void (*kern)(CUtensorMap, CUtensorMap, DWArgs) = lo->G >= 64 ? k_tc_dW<32> : k_tc_dW<16>;
     rc = set_smem(kern, smem);

@@ -303,10 +303,11 @@ def test_step_single_kernel_large_weights(oracle_mod):
     through the single-kernel step: those groups add their part of dh in fp32
     on CUDA cores, the rest on the tensor cores.  The large-weight groups read
     feature columns 320..447 (across the two CTAs' dh bands, so both take the
-    fp32 path), where h is scaled by 2^-20: their logits stay O(1), so dh is
-    well conditioned in them (with O(1) inputs, logits of ~10^6 would let
-    the fp32 rounding of a rare logit near 0 move dZ, and dh through the huge
-    weights, far beyond any tolerance)."""
+    fp32 path) where h >= 0, and their weights are positive: their logits are
+    ~10^7, sigmoid is exactly 1 and dZ = 1 - y is exact, so dh is well
+    conditioned in them.  (Inside the step dZ reaches dh as one fp16 plane:
+    with O(1) logits and |W| ~ 2^16 its rounding alone moves dh by ~|W| 2^-12
+    per term, beyond the tolerance wherever dh cancels to near zero.)"""
     w = _w("bigw1", B=128, H=768, L=32 * 40, G=32, F=128, pos=36, dist="zipf")
     p = generate(w)
     big = (np.arange(w.K) % 3) == 0
@@ -314,17 +315,16 @@ def test_step_single_kernel_large_weights(oracle_mod):
     idx = p.idx.copy()
     idx[big] = cols
     p.idx = idx
-    hb = p.h.astype(np.uint32)
-    he = (hb >> 7) & 0xFF
-    p.h = np.where(((he > 20) & (he < 0xFF))[:, :] & np.isin(np.arange(w.H), cols)[None, :],
-                   hb - (20 << 7), hb).astype(np.uint16)
-    # the layout sorts groups by label: scale the W rows of the big groups' slots
-    st, sol, los, ids = oracle_mod.layout_build(p.groups, p.idx, w.L, w.G, w.F, w.H)
-    assert st == 0
+    hb = p.h.copy()
+    hb[:, cols] &= np.uint16(0x7FFF)  # h >= 0 on the large-weight groups' columns
+    p.h = hb
+    # W is in slot order (slot s belongs to group s // G): positive and x 2^20
+    # in the large-weight groups' rows
     slot_big = big[np.arange(w.L) // w.G]
     wb = p.W.astype(np.uint32)
     we = (wb >> 7) & 0xFF
-    p.W = np.where((we > 0) & (we < 0xFF - 20) & slot_big[:, None], wb + (20 << 7), wb).astype(np.uint16)
+    scaled = ((wb & 0x7FFF) + (20 << 7)).astype(np.uint32)
+    p.W = np.where((we > 0) & (we < 0xFF - 20) & slot_big[:, None], scaled, wb).astype(np.uint16)
     assert np.abs(bf16_bits_to_f32(p.W)).max() > 2.0 ** 15
     ref = oracle_mod.step(p)
     lay = build_layout(p)
