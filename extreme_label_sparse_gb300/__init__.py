@@ -11,5 +11,6 @@ from .sg import (  # noqa: F401
     SG_ERR_TIMEOUT, SG_ERR_DATA, SG_ENGINE_AUTO, SG_ENGINE_SIMT, SG_ENGINE_TC, SG_ENGINE_FUSED,
     sg_layout_build, sg_layout_export, sg_layout_set_engine, sg_layout_status,
     sg_pos_export, sg_fwd, sg_bce_grad, sg_fwd_bce, sg_bwd, sg_bwd_dW, sg_bwd_dh,
-    sg_step, sg_step_sgd, sg_bce_grad_noalloc, sg_selftest_wait_timeout, sg_timing_start, sg_timing_stop, last_error, status_string, KIND_NAMES,
+    sg_step, sg_step_sgd, sg_bce_grad_noalloc, sg_selftest_wait_timeout, sg_proj_fwd, sg_proj_bwd,
+    sg_headtail_step, sg_timing_start, sg_timing_stop, last_error, status_string, KIND_NAMES,
 )

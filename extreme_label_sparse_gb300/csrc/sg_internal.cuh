@@ -48,6 +48,11 @@ struct sg_layout {
     // the step's max |W| as bf16 magnitude bits (scale of dh's fp16 operands)
     uint32_t *wmax = nullptr;
 
+    // scratch of sg_headtail_step when this layout is the tail (allocated on
+    // first use): projected activations, both branches' dh, bf16 planes
+    void *ht_ws = nullptr;
+    size_t ht_ws_bytes = 0;
+
     // resident clusters of the fused step kernel for the shape keyed by
     // step_ncl_key (0 until the first call)
     int64_t step_ncl = 0, step_ncl_key = 0;

@@ -93,7 +93,8 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
             return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
-            sg_flag(status, SG_ERR_TIMEOUT);
+            if (status)  // kernels without a status word only wind down
+                sg_flag(status, SG_ERR_TIMEOUT);
             return false;
         }
     }

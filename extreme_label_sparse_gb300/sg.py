@@ -64,6 +64,10 @@ def load():
             "sg_step_sgd": ([P, P, i32, P, P, P, i64, C.c_float, C.c_float, P, P, P, P, P], C.c_int),
             "sg_bce_grad_noalloc": ([P, i32, i64, i32, P, P, i64, P, P, P], C.c_int),
             "sg_selftest_wait_timeout": ([C.POINTER(i32)], C.c_int),
+            "sg_proj_fwd": ([P, i32, i32, P, i32, P, P], C.c_int),
+            "sg_proj_bwd": ([P, i32, i32, P, i32, P, P, P, P, i32, P], C.c_int),
+            "sg_headtail_step": ([P, P, P, i32, i32, P, P, P, P, P, i64, P, P, P, i64, P, P, P, P, P, P, P],
+                                 C.c_int),
             "sg_timing_start": ([P, i32], C.c_int),
             "sg_timing_stop": ([P, P, P], C.c_int),
             "sg_last_error": ([], C.c_char_p),
@@ -312,3 +316,39 @@ def sg_selftest_wait_timeout() -> int:
     code = C.c_int32(0)
     _check(load().sg_selftest_wait_timeout(C.byref(code)))
     return int(code.value)
+
+
+# ---------------------------------------------------------------- head-tail split
+def sg_proj_fwd(h: torch.Tensor, P: torch.Tensor, out: torch.Tensor):
+    """out[B][D] = bf16(h[B][E] P[D][E]^T) (bf16 tensors as int16/bfloat16)."""
+    B, E = h.shape
+    D = P.shape[0]
+    _check(load().sg_proj_fwd(_dev(h, "h", _BF16, B * E), B, E, _dev(P, "P", _BF16, D * E), D,
+                              _dev(out, "out", _BF16, B * D), _stream(h.device)))
+
+
+def sg_proj_bwd(h: torch.Tensor, P: torch.Tensor, g: torch.Tensor, work: torch.Tensor, dP: torch.Tensor,
+                dh: torch.Tensor, accumulate_dh: bool = False):
+    """dP = g^T h, dh (+)= g P (fp32); work holds 2*B*D bf16."""
+    B, E = h.shape
+    D = P.shape[0]
+    _check(load().sg_proj_bwd(_dev(h, "h", _BF16, B * E), B, E, _dev(P, "P", _BF16, D * E), D,
+                              _dev(g, "g", (torch.float32,), B * D), _dev(work, "work", _BF16, 2 * B * D),
+                              _dev(dP, "dP", (torch.float32,), D * E), _dev(dh, "dh", (torch.float32,), B * E),
+                              int(bool(accumulate_dh)), _stream(h.device)))
+
+
+def sg_headtail_step(head: "Layout", tail: "Layout", h, P_head, P_tail, W_head, head_rowptr, head_label,
+                     head_nnz, W_tail, tail_rowptr, tail_label, tail_nnz, dW_head, dW_tail, dP_head, dP_tail,
+                     dh, loss):
+    B, E = h.shape
+    Dh, H = head.H, tail.H
+    _check(load().sg_headtail_step(
+        head, tail, _dev(h, "h", _BF16, B * E), B, E, _dev(P_head, "P_head", _BF16, Dh * E),
+        _dev(P_tail, "P_tail", _BF16, H * E), _dev(W_head, "W_head", _BF16, head.L * head.F),
+        _dev(head_rowptr, "head_rowptr", _I32, B + 1), _dev(head_label, "head_label", _I32), int(head_nnz),
+        _dev(W_tail, "W_tail", _BF16, tail.L * tail.F), _dev(tail_rowptr, "tail_rowptr", _I32, B + 1),
+        _dev(tail_label, "tail_label", _I32), int(tail_nnz), _dev(dW_head, "dW_head", _BF16, head.L * head.F),
+        _dev(dW_tail, "dW_tail", _BF16, tail.L * tail.F), _dev(dP_head, "dP_head", (torch.float32,), Dh * E),
+        _dev(dP_tail, "dP_tail", (torch.float32,), H * E), _dev(dh, "dh", (torch.float32,), B * E),
+        _dev(loss, "loss", (torch.float64,), 1), _stream(h.device)))

@@ -216,6 +216,45 @@ SG_API sg_status sg_step_sgd(sg_layout *layout, const sg_bf16 *h, int32_t B,
                       float *mom, sg_bf16 *W_out, float *dh, double *loss,
                       void *stream);
 
+/* ---------------------------------------------------------------- head-tail split
+ * The output layer's head-tail split (HASTE, "Method / overall framework" and
+ * key design "head-tail split"): the encoder output h (B x E) reaches a dense
+ * head and the sparse tail through two light projections, and the objective
+ * is the sum of both branches' BCE terms.  All matrices are row-major; bf16
+ * inputs, fp32 accumulation on the tensor cores.  E, D, Dh and H must be
+ * multiples of 8; pointers 16-byte aligned.
+ *
+ * sg_proj_fwd -- out[B][D] = bf16(h[B][E] P[D][E]^T).                      */
+SG_API sg_status sg_proj_fwd(const sg_bf16 *h, int32_t B, int32_t E, const sg_bf16 *P, int32_t D,
+                             sg_bf16 *out, void *stream);
+
+/* sg_proj_bwd -- the projection's backward from g = dL/d out (fp32 [B][D]):
+ * dP[D][E] = g^T h (fp32, overwritten) and dh[B][E] = g P (fp32; added to dh
+ * when accumulate_dh is nonzero, else overwritten).  g enters the products as
+ * two bf16 planes (value and rounding residual, about 16 bits), written to
+ * work (caller-owned device memory of 2*B*D bf16).                         */
+SG_API sg_status sg_proj_bwd(const sg_bf16 *h, int32_t B, int32_t E, const sg_bf16 *P, int32_t D,
+                             const float *g, sg_bf16 *work, float *dP, float *dh, int32_t accumulate_dh,
+                             void *stream);
+
+/* sg_headtail_step -- the whole step of the split layer:
+ *   h_head = bf16(h P_head^T) (B x Dh),  h_tail = bf16(h P_tail^T) (B x H);
+ *   the head is the layer of `head` (built with every group's index set
+ *   [0, Dh), Dh = head's H: the dense logits h_head W_head^T) stepped on
+ *   h_head with the head positives; the tail is the layer of `tail` stepped
+ *   on h_tail with the tail positives (each as sg_step, same conventions);
+ *   dP_head[Dh][E] = dh_head^T h, dP_tail[H][E] = dh_tail^T h (fp32),
+ *   dh[B][E] = dh_head P_head + dh_tail P_tail (fp32), loss = head + tail.
+ * dW_head[Lh][Dh] and dW_tail[L][F] are bf16 in each layout's slot order.
+ * Scratch for the activations and branch gradients lives in `tail` (about
+ * 10 B (Dh + H) bytes, allocated on first use).                            */
+SG_API sg_status sg_headtail_step(sg_layout *head, sg_layout *tail, const sg_bf16 *h, int32_t B, int32_t E,
+                                  const sg_bf16 *P_head, const sg_bf16 *P_tail, const sg_bf16 *W_head,
+                                  const int32_t *head_rowptr, const int32_t *head_label, int64_t head_nnz,
+                                  const sg_bf16 *W_tail, const int32_t *tail_rowptr, const int32_t *tail_label,
+                                  int64_t tail_nnz, sg_bf16 *dW_head, sg_bf16 *dW_tail, float *dP_head,
+                                  float *dP_tail, float *dh, double *loss, void *stream);
+
 /* ---------------------------------------------------------------- timing
  * Per-kernel device timing for benchmarks: while enabled, every kernel the
  * library launches for this layout is bracketed by a pair of CUDA events
