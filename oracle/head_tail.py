@@ -17,6 +17,13 @@ is the exact gradient of the returned loss).  Backward, by the chain rule:
     dP_head   = dh_head^T h              dP_tail = dh_tail^T h
     dh        = dh_head P_head + dh_tail P_tail
 with dh_tail the tail layer's feature gradient (the oracle's O6).
+
+The pages leave the activations' precision open.  With hidden_bf16=True the
+projected activations h_head and h_tail are rounded to bf16 (fp64 -> fp32 ->
+bf16, round to nearest even each time) before the branches use them, which is
+the reading for a library whose layer takes bf16 inputs; the backward treats
+that rounding as the identity (the gradients reaching h are those of the
+unrounded product).  The default keeps everything in double.
 """
 from __future__ import annotations
 
@@ -33,6 +40,17 @@ def as_f64(a) -> np.ndarray:
     return a.astype(np.float64)
 
 
+def round_bf16(x) -> np.ndarray:
+    """float64 -> nearest fp32 -> nearest bf16 (ties to even), as float64.
+    A bf16 is the upper 16 bits of an fp32: keep them, adding half an ulp of
+    the dropped 16 bits first, less one when the kept part is even."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    keep_odd = (u >> np.uint64(16)) & np.uint64(1)
+    r = ((u + np.uint64(0x7FFF) + keep_odd) >> np.uint64(16)) << np.uint64(16)
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def bce_dense(A, Y):
     """dA = sigmoid(A) - Y and the summed BCE max(a, 0) - y a + log(1 + e^-|a|)
     over every entry (the overflow-free form of -y log s - (1 - y) log(1 - s))."""
@@ -44,11 +62,13 @@ def bce_dense(A, Y):
     return s - Y, loss
 
 
-def head_step(h, P_head, W_head, Y_head):
+def head_step(h, P_head, W_head, Y_head, hidden_bf16: bool = False):
     """Head branch: forward, BCE and its gradients.  Returns a dict with
     h_head, A, dA, loss, dW_head, dh_head (dh_head is w.r.t. h_head)."""
     h, P_head, W_head = as_f64(h), as_f64(P_head), as_f64(W_head)
     h_head = h @ P_head.T
+    if hidden_bf16:
+        h_head = round_bf16(h_head)
     A = h_head @ W_head.T
     dA, loss = bce_dense(A, Y_head)
     return dict(h_head=h_head, A=A, dA=dA, loss=loss, dW_head=dA.T @ h_head, dh_head=dA @ W_head)
@@ -61,14 +81,16 @@ def projections_backward(h, P_head, P_tail, dh_head, dh_tail):
 
 
 def step(h, P_head, P_tail, W_head, Y_head, W_tail, groups, idx, G: int, F: int,
-         pos_rowptr, pos_label):
+         pos_rowptr, pos_label, hidden_bf16: bool = False):
     """The whole head-tail step.  The tail is the group-shared layer (labels
     `groups`, index rows `idx`, weights W_tail in slot order, positives as
     per-sample label lists) on h_tail = h P_tail^T, computed by the oracle's
     O1-O6 in double.  Returns the loss and every gradient."""
     h64, P_tail64 = as_f64(h), as_f64(P_tail)
-    head = head_step(h64, P_head, W_head, Y_head)
+    head = head_step(h64, P_head, W_head, Y_head, hidden_bf16)
     h_tail = h64 @ P_tail64.T
+    if hidden_bf16:
+        h_tail = round_bf16(h_tail)
     H = h_tail.shape[1]
     L = len(groups)
     st, sol, _, ids = layout_build(groups, idx, L, G, F, H)
@@ -84,4 +106,5 @@ def step(h, P_head, P_tail, W_head, Y_head, W_tail, groups, idx, G: int, F: int,
     proj = projections_backward(h64, P_head, P_tail64, head["dh_head"], dh_tail)
     return dict(loss=head["loss"] + tail_loss, head_loss=head["loss"], tail_loss=tail_loss,
                 A=head["A"], Z=Z, dW_head=head["dW_head"], dW_tail=weight_grad(h_tail, dZ, ids, G, F),
-                dh_head=head["dh_head"], dh_tail=dh_tail, idx_sorted=ids, **proj)
+                dh_head=head["dh_head"], dh_tail=dh_tail, h_head=head["h_head"], h_tail=h_tail,
+                idx_sorted=ids, **proj)

@@ -7,12 +7,11 @@ two projections; the loss is the sum of both branches' BCE terms.  The library
 runs the projections and their backward as tcgen05 GEMMs and the head as the
 layer itself with every group's index set [0, Dh).
 
-Precision: the projected activations h_head, h_tail are rounded to bf16 (the
-layer's input type) and the branch gradients enter the backward GEMMs as two
-bf16 planes, so every output carries about 2^-8 relative error from those
-roundings on top of the layer's own; the oracle keeps everything in double.
-The layer's tolerance max |gpu - ref| <= 2e-2 (1 + |ref|) covers both at the
-unit-scale values drawn here.
+Precision: the layer takes bf16 inputs, so the projected activations h_head
+and h_tail are rounded to bf16; the oracle takes the same reading
+(hidden_bf16=True) and otherwise stays in double.  The branch gradients enter
+the backward GEMMs as two bf16 planes (about 16 bits).  The layer's tolerance
+max |gpu - ref| <= 2e-2 (1 + |ref|) applies to every output.
 """
 import numpy as np
 import pytest
@@ -102,7 +101,7 @@ def test_headtail_step_against_oracle(oracle_mod, case):
     P_tail = _scaled_bf16(23, H, E, 1.0 / np.sqrt(E))
     W_head, Y_head, hgroups, hidx, hrp, hlab = _head_problem(B, Dh, Lh, Gh, 31)
     ref = ht.step(h, P_head, P_tail, W_head, Y_head, tp.W, tp.groups, tp.idx, G, F, tp.pos_rowptr,
-                  tp.pos_label)
+                  tp.pos_label, hidden_bf16=True)
 
     head = sg.sg_layout_build(dev_i32(hgroups), Lh, Gh, dev_i32(hidx.reshape(-1)), Dh, Dh, B,
                               max(int(hrp[-1]), 1))

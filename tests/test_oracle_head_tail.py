@@ -80,3 +80,53 @@ def test_head_tail_identity_projections_reduce_to_the_layer():
     np.testing.assert_allclose(out["dW_tail"], ref["dW"], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(out["dh_tail"], ref["dh"], rtol=1e-12, atol=1e-12)
     assert out["tail_loss"] == pytest.approx(ref["loss"], rel=1e-12)
+
+
+def test_round_bf16_values():
+    """Rounding to bf16 (8 significant bits): exact values stay, halfway cases
+    go to the even neighbour, anything past halfway goes up; signs are kept."""
+    u = 2.0 ** -7  # one bf16 ulp at 1
+    cases = [(1.0, 1.0), (1.0 + u / 2, 1.0), (1.0 + 1.5 * u, 1.0 + 2 * u), (1.0 + u / 2 + 2 ** -20, 1.0 + u),
+             (-(1.0 + 1.5 * u), -(1.0 + 2 * u)), (3.0, 3.0), (0.0, 0.0), (2.0 ** -130, 2.0 ** -130),
+             (255.5, 256.0), (254.5, 254.0), (1e-3, 0.00099945068359375)]
+    for x, want in cases:
+        assert ht.round_bf16(np.array([x]))[0] == want, x
+
+
+def test_round_bf16_matches_torch_on_fp32():
+    """On fp32 inputs (no first rounding) the result is torch's own
+    float32 -> bfloat16 conversion, which rounds to nearest even."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(ht.round_bf16(x.astype(np.float64)), want)
+
+
+def test_hidden_bf16_rounds_only_the_activations():
+    """hidden_bf16 changes nothing when both projections already give bf16
+    values (identity projections of a bf16 h); otherwise the tail's gradients
+    are the plain layer's on the rounded activations, and dP, dh are taken
+    from the same branch gradients as without rounding."""
+    rng = np.random.default_rng(7)
+    p = _problem(rng, B=4, E=6, Dh=6, H=6)
+    hb = ht.round_bf16(p["h"])
+    I = np.eye(6)
+    base = dict(p, h=hb, P_head=I, P_tail=I)
+    a = ht.step(**base)
+    b = ht.step(**base, hidden_bf16=True)
+    for k in ("loss", "dW_head", "dW_tail", "dP_head", "dP_tail", "dh"):
+        np.testing.assert_array_equal(a[k], b[k])
+    r = ht.step(**p, hidden_bf16=True)
+    assert np.array_equal(r["h_tail"], ht.round_bf16(r["h_tail"]))
+    assert np.array_equal(r["h_head"], ht.round_bf16(p["h"] @ p["P_head"].T))
+    # the rounded activations change the loss of this draw
+    assert r["loss"] != ht.step(**p)["loss"]
+    # tail gradients: the unrounded oracle run on h_tail as the encoder output
+    # with an identity tail projection
+    q = dict(p, h=r["h_tail"], P_tail=np.eye(p["P_tail"].shape[0]), P_head=np.zeros_like(p["P_head"]))
+    t = ht.step(**q)
+    np.testing.assert_allclose(r["dW_tail"], t["dW_tail"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["dP_tail"], r["dh_tail"].T @ p["h"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["dh"], r["dh_head"] @ p["P_head"] + r["dh_tail"] @ p["P_tail"], rtol=1e-12,
+                               atol=1e-12)
