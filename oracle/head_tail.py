@@ -105,6 +105,6 @@ def step(h, P_head, P_tail, W_head, Y_head, W_tail, groups, idx, G: int, F: int,
     dh_tail = feature_grad(Wt, dZ, ids, G, H)
     proj = projections_backward(h64, P_head, P_tail64, head["dh_head"], dh_tail)
     return dict(loss=head["loss"] + tail_loss, head_loss=head["loss"], tail_loss=tail_loss,
-                A=head["A"], Z=Z, dW_head=head["dW_head"], dW_tail=weight_grad(h_tail, dZ, ids, G, F),
+                A=head["A"], Z=Z, dA=head["dA"], dZ=dZ, dW_head=head["dW_head"], dW_tail=weight_grad(h_tail, dZ, ids, G, F),
                 dh_head=head["dh_head"], dh_tail=dh_tail, h_head=head["h_head"], h_tail=h_tail,
                 idx_sorted=ids, **proj)
