@@ -15,6 +15,8 @@ around each launch, in a separate loop) against the measured HBM peak;
 time against both peaks; `workloads` = step time, per-kernel split and step
 roofline of the other label-space workloads and of the group-size sweep
 (G = 1, 16, 32, 64 with uniform and clustered index sets);
+`headtail` = the head-tail split's whole step (projections, dense head,
+sparse tail) on the same tail with a 3% dense head;
 `cpu_baseline` = the CPU oracle on a bounded sample of the same workload.
 `--impl reference` times that oracle alone (there is no other implementation
 of the method to run).
@@ -334,6 +336,76 @@ def measure_other(sg, torch, dev, p, engine, steps, warmup, stream, hbm, tflops)
     return out
 
 
+HEAD_SHARE_LABELS = 90_112   # ~3% of a 3M label space in the dense head (groups of 32)
+HEAD_DIM, HEAD_G = 128, 32    # head projection width Dh; head layout groups of 32 labels over [0, Dh)
+
+
+def measure_headtail(sg, torch, dev, p, steps, warmup, stream, hbm, tflops):
+    """The head-tail split's whole step (sg_headtail_step) with the tail of
+    workload p (h_tail = h P_tail^T, E = H) and a dense head of
+    HEAD_SHARE_LABELS labels over a Dh = HEAD_DIM projection; 5 uniform head
+    positives per sample."""
+    from workloads import Workload, draw_bf16_matrix
+    w = p.w
+    B, E, H, Dh = w.B, w.H, w.H, HEAD_DIM
+    hw = Workload("head", B=B, H=Dh, L=HEAD_SHARE_LABELS, G=HEAD_G, F=Dh, pos=5, pos_dist="uniform",
+                  zipf_s=0.0, idx_mode="uniform", seed=7)
+    hp = generate(hw)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    h = bf(draw_bf16_matrix(41, B, E, 1.0))
+    P_head = bf(draw_bf16_matrix(42, Dh, E, 1.0 / np.sqrt(E)))
+    P_tail = bf(draw_bf16_matrix(43, H, E, 1.0 / np.sqrt(E)))
+    head = sg.sg_layout_build(i32(hp.groups), hw.L, hw.G, i32(hp.idx.reshape(-1)), hw.F, hw.H, B, hp.nnz)
+    tail = sg.sg_layout_build(i32(p.groups), w.L, w.G, i32(p.idx.reshape(-1)), w.F, w.H, B, max(p.nnz, 1))
+    try:
+        args = dict(W_head=bf(hp.W), head_rowptr=i32(hp.pos_rowptr), head_label=i32(hp.pos_label),
+                    head_nnz=hp.nnz, W_tail=bf(p.W), tail_rowptr=i32(p.pos_rowptr),
+                    tail_label=i32(p.pos_label), tail_nnz=p.nnz,
+                    dW_head=torch.empty((hw.L, hw.F), dtype=torch.int16, device=dev),
+                    dW_tail=torch.empty((w.L, w.F), dtype=torch.int16, device=dev),
+                    dP_head=torch.empty((Dh, E), dtype=torch.float32, device=dev),
+                    dP_tail=torch.empty((H, E), dtype=torch.float32, device=dev),
+                    dh=torch.empty((B, E), dtype=torch.float32, device=dev),
+                    loss=torch.zeros(1, dtype=torch.float64, device=dev))
+
+        def step():
+            sg.sg_headtail_step(head, tail, h, P_head, P_tail, **args)
+
+        for _ in range(max(warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        st = sg.sg_layout_status(head) | sg.sg_layout_status(tail)
+    finally:
+        head.close()
+        tail.close()
+    tb, tf = algorithmic(w, B, "step")
+    hb, hf = algorithmic(hw, B, "step")
+    proj_b = (Dh + H) * E * (2 + 4) + B * E * (2 + 4)  # P read, dP written (fp32), h read, dh written
+    proj_f = 3 * 2 * B * E * (Dh + H)                  # forward, dP, dh
+    bytes_, flops = tb + hb + proj_b, tf + hf + proj_f
+    s = ms * 1e-3
+    return {"ms_per_step": ms, "status": st,
+            "config": {"B": B, "E": E, "head": {"L": hw.L, "G": hw.G, "Dh": Dh, "pos": hw.pos},
+                       "tail": {"L": w.L, "G": w.G, "F": w.F, "H": H}},
+            "roofline_step": {"bytes": bytes_, "flops": flops, "achieved_gbs": bytes_ / s / 1e9,
+                              "frac_hbm": bytes_ / s / 1e9 / hbm,
+                              "achieved_tflops": flops / s / 1e12,
+                              "frac_tensor": flops / s / 1e12 / tflops}}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -461,6 +533,9 @@ def run_ours(args):
     launches = sum(v[1] for v in kinds.values())
     r.close()
     del r
+    headtail = None
+    if rank == 0 and world == 1 and not args.labels and not args.no_others and not args.sgd:
+        headtail = measure_headtail(sg, torch, dev, p, args.other_steps, 2, stream, hbm, tflops)
 
     workloads = {}
     for name, fut in futures:
@@ -490,6 +565,8 @@ def run_ours(args):
     }
     if workloads:
         line["workloads"] = workloads
+    if headtail is not None:
+        line["headtail"] = headtail
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -317,8 +317,9 @@ sg_status sg_layout_set_engine(sg_layout *lo, int32_t engine)
         engine != SG_ENGINE_FUSED)
         FAIL(SG_ERR_INVALID, "%s: unknown engine %d", fn, engine);
     if ((engine == SG_ENGINE_TC || engine == SG_ENGINE_FUSED) && !lo->tc_ok)
-        FAIL(SG_ERR_UNSUPPORTED, "%s: the tensor-core engine needs G %% 16 == 0 and "
-             "F %% 16 == 0 (G=%d, F=%d)", fn, lo->G, lo->F);
+        FAIL(SG_ERR_UNSUPPORTED, "%s: the tensor-core engine needs G in {16, 32} or a multiple of 64, "
+             "F %% 16 == 0, and the group's tiles within shared memory and TMEM (G=%d, F=%d, max_B=%d)",
+             fn, lo->G, lo->F, lo->max_B);
     lo->engine = engine;
     return SG_OK;
 }
@@ -489,11 +490,16 @@ sg_status sg_bwd(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h, int32_t B,
 // ---------------------------------------------------------------- step
 namespace {
 
-// the step after argument checks; with sgd, dW receives the updated weights
-sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
-                    const int32_t *pos_rowptr, const int32_t *pos_label, int64_t nnz, sg_bf16 *dW,
-                    float *dh, double *loss, const sg_sgd *sgd, cudaStream_t st, const char *fn)
+// Which kernels a step of B samples runs: the whole step in one kernel on
+// CTA clusters, the fused forward + BCE + dW kernel then dh, or one kernel per
+// phase on the engine each phase fits.
+struct StepPath {
+    int single = 0, fused = 0, tc_f = 0, tc_w = 0, tc_h = 0;
+};
+
+sg_status step_path(const sg_layout *lo, int32_t B, bool sgd, StepPath *p, const char *fn)
 {
+    *p = StepPath();
     // shapes the fused forward + BCE + dW kernel and the dh kernel cannot run
     // (e.g. F not a multiple of 64) take the whole step in one kernel on CTA
     // clusters, where it fits: dZ never leaves the chip there, but on the
@@ -501,20 +507,39 @@ sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W
     const bool two_kernel = lo->engine != SG_ENGINE_SIMT && tc_fwdw_ok(lo, B) && tc_stage_ok(lo, SG_KIND_DH, B);
     if (!sgd && lo->engine != SG_ENGINE_SIMT && (!two_kernel || lo->engine == SG_ENGINE_FUSED) &&
         tc_step_ok(lo, B)) {
+        p->single = p->tc_f = p->tc_w = p->tc_h = 1;
+        return SG_OK;
+    }
+    // the fused forward + BCE + dW kernel and the tensor-core dh, with dZ in
+    // the group-tiled workspace, whenever the shape fits them
+    if (lo->engine != SG_ENGINE_SIMT && lo->tc_ok && two_kernel) {
+        p->fused = p->tc_f = p->tc_w = p->tc_h = 1;
+        return SG_OK;
+    }
+    bool f = false, w = false, h = false;
+    TRY(pick_tc(lo, SG_KIND_FWD, B, &f, fn));
+    TRY(pick_tc(lo, SG_KIND_DW, B, &w, fn));
+    TRY(pick_tc(lo, SG_KIND_DH, B, &h, fn));
+    p->tc_f = f;
+    p->tc_w = w;
+    p->tc_h = h;
+    return SG_OK;
+}
+
+// the step after argument checks; with sgd, dW receives the updated weights
+sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
+                    const int32_t *pos_rowptr, const int32_t *pos_label, int64_t nnz, sg_bf16 *dW,
+                    float *dh, double *loss, const sg_sgd *sgd, cudaStream_t st, const char *fn)
+{
+    StepPath path;
+    TRY(step_path(lo, B, sgd != nullptr, &path, fn));
+    if (path.single) {
         TRY(simt_transpose_h(lo, h, B, st));
         TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
         return tc_step(lo, B, W, dW, dh, loss, st);
     }
-    // the fused forward + BCE + dW kernel and the tensor-core dh, with dZ in
-    // the group-tiled workspace, whenever the shape fits them
-    const bool fused = lo->engine != SG_ENGINE_SIMT && lo->tc_ok && tc_fwdw_ok(lo, B) &&
-                       tc_stage_ok(lo, SG_KIND_DH, B);
-    bool tc_f = fused, tc_w = fused, tc_h = fused;
-    if (!fused) {
-        TRY(pick_tc(lo, SG_KIND_FWD, B, &tc_f, fn));
-        TRY(pick_tc(lo, SG_KIND_DW, B, &tc_w, fn));
-        TRY(pick_tc(lo, SG_KIND_DH, B, &tc_h, fn));
-    }
+    const bool fused = path.fused != 0;
+    const bool tc_f = path.tc_f, tc_w = path.tc_w, tc_h = path.tc_h;
     TRY(simt_transpose_h(lo, h, B, st));
     TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
     // forward + BCE into dZ scratch, then dW and dh from it.  Outside the
@@ -547,6 +572,22 @@ sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W
 }
 
 }  // namespace
+
+sg_status sg_step_plan(const sg_layout *lo, int32_t B, int32_t sgd, int32_t *plan)
+{
+    const char *fn = "sg_step_plan";
+    if (!lo || !plan)
+        FAIL(SG_ERR_INVALID, "%s: layout or plan is NULL", fn);
+    if (B < 1 || B > lo->max_B)
+        FAIL(SG_ERR_INVALID, "%s: B=%d outside [1, max_B=%d]", fn, B, lo->max_B);
+    StepPath p;
+    TRY(step_path(lo, B, sgd != 0, &p, fn));
+    plan[0] = p.single ? SG_PLAN_ONE_KERNEL : p.fused ? SG_PLAN_FUSED_FWDW : SG_PLAN_PER_PHASE;
+    plan[1] = p.tc_f;
+    plan[2] = p.tc_w;
+    plan[3] = p.tc_h;
+    return SG_OK;
+}
 
 sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
                   const int32_t *pos_rowptr, const int32_t *pos_label,

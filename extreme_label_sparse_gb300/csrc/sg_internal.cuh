@@ -9,7 +9,7 @@
 // ----------------------------------------------------------------- limits
 constexpr int SG_MAX_B = 256;
 constexpr int SG_MAX_F = 256;
-constexpr int SG_MAX_H = 1024;
+constexpr int SG_MAX_H = 65535;  // idx is u16
 constexpr int SG_MAX_G = 256;
 
 // ----------------------------------------------------------------- layout

@@ -270,21 +270,26 @@ struct DhArgs {
     int32_t B, G, F, H;
     int32_t nbt;      // sample tiles
     int64_t nchunk;   // slot chunks in total
-    int32_t nct;      // CTAs per sample tile
+    int32_t nct;      // CTAs per (sample tile, column window)
+    int32_t hw, ncw;  // dh columns per window, windows
 };
 
 __global__ void __launch_bounds__(kThreads) k_simt_dh(DhArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int F = a.F, H = a.H, G = a.G;
-    const int ldp = H + 1;
-    float *part = reinterpret_cast<float *>(smem);                 // [32][H+1]
+    const int ldp = a.hw + 1;
+    float *part = reinterpret_cast<float *>(smem);                 // [32][hw+1]
     float *Ws = part + kBT * ldp;                                  // [32][F]
     float *dZs = Ws + 32 * F;                                      // [32][33]
     uint16_t *idxc = reinterpret_cast<uint16_t *>(dZs + kBT * 33); // [32][F]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int bt = blockIdx.x % a.nbt, c = blockIdx.x / a.nbt;
+    const int bt = blockIdx.x % a.nbt;
+    const int cw = (blockIdx.x / a.nbt) % a.ncw;  // this CTA's window of dh columns
+    const int c = blockIdx.x / (a.nbt * a.ncw);
     const int brow0 = bt * kBT;
+    const int j0 = cw * a.hw;
+    const int jn = H - j0 < a.hw ? H - j0 : a.hw;
     const int64_t q0 = a.nchunk * c / a.nct, q1 = a.nchunk * (c + 1) / a.nct;
 
     for (int e = tid; e < kBT * ldp; e += kThreads)
@@ -313,6 +318,9 @@ __global__ void __launch_bounds__(kThreads) k_simt_dh(DhArgs a)
             idxc[e] = a.idx_s[kfirst * F + e];
         __syncthreads();
         for (int it = warp; it < ng * F; it += kThreads / 32) {
+            const int j = (int)idxc[it] - j0;  // the same for the whole warp
+            if (j < 0 || j >= jn)
+                continue;
             const int g = it / F, f = it - g * F;
             const int64_t kb = (kfirst + g) * G;
             const int sa = (int)(max(kb, s0) - s0);
@@ -320,15 +328,15 @@ __global__ void __launch_bounds__(kThreads) k_simt_dh(DhArgs a)
             float acc = 0.f;
             for (int s = sa; s < sb; ++s)
                 acc = fmaf(dZs[lane * 33 + s], Ws[s * F + f], acc);
-            atomicAdd(&part[lane * ldp + idxc[it]], acc);
+            atomicAdd(&part[lane * ldp + j], acc);
         }
     }
     __syncthreads();
-    for (int e = tid; e < kBT * H; e += kThreads) {
-        int b = e / H, i = e - b * H;
+    for (int e = tid; e < kBT * jn; e += kThreads) {
+        int b = e / jn, i = e - b * jn;
         int row = brow0 + b;
         if (row < a.B)
-            atomicAdd(&a.dh[(int64_t)row * H + i], part[b * ldp + i]);
+            atomicAdd(&a.dh[(int64_t)row * H + j0 + i], part[b * ldp + i]);
     }
 }
 
@@ -468,17 +476,22 @@ sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
     a.H = lo->H;
     a.nbt = (int)ceil_div(B, kBT);
     a.nchunk = ceil_div(lo->L, 32);
-    int64_t nct = ((int64_t)lo->num_sms * 2 + a.nbt - 1) / a.nbt;
+    // windows of at most 1024 dh columns (the CTA's shared-memory partial);
+    // every window scans all slots and keeps the products that land in it
+    a.ncw = (int)ceil_div(a.H, 1024);
+    a.hw = (int)ceil_div(a.H, a.ncw);
+    int64_t nct = ((int64_t)lo->num_sms * 2 + (int64_t)a.nbt * a.ncw - 1) / ((int64_t)a.nbt * a.ncw);
     if (nct > a.nchunk)
         nct = a.nchunk;
     if (nct < 1)
         nct = 1;
     a.nct = (int)nct;
-    const size_t smem = (size_t)kBT * (a.H + 1) * 4 + 32 * a.F * 4 + kBT * 33 * 4 +
+    const size_t smem = (size_t)kBT * (a.hw + 1) * 4 + 32 * a.F * 4 + kBT * 33 * 4 +
                         32 * a.F * 2;
     SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * a.H, st));
     SG_SET_SMEM(k_simt_dh, smem);
-    SG_LAUNCH(lo, SG_KIND_DH, st, k_simt_dh<<<a.nbt * a.nct, kThreads, smem, st>>>(a));
+    SG_LAUNCH(lo, SG_KIND_DH, st,
+              k_simt_dh<<<(unsigned)((int64_t)a.nbt * a.ncw * a.nct), kThreads, smem, st>>>(a));
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }

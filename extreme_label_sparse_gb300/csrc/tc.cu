@@ -78,11 +78,13 @@ struct DWPlan {
     int Nacc = 0;     // accumulator columns per (f tile, group)
     uint32_t a_bytes = 0, z_bytes = 0, stage_bytes = 0, tmem_cols = 0;
     uint32_t pad_bytes = 0;  // the last f tile's MMA reads this far past the last stage
+    int stream_t = 0;        // 1: a stage holds one 128-sample tile, a group takes MT stages
 };
 
 struct DhPlan {
     bool ok = false;
     int MT = 0, S = 0, zsw = 0, nbands = 0, band_w = 0, bwt = 0, nbuf = 0;
+    int gs = 0, sub = 1;  // subgroup size (<= 64) and subgroups per group
     uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, ws_bytes = 0, tmem_cols = 0;
 };
 
@@ -165,12 +167,23 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
     p.zsw = dz_swizzle(lo->G);
     p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
     p.planes = split ? 2 : 1;
-    p.ncat = (split && 2 * lo->G <= 256) ? 1 : 0;
+    // hi and lo side by side along N when that fits the MMA's N and, double
+    // buffered, TMEM; else the lo pass accumulates onto the hi pass
+    p.ncat = (split && 2 * lo->G <= 256 && 2 * p.FT * 2 * lo->G <= 512) ? 1 : 0;
     p.Nacc = p.ncat ? 2 * lo->G : lo->G;
     p.a_bytes = (uint32_t)p.MT * 2 * lo->F * 128;
     p.z_bytes = (uint32_t)p.planes * p.nzc * p.MT * 128 * p.zsw;
     p.stage_bytes = p.a_bytes + p.z_bytes;
     p.S = stages_for(p.stage_bytes);
+    if (p.S < 2 && p.MT > 1) {
+        // both sample tiles of a group do not fit twice: stream the tiles
+        // through the stages, accumulating over them in TMEM
+        p.stream_t = 1;
+        p.a_bytes = 2u * (uint32_t)lo->F * 128;
+        p.z_bytes = (uint32_t)p.planes * p.nzc * 128 * p.zsw;
+        p.stage_bytes = p.a_bytes + p.z_bytes;
+        p.S = stages_for(p.stage_bytes);
+    }
     if (p.S < 2)
         return p;
     const int per = p.FT * p.Nacc;
@@ -185,31 +198,41 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 DhPlan plan_dh(const sg_layout *lo, int B, bool split)
 {
     DhPlan p;
-    if (!shape_ok16(lo) || !dz_ok(lo->G) || lo->G > 64 || B < 1 || B > 256)
+    if (!shape_ok16(lo) || !dz_ok(lo->G) || lo->G > 256 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
         return p;
-    p.zsw = dz_swizzle(lo->G);
+    // groups of more than 64 labels run as G / 64 subgroups of 64 that share
+    // the group's I_k (dh = sum over the subgroups of dZ_sub Ws_sub)
+    const int Gs = lo->G > 64 ? 64 : lo->G;
+    p.gs = Gs;
+    p.sub = lo->G / Gs;
+    p.zsw = dz_swizzle(Gs);
     p.z_bytes = (uint32_t)(split ? 2 : 1) * 128 * p.zsw;
-    p.w_bytes = (uint32_t)lo->G * lo->F * 2;
-    // bands of at most 384 dh columns (TMEM accumulator: 128 samples x band)
-    p.nbands = (lo->H + 383) / 384;
-    p.bwt = ((lo->H + p.nbands - 1) / p.nbands + 127) / 128;
-    p.band_w = p.bwt * 128;
+    p.w_bytes = (uint32_t)Gs * lo->F * 2;
     // the group's sorted index row I_k (u16)
     p.i_bytes = (uint32_t)((lo->F * 2 + 127) / 128 * 128);
     // one unit = P groups: [dZ x P][W^T x P][I_k x P]
     // (whole KB, so that every stage's dZ tiles sit on swizzle-atom boundaries)
-    const uint32_t P = (uint32_t)dh_units(lo->G);
+    const uint32_t P = (uint32_t)dh_units(Gs);
     p.stage_bytes = (P * (p.z_bytes + p.w_bytes + p.i_bytes) + 1023u) & ~1023u;
-    p.ws_bytes = P * (uint32_t)p.band_w * 2 * lo->G;  // one row of G values per dh column
-    p.tmem_cols = pow2_cols(p.band_w);
     // two builder teams, one buffer each (a third team and buffer cost a
     // stage, and measured slower)
     p.nbuf = 2;
-    const long room = (long)kSmemBudget - (long)p.nbuf * p.ws_bytes;
-    p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
+    // bands of at most 384 dh columns (TMEM accumulator: 128 samples x band),
+    // narrower where two Ws buffers of that width leave no room for two stages
+    for (int maxw = 3; maxw >= 1; --maxw) {
+        p.nbands = (lo->H + 128 * maxw - 1) / (128 * maxw);
+        p.bwt = ((lo->H + p.nbands - 1) / p.nbands + 127) / 128;
+        p.band_w = p.bwt * 128;
+        p.ws_bytes = P * (uint32_t)p.band_w * 2 * Gs;  // one row of Gs values per dh column
+        const long room = (long)kSmemBudget - (long)p.nbuf * p.ws_bytes;
+        p.S = room > 0 ? (int)(room / p.stage_bytes) : 0;
+        if (p.S >= 2)
+            break;
+    }
+    p.tmem_cols = pow2_cols(p.band_w);
     if (p.S > kMaxStages)
         p.S = kMaxStages;
     // the flush transposes through 12 x 33 x 32 floats of shared memory
@@ -632,8 +655,48 @@ struct DWArgs {
     int32_t *status;
     int64_t K, L;
     int32_t B, G, F, MT, FT, S, nzc, zsw, planes, ncat, Nacc, issuers, ldB;
+    int32_t stream_t;  // 1: one 128-sample tile per stage, MT stages per group
     uint32_t a_bytes, z_bytes, stage_bytes, tmem_cols;
 };
+
+// The producers of the dW stage when a group's sample tiles stream through
+// the stages one at a time: group k, tile t fills stage (k's position) * MT + t
+// with the tile's H_k rows and dZ rows.
+template <typename IssueTma>
+__device__ __forceinline__ void producer_loop_tiles(Ctl &c, uint32_t stage0, uint32_t stage_bytes, int S,
+                                                    int64_t K, int MT, const uint16_t *idx_s,
+                                                    const uint16_t *hT, int ldB, int F, uint32_t tma_bytes,
+                                                    volatile int *abort_flag, int32_t *status,
+                                                    IssueTma issue_tma)
+{
+    const int t0 = threadIdx.x;
+    const int lane = t0 & 31;
+    int it = 0;
+    bool live = true;
+    for (int64_t k = blockIdx.x; k < K && live; k += gridDim.x) {
+        const GatherIdx cur = gather_idx_of(idx_s, k, F, lane);
+        for (int t = 0; t < MT; ++t, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status)) {
+                live = false;
+                break;
+            }
+            const uint32_t A = stage0 + (uint32_t)s * stage_bytes;
+            if (t0 == 0) {
+                mbar_arrive_expect_tx(bar_addr(c.full[s]), tma_bytes);
+                issue_tma(k, t, A, bar_addr(c.full[s]));
+            }
+            issue_gather(hT + (size_t)t * 128, ldB, A, F, 16, cur, lane);
+            cp_async_arrive_noinc(bar_addr(c.full[s]));
+        }
+    }
+    cp_async_wait_all();
+    if (*abort_flag) {
+        for (int j = it - S < 0 ? 0 : it - S; j < it; ++j)
+            mbar_wait_drain(bar_addr(c.full[j % S]), (uint32_t)(j / S) & 1u);
+    }
+}
 
 template <int CH>
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -645,7 +708,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t stage0 = (smem_u32(dsm) + 1023u) & ~1023u;
     const int G = a.G, F = a.F, S = a.S;
-    const uint32_t zrows = (uint32_t)a.MT * 128;
+    const int MTs = a.stream_t ? 1 : a.MT;  // sample tiles held by one stage
+    const int T = a.stream_t ? a.MT : 1;    // stages per group
+    const uint32_t zrows = (uint32_t)MTs * 128;
     const uint32_t zchunk = zrows * (uint32_t)a.zsw;          // one dZ chunk (<= 64 j)
     const uint32_t zplane = (uint32_t)a.nzc * zchunk;         // all of G for hi or lo
     const int nacc = 2 * a.issuers;
@@ -663,7 +728,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
 
-    if (warp < kProdWarps) {
+    if (warp < kProdWarps && T > 1) {
+        producer_loop_tiles(c, stage0, a.stage_bytes, S, a.K, T, a.idx_s, a.hT, a.ldB, F, a.z_bytes, abort_flag,
+                            a.status, [&](int64_t k, int t, uint32_t A, uint32_t fb) {
+                                const uint32_t Zs = A + a.a_bytes;
+                                for (int pc = 0; pc < a.planes * a.nzc; ++pc) {
+                                    const int pl = pc / a.nzc, cj = pc % a.nzc;
+                                    if (a.dZt) {
+                                        // rows [128 t, 128 t + 128) of chunk cj of plane pl
+                                        const size_t src = (size_t)k * a.tile_bytes +
+                                                           ((size_t)pc * a.MT * 128 + (size_t)t * 128) * a.zsw;
+                                        bulk_load(Zs + (uint32_t)pc * zchunk, a.dZt + src, zchunk, fb);
+                                    } else {
+                                        tma_load_2d(Zs + (uint32_t)pc * zchunk, pl ? &tm_zl : &tm_z,
+                                                    (int)(k * G + cj * 64), t * 128, fb);
+                                    }
+                                }
+                            });
+    } else if (warp < kProdWarps) {
         producer_loop(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.z_bytes,
                       abort_flag, a.status, [&](int64_t k, uint32_t A, uint32_t fb) {
                           const uint32_t Zs = A + a.a_bytes;
@@ -686,17 +768,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t idesc = idesc_bf16(128, a.Nacc, 0, 1);
         const int passes = a.ncat ? 1 : a.planes;
         int it = 0;
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
+        bool live = true;
+        for (int64_t k = blockIdx.x; k < a.K && live; k += gridDim.x, ++it) {
             if (it % a.issuers != me)
                 continue;
-            const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
             const int acc = acc_slot(it, a.issuers);
             if (!mbar_wait(bar_addr(c.tempty[acc]), acc_phase(it, a.issuers) ^ 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
-            if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status))
+          for (int t = 0; t < T; ++t) {
+            const int is = it * T + t;  // stage sequence number
+            const int s = is % S;
+            const uint32_t ph = (uint32_t)(is / S) & 1u;
+            if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status)) {
+                live = false;
                 break;
+            }
             tc_fence_after();
             fence_proxy_async();  // cp.async-written H_k -> the MMA (async proxy)
             if (lane == 0) {
@@ -705,7 +792,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 for (int tf = 0; tf < a.FT; ++tf) {
                     const uint32_t d = tbase + (uint32_t)(acc * per + tf * a.Nacc);
                     for (int ps = 0; ps < passes; ++ps) {
-                        for (int st = 0; st < a.MT * 8; ++st) {
+                        for (int st = 0; st < MTs * 8; ++st) {
                             // A: H_k^T, K-major (rows f, K = b): b chunk st/4, 32 B per 16 b
                             const uint64_t ad = sdesc(A + (uint32_t)(st / 4) * F * 128 +
                                                           (uint32_t)tf * 128 * 128 + (uint32_t)(st % 4) * 32,
@@ -713,14 +800,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                             // B: dZ_k, MN-major (N = j, K = b): 16 b rows per step
                             const uint64_t bd = sdesc(Zs + (uint32_t)ps * zplane + (uint32_t)st * 16 * a.zsw,
                                                       zchunk, 8 * a.zsw, zlayout);
-                            mma_bf16(d, ad, bd, idesc, (ps > 0 || st > 0) ? 1u : 0u);
+                            mma_bf16(d, ad, bd, idesc, (t > 0 || ps > 0 || st > 0) ? 1u : 0u);
                         }
                     }
                 }
                 mma_commit(bar_addr(c.empty[s]));
-                mma_commit(bar_addr(c.tfull[acc]));
+                if (t == T - 1)
+                    mma_commit(bar_addr(c.tfull[acc]));
             }
             __syncwarp();
+          }
         }
         if (lane == 0)
             mma_commit(bar_addr(c.drain[me]));
@@ -1189,8 +1278,9 @@ struct DhArgs {
     uint64_t tile_bytes;
     float *dh;
     int32_t *status;
-    int64_t K, L, Kc;      // Kc: groups per CTA (a contiguous range)
+    int64_t K, L, Kc;      // K: subgroups; Kc: subgroups per CTA (a contiguous range)
     int32_t B, G, F, H, MT, S, zsw, nbands, band_w, parts, npass, Bp, nbuf;
+    int32_t sub;           // subgroups of G (<= 64) labels per group
     uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, ws_bytes, tmem_cols;
 };
 
@@ -1293,10 +1383,14 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 const int64_t k = k0 + lane;
                 const uint32_t Zs = st + zoff + (uint32_t)lane * a.z_bytes;
                 if (a.dZt) {
-                    // rows [128 mt, 128 mt + 128) of each plane of the tile
-                    const uint8_t *tz = a.dZt + (size_t)k * a.tile_bytes + (size_t)mt * zchunk;
+                    // rows [128 mt, 128 mt + 128) of the subgroup's chunk of
+                    // each plane of its group's tile
+                    const int64_t kg = k / a.sub;
+                    const int cj = (int)(k - kg * a.sub);
+                    const uint8_t *tz = a.dZt + (size_t)kg * a.tile_bytes +
+                                        ((size_t)cj * a.Bp + (size_t)mt * 128) * a.zsw;
                     for (int pl = 0; pl < NPASS; ++pl)
-                        bulk_load(Zs + (uint32_t)pl * zchunk, tz + (size_t)pl * a.Bp * a.zsw, zchunk, fb);
+                        bulk_load(Zs + (uint32_t)pl * zchunk, tz + (size_t)pl * a.sub * a.Bp * a.zsw, zchunk, fb);
                 } else {
                     tma_load_2d(Zs, &tm_z, (int)(k * G), mt * 128, fb);
                     if (NPASS > 1)
@@ -1304,8 +1398,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 }
                 // W_k: G contiguous rows of F
                 bulk_load(st + woff + (uint32_t)lane * a.w_bytes, a.W + k * G * F, a.w_bytes, fb);
-                // I_k: the dh column of each f
-                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + k * F, (uint32_t)(2 * F), fb);
+                // I_k: the dh column of each f (shared by the group's subgroups)
+                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + (k / a.sub) * F, (uint32_t)(2 * F), fb);
             }
             __syncwarp();
         }
@@ -1518,7 +1612,11 @@ int persistent_grid(const sg_layout *lo, int64_t work)
 }  // namespace
 
 // ------------------------------------------------------------------ host side
-bool tc_supported(const sg_layout *lo) { return plan_fwd(lo, lo->max_B).ok; }
+// some phase of a step of up to max_B samples fits the tensor cores
+bool tc_supported(const sg_layout *lo)
+{
+    return plan_fwd(lo, lo->max_B).ok || plan_dW(lo, lo->max_B, true).ok || plan_dh(lo, lo->max_B, true).ok;
+}
 
 bool tc_stage_ok(const sg_layout *lo, int stage, int B)
 {
@@ -1700,14 +1798,14 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     memset(&tm_z, 0, sizeof(tm_z));
     if (!dZt) {
         rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
-                         (uint32_t)(p.MT * 128), p.zsw, "dZ");
+                         (uint32_t)(p.stream_t ? 128 : p.MT * 128), p.zsw, "dZ");
         if (rc != SG_OK)
             return rc;
     }
     tm_zl = tm_z;
     if (dZ_lo && !dZt) {
         rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)zbox,
-                         (uint32_t)(p.MT * 128), p.zsw, "dZ_lo");
+                         (uint32_t)(p.stream_t ? 128 : p.MT * 128), p.zsw, "dZ_lo");
         if (rc != SG_OK)
             return rc;
     }
@@ -1733,6 +1831,7 @@ sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.Nacc = p.Nacc;
     a.issuers = p.issuers;
     a.ldB = lo->ldB;
+    a.stream_t = p.stream_t;
     a.a_bytes = p.a_bytes;
     a.z_bytes = p.z_bytes;
     a.stage_bytes = p.stage_bytes;
@@ -1778,13 +1877,13 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     sg_status rc = SG_OK;
     memset(&tm_z, 0, sizeof(tm_z));
     if (!dZt) {
-        rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)lo->G, 128, p.zsw, "dZ");
+        rc = make_map_2d(&tm_z, dZ, (uint64_t)lo->L, (uint64_t)B, (uint32_t)p.gs, 128, p.zsw, "dZ");
         if (rc != SG_OK)
             return rc;
     }
     tm_zl = tm_z;
     if (dZ_lo && !dZt) {
-        rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)lo->G, 128, p.zsw,
+        rc = make_map_2d(&tm_zl, dZ_lo, (uint64_t)lo->L, (uint64_t)B, (uint32_t)p.gs, 128, p.zsw,
                          "dZ_lo");
         if (rc != SG_OK)
             return rc;
@@ -1801,15 +1900,16 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.tile_bytes = dzt_f16 ? tc_dz_tile_bytes(lo, B) / 2 : tc_dz_tile_bytes(lo, B);
     a.dh = dh;
     a.status = lo->status;
-    a.K = lo->K;
+    a.K = lo->K * p.sub;  // subgroups
+    a.sub = p.sub;
     a.L = lo->L;
     a.B = B;
-    a.G = lo->G;
+    a.G = p.gs;
     a.F = lo->F;
     a.H = lo->H;
     a.MT = p.MT;
     a.S = p.S;
-    a.zsw = p.zsw;  // = min(2G, 128), which the kernel also derives from G
+    a.zsw = p.zsw;  // = min(2 Gs, 128), which the kernel also derives from Gs
     a.nbands = p.nbands;
     a.band_w = p.band_w;
     a.npass = split ? 2 : 1;
@@ -1817,10 +1917,10 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     int parts = lo->num_sms / (p.nbands * p.MT);
     if (parts < 1)
         parts = 1;
-    // contiguous ranges of whole units of groups
-    int64_t kc = (lo->K + parts - 1) / parts;
-    kc = (kc + dh_units(lo->G) - 1) / dh_units(lo->G) * dh_units(lo->G);
-    parts = (int)((lo->K + kc - 1) / kc);
+    // contiguous ranges of whole units of subgroups
+    int64_t kc = (a.K + parts - 1) / parts;
+    kc = (kc + dh_units(p.gs) - 1) / dh_units(p.gs) * dh_units(p.gs);
+    parts = (int)((a.K + kc - 1) / kc);
     a.parts = parts;
     a.Kc = kc;
     a.z_bytes = p.z_bytes;
@@ -1832,7 +1932,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.tmem_cols = p.tmem_cols;
     // kernel instance for (planes, K steps per plane, 128-column blocks per band)
     void (*kern)(CUtensorMap, CUtensorMap, DhArgs) = nullptr;
-    const int nks = lo->G / 16;
+    const int nks = p.gs / 16;
 #define SG_DH_PICK(P, K, N, H16)                                          \
     if (a.npass == P && nks == K && p.bwt == N && dzt_f16 == H16)         \
         kern = k_tc_dh<P, K, N, H16>;
@@ -1847,7 +1947,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     SG_DH_PICK(1, 4, 1, true) SG_DH_PICK(1, 4, 2, true) SG_DH_PICK(1, 4, 3, true)
 #undef SG_DH_PICK
     if (!kern) {
-        sg_set_error("tc_dh: no kernel for G = %d, band of %d columns", lo->G, p.band_w);
+        sg_set_error("tc_dh: no kernel for G = %d (subgroups of %d), band of %d columns", lo->G, p.gs, p.band_w);
         return SG_ERR_UNSUPPORTED;
     }
     const size_t smem = (size_t)p.nbuf * p.ws_bytes + (size_t)p.S * p.stage_bytes + 1024;

@@ -65,6 +65,7 @@ def load():
             "sg_bce_grad_noalloc": ([P, i32, i64, i32, P, P, i64, P, P, P], C.c_int),
             "sg_selftest_wait_timeout": ([C.POINTER(i32)], C.c_int),
             "sg_proj_fwd": ([P, i32, i32, P, i32, P, P], C.c_int),
+            "sg_step_plan": ([P, i32, i32, C.POINTER(i32)], C.c_int),
             "sg_proj_bwd": ([P, i32, i32, P, i32, P, P, P, P, i32, P], C.c_int),
             "sg_headtail_step": ([P, P, P, i32, i32, P, P, P, P, P, i64, P, P, P, i64, P, P, P, P, P, P, P],
                                  C.c_int),
@@ -352,3 +353,14 @@ def sg_headtail_step(head: "Layout", tail: "Layout", h, P_head, P_tail, W_head, 
         _dev(dW_tail, "dW_tail", _BF16, tail.L * tail.F), _dev(dP_head, "dP_head", (torch.float32,), Dh * E),
         _dev(dP_tail, "dP_tail", (torch.float32,), H * E), _dev(dh, "dh", (torch.float32,), B * E),
         _dev(loss, "loss", (torch.float64,), 1), _stream(h.device)))
+
+
+SG_PLAN_PER_PHASE, SG_PLAN_FUSED_FWDW, SG_PLAN_ONE_KERNEL = 0, 1, 2
+
+
+def sg_step_plan(layout: "Layout", B: int, sgd: bool = False):
+    """(path, forward on tensor cores, dW on tensor cores, dh on tensor cores)
+    of a step of B samples on this layout."""
+    plan = (C.c_int32 * 4)()
+    _check(load().sg_step_plan(layout, int(B), int(bool(sgd)), plan))
+    return int(plan[0]), bool(plan[1]), bool(plan[2]), bool(plan[3])

@@ -39,10 +39,20 @@
  *     threads; sg_last_error is per host thread.
  *
  * Supported range (anything else returns SG_ERR_UNSUPPORTED)
- *   1 <= B <= 256, 1 <= F <= 256, F <= H <= 1024, 1 <= G <= 256, L = K*G
- *   < 2^31.  Tensor-core engine (used when possible): G % 16 == 0 and
- *   F % 16 == 0.  Every other G (including G = 1, per-label fixed fan-in) runs
- *   on the CUDA-core engine.
+ *   1 <= B <= 256, 1 <= F <= 256, F <= H <= 65535 (idx is u16), 1 <= G <=
+ *   256, L = K*G < 2^31.
+ *   Tensor-core engine (used when the shape fits it): G in {16, 32} or a
+ *   multiple of 64, F % 16 == 0, and a group's tiles within one CTA's shared
+ *   memory and TMEM.  All three phases (forward + BCE, dW, dh) run on the
+ *   tensor cores for F % 16 == 0 up to
+ *                      G = 16, 32   G = 64   G = 128   G = 192   G = 256
+ *       B <= 128          256         256       176        48      (dh only)
+ *       B <= 256          192         176       144     (dh only)  (dh only)
+ *   and dh does for every such G and F.  A phase outside that runs on CUDA
+ *   cores (SG_ENGINE_TC makes it an error instead).  Groups of more than 64
+ *   labels enter dh as subgroups of 64 sharing I_k.  Every other G
+ *   (including G = 1, per-label fixed fan-in) runs on the CUDA-core engine.
+ *   sg_step_plan reports which kernels and engines a step will use.
  */
 #ifndef SG_H
 #define SG_H
@@ -123,6 +133,20 @@ SG_API void sg_layout_free(sg_layout *layout);
  * SG_ENGINE_TC on a layout the tensor-core engine cannot run returns
  * SG_ERR_UNSUPPORTED and leaves the engine unchanged. */
 SG_API sg_status sg_layout_set_engine(sg_layout *layout, int32_t engine);
+
+/* The kernels a step (sg_step, or sg_step_sgd when sgd != 0) of B samples
+ * will run on this layout with its current engine: plan[0] is one of
+ * sg_step_path, plan[1..3] are 1 where the forward (+BCE), dW and dh run on
+ * the tensor cores and 0 where they run on CUDA cores.  plan holds 4 int32
+ * (host memory).  Synchronous, launches nothing; SG_ERR_UNSUPPORTED where the
+ * step itself would fail (a layout pinned to the tensor cores outside their
+ * range). */
+typedef enum sg_step_path {
+    SG_PLAN_PER_PHASE = 0,   /* one kernel per phase, dZ through HBM */
+    SG_PLAN_FUSED_FWDW = 1,  /* fused forward + BCE + dW kernel, then dh */
+    SG_PLAN_ONE_KERNEL = 2   /* the whole step in one kernel on CTA clusters */
+} sg_step_path;
+SG_API sg_status sg_step_plan(const sg_layout *layout, int32_t B, int32_t sgd, int32_t *plan);
 
 /* Sizes of a layout (any pointer may be NULL). */
 SG_API sg_status sg_layout_info(const sg_layout *layout, int64_t *L, int32_t *G,

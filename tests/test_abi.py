@@ -53,7 +53,7 @@ def test_layout_build_validates_before_any_cuda_call(lib):
         ((fake, 32, 4, fake, 3, 10, 1, -1), sgpkg.SG_ERR_INVALID),   # max_nnz < 0
         ((None, 32, 4, fake, 3, 10, 1, 0), sgpkg.SG_ERR_INVALID),    # null groups
         ((fake, 512, 512, fake, 3, 10, 1, 0), sgpkg.SG_ERR_UNSUPPORTED),  # G > 256
-        ((fake, 32, 4, fake, 3, 2000, 1, 0), sgpkg.SG_ERR_UNSUPPORTED),   # H too big
+        ((fake, 32, 4, fake, 3, 65536, 1, 0), sgpkg.SG_ERR_UNSUPPORTED),  # H above u16 idx
         ((fake, 32, 4, fake, 3, 10, 300, 0), sgpkg.SG_ERR_UNSUPPORTED),   # max_B
     ]
     for args, want in cases:

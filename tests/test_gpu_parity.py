@@ -42,6 +42,13 @@ CASES = [
     (_w("tc_b37_h320", B=37, H=320, L=16 * 64, G=16, F=128, pos=4), (SIMT, TC)),
     (_w("tc_g128", B=100, H=768, L=128 * 20, G=128, F=128, pos=6, dist="zipf"), (SIMT, TC)),
     (_w("tc_h1000", B=130, H=1000, L=32 * 40, G=32, F=128, pos=6), (SIMT, TC)),
+    # B = 256 at G = 64: dW streams the two sample tiles through its stages
+    (_w("g64_b256", B=256, H=768, L=64 * 30, G=64, F=128, pos=5, dist="zipf"), (SIMT, TC)),
+    # groups of 192 (dh as three subgroups of 64); wide H (eleven dh bands,
+    # and three column windows of the CUDA-core dh)
+    (_w("tc_g192_f48", B=100, H=256, L=192 * 8, G=192, F=48, pos=5), (SIMT, TC)),
+    (_w("tc_h4096", B=64, H=4096, L=32 * 60, G=32, F=64, pos=4), (SIMT, TC)),
+    (_w("simt_h2500_g5", B=40, H=2500, L=5 * 120, G=5, F=40, pos=3), (SIMT,)),
 ]
 
 
@@ -495,3 +502,49 @@ def test_call_argument_errors():
     with pytest.raises(sg.SGError) as e:
         sg.sg_layout_set_engine(build_layout(generate(_w("g3", 4, 30, 30, 3, 5))), TC)
     assert e.value.status == sg.SG_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ engine range
+# largest F (multiple of 16) at which all three phases of a step run on the
+# tensor cores, by batch class and G (the table of include/sg.h)
+_TC_MAX_F = {128: {16: 256, 32: 256, 64: 256, 128: 176, 192: 48, 256: 0},
+             256: {16: 192, 32: 192, 64: 176, 128: 144, 192: 0, 256: 0}}
+
+
+def test_step_plan_matches_documented_range():
+    """sg_step_plan over G in {16, ..., 256}, F in {16, ..., 256} and B from 1
+    to 256: the step runs every phase on the tensor cores exactly where the
+    header's table says, and dh on the tensor cores everywhere."""
+    for B in (1, 100, 128, 129, 256):
+        cls = 128 if B <= 128 else 256
+        for G in (16, 32, 64, 128, 192, 256):
+            for F in range(16, 257, 16):
+                L = G * 4
+                groups = np.arange(L, dtype=np.int32) // G
+                idx = np.tile(np.arange(F, dtype=np.int32), (4, 1))
+                lay = sg.sg_layout_build(dev_i32(groups), L, G, dev_i32(idx.reshape(-1)), F, 256, B, 1)
+                try:
+                    path, f, w, h = sg.sg_step_plan(lay, B)
+                finally:
+                    lay.close()
+                assert h, (B, G, F)
+                assert (f and w and h) == (F <= _TC_MAX_F[cls][G]), (B, G, F, path, f, w, h)
+
+
+@pytest.mark.parametrize("G,F", [(128, 128), (256, 64), (256, 256)])
+def test_dh_stage_large_groups_tc(G, F, oracle_mod):
+    """sg_bwd_dh on the tensor cores for groups of more than 64 labels (run as
+    subgroups of 64 sharing I_k), against the oracle's dh."""
+    w = _w(f"dh_g{G}_f{F}", B=96, H=512, L=G * 12, G=G, F=F, pos=3)
+    p = generate(w)
+    lay = build_layout(p)
+    sg.sg_layout_set_engine(lay, TC)
+    ids = sg.sg_layout_export(lay)[2].cpu().numpy().view(np.uint16)
+    dzbits = draw_bf16_matrix(98, w.B, w.L, 0.5)
+    want_dh = oracle_mod.feature_grad(p.W, dzbits, ids, w.G, w.H)
+    dh = torch.full((w.B, w.H), float("nan"), dtype=torch.float32, device="cuda")
+    sg.sg_bwd_dh(lay, dev_bf16(dzbits), w.B, dev_bf16(p.W), dh)
+    torch.cuda.synchronize()
+    assert_close(dh.cpu().numpy(), want_dh, what="dh")
+    _status_ok(lay)
+    lay.close()
