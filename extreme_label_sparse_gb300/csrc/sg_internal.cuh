@@ -107,6 +107,7 @@ void sg_set_error(const char *fmt, ...);
         if (e_ != cudaSuccess) {                                            \
             sg_set_error("%s failed: %s (%s:%d)", #expr,                    \
                          cudaGetErrorString(e_), __FILE__, __LINE__);       \
+            cudaGetLastError(); /* a later call must not see it again */    \
             return SG_ERR_CUDA;                                             \
         }                                                                   \
     } while (0)

@@ -175,6 +175,9 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
     p.z_bytes = (uint32_t)p.planes * p.nzc * p.MT * 128 * p.zsw;
     p.stage_bytes = p.a_bytes + p.z_bytes;
     p.S = stages_for(p.stage_bytes);
+    // the last f tile's pad sits after the last stage
+    while (p.S > 0 && (long)p.S * p.stage_bytes + p.pad_bytes > (long)kSmemBudget)
+        --p.S;
     if (p.S < 2 && p.MT > 1) {
         // both sample tiles of a group do not fit twice: stream the tiles
         // through the stages, accumulating over them in TMEM
@@ -183,6 +186,8 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
         p.z_bytes = (uint32_t)p.planes * p.nzc * 128 * p.zsw;
         p.stage_bytes = p.a_bytes + p.z_bytes;
         p.S = stages_for(p.stage_bytes);
+        while (p.S > 0 && (long)p.S * p.stage_bytes + p.pad_bytes > (long)kSmemBudget)
+            --p.S;
     }
     if (p.S < 2)
         return p;

@@ -46,7 +46,7 @@
  *   memory and TMEM.  All three phases (forward + BCE, dW, dh) run on the
  *   tensor cores for F % 16 == 0 up to
  *                      G = 16, 32   G = 64   G = 128   G = 192   G = 256
- *       B <= 128          256         256       176        48      (dh only)
+ *       B <= 128          256         256       160        32      (dh only)
  *       B <= 256          192         176       144     (dh only)  (dh only)
  *   and dh does for every such G and F.  A phase outside that runs on CUDA
  *   cores (SG_ENGINE_TC makes it an error instead).  Groups of more than 64

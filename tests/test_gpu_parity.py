@@ -46,7 +46,7 @@ CASES = [
     (_w("g64_b256", B=256, H=768, L=64 * 30, G=64, F=128, pos=5, dist="zipf"), (SIMT, TC)),
     # groups of 192 (dh as three subgroups of 64); wide H (eleven dh bands,
     # and three column windows of the CUDA-core dh)
-    (_w("tc_g192_f48", B=100, H=256, L=192 * 8, G=192, F=48, pos=5), (SIMT, TC)),
+    (_w("tc_g192_f32", B=100, H=256, L=192 * 8, G=192, F=32, pos=5), (SIMT, TC)),
     (_w("tc_h4096", B=64, H=4096, L=32 * 60, G=32, F=64, pos=4), (SIMT, TC)),
     (_w("simt_h2500_g5", B=40, H=2500, L=5 * 120, G=5, F=40, pos=3), (SIMT,)),
 ]
@@ -507,7 +507,7 @@ def test_call_argument_errors():
 # ------------------------------------------------------------------ engine range
 # largest F (multiple of 16) at which all three phases of a step run on the
 # tensor cores, by batch class and G (the table of include/sg.h)
-_TC_MAX_F = {128: {16: 256, 32: 256, 64: 256, 128: 176, 192: 48, 256: 0},
+_TC_MAX_F = {128: {16: 256, 32: 256, 64: 256, 128: 160, 192: 32, 256: 0},
              256: {16: 192, 32: 192, 64: 176, 128: 144, 192: 0, 256: 0}}
 
 
