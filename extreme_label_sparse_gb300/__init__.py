@@ -13,5 +13,7 @@ from .sg import (  # noqa: F401
     sg_pos_export, sg_fwd, sg_bce_grad, sg_fwd_bce, sg_bwd, sg_bwd_dW, sg_bwd_dh,
     sg_step, sg_step_sgd, sg_bce_grad_noalloc, sg_selftest_wait_timeout, sg_proj_fwd, sg_proj_bwd,
     sg_headtail_step, sg_step_plan, SG_PLAN_PER_PHASE, SG_PLAN_FUSED_FWDW, SG_PLAN_ONE_KERNEL,
-    sg_timing_start, sg_timing_stop, last_error, status_string, KIND_NAMES,
+    Grouping, sg_grouping_create, sg_grouping_status, sg_grouping_embed, sg_grouping_set_embeddings,
+    sg_grouping_kmeans_init, sg_grouping_set_centroids, sg_grouping_kmeans_batch, sg_grouping_groups,
+    sg_grouping_export, sg_timing_start, sg_timing_stop, last_error, status_string, KIND_NAMES,
 )

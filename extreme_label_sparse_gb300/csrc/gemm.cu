@@ -177,6 +177,163 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- argmax GEMM
+// For each row m of A (M x K, K-major) the column n of B (N x K, K-major) with
+// the largest <A_m, B_n> (fp32 accumulation; ties to the smaller n).  One CTA
+// per 128-row tile of A walks all 128-column tiles of B: the producer streams
+// (n tile, k block) pairs of A and B tiles, one thread issues the MMAs into two
+// TMEM accumulators used alternately, and each epilogue thread keeps its row's
+// running best over the tiles in registers.
+struct ArgmaxCtl {
+    uint64_t full[kGS], empty[kGS];
+    uint64_t tfull[2], tempty[2], drain;
+    uint32_t tmem;
+    int abort_flag;
+};
+
+struct ArgmaxArgs {
+    int32_t *best_idx;
+    float *best_val;
+    int32_t M, N, K;
+    int32_t *status;
+};
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    k_gemm_argmax(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                  const ArgmaxArgs a)
+{
+    __shared__ ArgmaxCtl c;
+    extern __shared__ uint8_t dsm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+    const int m0 = blockIdx.x * 128;
+    const int nkb = (a.K + 63) / 64;
+    const int ntiles = (a.N + 127) / 128;
+    if (threadIdx.x == 0) {
+        c.abort_flag = 0;
+        for (int s = 0; s < kGS; ++s) {
+            mbar_init(bar_of(c.full[s]), 1);
+            mbar_init(bar_of(c.empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_of(c.tfull[i]), 1);
+            mbar_init(bar_of(c.tempty[i]), 128);
+        }
+        mbar_init(bar_of(c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = c.tmem;
+    volatile int *abort_flag = &c.abort_flag;
+    const int total = ntiles * nkb;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        int it = 0;
+        if (lane == 0) {
+            for (; it < total; ++it) {
+                const int s = it % kGS;
+                if (!mbar_wait(bar_of(c.empty[s]), ((uint32_t)(it / kGS) & 1u) ^ 1u, abort_flag, a.status))
+                    break;
+                const int n = it / nkb, kb = it - n * nkb;
+                const uint32_t st = base + (uint32_t)s * 2 * kTileBytes;
+                mbar_arrive_expect_tx(bar_of(c.full[s]), 2 * kTileBytes);
+                tma_load_2d(st, &tm_a, kb * 64, m0, bar_of(c.full[s]));
+                tma_load_2d(st + kTileBytes, &tm_b, kb * 64, n * 128, bar_of(c.full[s]));
+            }
+            if (*abort_flag)
+                for (int j = it - kGS < 0 ? 0 : it - kGS; j < it; ++j)
+                    mbar_wait_drain(bar_of(c.full[j % kGS]), (uint32_t)(j / kGS) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA
+        const uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+        int it = 0;
+        bool live = true;
+        for (int n = 0; n < ntiles && live; ++n) {
+            const int acc = n & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.tempty[acc]), ((uint32_t)(n >> 1) & 1u) ^ 1u,
+                                                   abort_flag, a.status)))
+                break;
+            tc_fence_after();
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int s = it % kGS;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.full[s]), (uint32_t)(it / kGS) & 1u, abort_flag,
+                                                       a.status))) {
+                    live = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t st = base + (uint32_t)s * 2 * kTileBytes;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tbase + (uint32_t)(acc * 128), tile_desc(st, 0, ks),
+                                 tile_desc(st + kTileBytes, 0, ks), idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(bar_of(c.empty[s]));
+                    if (kb == nkb - 1)
+                        mma_commit(bar_of(c.tfull[acc]));
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0)
+            mma_commit(bar_of(c.drain));
+        __syncwarp();
+        mbar_wait_drain(bar_of(c.drain), 0);
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int m = m0 + q * 32 + lane;
+        float best = -INFINITY;
+        int bidx = -1;
+        bool ok = true;
+        for (int n = 0; n < ntiles; ++n) {
+            const int acc = n & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.tfull[acc]), (uint32_t)(n >> 1) & 1u, abort_flag,
+                                                   a.status))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int cc = 0; cc < 128; cc += 32) {
+                uint32_t r[32];
+                tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 128 + cc), r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const int col = n * 128 + cc + x;
+                    const float v = __uint_as_float(r[x]);
+                    if (col < a.N && v > best) {  // ascending columns: ties keep the smaller
+                        best = v;
+                        bidx = col;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_of(c.tempty[acc]));
+        }
+        if (ok && m < a.M) {
+            a.best_idx[m] = bidx;
+            if (a.best_val)
+                a.best_val[m] = best;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 256);
+    }
+}
+
 // fp32 -> bf16 value plane + residual plane (x - bf16(x), rounded to bf16):
 // the pair carries about 16 significant bits into a bf16 GEMM
 __global__ void k_split_hilo(const float *__restrict__ x, int64_t n, uint16_t *__restrict__ hi,
@@ -259,6 +416,36 @@ sg_status gemm_bf16(const uint16_t *A, int a_mn, int64_t lda, const uint16_t *B,
     SG_TRY_CUDA(cudaFuncSetAttribute(k_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     dim3 grid((unsigned)((N + 127) / 128), (unsigned)((M + 127) / 128));
     k_gemm<<<grid, kGThreads, smem, st>>>(ta, tb, a);
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+sg_status gemm_argmax_bf16(const uint16_t *A, int64_t lda, int M, const uint16_t *B, int64_t ldb, int N, int K,
+                           int32_t *best_idx, float *best_val, int32_t *status, cudaStream_t st)
+{
+    if (M < 1)
+        return SG_OK;
+    if (N < 1 || K < 1) {
+        sg_set_error("argmax GEMM: N and K must be positive (N=%d K=%d)", N, K);
+        return SG_ERR_INVALID;
+    }
+    CUtensorMap ta, tb;
+    sg_status rc = map_2d(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, 64, 128, "A");
+    if (rc != SG_OK)
+        return rc;
+    rc = map_2d(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, 64, 128, "B");
+    if (rc != SG_OK)
+        return rc;
+    ArgmaxArgs a;
+    a.best_idx = best_idx;
+    a.best_val = best_val;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.status = status;
+    const size_t smem = (size_t)kGS * 2 * kTileBytes + 1024;
+    SG_TRY_CUDA(cudaFuncSetAttribute(k_gemm_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    k_gemm_argmax<<<(unsigned)((M + 127) / 128), kGThreads, smem, st>>>(ta, tb, a);
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }

@@ -66,6 +66,16 @@ def load():
             "sg_selftest_wait_timeout": ([C.POINTER(i32)], C.c_int),
             "sg_proj_fwd": ([P, i32, i32, P, i32, P, P], C.c_int),
             "sg_step_plan": ([P, i32, i32, C.POINTER(i32)], C.c_int),
+            "sg_grouping_create": ([i64, i32, i32, i32, C.POINTER(P)], C.c_int),
+            "sg_grouping_free": ([P], None),
+            "sg_grouping_status": ([P, C.POINTER(i32)], C.c_int),
+            "sg_grouping_embed": ([P, P, i32, P, P, i64, C.POINTER(i64), P], C.c_int),
+            "sg_grouping_set_embeddings": ([P, P, P, P], C.c_int),
+            "sg_grouping_kmeans_init": ([P, P, P], C.c_int),
+            "sg_grouping_set_centroids": ([P, P, P, P], C.c_int),
+            "sg_grouping_kmeans_batch": ([P, P, i32, P, P], C.c_int),
+            "sg_grouping_groups": ([P, P, P, P], C.c_int),
+            "sg_grouping_export": ([P, P, P, P, P, P], C.c_int),
             "sg_proj_bwd": ([P, i32, i32, P, i32, P, P, P, P, i32, P], C.c_int),
             "sg_headtail_step": ([P, P, P, i32, i32, P, P, P, P, P, i64, P, P, P, i64, P, P, P, P, P, P, P],
                                  C.c_int),
@@ -364,3 +374,91 @@ def sg_step_plan(layout: "Layout", B: int, sgd: bool = False):
     plan = (C.c_int32 * 4)()
     _check(load().sg_step_plan(layout, int(B), int(bool(sgd)), plan))
     return int(plan[0]), bool(plan[1]), bool(plan[2]), bool(plan[3])
+
+
+# ---------------------------------------------------------------- semantic grouping
+class Grouping:
+    """Owner of an sg_grouping handle (freed on close / garbage collection)."""
+
+    def __init__(self, handle, L, D, G, C, device):
+        self.handle = handle
+        self.L, self.D, self.G, self.C = int(L), int(D), int(G), int(C)
+        self.device = device
+
+    def close(self):
+        if self.handle is not None and _lib is not None:
+            _lib.sg_grouping_free(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def _as_parameter_(self):
+        if self.handle is None:
+            raise ValueError("grouping is closed")
+        return self.handle
+
+
+def sg_grouping_create(L: int, D: int, G: int, n_clusters: int, device=None) -> Grouping:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        out = C.c_void_p()
+        _check(load().sg_grouping_create(int(L), int(D), int(G), int(n_clusters), C.byref(out)))
+    return Grouping(out, L, D, G, n_clusters, dev)
+
+
+def sg_grouping_status(g: Grouping) -> int:
+    code = C.c_int32(0)
+    _check(load().sg_grouping_status(g, C.byref(code)))
+    return int(code.value)
+
+
+def sg_grouping_embed(g: Grouping, h, rowptr, labels, nnz: int) -> int:
+    N = h.shape[0]
+    n = C.c_int64(0)
+    lb = _dev(labels, "labels", _I32) if nnz else C.c_void_p(0)
+    _check(load().sg_grouping_embed(g, _dev(h, "h", _BF16, N * g.D), N, _dev(rowptr, "rowptr", _I32, N + 1), lb,
+                                    int(nnz), C.byref(n), _stream(h.device)))
+    return int(n.value)
+
+
+def sg_grouping_set_embeddings(g: Grouping, E, has):
+    _check(load().sg_grouping_set_embeddings(g, _dev(E, "E", _BF16, g.L * g.D), _dev(has, "has", (torch.uint8,), g.L),
+                                             _stream(E.device)))
+
+
+def sg_grouping_kmeans_init(g: Grouping, init_labels):
+    _check(load().sg_grouping_kmeans_init(g, _dev(init_labels, "init_labels", _I32, g.C),
+                                          _stream(init_labels.device)))
+
+
+def sg_grouping_set_centroids(g: Grouping, centroids, counts=None):
+    cp = _dev(counts, "counts", (torch.int64,), g.C) if counts is not None else C.c_void_p(0)
+    _check(load().sg_grouping_set_centroids(g, _dev(centroids, "centroids", (torch.float32,), g.C * g.D), cp,
+                                            _stream(centroids.device)))
+
+
+def sg_grouping_kmeans_batch(g: Grouping, batch, assign_out=None):
+    M = batch.numel()
+    ap = _dev(assign_out, "assign_out", _I32, M) if assign_out is not None else C.c_void_p(0)
+    _check(load().sg_grouping_kmeans_batch(g, _dev(batch, "batch", _I32, M), M, ap, _stream(batch.device)))
+
+
+def sg_grouping_groups(g: Grouping, groups, cluster_out=None):
+    cp = _dev(cluster_out, "cluster_out", _I32, g.L) if cluster_out is not None else C.c_void_p(0)
+    _check(load().sg_grouping_groups(g, _dev(groups, "groups", _I32, g.L), cp, _stream(groups.device)))
+
+
+def sg_grouping_export(g: Grouping, E=None, has=None, centroids=None, counts=None):
+    dev = g.device
+
+    def ptr(t, name, dt, n):
+        return _dev(t, name, dt, n) if t is not None else C.c_void_p(0)
+
+    _check(load().sg_grouping_export(g, ptr(E, "E", _BF16, g.L * g.D), ptr(has, "has", (torch.uint8,), g.L),
+                                     ptr(centroids, "centroids", (torch.float32,), g.C * g.D),
+                                     ptr(counts, "counts", (torch.int64,), g.C), _stream(dev)))

@@ -279,6 +279,77 @@ SG_API sg_status sg_headtail_step(sg_layout *head, sg_layout *tail, const sg_bf1
                                   int64_t tail_nnz, sg_bf16 *dW_head, sg_bf16 *dW_tail, float *dP_head,
                                   float *dP_tail, float *dh, double *loss, void *stream);
 
+/* ---------------------------------------------------------------- semantic grouping
+ * Grouping of the labels before training (HASTE, key design "group-shared
+ * fixed fan-in sparsity": group members close in embedding space, label
+ * embeddings from the encoder outputs of each label's positives, two stages:
+ * mini-batch spherical k-means into about L / (beta G) coarse clusters, then
+ * greedy groups of a seed and its G - 1 nearest remaining neighbours inside
+ * each cluster).  The groups[] it writes feed sg_layout_build.
+ *   * e_l = bf16(Normalize(sum of h_i over the distinct samples i with l
+ *     positive)); labels without a positive (or with a zero sum) have no
+ *     embedding and are grouped last.
+ *   * Similarity = dot product of bf16 vectors; centroids are kept in fp32
+ *     and rounded to bf16 for scoring (tcgen05 argmax GEMM).
+ *   * A k-means batch is assigned with the centroids of its start (ties to the
+ *     smaller centroid); then mu_c <- Normalize((n_c mu_c + S_c) / (n_c + m_c))
+ *     (per-centre learning rate 1/n_c), n_c += m_c.
+ *   * Greedy: clusters in index order; seed = the remaining member most
+ *     similar to the centroid; its group = the seed and the G - 1 remaining
+ *     members most similar to it (ties to the smaller label id); groups are
+ *     numbered as formed.  What a cluster leaves over (in cluster order,
+ *     ascending id), then the labels without embedding (ascending id), are cut
+ *     into consecutive groups of G, numbered after the greedy ones.
+ * Sums accumulate in 64-bit fixed point, so results do not depend on the
+ * order of atomics.  The handle owns its device memory (about
+ * L * (16 + 2 D) + C * 14 D bytes after embedding); calls on one handle must
+ * not overlap.  Data errors (a malformed row, a label outside [0, L), |h| >=
+ * 2^14, a k-means label without embedding) set the handle's status word,
+ * read and cleared with sg_grouping_status.                                 */
+typedef struct sg_grouping sg_grouping;
+
+/* L labels (L % G == 0), embeddings of D features (D % 16 == 0, <= 4096),
+ * C clusters (1 <= C <= L).  The current device is the handle's. */
+SG_API sg_status sg_grouping_create(int64_t L, int32_t D, int32_t G, int32_t C, sg_grouping **out);
+SG_API void sg_grouping_free(sg_grouping *g);
+SG_API sg_status sg_grouping_status(sg_grouping *g, int32_t *code);
+
+/* Embeddings from N samples h[N][D] (bf16, row-major) and their positive
+ * labels (CSR: rowptr[N+1], labels[nnz], device).  N <= 2^22.  Synchronous;
+ * *n_embedded (host, may be NULL) = labels that got an embedding. */
+SG_API sg_status sg_grouping_embed(sg_grouping *g, const sg_bf16 *h, int32_t N, const int32_t *rowptr,
+                                   const int32_t *labels, int64_t nnz, int64_t *n_embedded, void *stream);
+
+/* Embeddings given directly: E[L][D] bf16 and has[L] (0/1), device.
+ * Synchronous. */
+SG_API sg_status sg_grouping_set_embeddings(sg_grouping *g, const sg_bf16 *E, const uint8_t *has, void *stream);
+
+/* Centroid c = Normalize(e of init_labels[c]) (device int32[C]; each label
+ * must have an embedding), counts 0. */
+SG_API sg_status sg_grouping_kmeans_init(sg_grouping *g, const int32_t *init_labels, void *stream);
+
+/* Centroids given directly: centroids[C][D] fp32 (unit rows), counts[C]
+ * int64 (NULL: zeros), device.  Synchronous. */
+SG_API sg_status sg_grouping_set_centroids(sg_grouping *g, const float *centroids, const int64_t *counts,
+                                           void *stream);
+
+/* One k-means batch of M label ids (device int32[M], each with an
+ * embedding, M <= 2^22); assign_out (device int32[M], may be NULL) receives
+ * the batch's assignment. */
+SG_API sg_status sg_grouping_kmeans_batch(sg_grouping *g, const int32_t *batch, int32_t M, int32_t *assign_out,
+                                          void *stream);
+
+/* Final assignment of every label with an embedding to its nearest centroid,
+ * then the greedy stage and the pool: groups[L] (device int32, ids in
+ * [0, L / G)); cluster_out[L] (device int32, may be NULL): the cluster of
+ * each label, -1 without embedding. */
+SG_API sg_status sg_grouping_groups(sg_grouping *g, int32_t *groups, int32_t *cluster_out, void *stream);
+
+/* Copy out (device outputs, each may be NULL): E[L][D] and has[L] (has only
+ * with E), centroids[C][D], counts[C].  Synchronous. */
+SG_API sg_status sg_grouping_export(sg_grouping *g, sg_bf16 *E, uint8_t *has, float *centroids, int64_t *counts,
+                                    void *stream);
+
 /* ---------------------------------------------------------------- timing
  * Per-kernel device timing for benchmarks: while enabled, every kernel the
  * library launches for this layout is bracketed by a pair of CUDA events

@@ -95,9 +95,17 @@ def kmeans_batch(E, centroids, counts, batch):
     """One mini-batch of spherical k-means.  E [L, D], centroids [C, D]
     (float64, unit rows), counts [C] int64, batch: label ids in batch order.
     Returns (new centroids, new counts, the batch's assignment)."""
+    a = assign(E[batch], np.asarray(centroids, dtype=np.float64))
+    mu, n = kmeans_update(E, centroids, counts, batch, a)
+    return mu, n, a
+
+
+def kmeans_update(E, centroids, counts, batch, a):
+    """The update half of a batch, given its assignment a: each member in
+    batch order moves its centroid by (e - mu) / n_c, then every moved
+    centroid is normalised.  Returns (centroids, counts)."""
     mu = np.array(centroids, dtype=np.float64, copy=True)
     n = np.array(counts, dtype=np.int64, copy=True)
-    a = assign(E[batch], mu)
     moved = set()
     for l, c in zip(batch, a):
         n[c] += 1
@@ -107,7 +115,7 @@ def kmeans_batch(E, centroids, counts, batch):
         nrm = np.sqrt(np.dot(mu[c], mu[c]))
         if nrm > 0:
             mu[c] /= nrm
-    return mu, n, a
+    return mu, n
 
 
 def kmeans(E, init_labels, batches):
