@@ -16,7 +16,8 @@ time against both peaks; `workloads` = step time, per-kernel split and step
 roofline of the other label-space workloads and of the group-size sweep
 (G = 1, 16, 32, 64 with uniform and clustered index sets);
 `headtail` = the head-tail split's whole step (projections, dense head,
-sparse tail) on the same tail with a 3% dense head;
+sparse tail) on the same tail with a 3% dense head; `grouping` = the semantic
+grouping of the same L labels (embeddings, mini-batch k-means, greedy groups);
 `cpu_baseline` = the CPU oracle on a bounded sample of the same workload.
 `--impl reference` times that oracle alone (there is no other implementation
 of the method to run).
@@ -406,6 +407,64 @@ def measure_headtail(sg, torch, dev, p, steps, warmup, stream, hbm, tflops):
                               "frac_tensor": flops / s / 1e12 / tflops}}
 
 
+GROUPING_SAMPLES, GROUPING_BETA, GROUPING_BATCHES, GROUPING_BATCH = 8192, 4, 10, 65536
+
+
+def measure_grouping(sg, torch, dev, w, tflops):
+    """Semantic grouping of the workload's L labels from GROUPING_SAMPLES
+    samples (h ~ N(0, 1) bf16 of H features, w.pos positives each, drawn like
+    the workload's): embeddings, k-means into C = (labels with an embedding)
+    / (beta G) clusters over GROUPING_BATCHES batches, final assignment and
+    greedy groups.  Host-timed around each call (they synchronise)."""
+    from workloads import draw_bf16_matrix, draw_positives
+    N, D, L, G = GROUPING_SAMPLES, w.H, w.L, w.G
+    rowptr, labels = draw_positives(21, N, L, w.pos, w.pos_dist, w.zipf_s)
+    hbits = draw_bf16_matrix(22, N, D, 1.0)
+    active = np.unique(labels)
+    C = max(1, int(round(len(active) / (GROUPING_BETA * G))))
+    rng = np.random.default_rng(23)
+    init = rng.choice(active, C, replace=False).astype(np.int32)
+    M = min(GROUPING_BATCH, len(active))
+    batches = [rng.choice(active, M, replace=False).astype(np.int32) for _ in range(GROUPING_BATCHES)]
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    h_d = torch.from_numpy(hbits.view(np.int16)).to(dev)
+    rp_d, lb_d, init_d = i32(rowptr), i32(labels), i32(init)
+    b_d = [i32(b) for b in batches]
+    groups = torch.empty(L, dtype=torch.int32, device=dev)
+    g = sg.sg_grouping_create(L, D, G, C, dev)
+    try:
+        def run():
+            t = [time.perf_counter()]
+            n = sg.sg_grouping_embed(g, h_d, rp_d, lb_d, len(labels))
+            torch.cuda.synchronize()
+            t.append(time.perf_counter())
+            sg.sg_grouping_kmeans_init(g, init_d)
+            for b in b_d:
+                sg.sg_grouping_kmeans_batch(g, b)
+            torch.cuda.synchronize()
+            t.append(time.perf_counter())
+            sg.sg_grouping_groups(g, groups)
+            torch.cuda.synchronize()
+            t.append(time.perf_counter())
+            return n, [1e3 * (b - a) for a, b in zip(t, t[1:])]
+
+        run()  # warm-up (allocation of the compact arrays, module load)
+        n, ms = run()
+        st = sg.sg_grouping_status(g)
+    finally:
+        g.close()
+    sizes = np.bincount(groups.cpu().numpy(), minlength=L // G)
+    gemm_flops = 2.0 * D * C * (GROUPING_BATCHES * M + n)  # batch assignments + the final one
+    return {"config": {"L": L, "G": G, "D": D, "samples": N, "positives_per_sample": w.pos, "beta": GROUPING_BETA,
+                       "clusters": C, "labels_with_embedding": n, "batches": GROUPING_BATCHES, "batch": M},
+            "ms": {"embed": ms[0], "kmeans": ms[1], "groups": ms[2], "total": sum(ms)},
+            "argmax_gemm_flops": gemm_flops, "status": st,
+            "groups_all_of_size_G": bool(np.all(sizes == G))}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -533,9 +592,10 @@ def run_ours(args):
     launches = sum(v[1] for v in kinds.values())
     r.close()
     del r
-    headtail = None
+    headtail = grouping = None
     if rank == 0 and world == 1 and not args.labels and not args.no_others and not args.sgd:
         headtail = measure_headtail(sg, torch, dev, p, args.other_steps, 2, stream, hbm, tflops)
+        grouping = measure_grouping(sg, torch, dev, w, tflops)
 
     workloads = {}
     for name, fut in futures:
@@ -567,6 +627,8 @@ def run_ours(args):
         line["workloads"] = workloads
     if headtail is not None:
         line["headtail"] = headtail
+    if grouping is not None:
+        line["grouping"] = grouping
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

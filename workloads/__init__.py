@@ -30,7 +30,7 @@ from typing import Optional
 import numpy as np
 
 __all__ = ["Workload", "CONFIGS", "Problem", "generate", "to_bf16_bits",
-           "bf16_bits_to_f32", "sweep_config"]
+           "bf16_bits_to_f32", "sweep_config", "draw_bf16_matrix", "draw_positives"]
 
 
 @dataclass(frozen=True)
@@ -224,3 +224,10 @@ def generate(w: Workload, *, B: Optional[int] = None, shard: int = 0) -> Problem
 def draw_bf16_matrix(seed: int, rows: int, cols: int, scale: float) -> np.ndarray:
     """Stand-alone N(0, scale^2) bf16 matrix (stage inputs such as Z or dZ)."""
     return _draw_normal_bf16(_rng(np.random.SeedSequence(seed)), rows, cols, scale)
+
+
+def draw_positives(seed: int, B: int, L: int, n: int, dist: str = "zipf", s: float = 1.1):
+    """Stand-alone positive lists: B rows of n distinct labels in [0, L)
+    ("zipf": rank r with P ~ r^-s, label r - 1; "uniform").  -> (rowptr, labels)."""
+    return _draw_positives(_rng(np.random.SeedSequence(seed)), B, L, n, dist, s)
+
