@@ -15,5 +15,5 @@ from .sg import (  # noqa: F401
     sg_headtail_step, sg_step_plan, SG_PLAN_PER_PHASE, SG_PLAN_FUSED_FWDW, SG_PLAN_ONE_KERNEL,
     Grouping, sg_grouping_create, sg_grouping_status, sg_grouping_embed, sg_grouping_set_embeddings,
     sg_grouping_kmeans_init, sg_grouping_set_centroids, sg_grouping_kmeans_batch, sg_grouping_groups,
-    sg_grouping_export, sg_timing_start, sg_timing_stop, last_error, status_string, KIND_NAMES,
+    sg_grouping_export, sg_rewire, sg_timing_start, sg_timing_stop, last_error, status_string, KIND_NAMES,
 )

@@ -116,7 +116,7 @@ void free_layout(sg_layout *lo)
     void *bufs[] = {lo->slot_of_label, lo->label_of_slot, lo->idx_s, lo->hT,
                     lo->gcount, lo->gptr, lo->gent, lo->tsorted, lo->tslots,
                     lo->rowcnt, lo->loss_part, lo->status, lo->dZ_ws, lo->scan_part, lo->wmax,
-                    lo->ht_ws};
+                    lo->ht_ws, lo->rw_ws};
     for (void *p : bufs)
         if (p)
             cudaFree(p);

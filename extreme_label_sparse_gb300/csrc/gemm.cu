@@ -177,6 +177,151 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- group |.|-sum GEMM
+// out[m / G][n] = sum over the G rows m of a group of |sum_k A[m][k] B[n][k]|
+// (A and B MN-major, G a power of two <= 128, so a 128-row tile holds whole
+// groups).  The same tile loop as k_gemm; the epilogue reduces |acc| over
+// the group's TMEM lanes with shuffles (G <= 32) or across the four epilogue
+// warps through shared memory (G = 64, 128).
+__global__ void __launch_bounds__(kGThreads, 1)
+    k_gemm_gabs(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, float *out,
+                int32_t M, int32_t N, int32_t K, int32_t G, int32_t *status)
+{
+    __shared__ GemmCtl c;
+    __shared__ float part[4][32];
+    extern __shared__ uint8_t dsm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+    const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+    const int nkb = (K + 63) / 64;
+    if (threadIdx.x == 0) {
+        c.abort_flag = 0;
+        for (int s = 0; s < kGS; ++s) {
+            mbar_init(bar_of(c.full[s]), 1);
+            mbar_init(bar_of(c.empty[s]), 1);
+        }
+        mbar_init(bar_of(c.tfull), 1);
+        mbar_init(bar_of(c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem), 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = c.tmem;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp == 0) {
+        int kb = 0;
+        if (lane == 0) {
+            for (; kb < nkb; ++kb) {
+                const int s = kb % kGS;
+                if (!mbar_wait(bar_of(c.empty[s]), ((uint32_t)(kb / kGS) & 1u) ^ 1u, abort_flag, status))
+                    break;
+                const uint32_t st = base + (uint32_t)s * 2 * kTileBytes;
+                mbar_arrive_expect_tx(bar_of(c.full[s]), 2 * kTileBytes);
+                load_tile(st, &tm_a, 1, m0, kb * 64, bar_of(c.full[s]));
+                load_tile(st + kTileBytes, &tm_b, 1, n0, kb * 64, bar_of(c.full[s]));
+            }
+            if (*abort_flag)
+                for (int j = kb - kGS < 0 ? 0 : kb - kGS; j < kb; ++j)
+                    mbar_wait_drain(bar_of(c.full[j % kGS]), (uint32_t)(j / kGS) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        const uint32_t idesc = idesc_bf16(128, 128, 1, 1);
+        int kb = 0;
+        for (; kb < nkb; ++kb) {
+            const int s = kb % kGS;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.full[s]), (uint32_t)(kb / kGS) & 1u, abort_flag,
+                                                   status)))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t st = base + (uint32_t)s * 2 * kTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tbase, tile_desc(st, 1, ks), tile_desc(st + kTileBytes, 1, ks), idesc,
+                             (kb > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(bar_of(c.empty[s]));
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            if (kb == nkb)
+                mma_commit(bar_of(c.tfull));
+            mma_commit(bar_of(c.drain));
+        }
+        __syncwarp();
+        mbar_wait_drain(bar_of(c.drain), 0);
+    } else {
+        const int q = warp & 3;
+        const int m = m0 + q * 32 + lane;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_of(c.tfull), 0, abort_flag, status));
+        if (ok)
+            tc_fence_after();
+        for (int cc = 0; cc < 128; cc += 32) {
+            float v[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+                v[x] = 0.f;
+            if (ok) {
+                uint32_t r[32];
+                tmem_ld32(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)cc, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int x = 0; x < 32; ++x)
+                    v[x] = fabsf(__uint_as_float(r[x]));
+            }
+            const int gl = G < 32 ? G : 32;  // lanes of a group inside the warp
+            for (int off = 1; off < gl; off <<= 1) {
+#pragma unroll
+                for (int x = 0; x < 32; ++x)
+                    v[x] += __shfl_xor_sync(0xffffffffu, v[x], off);
+            }
+            if (G <= 32) {
+                // lane i of a group writes the columns x = i (mod G)
+                const int64_t k = m / G;
+                if (ok && m < M) {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        const int n = n0 + cc + x;
+                        if ((x & (G - 1)) == (lane & (G - 1)) && n < N)
+                            out[k * N + n] = v[x];
+                    }
+                }
+            } else {
+                // warp sums to shared memory, then the first warp of each
+                // group adds the group's warps (named barrier of the four)
+#pragma unroll
+                for (int x = 0; x < 32; ++x)
+                    if (x == lane)
+                        part[q][x] = v[x];
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                const int wpg = G / 32;  // warps per group
+                if (ok && q % wpg == 0 && m0 + q * 32 < M) {
+                    float sum = 0.f;
+                    for (int w2 = q; w2 < q + wpg; ++w2)
+                        sum += part[w2][lane];
+                    const int n = n0 + cc + lane;
+                    if (n < N)
+                        out[(int64_t)((m0 + q * 32) / G) * N + n] = sum;
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 128);
+    }
+}
+
 // ---------------------------------------------------------------- argmax GEMM
 // For each row m of A (M x K, K-major) the column n of B (N x K, K-major) with
 // the largest <A_m, B_n> (fp32 accumulation; ties to the smaller n).  One CTA
@@ -446,6 +591,30 @@ sg_status gemm_argmax_bf16(const uint16_t *A, int64_t lda, int M, const uint16_t
     const size_t smem = (size_t)kGS * 2 * kTileBytes + 1024;
     SG_TRY_CUDA(cudaFuncSetAttribute(k_gemm_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     k_gemm_argmax<<<(unsigned)((M + 127) / 128), kGThreads, smem, st>>>(ta, tb, a);
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+sg_status gemm_group_abs(const uint16_t *A, int64_t lda, int M, const uint16_t *B, int64_t ldb, int N, int K, int G,
+                         float *out, int32_t *status, cudaStream_t st)
+{
+    if (M < 1 || N < 1 || K < 1)
+        return SG_OK;
+    if (G < 1 || G > 128 || (G & (G - 1)) != 0 || M % G != 0) {
+        sg_set_error("group |.|-sum GEMM: G must be a power of two <= 128 dividing M (G=%d M=%d)", G, M);
+        return SG_ERR_UNSUPPORTED;
+    }
+    CUtensorMap ta, tb;
+    sg_status rc = map_2d(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, 64, 64, "A");
+    if (rc != SG_OK)
+        return rc;
+    rc = map_2d(&tb, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, 64, "B");
+    if (rc != SG_OK)
+        return rc;
+    const size_t smem = (size_t)kGS * 2 * kTileBytes + 1024;
+    SG_TRY_CUDA(cudaFuncSetAttribute(k_gemm_gabs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    dim3 grid((unsigned)((N + 127) / 128), (unsigned)((M + 127) / 128));
+    k_gemm_gabs<<<grid, kGThreads, smem, st>>>(ta, tb, out, M, N, K, G, status);
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }

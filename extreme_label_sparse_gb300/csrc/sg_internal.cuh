@@ -52,6 +52,9 @@ struct sg_layout {
     // first use): projected activations, both branches' dh, bf16 planes
     void *ht_ws = nullptr;
     size_t ht_ws_bytes = 0;
+    // grow scores of sg_rewire ([K][H] fp32, allocated on first use)
+    float *rw_ws = nullptr;
+    size_t rw_ws_bytes = 0;
 
     // resident clusters of the fused step kernel for the shape keyed by
     // step_ncl_key (0 until the first call)

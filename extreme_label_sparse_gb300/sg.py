@@ -66,6 +66,7 @@ def load():
             "sg_selftest_wait_timeout": ([C.POINTER(i32)], C.c_int),
             "sg_proj_fwd": ([P, i32, i32, P, i32, P, P], C.c_int),
             "sg_step_plan": ([P, i32, i32, C.POINTER(i32)], C.c_int),
+            "sg_rewire": ([P, P, i32, P, P, i32, P, P, P], C.c_int),
             "sg_grouping_create": ([i64, i32, i32, i32, C.POINTER(P)], C.c_int),
             "sg_grouping_free": ([P], None),
             "sg_grouping_status": ([P, C.POINTER(i32)], C.c_int),
@@ -462,3 +463,13 @@ def sg_grouping_export(g: Grouping, E=None, has=None, centroids=None, counts=Non
     _check(load().sg_grouping_export(g, ptr(E, "E", _BF16, g.L * g.D), ptr(has, "has", (torch.uint8,), g.L),
                                      ptr(centroids, "centroids", (torch.float32,), g.C * g.D),
                                      ptr(counts, "counts", (torch.int64,), g.C), _stream(dev)))
+
+
+# ---------------------------------------------------------------- rewiring
+def sg_rewire(layout: Layout, h, dZ, W, n_drop: int, idx_out, W_out):
+    """One RigL-style re-selection of every group's fan-in set (see sg.h)."""
+    B = h.shape[0]
+    _check(load().sg_rewire(layout, _dev(h, "h", _BF16, B * layout.H), B, _dev(dZ, "dZ", _BF16, B * layout.L),
+                            _dev(W, "W", _BF16, layout.L * layout.F), int(n_drop),
+                            _dev(idx_out, "idx_out", _I32, layout.K * layout.F),
+                            _dev(W_out, "W_out", _BF16, layout.L * layout.F), _stream(h.device)))

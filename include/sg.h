@@ -279,6 +279,30 @@ SG_API sg_status sg_headtail_step(sg_layout *head, sg_layout *tail, const sg_bf1
                                   int64_t tail_nnz, sg_bf16 *dW_head, sg_bf16 *dW_tail, float *dP_head,
                                   float *dP_tail, float *dh, double *loss, void *stream);
 
+/* ---------------------------------------------------------------- rewiring
+ * sg_rewire -- one discrete phase of the training (HASTE, "Method / overall
+ * framework" and "Loss and training strategy": each group's fan-in set is
+ * re-selected periodically by the RigL protocol, |I_k| = F).  The pages do not
+ * give the rule; this is the RigL reading for group-shared fan-in:
+ *   prune score of an active index f of group k: sum over the group's labels
+ *     of |W[l][f]|;  grow score of a feature j: sum over the group's labels of
+ *     |sum_b dZ[b][l] h[b][j]| (the dense gradient a weight at (l, j) would get);
+ *   per group, drop the n_drop smallest prune scores and grow the n_drop
+ *   largest grow scores among the features outside the old I_k (ties: the
+ *   smaller feature index first); kept columns keep their weights, grown ones
+ *   start at zero; the new I_k is sorted ascending.
+ *   h[B][H] bf16 (the samples the gradient is taken on), dZ[B][L] bf16 in
+ *   slot order (e.g. from sg_fwd_bce), W[L][F] in slot order (columns follow
+ *   the layout's sorted I_k).  Outputs: idx_out[K][F] int32 (sorted rows; pass
+ *   it with the same groups to sg_layout_build for the next phase) and
+ *   W_out[L][F] bf16 (columns follow idx_out), which must not overlap W.
+ * Needs G a power of two <= 128, F <= 256, L and H multiples of 8, 0 <=
+ * n_drop <= min(F, H - F).  The grow scores are one tcgen05 GEMM (dZ^T h with
+ * the group |.|-sum in its epilogue) into K*H floats of scratch the layout
+ * keeps (allocated on first use).  Asynchronous on `stream`.               */
+SG_API sg_status sg_rewire(sg_layout *layout, const sg_bf16 *h, int32_t B, const sg_bf16 *dZ, const sg_bf16 *W,
+                           int32_t n_drop, int32_t *idx_out, sg_bf16 *W_out, void *stream);
+
 /* ---------------------------------------------------------------- semantic grouping
  * Grouping of the labels before training (HASTE, key design "group-shared
  * fixed fan-in sparsity": group members close in embedding space, label
