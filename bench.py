@@ -18,6 +18,7 @@ roofline of the other label-space workloads and of the group-size sweep
 `headtail` = the head-tail split's whole step (projections, dense head,
 sparse tail) on the same tail with a 3% dense head; `grouping` = the semantic
 grouping of the same L labels (embeddings, mini-batch k-means, greedy groups);
+`rewire` = one re-selection of every group's fan-in set on the same layout;
 `cpu_baseline` = the CPU oracle on a bounded sample of the same workload.
 `--impl reference` times that oracle alone (there is no other implementation
 of the method to run).
@@ -465,6 +466,41 @@ def measure_grouping(sg, torch, dev, w, tflops):
             "groups_all_of_size_G": bool(np.all(sizes == G))}
 
 
+def measure_rewire(sg, torch, dev, p, steps, stream, hbm, tflops):
+    """One rewiring phase (sg_rewire, n_drop = F / 8) on the workload's
+    layout, with dZ = sigmoid(Z) - Y of its batch (sg_fwd_bce).  CUDA events
+    around `steps` calls."""
+    w = p.w
+    r = Runner(sg, torch, dev, p, sg.SG_ENGINE_AUTO)
+    try:
+        dZ = torch.empty((w.B, w.L), dtype=torch.int16, device=dev)
+        loss = torch.zeros(1, dtype=torch.float64, device=dev)
+        sg.sg_fwd_bce(r.lay, r.h, r.W, r.rowptr, r.labels, p.nnz, dZ, loss)
+        idx_out = torch.empty((w.K, w.F), dtype=torch.int32, device=dev)
+        W_out = torch.empty((w.L, w.F), dtype=torch.int16, device=dev)
+        nd = w.F // 8
+        for _ in range(2):
+            sg.sg_rewire(r.lay, r.h, dZ, r.W, nd, idx_out, W_out)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            sg.sg_rewire(r.lay, r.h, dZ, r.W, nd, idx_out, W_out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        st = r.status()
+    finally:
+        r.close()
+    # dZ, W read, W_out written, idx read and written, the K x H scores written and read
+    bytes_ = w.B * w.L * 2 + 2 * w.L * w.F * 2 + w.K * w.F * (2 + 4) + 2 * w.K * w.H * 4 + w.B * w.H * 2
+    flops = 2.0 * w.L * w.H * w.B  # the grow-score GEMM dZ^T h
+    s = ms * 1e-3
+    return {"ms": ms, "n_drop": nd, "status": st, "bytes": bytes_, "flops": flops,
+            "achieved_gbs": bytes_ / s / 1e9, "frac_hbm": bytes_ / s / 1e9 / hbm,
+            "achieved_tflops": flops / s / 1e12, "frac_tensor": flops / s / 1e12 / tflops}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -592,10 +628,11 @@ def run_ours(args):
     launches = sum(v[1] for v in kinds.values())
     r.close()
     del r
-    headtail = grouping = None
+    headtail = grouping = rewire = None
     if rank == 0 and world == 1 and not args.labels and not args.no_others and not args.sgd:
         headtail = measure_headtail(sg, torch, dev, p, args.other_steps, 2, stream, hbm, tflops)
         grouping = measure_grouping(sg, torch, dev, w, tflops)
+        rewire = measure_rewire(sg, torch, dev, p, args.other_steps, stream, hbm, tflops)
 
     workloads = {}
     for name, fut in futures:
@@ -629,6 +666,8 @@ def run_ours(args):
         line["headtail"] = headtail
     if grouping is not None:
         line["grouping"] = grouping
+    if rewire is not None:
+        line["rewire"] = rewire
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
