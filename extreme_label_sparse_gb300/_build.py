@@ -12,7 +12,7 @@ CSRC = PKG / "csrc"
 INCLUDE = PKG.parent / "include"
 BUILD_DIR = PKG / "_build"
 LIB = PKG / "libsg.so"
-SOURCES = ["api.cu", "layout.cu", "pos.cu", "simt.cu", "tc.cu", "step.cu", "noalloc.cu", "selftest.cu", "gemm.cu", "headtail.cu", "grouping.cu", "rewire.cu"]
+SOURCES = ["api.cu", "layout.cu", "pos.cu", "simt.cu", "tc.cu", "step.cu", "noalloc.cu", "selftest.cu", "gemm.cu", "headtail.cu", "grouping.cu", "rewire.cu", "g1.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]

@@ -1,0 +1,420 @@
+// Per-label fixed fan-in (G = 1) on CUDA cores: the comparator the group-shared
+// layer is measured against (HASTE, "Key findings": the per-label form has no
+// shared feature tile, so every label is a thin dot product of F gathered
+// features).  Each kernel keeps what it reuses in shared memory and streams the
+// labels past it:
+//   forward: a 64-sample tile of h^T (every feature, two samples per 32-bit
+//            word) stays in shared memory; a warp takes one label at a time,
+//            lane l computing the logits of samples 2l and 2l + 1 from the
+//            label's F (index, weight) pairs; the BCE follows in registers and
+//            dZ leaves through a shared-memory staging tile in 128-byte rows.
+//   dW:      per 64-label chunk and 64-sample tile, the h^T tile and the dZ
+//            tile in shared memory; a warp owns 8 labels, lane l the features
+//            f = l + 32 q, accumulating over every sample tile in registers.
+//   dh:      each thread owns one sample and its own row of a shared-memory
+//            dh partial (no atomics per product); a CTA streams a contiguous
+//            range of labels and adds its partial to dh once.
+#include "sg_internal.cuh"
+
+namespace {
+
+constexpr int kG1T = 256;  // threads (8 warps)
+constexpr int kSB = 64;    // samples per tile
+constexpr int kLC = 64;    // labels per staged round / dW chunk
+
+__device__ __forceinline__ float lo_bf(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ double g1_block_sum(double v)
+{
+    __shared__ double red[kG1T / 32];
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_down_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    double s = 0.0;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kG1T / 32; ++w)
+            s += red[w];
+    return s;
+}
+
+struct G1Fwd {
+    const uint16_t *hT, *W, *idx_s;
+    uint16_t *Z, *dZ, *dZ_lo;
+    const int32_t *gptr, *gent;
+    double *loss_part;
+    int64_t L, lchunk;
+    int32_t B, ldB, F, H, ntile;
+};
+
+// CTA: sample tile blockIdx % ntile, labels [chunk * lchunk, +lchunk)
+template <bool BCE>
+__global__ void __launch_bounds__(kG1T) k_g1_fwd(G1Fwd a)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint32_t *hs = reinterpret_cast<uint32_t *>(smem);  // [H][32]: samples (2w, 2w + 1) of the tile
+    float *zt = reinterpret_cast<float *>(smem + (size_t)a.H * 128);  // [kSB][kLC + 1] logits
+    float *dt = zt + kSB * (kLC + 1);                                 // [kSB][kLC + 1] dZ
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x % a.ntile;
+    const int64_t chunk = blockIdx.x / a.ntile;
+    const int b0 = tile * kSB;
+    for (int e = threadIdx.x; e < a.H * 32; e += kG1T) {
+        const int j = e >> 5, w = e & 31;
+        hs[e] = *reinterpret_cast<const uint32_t *>(a.hT + (int64_t)j * a.ldB + b0 + 2 * w);
+    }
+    __syncthreads();
+    const int F = a.F;
+    const int64_t l_begin = chunk * a.lchunk;
+    const int64_t l_end = min(a.L, l_begin + a.lchunk);
+    const int bA = b0 + 2 * lane, bB = bA + 1;
+    double lacc = 0.0;
+    for (int64_t r0 = l_begin; r0 < l_end; r0 += kLC) {
+        const int nl = (int)min((int64_t)kLC, l_end - r0);
+        float lf = 0.f;
+        for (int li = warp; li < nl; li += kG1T / 32) {
+            const int64_t l = r0 + li;
+            const uint4 *I = reinterpret_cast<const uint4 *>(a.idx_s + l * F);
+            const uint4 *Wl = reinterpret_cast<const uint4 *>(a.W + l * F);
+            float z0 = 0.f, z1 = 0.f;
+            for (int f8 = 0; f8 < F / 8; ++f8) {
+                const uint4 iv = __ldg(I + f8), wv = __ldg(Wl + f8);
+                const uint32_t ii[4] = {iv.x, iv.y, iv.z, iv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t h0 = hs[(ii[q] & 0xffffu) * 32 + lane];
+                    const uint32_t h1 = hs[(ii[q] >> 16) * 32 + lane];
+                    const float w0 = lo_bf(ww[q]), w1 = hi_bf(ww[q]);
+                    z0 = fmaf(lo_bf(h0), w0, z0);
+                    z1 = fmaf(hi_bf(h0), w0, z1);
+                    z0 = fmaf(lo_bf(h1), w1, z0);
+                    z1 = fmaf(hi_bf(h1), w1, z1);
+                }
+            }
+            zt[(2 * lane) * (kLC + 1) + li] = z0;
+            zt[(2 * lane + 1) * (kLC + 1) + li] = z1;
+            if (BCE) {
+                int y0 = 0, y1 = 0;
+                const int e1 = a.gptr[l + 1];
+                for (int e = a.gptr[l]; e < e1; ++e) {
+                    const int b = a.gent[e] >> 16;
+                    y0 |= b == bA;
+                    y1 |= b == bB;
+                }
+                float l0, l1;
+                const float d0 = bce_grad_loss(z0, y0, &l0), d1 = bce_grad_loss(z1, y1, &l1);
+                lf += (bA < a.B ? l0 : 0.f) + (bB < a.B ? l1 : 0.f);
+                dt[(2 * lane) * (kLC + 1) + li] = d0;
+                dt[(2 * lane + 1) * (kLC + 1) + li] = d1;
+            }
+        }
+        lacc += (double)lf;
+        __syncthreads();
+        // rows of nl labels per sample, 2 bytes each: consecutive threads,
+        // consecutive labels
+        for (int e = threadIdx.x; e < kSB * kLC; e += kG1T) {
+            const int rb = e / kLC, c = e - rb * kLC;
+            const int b = b0 + rb;
+            if (c >= nl || b >= a.B)
+                continue;
+            const int64_t at = (int64_t)b * a.L + r0 + c;
+            if (a.Z)
+                a.Z[at] = f2bf(zt[rb * (kLC + 1) + c]);
+            if (BCE) {
+                const float d = dt[rb * (kLC + 1) + c];
+                const uint16_t hi = f2bf(d);
+                a.dZ[at] = hi;
+                if (a.dZ_lo)
+                    a.dZ_lo[at] = f2bf(d - bf2f(hi));
+            }
+        }
+        __syncthreads();
+    }
+    if (BCE) {
+        const double s = g1_block_sum(lacc);
+        if (threadIdx.x == 0)
+            a.loss_part[blockIdx.x] = s;
+    }
+}
+
+struct G1DW {
+    const uint16_t *hT, *dZ, *dZ_lo, *idx_s;
+    uint16_t *dW;
+    int64_t L;
+    int32_t B, ldB, F, H;
+};
+
+// CTA loops over 64-label chunks; FQ = F / 32 features per lane
+template <int FQ>
+__global__ void __launch_bounds__(kG1T) k_g1_dW(G1DW a)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int HLD = 33;  // words per h^T row (odd: rows of different j spread over banks)
+    uint32_t *hs = reinterpret_cast<uint32_t *>(smem);                 // [H][33]
+    float *dzs = reinterpret_cast<float *>(smem + (size_t)a.H * HLD * 4);  // [kSB][kLC + 1]
+    uint16_t *is = reinterpret_cast<uint16_t *>(dzs + kSB * (kLC + 1));   // [kLC][F]
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const int F = a.F;
+    const int ntile = (a.B + kSB - 1) / kSB;
+    const int64_t nchunk = (a.L + kLC - 1) / kLC;
+    for (int64_t ch = blockIdx.x; ch < nchunk; ch += gridDim.x) {
+        const int64_t r0 = ch * kLC;
+        const int nl = (int)min((int64_t)kLC, a.L - r0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nl * F; e += kG1T)
+            is[e] = a.idx_s[r0 * F + e];
+        float acc[8][FQ];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+#pragma unroll
+            for (int q = 0; q < FQ; ++q)
+                acc[t][q] = 0.f;
+        for (int tile = 0; tile < ntile; ++tile) {
+            const int b0 = tile * kSB;
+            __syncthreads();
+            for (int e = threadIdx.x; e < a.H * 32; e += kG1T) {
+                const int j = e >> 5, w = e & 31;
+                hs[j * HLD + w] = *reinterpret_cast<const uint32_t *>(a.hT + (int64_t)j * a.ldB + b0 + 2 * w);
+            }
+            for (int e = threadIdx.x; e < kSB * kLC; e += kG1T) {
+                const int rb = e / kLC, c = e - rb * kLC;
+                const int b = b0 + rb;
+                float v = 0.f;
+                if (c < nl && b < a.B) {
+                    const int64_t at = (int64_t)b * a.L + r0 + c;
+                    v = bf2f(a.dZ[at]) + (a.dZ_lo ? bf2f(a.dZ_lo[at]) : 0.f);
+                }
+                dzs[rb * (kLC + 1) + c] = v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int li = warp + 8 * t;
+                if (li >= nl)
+                    break;
+                int j[FQ];
+#pragma unroll
+                for (int q = 0; q < FQ; ++q)
+                    j[q] = is[li * F + q * 32 + lane] * HLD;
+#pragma unroll 4
+                for (int w = 0; w < 32; ++w) {
+                    const float d0 = dzs[(2 * w) * (kLC + 1) + li], d1 = dzs[(2 * w + 1) * (kLC + 1) + li];
+#pragma unroll
+                    for (int q = 0; q < FQ; ++q) {
+                        const uint32_t h = hs[j[q] + w];
+                        acc[t][q] = fmaf(lo_bf(h), d0, acc[t][q]);
+                        acc[t][q] = fmaf(hi_bf(h), d1, acc[t][q]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int li = warp + 8 * t;
+            if (li < nl)
+#pragma unroll
+                for (int q = 0; q < FQ; ++q)
+                    a.dW[(r0 + li) * F + q * 32 + lane] = f2bf(acc[t][q]);
+        }
+    }
+}
+
+struct G1Dh {
+    const uint16_t *dZ, *dZ_lo, *W, *idx_s;
+    float *dh;
+    int64_t L, lchunk;
+    int32_t B, F, H, SB, ntile;
+};
+
+// CTA: sample tile blockIdx % ntile (SB samples, one per thread of a label
+// lane), labels [chunk * lchunk, +lchunk); 256 / SB label lanes share the
+// tile's dh partial (shared-memory adds; lanes rarely meet on one entry)
+__global__ void __launch_bounds__(kG1T) k_g1_dh(G1Dh a)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int SB = a.SB, ldp = a.H + 1;  // odd row stride: a warp's samples on distinct banks
+    float *part = reinterpret_cast<float *>(smem);     // [SB][H + 1]
+    float *dzs = part + (size_t)SB * ldp;              // [SB][kLC + 1]
+    const int tile = blockIdx.x % a.ntile;
+    const int64_t chunk = blockIdx.x / a.ntile;
+    const int b0 = tile * SB;
+    const int rb = threadIdx.x % SB, lanes = kG1T / SB, ln = threadIdx.x / SB;
+    const int F = a.F;
+    for (int e = threadIdx.x; e < SB * ldp; e += kG1T)
+        part[e] = 0.f;
+    const int64_t l_begin = chunk * a.lchunk;
+    const int64_t l_end = min(a.L, l_begin + a.lchunk);
+    float *prow = part + (size_t)rb * ldp;
+    for (int64_t r0 = l_begin; r0 < l_end; r0 += kLC) {
+        const int nl = (int)min((int64_t)kLC, l_end - r0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < SB * kLC; e += kG1T) {
+            const int r = e / kLC, c = e - r * kLC;
+            const int b = b0 + r;
+            float v = 0.f;
+            if (c < nl && b < a.B) {
+                const int64_t at = (int64_t)b * a.L + r0 + c;
+                v = bf2f(a.dZ[at]) + (a.dZ_lo ? bf2f(a.dZ_lo[at]) : 0.f);
+            }
+            dzs[r * (kLC + 1) + c] = v;
+        }
+        __syncthreads();
+        for (int li = ln; li < nl; li += lanes) {
+            const float dz = dzs[rb * (kLC + 1) + li];
+            if (dz == 0.f)
+                continue;
+            const int64_t l = r0 + li;
+            const uint4 *I = reinterpret_cast<const uint4 *>(a.idx_s + l * F);
+            const uint4 *Wl = reinterpret_cast<const uint4 *>(a.W + l * F);
+            for (int f8 = 0; f8 < F / 8; ++f8) {
+                const uint4 iv = __ldg(I + f8), wv = __ldg(Wl + f8);
+                const uint32_t ii[4] = {iv.x, iv.y, iv.z, iv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    atomicAdd(prow + (ii[q] & 0xffffu), dz * lo_bf(ww[q]));
+                    atomicAdd(prow + (ii[q] >> 16), dz * hi_bf(ww[q]));
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < SB * a.H; e += kG1T) {
+        const int r = e / a.H, i = e - r * a.H;
+        const int b = b0 + r;
+        if (b < a.B)
+            atomicAdd(a.dh + (int64_t)b * a.H + i, part[(size_t)r * ldp + i]);
+    }
+}
+
+int g1_grid(const sg_layout *lo)
+{
+    int g = lo->num_sms;
+    if (g > lo->loss_part_n)
+        g = lo->loss_part_n;
+    return g < 1 ? 1 : g;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+}  // namespace
+
+// The per-label kernels take F % 32 == 0 (F <= 256) and an h^T tile of every
+// feature in shared memory; other shapes keep the general CUDA-core kernels.
+bool g1_ok(const sg_layout *lo)
+{
+    return lo->G == 1 && lo->F % 32 == 0 && lo->F <= 256 && (size_t)lo->H * 132 + 64 * 65 * 4 + 64 * 256 * 2 <= 220 * 1024 &&
+           lo->ldB % 64 == 0;
+}
+
+sg_status g1_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint16_t *dZ, uint16_t *dZ_lo,
+                 double *loss, cudaStream_t st)
+{
+    if (!aligned16(W)) {
+        sg_set_error("W: device pointer must be 16-byte aligned");
+        return SG_ERR_INVALID;
+    }
+    G1Fwd a;
+    a.hT = lo->hT;
+    a.W = W;
+    a.idx_s = lo->idx_s;
+    a.Z = Z;
+    a.dZ = dZ;
+    a.dZ_lo = dZ_lo;
+    a.gptr = lo->gptr;
+    a.gent = lo->gent;
+    a.loss_part = lo->loss_part;
+    a.L = lo->L;
+    a.B = B;
+    a.ldB = lo->ldB;
+    a.F = lo->F;
+    a.H = lo->H;
+    a.ntile = (B + kSB - 1) / kSB;
+    int grid = g1_grid(lo);
+    int chunks = grid / a.ntile;
+    if (chunks < 1)
+        chunks = 1;
+    a.lchunk = (lo->L + chunks - 1) / chunks;
+    grid = (int)((lo->L + a.lchunk - 1) / a.lchunk) * a.ntile;
+    const size_t smem = (size_t)lo->H * 128 + 2 * (size_t)kSB * (kLC + 1) * 4;
+    const bool bce = dZ != nullptr;
+    void (*kern)(G1Fwd) = bce ? k_g1_fwd<true> : k_g1_fwd<false>;
+    SG_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, kG1T, smem, st>>>(a));
+    SG_TRY_CUDA(cudaGetLastError());
+    if (bce)
+        return sg_loss_finalize(lo, grid, loss, st);
+    return SG_OK;
+}
+
+sg_status g1_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B, uint16_t *dW, cudaStream_t st)
+{
+    G1DW a;
+    a.hT = lo->hT;
+    a.dZ = dZ;
+    a.dZ_lo = dZ_lo;
+    a.idx_s = lo->idx_s;
+    a.dW = dW;
+    a.L = lo->L;
+    a.B = B;
+    a.ldB = lo->ldB;
+    a.F = lo->F;
+    a.H = lo->H;
+    const size_t smem = (size_t)lo->H * 33 * 4 + (size_t)kSB * (kLC + 1) * 4 + (size_t)kLC * lo->F * 2;
+    void (*kern)(G1DW) = nullptr;
+    switch (lo->F / 32) {
+    case 1: kern = k_g1_dW<1>; break;
+    case 2: kern = k_g1_dW<2>; break;
+    case 3: kern = k_g1_dW<3>; break;
+    case 4: kern = k_g1_dW<4>; break;
+    case 5: kern = k_g1_dW<5>; break;
+    case 6: kern = k_g1_dW<6>; break;
+    case 7: kern = k_g1_dW<7>; break;
+    default: kern = k_g1_dW<8>; break;
+    }
+    int64_t nchunk = (lo->L + kLC - 1) / kLC;
+    int grid = lo->num_sms;
+    if (grid > nchunk)
+        grid = (int)nchunk;
+    SG_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    SG_LAUNCH(lo, SG_KIND_DW, st, kern<<<grid, kG1T, smem, st>>>(a));
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+sg_status g1_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B, const uint16_t *W, float *dh,
+                cudaStream_t st)
+{
+    if (!aligned16(W)) {
+        sg_set_error("W: device pointer must be 16-byte aligned");
+        return SG_ERR_INVALID;
+    }
+    G1Dh a;
+    a.dZ = dZ;
+    a.dZ_lo = dZ_lo;
+    a.W = W;
+    a.idx_s = lo->idx_s;
+    a.dh = dh;
+    a.L = lo->L;
+    a.B = B;
+    a.F = lo->F;
+    a.H = lo->H;
+    // the largest sample tile whose partial fits shared memory
+    a.SB = 64;
+    while (a.SB > 8 && (size_t)a.SB * (lo->H + 1 + kLC + 1) * 4 > 220 * 1024)
+        a.SB /= 2;
+    a.ntile = (B + a.SB - 1) / a.SB;
+    int chunks = lo->num_sms / a.ntile;
+    if (chunks < 1)
+        chunks = 1;
+    a.lchunk = (lo->L + chunks - 1) / chunks;
+    const int grid = (int)((lo->L + a.lchunk - 1) / a.lchunk) * a.ntile;
+    const size_t smem = (size_t)a.SB * (lo->H + 1 + kLC + 1) * 4;
+    SG_TRY_CUDA(cudaFuncSetAttribute(k_g1_dh, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
+    SG_LAUNCH(lo, SG_KIND_DH, st, k_g1_dh<<<grid, kG1T, smem, st>>>(a));
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}

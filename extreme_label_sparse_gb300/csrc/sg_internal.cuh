@@ -159,6 +159,14 @@ sg_status sg_pos_prepare(sg_layout *lo, int32_t B, const int32_t *rowptr,
 sg_status sg_pos_compact(sg_layout *lo, int32_t B, const int32_t *rowptr,
                          int32_t *out_rowptr, int32_t *out_slots,
                          cudaStream_t st);
+// per-label fan-in (G = 1) kernels of the CUDA-core engine (g1.cu)
+bool g1_ok(const sg_layout *lo);
+sg_status g1_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint16_t *dZ, uint16_t *dZ_lo,
+                 double *loss, cudaStream_t st);
+sg_status g1_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B, uint16_t *dW, cudaStream_t st);
+sg_status g1_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_t B, const uint16_t *W, float *dh,
+                cudaStream_t st);
+
 sg_status sg_loss_finalize(sg_layout *lo, int32_t nparts, double *loss,
                            cudaStream_t st);
 // simt.cu

@@ -383,6 +383,8 @@ sg_status simt_transpose_h(sg_layout *lo, const uint16_t *h, int32_t B,
 sg_status simt_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z,
                    uint16_t *dZ, uint16_t *dZ_lo, double *loss, cudaStream_t st)
 {
+    if (g1_ok(lo))  // per-label fan-in: its own kernels (g1.cu)
+        return g1_fwd(lo, B, W, Z, dZ, dZ_lo, loss, st);
     FwdArgs a;
     a.hT = lo->hT;
     a.W = W;
@@ -432,6 +434,8 @@ sg_status simt_bce(sg_layout *lo, const uint16_t *Z, int32_t B, uint16_t *dZ,
 sg_status simt_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
                   int32_t B, uint16_t *dW, cudaStream_t st)
 {
+    if (g1_ok(lo))
+        return g1_dW(lo, dZ, dZ_lo, B, dW, st);
     DWArgs a;
     a.hT = lo->hT;
     a.dZ = dZ;
@@ -462,6 +466,8 @@ sg_status simt_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
 sg_status simt_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo,
                   int32_t B, const uint16_t *W, float *dh, cudaStream_t st)
 {
+    if (g1_ok(lo))
+        return g1_dh(lo, dZ, dZ_lo, B, W, dh, st);
     DhArgs a;
     a.dZ = dZ;
     a.dZ_lo = dZ_lo;

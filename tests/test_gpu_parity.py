@@ -49,6 +49,10 @@ CASES = [
     (_w("tc_g192_f32", B=100, H=256, L=192 * 8, G=192, F=32, pos=5), (SIMT, TC)),
     (_w("tc_h4096", B=64, H=4096, L=32 * 60, G=32, F=64, pos=4), (SIMT, TC)),
     (_w("simt_h2500_g5", B=40, H=2500, L=5 * 120, G=5, F=40, pos=3), (SIMT,)),
+    # per-label fan-in through the dedicated G = 1 kernels: several sample
+    # tiles and label chunks, a ragged last tile, F = 64 and 128
+    (_w("g1_f128", B=100, H=256, L=700, G=1, F=128, pos=4, dist="zipf"), (SIMT,)),
+    (_w("g1_f64_b256", B=256, H=512, L=1000, G=1, F=64, pos=5, dist="zipf"), (SIMT,)),
 ]
 
 
