@@ -11,8 +11,9 @@
 //   dW:      per 64-label chunk and 64-sample tile, the h^T tile and the dZ
 //            tile in shared memory; a warp owns 8 labels, lane l the features
 //            f = l + 32 q, accumulating over every sample tile in registers.
-//   dh:      each thread owns one sample and its own row of a shared-memory
-//            dh partial (no atomics per product); a CTA streams a contiguous
+//   dh:      a CTA holds a 32-sample dh partial; warp w owns a window of
+//            dh columns and lane l sample l, so every thread adds into its own
+//            entries (no atomics per product); a CTA streams a contiguous
 //            range of labels and adds its partial to dh once.
 #include "sg_internal.cuh"
 
@@ -58,6 +59,8 @@ __global__ void __launch_bounds__(kG1T) k_g1_fwd(G1Fwd a)
     uint32_t *hs = reinterpret_cast<uint32_t *>(smem);  // [H][32]: samples (2w, 2w + 1) of the tile
     float *zt = reinterpret_cast<float *>(smem + (size_t)a.H * 128);  // [kSB][kLC + 1] logits
     float *dt = zt + kSB * (kLC + 1);                                 // [kSB][kLC + 1] dZ
+    uint16_t *is = reinterpret_cast<uint16_t *>(dt + kSB * (kLC + 1));  // [kLC][F] the round's I_l
+    uint16_t *wsm = is + kLC * a.F;                                     // [kLC][F] the round's w_l
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int tile = blockIdx.x % a.ntile;
     const int64_t chunk = blockIdx.x / a.ntile;
@@ -75,13 +78,20 @@ __global__ void __launch_bounds__(kG1T) k_g1_fwd(G1Fwd a)
     for (int64_t r0 = l_begin; r0 < l_end; r0 += kLC) {
         const int nl = (int)min((int64_t)kLC, l_end - r0);
         float lf = 0.f;
+        // the round's index rows and weights, all loads in flight at once
+        for (int e = threadIdx.x; e < nl * F / 8; e += kG1T) {
+            reinterpret_cast<uint4 *>(is)[e] = __ldg(reinterpret_cast<const uint4 *>(a.idx_s + r0 * F) + e);
+            reinterpret_cast<uint4 *>(wsm)[e] = __ldg(reinterpret_cast<const uint4 *>(a.W + r0 * F) + e);
+        }
+        __syncthreads();
         for (int li = warp; li < nl; li += kG1T / 32) {
             const int64_t l = r0 + li;
-            const uint4 *I = reinterpret_cast<const uint4 *>(a.idx_s + l * F);
-            const uint4 *Wl = reinterpret_cast<const uint4 *>(a.W + l * F);
+            const uint4 *I = reinterpret_cast<const uint4 *>(is + li * F);
+            const uint4 *Wl = reinterpret_cast<const uint4 *>(wsm + li * F);
             float z0 = 0.f, z1 = 0.f;
+#pragma unroll 2
             for (int f8 = 0; f8 < F / 8; ++f8) {
-                const uint4 iv = __ldg(I + f8), wv = __ldg(Wl + f8);
+                const uint4 iv = I[f8], wv = Wl[f8];
                 const uint32_t ii[4] = {iv.x, iv.y, iv.z, iv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -226,28 +236,34 @@ struct G1Dh {
     const uint16_t *dZ, *dZ_lo, *W, *idx_s;
     float *dh;
     int64_t L, lchunk;
-    int32_t B, F, H, SB, ntile;
+    int32_t B, F, H, ntile, hw;
 };
 
-// CTA: sample tile blockIdx % ntile (SB samples, one per thread of a label
-// lane), labels [chunk * lchunk, +lchunk); 256 / SB label lanes share the
-// tile's dh partial (shared-memory adds; lanes rarely meet on one entry)
+// CTA: 32 samples (tile blockIdx % ntile) x labels [chunk * lchunk, +lchunk).
+// Warp w owns the dh columns [w hw, w hw + hw) and lane l sample l: each
+// thread adds into its own part of its own row, so no two threads ever meet
+// on an entry and there is no atomic per product.  The round's index rows are
+// sorted, so a warp finds its window's entries by binary search.
 __global__ void __launch_bounds__(kG1T) k_g1_dh(G1Dh a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
-    const int SB = a.SB, ldp = a.H + 1;  // odd row stride: a warp's samples on distinct banks
-    float *part = reinterpret_cast<float *>(smem);     // [SB][H + 1]
-    float *dzs = part + (size_t)SB * ldp;              // [SB][kLC + 1]
+    constexpr int SB = 32;
+    const int ldp = a.H + 1;  // odd row stride: a warp's 32 rows on distinct banks
+    float *part = reinterpret_cast<float *>(smem);                     // [SB][H + 1]
+    float *dzs = part + (size_t)SB * ldp;                              // [SB][kLC + 1]
+    uint16_t *is = reinterpret_cast<uint16_t *>(dzs + SB * (kLC + 1));  // [kLC][F]
+    uint16_t *wsm = is + kLC * a.F;                                     // [kLC][F]
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int tile = blockIdx.x % a.ntile;
     const int64_t chunk = blockIdx.x / a.ntile;
     const int b0 = tile * SB;
-    const int rb = threadIdx.x % SB, lanes = kG1T / SB, ln = threadIdx.x / SB;
     const int F = a.F;
+    const int j0 = warp * a.hw, j1 = min(a.H, j0 + a.hw);
     for (int e = threadIdx.x; e < SB * ldp; e += kG1T)
         part[e] = 0.f;
     const int64_t l_begin = chunk * a.lchunk;
     const int64_t l_end = min(a.L, l_begin + a.lchunk);
-    float *prow = part + (size_t)rb * ldp;
+    float *prow = part + (size_t)lane * ldp;
     for (int64_t r0 = l_begin; r0 < l_end; r0 += kLC) {
         const int nl = (int)min((int64_t)kLC, l_end - r0);
         __syncthreads();
@@ -261,23 +277,39 @@ __global__ void __launch_bounds__(kG1T) k_g1_dh(G1Dh a)
             }
             dzs[r * (kLC + 1) + c] = v;
         }
+        for (int e = threadIdx.x; e < nl * F / 8; e += kG1T) {
+            reinterpret_cast<uint4 *>(is)[e] = __ldg(reinterpret_cast<const uint4 *>(a.idx_s + r0 * F) + e);
+            reinterpret_cast<uint4 *>(wsm)[e] = __ldg(reinterpret_cast<const uint4 *>(a.W + r0 * F) + e);
+        }
         __syncthreads();
-        for (int li = ln; li < nl; li += lanes) {
-            const float dz = dzs[rb * (kLC + 1) + li];
-            if (dz == 0.f)
-                continue;
-            const int64_t l = r0 + li;
-            const uint4 *I = reinterpret_cast<const uint4 *>(a.idx_s + l * F);
-            const uint4 *Wl = reinterpret_cast<const uint4 *>(a.W + l * F);
-            for (int f8 = 0; f8 < F / 8; ++f8) {
-                const uint4 iv = __ldg(I + f8), wv = __ldg(Wl + f8);
-                const uint32_t ii[4] = {iv.x, iv.y, iv.z, iv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    atomicAdd(prow + (ii[q] & 0xffffu), dz * lo_bf(ww[q]));
-                    atomicAdd(prow + (ii[q] >> 16), dz * hi_bf(ww[q]));
-                }
+        if (j0 >= j1)
+            continue;
+        for (int li = 0; li < nl; ++li) {
+            const uint16_t *I = is + li * F;
+            // entries [fa, fb) of the sorted row fall in the window
+            int lo = 0, hi = F;
+            while (lo < hi) {
+                const int m = (lo + hi) >> 1;
+                if ((int)I[m] < j0)
+                    lo = m + 1;
+                else
+                    hi = m;
             }
+            const int fa = lo;
+            hi = F;
+            while (lo < hi) {
+                const int m = (lo + hi) >> 1;
+                if ((int)I[m] < j1)
+                    lo = m + 1;
+                else
+                    hi = m;
+            }
+            const int fb = lo;
+            const float dz = dzs[lane * (kLC + 1) + li];
+            const uint16_t *Wl = wsm + li * F;
+#pragma unroll 4
+            for (int f = fa; f < fb; ++f)
+                prow[I[f]] = fmaf(dz, bf2f(Wl[f]), prow[I[f]]);
         }
     }
     __syncthreads();
@@ -299,14 +331,28 @@ int g1_grid(const sg_layout *lo)
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
+size_t g1_fwd_smem(const sg_layout *lo)
+{
+    return (size_t)lo->H * 128 + 2 * (size_t)kSB * (kLC + 1) * 4 + 2 * (size_t)kLC * lo->F * 2;
+}
+size_t g1_dW_smem(const sg_layout *lo)
+{
+    return (size_t)lo->H * 33 * 4 + (size_t)kSB * (kLC + 1) * 4 + (size_t)kLC * lo->F * 2;
+}
+size_t g1_dh_smem(const sg_layout *lo)
+{
+    return (size_t)32 * (lo->H + 1) * 4 + (size_t)32 * (kLC + 1) * 4 + 2 * (size_t)kLC * lo->F * 2;
+}
+
 }  // namespace
 
 // The per-label kernels take F % 32 == 0 (F <= 256) and an h^T tile of every
 // feature in shared memory; other shapes keep the general CUDA-core kernels.
 bool g1_ok(const sg_layout *lo)
 {
-    return lo->G == 1 && lo->F % 32 == 0 && lo->F <= 256 && (size_t)lo->H * 132 + 64 * 65 * 4 + 64 * 256 * 2 <= 220 * 1024 &&
-           lo->ldB % 64 == 0;
+    constexpr size_t kMax = 220 * 1024;
+    return lo->G == 1 && lo->F % 32 == 0 && lo->F <= 256 && lo->ldB % 64 == 0 && g1_fwd_smem(lo) <= kMax &&
+           g1_dW_smem(lo) <= kMax && g1_dh_smem(lo) <= kMax;
 }
 
 sg_status g1_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint16_t *dZ, uint16_t *dZ_lo,
@@ -338,7 +384,7 @@ sg_status g1_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
         chunks = 1;
     a.lchunk = (lo->L + chunks - 1) / chunks;
     grid = (int)((lo->L + a.lchunk - 1) / a.lchunk) * a.ntile;
-    const size_t smem = (size_t)lo->H * 128 + 2 * (size_t)kSB * (kLC + 1) * 4;
+    const size_t smem = g1_fwd_smem(lo);
     const bool bce = dZ != nullptr;
     void (*kern)(G1Fwd) = bce ? k_g1_fwd<true> : k_g1_fwd<false>;
     SG_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
@@ -362,7 +408,7 @@ sg_status g1_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     a.ldB = lo->ldB;
     a.F = lo->F;
     a.H = lo->H;
-    const size_t smem = (size_t)lo->H * 33 * 4 + (size_t)kSB * (kLC + 1) * 4 + (size_t)kLC * lo->F * 2;
+    const size_t smem = g1_dW_smem(lo);
     void (*kern)(G1DW) = nullptr;
     switch (lo->F / 32) {
     case 1: kern = k_g1_dW<1>; break;
@@ -401,17 +447,14 @@ sg_status g1_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
     a.B = B;
     a.F = lo->F;
     a.H = lo->H;
-    // the largest sample tile whose partial fits shared memory
-    a.SB = 64;
-    while (a.SB > 8 && (size_t)a.SB * (lo->H + 1 + kLC + 1) * 4 > 220 * 1024)
-        a.SB /= 2;
-    a.ntile = (B + a.SB - 1) / a.SB;
+    a.hw = (lo->H + kG1T / 32 - 1) / (kG1T / 32);  // one window of columns per warp
+    a.ntile = (B + 31) / 32;
     int chunks = lo->num_sms / a.ntile;
     if (chunks < 1)
         chunks = 1;
     a.lchunk = (lo->L + chunks - 1) / chunks;
     const int grid = (int)((lo->L + a.lchunk - 1) / a.lchunk) * a.ntile;
-    const size_t smem = (size_t)a.SB * (lo->H + 1 + kLC + 1) * 4;
+    const size_t smem = g1_dh_smem(lo);
     SG_TRY_CUDA(cudaFuncSetAttribute(k_g1_dh, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
     SG_LAUNCH(lo, SG_KIND_DH, st, k_g1_dh<<<grid, kG1T, smem, st>>>(a));
