@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kG1T) k_g1_fwd(G1Fwd a)
     float *dt = zt + kSB * (kLC + 1);                                 // [kSB][kLC + 1] dZ
     uint16_t *is = reinterpret_cast<uint16_t *>(dt + kSB * (kLC + 1));  // [kLC][F] the round's I_l
     uint16_t *wsm = is + kLC * a.F;                                     // [kLC][F] the round's w_l
+    __shared__ int32_t gp[kLC + 1];  // the round's positive-list bounds
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int tile = blockIdx.x % a.ntile;
     const int64_t chunk = blockIdx.x / a.ntile;
@@ -83,9 +84,11 @@ __global__ void __launch_bounds__(kG1T) k_g1_fwd(G1Fwd a)
             reinterpret_cast<uint4 *>(is)[e] = __ldg(reinterpret_cast<const uint4 *>(a.idx_s + r0 * F) + e);
             reinterpret_cast<uint4 *>(wsm)[e] = __ldg(reinterpret_cast<const uint4 *>(a.W + r0 * F) + e);
         }
+        if (BCE)
+            for (int e = threadIdx.x; e <= nl; e += kG1T)
+                gp[e] = a.gptr[r0 + e];
         __syncthreads();
         for (int li = warp; li < nl; li += kG1T / 32) {
-            const int64_t l = r0 + li;
             const uint4 *I = reinterpret_cast<const uint4 *>(is + li * F);
             const uint4 *Wl = reinterpret_cast<const uint4 *>(wsm + li * F);
             float z0 = 0.f, z1 = 0.f;
@@ -108,8 +111,8 @@ __global__ void __launch_bounds__(kG1T) k_g1_fwd(G1Fwd a)
             zt[(2 * lane + 1) * (kLC + 1) + li] = z1;
             if (BCE) {
                 int y0 = 0, y1 = 0;
-                const int e1 = a.gptr[l + 1];
-                for (int e = a.gptr[l]; e < e1; ++e) {
+                const int e1 = gp[li + 1];
+                for (int e = gp[li]; e < e1; ++e) {
                     const int b = a.gent[e] >> 16;
                     y0 |= b == bA;
                     y1 |= b == bB;
@@ -286,30 +289,35 @@ __global__ void __launch_bounds__(kG1T) k_g1_dh(G1Dh a)
             continue;
         for (int li = 0; li < nl; ++li) {
             const uint16_t *I = is + li * F;
-            // entries [fa, fb) of the sorted row fall in the window
-            int lo = 0, hi = F;
-            while (lo < hi) {
-                const int m = (lo + hi) >> 1;
-                if ((int)I[m] < j0)
-                    lo = m + 1;
-                else
-                    hi = m;
+            // entries [fa, fb) of the sorted row fall in the window: count
+            // the entries below each bound, 32 at a time (no load chain)
+            int fa = 0, fb = 0;
+            for (int f0 = 0; f0 < F; f0 += 32) {
+                const int v = I[f0 + lane];
+                fa += __popc(__ballot_sync(0xffffffffu, v < j0));
+                fb += __popc(__ballot_sync(0xffffffffu, v < j1));
             }
-            const int fa = lo;
-            hi = F;
-            while (lo < hi) {
-                const int m = (lo + hi) >> 1;
-                if ((int)I[m] < j1)
-                    lo = m + 1;
-                else
-                    hi = m;
-            }
-            const int fb = lo;
             const float dz = dzs[lane * (kLC + 1) + li];
             const uint16_t *Wl = wsm + li * F;
-#pragma unroll 4
-            for (int f = fa; f < fb; ++f)
-                prow[I[f]] = fmaf(dz, bf2f(Wl[f]), prow[I[f]]);
+            // a label's indices are distinct: eight updates at a time with
+            // their loads in flight together
+            for (int f0 = fa; f0 < fb; f0 += 8) {
+                int j[8];
+                float w[8], p[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int f = f0 + u < fb ? f0 + u : fa;
+                    j[u] = I[f];
+                    w[u] = f0 + u < fb ? bf2f(Wl[f]) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    p[u] = prow[j[u]];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (f0 + u < fb)
+                        prow[j[u]] = fmaf(dz, w[u], p[u]);
+            }
         }
     }
     __syncthreads();
