@@ -193,6 +193,7 @@ sg_status sg_layout_build(const int32_t *groups, int64_t L, int32_t G,
                           sg_layout **out)
 {
     const char *fn = "sg_layout_build";
+    NvtxRange nvtx_(fn);
     if (!out)
         FAIL(SG_ERR_INVALID, "%s: out is NULL", fn);
     *out = nullptr;
@@ -282,6 +283,7 @@ sg_status sg_layout_export(const sg_layout *lo, int32_t *slot_of_label,
                            void *stream)
 {
     const char *fn = "sg_layout_export";
+    NvtxRange nvtx_(fn);
     if (!lo)
         FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
     DeviceGuard dg(lo->device);
@@ -340,6 +342,7 @@ sg_status sg_layout_info(const sg_layout *lo, int64_t *L, int32_t *G,
 sg_status sg_layout_status(sg_layout *lo, int32_t *code, int32_t clear)
 {
     const char *fn = "sg_layout_status";
+    NvtxRange nvtx_(fn);
     if (!lo)
         FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
     REQUIRE(code, fn);
@@ -359,6 +362,7 @@ sg_status sg_pos_export(sg_layout *lo, int32_t B, const int32_t *pos_rowptr,
                         int32_t *out_gptr, int32_t *out_gentry, void *stream)
 {
     const char *fn = "sg_pos_export";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
     DeviceGuard dg(lo->device);
@@ -384,6 +388,7 @@ sg_status sg_fwd(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
                  sg_bf16 *Z, void *stream)
 {
     const char *fn = "sg_fwd";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     REQUIRE(h, fn);
     REQUIRE(W, fn);
@@ -403,6 +408,7 @@ sg_status sg_bce_grad(sg_layout *lo, const sg_bf16 *Z, int32_t B,
                       int64_t nnz, sg_bf16 *dZ, double *loss, void *stream)
 {
     const char *fn = "sg_bce_grad";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
     REQUIRE(Z, fn);
@@ -420,6 +426,7 @@ sg_status sg_fwd_bce(sg_layout *lo, const sg_bf16 *h, int32_t B,
                      double *loss, sg_bf16 *Z_or_null, void *stream)
 {
     const char *fn = "sg_fwd_bce";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
     REQUIRE(h, fn);
@@ -442,6 +449,7 @@ sg_status sg_bwd_dW(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h,
                     int32_t B, sg_bf16 *dW, void *stream)
 {
     const char *fn = "sg_bwd_dW";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     REQUIRE(dZ, fn);
     REQUIRE(h, fn);
@@ -460,6 +468,7 @@ sg_status sg_bwd_dh(sg_layout *lo, const sg_bf16 *dZ, int32_t B,
                     const sg_bf16 *W, float *dh, void *stream)
 {
     const char *fn = "sg_bwd_dh";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     REQUIRE(dZ, fn);
     REQUIRE(W, fn);
@@ -477,6 +486,7 @@ sg_status sg_bwd(sg_layout *lo, const sg_bf16 *dZ, const sg_bf16 *h, int32_t B,
                  const sg_bf16 *W, sg_bf16 *dW, float *dh, void *stream)
 {
     const char *fn = "sg_bwd";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     REQUIRE(dZ, fn);
     REQUIRE(h, fn);
@@ -576,6 +586,7 @@ sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W
 sg_status sg_step_plan(const sg_layout *lo, int32_t B, int32_t sgd, int32_t *plan)
 {
     const char *fn = "sg_step_plan";
+    NvtxRange nvtx_(fn);
     if (!lo || !plan)
         FAIL(SG_ERR_INVALID, "%s: layout or plan is NULL", fn);
     if (B < 1 || B > lo->max_B)
@@ -595,6 +606,7 @@ sg_status sg_step(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W,
                   void *stream)
 {
     const char *fn = "sg_step";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
     REQUIRE(h, fn);
@@ -612,6 +624,7 @@ sg_status sg_step_sgd(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 
                       float mu, float *mom, sg_bf16 *W_out, float *dh, double *loss, void *stream)
 {
     const char *fn = "sg_step_sgd";
+    NvtxRange nvtx_(fn);
     TRY(check_call(lo, B, fn));
     TRY(check_pos(lo, pos_rowptr, pos_label, nnz, fn));
     REQUIRE(h, fn);
@@ -637,6 +650,7 @@ sg_status sg_step_sgd(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 
 sg_status sg_timing_start(sg_layout *lo, int32_t capacity)
 {
     const char *fn = "sg_timing_start";
+    NvtxRange nvtx_(fn);
     if (!lo)
         FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
     if (capacity < 0 || capacity > (1 << 20))
@@ -675,6 +689,7 @@ sg_status sg_timing_stop(sg_layout *lo, double *ms_per_kind,
                          int32_t *launches_per_kind)
 {
     const char *fn = "sg_timing_stop";
+    NvtxRange nvtx_(fn);
     if (!lo)
         FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
     DeviceGuard dg(lo->device);

@@ -782,6 +782,7 @@ sg_status sg_grouping_embed(sg_grouping *g, const sg_bf16 *h, int32_t N, const i
                             const int32_t *labels, int64_t nnz, int64_t *n_embedded, void *stream)
 {
     const char *fn = "sg_grouping_embed";
+    NvtxRange nvtx_(fn);
     if (!g || !h || !rowptr || (nnz > 0 && !labels))
         GR_FAIL(SG_ERR_INVALID, "%s: a required pointer is NULL", fn);
     if (N < 1 || N > kMaxSamples || nnz < 0)
@@ -853,6 +854,7 @@ sg_status sg_grouping_set_embeddings(sg_grouping *g, const sg_bf16 *E, const uin
 sg_status sg_grouping_kmeans_init(sg_grouping *g, const int32_t *init_labels, void *stream)
 {
     const char *fn = "sg_grouping_kmeans_init";
+    NvtxRange nvtx_(fn);
     if (!g || !init_labels)
         GR_FAIL(SG_ERR_INVALID, "%s: a required pointer is NULL", fn);
     if (!g->embedded)
@@ -901,6 +903,7 @@ sg_status sg_grouping_kmeans_batch(sg_grouping *g, const int32_t *batch, int32_t
                                    void *stream)
 {
     const char *fn = "sg_grouping_kmeans_batch";
+    NvtxRange nvtx_(fn);
     if (!g || !batch)
         GR_FAIL(SG_ERR_INVALID, "%s: a required pointer is NULL", fn);
     if (!g->centred)
@@ -931,6 +934,7 @@ sg_status sg_grouping_kmeans_batch(sg_grouping *g, const int32_t *batch, int32_t
 sg_status sg_grouping_groups(sg_grouping *g, int32_t *groups, int32_t *cluster_out, void *stream)
 {
     const char *fn = "sg_grouping_groups";
+    NvtxRange nvtx_(fn);
     if (!g || !groups)
         GR_FAIL(SG_ERR_INVALID, "%s: a required pointer is NULL", fn);
     if (!g->centred)

@@ -80,6 +80,7 @@ sg_status sg_proj_fwd(const sg_bf16 *h, int32_t B, int32_t E, const sg_bf16 *P, 
                       void *stream)
 {
     const char *fn = "sg_proj_fwd";
+    NvtxRange nvtx_(fn);
     if (!h || !P || !out)
         HT_FAIL(SG_ERR_INVALID, "%s: a required pointer is NULL", fn);
     if (!sizes_ok(B, E, D))
@@ -92,6 +93,7 @@ sg_status sg_proj_bwd(const sg_bf16 *h, int32_t B, int32_t E, const sg_bf16 *P, 
                       sg_bf16 *work, float *dP, float *dh, int32_t accumulate_dh, void *stream)
 {
     const char *fn = "sg_proj_bwd";
+    NvtxRange nvtx_(fn);
     if (!h || !P || !g || !work || !dP || !dh)
         HT_FAIL(SG_ERR_INVALID, "%s: a required pointer is NULL", fn);
     if (!sizes_ok(B, E, D))
@@ -108,6 +110,7 @@ sg_status sg_headtail_step(sg_layout *head, sg_layout *tail, const sg_bf16 *h, i
                            float *dh, double *loss, void *stream)
 {
     const char *fn = "sg_headtail_step";
+    NvtxRange nvtx_(fn);
     if (!head || !tail)
         HT_FAIL(SG_ERR_INVALID, "%s: layout is NULL", fn);
     if (!h || !P_head || !P_tail || !W_head || !W_tail || !dW_head || !dW_tail || !dP_head || !dP_tail || !dh ||

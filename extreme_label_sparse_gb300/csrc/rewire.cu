@@ -165,6 +165,7 @@ extern "C" sg_status sg_rewire(sg_layout *lo, const sg_bf16 *h, int32_t B, const
                                int32_t n_drop, int32_t *idx_out, sg_bf16 *W_out, void *stream)
 {
     const char *fn = "sg_rewire";
+    NvtxRange nvtx_(fn);
     if (!lo || !h || !dZ || !W || !idx_out || !W_out) {
         sg_set_error("%s: a required pointer is NULL", fn);
         return SG_ERR_INVALID;

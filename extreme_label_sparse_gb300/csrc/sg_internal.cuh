@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/sg.h"
@@ -159,6 +160,16 @@ sg_status sg_pos_prepare(sg_layout *lo, int32_t B, const int32_t *rowptr,
 sg_status sg_pos_compact(sg_layout *lo, int32_t B, const int32_t *rowptr,
                          int32_t *out_rowptr, int32_t *out_slots,
                          cudaStream_t st);
+// An NVTX range around a public entry point, named after it (a profiler shows
+// the library's calls on its timeline; without one attached the calls cost
+// nothing beyond a branch)
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 // per-label fan-in (G = 1) kernels of the CUDA-core engine (g1.cu)
 bool g1_ok(const sg_layout *lo);
 sg_status g1_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint16_t *dZ, uint16_t *dZ_lo,
