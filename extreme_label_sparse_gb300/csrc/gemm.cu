@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 // warps through shared memory (G = 64, 128).
 __global__ void __launch_bounds__(kGThreads, 1)
     k_gemm_gabs(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, float *out,
-                int32_t M, int32_t N, int32_t K, int32_t G, int32_t *status)
+                int32_t M, int32_t N, int32_t K, int32_t G, int32_t NS, int32_t *status)
 {
     __shared__ GemmCtl c;
     __shared__ float part[4][32];
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int nkb = (K + 63) / 64;
     if (threadIdx.x == 0) {
         c.abort_flag = 0;
-        for (int s = 0; s < kGS; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(bar_of(c.full[s]), 1);
             mbar_init(bar_of(c.empty[s]), 1);
         }
@@ -218,8 +218,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         int kb = 0;
         if (lane == 0) {
             for (; kb < nkb; ++kb) {
-                const int s = kb % kGS;
-                if (!mbar_wait(bar_of(c.empty[s]), ((uint32_t)(kb / kGS) & 1u) ^ 1u, abort_flag, status))
+                const int s = kb % NS;
+                if (!mbar_wait(bar_of(c.empty[s]), ((uint32_t)(kb / NS) & 1u) ^ 1u, abort_flag, status))
                     break;
                 const uint32_t st = base + (uint32_t)s * 2 * kTileBytes;
                 mbar_arrive_expect_tx(bar_of(c.full[s]), 2 * kTileBytes);
@@ -227,16 +227,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 load_tile(st + kTileBytes, &tm_b, 1, n0, kb * 64, bar_of(c.full[s]));
             }
             if (*abort_flag)
-                for (int j = kb - kGS < 0 ? 0 : kb - kGS; j < kb; ++j)
-                    mbar_wait_drain(bar_of(c.full[j % kGS]), (uint32_t)(j / kGS) & 1u);
+                for (int j = kb - NS < 0 ? 0 : kb - NS; j < kb; ++j)
+                    mbar_wait_drain(bar_of(c.full[j % NS]), (uint32_t)(j / NS) & 1u);
         }
         __syncwarp();
     } else if (warp == 1) {
         const uint32_t idesc = idesc_bf16(128, 128, 1, 1);
         int kb = 0;
         for (; kb < nkb; ++kb) {
-            const int s = kb % kGS;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.full[s]), (uint32_t)(kb / kGS) & 1u, abort_flag,
+            const int s = kb % NS;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.full[s]), (uint32_t)(kb / NS) & 1u, abort_flag,
                                                    status)))
                 break;
             tc_fence_after();
@@ -611,10 +611,13 @@ sg_status gemm_group_abs(const uint16_t *A, int64_t lda, int M, const uint16_t *
     rc = map_2d(&tb, B, (uint64_t)N, (uint64_t)K, (uint64_t)ldb, 64, 64, "B");
     if (rc != SG_OK)
         return rc;
-    const size_t smem = (size_t)kGS * 2 * kTileBytes + 1024;
+    // stages: no more than the K blocks (with few of them, several CTAs share an SM)
+    const int nkb = (K + 63) / 64;
+    const int NS = nkb < kGS ? nkb : kGS;
+    const size_t smem = (size_t)NS * 2 * kTileBytes + 1024;
     SG_TRY_CUDA(cudaFuncSetAttribute(k_gemm_gabs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     dim3 grid((unsigned)((N + 127) / 128), (unsigned)((M + 127) / 128));
-    k_gemm_gabs<<<grid, kGThreads, smem, st>>>(ta, tb, out, M, N, K, G, status);
+    k_gemm_gabs<<<grid, kGThreads, smem, st>>>(ta, tb, out, M, N, K, G, NS, status);
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }

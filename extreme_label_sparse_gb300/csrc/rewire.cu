@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kRwWarps = 4;
 constexpr int kRwMaxF = 256;
+constexpr int kRwRegs = 32;  // grow-score registers per lane (H <= 1024 held in registers)
 
 __device__ __forceinline__ float bfv(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
 
@@ -100,22 +101,53 @@ __global__ void __launch_bounds__(32 * kRwWarps)
     for (int f = lane; f < F; f += 32)
         sc[I[f]] = -1.f;
     __syncwarp();
-    // grow the n_drop largest
-    for (int r = 0; r < n_drop; ++r) {
-        float v = -1.f;
-        int j = -1;
-        for (int x = lane; x < H; x += 32) {
-            const float s = sc[x];
-            if (s >= 0.f && (j < 0 || s > v))  // ascending x: ties keep the smaller
-                v = s, j = x;
+    // grow the n_drop largest: the row in registers (feature x = lane + 32 t)
+    // when it fits, else scanned from memory each time
+    if (H <= 32 * kRwRegs) {
+        float rv[kRwRegs];
+#pragma unroll
+        for (int t = 0; t < kRwRegs; ++t) {
+            const int x = lane + 32 * t;
+            rv[t] = x < H ? sc[x] : -1.f;
         }
-        warp_best(v, j, true);
-        if (lane == 0) {
-            grow[r] = j;
-            if (j >= 0)
-                sc[j] = -1.f;
+        for (int r = 0; r < n_drop; ++r) {
+            float v = -1.f;
+            int j = -1, tt = -1;
+#pragma unroll
+            for (int t = 0; t < kRwRegs; ++t)
+                if (rv[t] >= 0.f && (j < 0 || rv[t] > v)) {  // ascending x: ties keep the smaller
+                    v = rv[t];
+                    j = lane + 32 * t;
+                    tt = t;
+                }
+            const int mine = j;
+            warp_best(v, j, true);
+            if (j >= 0 && mine == j) {
+#pragma unroll
+                for (int t = 0; t < kRwRegs; ++t)
+                    if (t == tt)
+                        rv[t] = -1.f;
+            }
+            if (lane == 0)
+                grow[r] = j;
         }
-        __syncwarp();
+    } else {
+        for (int r = 0; r < n_drop; ++r) {
+            float v = -1.f;
+            int j = -1;
+            for (int x = lane; x < H; x += 32) {
+                const float s = sc[x];
+                if (s >= 0.f && (j < 0 || s > v))  // ascending x: ties keep the smaller
+                    v = s, j = x;
+            }
+            warp_best(v, j, true);
+            if (lane == 0) {
+                grow[r] = j;
+                if (j >= 0)
+                    sc[j] = -1.f;
+            }
+            __syncwarp();
+        }
     }
     __syncwarp();
     // the new set, ascending: a kept index at old position p lands at
