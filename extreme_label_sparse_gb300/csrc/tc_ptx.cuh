@@ -13,6 +13,9 @@ namespace tc {
 // A bounded wait gives up after this long; the kernel then records
 // SG_ERR_TIMEOUT and winds down instead of hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// how long one try_wait may park a thread before it looks at the abort flag
+// and the clock again
+constexpr uint32_t kSuspendHintNs = 20000u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -69,29 +72,33 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
                                             int32_t *status, bool cluster)
 {
     const uint64_t t0 = global_ns();
-    while (true) {
+    for (uint32_t n = 1;; ++n) {
+        // the suspend-time hint lets the hardware park the waiting thread
+        // until the phase completes (or the hint runs out) instead of
+        // returning at once, so waiting warps do not take issue slots from
+        // working ones
         uint32_t ok;
         if (cluster)
             asm volatile(
                 "{\n\t.reg .pred p;\n\t"
-                "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
                 "selp.u32 %0, 1, 0, p;\n\t}"
                 : "=r"(ok)
-                : "r"(bar), "r"(parity)
+                : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
                 : "memory");
         else
             asm volatile(
                 "{\n\t.reg .pred p;\n\t"
-                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                 "selp.u32 %0, 1, 0, p;\n\t}"
                 : "=r"(ok)
-                : "r"(bar), "r"(parity)
+                : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
                 : "memory");
         if (ok)
             return true;
         if (*abort_flag)
             return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if ((n & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
             if (status)  // kernels without a status word only wind down
                 sg_flag(status, SG_ERR_TIMEOUT);
