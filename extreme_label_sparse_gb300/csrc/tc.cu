@@ -43,6 +43,28 @@
 
 using namespace tc;
 
+// Timeline hooks for profiling builds (-DSG_FW_TRACE): every warp of CTA 0
+// of the fused forward kernel records clock64() at marked points of its
+// groups [kFwT0, kFwT0 + kFwN) into the buffer set with sg_fw_trace_set.
+// Compiled out otherwise.
+#ifdef SG_FW_TRACE
+__device__ unsigned long long *g_fw_trace = nullptr;
+constexpr int kFwT0 = 100, kFwN = 64, kFwW = 22, kFwS = 8;
+#define FW_TRACE(slot, itv)                                                                                  \
+    do {                                                                                                     \
+        if (g_fw_trace && blockIdx.x == 0 && (itv) >= kFwT0 && (itv) < kFwT0 + kFwN && (threadIdx.x & 31) == 0) \
+            g_fw_trace[(((size_t)(threadIdx.x >> 5) * kFwN + ((itv) - kFwT0)) * kFwS) + (slot)] = clock64();   \
+    } while (0)
+extern "C" __attribute__((visibility("default"))) int sg_fw_trace_set(void *p)
+{
+    return (int)cudaMemcpyToSymbol(g_fw_trace, &p, sizeof(p));
+}
+#else
+#define FW_TRACE(slot, itv) \
+    do {                    \
+    } while (0)
+#endif
+
 namespace {
 
 constexpr int kMaxStages = 8;
@@ -431,8 +453,10 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
         GatherIdx nxt = cur;
         if (k + gridDim.x < K)
             nxt = gather_idx_of(idx_s, k + gridDim.x, F, lane);
+        FW_TRACE(0, it);
         if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status))
             break;
+        FW_TRACE(1, it);
         const uint32_t A = stage0 + (uint32_t)s * stage_bytes;
         if (t == 0) {
             mbar_arrive_expect_tx(bar_addr(c.full[s]), tma_bytes);
@@ -443,6 +467,7 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
         else
             issue_gather(hT, ldB, A, F, units, cur, lane);
         cp_async_arrive_noinc(bar_addr(c.full[s]));
+        FW_TRACE(2, it);
         cur = nxt;
     }
     cp_async_wait_all();
@@ -1026,11 +1051,14 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
             const int s = it % S;
             const int zs = it % NS;
+            FW_TRACE(0, it);
             if (!mbar_wait(bar_addr(c.tempty[zs]), ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, a.status))
                 break;
+            FW_TRACE(1, it);
             tc_fence_after();
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
+            FW_TRACE(2, it);
             tc_fence_after();
             fence_proxy_async();  // cp.async-written H_k -> the MMA (async proxy)
             if (lane == 0) {
@@ -1065,11 +1093,14 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             const int s = it % S;
             const int ws = it % NS;
             const int db = it & 1;
+            FW_TRACE(0, it);
             if (!mbar_wait(bar_addr(cf.wempty[ws]), ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, a.status))
                 break;
+            FW_TRACE(1, it);
             tc_fence_after();
             if (!mbar_wait(bar_addr(cf.dzfull[db]), (uint32_t)(it >> 1) & 1u, abort_flag, a.status))
                 break;
+            FW_TRACE(2, it);
             // H_k of this stage landed long ago (the forward MMA used it); this
             // warp sees the barrier itself before its MMAs read the cp.async data
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
@@ -1127,11 +1158,14 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     e0n = __ldg(a.gptr + k + gridDim.x);
                     e1n = __ldg(a.gptr + k + gridDim.x + 1);
                 }
+                FW_TRACE(0, it);
                 if (!mbar_wait(bar_addr(c.tfull[zs]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
                     break;
+                FW_TRACE(1, it);
                 // the dZ buffer of two groups ago must have been consumed by its dW MMA
                 if (!mbar_wait(bar_addr(cf.dzempty[db]), ((uint32_t)(it >> 1) & 1u) ^ 1u, abort_flag, a.status))
                     break;
+                FW_TRACE(2, it);
                 tc_fence_after();
                 uint8_t *zs_smem = base_ptr + (size_t)db * a.dz_bytes;
 #pragma unroll
@@ -1153,6 +1187,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     store_dz_tile<CH>(zs_smem, b, c0, v, ZSW, NZC, MT * 128);
                     store_dz_tile_f16<CH>(a.dZt + (size_t)k * a.tile_bytes, b, c0, v, ZSW, MT * 128);
                 }
+                FW_TRACE(3, it);
                 tc_fence_before();
                 mbar_arrive(bar_addr(c.tempty[zs]));
                 fence_proxy_async();  // dZ_k in shared memory -> the dW MMA (async proxy)
@@ -1181,9 +1216,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 // ---- max |W_k|
                 // the team leaves together: every named barrier below is then
                 // reached by all of its warps or by none
+                FW_TRACE(0, it);
                 if (named_bar_any(2, kFWDw * 32,
                                   !mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status)))
                     break;
+                FW_TRACE(1, it);
                 const uint4 *Wsm = reinterpret_cast<const uint4 *>(base_ptr + (stage0 - base) +
                                                                    (size_t)s * a.stage_bytes + a.a_bytes);
 #pragma unroll
@@ -1210,9 +1247,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                         }
                     }
                 }
+                FW_TRACE(2, it);
                 if (named_bar_any(2, kFWDw * 32,
                                   !mbar_wait(bar_addr(cf.wfull[ws]), (uint32_t)(it / NS) & 1u, abort_flag, a.status)))
                     break;
+                FW_TRACE(3, it);
                 tc_fence_after();
                 // the staging buffer's store of two groups ago has read it
                 if (dw == 0 && lane == 0)
@@ -1248,6 +1287,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                             stg[(c0 + i) * F + f] = bf16_rn(v[i] + w[i]);
                     }
                 }
+                FW_TRACE(4, it);
                 tc_fence_before();
                 mbar_arrive(bar_addr(cf.wempty[ws]));
                 fence_proxy_async();  // staged dW_k -> the bulk store (async proxy)
