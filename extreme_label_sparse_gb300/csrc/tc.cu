@@ -50,7 +50,7 @@ using namespace tc;
 #ifdef SG_FW_TRACE
 __device__ unsigned long long *g_fw_trace = nullptr;
 constexpr int kFwT0 = 100, kFwN = 64, kFwW = 22, kFwS = 8;
-#define FW_TRACE(slot, itv)                                                                                  \
+#define TRACE_REC(slot, itv)                                                                                 \
     do {                                                                                                     \
         if (g_fw_trace && blockIdx.x == 0 && (itv) >= kFwT0 && (itv) < kFwT0 + kFwN && (threadIdx.x & 31) == 0) \
             g_fw_trace[(((size_t)(threadIdx.x >> 5) * kFwN + ((itv) - kFwT0)) * kFwS) + (slot)] = clock64();   \
@@ -60,7 +60,19 @@ extern "C" __attribute__((visibility("default"))) int sg_fw_trace_set(void *p)
     return (int)cudaMemcpyToSymbol(g_fw_trace, &p, sizeof(p));
 }
 #else
+#define TRACE_REC(slot, itv) \
+    do {                     \
+    } while (0)
+#endif
+// the forward kernel's hooks, or (-DSG_DH_TRACE) the dh kernel's instead
+#ifdef SG_DH_TRACE
 #define FW_TRACE(slot, itv) \
+    do {                    \
+    } while (0)
+#define DH_TRACE(slot, itv) TRACE_REC(slot, itv)
+#else
+#define FW_TRACE(slot, itv) TRACE_REC(slot, itv)
+#define DH_TRACE(slot, itv) \
     do {                    \
     } while (0)
 #endif
@@ -1416,8 +1428,10 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it) {
             const int s = it % S;
             const int np = kend - k0 < P ? (int)(kend - k0) : P;
+            DH_TRACE(0, it);
             if (!mbar_wait(bar_addr(c.empty[s]), ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, a.status))
                 break;
+            DH_TRACE(1, it);
             const uint32_t st = stage0 + (uint32_t)s * a.stage_bytes;
             const uint32_t fb = bar_addr(c.full[s]);
             if (lane == 0)
@@ -1466,10 +1480,13 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it) {
             const int s = it % S;
             const int np = kend - k0 < P ? (int)(kend - k0) : P;
+            DH_TRACE(0, it);
             if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
                 break;
+            DH_TRACE(1, it);
             if (!mbar_wait(bar_addr(cd.wfull[buf]), wph, abort_flag, a.status))
                 break;
+            DH_TRACE(2, it);
             tc_fence_after();
             if (lane == 0) {
                 // A: dZ (rows = samples), B: Ws rows (dh columns); 16 j per K step
@@ -1536,7 +1553,9 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         for (int64_t k0 = kbeg + (int64_t)team * P; k0 < kend; k0 += (int64_t)NB * P, it += NB) {
             const int s = it % S;
             const int np = kend - k0 < P ? (int)(kend - k0) : P;
+            DH_TRACE(0, it);
             bool ok = mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status);
+            DH_TRACE(1, it);
             const uint8_t *st = stage0_ptr + (size_t)s * a.stage_bytes;
             // this thread's rows, read from the stage before waiting for the buffer
             uint4 row[NSLOT][NCW];
@@ -1567,10 +1586,13 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                     }
                 }
             }
+            DH_TRACE(2, it);
             // the buffer's last unit must be through its MMAs before it is rewritten
             ok = ok && mbar_wait(bar_addr(cd.wempty[team]), wph ^ 1u, abort_flag, a.status);
+            DH_TRACE(3, it);
             if (named_bar_any(1 + team, NT, !ok))
                 break;  // the whole team leaves together
+            DH_TRACE(4, it);
             // zero the rows of the buffer's last unit, then write this unit's
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
@@ -1582,6 +1604,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 }
             }
             named_bar(1 + team, NT);
+            DH_TRACE(5, it);
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
                 if (dst[x] >= 0) {
@@ -1595,6 +1618,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             }
             fence_proxy_async();  // Ws rows (generic writes) -> the MMA (async proxy)
             __syncwarp();
+            DH_TRACE(6, it);
             if (lane == 0)
                 mbar_arrive(bar_addr(cd.wfull[team]));
             wph ^= 1u;
