@@ -118,7 +118,8 @@ struct DWPlan {
 struct DhPlan {
     bool ok = false;
     int MT = 0, S = 0, zsw = 0, nbands = 0, band_w = 0, bwt = 0, nbuf = 0;
-    int gs = 0, sub = 1;  // subgroup size (<= 64) and subgroups per group
+    int gs = 0, sub = 1;  // subgroup size (<= 64) and subgroups per dZ tile
+    int idiv = 1;         // subgroups per index row (per group)
     uint32_t z_bytes = 0, w_bytes = 0, i_bytes = 0, stage_bytes = 0, ws_bytes = 0, tmem_cols = 0;
 };
 
@@ -234,19 +235,25 @@ DWPlan plan_dW(const sg_layout *lo, int B, bool split)
     return p;
 }
 
-DhPlan plan_dh(const sg_layout *lo, int B, bool split)
+// tile_g: labels per dZ workspace tile (G, or the fused forward kernel's
+// subgroup size when it ran the groups as subgroups)
+DhPlan plan_dh(const sg_layout *lo, int B, bool split, int tile_g = 0)
 {
     DhPlan p;
-    if (!shape_ok16(lo) || !dz_ok(lo->G) || lo->G > 256 || B < 1 || B > 256)
+    if (tile_g <= 0)
+        tile_g = lo->G;
+    if (!shape_ok16(lo) || !dz_ok(lo->G) || !dz_ok(tile_g) || lo->G > 256 || lo->G % tile_g != 0 || B < 1 ||
+        B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
         return p;
-    // groups of more than 64 labels run as G / 64 subgroups of 64 that share
-    // the group's I_k (dh = sum over the subgroups of dZ_sub Ws_sub)
-    const int Gs = lo->G > 64 ? 64 : lo->G;
+    // groups of more than 64 labels run as subgroups of 64 that share the
+    // group's I_k (dh = sum over the subgroups of dZ_sub Ws_sub)
+    const int Gs = tile_g > 64 ? 64 : tile_g;
     p.gs = Gs;
-    p.sub = lo->G / Gs;
+    p.sub = tile_g / Gs;      // subgroups per workspace tile
+    p.idiv = lo->G / Gs;      // subgroups per index row
     p.zsw = dz_swizzle(Gs);
     p.z_bytes = (uint32_t)(split ? 2 : 1) * 128 * p.zsw;
     p.w_bytes = (uint32_t)Gs * lo->F * 2;
@@ -450,7 +457,7 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
                                               int64_t K, const uint16_t *idx_s, const uint16_t *hT,
                                               int ldB, int F, int MT, uint32_t tma_bytes,
                                               volatile int *abort_flag, int32_t *status,
-                                              IssueTma issue_tma)
+                                              IssueTma issue_tma, int idiv = 1)
 {
     const int t = threadIdx.x;  // producer threads are 0 .. kProdWarps*32-1
     const int lane = t & 31;
@@ -458,13 +465,13 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
     int it = 0;
     GatherIdx cur = {{0u, 0u}};
     if (blockIdx.x < K)
-        cur = gather_idx_of(idx_s, blockIdx.x, F, lane);
+        cur = gather_idx_of(idx_s, blockIdx.x / idiv, F, lane);
     for (int64_t k = blockIdx.x; k < K; k += gridDim.x, ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
         GatherIdx nxt = cur;
         if (k + gridDim.x < K)
-            nxt = gather_idx_of(idx_s, k + gridDim.x, F, lane);
+            nxt = gather_idx_of(idx_s, (k + gridDim.x) / idiv, F, lane);
         FW_TRACE(0, it);
         if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status))
             break;
@@ -920,15 +927,17 @@ constexpr int kFWBudget = 224 * 1024;
 struct FWPlan {
     bool ok = false;
     int MT = 0, FT = 0, nk = 0, S = 0, zsw = 0, nzc = 0, nslot = 0;
+    int gs = 0, sub = 1;  // labels per kernel group (a subgroup sharing I_k) and subgroups per group
     uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, dz_bytes = 0, stg_bytes = 0, zcols = 0, wcols = 0,
              tmem_cols = 0, pad_bytes = 0;
 };
 
-FWPlan plan_fwdw(const sg_layout *lo, int B)
+// the plan for groups of Gv labels (Gv = G, or a subgroup size)
+FWPlan plan_fwdw_g(const sg_layout *lo, int B, int Gv)
 {
     FWPlan p;
-    if (!shape_ok(lo) || !dz_ok(lo->G) || (lo->F != 64 && lo->F != 128 && lo->F != 256) ||
-        2 * lo->G > 256 || B < 1 || B > 256)
+    if (!shape_ok(lo) || !dz_ok(Gv) || (lo->F != 64 && lo->F != 128 && lo->F != 256) ||
+        2 * Gv > 256 || B < 1 || B > 256)
         return p;
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
@@ -937,15 +946,15 @@ FWPlan plan_fwdw(const sg_layout *lo, int B)
     // lanes read the next 64 rows of shared memory and are never stored
     p.FT = (lo->F + 127) / 128;
     p.nk = lo->F / 64;
-    p.zsw = dz_swizzle(lo->G);
-    p.nzc = lo->G * 2 > 128 ? lo->G / 64 : 1;
+    p.zsw = dz_swizzle(Gv);
+    p.nzc = Gv * 2 > 128 ? Gv / 64 : 1;
     p.a_bytes = (uint32_t)p.MT * 2 * lo->F * 128;
-    p.w_bytes = (uint32_t)p.nk * lo->G * 128;
+    p.w_bytes = (uint32_t)p.nk * Gv * 128;
     p.stage_bytes = p.a_bytes + p.w_bytes;
     p.dz_bytes = 2u * (uint32_t)p.nzc * p.MT * 128 * p.zsw;  // both planes, all rows
-    p.stg_bytes = (uint32_t)lo->G * lo->F * 2;                 // dW_k staged for its store
-    p.zcols = (uint32_t)p.MT * lo->G;
-    p.wcols = (uint32_t)p.FT * 2 * lo->G;
+    p.stg_bytes = (uint32_t)Gv * lo->F * 2;                 // dW_k staged for its store
+    p.zcols = (uint32_t)p.MT * Gv;
+    p.wcols = (uint32_t)p.FT * 2 * Gv;
     p.nslot = 4 * (p.zcols + p.wcols) <= 512 ? 4 : 2;
     if (p.nslot * (p.zcols + p.wcols) > 512)
         return p;
@@ -959,6 +968,24 @@ FWPlan plan_fwdw(const sg_layout *lo, int B)
         p.S = 6;
     p.ok = p.S >= 2;
     return p;
+}
+
+// Groups whose tiles do not fit the fused kernel (G = 64 at B = 256) run as
+// subgroups of half the labels sharing the group's I_k: the kernel then sees
+// K * sub groups of G / sub labels, each with its own workspace tile.
+FWPlan plan_fwdw(const sg_layout *lo, int B)
+{
+    for (int gs = lo->G; gs >= 16 && lo->G % gs == 0; gs /= 2) {
+        FWPlan p = plan_fwdw_g(lo, B, gs);
+        if (p.ok) {
+            p.gs = gs;
+            p.sub = lo->G / gs;
+            return p;
+        }
+        if (gs % 2)
+            break;
+    }
+    return FWPlan();
 }
 
 struct FWArgs {
@@ -977,6 +1004,7 @@ struct FWArgs {
     int32_t *status;
     int64_t K, L;
     int32_t B, G, F, MT, FT, nk, S, zsw, nzc, nslot, Bp, ldB;
+    int32_t sub;  // kernel groups per layout group (they share its I_k and positive list)
     uint32_t a_bytes, w_bytes, stage_bytes, dz_bytes, stg_bytes, zcols, wcols, tmem_cols;
 };
 
@@ -1055,7 +1083,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                           const uint32_t Wt = A + a.a_bytes;
                           for (int kc = 0; kc < a.nk; ++kc)
                               tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
-                      });
+                      }, a.sub);
     } else if (warp == kProdWarps) {
         // ---------------------------------------------------------- forward MMA
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
@@ -1158,8 +1186,8 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             // positive-list bounds of the group, loaded one group ahead
             int e0n = 0, e1n = 0;
             if (blockIdx.x < a.K) {
-                e0n = __ldg(a.gptr + blockIdx.x);
-                e1n = __ldg(a.gptr + blockIdx.x + 1);
+                e0n = __ldg(a.gptr + blockIdx.x / a.sub);
+                e1n = __ldg(a.gptr + blockIdx.x / a.sub + 1);
             }
             int it = 0;
             for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
@@ -1167,9 +1195,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 const int db = it & 1;
                 const int e0 = e0n, e1 = e1n;
                 if (k + gridDim.x < a.K) {
-                    e0n = __ldg(a.gptr + k + gridDim.x);
-                    e1n = __ldg(a.gptr + k + gridDim.x + 1);
+                    e0n = __ldg(a.gptr + (k + gridDim.x) / a.sub);
+                    e1n = __ldg(a.gptr + (k + gridDim.x) / a.sub + 1);
                 }
+                // columns of the layout group this kernel group starts at
+                const int coff = (int)(k % a.sub) * G;
                 FW_TRACE(0, it);
                 if (!mbar_wait(bar_addr(c.tfull[zs]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
                     break;
@@ -1187,7 +1217,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     float v[CH];
                     tmem_ld_chunk<CH>(tbase + lane_off + (uint32_t)(zs * a.zcols + t * G + c0), v);
                     if (b < a.B) {
-                        const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, c0, CH) : 0u;
+                        const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, coff + c0, CH) : 0u;
                         lf += bce_chunk_ftz<CH>(v, y);
                     } else {
 #pragma unroll
@@ -1337,7 +1367,8 @@ struct DhArgs {
     int32_t *status;
     int64_t K, L, Kc;      // K: subgroups; Kc: subgroups per CTA (a contiguous range)
     int32_t B, G, F, H, MT, S, zsw, nbands, band_w, parts, npass, Bp, nbuf;
-    int32_t sub;           // subgroups of G (<= 64) labels per group
+    int32_t sub;           // subgroups (<= 64 labels) per dZ workspace tile
+    int32_t idiv;          // subgroups per group (they share its index row)
     uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, ws_bytes, tmem_cols;
 };
 
@@ -1458,7 +1489,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 // W_k: G contiguous rows of F
                 bulk_load(st + woff + (uint32_t)lane * a.w_bytes, a.W + k * G * F, a.w_bytes, fb);
                 // I_k: the dh column of each f (shared by the group's subgroups)
-                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + (k / a.sub) * F, (uint32_t)(2 * F), fb);
+                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + (k / a.idiv) * F, (uint32_t)(2 * F), fb);
             }
             __syncwarp();
         }
@@ -1784,7 +1815,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
         return SG_ERR_UNSUPPORTED;
     }
     CUtensorMap tm_w;
-    sg_status rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)lo->G, 128, "W");
+    sg_status rc = make_map_2d(&tm_w, W, (uint64_t)lo->F, (uint64_t)lo->L, 64, (uint32_t)p.gs, 128, "W");
     if (rc != SG_OK)
         return rc;
     FWArgs a;
@@ -1794,7 +1825,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     if (rc != SG_OK)
         return rc;
     a.dZt = dZt;
-    a.tile_bytes = tc_dz_tile_bytes(lo, B) / 2;  // one fp16 plane
+    a.tile_bytes = tc_dz_tile_bytes(lo, B) / 2 / p.sub;  // one fp16 plane of a kernel group
     a.dW = dW;
     a.wmax = lo->wmax;
     a.W = W;
@@ -1805,10 +1836,11 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.gent = lo->gent;
     a.loss_part = lo->loss_part;
     a.status = lo->status;
-    a.K = lo->K;
+    a.K = lo->K * p.sub;
+    a.sub = p.sub;
     a.L = lo->L;
     a.B = B;
-    a.G = lo->G;
+    a.G = p.gs;
     a.F = lo->F;
     a.MT = p.MT;
     a.FT = p.FT;
@@ -1829,10 +1861,10 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.tmem_cols = p.tmem_cols;
     const size_t smem =
         2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
-    const int grid = persistent_grid(lo, lo->K);
+    const int grid = persistent_grid(lo, a.K);
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
 #define SG_FW_PICK(GG, KK, MM)                                           \
-    if (lo->G == GG && lo->F == KK * 16 && p.MT == MM)                   \
+    if (p.gs == GG && lo->F == KK * 16 && p.MT == MM)                   \
         kern = sgd ? k_tc_fwdw<GG, KK, MM, true> : k_tc_fwdw<GG, KK, MM, false>;
     SG_FW_PICK(16, 4, 1) SG_FW_PICK(16, 4, 2) SG_FW_PICK(32, 4, 1) SG_FW_PICK(32, 4, 2)
     SG_FW_PICK(64, 4, 1) SG_FW_PICK(64, 4, 2)
@@ -1937,7 +1969,9 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
         return SG_ERR_INVALID;
     }
     const bool split = dZ_lo != nullptr || (dZt != nullptr && !dzt_f16);
-    const DhPlan p = plan_dh(lo, B, split);
+    // the fp16 workspace comes from the fused forward kernel, whose tiles may
+    // hold subgroups of the layout's groups
+    const DhPlan p = plan_dh(lo, B, split, dzt_f16 ? plan_fwdw(lo, B).gs : 0);
     if (!p.ok) {
         sg_set_error("tc_dh: shape not supported by the tensor-core engine");
         return SG_ERR_UNSUPPORTED;
@@ -1966,11 +2000,14 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.W = W;
     a.wmax = lo->wmax;
     a.dZt = dZt;
-    a.tile_bytes = dzt_f16 ? tc_dz_tile_bytes(lo, B) / 2 : tc_dz_tile_bytes(lo, B);
+    // one tile holds sub subgroups of gs labels (a whole group, or the fused
+    // forward kernel's subgroup)
+    a.tile_bytes = (dzt_f16 ? tc_dz_tile_bytes(lo, B) / 2 : tc_dz_tile_bytes(lo, B)) / (uint64_t)(lo->G / (p.gs * p.sub));
     a.dh = dh;
     a.status = lo->status;
-    a.K = lo->K * p.sub;  // subgroups
+    a.K = lo->K * p.idiv;  // subgroups
     a.sub = p.sub;
+    a.idiv = p.idiv;
     a.L = lo->L;
     a.B = B;
     a.G = p.gs;

@@ -48,9 +48,13 @@
  *                      G = 16, 32   G = 64   G = 128   G = 192   G = 256
  *       B <= 128          256         256       160        32      (dh only)
  *       B <= 256          192         176       144     (dh only)  (dh only)
- *   and dh does for every such G and F.  A phase outside that runs on CUDA
- *   cores (SG_ENGINE_TC makes it an error instead).  Groups of more than 64
- *   labels enter dh as subgroups of 64 sharing I_k.  Every other G
+ *   and also, through the fused forward + BCE + dW kernel (F = 64, 128 or
+ *   256), at G = 128, F = 256 (B <= 128) and at G = 256, F = 64 or 128
+ *   (F = 256 too for B <= 128).  dh runs on them for every such G and F.  A
+ *   phase outside that runs on CUDA cores (SG_ENGINE_TC makes it an error
+ *   instead).  Groups whose tiles do not fit the fused kernel run there as
+ *   subgroups of G/2 or G/4 labels sharing I_k, and groups of more than 64
+ *   labels enter dh as subgroups of at most 64.  Every other G
  *   (including G = 1, per-label fixed fan-in) runs on the CUDA-core engine.
  *   sg_step_plan reports which kernels and engines a step will use.
  */

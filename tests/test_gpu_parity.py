@@ -44,6 +44,9 @@ CASES = [
     (_w("tc_h1000", B=130, H=1000, L=32 * 40, G=32, F=128, pos=6), (SIMT, TC)),
     # B = 256 at G = 64: dW streams the two sample tiles through its stages
     (_w("g64_b256", B=256, H=768, L=64 * 30, G=64, F=128, pos=5, dist="zipf"), (SIMT, TC)),
+    # the fused kernel on subgroups sharing I_k: G = 128 at B = 256, G = 256
+    (_w("g128_b256_sub", B=256, H=512, L=128 * 12, G=128, F=128, pos=6, dist="zipf"), (SIMT, TC)),
+    (_w("g256_f64_sub", B=100, H=384, L=256 * 8, G=256, F=64, pos=6, dist="zipf"), (SIMT, TC)),
     # groups of 192 (dh as three subgroups of 64); wide H (eleven dh bands,
     # and three column windows of the CUDA-core dh)
     (_w("tc_g192_f32", B=100, H=256, L=192 * 8, G=192, F=32, pos=5), (SIMT, TC)),
@@ -247,10 +250,11 @@ _BY_NAME = {w.name: w for w, _ in CASES}
 # kernels each workload shape launches: the fused forward + BCE + dW kernel
 # and the dh kernel
 _FUSED_KINDS = {"like3m": {"prep", "fwd", "dh"}, "like8p6m": {"prep", "fwd", "dh"},
-                "like670k": {"prep", "fwd", "dh"}}
+                "like670k": {"prep", "fwd", "dh"}, "g64_b256": {"prep", "fwd", "dh"},
+                "g128_b256_sub": {"prep", "fwd", "dh"}}
 
 
-@pytest.mark.parametrize("name", ["like3m", "like670k", "like8p6m"])
+@pytest.mark.parametrize("name", ["like3m", "like670k", "like8p6m", "g64_b256", "g128_b256_sub"])
 def test_step_fused_on_tensor_cores(name, oracle_mod):
     """The shapes of the three label-space workloads run the whole step on
     the tensor cores (engine pinned: a CUDA-core fallback would raise) through
@@ -513,6 +517,9 @@ def test_call_argument_errors():
 # tensor cores, by batch class and G (the table of include/sg.h)
 _TC_MAX_F = {128: {16: 256, 32: 256, 64: 256, 128: 160, 192: 32, 256: 0},
              256: {16: 192, 32: 192, 64: 176, 128: 144, 192: 0, 256: 0}}
+# F beyond that which the fused forward + BCE + dW kernel still takes (as
+# subgroups of the group sharing I_k)
+_TC_FUSED_EXTRA = {128: {128: {256}, 256: {64, 128, 256}}, 256: {256: {64, 128}}}
 
 
 def test_step_plan_matches_documented_range():
@@ -532,7 +539,8 @@ def test_step_plan_matches_documented_range():
                 finally:
                     lay.close()
                 assert h, (B, G, F)
-                assert (f and w and h) == (F <= _TC_MAX_F[cls][G]), (B, G, F, path, f, w, h)
+                want = F <= _TC_MAX_F[cls][G] or F in _TC_FUSED_EXTRA.get(cls, {}).get(G, set())
+                assert (f and w and h) == want, (B, G, F, path, f, w, h)
 
 
 @pytest.mark.parametrize("G,F", [(128, 128), (256, 64), (256, 256)])
