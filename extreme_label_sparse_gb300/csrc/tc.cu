@@ -457,7 +457,7 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
                                               int64_t K, const uint16_t *idx_s, const uint16_t *hT,
                                               int ldB, int F, int MT, uint32_t tma_bytes,
                                               volatile int *abort_flag, int32_t *status,
-                                              IssueTma issue_tma, int idiv = 1)
+                                              IssueTma issue_tma, int ishift = 0)
 {
     const int t = threadIdx.x;  // producer threads are 0 .. kProdWarps*32-1
     const int lane = t & 31;
@@ -465,13 +465,13 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
     int it = 0;
     GatherIdx cur = {{0u, 0u}};
     if (blockIdx.x < K)
-        cur = gather_idx_of(idx_s, blockIdx.x / idiv, F, lane);
+        cur = gather_idx_of(idx_s, (int64_t)blockIdx.x >> ishift, F, lane);
     for (int64_t k = blockIdx.x; k < K; k += gridDim.x, ++it) {
         const int s = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
         GatherIdx nxt = cur;
         if (k + gridDim.x < K)
-            nxt = gather_idx_of(idx_s, (k + gridDim.x) / idiv, F, lane);
+            nxt = gather_idx_of(idx_s, (k + gridDim.x) >> ishift, F, lane);
         FW_TRACE(0, it);
         if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status))
             break;
@@ -1004,7 +1004,7 @@ struct FWArgs {
     int32_t *status;
     int64_t K, L;
     int32_t B, G, F, MT, FT, nk, S, zsw, nzc, nslot, Bp, ldB;
-    int32_t sub;  // kernel groups per layout group (they share its I_k and positive list)
+    int32_t sub_shift;  // log2 of the kernel groups per layout group (they share its I_k and positives)
     uint32_t a_bytes, w_bytes, stage_bytes, dz_bytes, stg_bytes, zcols, wcols, tmem_cols;
 };
 
@@ -1083,7 +1083,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                           const uint32_t Wt = A + a.a_bytes;
                           for (int kc = 0; kc < a.nk; ++kc)
                               tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
-                      }, a.sub);
+                      }, a.sub_shift);
     } else if (warp == kProdWarps) {
         // ---------------------------------------------------------- forward MMA
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
@@ -1186,8 +1186,8 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             // positive-list bounds of the group, loaded one group ahead
             int e0n = 0, e1n = 0;
             if (blockIdx.x < a.K) {
-                e0n = __ldg(a.gptr + blockIdx.x / a.sub);
-                e1n = __ldg(a.gptr + blockIdx.x / a.sub + 1);
+                e0n = __ldg(a.gptr + (blockIdx.x >> a.sub_shift));
+                e1n = __ldg(a.gptr + (blockIdx.x >> a.sub_shift) + 1);
             }
             int it = 0;
             for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
@@ -1195,11 +1195,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 const int db = it & 1;
                 const int e0 = e0n, e1 = e1n;
                 if (k + gridDim.x < a.K) {
-                    e0n = __ldg(a.gptr + (k + gridDim.x) / a.sub);
-                    e1n = __ldg(a.gptr + (k + gridDim.x) / a.sub + 1);
+                    e0n = __ldg(a.gptr + ((k + gridDim.x) >> a.sub_shift));
+                    e1n = __ldg(a.gptr + ((k + gridDim.x) >> a.sub_shift) + 1);
                 }
                 // columns of the layout group this kernel group starts at
-                const int coff = (int)(k % a.sub) * G;
+                const int coff = (int)(k & ((1 << a.sub_shift) - 1)) * G;
                 FW_TRACE(0, it);
                 if (!mbar_wait(bar_addr(c.tfull[zs]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
                     break;
@@ -1475,7 +1475,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 if (a.dZt) {
                     // rows [128 mt, 128 mt + 128) of the subgroup's chunk of
                     // each plane of its group's tile
-                    const int64_t kg = k / a.sub;
+                    const int64_t kg = (int64_t)((uint32_t)k / (uint32_t)a.sub);
                     const int cj = (int)(k - kg * a.sub);
                     const uint8_t *tz = a.dZt + (size_t)kg * a.tile_bytes +
                                         ((size_t)cj * a.Bp + (size_t)mt * 128) * a.zsw;
@@ -1489,7 +1489,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 // W_k: G contiguous rows of F
                 bulk_load(st + woff + (uint32_t)lane * a.w_bytes, a.W + k * G * F, a.w_bytes, fb);
                 // I_k: the dh column of each f (shared by the group's subgroups)
-                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + (k / a.idiv) * F, (uint32_t)(2 * F), fb);
+                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + (int64_t)((uint32_t)k / (uint32_t)a.idiv) * F, (uint32_t)(2 * F), fb);
             }
             __syncwarp();
         }
@@ -1837,7 +1837,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.loss_part = lo->loss_part;
     a.status = lo->status;
     a.K = lo->K * p.sub;
-    a.sub = p.sub;
+    a.sub_shift = p.sub == 4 ? 2 : p.sub == 2 ? 1 : 0;
     a.L = lo->L;
     a.B = B;
     a.G = p.gs;
