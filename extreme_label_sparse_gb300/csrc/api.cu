@@ -8,11 +8,34 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <vector>
 
 namespace {
 
 thread_local char g_err[512];
+
+// Every layout between a successful sg_layout_build and its sg_layout_free,
+// in creation order, so that sg_device_status can read their status words.
+std::mutex g_live_mu;
+std::vector<sg_layout *> g_live;
+
+void live_add(sg_layout *lo)
+{
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    g_live.push_back(lo);
+}
+
+void live_remove(sg_layout *lo)
+{
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    for (size_t i = 0; i < g_live.size(); ++i)
+        if (g_live[i] == lo) {
+            g_live.erase(g_live.begin() + (long)i);
+            return;
+        }
+}
 
 // Makes the layout's device current for the duration of a call.
 struct DeviceGuard {
@@ -274,6 +297,7 @@ sg_status sg_layout_build(const int32_t *groups, int64_t L, int32_t G,
         return rc;
     }
     lo->tc_ok = tc_supported(lo) || tc_step_ok(lo, max_B < 128 ? max_B : 128);
+    live_add(lo);
     *out = lo;
     return SG_OK;
 }
@@ -305,6 +329,7 @@ void sg_layout_free(sg_layout *lo)
 {
     if (!lo)
         return;
+    live_remove(lo);
     DeviceGuard dg(lo->device);
     cudaDeviceSynchronize();
     free_layout(lo);
@@ -352,6 +377,29 @@ sg_status sg_layout_status(sg_layout *lo, int32_t *code, int32_t clear)
     if (clear)
         SG_TRY_CUDA(cudaMemset(lo->status, 0, sizeof(int32_t)));
     SG_TRY_CUDA(cudaDeviceSynchronize());
+    return SG_OK;
+}
+
+sg_status sg_device_status(int32_t *code)
+{
+    const char *fn = "sg_device_status";
+    NvtxRange nvtx_(fn);
+    REQUIRE(code, fn);
+    *code = SG_OK;
+    int dev = 0;
+    SG_TRY_CUDA(cudaGetDevice(&dev));
+    SG_TRY_CUDA(cudaDeviceSynchronize());
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    for (sg_layout *lo : g_live) {
+        if (lo->device != dev)
+            continue;
+        int32_t c = 0;
+        SG_TRY_CUDA(cudaMemcpy(&c, lo->status, sizeof(int32_t), cudaMemcpyDeviceToHost));
+        if (c != SG_OK) {
+            *code = c;
+            break;
+        }
+    }
     return SG_OK;
 }
 

@@ -53,6 +53,7 @@ def load():
             "sg_layout_info": ([P, C.POINTER(i64), C.POINTER(i32), C.POINTER(i32),
                                 C.POINTER(i32), C.POINTER(i64)], C.c_int),
             "sg_layout_status": ([P, C.POINTER(i32), i32], C.c_int),
+            "sg_device_status": ([C.POINTER(i32)], C.c_int),
             "sg_pos_export": ([P, i32, P, P, i64, P, P, P, P, P], C.c_int),
             "sg_fwd": ([P, P, i32, P, P, P], C.c_int),
             "sg_bce_grad": ([P, P, i32, P, P, i64, P, P, P], C.c_int),
@@ -196,6 +197,14 @@ def sg_layout_set_engine(layout: Layout, engine: int):
 def sg_layout_status(layout: Layout, clear: bool = True) -> int:
     code = C.c_int32(0)
     _check(load().sg_layout_status(layout, C.byref(code), int(bool(clear))))
+    return int(code.value)
+
+
+def sg_device_status() -> int:
+    """First non-zero status word among the live layouts of the current
+    device (0 if none); reads without clearing."""
+    code = C.c_int32(0)
+    _check(load().sg_device_status(C.byref(code)))
     return int(code.value)
 
 

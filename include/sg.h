@@ -160,6 +160,14 @@ SG_API sg_status sg_layout_info(const sg_layout *layout, int64_t *L, int32_t *G,
  * Synchronous (waits for the device).  *code is an sg_status value. */
 SG_API sg_status sg_layout_status(sg_layout *layout, int32_t *code, int32_t clear);
 
+/* The device-wide view of the same words: waits for the current device, then
+ * sets *code to the first non-zero status word among the live layouts built on
+ * that device (in the order they were built), or SG_OK.  Clears nothing: a
+ * layout's word is reset with sg_layout_status(..., clear = 1).  Returns
+ * SG_ERR_INVALID for a NULL `code` and SG_ERR_CUDA if the device reports an
+ * error.  Thread-safe against concurrent build and free. */
+SG_API sg_status sg_device_status(int32_t *code);
+
 /* ---------------------------------------------------------------- positives
  * sg_pos_export -- the positive lists as the step uses them (Y of the BCE in
  * key design "head-tail split"): labels mapped to slots, sorted ascending and

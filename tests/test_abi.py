@@ -26,7 +26,8 @@ def _declared():
 def test_header_declares_the_entry_points():
     names = _declared()
     for want in ("sg_layout_build", "sg_fwd", "sg_bce_grad", "sg_bwd", "sg_fwd_bce",
-                 "sg_bwd_dW", "sg_bwd_dh", "sg_step", "sg_pos_export", "sg_layout_export"):
+                 "sg_bwd_dW", "sg_bwd_dh", "sg_step", "sg_pos_export", "sg_layout_export",
+                 "sg_device_status", "sg_last_error"):
         assert want in names
 
 

@@ -2,6 +2,8 @@
 same seeded inputs, element by element (small and ragged sizes), for both
 engines where they apply.  Bit-exact for the layout and the positive lists;
 max |gpu - ref| <= 2e-2 (1 + |ref|) for Z, dZ, dW, dh; loss within 1e-3."""
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -491,6 +493,34 @@ def test_bad_positive_label_sets_status():
     rp[3] = rp[4] + 1  # non-monotone row pointers
     sg.sg_fwd_bce(lay, d["h"], d["W"], dev_i32(rp), d["labels"], p.nnz, dZ, loss)
     assert sg.sg_layout_status(lay) == sg.SG_ERR_DATA
+    lay.close()
+
+
+def test_device_status_reports_a_layouts_word_without_clearing_it():
+    gc.collect()  # free layouts other tests left to the collector
+    if sg.sg_device_status() != 0:
+        pytest.skip("another live layout on this device already holds an error")
+    w = CONFIGS["tiny"]
+    p = generate(w)
+    good = build_layout(p)
+    bad = build_layout(p)
+    d = dev_problem(p)
+    labels = p.pos_label.copy()
+    labels[1] = w.L + 1
+    dZ = torch.empty((w.B, w.L), dtype=torch.int16, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float64, device="cuda")
+    sg.sg_fwd_bce(good, d["h"], d["W"], d["rowptr"], d["labels"], p.nnz, dZ, loss)
+    assert sg.sg_device_status() == 0
+    sg.sg_fwd_bce(bad, d["h"], d["W"], d["rowptr"], dev_i32(labels), p.nnz, dZ, loss)
+    assert sg.sg_device_status() == sg.SG_ERR_DATA
+    assert sg.sg_device_status() == sg.SG_ERR_DATA  # reading does not clear
+    assert sg.sg_layout_status(good) == 0
+    assert sg.sg_layout_status(bad) == sg.SG_ERR_DATA  # clears the word
+    assert sg.sg_device_status() == 0
+    sg.sg_fwd_bce(bad, d["h"], d["W"], d["rowptr"], dev_i32(labels), p.nnz, dZ, loss)
+    bad.close()  # a freed layout no longer counts
+    assert sg.sg_device_status() == 0
+    good.close()
 
 
 def test_call_argument_errors():
