@@ -186,6 +186,17 @@ FwdPlan plan_fwd(const sg_layout *lo, int B)
 
 int dz_swizzle(int G) { return G * 2 >= 128 ? 128 : G * 2; }
 
+// log2 of a power of two, else -1
+int log2_exact(int v)
+{
+    if (v < 1 || (v & (v - 1)))
+        return -1;
+    int l = 0;
+    while ((1 << l) < v)
+        ++l;
+    return l;
+}
+
 DWPlan plan_dW(const sg_layout *lo, int B, bool split)
 {
     DWPlan p;
@@ -445,19 +456,28 @@ __device__ __forceinline__ void issue_gather_t(const uint16_t *hT, int ldB, uint
     }
 }
 
+// nothing to do after a group's copies are issued
+struct NoAfterIssue {
+    __device__ bool operator()(int, uint32_t) const { return true; }
+};
+
 // Producer loop shared by the forward and the weight gradient: per group, one
 // thread arms the stage barrier with the TMA bytes (`tma_bytes`, issued by
 // `issue_tma`), every producer thread copies its share of H_k and has the
 // copy hardware arrive on the stage barrier once its copies land, so the
 // producers run ahead as far as free stages allow.  The cp.async writes are
 // generic-proxy writes: every MMA warp fences (proxy.async) after it has seen
-// the stage barrier and before its MMAs read the stage.
-template <int F_ = 0, int U_ = 0, typename IssueTma>
+// the stage barrier and before its MMAs read the stage.  `after(s, ph)` runs
+// once per group, with the group's stage and phase, right after the copies of
+// the next group are issued (the last group's after the loop); it returns
+// false if a wait in it gave up.
+template <int F_ = 0, int U_ = 0, typename IssueTma, typename AfterIssue = NoAfterIssue>
 __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t stage_bytes, int S,
                                               int64_t K, const uint16_t *idx_s, const uint16_t *hT,
                                               int ldB, int F, int MT, uint32_t tma_bytes,
                                               volatile int *abort_flag, int32_t *status,
-                                              IssueTma issue_tma, int ishift = 0)
+                                              IssueTma issue_tma, int ishift = 0,
+                                              AfterIssue after = AfterIssue())
 {
     const int t = threadIdx.x;  // producer threads are 0 .. kProdWarps*32-1
     const int lane = t & 31;
@@ -466,9 +486,12 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
     GatherIdx cur = {{0u, 0u}};
     if (blockIdx.x < K)
         cur = gather_idx_of(idx_s, (int64_t)blockIdx.x >> ishift, F, lane);
-    for (int64_t k = blockIdx.x; k < K; k += gridDim.x, ++it) {
-        const int s = it % S;
-        const uint32_t ph = (uint32_t)(it / S) & 1u;
+    Ring r;
+    int prev_s = 0;
+    uint32_t prev_ph = 0;
+    for (int64_t k = blockIdx.x; k < K; k += gridDim.x, ++it, r.next(S)) {
+        const int s = r.i;
+        const uint32_t ph = r.ph;
         GatherIdx nxt = cur;
         if (k + gridDim.x < K)
             nxt = gather_idx_of(idx_s, (k + gridDim.x) >> ishift, F, lane);
@@ -488,7 +511,15 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
         cp_async_arrive_noinc(bar_addr(c.full[s]));
         FW_TRACE(2, it);
         cur = nxt;
+        if (it > 0 && !after(prev_s, prev_ph)) {
+            ++it;
+            break;
+        }
+        prev_s = s;
+        prev_ph = ph;
     }
+    if (it > 0 && !*abort_flag)
+        after(prev_s, prev_ph);
     cp_async_wait_all();
     if (*abort_flag) {
         // wait (bounded) for the TMA bytes of the stages still in flight
@@ -1045,13 +1076,19 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     const int F = a.F, S = a.S, NS = a.nslot;
     constexpr uint32_t zrows = (uint32_t)MT * 128;
     constexpr uint32_t zchunk = zrows * (uint32_t)ZSW;
+    // the stage geometry follows from the shape: H_k (MT sample tiles of
+    // 2 x 64 samples x F rows) then W_k (F/64 chunks of G rows x 128 bytes)
+    constexpr uint32_t kABytes = (uint32_t)MT * 2 * FK * 16 * 128;
+    constexpr uint32_t kWBytes = (uint32_t)((FK + 3) / 4) * G_ * 128;
+    constexpr uint32_t kDzBytes = 2u * NZC * MT * 128 * ZSW;
     const uint32_t wbase = (uint32_t)NS * a.zcols;  // first dW accumulator column
 
     // the epilogue is two teams: the BCE warps turn Z_k into dZ_k, the dW
-    // warps store dW of the group and take max |W_k|.  A stage is freed by the
-    // dW MMA (last reader of H_k) and by the dW warps (last readers of W_k).
+    // warps store dW of the group.  A stage is freed by the dW MMA (last
+    // reader of H_k) and by the producer warps, which take max |W_k| from it
+    // one group after they issued its copies.
     if (threadIdx.x == 0) {
-        setup_ctl(c, S, 0, kProdWarps * 32 + 1, 2);
+        setup_ctl(c, S, 0, kProdWarps * 32 + 1, kProdWarps + 1);
         for (int i = 0; i < NS && i < 4; ++i) {
             mbar_init(bar_addr(c.tfull[i]), 1);
             mbar_init(bar_addr(c.tempty[i]), kFWBce * 32);
@@ -1078,43 +1115,78 @@ __global__ void __launch_bounds__(kFWThreads, 1)
 
     if (warp < kProdWarps) {
         // ---------------------------------------------------------- producers
-        producer_loop<FK * 16, MT * 16>(c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes,
-                      abort_flag, a.status, [&](int64_t k, uint32_t A, uint32_t fb) {
-                          const uint32_t Wt = A + a.a_bytes;
-                          for (int kc = 0; kc < a.nk; ++kc)
-                              tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
-                      }, a.sub_shift);
+        // After issuing a group's copies the producers take max |W| over the
+        // previous group's W_k (the scale of the feature gradient's fp16
+        // operands; that group's copies have landed by then) and release its
+        // stage, so no epilogue warp holds a stage.
+        uint32_t wmag = 0;  // running max of |W| bits, two bf16 lanes
+        const int t = threadIdx.x;
+        producer_loop<FK * 16, MT * 16>(
+            c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes, abort_flag, a.status,
+            [&](int64_t k, uint32_t A, uint32_t fb) {
+                const uint32_t Wt = A + a.a_bytes;
+                for (int kc = 0; kc < a.nk; ++kc)
+                    tma_load_2d(Wt + (uint32_t)kc * G * 128, &tm_w, kc * 64, (int)(k * G), fb);
+            },
+            a.sub_shift,
+            [&](int sj, uint32_t phj) -> bool {
+                if (!mbar_wait(bar_addr(c.full[sj]), phj, abort_flag, a.status))
+                    return false;
+                const uint4 *Wsm = reinterpret_cast<const uint4 *>(base_ptr + (stage0 - base) +
+                                                                   (size_t)sj * a.stage_bytes + kABytes);
+#pragma unroll
+                for (int x = t; x < (int)(kWBytes / 16); x += kProdWarps * 32) {
+                    const uint4 v = Wsm[x];
+                    wmag = __vmaxu2(wmag, v.x & 0x7fff7fffu);
+                    wmag = __vmaxu2(wmag, v.y & 0x7fff7fffu);
+                    wmag = __vmaxu2(wmag, v.z & 0x7fff7fffu);
+                    wmag = __vmaxu2(wmag, v.w & 0x7fff7fffu);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar_addr(c.empty[sj]));  // done with the stage's W_k
+                return true;
+            });
+        wmag = max(wmag & 0xffffu, wmag >> 16);
+        for (int o = 16; o > 0; o >>= 1)
+            wmag = max(wmag, __shfl_xor_sync(0xffffffffu, wmag, o));
+        if (lane == 0)
+            atomicMax(a.wmax, wmag);
     } else if (warp == kProdWarps) {
         // ---------------------------------------------------------- forward MMA
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
         int it = 0;
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            const int s = it % S;
-            const int zs = it % NS;
+        Ring rs, rz;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rs.next(S), rz.next(NS)) {
+            const int s = rs.i;
+            const int zs = rz.i;
             FW_TRACE(0, it);
-            if (!mbar_wait(bar_addr(c.tempty[zs]), ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.tempty[zs]), rz.ph ^ 1u, abort_flag, a.status))
                 break;
             FW_TRACE(1, it);
             tc_fence_after();
-            if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.full[s]), rs.ph, abort_flag, a.status))
                 break;
             FW_TRACE(2, it);
             tc_fence_after();
             fence_proxy_async();  // cp.async-written H_k -> the MMA (async proxy)
             if (lane == 0) {
-                const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
-                const uint32_t Wt = A + a.a_bytes;
+                // one thread issues an MMA about every 100 cycles at best, and
+                // address arithmetic between the MMAs adds to that: the
+                // descriptors are the stage's base descriptor plus constants.
+                // A descriptor's address field is addr >> 4 (below 2^14 for
+                // any shared address), so an offset adds to the whole word.
+                const uint32_t A = stage0 + (uint32_t)s * (kABytes + kWBytes);
+                const uint64_t ad0 = sdesc(A, (uint32_t)FK * 2048, 1024, kLayoutSW128);
+                const uint64_t bd0 = sdesc(A + kABytes, 16, 1024, kLayoutSW128);
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
                     const uint32_t d = tbase + (uint32_t)(zs * a.zcols + t * G);
 #pragma unroll
-                    for (int st = 0; st < FK; ++st) {
-                        const uint64_t ad = sdesc(A + (uint32_t)t * 2 * FK * 2048 + (uint32_t)st * 2048,
-                                                  (uint32_t)FK * 2048, 1024, kLayoutSW128);
-                        const uint64_t bd = sdesc(Wt + (uint32_t)(st / 4) * G * 128 + (uint32_t)(st % 4) * 32,
-                                                  16, 1024, kLayoutSW128);
-                        mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
-                    }
+                    for (int st = 0; st < FK; ++st)
+                        mma_bf16(d, ad0 + (uint64_t)(((uint32_t)t * 2 * FK * 2048 + (uint32_t)st * 2048) >> 4),
+                                 bd0 + (uint64_t)(((uint32_t)(st / 4) * G * 128 + (uint32_t)(st % 4) * 32) >> 4),
+                                 idesc, st > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_addr(c.tfull[zs]));
             }
@@ -1129,12 +1201,13 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         const uint32_t zlayout = layout_for_swizzle(ZSW);
         const uint32_t idesc = idesc_bf16(128, 2 * G, 0, 1);  // N = [hi | lo] along j
         int it = 0;
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            const int s = it % S;
-            const int ws = it % NS;
+        Ring rs, rw;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rs.next(S), rw.next(NS)) {
+            const int s = rs.i;
+            const int ws = rw.i;
             const int db = it & 1;
             FW_TRACE(0, it);
-            if (!mbar_wait(bar_addr(cf.wempty[ws]), ((uint32_t)(it / NS) & 1u) ^ 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(cf.wempty[ws]), rw.ph ^ 1u, abort_flag, a.status))
                 break;
             FW_TRACE(1, it);
             tc_fence_after();
@@ -1143,24 +1216,25 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             FW_TRACE(2, it);
             // H_k of this stage landed long ago (the forward MMA used it); this
             // warp sees the barrier itself before its MMAs read the cp.async data
-            if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.full[s]), rs.ph, abort_flag, a.status))
                 break;
             tc_fence_after();
             fence_proxy_async();
             if (lane == 0) {
-                const uint32_t A = stage0 + (uint32_t)s * a.stage_bytes;
-                const uint32_t Zs = base + (uint32_t)db * a.dz_bytes;
+                // base descriptors plus constants (as above)
+                constexpr int NT = (FK + 7) / 8, NKS = MT * 8;
+                const uint32_t A = stage0 + (uint32_t)s * (kABytes + kWBytes);
+                const uint64_t ad0 = sdesc(A, 16, 1024, kLayoutSW128);
+                const uint64_t bd0 = sdesc(base + (uint32_t)db * kDzBytes, zchunk, 8 * ZSW, zlayout);
 #pragma unroll
-                for (int tf = 0; tf < (FK + 7) / 8; ++tf) {
+                for (int tf = 0; tf < NT; ++tf) {
                     const uint32_t d = tbase + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G);
 #pragma unroll
-                    for (int st = 0; st < MT * 8; ++st) {
-                        const uint64_t ad = sdesc(A + (uint32_t)(st / 4) * FK * 2048 + (uint32_t)tf * 128 * 128 +
-                                                      (uint32_t)(st % 4) * 32,
-                                                  16, 1024, kLayoutSW128);
-                        const uint64_t bd = sdesc(Zs + (uint32_t)st * 16 * ZSW, zchunk, 8 * ZSW, zlayout);
-                        mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
-                    }
+                    for (int st = 0; st < NKS; ++st)
+                        mma_bf16(d,
+                                 ad0 + (uint64_t)(((uint32_t)(st / 4) * FK * 2048 + (uint32_t)tf * 128 * 128 +
+                                                   (uint32_t)(st % 4) * 32) >> 4),
+                                 bd0 + (uint64_t)(((uint32_t)st * 16 * ZSW) >> 4), idesc, st > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_addr(cf.wfull[ws]));
                 mma_commit(bar_addr(cf.dzempty[db]));
@@ -1190,8 +1264,9 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 e1n = __ldg(a.gptr + (blockIdx.x >> a.sub_shift) + 1);
             }
             int it = 0;
-            for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-                const int zs = it % NS;
+            Ring rz;
+            for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rz.next(NS)) {
+                const int zs = rz.i;
                 const int db = it & 1;
                 const int e0 = e0n, e1 = e1n;
                 if (k + gridDim.x < a.K) {
@@ -1201,7 +1276,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 // columns of the layout group this kernel group starts at
                 const int coff = (int)(k & ((1 << a.sub_shift) - 1)) * G;
                 FW_TRACE(0, it);
-                if (!mbar_wait(bar_addr(c.tfull[zs]), (uint32_t)(it / NS) & 1u, abort_flag, a.status))
+                if (!mbar_wait(bar_addr(c.tfull[zs]), rz.ph, abort_flag, a.status))
                     break;
                 FW_TRACE(1, it);
                 // the dZ buffer of two groups ago must have been consumed by its dW MMA
@@ -1243,39 +1318,17 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         } else {
             // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
             // staged in shared memory as [j][f] and stored with one bulk copy.
-            // Before that, the warps take max |W| over the stage's W_k (the
-            // scale of the feature gradient's fp16 operands).
+            // The team leaves together: every named barrier below is then
+            // reached by all of its warps or by none.
             const int dw = ew - kFWBce;  // 0 .. kFWDw-1
             constexpr int wunits = ((FK + 7) / 8) * (G / CH);
-            constexpr int WU = G * FK * 2 / kFWDw / 32;  // 16-byte units of W_k per thread
-            uint32_t wmag = 0;  // running max of |W| bits, two bf16 lanes
             int it = 0;
-            for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-                const int s = it % S;
-                const int ws = it % NS;
+            Ring rw;
+            for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rw.next(NS)) {
+                const int ws = rw.i;
                 const int wb = it & 1;
                 uint16_t *stg = reinterpret_cast<uint16_t *>(base_ptr + 2 * (size_t)a.dz_bytes + (size_t)wb * a.stg_bytes);
-                // ---- max |W_k|
-                // the team leaves together: every named barrier below is then
-                // reached by all of its warps or by none
                 FW_TRACE(0, it);
-                if (named_bar_any(2, kFWDw * 32,
-                                  !mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status)))
-                    break;
-                FW_TRACE(1, it);
-                const uint4 *Wsm = reinterpret_cast<const uint4 *>(base_ptr + (stage0 - base) +
-                                                                   (size_t)s * a.stage_bytes + a.a_bytes);
-#pragma unroll
-                for (int x = 0; x < WU; ++x) {
-                    const uint4 v = Wsm[(x * kFWDw + dw) * 32 + lane];
-                    wmag = __vmaxu2(wmag, v.x & 0x7fff7fffu);
-                    wmag = __vmaxu2(wmag, v.y & 0x7fff7fffu);
-                    wmag = __vmaxu2(wmag, v.z & 0x7fff7fffu);
-                    wmag = __vmaxu2(wmag, v.w & 0x7fff7fffu);
-                }
-                named_bar(2, kFWDw * 32);
-                if (dw == 0 && lane == 0)
-                    mbar_arrive(bar_addr(c.empty[s]));  // done with the stage's W_k
                 // ---- dW_k
                 if (SGD) {
                     // the optimiser step's rows of m and W into L2 while the
@@ -1289,11 +1342,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                         }
                     }
                 }
-                FW_TRACE(2, it);
+                FW_TRACE(1, it);
                 if (named_bar_any(2, kFWDw * 32,
-                                  !mbar_wait(bar_addr(cf.wfull[ws]), (uint32_t)(it / NS) & 1u, abort_flag, a.status)))
+                                  !mbar_wait(bar_addr(cf.wfull[ws]), rw.ph, abort_flag, a.status)))
                     break;
-                FW_TRACE(3, it);
+                FW_TRACE(2, it);
                 tc_fence_after();
                 // the staging buffer's store of two groups ago has read it
                 if (dw == 0 && lane == 0)
@@ -1329,7 +1382,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                             stg[(c0 + i) * F + f] = bf16_rn(v[i] + w[i]);
                     }
                 }
-                FW_TRACE(4, it);
+                FW_TRACE(3, it);
                 tc_fence_before();
                 mbar_arrive(bar_addr(cf.wempty[ws]));
                 fence_proxy_async();  // staged dW_k -> the bulk store (async proxy)
@@ -1339,11 +1392,6 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     bulk_commit();
                 }
             }
-            wmag = max(wmag & 0xffffu, wmag >> 16);
-            for (int o = 16; o > 0; o >>= 1)
-                wmag = max(wmag, __shfl_xor_sync(0xffffffffu, wmag, o));
-            if (lane == 0)
-                atomicMax(a.wmax, wmag);
             if (dw == 0 && lane == 0)
                 bulk_wait<0>();  // every dW store has landed
         }
@@ -1369,6 +1417,7 @@ struct DhArgs {
     int32_t B, G, F, H, MT, S, zsw, nbands, band_w, parts, npass, Bp, nbuf;
     int32_t sub;           // subgroups (<= 64 labels) per dZ workspace tile
     int32_t idiv;          // subgroups per group (they share its index row)
+    int32_t sub_shift, idiv_shift;  // log2 of sub and idiv where they are powers of two, else -1
     uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, ws_bytes, tmem_cols;
 };
 
@@ -1456,11 +1505,12 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         int it = 0;
-        for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it) {
-            const int s = it % S;
+        Ring rs;
+        for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it, rs.next(S)) {
+            const int s = rs.i;
             const int np = kend - k0 < P ? (int)(kend - k0) : P;
             DH_TRACE(0, it);
-            if (!mbar_wait(bar_addr(c.empty[s]), ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.empty[s]), rs.ph ^ 1u, abort_flag, a.status))
                 break;
             DH_TRACE(1, it);
             const uint32_t st = stage0 + (uint32_t)s * a.stage_bytes;
@@ -1475,7 +1525,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 if (a.dZt) {
                     // rows [128 mt, 128 mt + 128) of the subgroup's chunk of
                     // each plane of its group's tile
-                    const int64_t kg = (int64_t)((uint32_t)k / (uint32_t)a.sub);
+                    const int64_t kg = a.sub_shift >= 0 ? (k >> a.sub_shift) : (int64_t)((uint32_t)k / (uint32_t)a.sub);
                     const int cj = (int)(k - kg * a.sub);
                     const uint8_t *tz = a.dZt + (size_t)kg * a.tile_bytes +
                                         ((size_t)cj * a.Bp + (size_t)mt * 128) * a.zsw;
@@ -1489,7 +1539,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 // W_k: G contiguous rows of F
                 bulk_load(st + woff + (uint32_t)lane * a.w_bytes, a.W + k * G * F, a.w_bytes, fb);
                 // I_k: the dh column of each f (shared by the group's subgroups)
-                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + (int64_t)((uint32_t)k / (uint32_t)a.idiv) * F, (uint32_t)(2 * F), fb);
+                const int64_t ki = a.idiv_shift >= 0 ? (k >> a.idiv_shift) : (int64_t)((uint32_t)k / (uint32_t)a.idiv);
+                bulk_load(st + ioff + (uint32_t)lane * a.i_bytes, a.idx_s + ki * F, (uint32_t)(2 * F), fb);
             }
             __syncwarp();
         }
@@ -1508,11 +1559,12 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                                                      : idesc_bf16(128, N1 > 0 ? N1 : 16, 0, 0);
         int it = 0, buf = 0;
         uint32_t wph = 0;
-        for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it) {
-            const int s = it % S;
+        Ring rs;
+        for (int64_t k0 = kbeg; k0 < kend; k0 += P, ++it, rs.next(S)) {
+            const int s = rs.i;
             const int np = kend - k0 < P ? (int)(kend - k0) : P;
             DH_TRACE(0, it);
-            if (!mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.full[s]), rs.ph, abort_flag, a.status))
                 break;
             DH_TRACE(1, it);
             if (!mbar_wait(bar_addr(cd.wfull[buf]), wph, abort_flag, a.status))
@@ -1579,13 +1631,23 @@ __global__ void __launch_bounds__(kDhThreads, 1)
 #pragma unroll
         for (int x = 0; x < NSLOT; ++x)
             prev[x] = -1;
+        // (group, feature) of each slot: fixed per thread
+        int gsl[NSLOT], fsl[NSLOT];
+#pragma unroll
+        for (int x = 0; x < NSLOT; ++x) {
+            const int e = tt + x * NT;
+            gsl[x] = e / F;
+            fsl[x] = e - gsl[x] * F;
+        }
         int it = team;
         uint32_t wph = 0;
+        // stage and phase of unit `it`, advanced by NB units per turn
+        int s = team % S;
+        uint32_t sph = (uint32_t)(team / S) & 1u;
         for (int64_t k0 = kbeg + (int64_t)team * P; k0 < kend; k0 += (int64_t)NB * P, it += NB) {
-            const int s = it % S;
             const int np = kend - k0 < P ? (int)(kend - k0) : P;
             DH_TRACE(0, it);
-            bool ok = mbar_wait(bar_addr(c.full[s]), (uint32_t)(it / S) & 1u, abort_flag, a.status);
+            bool ok = mbar_wait(bar_addr(c.full[s]), sph, abort_flag, a.status);
             DH_TRACE(1, it);
             const uint8_t *st = stage0_ptr + (size_t)s * a.stage_bytes;
             // this thread's rows, read from the stage before waiting for the buffer
@@ -1594,8 +1656,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
                 dst[x] = -1;
-                const int e = tt + x * NT;
-                const int g = e / F, f = e - g * F;
+                const int g = gsl[x], f = fsl[x];
                 if (ok && g < np && x * NT < P * F) {
                     const int i = (int)reinterpret_cast<const uint16_t *>(st + ioff + (size_t)g * a.i_bytes)[f] - i0;
                     if (i >= 0 && i < BW) {
@@ -1653,6 +1714,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             if (lane == 0)
                 mbar_arrive(bar_addr(cd.wfull[team]));
             wph ^= 1u;
+            for (s += NB; s >= S; s -= S)
+                sph ^= 1u;
         }
         // the accumulator (lanes = samples, columns = the band's dh columns)
         // holds this CTA's partial: add it in, transposed through shared memory
@@ -1812,6 +1875,12 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     const FWPlan p = plan_fwdw(lo, B);
     if (!p.ok) {
         sg_set_error("tc_fwdw: shape not supported by the fused forward + dW kernel");
+        return SG_ERR_UNSUPPORTED;
+    }
+    // the kernel derives its stage and dZ buffer sizes from its template shape
+    if (p.stage_bytes != (uint32_t)p.MT * 2 * lo->F * 128 + (uint32_t)(lo->F / 64) * p.gs * 128 ||
+        p.dz_bytes != 2u * (uint32_t)p.nzc * p.MT * 128 * p.zsw || p.zsw != dz_swizzle(p.gs)) {
+        sg_set_error("tc_fwdw: internal error: plan and kernel disagree on the stage layout");
         return SG_ERR_UNSUPPORTED;
     }
     CUtensorMap tm_w;
@@ -2008,6 +2077,8 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     a.K = lo->K * p.idiv;  // subgroups
     a.sub = p.sub;
     a.idiv = p.idiv;
+    a.sub_shift = log2_exact(p.sub);
+    a.idiv_shift = log2_exact(p.idiv);
     a.L = lo->L;
     a.B = B;
     a.G = p.gs;

@@ -29,6 +29,22 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
+// Slot of a ring of n buffers and the parity of the current pass over it,
+// advanced once per group: cheaper than deriving both from the group counter
+// (it % n, it / n), since an integer division by a run-time divisor is a
+// sequence of some twenty instructions.
+struct Ring {
+    int i = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int n)
+    {
+        if (++i == n) {
+            i = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
