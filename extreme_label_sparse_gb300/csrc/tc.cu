@@ -961,6 +961,9 @@ struct FWPlan {
     int gs = 0, sub = 1;  // labels per kernel group (a subgroup sharing I_k) and subgroups per group
     uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, dz_bytes = 0, stg_bytes = 0, zcols = 0, wcols = 0,
              tmem_cols = 0, pad_bytes = 0;
+    // the fp16 dZ tile staged in shared memory (two buffers) and bulk-stored,
+    // where that costs no stage; 0: the epilogue stores it to global memory
+    uint32_t f16_bytes = 0;
 };
 
 // the plan for groups of Gv labels (Gv = G, or a subgroup size)
@@ -998,6 +1001,19 @@ FWPlan plan_fwdw_g(const sg_layout *lo, int B, int Gv)
     if (p.S > 6)
         p.S = 6;
     p.ok = p.S >= 2;
+    // two staging buffers for the fp16 tile when the stages still fit: the
+    // epilogue's 16-byte global stores of the tile measured ~10 % of the
+    // kernel's time at B <= 128, F >= 128 (3M shape: 4.5 % faster with one
+    // bulk store per group); with F = 64 or two sample tiles the groups are
+    // shorter and the dW MMA warp's wait for the store's reads measured 1-3 %
+    // slower, so those keep the direct stores
+    const uint32_t f16 = (uint32_t)p.nzc * p.MT * 128 * p.zsw;
+    const long room2 = room - 2l * f16;
+    const int S2 = room2 > 0 ? (int)(room2 / p.stage_bytes) : 0;
+    if (p.ok && p.MT == 1 && lo->F >= 128 && S2 >= 2 && S2 >= (p.S < 4 ? p.S : 4)) {
+        p.f16_bytes = f16;
+        p.S = S2 > 6 ? 6 : S2;
+    }
     return p;
 }
 
@@ -1037,6 +1053,7 @@ struct FWArgs {
     int32_t B, G, F, MT, FT, nk, S, zsw, nzc, nslot, Bp, ldB;
     int32_t sub_shift;  // log2 of the kernel groups per layout group (they share its I_k and positives)
     uint32_t a_bytes, w_bytes, stage_bytes, dz_bytes, stg_bytes, zcols, wcols, tmem_cols;
+    uint32_t f16_bytes;  // fp16 tile staging buffer (0: stored from registers)
 };
 
 // the common control block (stages; tfull/tempty = Z accumulators; drain of
@@ -1069,9 +1086,10 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
     uint8_t *base_ptr = dsm + (base - smem_u32(dsm));
-    // [dZ_k buffer 0][dZ_k buffer 1][dW_k staging 0, 1][stages]
+    // [dZ_k buffer 0][dZ_k buffer 1][dW_k staging 0, 1][fp16 tile staging 0, 1][stages]
     const uint32_t stg0 = base + 2 * a.dz_bytes;
-    const uint32_t stage0 = stg0 + 2 * a.stg_bytes;
+    const uint32_t f160 = stg0 + 2 * a.stg_bytes;  // fp16 tile staging (two buffers, or none)
+    const uint32_t stage0 = f160 + 2 * a.f16_bytes;
     constexpr int G = G_;
     const int F = a.F, S = a.S, NS = a.nslot;
     constexpr uint32_t zrows = (uint32_t)MT * 128;
@@ -1220,6 +1238,12 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 break;
             tc_fence_after();
             fence_proxy_async();
+            if (lane == 0 && a.f16_bytes) {
+                // the staged fp16 tile to the workspace; its shared-memory
+                // reads are waited for before the buffer is released (dzempty)
+                bulk_store(a.dZt + (size_t)k * a.tile_bytes, f160 + (uint32_t)db * a.f16_bytes, a.f16_bytes);
+                bulk_commit();
+            }
             if (lane == 0) {
                 // base descriptors plus constants (as above)
                 constexpr int NT = (FK + 7) / 8, NKS = MT * 8;
@@ -1237,13 +1261,18 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                                  bd0 + (uint64_t)(((uint32_t)st * 16 * ZSW) >> 4), idesc, st > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_addr(cf.wfull[ws]));
+                if (a.f16_bytes)
+                    bulk_wait_read<0>();  // the fp16 tile store has read the buffer
                 mma_commit(bar_addr(cf.dzempty[db]));
                 mma_commit(bar_addr(c.empty[s]));  // last reader of the stage's H_k
             }
             __syncwarp();
         }
-        if (lane == 0)
+        if (lane == 0) {
+            if (a.f16_bytes)
+                bulk_wait<0>();  // every fp16 tile store has landed
             mma_commit(bar_addr(cf.wdrain[0]));
+        }
         __syncwarp();
         mbar_wait_drain(bar_addr(cf.wdrain[0]), 0);
     } else {
@@ -1302,7 +1331,11 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     // bf16 value + residual planes for the dW MMA; the fp16
                     // tile for the feature gradient straight to the workspace
                     store_dz_tile<CH>(zs_smem, b, c0, v, ZSW, NZC, MT * 128);
-                    store_dz_tile_f16<CH>(a.dZt + (size_t)k * a.tile_bytes, b, c0, v, ZSW, MT * 128);
+                    if (a.f16_bytes)  // bulk-stored by the dW MMA warp
+                        store_dz_tile_f16<CH>(base_ptr + (f160 - base) + (size_t)db * a.f16_bytes, b, c0, v, ZSW,
+                                              MT * 128);
+                    else
+                        store_dz_tile_f16<CH>(a.dZt + (size_t)k * a.tile_bytes, b, c0, v, ZSW, MT * 128);
                 }
                 FW_TRACE(3, it);
                 tc_fence_before();
@@ -1928,8 +1961,10 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.zcols = p.zcols;
     a.wcols = p.wcols;
     a.tmem_cols = p.tmem_cols;
-    const size_t smem =
-        2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
+    // the staged tile is the kernel group's whole workspace tile
+    a.f16_bytes = (uint64_t)p.f16_bytes == a.tile_bytes ? p.f16_bytes : 0u;
+    const size_t smem = 2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + 2 * (size_t)p.f16_bytes +
+                        (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
     const int grid = persistent_grid(lo, a.K);
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
 #define SG_FW_PICK(GG, KK, MM)                                           \
