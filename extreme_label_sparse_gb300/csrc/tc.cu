@@ -86,9 +86,10 @@ constexpr int kProdWarps = 8;  // cp.async gather + TMA issue (8: measured ~2x t
 // forward / dW: producers, two MMA-issuing warps, epilogue
 constexpr int kFwdThreads = 32 * (kProdWarps + 2 + kEpiWarps);
 constexpr int kFirstEpi = kProdWarps + 2;
-// dh: one load warp, one MMA warp, twelve builder warps (one thread per
-// dh column of a band of up to 384)
-constexpr int kDhBuilders = 12;
+// dh: one load warp, one MMA warp, sixteen builder warps in two teams of
+// eight (a team thread per (group, feature) slot of a unit: 2 x 128 at the
+// 3M shape, so the slots spread evenly; teams of six measured slower)
+constexpr int kDhBuilders = 16;
 constexpr int kDhMaxBuf = 3;  // scattered-W buffers in shared memory (one per builder team)
 // groups per pipeline unit (one stage, one scattered-W buffer): a stage's
 // round trip costs about the same from 2 KB to 32 KB of loads, so each stage
@@ -292,8 +293,8 @@ DhPlan plan_dh(const sg_layout *lo, int B, bool split, int tile_g = 0)
     p.tmem_cols = pow2_cols(p.band_w);
     if (p.S > kMaxStages)
         p.S = kMaxStages;
-    // the flush transposes through 12 x 33 x 32 floats of shared memory
-    p.ok = p.S >= 2 && (long)p.nbuf * p.ws_bytes + (long)p.S * p.stage_bytes >= 12l * 33 * 32 * 4;
+    // the flush transposes through kDhBuilders x 33 x 32 floats of shared memory
+    p.ok = p.S >= 2 && (long)p.nbuf * p.ws_bytes + (long)p.S * p.stage_bytes >= (long)kDhBuilders * 33 * 32 * 4;
     return p;
 }
 
@@ -1483,6 +1484,29 @@ struct CtlDh {
 // workspace) and the builders write W_k as fp16, scaled by 2^-s so that the
 // step's largest |W| stays finite (s = 0 unless |W| >= 2^15); the flush
 // scales the sums back by 2^s.
+// Column f of a staged W_k ([G][F] row-major, bf16) as one Ws row: G values
+// packed in 16-byte units, as bf16, or as fp16 (times `down` when SCALED;
+// unscaled when the step's largest |W| is below 2^15, which spares a multiply
+// per value)
+template <int NCW, bool F16, bool SCALED>
+__device__ __forceinline__ void read_w_column(const uint16_t *Wk, int F, float down, uint4 (&row)[NCW])
+{
+#pragma unroll
+    for (int u = 0; u < NCW; ++u) {
+        uint32_t w[4];
+#pragma unroll
+        for (int c2 = 0; c2 < 4; ++c2) {
+            const uint32_t lo = Wk[(8 * u + 2 * c2) * F], hi = Wk[(8 * u + 2 * c2 + 1) * F];
+            if (F16)
+                w[c2] = SCALED ? pack2_f16(__uint_as_float(lo << 16) * down, __uint_as_float(hi << 16) * down)
+                               : pack2_f16(__uint_as_float(lo << 16), __uint_as_float(hi << 16));
+            else
+                w[c2] = lo | (hi << 16);
+        }
+        row[u] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 template <int NPASS, int NKS, int BWT, bool F16>
 __global__ void __launch_bounds__(kDhThreads, 1)
     k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
@@ -1638,14 +1662,15 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         mbar_wait_drain(bar_addr(c.drain[0]), 0);  // no MMA in flight at the dealloc
     } else {
         // ---------------------------------------------------------- builders
-        // NB teams of 12 / NB warps take turns at the units (team t: units t,
-        // t + NB, ..., always Ws buffer t), so the teams build concurrently
-        // while the MMAs consume.  Team thread tt handles the slots e = tt,
-        // tt + NT, ... of the unit's P x F (group g = e / F, feature f = e % F).
+        // NB = 2 teams of kDhBuilders / 2 warps take turns at the units (team
+        // t: units t, t + 2, ..., always Ws buffer t), so the teams build
+        // concurrently while the MMAs consume.  Team thread tt handles the
+        // slots e = tt, tt + NT, ... of the unit's P x F (group g = e / F,
+        // feature f = e % F; F <= 256).
         const int NT = kDhBuilders * 32 / NB;  // threads of a team
-        constexpr int NT_MIN = kDhBuilders * 32 / (P == 2 ? 3 : 2);
+        constexpr int NT_MIN = kDhBuilders * 32 / 2;
         constexpr int NSLOT = (P * 256 + NT_MIN - 1) / NT_MIN;
-        const int tb = threadIdx.x - kDhFirstEpi * 32;  // 0 .. 383
+        const int tb = threadIdx.x - kDhFirstEpi * 32;  // 0 .. kDhBuilders * 32 - 1
         const int team = tb / NT, tt = tb - team * NT;
         const int q = warp & 3, sub = (warp - kDhFirstEpi) / 4;
         float down = 1.f, up = 1.f;  // 2^-s, 2^s (fp16 operands)
@@ -1656,6 +1681,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             down = __uint_as_float((uint32_t)(127 - sh) << 23);
             up = __uint_as_float((uint32_t)(127 + sh) << 23);
         }
+        const bool scaled = down != 1.f;  // the same for every thread of the grid
         // the team's buffer starts zeroed; prev[x]: the row slot x wrote in it
         uint8_t *Wb = base_ptr + (size_t)team * a.ws_bytes;
         for (uint32_t o = (uint32_t)tt * 16; o < a.ws_bytes; o += NT * 16)
@@ -1697,17 +1723,10 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                         // column f of W_k ([G][F] row-major): consecutive
                         // threads read consecutive f
                         const uint16_t *Wk = reinterpret_cast<const uint16_t *>(st + woff + (size_t)g * a.w_bytes) + f;
-#pragma unroll
-                        for (int u = 0; u < NCW; ++u) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int c2 = 0; c2 < 4; ++c2) {
-                                const uint32_t lo = Wk[(8 * u + 2 * c2) * F], hi = Wk[(8 * u + 2 * c2 + 1) * F];
-                                w[c2] = F16 ? pack2_f16(__uint_as_float(lo << 16) * down, __uint_as_float(hi << 16) * down)
-                                            : (lo | (hi << 16));
-                            }
-                            row[x][u] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        if (F16 && scaled)
+                            read_w_column<NCW, true, true>(Wk, F, down, row[x]);
+                        else
+                            read_w_column<NCW, F16, false>(Wk, F, down, row[x]);
                     }
                 }
             }
