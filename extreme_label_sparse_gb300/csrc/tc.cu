@@ -91,11 +91,13 @@ constexpr int kFirstEpi = kProdWarps + 2;
 // 3M shape, so the slots spread evenly; teams of six measured slower)
 constexpr int kDhBuilders = 16;
 constexpr int kDhMaxBuf = 3;  // scattered-W buffers in shared memory (one per builder team)
-// groups per pipeline unit (one stage, one scattered-W buffer): a stage's
-// round trip costs about the same from 2 KB to 32 KB of loads, so each stage
-// carries the loads of several groups -- two while their W rows fit twice in
-// shared memory (G <= 32), else one
-__host__ __device__ constexpr int dh_units(int G) { return G <= 32 ? 2 : 1; }
+// groups per pipeline unit (one stage, one scattered-W buffer): a unit's
+// fixed costs (barrier round trips, the builders' team barriers, the MMA
+// commits) outweigh deeper pipelining, so a unit carries as many groups as two
+// scattered-W buffers of 384 columns allow: 64 labels (four groups at G = 16:
+// 14 % faster than two at B = 256; two at G = 32), else one group (one group
+// per unit measured 4-40 % slower than two at G <= 32)
+__host__ __device__ constexpr int dh_units(int G) { return G <= 16 ? 4 : G <= 32 ? 2 : 1; }
 constexpr int kDhThreads = 32 * (2 + kDhBuilders);
 
 // ------------------------------------------------------------------ plans
