@@ -617,12 +617,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int me = warp - kProdWarps;
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
         const uint32_t wlay = layout_for_swizzle(2 * a.cw);
+        const int cw_shift = a.cw == 64 ? 6 : a.cw == 32 ? 5 : 4;  // cw is 16, 32 or 64
         int it = 0;
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it) {
-            if (it % a.issuers != me)
+        Ring rs;
+        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rs.next(S)) {
+            if ((a.issuers == 2 ? (it & 1) : 0) != me)
                 continue;
-            const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
+            const int s = rs.i;
+            const uint32_t ph = rs.ph;
             const int acc = acc_slot(it, a.issuers);
             if (!mbar_wait(bar_addr(c.tempty[acc]), acc_phase(it, a.issuers) ^ 1u, abort_flag, a.status))
                 break;
@@ -642,7 +644,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                                   (uint32_t)F * 128, 1024, kLayoutSW128);
                         // B: W_k, K-major; box 16 st / cw, 32 bytes per 16 f inside a 2 cw-byte row
                         const int f0 = st * 16;
-                        const uint64_t bd = sdesc(Wt + (uint32_t)(f0 / a.cw) * G * 2 * a.cw + (uint32_t)(f0 % a.cw) * 2,
+                        const uint64_t bd = sdesc(Wt + (uint32_t)(f0 >> cw_shift) * G * 2 * a.cw +
+                                                      (uint32_t)(f0 & (a.cw - 1)) * 2,
                                                   16, 16 * a.cw, wlay);
                         mma_bf16(d, ad, bd, idesc, st > 0 ? 1u : 0u);
                     }
@@ -682,8 +685,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!mbar_wait(bar_addr(c.tfull[acc]), acc_phase(it, a.issuers), abort_flag, a.status))
                 break;
             tc_fence_after();
-            for (int u = sub; u < units; u += 2) {
-                const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
+            // unit u = (tile t, columns c0 ..): t = u / (G / CH), c0 = (u % (G / CH)) CH,
+            // stepped without dividing by the run-time G
+            int t = 0, c0 = sub * CH;
+            auto next_unit = [&]() {
+                for (; c0 >= G; c0 -= G)
+                    ++t;
+            };
+            next_unit();
+            for (int u = sub; u < units; u += 2, c0 += 2 * CH, next_unit()) {
                 const int b = t * 128 + q * 32 + lane;
                 float v[CH];
                 tmem_ld_chunk<CH>(tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * per + t * G + c0), v);
@@ -756,11 +766,12 @@ __device__ __forceinline__ void producer_loop_tiles(Ctl &c, uint32_t stage0, uin
     const int lane = t0 & 31;
     int it = 0;
     bool live = true;
+    Ring r;
     for (int64_t k = blockIdx.x; k < K && live; k += gridDim.x) {
         const GatherIdx cur = gather_idx_of(idx_s, k, F, lane);
-        for (int t = 0; t < MT; ++t, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (uint32_t)(it / S) & 1u;
+        for (int t = 0; t < MT; ++t, ++it, r.next(S)) {
+            const int s = r.i;
+            const uint32_t ph = r.ph;
             if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status)) {
                 live = false;
                 break;
@@ -852,17 +863,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int passes = a.ncat ? 1 : a.planes;
         int it = 0;
         bool live = true;
+        Ring rs;  // stage of sequence number it * T + t
         for (int64_t k = blockIdx.x; k < a.K && live; k += gridDim.x, ++it) {
-            if (it % a.issuers != me)
+            if ((a.issuers == 2 ? (it & 1) : 0) != me) {
+                for (int t = 0; t < T; ++t)
+                    rs.next(S);
                 continue;
+            }
             const int acc = acc_slot(it, a.issuers);
             if (!mbar_wait(bar_addr(c.tempty[acc]), acc_phase(it, a.issuers) ^ 1u, abort_flag, a.status))
                 break;
             tc_fence_after();
-          for (int t = 0; t < T; ++t) {
-            const int is = it * T + t;  // stage sequence number
-            const int s = is % S;
-            const uint32_t ph = (uint32_t)(is / S) & 1u;
+          for (int t = 0; t < T; ++t, rs.next(S)) {
+            const int s = rs.i;
+            const uint32_t ph = rs.ph;
             if (!mbar_wait(bar_addr(c.full[s]), ph, abort_flag, a.status)) {
                 live = false;
                 break;
@@ -908,8 +922,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (!mbar_wait(bar_addr(c.tfull[acc]), acc_phase(it, a.issuers), abort_flag, a.status))
                 break;
             tc_fence_after();
-            for (int u = sub; u < units; u += 2) {
-                const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
+            // unit u = (f tile tf, columns c0 ..), stepped as in the forward stage
+            int tf = 0, c0 = sub * CH;
+            auto next_unit = [&]() {
+                for (; c0 >= G; c0 -= G)
+                    ++tf;
+            };
+            next_unit();
+            for (int u = sub; u < units; u += 2, c0 += 2 * CH, next_unit()) {
                 const int f = tf * 128 + q * 32 + lane;
                 const uint32_t col = tbase + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * per + tf * a.Nacc + c0);
                 float v[CH];
