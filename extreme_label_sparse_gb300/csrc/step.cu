@@ -250,8 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             nrow = __ldg(a.idx_s + ((int64_t)cl * C + rank) * F + warp * RW + lane);
         int it = 0;
         bool ok = true;
-        for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it) {
-            const int sh = it % SH, sw = it % SW;
+        Ring rh, rw;
+        for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it, rh.next(SH), rw.next(SW)) {
+            const int sh = rh.i, sw = rw.i;
             const int64_t k0 = ps * C;
             const int ng = groups_in_step(a, ps);
             const bool own = (int)rank < ng;
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
             if (ps + ncl < a.NPS && kn < a.K && lane < RW)
                 nrow = __ldg(a.idx_s + kn * F + warp * RW + lane);
             if (t == 0 && ok) {
-                ok = mbar_wait(bar_addr(c.wempty[sw]), ((uint32_t)(it / SW) & 1u) ^ 1u, abort_flag, a.status);
+                ok = mbar_wait(bar_addr(c.wempty[sw]), rw.ph ^ 1u, abort_flag, a.status);
                 if (ok) {
                     const uint32_t wfb = bar_addr(c.wfull[sw]);
                     const uint32_t ws = base + a.off_w + (uint32_t)sw * a.wslot_bytes;
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
                 }
             }
             STEP_TRACE(1, it);
-            if (!mbar_wait(bar_addr(c.hempty[sh]), ((uint32_t)(it / SH) & 1u) ^ 1u, abort_flag, a.status))
+            if (!mbar_wait(bar_addr(c.hempty[sh]), rh.ph ^ 1u, abort_flag, a.status))
                 break;
             STEP_TRACE(2, it);
             if (own) {  // warp-uniform: every lane takes part in the shuffles
@@ -307,10 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
         const uint32_t idf = idesc_bf16(128, G, 1, 0);
         constexpr uint32_t wlay = CW == 64 ? kLayoutSW128 : CW == 32 ? kLayoutSW64 : kLayoutSW32;
         int it = 0, io = 0;
-        for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it) {
-            const int sh = it % SH, sw = it % SW;
+        Ring rh, rw;
+        for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it, rh.next(SH), rw.next(SW)) {
+            const int sh = rh.i, sw = rw.i;
             STEP_TRACE(0, it);
-            if (!warp_wait(bar_addr(c.wfull[sw]), (uint32_t)(it / SW) & 1u, abort_flag, a.status))
+            if (!warp_wait(bar_addr(c.wfull[sw]), rw.ph, abort_flag, a.status))
                 break;
             STEP_TRACE(1, it);
             if ((int)rank >= groups_in_step(a, ps)) {  // no own group this step
@@ -320,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
                 continue;
             }
             const int zs = io & 1;
-            if (!warp_wait(bar_addr(c.hfull[sh]), (uint32_t)(it / SH) & 1u, abort_flag, a.status))
+            if (!warp_wait(bar_addr(c.hfull[sh]), rh.ph, abort_flag, a.status))
                 break;
             STEP_TRACE(2, it);
             if (!warp_wait(bar_addr(c.zempty[zs]), ((uint32_t)(io >> 1) & 1u) ^ 1u, abort_flag, a.status))
@@ -357,10 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
         constexpr uint32_t zlay = ZSW == 128 ? kLayoutSW128 : ZSW == 64 ? kLayoutSW64 : kLayoutSW32;
         const int kb = a.nbc * 4;  // K steps of 16 samples
         int it = 0, io = 0;
-        for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it) {
-            const int sh = it % SH;
+        Ring rh;
+        for (int64_t ps = cl; ps < a.NPS; ps += ncl, ++it, rh.next(SH)) {
+            const int sh = rh.i;
             // this warp sees the H barrier itself before its MMAs read the cp.async data
-            if (!warp_wait(bar_addr(c.hfull[sh]), (uint32_t)(it / SH) & 1u, abort_flag, a.status))
+            if (!warp_wait(bar_addr(c.hfull[sh]), rh.ph, abort_flag, a.status))
                 break;
             if ((int)rank >= groups_in_step(a, ps)) {
                 if (lane == 0)
@@ -682,13 +685,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_step(const __grid_constant__
         const int nblk = F / 8;
         int it = 0, gi = 0;
         bool ok = true;
-        for (int64_t ps = cl; ps < a.NPS && ok; ps += ncl, ++it) {
-            const int sw = it % SW;
+        Ring rw;
+        for (int64_t ps = cl; ps < a.NPS && ok; ps += ncl, ++it, rw.next(SW)) {
+            const int sw = rw.i;
             const int db = it & 1;
             const uint32_t dph = (uint32_t)(it >> 1) & 1u;
             const int ng = groups_in_step(a, ps);
             STEP_TRACE(0, it);
-            ok = mbar_wait(bar_addr(c.wfull[sw]), (uint32_t)(it / SW) & 1u, abort_flag, a.status);
+            ok = mbar_wait(bar_addr(c.wfull[sw]), rw.ph, abort_flag, a.status);
             STEP_TRACE(1, it);
             if (named_bar_any(kBarBld, kBld * 32, !ok))
                 break;
