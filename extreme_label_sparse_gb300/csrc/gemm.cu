@@ -322,6 +322,216 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- group |.|-sum GEMM, label-streaming form
+// The same sums with the product transposed: out[l / G][m] = sum over the G
+// labels l of a group of |sum_k A[m][k] B[l][k]|, A (M <= a few hundred rows,
+// MN-major) resident in shared memory, B (the long label side, MN-major)
+// streamed in chunks of NW = 256 (or 128) labels.  The accumulator's lanes
+// are A's rows and its columns the chunk's labels, so a group's sum runs
+// along one thread's registers (no shuffles) and 32 lanes store 32
+// consecutive outputs.  CTA (mt, r): rows [128 mt, 128 mt + 128), chunks of
+// label range r; the CTAs of one range follow each other's chunks closely,
+// so each chunk comes from HBM once and from L2 to the other row tiles.
+struct GabsTCtl {
+    uint64_t full[4], empty[4];
+    uint64_t afull, tfull[2], tempty[2], drain;
+    uint32_t tmem;
+    int abort_flag;
+};
+
+struct GabsTArgs {
+    float *out;
+    int32_t M, L, K, G, NW, S, nkb, mtiles;
+    int64_t nchunks;
+    int32_t *status;
+};
+
+template <int NW>
+__global__ void __launch_bounds__(kGThreads, 1)
+    k_gemm_gabs_t(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                  const GabsTArgs a)
+{
+    __shared__ GabsTCtl c;
+    extern __shared__ uint8_t dsm[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    const uint32_t base = (smem_u32(dsm) + 1023u) & ~1023u;
+    const int mt = blockIdx.x % a.mtiles;
+    const int r = blockIdx.x / a.mtiles;
+    const int nr = gridDim.x / a.mtiles;
+    const int64_t c0 = a.nchunks * r / nr, c1 = a.nchunks * (r + 1) / nr;  // this CTA's chunks
+    const int m0 = mt * 128;
+    const int S = a.S, nkb = a.nkb;
+    constexpr uint32_t kChunkTile = (uint32_t)NW * 128;  // one K block of a chunk: NW labels x 64 k
+    const uint32_t stage0 = base + (uint32_t)nkb * kTileBytes;  // A: nkb tiles of 128 rows x 64 k
+    const uint32_t stage_bytes = (uint32_t)nkb * kChunkTile;
+    if (threadIdx.x == 0) {
+        c.abort_flag = 0;
+        for (int i = 0; i < S; ++i) {
+            mbar_init(bar_of(c.full[i]), 1);
+            mbar_init(bar_of(c.empty[i]), 1);
+        }
+        mbar_init(bar_of(c.afull), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_of(c.tfull[i]), 1);
+            mbar_init(bar_of(c.tempty[i]), 128);
+        }
+        mbar_init(bar_of(c.drain), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&c.tmem), 2 * NW);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = c.tmem;
+    volatile int *abort_flag = &c.abort_flag;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- loads
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_of(c.afull), (uint32_t)nkb * kTileBytes);
+            for (int kb = 0; kb < nkb; ++kb)
+                load_tile(base + (uint32_t)kb * kTileBytes, &tm_a, 1, m0, kb * 64, bar_of(c.afull));
+            Ring rs;
+            int64_t ch = c0;
+            for (; ch < c1; ++ch, rs.next(S)) {
+                if (!mbar_wait(bar_of(c.empty[rs.i]), rs.ph ^ 1u, abort_flag, a.status))
+                    break;
+                const uint32_t st = stage0 + (uint32_t)rs.i * stage_bytes;
+                mbar_arrive_expect_tx(bar_of(c.full[rs.i]), stage_bytes);
+                for (int kb = 0; kb < nkb; ++kb)
+                    for (int q = 0; q < NW / 64; ++q)
+                        tma_load_2d(st + (uint32_t)kb * kChunkTile + (uint32_t)q * (kTileBytes / 2), &tm_b,
+                                    (int)(ch * NW) + 64 * q, kb * 64, bar_of(c.full[rs.i]));
+            }
+            // winding down after an abort: the loads in flight land first
+            mbar_wait_drain(bar_of(c.afull), 0);
+            if (*abort_flag) {
+                Ring rd;
+                for (int64_t j = c0; j < ch; ++j, rd.next(S))
+                    if (j + S >= ch)
+                        mbar_wait_drain(bar_of(c.full[rd.i]), rd.ph);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA
+        // D[128 rows][NW labels] += A (MN-major, 128 rows) x B (MN-major, NW labels)
+        const uint32_t idesc = idesc_bf16(128, NW, 1, 1);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_of(c.afull), 0, abort_flag, a.status));
+        Ring rs;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int64_t ch = c0; ok && ch < c1; ++ch, rs.next(S)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.tempty[acc]), aph ^ 1u, abort_flag, a.status)))
+                break;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.full[rs.i]), rs.ph, abort_flag, a.status)))
+                break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t st = stage0 + (uint32_t)rs.i * stage_bytes;
+                const uint32_t d = tbase + (uint32_t)(acc * NW);
+                for (int kb = 0; kb < nkb; ++kb) {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(d, tile_desc(base + (uint32_t)kb * kTileBytes, 1, ks),
+                                 sdesc(st + (uint32_t)kb * kChunkTile + (uint32_t)ks * 2048, kTileBytes / 2, 1024,
+                                       kLayoutSW128),
+                                 idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+                }
+                mma_commit(bar_of(c.empty[rs.i]));
+                mma_commit(bar_of(c.tfull[acc]));
+            }
+            __syncwarp();
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1u;
+            }
+        }
+        if (lane == 0)
+            mma_commit(bar_of(c.drain));
+        __syncwarp();
+        mbar_wait_drain(bar_of(c.drain), 0);
+    } else {
+        // ---------------------------------------------------------- epilogue
+        // warp w reads TMEM lanes 32 (w % 4) .. (its A rows); a group of G
+        // labels is G consecutive columns of the accumulator
+        const int q = warp & 3;
+        const int m = m0 + q * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int64_t K = a.L / a.G;  // groups
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int64_t ch = c0; ch < c1; ++ch) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_of(c.tfull[acc]), aph, abort_flag, a.status)))
+                break;
+            tc_fence_after();
+            // 128 columns per round: four loads in flight, one wait (a
+            // load-wait pair per 32 columns left the epilogue the slowest
+            // role); |.| summed in four independent chains
+            float sum = 0.f;
+            for (int cb = 0; cb < NW; cb += 128) {
+                uint32_t v[4][32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tmem_ld32(tbase + lane_off + (uint32_t)(acc * NW + cb + 32 * j), v[j]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int cc = cb + 32 * j;
+                    if (a.G >= 32) {
+                        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+                        for (int x = 0; x < 32; x += 4) {
+                            p0 += fabsf(__uint_as_float(v[j][x]));
+                            p1 += fabsf(__uint_as_float(v[j][x + 1]));
+                            p2 += fabsf(__uint_as_float(v[j][x + 2]));
+                            p3 += fabsf(__uint_as_float(v[j][x + 3]));
+                        }
+                        sum += (p0 + p1) + (p2 + p3);
+                        if (((cc + 32) & (a.G - 1)) == 0) {  // the group ends here
+                            const int64_t k = (ch * NW + cc + 32) / a.G - 1;
+                            if (k < K && m < a.M)
+                                a.out[k * a.M + m] = sum;
+                            sum = 0.f;
+                        }
+                    } else {  // G = 16: two groups per 32 columns
+                        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                        for (int x = 0; x < 16; x += 2) {
+                            s0 += fabsf(__uint_as_float(v[j][x]));
+                            s1 += fabsf(__uint_as_float(v[j][x + 1]));
+                            s2 += fabsf(__uint_as_float(v[j][x + 16]));
+                            s3 += fabsf(__uint_as_float(v[j][x + 17]));
+                        }
+                        const int64_t k = (ch * NW + cc) / 16;
+                        if (m < a.M) {
+                            if (k < K)
+                                a.out[k * a.M + m] = s0 + s1;
+                            if (k + 1 < K)
+                                a.out[(k + 1) * a.M + m] = s2 + s3;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar_of(c.tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1u;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 2 * NW);
+    }
+}
+
 // ---------------------------------------------------------------- argmax GEMM
 // For each row m of A (M x K, K-major) the column n of B (N x K, K-major) with
 // the largest <A_m, B_n> (fp32 accumulation; ties to the smaller n).  One CTA
@@ -618,6 +828,71 @@ sg_status gemm_group_abs(const uint16_t *A, int64_t lda, int M, const uint16_t *
     SG_TRY_CUDA(cudaFuncSetAttribute(k_gemm_gabs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     dim3 grid((unsigned)((N + 127) / 128), (unsigned)((M + 127) / 128));
     k_gemm_gabs<<<grid, kGThreads, smem, st>>>(ta, tb, out, M, N, K, G, NS, status);
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+// out[l / G][m] = sum over the G labels l of a group of |sum_k A[m][k] B[l][k]|
+// (A: M x K MN-major, leading dimension lda; B: L x K MN-major, ldb), with
+// G in {16, 32, 64, 128, 256} dividing L and K <= 256.  Returns
+// SG_ERR_UNSUPPORTED for other shapes (the caller then takes gemm_group_abs).
+sg_status gemm_group_abs_t(const uint16_t *A, int64_t lda, int M, const uint16_t *B, int64_t ldb, int64_t L, int K,
+                           int G, float *out, int num_sms, int32_t *status, cudaStream_t st)
+{
+    if (M < 1 || L < 1 || K < 1)
+        return SG_OK;
+    if (G < 16 || G > 256 || (G & (G - 1)) != 0 || L % G != 0 || K > 256) {
+        sg_set_error("label-streaming group |.|-sum GEMM: G in 16..256 a power of two dividing L, K <= 256");
+        return SG_ERR_UNSUPPORTED;
+    }
+    const int nkb = (K + 63) / 64;
+    // stages of NW labels x K: 256 labels while three stages fit, else 128
+    const long budget = 227l * 1024 - 1024 - (long)nkb * kTileBytes;
+    int NW = 256;
+    int S = (int)(budget / ((long)nkb * NW * 128));
+    if (S < 3) {
+        NW = 128;
+        S = (int)(budget / ((long)nkb * NW * 128));
+    }
+    if (S > 4)
+        S = 4;
+    if (S < 2 || G > NW) {
+        sg_set_error("label-streaming group |.|-sum GEMM: no room for two stages of whole groups (K=%d G=%d)", K, G);
+        return SG_ERR_UNSUPPORTED;
+    }
+    CUtensorMap ta, tb;
+    sg_status rc = map_2d(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, 64, 64, "A");
+    if (rc != SG_OK)
+        return rc;
+    rc = map_2d(&tb, B, (uint64_t)L, (uint64_t)K, (uint64_t)ldb, 64, 64, "B");
+    if (rc != SG_OK)
+        return rc;
+    GabsTArgs a;
+    a.out = out;
+    a.M = M;
+    a.L = (int32_t)L;
+    a.K = K;
+    a.G = G;
+    a.NW = NW;
+    a.S = S;
+    a.nkb = nkb;
+    a.mtiles = (M + 127) / 128;
+    a.nchunks = (L + NW - 1) / NW;
+    a.status = status;
+    if (L > INT32_MAX) {
+        sg_set_error("label-streaming group |.|-sum GEMM: L must fit 31 bits");
+        return SG_ERR_UNSUPPORTED;
+    }
+    // ranges of chunks: the row tiles of one range run side by side
+    int64_t ranges = num_sms / a.mtiles;
+    if (ranges < 1)
+        ranges = 1;
+    if (ranges > a.nchunks)
+        ranges = a.nchunks;
+    const size_t smem = (size_t)nkb * kTileBytes + (size_t)S * nkb * NW * 128 + 1024;
+    void (*kern)(CUtensorMap, CUtensorMap, GabsTArgs) = NW == 256 ? k_gemm_gabs_t<256> : k_gemm_gabs_t<128>;
+    SG_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    kern<<<(unsigned)(ranges * a.mtiles), kGThreads, smem, st>>>(ta, tb, a);
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }

@@ -9,13 +9,16 @@
 // outside the old I_k (ties: smaller feature); kept columns keep their
 // weights, grown ones start at zero, the new I_k is sorted ascending.
 //
-// The grow scores of every (group, feature) are one tcgen05 GEMM, dZ^T h,
-// whose epilogue sums |.| over each group's rows (gemm.cu); the selection is
-// one warp per group.
+// The grow scores of every (group, feature) are one tcgen05 GEMM, h^T dZ,
+// whose epilogue sums |.| over each group's labels (gemm.cu: the labels
+// streamed past a resident tile of h; groups below 16 labels take the tiled
+// form dZ^T h); the selection is one warp per group.
 #include "sg_internal.cuh"
 
 sg_status gemm_group_abs(const uint16_t *A, int64_t lda, int M, const uint16_t *B, int64_t ldb, int N, int K, int G,
                          float *out, int32_t *status, cudaStream_t st);
+sg_status gemm_group_abs_t(const uint16_t *A, int64_t lda, int M, const uint16_t *B, int64_t ldb, int64_t L, int K,
+                           int G, float *out, int num_sms, int32_t *status, cudaStream_t st);
 
 namespace {
 
@@ -239,9 +242,17 @@ extern "C" sg_status sg_rewire(sg_layout *lo, const sg_bf16 *h, int32_t B, const
             lo->rw_ws_bytes = need;
         }
     }
-    // grow scores: A = dZ^T (MN-major, M = L), B = h^T (MN-major, N = H), K = samples
-    if (rc == SG_OK)
-        rc = gemm_group_abs(dZ, lo->L, (int)lo->L, h, lo->H, lo->H, B, G, lo->rw_ws, lo->status, st);
+    // grow scores: the labels streamed past a resident tile of h (A = h,
+    // MN-major, M = H; B = dZ, MN-major, the L labels; K = samples), or for
+    // groups below 16 labels A = dZ^T (M = L) against B = h^T (N = H)
+    if (rc == SG_OK) {
+        if (G >= 16 && B <= 256 && lo->L <= INT32_MAX)
+            rc = gemm_group_abs_t(h, lo->H, lo->H, dZ, lo->L, lo->L, B, G, lo->rw_ws, lo->num_sms, lo->status, st);
+        else
+            rc = SG_ERR_UNSUPPORTED;
+        if (rc == SG_ERR_UNSUPPORTED)
+            rc = gemm_group_abs(dZ, lo->L, (int)lo->L, h, lo->H, lo->H, B, G, lo->rw_ws, lo->status, st);
+    }
     if (rc == SG_OK) {
         const unsigned grid = (unsigned)((lo->K + kRwWarps - 1) / kRwWarps);
         k_rewire_select<<<grid, 32 * kRwWarps, 0, st>>>(lo->K, G, lo->F, lo->H, n_drop, lo->idx_s, W, lo->rw_ws,

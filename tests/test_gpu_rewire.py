@@ -26,6 +26,7 @@ CASES = [
     (128, 768, 64, 12, 128, 16),
     (96, 512, 128, 6, 48, 48),
     (50, 96, 1, 304, 24, 3),
+    (200, 256, 32, 20, 64, 8),  # B > 128: chunks of 128 labels in the grow-score GEMM
 ]
 
 
