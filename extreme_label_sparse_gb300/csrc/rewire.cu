@@ -73,29 +73,45 @@ __global__ void __launch_bounds__(32 * kRwWarps)
         m[t] = s;
         dropped[t] = false;
     }
-    // drop the n_drop smallest
-    for (int r = 0; r < n_drop; ++r) {
-        float v = 0.f;
-        int j = -1, tt = -1;
+    // drop the n_drop smallest.  Each lane keeps the best of its own slots
+    // (smallest m, then smallest feature); a round takes the warp's best and
+    // only the lane that held it looks at its slots again.  Slot loops stop
+    // at the slots that hold features (a warp-uniform bound).
+    const int ftn = (F + 31) / 32;
+    int feat[FT];
+#pragma unroll
+    for (int t = 0; t < FT; ++t) {
+        const int f = lane + 32 * t;
+        feat[t] = t < ftn && f < F ? (int)I[f] : -1;
+    }
+    float dv = 0.f;
+    int dj = -1, dt = -1;
+    auto drop_best = [&]() {
+        dv = 0.f;
+        dj = -1;
+        dt = -1;
 #pragma unroll
         for (int t = 0; t < FT; ++t) {
-            const int f = lane + 32 * t;
-            if (f < F && !dropped[t]) {
-                const int feat = I[f];
-                if (j < 0 || m[t] < v || (m[t] == v && feat < j)) {
-                    v = m[t];
-                    j = feat;
-                    tt = t;
-                }
+            if (t >= ftn)
+                break;
+            if (feat[t] >= 0 && !dropped[t] && (dj < 0 || m[t] < dv || (m[t] == dv && feat[t] < dj))) {
+                dv = m[t];
+                dj = feat[t];
+                dt = t;
             }
         }
-        const int mine = j;
+    };
+    drop_best();
+    for (int r = 0; r < n_drop; ++r) {
+        float v = dv;
+        int j = dj;
         warp_best(v, j, false);
-        if (mine == j && j >= 0) {
+        if (j >= 0 && dj == j) {  // this lane held it (features of a group are distinct)
 #pragma unroll
             for (int t = 0; t < FT; ++t)
-                if (t == tt)
+                if (t == dt)
                     dropped[t] = true;
+            drop_best();
         }
         if (lane == 0)
             drop[r] = j;
@@ -105,31 +121,45 @@ __global__ void __launch_bounds__(32 * kRwWarps)
         sc[I[f]] = -1.f;
     __syncwarp();
     // grow the n_drop largest: the row in registers (feature x = lane + 32 t)
-    // when it fits, else scanned from memory each time
+    // when it fits, else scanned from memory each time; as for the drop, a
+    // lane keeps its best (largest, then smallest x) and only the lane that
+    // held a round's winner looks again
     if (H <= 32 * kRwRegs) {
+        const int htn = (H + 31) / 32;
         float rv[kRwRegs];
 #pragma unroll
         for (int t = 0; t < kRwRegs; ++t) {
             const int x = lane + 32 * t;
-            rv[t] = x < H ? sc[x] : -1.f;
+            rv[t] = t < htn && x < H ? sc[x] : -1.f;
         }
-        for (int r = 0; r < n_drop; ++r) {
-            float v = -1.f;
-            int j = -1, tt = -1;
+        float gv = -1.f;
+        int gj = -1, gt = -1;
+        auto grow_best = [&]() {
+            gv = -1.f;
+            gj = -1;
+            gt = -1;
 #pragma unroll
-            for (int t = 0; t < kRwRegs; ++t)
-                if (rv[t] >= 0.f && (j < 0 || rv[t] > v)) {  // ascending x: ties keep the smaller
-                    v = rv[t];
-                    j = lane + 32 * t;
-                    tt = t;
+            for (int t = 0; t < kRwRegs; ++t) {
+                if (t >= htn)
+                    break;
+                if (rv[t] >= 0.f && (gj < 0 || rv[t] > gv)) {  // ascending x: ties keep the smaller
+                    gv = rv[t];
+                    gj = lane + 32 * t;
+                    gt = t;
                 }
-            const int mine = j;
+            }
+        };
+        grow_best();
+        for (int r = 0; r < n_drop; ++r) {
+            float v = gv;
+            int j = gj;
             warp_best(v, j, true);
-            if (j >= 0 && mine == j) {
+            if (j >= 0 && gj == j) {
 #pragma unroll
                 for (int t = 0; t < kRwRegs; ++t)
-                    if (t == tt)
+                    if (t == gt)
                         rv[t] = -1.f;
+                grow_best();
             }
             if (lane == 0)
                 grow[r] = j;
