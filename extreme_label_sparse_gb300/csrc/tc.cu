@@ -438,22 +438,30 @@ __device__ __forceinline__ void issue_gather(const uint16_t *hT, int ldB, uint32
 // The same copy with the shape known at compile time (F rows, U 16-byte units
 // per row): the loop unrolls, the per-lane offsets are computed once, and an
 // instruction costs a shuffle, a 32-bit multiply-add and the copy.
-template <int F_, int U_>
+//
+// PAIR (U_ = 16): the second 64-sample chunk holds samples 0 .. 63 of the
+// rows I_k2[f] of a second group instead of samples 64 .. 127 of I_k[f].
+template <int F_, int U_, bool PAIR = false>
 __device__ __forceinline__ void issue_gather_t(const uint16_t *hT, int ldB, uint32_t A, const GatherIdx &g,
-                                               int lane)
+                                               int lane, const GatherIdx &g2 = GatherIdx{{0u, 0u}})
 {
     constexpr int RW = F_ / kProdWarps;
     constexpr int LPR = U_ < 32 ? U_ : 32;  // lanes per row
     constexpr int RPI = 32 / LPR;           // rows per instruction
     static_assert(RW % RPI == 0 && RW <= 64, "rows per producer warp");
+    static_assert(!PAIR || U_ == 16, "pairs take the two chunks of one 128-sample tile");
     const int pw = threadIdx.x / 32;
     const int u = lane % LPR, rsub = lane / LPR;
     const uint32_t dst0 = A + (uint32_t)(u >> 3) * F_ * 128 + (uint32_t)(pw * RW + rsub) * 128;
-    const uint16_t *src0 = hT + u * 8;
+    const uint16_t *src0 = hT + (PAIR ? (u & 7) : u) * 8;
 #pragma unroll
     for (int t = 0; t < RW / RPI; ++t) {
         const int r = t * RPI + rsub;  // row within the warp's RW rows (RW is a multiple of 8)
-        const uint32_t row = __shfl_sync(0xffffffffu, t * RPI < 32 ? g.i[0] : g.i[1], r & 31);
+        uint32_t row = __shfl_sync(0xffffffffu, t * RPI < 32 ? g.i[0] : g.i[1], r & 31);
+        if (PAIR) {
+            const uint32_t row2 = __shfl_sync(0xffffffffu, t * RPI < 32 ? g2.i[0] : g2.i[1], r & 31);
+            row = u < 8 ? row : row2;
+        }
         cp_async16(dst0 + (uint32_t)(t * RPI) * 128 + (uint32_t)(((u & 7) ^ (r & 7)) << 4),
                    src0 + row * (uint32_t)ldB);
     }
@@ -474,7 +482,7 @@ struct NoAfterIssue {
 // once per group, with the group's stage and phase, right after the copies of
 // the next group are issued (the last group's after the loop); it returns
 // false if a wait in it gave up.
-template <int F_ = 0, int U_ = 0, typename IssueTma, typename AfterIssue = NoAfterIssue>
+template <int F_ = 0, int U_ = 0, bool PAIR = false, typename IssueTma, typename AfterIssue = NoAfterIssue>
 __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t stage_bytes, int S,
                                               int64_t K, const uint16_t *idx_s, const uint16_t *hT,
                                               int ldB, int F, int MT, uint32_t tma_bytes,
@@ -486,18 +494,25 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
     const int lane = t & 31;
     const int units = MT * 16;
     int it = 0;
-    GatherIdx cur = {{0u, 0u}};
-    if (blockIdx.x < K)
-        cur = gather_idx_of(idx_s, (int64_t)blockIdx.x >> ishift, F, lane);
+    // PAIR: kernel group k is the layout groups 2k (first chunk) and 2k + 1
+    GatherIdx cur = {{0u, 0u}}, cur2 = {{0u, 0u}};
+    if (blockIdx.x < K) {
+        cur = gather_idx_of(idx_s, PAIR ? 2 * (int64_t)blockIdx.x : (int64_t)blockIdx.x >> ishift, F, lane);
+        if (PAIR)
+            cur2 = gather_idx_of(idx_s, 2 * (int64_t)blockIdx.x + 1, F, lane);
+    }
     Ring r;
     int prev_s = 0;
     uint32_t prev_ph = 0;
     for (int64_t k = blockIdx.x; k < K; k += gridDim.x, ++it, r.next(S)) {
         const int s = r.i;
         const uint32_t ph = r.ph;
-        GatherIdx nxt = cur;
-        if (k + gridDim.x < K)
-            nxt = gather_idx_of(idx_s, (k + gridDim.x) >> ishift, F, lane);
+        GatherIdx nxt = cur, nxt2 = cur2;
+        if (k + gridDim.x < K) {
+            nxt = gather_idx_of(idx_s, PAIR ? 2 * (k + gridDim.x) : (k + gridDim.x) >> ishift, F, lane);
+            if (PAIR)
+                nxt2 = gather_idx_of(idx_s, 2 * (k + gridDim.x) + 1, F, lane);
+        }
         FW_TRACE(0, it);
         if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status))
             break;
@@ -508,12 +523,13 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
             issue_tma(k, A, bar_addr(c.full[s]));
         }
         if constexpr (F_ > 0)
-            issue_gather_t<F_, U_>(hT, ldB, A, cur, lane);
+            issue_gather_t<F_, U_, PAIR>(hT, ldB, A, cur, lane, cur2);
         else
             issue_gather(hT, ldB, A, F, units, cur, lane);
         cp_async_arrive_noinc(bar_addr(c.full[s]));
         FW_TRACE(2, it);
         cur = nxt;
+        cur2 = nxt2;
         if (it > 0 && !after(prev_s, prev_ph)) {
             ++it;
             break;
@@ -1094,13 +1110,26 @@ struct CtlFW {
 //
 // SGD: the dW epilogue applies the momentum-SGD update instead of storing dW
 // (its own instance, so the plain step's kernel carries none of that code).
-template <int G_, int FK, int MT, bool SGD>
+//
+// PAIR (B <= 64, one 128-row sample tile): kernel group k is the layout
+// groups 2k and 2k + 1 of GL = G_ / 2 labels each.  The stage's two 64-sample
+// chunks hold their H rows (the first group's samples as rows 0 .. 63, the
+// second's as rows 64 .. 127) and W_k their 2 GL consecutive weight rows, so
+// one forward MMA of N = 2 GL computes both groups' logits (plus two unused
+// off-diagonal blocks) and one dW MMA set over the 128 rows both weight
+// gradients, with dZ block-diagonal in shared memory (the off-diagonal
+// blocks are cleared once and never written).  Each layout group's fp16 dZ
+// tile is written as without pairing.
+template <int G_, int FK, int MT, bool SGD, bool PAIR = false>
 __global__ void __launch_bounds__(kFWThreads, 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
 {
-    // compile-time group width: column chunk of the epilogue, dZ row width
-    // (swizzle) and 64-column chunks of the dZ tile
-    constexpr int CH = G_ >= 64 ? 32 : 16;
+    static_assert(!PAIR || MT == 1, "pairs share one 128-row sample tile");
+    // compile-time group width: column chunk of the epilogue (with pairs,
+    // half a layout group's columns, so that both BCE warps of a lane quarter
+    // work on its diagonal block), dZ row width (swizzle) and 64-column chunks
+    // of the dZ tile
+    constexpr int CH = PAIR ? G_ / 4 : G_ >= 64 ? 32 : 16;
     constexpr int ZSW = G_ * 2 >= 128 ? 128 : G_ * 2;
     constexpr int NZC = G_ * 2 > 128 ? G_ / 64 : 1;
     __shared__ CtlFW cf;
@@ -1148,6 +1177,12 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
         tmem_relinquish();
     }
+    if (PAIR) {
+        // both dZ buffers start zero: the BCE writes only the diagonal blocks
+        for (uint32_t o = threadIdx.x * 16u; o < 2 * a.dz_bytes; o += kFWThreads * 16u)
+            *reinterpret_cast<uint4 *>(base_ptr + o) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async();  // generic writes -> the dW MMA (async proxy)
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1162,7 +1197,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         // stage, so no epilogue warp holds a stage.
         uint32_t wmag = 0;  // running max of |W| bits, two bf16 lanes
         const int t = threadIdx.x;
-        producer_loop<FK * 16, MT * 16>(
+        producer_loop<FK * 16, MT * 16, PAIR>(
             c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes, abort_flag, a.status,
             [&](int64_t k, uint32_t A, uint32_t fb) {
                 const uint32_t Wt = A + a.a_bytes;
@@ -1309,21 +1344,28 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             const int sub = ew / 4;  // two warps per lane quarter split the column units
             // Z_k -> BCE -> dZ_k (workspace tile and shared memory for the dW MMA)
             constexpr int zunits = MT * (G / CH);
-            // positive-list bounds of the group, loaded one group ahead
-            int e0n = 0, e1n = 0;
+            // positive-list bounds of the group, loaded one group ahead (with
+            // pairs, of both groups: entries e0 .. e1 and e1 .. e2)
+            int e0n = 0, e1n = 0, e2n = 0;
             if (blockIdx.x < a.K) {
-                e0n = __ldg(a.gptr + (blockIdx.x >> a.sub_shift));
-                e1n = __ldg(a.gptr + (blockIdx.x >> a.sub_shift) + 1);
+                const int64_t kl = PAIR ? 2 * (int64_t)blockIdx.x : (int64_t)blockIdx.x >> a.sub_shift;
+                e0n = __ldg(a.gptr + kl);
+                e1n = __ldg(a.gptr + kl + 1);
+                if (PAIR)
+                    e2n = __ldg(a.gptr + kl + 2);
             }
             int it = 0;
             Ring rz;
             for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rz.next(NS)) {
                 const int zs = rz.i;
                 const int db = it & 1;
-                const int e0 = e0n, e1 = e1n;
+                const int e0 = e0n, e1 = e1n, e2 = e2n;
                 if (k + gridDim.x < a.K) {
-                    e0n = __ldg(a.gptr + ((k + gridDim.x) >> a.sub_shift));
-                    e1n = __ldg(a.gptr + ((k + gridDim.x) >> a.sub_shift) + 1);
+                    const int64_t kl = PAIR ? 2 * (k + gridDim.x) : (k + gridDim.x) >> a.sub_shift;
+                    e0n = __ldg(a.gptr + kl);
+                    e1n = __ldg(a.gptr + kl + 1);
+                    if (PAIR)
+                        e2n = __ldg(a.gptr + kl + 2);
                 }
                 // columns of the layout group this kernel group starts at
                 const int coff = (int)(k & ((1 << a.sub_shift) - 1)) * G;
@@ -1337,6 +1379,30 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 FW_TRACE(2, it);
                 tc_fence_after();
                 uint8_t *zs_smem = base_ptr + (size_t)db * a.dz_bytes;
+                if constexpr (PAIR) {
+                    // lane quarters 0, 1: the first group's samples (rows
+                    // 0 .. 63), columns 0 .. GL - 1; quarters 2, 3: the second
+                    // group's, columns GL .. 2 GL - 1
+                    constexpr int GL = G / 2;
+                    constexpr int ZSW_L = GL * 2 >= 128 ? 128 : GL * 2;  // the layout group's tile rows
+                    const int grp = q >> 1;
+                    const int ga = grp ? e1 : e0, gb = grp ? e2 : e1;
+                    const int64_t kl = 2 * k + grp;
+                    const int bz = q * 32 + lane, b = bz & 63;
+                    const int cl = sub * CH, c0 = grp * GL + cl;
+                    float v[CH];
+                    tmem_ld_chunk<CH>(tbase + lane_off + (uint32_t)(zs * a.zcols + c0), v);
+                    if (b < a.B) {
+                        const uint32_t y = gb > ga ? group_pos_mask(a.gent, ga, gb, b, cl, CH) : 0u;
+                        lf += bce_chunk_ftz<CH>(v, y);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < CH; ++i)
+                            v[i] = 0.f;
+                    }
+                    store_dz_tile<CH>(zs_smem, bz, c0, v, ZSW, NZC, 128);
+                    store_dz_tile_f16<CH>(a.dZt + (size_t)kl * a.tile_bytes, b, cl, v, ZSW_L, 128);
+                } else {
 #pragma unroll
                 for (int u = sub; u < zunits; u += 2) {
                     const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
@@ -1359,6 +1425,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                                               MT * 128);
                     else
                         store_dz_tile_f16<CH>(a.dZt + (size_t)k * a.tile_bytes, b, c0, v, ZSW, MT * 128);
+                }
                 }
                 FW_TRACE(3, it);
                 tc_fence_before();
@@ -1943,10 +2010,28 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
 
 bool tc_fwdw_ok(const sg_layout *lo, int32_t B) { return plan_fwdw(lo, B).ok; }
 
+// Pairs of groups (the kernel's PAIR form) when one 64-sample chunk holds a
+// group's samples: B <= 64, G of 16 or 32 (pairs of 32 or 64 columns), an
+// even number of groups, and the plan for 2G-label kernel groups fits.
+FWPlan plan_fwdw_pair(const sg_layout *lo, int B)
+{
+    if (B > 64 || (lo->G != 16 && lo->G != 32) || lo->K % 2 != 0)
+        return FWPlan();
+    FWPlan p = plan_fwdw_g(lo, B, 2 * lo->G);
+    if (!p.ok || p.MT != 1)
+        return FWPlan();
+    p.gs = 2 * lo->G;
+    p.sub = 1;
+    p.f16_bytes = 0;  // each layout group's tile is stored from registers
+    return p;
+}
+
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
                   const sg_sgd *sgd, double *loss, cudaStream_t st)
 {
-    const FWPlan p = plan_fwdw(lo, B);
+    const FWPlan pp = plan_fwdw_pair(lo, B);
+    const bool pair = pp.ok;
+    const FWPlan p = pair ? pp : plan_fwdw(lo, B);
     if (!p.ok) {
         sg_set_error("tc_fwdw: shape not supported by the fused forward + dW kernel");
         return SG_ERR_UNSUPPORTED;
@@ -1968,7 +2053,8 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     if (rc != SG_OK)
         return rc;
     a.dZt = dZt;
-    a.tile_bytes = tc_dz_tile_bytes(lo, B) / 2 / p.sub;  // one fp16 plane of a kernel group
+    // one fp16 plane of a kernel group's tile (with pairs: of a layout group's)
+    a.tile_bytes = tc_dz_tile_bytes(lo, B) / 2 / p.sub;
     a.dW = dW;
     a.wmax = lo->wmax;
     a.W = W;
@@ -1979,7 +2065,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.gent = lo->gent;
     a.loss_part = lo->loss_part;
     a.status = lo->status;
-    a.K = lo->K * p.sub;
+    a.K = pair ? lo->K / 2 : lo->K * p.sub;
     a.sub_shift = p.sub == 4 ? 2 : p.sub == 2 ? 1 : 0;
     a.L = lo->L;
     a.B = B;
@@ -2009,8 +2095,13 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     const int grid = persistent_grid(lo, a.K);
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
 #define SG_FW_PICK(GG, KK, MM)                                           \
-    if (p.gs == GG && lo->F == KK * 16 && p.MT == MM)                   \
+    if (!pair && p.gs == GG && lo->F == KK * 16 && p.MT == MM)          \
         kern = sgd ? k_tc_fwdw<GG, KK, MM, true> : k_tc_fwdw<GG, KK, MM, false>;
+#define SG_FW_PAIR(GG, KK)                                               \
+    if (pair && p.gs == GG && lo->F == KK * 16)                         \
+        kern = sgd ? k_tc_fwdw<GG, KK, 1, true, true> : k_tc_fwdw<GG, KK, 1, false, true>;
+    SG_FW_PAIR(32, 4) SG_FW_PAIR(32, 8) SG_FW_PAIR(32, 16) SG_FW_PAIR(64, 4) SG_FW_PAIR(64, 8) SG_FW_PAIR(64, 16)
+#undef SG_FW_PAIR
     SG_FW_PICK(16, 4, 1) SG_FW_PICK(16, 4, 2) SG_FW_PICK(32, 4, 1) SG_FW_PICK(32, 4, 2)
     SG_FW_PICK(64, 4, 1) SG_FW_PICK(64, 4, 2)
     SG_FW_PICK(16, 8, 1) SG_FW_PICK(16, 8, 2) SG_FW_PICK(16, 16, 1) SG_FW_PICK(16, 16, 2)

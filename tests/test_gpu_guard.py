@@ -45,6 +45,7 @@ SHAPES = [
     ("b256_g64", 256, 768, 64 * 21, 64, 128),
     ("one_kernel_f48", 70, 200, 32 * 45, 32, 48),
     ("g1", 45, 256, 333, 1, 64),
+    ("pair_b40", 40, 256, 16 * 60, 16, 128),
     ("g5", 9, 64, 5 * 41, 5, 24),
 ]
 

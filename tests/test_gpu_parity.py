@@ -53,6 +53,10 @@ CASES = [
     # and three column windows of the CUDA-core dh)
     (_w("tc_g192_f32", B=100, H=256, L=192 * 8, G=192, F=32, pos=5), (SIMT, TC)),
     (_w("tc_h4096", B=64, H=4096, L=32 * 60, G=32, F=64, pos=4), (SIMT, TC)),
+    # B <= 64: the fused forward pairs consecutive groups (an even count);
+    # with an odd count it runs them one by one
+    (_w("pair_g16_b40", B=40, H=320, L=16 * 62, G=16, F=128, pos=4), (SIMT, TC)),
+    (_w("like8p6m_oddK", B=64, H=768, L=32 * 301, G=32, F=64, pos=10, dist="zipf"), (SIMT, TC)),
     (_w("simt_h2500_g5", B=40, H=2500, L=5 * 120, G=5, F=40, pos=3), (SIMT,)),
     # per-label fan-in through the dedicated G = 1 kernels: several sample
     # tiles and label chunks, a ragged last tile, F = 64 and 128
