@@ -984,7 +984,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // second MMA warp computes dW_k^T = H_k^T [dZ_hi | dZ_lo] from the same
 // shared-memory H_k, so H_k is gathered once and dZ_k is never read back for
 // dW.  The dW warps store dW_k (or, in the SGD instance, apply the momentum
-// update to it and store the new W_k) and record max |W| for dh's fp16 scale.
+// update to it and store the new W_k); the producers record max |W| for
+// dh's fp16 scale.
 // Warps: the producers, one forward MMA warp, one dW MMA warp, eight BCE
 // warps and four dW warps.
 constexpr int kFWBce = 8;  // BCE warps: two per TMEM lane quarter
