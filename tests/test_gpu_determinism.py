@@ -29,6 +29,8 @@ SHAPES = [
                                idx_mode="uniform")),
     ("per_label", Workload("d5", B=100, H=256, L=700, G=1, F=64, pos=4, pos_dist="zipf", zipf_s=1.1,
                            idx_mode="uniform")),
+    ("paired_groups", Workload("d6", B=48, H=256, L=32 * 40, G=32, F=64, pos=4, pos_dist="zipf", zipf_s=1.1,
+                               idx_mode="uniform")),
 ]
 
 

@@ -27,6 +27,7 @@ CASES = [
     (96, 512, 128, 6, 48, 48),
     (50, 96, 1, 304, 24, 3),
     (200, 256, 32, 20, 64, 8),  # B > 128: chunks of 128 labels in the grow-score GEMM
+    (48, 200, 32, 24, 64, 8),   # H not a multiple of 128: a partial feature tile
 ]
 
 
