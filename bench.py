@@ -629,7 +629,7 @@ def run_ours(args):
     r.close()
     del r
     headtail = grouping = rewire = None
-    if rank == 0 and world == 1 and not args.labels and not args.no_others and not args.sgd:
+    if rank == 0 and world == 1 and not args.sgd and (args.extras or (not args.labels and not args.no_others)):
         headtail = measure_headtail(sg, torch, dev, p, args.other_steps, 2, stream, hbm, tflops)
         grouping = measure_grouping(sg, torch, dev, w, tflops)
         rewire = measure_rewire(sg, torch, dev, p, args.other_steps, stream, hbm, tflops)
@@ -692,6 +692,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the group-size sweep (G = 1, 16, 32, 64; uniform and clustered idx)")
+    ap.add_argument("--extras", action="store_true",
+                    help="measure the head-tail step, grouping and rewiring also with --labels "
+                         "(on the reduced workload; for profiling runs)")
     ap.add_argument("--no-others", action="store_true",
                     help="skip the other label-space workloads (670K- and 8.6M-shaped tails)")
     ap.add_argument("--other-steps", type=int, default=5,
