@@ -467,6 +467,23 @@ __device__ __forceinline__ void issue_gather_t(const uint16_t *hT, int ldB, uint
     }
 }
 
+// The items a persistent CTA works through: its groups k = blockIdx.x,
+// blockIdx.x + gridDim.x, ..., each as TI consecutive items (its sample tiles
+// when TI > 1).
+template <int TI>
+struct Items {
+    int64_t k;
+    int ti = 0;
+    __device__ explicit Items(int64_t k0) : k(k0) {}
+    __device__ void next()
+    {
+        if (++ti == TI) {
+            ti = 0;
+            k += gridDim.x;
+        }
+    }
+};
+
 // nothing to do after a group's copies are issued
 struct NoAfterIssue {
     __device__ bool operator()(int, uint32_t) const { return true; }
@@ -481,8 +498,10 @@ struct NoAfterIssue {
 // the stage barrier and before its MMAs read the stage.  `after(s, ph)` runs
 // once per group, with the group's stage and phase, right after the copies of
 // the next group are issued (the last group's after the loop); it returns
-// false if a wait in it gave up.
-template <int F_ = 0, int U_ = 0, bool PAIR = false, typename IssueTma, typename AfterIssue = NoAfterIssue>
+// false if a wait in it gave up.  TI > 1: each group is TI items, item ti
+// gathering samples 128 ti .. 128 ti + 127 (and the TMA copies again).
+template <int F_ = 0, int U_ = 0, bool PAIR = false, int TI = 1, typename IssueTma,
+          typename AfterIssue = NoAfterIssue>
 __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t stage_bytes, int S,
                                               int64_t K, const uint16_t *idx_s, const uint16_t *hT,
                                               int ldB, int F, int MT, uint32_t tma_bytes,
@@ -490,6 +509,7 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
                                               IssueTma issue_tma, int ishift = 0,
                                               AfterIssue after = AfterIssue())
 {
+    static_assert(TI == 1 || !PAIR, "pairs hold one sample tile");
     const int t = threadIdx.x;  // producer threads are 0 .. kProdWarps*32-1
     const int lane = t & 31;
     const int units = MT * 16;
@@ -504,11 +524,12 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
     Ring r;
     int prev_s = 0;
     uint32_t prev_ph = 0;
-    for (int64_t k = blockIdx.x; k < K; k += gridDim.x, ++it, r.next(S)) {
+    for (Items<TI> itm(blockIdx.x); itm.k < K; itm.next(), ++it, r.next(S)) {
+        const int64_t k = itm.k;
         const int s = r.i;
         const uint32_t ph = r.ph;
         GatherIdx nxt = cur, nxt2 = cur2;
-        if (k + gridDim.x < K) {
+        if (itm.ti == TI - 1 && k + gridDim.x < K) {
             nxt = gather_idx_of(idx_s, PAIR ? 2 * (k + gridDim.x) : (k + gridDim.x) >> ishift, F, lane);
             if (PAIR)
                 nxt2 = gather_idx_of(idx_s, 2 * (k + gridDim.x) + 1, F, lane);
@@ -522,10 +543,11 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
             mbar_arrive_expect_tx(bar_addr(c.full[s]), tma_bytes);
             issue_tma(k, A, bar_addr(c.full[s]));
         }
+        const uint16_t *hTi = TI > 1 ? hT + itm.ti * 128 : hT;
         if constexpr (F_ > 0)
-            issue_gather_t<F_, U_, PAIR>(hT, ldB, A, cur, lane, cur2);
+            issue_gather_t<F_, U_, PAIR>(hTi, ldB, A, cur, lane, cur2);
         else
-            issue_gather(hT, ldB, A, F, units, cur, lane);
+            issue_gather(hTi, ldB, A, F, units, cur, lane);
         cp_async_arrive_noinc(bar_addr(c.full[s]));
         FW_TRACE(2, it);
         cur = nxt;
@@ -998,6 +1020,7 @@ constexpr int kFWBudget = 224 * 1024;
 struct FWPlan {
     bool ok = false;
     int MT = 0, FT = 0, nk = 0, S = 0, zsw = 0, nzc = 0, nslot = 0;
+    int TI = 1;  // sample tiles of a group streamed through the stages as separate items (MT = 1)
     int gs = 0, sub = 1;  // labels per kernel group (a subgroup sharing I_k) and subgroups per group
     uint32_t a_bytes = 0, w_bytes = 0, stage_bytes = 0, dz_bytes = 0, stg_bytes = 0, zcols = 0, wcols = 0,
              tmem_cols = 0, pad_bytes = 0;
@@ -1006,8 +1029,11 @@ struct FWPlan {
     uint32_t f16_bytes = 0;
 };
 
-// the plan for groups of Gv labels (Gv = G, or a subgroup size)
-FWPlan plan_fwdw_g(const sg_layout *lo, int B, int Gv)
+// the plan for groups of Gv labels (Gv = G, or a subgroup size).  `stream`
+// (B > 128): a group's two sample tiles pass through the stages as two items
+// of one tile each, the dW MMA accumulating over both, so a stage, the dZ
+// buffers and the fp16 staging hold one tile's rows.
+FWPlan plan_fwdw_g(const sg_layout *lo, int B, int Gv, bool stream = false)
 {
     FWPlan p;
     if (!shape_ok(lo) || !dz_ok(Gv) || (lo->F != 64 && lo->F != 128 && lo->F != 256) ||
@@ -1016,6 +1042,14 @@ FWPlan plan_fwdw_g(const sg_layout *lo, int B, int Gv)
     p.MT = (B + 127) / 128;
     if (p.MT * 128 > lo->ldB)
         return p;
+    if (stream) {
+        // the items' rows are contiguous in the workspace tile only with one
+        // 64-column chunk
+        if (p.MT < 2 || Gv > 64)
+            return p;
+        p.TI = p.MT;
+        p.MT = 1;
+    }
     // dW tiles of M = 128 rows of f; with F = 64 the upper 64 accumulator
     // lanes read the next 64 rows of shared memory and are never stored
     p.FT = (lo->F + 127) / 128;
@@ -1057,13 +1091,17 @@ FWPlan plan_fwdw_g(const sg_layout *lo, int B, int Gv)
     return p;
 }
 
-// Groups whose tiles do not fit the fused kernel (G = 64 at B = 256) run as
-// subgroups of half the labels sharing the group's I_k: the kernel then sees
-// K * sub groups of G / sub labels, each with its own workspace tile.
+// Groups whose two sample tiles do not fit the fused kernel together (G = 64
+// at B = 256) stream the tiles as separate items; groups that fit neither way
+// run as subgroups of half the labels sharing the group's I_k: the kernel then
+// sees K * sub groups of G / sub labels, each with its own workspace tile.
 FWPlan plan_fwdw(const sg_layout *lo, int B)
 {
-    for (int gs = lo->G; gs >= 16 && lo->G % gs == 0; gs /= 2) {
+    // subgroups of G, G / 2 or G / 4 labels
+    for (int gs = lo->G; gs >= 16 && lo->G % gs == 0 && 4 * gs >= lo->G; gs /= 2) {
         FWPlan p = plan_fwdw_g(lo, B, gs);
+        if (!p.ok)
+            p = plan_fwdw_g(lo, B, gs, true);
         if (p.ok) {
             p.gs = gs;
             p.sub = lo->G / gs;
@@ -1121,7 +1159,14 @@ struct CtlFW {
 // gradients, with dZ block-diagonal in shared memory (the off-diagonal
 // blocks are cleared once and never written).  Each layout group's fp16 dZ
 // tile is written as without pairing.
-template <int G_, int FK, int MT, bool SGD, bool PAIR = false>
+//
+// TI = 2 (B > 128, one 64-column dZ chunk): a group's two sample tiles are two
+// items, each with its own stage (H rows of its 128 samples and W_k), forward
+// MMA, BCE and dZ buffer; the dW MMA accumulates over both items and the dW
+// warps see the group once.  A group of 64 labels then needs the shared
+// memory of one tile instead of two, and runs as one group with N = 64 MMAs
+// instead of two subgroups of 32 with twice as many.
+template <int G_, int FK, int MT, bool SGD, bool PAIR = false, int TI = 1>
 __global__ void __launch_bounds__(kFWThreads, 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
 {
@@ -1130,9 +1175,10 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     // half a layout group's columns, so that both BCE warps of a lane quarter
     // work on its diagonal block), dZ row width (swizzle) and 64-column chunks
     // of the dZ tile
-    constexpr int CH = PAIR ? G_ / 4 : G_ >= 64 ? 32 : 16;
+    constexpr int CH = PAIR ? G_ / 4 : G_ >= 64 && TI == 1 ? 32 : 16;
     constexpr int ZSW = G_ * 2 >= 128 ? 128 : G_ * 2;
     constexpr int NZC = G_ * 2 > 128 ? G_ / 64 : 1;
+    static_assert(TI == 1 || (MT == 1 && !PAIR && NZC == 1), "streamed tiles: one tile per item, one dZ chunk");
     __shared__ CtlFW cf;
     Ctl &c = cf.c;
     extern __shared__ uint8_t dsm[];
@@ -1198,7 +1244,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         // stage, so no epilogue warp holds a stage.
         uint32_t wmag = 0;  // running max of |W| bits, two bf16 lanes
         const int t = threadIdx.x;
-        producer_loop<FK * 16, MT * 16, PAIR>(
+        producer_loop<FK * 16, MT * 16, PAIR, TI>(
             c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes, abort_flag, a.status,
             [&](int64_t k, uint32_t A, uint32_t fb) {
                 const uint32_t Wt = A + a.a_bytes;
@@ -1234,7 +1280,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
         int it = 0;
         Ring rs, rz;
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rs.next(S), rz.next(NS)) {
+        for (Items<TI> itm(blockIdx.x); itm.k < a.K; itm.next(), ++it, rs.next(S), rz.next(NS)) {
             const int s = rs.i;
             const int zs = rz.i;
             FW_TRACE(0, it);
@@ -1278,13 +1324,14 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         const uint32_t zlayout = layout_for_swizzle(ZSW);
         const uint32_t idesc = idesc_bf16(128, 2 * G, 0, 1);  // N = [hi | lo] along j
         int it = 0;
-        Ring rs, rw;
-        for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rs.next(S), rw.next(NS)) {
+        Ring rs, rw;  // rs per item, rw per group
+        for (Items<TI> itm(blockIdx.x); itm.k < a.K; itm.next(), ++it, rs.next(S)) {
+            const int64_t k = itm.k;
             const int s = rs.i;
             const int ws = rw.i;
             const int db = it & 1;
             FW_TRACE(0, it);
-            if (!mbar_wait(bar_addr(cf.wempty[ws]), rw.ph ^ 1u, abort_flag, a.status))
+            if (itm.ti == 0 && !mbar_wait(bar_addr(cf.wempty[ws]), rw.ph ^ 1u, abort_flag, a.status))
                 break;
             FW_TRACE(1, it);
             tc_fence_after();
@@ -1300,7 +1347,8 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             if (lane == 0 && a.f16_bytes) {
                 // the staged fp16 tile to the workspace; its shared-memory
                 // reads are waited for before the buffer is released (dzempty)
-                bulk_store(a.dZt + (size_t)k * a.tile_bytes, f160 + (uint32_t)db * a.f16_bytes, a.f16_bytes);
+                bulk_store(a.dZt + (size_t)k * a.tile_bytes + (size_t)itm.ti * a.f16_bytes,
+                           f160 + (uint32_t)db * a.f16_bytes, a.f16_bytes);
                 bulk_commit();
             }
             if (lane == 0) {
@@ -1310,6 +1358,9 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 const uint64_t ad0 = sdesc(A, 16, 1024, kLayoutSW128);
                 const uint64_t bd0 = sdesc(base + (uint32_t)db * kDzBytes, zchunk, 8 * ZSW, zlayout);
 #pragma unroll
+                // the second and later items of a group add to its accumulator
+                const uint32_t acc0 = TI > 1 && itm.ti > 0 ? 1u : 0u;
+#pragma unroll
                 for (int tf = 0; tf < NT; ++tf) {
                     const uint32_t d = tbase + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G);
 #pragma unroll
@@ -1317,15 +1368,18 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                         mma_bf16(d,
                                  ad0 + (uint64_t)(((uint32_t)(st / 4) * FK * 2048 + (uint32_t)tf * 128 * 128 +
                                                    (uint32_t)(st % 4) * 32) >> 4),
-                                 bd0 + (uint64_t)(((uint32_t)st * 16 * ZSW) >> 4), idesc, st > 0 ? 1u : 0u);
+                                 bd0 + (uint64_t)(((uint32_t)st * 16 * ZSW) >> 4), idesc, st > 0 ? 1u : acc0);
                 }
-                mma_commit(bar_addr(cf.wfull[ws]));
+                if (itm.ti == TI - 1)
+                    mma_commit(bar_addr(cf.wfull[ws]));
                 if (a.f16_bytes)
                     bulk_wait_read<0>();  // the fp16 tile store has read the buffer
                 mma_commit(bar_addr(cf.dzempty[db]));
                 mma_commit(bar_addr(c.empty[s]));  // last reader of the stage's H_k
             }
             __syncwarp();
+            if (itm.ti == TI - 1)
+                rw.next(NS);
         }
         if (lane == 0) {
             if (a.f16_bytes)
@@ -1357,16 +1411,22 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             }
             int it = 0;
             Ring rz;
-            for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rz.next(NS)) {
+            int e0 = 0, e1 = 0, e2 = 0;
+            for (Items<TI> itm(blockIdx.x); itm.k < a.K; itm.next(), ++it, rz.next(NS)) {
+                const int64_t k = itm.k;
                 const int zs = rz.i;
                 const int db = it & 1;
-                const int e0 = e0n, e1 = e1n, e2 = e2n;
-                if (k + gridDim.x < a.K) {
-                    const int64_t kl = PAIR ? 2 * (k + gridDim.x) : (k + gridDim.x) >> a.sub_shift;
-                    e0n = __ldg(a.gptr + kl);
-                    e1n = __ldg(a.gptr + kl + 1);
-                    if (PAIR)
-                        e2n = __ldg(a.gptr + kl + 2);
+                if (itm.ti == 0) {
+                    e0 = e0n;
+                    e1 = e1n;
+                    e2 = e2n;
+                    if (k + gridDim.x < a.K) {
+                        const int64_t kl = PAIR ? 2 * (k + gridDim.x) : (k + gridDim.x) >> a.sub_shift;
+                        e0n = __ldg(a.gptr + kl);
+                        e1n = __ldg(a.gptr + kl + 1);
+                        if (PAIR)
+                            e2n = __ldg(a.gptr + kl + 2);
+                    }
                 }
                 // columns of the layout group this kernel group starts at
                 const int coff = (int)(k & ((1 << a.sub_shift) - 1)) * G;
@@ -1407,11 +1467,12 @@ __global__ void __launch_bounds__(kFWThreads, 1)
 #pragma unroll
                 for (int u = sub; u < zunits; u += 2) {
                     const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
-                    const int b = t * 128 + q * 32 + lane;
+                    const int b = t * 128 + q * 32 + lane;  // row of the item's tiles
+                    const int bg = TI > 1 ? itm.ti * 128 + b : b;  // sample
                     float v[CH];
                     tmem_ld_chunk<CH>(tbase + lane_off + (uint32_t)(zs * a.zcols + t * G + c0), v);
-                    if (b < a.B) {
-                        const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, b, coff + c0, CH) : 0u;
+                    if (bg < a.B) {
+                        const uint32_t y = e1 > e0 ? group_pos_mask(a.gent, e0, e1, bg, coff + c0, CH) : 0u;
                         lf += bce_chunk_ftz<CH>(v, y);
                     } else {
 #pragma unroll
@@ -1425,7 +1486,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                         store_dz_tile_f16<CH>(base_ptr + (f160 - base) + (size_t)db * a.f16_bytes, b, c0, v, ZSW,
                                               MT * 128);
                     else
-                        store_dz_tile_f16<CH>(a.dZt + (size_t)k * a.tile_bytes, b, c0, v, ZSW, MT * 128);
+                        store_dz_tile_f16<CH>(a.dZt + (size_t)k * a.tile_bytes, bg, c0, v, ZSW, TI * MT * 128);
                 }
                 }
                 FW_TRACE(3, it);
@@ -2067,7 +2128,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.loss_part = lo->loss_part;
     a.status = lo->status;
     a.K = pair ? lo->K / 2 : lo->K * p.sub;
-    a.sub_shift = p.sub == 4 ? 2 : p.sub == 2 ? 1 : 0;
+    a.sub_shift = log2_exact(p.sub);  // 0, 1 or 2
     a.L = lo->L;
     a.B = B;
     a.G = p.gs;
@@ -2079,7 +2140,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.zsw = p.zsw;
     a.nzc = p.nzc;
     a.nslot = p.nslot;
-    a.Bp = p.MT * 128;
+    a.Bp = p.TI * p.MT * 128;
     a.ldB = lo->ldB;
     a.a_bytes = p.a_bytes;
     a.w_bytes = p.w_bytes;
@@ -2089,15 +2150,21 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.zcols = p.zcols;
     a.wcols = p.wcols;
     a.tmem_cols = p.tmem_cols;
-    // the staged tile is the kernel group's whole workspace tile
-    a.f16_bytes = (uint64_t)p.f16_bytes == a.tile_bytes ? p.f16_bytes : 0u;
+    // the staged rows are the kernel group's whole workspace tile (with
+    // streamed tiles, the item's share of it)
+    a.f16_bytes = (uint64_t)p.f16_bytes * p.TI == a.tile_bytes ? p.f16_bytes : 0u;
     const size_t smem = 2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + 2 * (size_t)p.f16_bytes +
                         (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
     const int grid = persistent_grid(lo, a.K);
     void (*kern)(CUtensorMap, FWArgs) = nullptr;
 #define SG_FW_PICK(GG, KK, MM)                                           \
-    if (!pair && p.gs == GG && lo->F == KK * 16 && p.MT == MM)          \
+    if (!pair && p.TI == 1 && p.gs == GG && lo->F == KK * 16 && p.MT == MM) \
         kern = sgd ? k_tc_fwdw<GG, KK, MM, true> : k_tc_fwdw<GG, KK, MM, false>;
+#define SG_FW_STREAM(GG, KK)                                             \
+    if (!pair && p.TI == 2 && p.gs == GG && lo->F == KK * 16)           \
+        kern = sgd ? k_tc_fwdw<GG, KK, 1, true, false, 2> : k_tc_fwdw<GG, KK, 1, false, false, 2>;
+    SG_FW_STREAM(16, 16) SG_FW_STREAM(32, 16) SG_FW_STREAM(64, 4) SG_FW_STREAM(64, 8)
+#undef SG_FW_STREAM
 #define SG_FW_PAIR(GG, KK)                                               \
     if (pair && p.gs == GG && lo->F == KK * 16)                         \
         kern = sgd ? k_tc_fwdw<GG, KK, 1, true, true> : k_tc_fwdw<GG, KK, 1, false, true>;

@@ -49,10 +49,11 @@
  *       B <= 128          256         256       160        32      (dh only)
  *       B <= 256          192         176       144     (dh only)  (dh only)
  *   and also, through the fused forward + BCE + dW kernel (F = 64, 128 or
- *   256), at G = 128, F = 256 (B <= 128) and at G = 256, F = 64 or 128
- *   (F = 256 too for B <= 128).  dh runs on them for every such G and F.  A
- *   phase outside that runs on CUDA cores (SG_ENGINE_TC makes it an error
- *   instead).  Groups whose tiles do not fit the fused kernel run there as
+ *   256), at F = 256 for every G up to 128 and at G = 256 with F = 64 or
+ *   128.  dh runs on them for every such G and F.  A phase outside that runs
+ *   on CUDA cores (SG_ENGINE_TC makes it an error instead).  With B > 128 the
+ *   fused kernel takes a group's two sample tiles one after the other where
+ *   both do not fit it together; groups that still do not fit run there as
  *   subgroups of G/2 or G/4 labels sharing I_k, and groups of more than 64
  *   labels enter dh as subgroups of at most 64.  Every other G
  *   (including G = 1, per-label fixed fan-in) runs on the CUDA-core engine.

@@ -43,6 +43,8 @@ SHAPES = [
     ("tc_ragged", 37, 320, 16 * 61, 16, 128),
     ("fused_b100", 100, 768, 32 * 301, 32, 128),
     ("b256_g64", 256, 768, 64 * 21, 64, 128),
+    ("b200_g64_f64", 200, 640, 64 * 27, 64, 64),
+    ("b256_g256", 256, 512, 256 * 5, 256, 128),
     ("one_kernel_f48", 70, 200, 32 * 45, 32, 48),
     ("g1", 45, 256, 333, 1, 64),
     ("pair_b40", 40, 256, 16 * 60, 16, 128),

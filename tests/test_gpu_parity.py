@@ -44,8 +44,16 @@ CASES = [
     (_w("tc_b37_h320", B=37, H=320, L=16 * 64, G=16, F=128, pos=4), (SIMT, TC)),
     (_w("tc_g128", B=100, H=768, L=128 * 20, G=128, F=128, pos=6, dist="zipf"), (SIMT, TC)),
     (_w("tc_h1000", B=130, H=1000, L=32 * 40, G=32, F=128, pos=6), (SIMT, TC)),
-    # B = 256 at G = 64: dW streams the two sample tiles through its stages
+    # B = 256 at G = 64: the fused kernel takes the two sample tiles one
+    # after the other (dW accumulated over both), F = 128 and F = 64; F = 256
+    # the same way at G = 16 and G = 32 (ragged B), at G = 64 as subgroups of
+    # 32; G = 256 as four subgroups of 64
     (_w("g64_b256", B=256, H=768, L=64 * 30, G=64, F=128, pos=5, dist="zipf"), (SIMT, TC)),
+    (_w("g64_b200_f64", B=200, H=640, L=64 * 27, G=64, F=64, pos=5, dist="zipf"), (SIMT, TC)),
+    (_w("g32_b150_f256", B=150, H=512, L=32 * 25, G=32, F=256, pos=4), (SIMT, TC)),
+    (_w("g16_b256_f256", B=256, H=384, L=16 * 41, G=16, F=256, pos=4), (SIMT, TC)),
+    (_w("g64_b256_f256", B=256, H=512, L=64 * 9, G=64, F=256, pos=4), (SIMT, TC)),
+    (_w("g256_b256", B=256, H=512, L=256 * 5, G=256, F=128, pos=6, dist="zipf"), (SIMT, TC)),
     # the fused kernel on subgroups sharing I_k: G = 128 at B = 256, G = 256
     (_w("g128_b256_sub", B=256, H=512, L=128 * 12, G=128, F=128, pos=6, dist="zipf"), (SIMT, TC)),
     (_w("g256_f64_sub", B=100, H=384, L=256 * 8, G=256, F=64, pos=6, dist="zipf"), (SIMT, TC)),
@@ -255,12 +263,12 @@ _BY_NAME = {w.name: w for w, _ in CASES}
 
 # kernels each workload shape launches: the fused forward + BCE + dW kernel
 # and the dh kernel
-_FUSED_KINDS = {"like3m": {"prep", "fwd", "dh"}, "like8p6m": {"prep", "fwd", "dh"},
-                "like670k": {"prep", "fwd", "dh"}, "g64_b256": {"prep", "fwd", "dh"},
-                "g128_b256_sub": {"prep", "fwd", "dh"}}
+_FUSED = ["like3m", "like670k", "like8p6m", "g64_b256", "g128_b256_sub", "g64_b200_f64",
+          "g32_b150_f256", "g16_b256_f256", "g64_b256_f256", "g256_b256"]
+_FUSED_KINDS = {n: {"prep", "fwd", "dh"} for n in _FUSED}
 
 
-@pytest.mark.parametrize("name", ["like3m", "like670k", "like8p6m", "g64_b256", "g128_b256_sub"])
+@pytest.mark.parametrize("name", _FUSED)
 def test_step_fused_on_tensor_cores(name, oracle_mod):
     """The shapes of the three label-space workloads run the whole step on
     the tensor cores (engine pinned: a CUDA-core fallback would raise) through
@@ -361,7 +369,8 @@ def test_step_single_kernel_large_weights(oracle_mod):
     assert float(loss.item()) == pytest.approx(ref["loss"], rel=LOSS_RTOL)
 
 
-@pytest.mark.parametrize("name", ["tiny", "like3m", "like670k", "like8p6m", "b256_f256"])
+@pytest.mark.parametrize("name", ["tiny", "like3m", "like670k", "like8p6m", "b256_f256", "g64_b256",
+                                  "g64_b200_f64"])
 def test_step_sgd_two_steps(name, oracle_mod):
     """sg_step_sgd against the oracle's step followed by its momentum-SGD update
     (Loss and training strategy), twice, each step from the library's own W and
@@ -553,7 +562,8 @@ _TC_MAX_F = {128: {16: 256, 32: 256, 64: 256, 128: 160, 192: 32, 256: 0},
              256: {16: 192, 32: 192, 64: 176, 128: 144, 192: 0, 256: 0}}
 # F beyond that which the fused forward + BCE + dW kernel still takes (as
 # subgroups of the group sharing I_k)
-_TC_FUSED_EXTRA = {128: {128: {256}, 256: {64, 128, 256}}, 256: {256: {64, 128}}}
+_TC_FUSED_EXTRA = {128: {128: {256}, 256: {64, 128}},
+                   256: {16: {256}, 32: {256}, 64: {256}, 128: {256}, 256: {64, 128}}}
 
 
 def test_step_plan_matches_documented_range():
