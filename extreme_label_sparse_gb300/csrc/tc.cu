@@ -1091,17 +1091,21 @@ FWPlan plan_fwdw_g(const sg_layout *lo, int B, int Gv, bool stream = false)
     return p;
 }
 
-// Groups whose two sample tiles do not fit the fused kernel together (G = 64
-// at B = 256) stream the tiles as separate items; groups that fit neither way
-// run as subgroups of half the labels sharing the group's I_k: the kernel then
-// sees K * sub groups of G / sub labels, each with its own workspace tile.
+// With B > 128, groups of 32 or more labels stream their two sample tiles as
+// separate items (at B = 256, F = 128: 5 % faster than both tiles in one
+// stage at G = 32, and the only way G = 64 fits); groups of 16 keep both
+// tiles in one stage (streaming measured 3.5 % slower) unless they do not
+// fit.  Groups that fit neither way run as subgroups of half the labels
+// sharing the group's I_k: the kernel then sees K * sub groups of G / sub
+// labels, each with its own workspace tile.
 FWPlan plan_fwdw(const sg_layout *lo, int B)
 {
     // subgroups of G, G / 2 or G / 4 labels
     for (int gs = lo->G; gs >= 16 && lo->G % gs == 0 && 4 * gs >= lo->G; gs /= 2) {
-        FWPlan p = plan_fwdw_g(lo, B, gs);
+        const bool stream_first = gs >= 32;
+        FWPlan p = plan_fwdw_g(lo, B, gs, stream_first);
         if (!p.ok)
-            p = plan_fwdw_g(lo, B, gs, true);
+            p = plan_fwdw_g(lo, B, gs, !stream_first);
         if (p.ok) {
             p.gs = gs;
             p.sub = lo->G / gs;
@@ -2070,7 +2074,6 @@ sg_status tc_fwd(sg_layout *lo, int32_t B, const uint16_t *W, uint16_t *Z, uint1
     return SG_OK;
 }
 
-bool tc_fwdw_ok(const sg_layout *lo, int32_t B) { return plan_fwdw(lo, B).ok; }
 
 // Pairs of groups (the kernel's PAIR form) when one 64-sample chunk holds a
 // group's samples: B <= 64, G of 16 or 32 (pairs of 32 or 64 columns), an
@@ -2088,12 +2091,55 @@ FWPlan plan_fwdw_pair(const sg_layout *lo, int B)
     return p;
 }
 
+using FwdwKernel = void (*)(CUtensorMap, FWArgs);
+
+// The instance for a plan (nullptr: none).  Only the instances some plan
+// reaches are built: with B > 128 subgroups of 32 and 64 labels always
+// stream their sample tiles, and G = 64, F = 256 runs as subgroups of 32.
+FwdwKernel fwdw_kernel(const FWPlan &p, int F, bool pair, bool sgd)
+{
+    FwdwKernel kern = nullptr;
+#define SG_FW_PICK(GG, KK, MM)                                           \
+    if (!pair && p.TI == 1 && p.gs == GG && F == KK * 16 && p.MT == MM)  \
+        kern = sgd ? k_tc_fwdw<GG, KK, MM, true> : k_tc_fwdw<GG, KK, MM, false>;
+#define SG_FW_STREAM(GG, KK)                                             \
+    if (!pair && p.TI == 2 && p.gs == GG && F == KK * 16)               \
+        kern = sgd ? k_tc_fwdw<GG, KK, 1, true, false, 2> : k_tc_fwdw<GG, KK, 1, false, false, 2>;
+#define SG_FW_PAIR(GG, KK)                                               \
+    if (pair && p.gs == GG && F == KK * 16)                             \
+        kern = sgd ? k_tc_fwdw<GG, KK, 1, true, true> : k_tc_fwdw<GG, KK, 1, false, true>;
+    SG_FW_PICK(16, 4, 1) SG_FW_PICK(16, 4, 2) SG_FW_PICK(16, 8, 1) SG_FW_PICK(16, 8, 2) SG_FW_PICK(16, 16, 1)
+    SG_FW_PICK(32, 4, 1) SG_FW_PICK(32, 8, 1) SG_FW_PICK(32, 16, 1)
+    SG_FW_PICK(64, 4, 1) SG_FW_PICK(64, 8, 1)
+    SG_FW_STREAM(16, 16) SG_FW_STREAM(32, 4) SG_FW_STREAM(32, 8) SG_FW_STREAM(32, 16) SG_FW_STREAM(64, 4)
+    SG_FW_STREAM(64, 8)
+    SG_FW_PAIR(32, 4) SG_FW_PAIR(32, 8) SG_FW_PAIR(32, 16) SG_FW_PAIR(64, 4) SG_FW_PAIR(64, 8) SG_FW_PAIR(64, 16)
+#undef SG_FW_PICK
+#undef SG_FW_STREAM
+#undef SG_FW_PAIR
+    return kern;
+}
+
+// the step's fused kernel for a plan: pairs of groups where they apply
+static FWPlan fwdw_plan_of(const sg_layout *lo, int32_t B, bool *pair)
+{
+    const FWPlan pp = plan_fwdw_pair(lo, B);
+    *pair = pp.ok;
+    return pp.ok ? pp : plan_fwdw(lo, B);
+}
+
+bool tc_fwdw_ok(const sg_layout *lo, int32_t B)
+{
+    bool pair = false;
+    const FWPlan p = fwdw_plan_of(lo, B, &pair);
+    return p.ok && fwdw_kernel(p, lo->F, pair, false) != nullptr;
+}
+
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
                   const sg_sgd *sgd, double *loss, cudaStream_t st)
 {
-    const FWPlan pp = plan_fwdw_pair(lo, B);
-    const bool pair = pp.ok;
-    const FWPlan p = pair ? pp : plan_fwdw(lo, B);
+    bool pair = false;
+    const FWPlan p = fwdw_plan_of(lo, B, &pair);
     if (!p.ok) {
         sg_set_error("tc_fwdw: shape not supported by the fused forward + dW kernel");
         return SG_ERR_UNSUPPORTED;
@@ -2156,26 +2202,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     const size_t smem = 2 * (size_t)p.dz_bytes + 2 * (size_t)p.stg_bytes + 2 * (size_t)p.f16_bytes +
                         (size_t)p.S * p.stage_bytes + p.pad_bytes + 1024;
     const int grid = persistent_grid(lo, a.K);
-    void (*kern)(CUtensorMap, FWArgs) = nullptr;
-#define SG_FW_PICK(GG, KK, MM)                                           \
-    if (!pair && p.TI == 1 && p.gs == GG && lo->F == KK * 16 && p.MT == MM) \
-        kern = sgd ? k_tc_fwdw<GG, KK, MM, true> : k_tc_fwdw<GG, KK, MM, false>;
-#define SG_FW_STREAM(GG, KK)                                             \
-    if (!pair && p.TI == 2 && p.gs == GG && lo->F == KK * 16)           \
-        kern = sgd ? k_tc_fwdw<GG, KK, 1, true, false, 2> : k_tc_fwdw<GG, KK, 1, false, false, 2>;
-    SG_FW_STREAM(16, 16) SG_FW_STREAM(32, 16) SG_FW_STREAM(64, 4) SG_FW_STREAM(64, 8)
-#undef SG_FW_STREAM
-#define SG_FW_PAIR(GG, KK)                                               \
-    if (pair && p.gs == GG && lo->F == KK * 16)                         \
-        kern = sgd ? k_tc_fwdw<GG, KK, 1, true, true> : k_tc_fwdw<GG, KK, 1, false, true>;
-    SG_FW_PAIR(32, 4) SG_FW_PAIR(32, 8) SG_FW_PAIR(32, 16) SG_FW_PAIR(64, 4) SG_FW_PAIR(64, 8) SG_FW_PAIR(64, 16)
-#undef SG_FW_PAIR
-    SG_FW_PICK(16, 4, 1) SG_FW_PICK(16, 4, 2) SG_FW_PICK(32, 4, 1) SG_FW_PICK(32, 4, 2)
-    SG_FW_PICK(64, 4, 1) SG_FW_PICK(64, 4, 2)
-    SG_FW_PICK(16, 8, 1) SG_FW_PICK(16, 8, 2) SG_FW_PICK(16, 16, 1) SG_FW_PICK(16, 16, 2)
-    SG_FW_PICK(32, 8, 1) SG_FW_PICK(32, 8, 2) SG_FW_PICK(32, 16, 1) SG_FW_PICK(32, 16, 2)
-    SG_FW_PICK(64, 8, 1) SG_FW_PICK(64, 8, 2) SG_FW_PICK(64, 16, 1) SG_FW_PICK(64, 16, 2)
-#undef SG_FW_PICK
+    void (*kern)(CUtensorMap, FWArgs) = fwdw_kernel(p, lo->F, pair, sgd != nullptr);
     if (!kern) {
         sg_set_error("tc_fwdw: G = %d, F = %d has no fused kernel", lo->G, lo->F);
         return SG_ERR_UNSUPPORTED;
