@@ -1820,11 +1820,16 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         // NB = 2 teams of kDhBuilders / 2 warps take turns at the units (team
         // t: units t, t + 2, ..., always Ws buffer t), so the teams build
         // concurrently while the MMAs consume.  Team thread tt handles the
-        // slots e = tt, tt + NT, ... of the unit's P x F (group g = e / F,
-        // feature f = e % F; F <= 256).
+        // slots e = tt, tt + NT, ... of the unit's P x HS x F (group
+        // g = e / (HS F), then the half h of the row, then feature f; F <= 256).
+        // A row of 64 labels is two slots of 32: one slot per (g, f) left half
+        // the team idle at F = 128 and gave the other half twice the chain of
+        // dependent loads (G = 64, B = 256, F = 128: 1-2 % slower).
         const int NT = kDhBuilders * 32 / NB;  // threads of a team
         constexpr int NT_MIN = kDhBuilders * 32 / 2;
-        constexpr int NSLOT = (P * 256 + NT_MIN - 1) / NT_MIN;
+        constexpr int HS = G == 64 ? 2 : 1;  // slots per Ws row
+        constexpr int NCWH = NCW / HS;       // 16-byte units of a slot
+        constexpr int NSLOT = (P * HS * 256 + NT_MIN - 1) / NT_MIN;
         const int tb = threadIdx.x - kDhFirstEpi * 32;  // 0 .. kDhBuilders * 32 - 1
         const int team = tb / NT, tt = tb - team * NT;
         const int q = warp & 3, sub = (warp - kDhFirstEpi) / 4;
@@ -1845,13 +1850,15 @@ __global__ void __launch_bounds__(kDhThreads, 1)
 #pragma unroll
         for (int x = 0; x < NSLOT; ++x)
             prev[x] = -1;
-        // (group, feature) of each slot: fixed per thread
-        int gsl[NSLOT], fsl[NSLOT];
+        // (group, row half, feature) of each slot: fixed per thread
+        int gsl[NSLOT], fsl[NSLOT], hsl[NSLOT];
 #pragma unroll
         for (int x = 0; x < NSLOT; ++x) {
             const int e = tt + x * NT;
-            gsl[x] = e / F;
-            fsl[x] = e - gsl[x] * F;
+            gsl[x] = e / (HS * F);
+            const int r = e - gsl[x] * HS * F;
+            hsl[x] = HS > 1 ? r / F : 0;
+            fsl[x] = r - hsl[x] * F;
         }
         int it = team;
         uint32_t wph = 0;
@@ -1865,23 +1872,24 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             DH_TRACE(1, it);
             const uint8_t *st = stage0_ptr + (size_t)s * a.stage_bytes;
             // this thread's rows, read from the stage before waiting for the buffer
-            uint4 row[NSLOT][NCW];
+            uint4 row[NSLOT][NCWH];
             int dst[NSLOT];
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
                 dst[x] = -1;
                 const int g = gsl[x], f = fsl[x];
-                if (ok && g < np && x * NT < P * F) {
+                if (ok && g < np && x * NT < P * HS * F) {
                     const int i = (int)reinterpret_cast<const uint16_t *>(st + ioff + (size_t)g * a.i_bytes)[f] - i0;
                     if (i >= 0 && i < BW) {
                         dst[x] = g * BW + i;
                         // column f of W_k ([G][F] row-major): consecutive
                         // threads read consecutive f
-                        const uint16_t *Wk = reinterpret_cast<const uint16_t *>(st + woff + (size_t)g * a.w_bytes) + f;
+                        const uint16_t *Wk = reinterpret_cast<const uint16_t *>(st + woff + (size_t)g * a.w_bytes) + f +
+                                             (size_t)hsl[x] * NCWH * 8 * F;
                         if (F16 && scaled)
-                            read_w_column<NCW, true, true>(Wk, F, down, row[x]);
+                            read_w_column<NCWH, true, true>(Wk, F, down, row[x]);
                         else
-                            read_w_column<NCW, F16, false>(Wk, F, down, row[x]);
+                            read_w_column<NCWH, F16, false>(Wk, F, down, row[x]);
                     }
                 }
             }
@@ -1893,13 +1901,15 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                 break;  // the whole team leaves together
             DH_TRACE(4, it);
             // zero the rows of the buffer's last unit, then write this unit's
+            // (the slots of one row share its (g, f), hence its row: together
+            // they clear all of it, each its own span of 16-byte units)
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
                 if (prev[x] >= 0) {
                     uint8_t *d = Wb + (size_t)prev[x] * RB;
 #pragma unroll
-                    for (int u = 0; u < NCW; ++u)
-                        *reinterpret_cast<uint4 *>(d + (u << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    for (int u = 0; u < NCWH; ++u)
+                        *reinterpret_cast<uint4 *>(d + ((hsl[x] * NCWH + u) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             named_bar(1 + team, NT);
@@ -1910,8 +1920,8 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                     uint8_t *d = Wb + (size_t)dst[x] * RB;
                     const int sw = swz_of(dst[x], RB);
 #pragma unroll
-                    for (int u = 0; u < NCW; ++u)
-                        *reinterpret_cast<uint4 *>(d + ((u ^ sw) << 4)) = row[x][u];
+                    for (int u = 0; u < NCWH; ++u)
+                        *reinterpret_cast<uint4 *>(d + (((hsl[x] * NCWH + u) ^ sw) << 4)) = row[x][u];
                 }
                 prev[x] = dst[x];
             }
