@@ -1900,16 +1900,20 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             if (named_bar_any(1 + team, NT, !ok))
                 break;  // the whole team leaves together
             DH_TRACE(4, it);
-            // zero the rows of the buffer's last unit, then write this unit's
-            // (the slots of one row share its (g, f), hence its row: together
-            // they clear all of it, each its own span of 16-byte units)
+            // zero the rows of the buffer's last unit, then write this unit's.
+            // Each slot clears the 16-byte units it wrote there (the slots of
+            // one row share its (g, f), hence its row, and together cover it),
+            // at their swizzled places: unswizzled, every thread of a warp
+            // stored unit u of its row into the same banks (a warp's 32 random
+            // rows, one wavefront each)
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
                 if (prev[x] >= 0) {
                     uint8_t *d = Wb + (size_t)prev[x] * RB;
+                    const int sw = swz_of(prev[x], RB);
 #pragma unroll
                     for (int u = 0; u < NCWH; ++u)
-                        *reinterpret_cast<uint4 *>(d + ((hsl[x] * NCWH + u) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(d + (((hsl[x] * NCWH + u) ^ sw) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             named_bar(1 + team, NT);
