@@ -405,9 +405,10 @@ struct GatherIdx {
     uint32_t i[2];
 };
 
+template <int NPW = kProdWarps>
 __device__ __forceinline__ GatherIdx gather_idx_of(const uint16_t *idx_s, int64_t k, int F, int lane)
 {
-    const int RW = F / kProdWarps;
+    const int RW = F / NPW;
     const int pw = threadIdx.x / 32;
     const uint16_t *I = idx_s + k * F + pw * RW;
     GatherIdx g;
@@ -441,11 +442,11 @@ __device__ __forceinline__ void issue_gather(const uint16_t *hT, int ldB, uint32
 //
 // PAIR (U_ = 16): the second 64-sample chunk holds samples 0 .. 63 of the
 // rows I_k2[f] of a second group instead of samples 64 .. 127 of I_k[f].
-template <int F_, int U_, bool PAIR = false>
+template <int F_, int U_, bool PAIR = false, int NPW = kProdWarps>
 __device__ __forceinline__ void issue_gather_t(const uint16_t *hT, int ldB, uint32_t A, const GatherIdx &g,
                                                int lane, const GatherIdx &g2 = GatherIdx{{0u, 0u}})
 {
-    constexpr int RW = F_ / kProdWarps;
+    constexpr int RW = F_ / NPW;
     constexpr int LPR = U_ < 32 ? U_ : 32;  // lanes per row
     constexpr int RPI = 32 / LPR;           // rows per instruction
     static_assert(RW % RPI == 0 && RW <= 64, "rows per producer warp");
@@ -500,7 +501,7 @@ struct NoAfterIssue {
 // the next group are issued (the last group's after the loop); it returns
 // false if a wait in it gave up.  TI > 1: each group is TI items, item ti
 // gathering samples 128 ti .. 128 ti + 127 (and the TMA copies again).
-template <int F_ = 0, int U_ = 0, bool PAIR = false, int TI = 1, typename IssueTma,
+template <int F_ = 0, int U_ = 0, bool PAIR = false, int TI = 1, int NPW = kProdWarps, typename IssueTma,
           typename AfterIssue = NoAfterIssue>
 __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t stage_bytes, int S,
                                               int64_t K, const uint16_t *idx_s, const uint16_t *hT,
@@ -510,16 +511,16 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
                                               AfterIssue after = AfterIssue())
 {
     static_assert(TI == 1 || !PAIR, "pairs hold one sample tile");
-    const int t = threadIdx.x;  // producer threads are 0 .. kProdWarps*32-1
+    const int t = threadIdx.x;  // producer threads are 0 .. NPW*32-1
     const int lane = t & 31;
     const int units = MT * 16;
     int it = 0;
     // PAIR: kernel group k is the layout groups 2k (first chunk) and 2k + 1
     GatherIdx cur = {{0u, 0u}}, cur2 = {{0u, 0u}};
     if (blockIdx.x < K) {
-        cur = gather_idx_of(idx_s, PAIR ? 2 * (int64_t)blockIdx.x : (int64_t)blockIdx.x >> ishift, F, lane);
+        cur = gather_idx_of<NPW>(idx_s, PAIR ? 2 * (int64_t)blockIdx.x : (int64_t)blockIdx.x >> ishift, F, lane);
         if (PAIR)
-            cur2 = gather_idx_of(idx_s, 2 * (int64_t)blockIdx.x + 1, F, lane);
+            cur2 = gather_idx_of<NPW>(idx_s, 2 * (int64_t)blockIdx.x + 1, F, lane);
     }
     Ring r;
     int prev_s = 0;
@@ -530,9 +531,9 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
         const uint32_t ph = r.ph;
         GatherIdx nxt = cur, nxt2 = cur2;
         if (itm.ti == TI - 1 && k + gridDim.x < K) {
-            nxt = gather_idx_of(idx_s, PAIR ? 2 * (k + gridDim.x) : (k + gridDim.x) >> ishift, F, lane);
+            nxt = gather_idx_of<NPW>(idx_s, PAIR ? 2 * (k + gridDim.x) : (k + gridDim.x) >> ishift, F, lane);
             if (PAIR)
-                nxt2 = gather_idx_of(idx_s, 2 * (k + gridDim.x) + 1, F, lane);
+                nxt2 = gather_idx_of<NPW>(idx_s, 2 * (k + gridDim.x) + 1, F, lane);
         }
         FW_TRACE(0, it);
         if (!mbar_wait(bar_addr(c.empty[s]), ph ^ 1u, abort_flag, status))
@@ -545,7 +546,7 @@ __device__ __forceinline__ void producer_loop(Ctl &c, uint32_t stage0, uint32_t 
         }
         const uint16_t *hTi = TI > 1 ? hT + itm.ti * 128 : hT;
         if constexpr (F_ > 0)
-            issue_gather_t<F_, U_, PAIR>(hTi, ldB, A, cur, lane, cur2);
+            issue_gather_t<F_, U_, PAIR, NPW>(hTi, ldB, A, cur, lane, cur2);
         else
             issue_gather(hTi, ldB, A, F, units, cur, lane);
         cp_async_arrive_noinc(bar_addr(c.full[s]));
@@ -1012,8 +1013,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // warps and four dW warps.
 constexpr int kFWBce = 8;  // BCE warps: two per TMEM lane quarter
 constexpr int kFWDw = 4;   // dW store warps: one per lane quarter
-constexpr int kFWThreads = 32 * (kProdWarps + 2 + kFWBce + kFWDw);
-constexpr int kFWFirstEpi = kProdWarps + 2;
+// Producer warps: four where a stage holds one 128-sample tile (eight
+// measured up to 4 % slower there: each producer warp's per-group costs of
+// waits, index loads, the max |W| pass and arrivals took issue slots from the
+// rest), eight where it holds two (four: 2.4 % slower; twice the gather per
+// group).
+__host__ __device__ constexpr int fw_prod(int MT) { return MT > 1 ? 8 : 4; }
+__host__ __device__ constexpr int fw_threads(int MT) { return 32 * (fw_prod(MT) + 2 + kFWBce + kFWDw); }
 // dynamic shared memory the fused plan may use (the opt-in maximum is 227 KB)
 constexpr int kFWBudget = 224 * 1024;
 
@@ -1171,9 +1177,10 @@ struct CtlFW {
 // memory of one tile instead of two, and runs as one group with N = 64 MMAs
 // instead of two subgroups of 32 with twice as many.
 template <int G_, int FK, int MT, bool SGD, bool PAIR = false, int TI = 1>
-__global__ void __launch_bounds__(kFWThreads, 1)
+__global__ void __launch_bounds__(fw_threads(MT), 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
 {
+    constexpr int NPW = fw_prod(MT), NTHR = fw_threads(MT), FIRST_EPI = NPW + 2;
     static_assert(!PAIR || MT == 1, "pairs share one 128-row sample tile");
     // compile-time group width: column chunk of the epilogue (with pairs,
     // half a layout group's columns, so that both BCE warps of a lane quarter
@@ -1209,7 +1216,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     // reader of H_k) and by the producer warps, which take max |W_k| from it
     // one group after they issued its copies.
     if (threadIdx.x == 0) {
-        setup_ctl(c, S, 0, kProdWarps * 32 + 1, kProdWarps + 1);
+        setup_ctl(c, S, 0, NPW * 32 + 1, NPW + 1);
         for (int i = 0; i < NS && i < 4; ++i) {
             mbar_init(bar_addr(c.tfull[i]), 1);
             mbar_init(bar_addr(c.tempty[i]), kFWBce * 32);
@@ -1224,13 +1231,13 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         }
         fence_mbar_init();
     }
-    if (warp == kProdWarps) {
+    if (warp == NPW) {
         tmem_alloc(smem_u32(&c.tmem), a.tmem_cols);
         tmem_relinquish();
     }
     if (PAIR) {
         // both dZ buffers start zero: the BCE writes only the diagonal blocks
-        for (uint32_t o = threadIdx.x * 16u; o < 2 * a.dz_bytes; o += kFWThreads * 16u)
+        for (uint32_t o = threadIdx.x * 16u; o < 2 * a.dz_bytes; o += NTHR * 16u)
             *reinterpret_cast<uint4 *>(base_ptr + o) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async();  // generic writes -> the dW MMA (async proxy)
     }
@@ -1240,7 +1247,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
 
-    if (warp < kProdWarps) {
+    if (warp < NPW) {
         // ---------------------------------------------------------- producers
         // After issuing a group's copies the producers take max |W| over the
         // previous group's W_k (the scale of the feature gradient's fp16
@@ -1248,7 +1255,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
         // stage, so no epilogue warp holds a stage.
         uint32_t wmag = 0;  // running max of |W| bits, two bf16 lanes
         const int t = threadIdx.x;
-        producer_loop<FK * 16, MT * 16, PAIR, TI>(
+        producer_loop<FK * 16, MT * 16, PAIR, TI, NPW>(
             c, stage0, a.stage_bytes, S, a.K, a.idx_s, a.hT, a.ldB, F, a.MT, a.w_bytes, abort_flag, a.status,
             [&](int64_t k, uint32_t A, uint32_t fb) {
                 const uint32_t Wt = A + a.a_bytes;
@@ -1262,7 +1269,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                 const uint4 *Wsm = reinterpret_cast<const uint4 *>(base_ptr + (stage0 - base) +
                                                                    (size_t)sj * a.stage_bytes + kABytes);
 #pragma unroll
-                for (int x = t; x < (int)(kWBytes / 16); x += kProdWarps * 32) {
+                for (int x = t; x < (int)(kWBytes / 16); x += NPW * 32) {
                     const uint4 v = Wsm[x];
                     wmag = __vmaxu2(wmag, v.x & 0x7fff7fffu);
                     wmag = __vmaxu2(wmag, v.y & 0x7fff7fffu);
@@ -1279,7 +1286,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             wmag = max(wmag, __shfl_xor_sync(0xffffffffu, wmag, o));
         if (lane == 0)
             atomicMax(a.wmax, wmag);
-    } else if (warp == kProdWarps) {
+    } else if (warp == NPW) {
         // ---------------------------------------------------------- forward MMA
         const uint32_t idesc = idesc_bf16(128, G, 1, 0);
         int it = 0;
@@ -1323,7 +1330,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
             mma_commit(bar_addr(c.drain[0]));
         __syncwarp();
         mbar_wait_drain(bar_addr(c.drain[0]), 0);
-    } else if (warp < kFWFirstEpi) {
+    } else if (warp < FIRST_EPI) {
         // ---------------------------------------------------------- dW MMA
         const uint32_t zlayout = layout_for_swizzle(ZSW);
         const uint32_t idesc = idesc_bf16(128, 2 * G, 0, 1);  // N = [hi | lo] along j
@@ -1395,7 +1402,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
-        const int ew = warp - kFWFirstEpi;  // BCE warps 0 .. kFWBce-1, then the dW warps
+        const int ew = warp - FIRST_EPI;  // BCE warps 0 .. kFWBce-1, then the dW warps
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         if (ew < kFWBce) {
             double lacc = 0.0;  // folded in from lf every 32 groups (fp64 is slow on this part)
@@ -1503,7 +1510,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
                     lf = 0.f;
                 }
             }
-            epi_sum_to(lacc + (double)lf, c, a.loss_part + blockIdx.x, kFWFirstEpi);
+            epi_sum_to(lacc + (double)lf, c, a.loss_part + blockIdx.x, FIRST_EPI);
         } else {
             // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
             // staged in shared memory as [j][f] and stored with one bulk copy.
@@ -1587,7 +1594,7 @@ __global__ void __launch_bounds__(kFWThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kProdWarps) {
+    if (warp == NPW) {
         tc_fence_after();
         tmem_dealloc(tbase, a.tmem_cols);
     }
@@ -2225,7 +2232,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     if (rc != SG_OK)
         return rc;
     SG_TRY_CUDA(cudaMemsetAsync(lo->wmax, 0, sizeof(uint32_t), st));
-    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, kFWThreads, smem, st>>>(tm_w, a));
+    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, fw_threads(p.MT), smem, st>>>(tm_w, a));
     SG_TRY_CUDA(cudaGetLastError());
     return sg_loss_finalize(lo, grid, loss, st);
 }
