@@ -1646,10 +1646,8 @@ struct CtlDh {
 // workspace) and the builders write W_k as fp16, scaled by 2^-s so that the
 // step's largest |W| stays finite (s = 0 unless |W| >= 2^15); the flush
 // scales the sums back by 2^s.
-// Column f of a staged W_k ([G][F] row-major, bf16) as one Ws row: G values
-// packed in 16-byte units, as bf16, or as fp16 (times `down` when SCALED;
-// unscaled when the step's largest |W| is below 2^15, which spares a multiply
-// per value)
+// Column f of a staged W_k ([G][F] row-major, bf16) as NCW 16-byte units (8
+// labels each) of its Ws row, kept as bf16 or converted to fp16 as below
 template <int NCW, bool F16, bool SCALED>
 __device__ __forceinline__ void read_w_column(const uint16_t *Wk, int F, float down, uint4 (&row)[NCW])
 {
@@ -1666,6 +1664,37 @@ __device__ __forceinline__ void read_w_column(const uint16_t *Wk, int F, float d
                 w[c2] = lo | (hi << 16);
         }
         row[u] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Columns f and f + 1 of a staged W_k ([G][F] row-major, bf16) as the same
+// NCWH 16-byte units (8 labels each) of their two Ws rows, from one 4-byte
+// load per label: `Wp` points at the word (first label, f), F2 = F / 2 words
+// per W_k row.  The values are kept as bf16, or converted to fp16 (times
+// `down` when SCALED; unscaled when the step's largest |W| is below 2^15,
+// which spares a multiply per value).
+template <int NCWH, bool F16, bool SCALED>
+__device__ __forceinline__ void read_w_pair(const uint32_t *Wp, int F2, float down, uint4 (&ra)[NCWH],
+                                            uint4 (&rb)[NCWH])
+{
+#pragma unroll
+    for (int u = 0; u < NCWH; ++u) {
+        uint32_t wa[4], wb[4];
+#pragma unroll
+        for (int c2 = 0; c2 < 4; ++c2) {
+            const uint32_t w0 = Wp[(8 * u + 2 * c2) * F2], w1 = Wp[(8 * u + 2 * c2 + 1) * F2];
+            if (F16) {
+                const float a0 = __uint_as_float(w0 << 16), a1 = __uint_as_float(w1 << 16);
+                const float b0 = __uint_as_float(w0 & 0xffff0000u), b1 = __uint_as_float(w1 & 0xffff0000u);
+                wa[c2] = SCALED ? pack2_f16(a0 * down, a1 * down) : pack2_f16(a0, a1);
+                wb[c2] = SCALED ? pack2_f16(b0 * down, b1 * down) : pack2_f16(b0, b1);
+            } else {
+                wa[c2] = __byte_perm(w0, w1, 0x5410);  // the low halves: column f
+                wb[c2] = __byte_perm(w0, w1, 0x7632);  // the high halves: column f + 1
+            }
+        }
+        ra[u] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        rb[u] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
     }
 }
 
@@ -1826,17 +1855,26 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         // ---------------------------------------------------------- builders
         // NB = 2 teams of kDhBuilders / 2 warps take turns at the units (team
         // t: units t, t + 2, ..., always Ws buffer t), so the teams build
-        // concurrently while the MMAs consume.  Team thread tt handles the
-        // slots e = tt, tt + NT, ... of the unit's P x HS x F (group
-        // g = e / (HS F), then the half h of the row, then feature f; F <= 256).
-        // A row of 64 labels is two slots of 32: one slot per (g, f) left half
-        // the team idle at F = 128 and gave the other half twice the chain of
-        // dependent loads (G = 64, B = 256, F = 128: 1-2 % slower).
+        // concurrently while the MMAs consume.  A slot is FP consecutive
+        // features of one group and one span of NCWH 16-byte units (8 labels
+        // each) of their Ws rows; a unit has P x HS x F/FP slots (HS spans per
+        // row), and team thread tt handles slots e = tt, tt + NT, ... (group
+        // g = e / (HS F/FP), then the span h, then the feature block fq).
+        //   G = 16: FP = 2, one 4-byte load per label gives both features, so
+        //     a warp's load moves 128 contiguous bytes instead of 64 (dh at
+        //     G = 16: 5 % faster; at G = 32 pairs measured 2 % slower);
+        //   G = 32: one feature, whole rows of 32 labels;
+        //   G = 64: one feature, half rows: one slot per (g, f) left half the
+        //     team idle at F = 128 and gave the other half twice the chain of
+        //     dependent loads (1-2 % slower).
         const int NT = kDhBuilders * 32 / NB;  // threads of a team
         constexpr int NT_MIN = kDhBuilders * 32 / 2;
-        constexpr int HS = G == 64 ? 2 : 1;  // slots per Ws row
-        constexpr int NCWH = NCW / HS;       // 16-byte units of a slot
-        constexpr int NSLOT = (P * HS * 256 + NT_MIN - 1) / NT_MIN;
+        constexpr int FP = G == 16 ? 2 : 1;                    // features per slot
+        constexpr int NCWH = FP == 2 ? 2 : G == 64 ? 4 : NCW;  // 16-byte units of a span
+        constexpr int HS = NCW / NCWH;                         // spans per Ws row
+        constexpr int NSLOT = (P * HS * (256 / FP) + NT_MIN - 1) / NT_MIN;
+        static_assert(NCW % NCWH == 0, "rows of whole spans");
+        const int FW = F / FP;  // feature blocks per row of W_k
         const int tb = threadIdx.x - kDhFirstEpi * 32;  // 0 .. kDhBuilders * 32 - 1
         const int team = tb / NT, tt = tb - team * NT;
         const int q = warp & 3, sub = (warp - kDhFirstEpi) / 4;
@@ -1849,23 +1887,26 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             up = __uint_as_float((uint32_t)(127 + sh) << 23);
         }
         const bool scaled = down != 1.f;  // the same for every thread of the grid
-        // the team's buffer starts zeroed; prev[x]: the row slot x wrote in it
+        // the team's buffer starts zeroed; prev[x][c]: the row that feature
+        // FP fq + c of slot x wrote in it
         uint8_t *Wb = base_ptr + (size_t)team * a.ws_bytes;
         for (uint32_t o = (uint32_t)tt * 16; o < a.ws_bytes; o += NT * 16)
             *reinterpret_cast<uint4 *>(Wb + o) = make_uint4(0u, 0u, 0u, 0u);
-        int prev[NSLOT];
+        int prev[NSLOT][FP];
 #pragma unroll
         for (int x = 0; x < NSLOT; ++x)
-            prev[x] = -1;
-        // (group, row half, feature) of each slot: fixed per thread
-        int gsl[NSLOT], fsl[NSLOT], hsl[NSLOT];
+#pragma unroll
+            for (int c = 0; c < FP; ++c)
+                prev[x][c] = -1;
+        // (group, span, feature block) of each slot: fixed per thread
+        int gsl[NSLOT], psl[NSLOT], hsl[NSLOT];
 #pragma unroll
         for (int x = 0; x < NSLOT; ++x) {
             const int e = tt + x * NT;
-            gsl[x] = e / (HS * F);
-            const int r = e - gsl[x] * HS * F;
-            hsl[x] = HS > 1 ? r / F : 0;
-            fsl[x] = r - hsl[x] * F;
+            gsl[x] = e / (HS * FW);
+            const int r = e - gsl[x] * HS * FW;
+            hsl[x] = HS > 1 ? r / FW : 0;
+            psl[x] = r - hsl[x] * FW;
         }
         int it = team;
         uint32_t wph = 0;
@@ -1879,24 +1920,47 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             DH_TRACE(1, it);
             const uint8_t *st = stage0_ptr + (size_t)s * a.stage_bytes;
             // this thread's rows, read from the stage before waiting for the buffer
-            uint4 row[NSLOT][NCWH];
-            int dst[NSLOT];
+            uint4 row[NSLOT][FP][NCWH];
+            int dst[NSLOT][FP];
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
-                dst[x] = -1;
-                const int g = gsl[x], f = fsl[x];
-                if (ok && g < np && x * NT < P * HS * F) {
-                    const int i = (int)reinterpret_cast<const uint16_t *>(st + ioff + (size_t)g * a.i_bytes)[f] - i0;
-                    if (i >= 0 && i < BW) {
-                        dst[x] = g * BW + i;
-                        // column f of W_k ([G][F] row-major): consecutive
-                        // threads read consecutive f
-                        const uint16_t *Wk = reinterpret_cast<const uint16_t *>(st + woff + (size_t)g * a.w_bytes) + f +
-                                             (size_t)hsl[x] * NCWH * 8 * F;
-                        if (F16 && scaled)
-                            read_w_column<NCWH, true, true>(Wk, F, down, row[x]);
-                        else
-                            read_w_column<NCWH, F16, false>(Wk, F, down, row[x]);
+                bool any = false;
+                const int g = gsl[x], fq = psl[x];
+#pragma unroll
+                for (int c = 0; c < FP; ++c)
+                    dst[x][c] = -1;
+                if (ok && g < np && x * NT < P * HS * FW) {
+                    const uint8_t *Ig = st + ioff + (size_t)g * a.i_bytes;
+                    // I_k of the slot's features: one 4-byte load for a pair
+                    // (F even, rows 4-byte aligned)
+                    const uint32_t ii = FP == 2 ? reinterpret_cast<const uint32_t *>(Ig)[fq]
+                                                : (uint32_t)reinterpret_cast<const uint16_t *>(Ig)[fq];
+#pragma unroll
+                    for (int c = 0; c < FP; ++c) {
+                        const int i = (int)((ii >> (16 * c)) & 0xffffu) - i0;
+                        if (i >= 0 && i < BW) {
+                            dst[x][c] = g * BW + i;
+                            any = true;
+                        }
+                    }
+                    if (any) {
+                        // consecutive threads read consecutive features of a W_k row
+                        const uint8_t *Wg = st + woff + (size_t)g * a.w_bytes;
+                        if constexpr (FP == 2) {
+                            const uint32_t *Wp = reinterpret_cast<const uint32_t *>(Wg) + fq +
+                                                 (size_t)hsl[x] * NCWH * 8 * FW;
+                            if (F16 && scaled)
+                                read_w_pair<NCWH, true, true>(Wp, FW, down, row[x][0], row[x][FP - 1]);
+                            else
+                                read_w_pair<NCWH, F16, false>(Wp, FW, down, row[x][0], row[x][FP - 1]);
+                        } else {
+                            const uint16_t *Wk = reinterpret_cast<const uint16_t *>(Wg) + fq +
+                                                 (size_t)hsl[x] * NCWH * 8 * F;
+                            if (F16 && scaled)
+                                read_w_column<NCWH, true, true>(Wk, F, down, row[x][0]);
+                            else
+                                read_w_column<NCWH, F16, false>(Wk, F, down, row[x][0]);
+                        }
                     }
                 }
             }
@@ -1915,26 +1979,33 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             // rows, one wavefront each)
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
-                if (prev[x] >= 0) {
-                    uint8_t *d = Wb + (size_t)prev[x] * RB;
-                    const int sw = swz_of(prev[x], RB);
 #pragma unroll
-                    for (int u = 0; u < NCWH; ++u)
-                        *reinterpret_cast<uint4 *>(d + (((hsl[x] * NCWH + u) ^ sw) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                for (int c2 = 0; c2 < FP; ++c2) {
+                    if (prev[x][c2] >= 0) {
+                        uint8_t *d = Wb + (size_t)prev[x][c2] * RB;
+                        const int sw = swz_of(prev[x][c2], RB);
+#pragma unroll
+                        for (int u = 0; u < NCWH; ++u)
+                            *reinterpret_cast<uint4 *>(d + (((hsl[x] * NCWH + u) ^ sw) << 4)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
             }
             named_bar(1 + team, NT);
             DH_TRACE(5, it);
 #pragma unroll
             for (int x = 0; x < NSLOT; ++x) {
-                if (dst[x] >= 0) {
-                    uint8_t *d = Wb + (size_t)dst[x] * RB;
-                    const int sw = swz_of(dst[x], RB);
 #pragma unroll
-                    for (int u = 0; u < NCWH; ++u)
-                        *reinterpret_cast<uint4 *>(d + (((hsl[x] * NCWH + u) ^ sw) << 4)) = row[x][u];
+                for (int c2 = 0; c2 < FP; ++c2) {
+                    if (dst[x][c2] >= 0) {
+                        uint8_t *d = Wb + (size_t)dst[x][c2] * RB;
+                        const int sw = swz_of(dst[x][c2], RB);
+#pragma unroll
+                        for (int u = 0; u < NCWH; ++u)
+                            *reinterpret_cast<uint4 *>(d + (((hsl[x] * NCWH + u) ^ sw) << 4)) = row[x][c2][u];
+                    }
+                    prev[x][c2] = dst[x][c2];
                 }
-                prev[x] = dst[x];
             }
             fence_proxy_async();  // Ws rows (generic writes) -> the MMA (async proxy)
             __syncwarp();
