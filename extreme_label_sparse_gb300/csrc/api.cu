@@ -485,8 +485,7 @@ sg_status sg_fwd_bce(sg_layout *lo, const sg_bf16 *h, int32_t B,
     cudaStream_t st = (cudaStream_t)stream;
     bool tc = false;
     TRY(pick_tc(lo, SG_KIND_FWD, B, &tc, fn));
-    TRY(simt_transpose_h(lo, h, B, st));
-    TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+    TRY(sg_step_prepare(lo, h, B, pos_rowptr, pos_label, nnz, st));
     if (tc)
         return tc_fwd(lo, B, W, Z_or_null, dZ, nullptr, nullptr, loss, st);
     return simt_fwd(lo, B, W, Z_or_null, dZ, nullptr, loss, st);
@@ -592,14 +591,12 @@ sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W
     StepPath path;
     TRY(step_path(lo, B, sgd != nullptr, &path, fn));
     if (path.single) {
-        TRY(simt_transpose_h(lo, h, B, st));
-        TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+        TRY(sg_step_prepare(lo, h, B, pos_rowptr, pos_label, nnz, st));
         return tc_step(lo, B, W, dW, dh, loss, st);
     }
     const bool fused = path.fused != 0;
     const bool tc_f = path.tc_f, tc_w = path.tc_w, tc_h = path.tc_h;
-    TRY(simt_transpose_h(lo, h, B, st));
-    TRY(sg_pos_prepare(lo, B, pos_rowptr, pos_label, nnz, st));
+    TRY(sg_step_prepare(lo, h, B, pos_rowptr, pos_label, nnz, st));
     // forward + BCE into dZ scratch, then dW and dh from it.  Outside the
     // fused kernel dZ is kept as two bf16 planes (hi + lo): a single bf16
     // rounding of dZ, summed over B samples (dW) or over every label (dh),

@@ -14,17 +14,13 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__global__ void k_pos_rows(int32_t B, const int32_t *__restrict__ rowptr,
-                           const int32_t *__restrict__ labels, int64_t nnz,
-                           int64_t L, int32_t G,
-                           const int32_t *__restrict__ slot_of_label,
-                           int32_t *tsorted, int32_t *tslots, int32_t *rowcnt,
-                           int32_t *gcount, int32_t *status)
+// sample row b, by one warp
+__device__ __forceinline__ void pos_row(int b, int32_t B, const int32_t *__restrict__ rowptr,
+                                        const int32_t *__restrict__ labels, int64_t nnz, int64_t L, int32_t G,
+                                        const int32_t *__restrict__ slot_of_label, int32_t *tsorted,
+                                        int32_t *tslots, int32_t *rowcnt, int32_t *gcount, int32_t *status)
 {
     const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-    if (b >= B)
-        return;
     if (b == 0 && lane == 0 && (rowptr[0] != 0 || (int64_t)rowptr[B] != nnz))
         sg_flag(status, SG_ERR_DATA);
     const int64_t r0 = rowptr[b], r1 = rowptr[b + 1];
@@ -73,6 +69,43 @@ __global__ void k_pos_rows(int32_t B, const int32_t *__restrict__ rowptr,
     }
     if (lane == 0)
         rowcnt[b] = kept;
+}
+
+__global__ void k_pos_rows(int32_t B, const int32_t *__restrict__ rowptr,
+                           const int32_t *__restrict__ labels, int64_t nnz,
+                           int64_t L, int32_t G,
+                           const int32_t *__restrict__ slot_of_label,
+                           int32_t *tsorted, int32_t *tslots, int32_t *rowcnt,
+                           int32_t *gcount, int32_t *status)
+{
+    const int b = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    if (b < B)
+        pos_row(b, B, rowptr, labels, nnz, L, G, slot_of_label, tsorted, tslots, rowcnt, gcount, status);
+}
+
+// The step's first launch: blocks [0, rows_blocks) take the positive rows
+// (a warp per sample), the others one 32 x 32 tile of h^T each (tiles_x tiles
+// along H), so the two independent parts run side by side.
+__global__ void __launch_bounds__(kThreads) k_prep_step(int rows_blocks, int tiles_x, int32_t B,
+                                                        const int32_t *__restrict__ rowptr,
+                                                        const int32_t *__restrict__ labels, int64_t nnz,
+                                                        int64_t L, int32_t G,
+                                                        const int32_t *__restrict__ slot_of_label,
+                                                        int32_t *tsorted, int32_t *tslots, int32_t *rowcnt,
+                                                        int32_t *gcount, int32_t *status,
+                                                        const uint16_t *__restrict__ h, int32_t H, int32_t ldB,
+                                                        uint16_t *__restrict__ hT)
+{
+    __shared__ uint16_t tile[32][34];
+    if ((int)blockIdx.x >= rows_blocks) {
+        const int t = (int)blockIdx.x - rows_blocks;
+        transpose_h_tile(h, B, H, ldB, hT, (t % tiles_x) * 32, (t / tiles_x) * 32, threadIdx.x & 31,
+                         threadIdx.x >> 5, tile);
+        return;
+    }
+    const int b = blockIdx.x * (kThreads / 32) + threadIdx.x / 32;
+    if (b < B)
+        pos_row(b, B, rowptr, labels, nnz, L, G, slot_of_label, tsorted, tslots, rowcnt, gcount, status);
 }
 
 // Exclusive scan out[i] = sum_{j<i} in[j], out[n] = total, in two passes over
@@ -213,6 +246,27 @@ sg_status sg_pos_prepare(sg_layout *lo, int32_t B, const int32_t *rowptr,
                                                lo->tsorted, lo->tslots,
                                                lo->rowcnt, lo->gcount,
                                                lo->status));
+    const int tiles = (int)((lo->K + kScanTile - 1) / kScanTile);
+    SG_LAUNCH(lo, SG_KIND_PREP, st,
+              k_scan_tiles<<<tiles, 1024, 0, st>>>(lo->gcount, lo->K, lo->gptr, lo->scan_part));
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_scan_add<<<tiles, 1024, 0, st>>>(lo->K, lo->gptr, lo->scan_part));
+    SG_LAUNCH(lo, SG_KIND_PREP, st, k_pos_place<<<rows_grid, kThreads, 0, st>>>(B, rowptr, lo->tslots,
+                                                lo->rowcnt, lo->G, lo->gptr,
+                                                lo->gcount, lo->gent));
+    SG_TRY_CUDA(cudaGetLastError());
+    return SG_OK;
+}
+
+sg_status sg_step_prepare(sg_layout *lo, const uint16_t *h, int32_t B, const int32_t *rowptr,
+                          const int32_t *labels, int64_t nnz, cudaStream_t st)
+{
+    const int wpb = kThreads / 32;
+    const int rows_grid = (int)ceil_div(B, wpb);
+    const int tiles_x = (int)ceil_div(lo->H, 32), tiles_y = (int)ceil_div(lo->ldB, 32);
+    SG_LAUNCH(lo, SG_KIND_PREP, st,
+              k_prep_step<<<rows_grid + tiles_x * tiles_y, kThreads, 0, st>>>(
+                  rows_grid, tiles_x, B, rowptr, labels, nnz, lo->L, lo->G, lo->slot_of_label, lo->tsorted,
+                  lo->tslots, lo->rowcnt, lo->gcount, lo->status, h, lo->H, lo->ldB, lo->hT));
     const int tiles = (int)((lo->K + kScanTile - 1) / kScanTile);
     SG_LAUNCH(lo, SG_KIND_PREP, st,
               k_scan_tiles<<<tiles, 1024, 0, st>>>(lo->gcount, lo->K, lo->gptr, lo->scan_part));

@@ -181,6 +181,31 @@ sg_status g1_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, int32_
 sg_status sg_loss_finalize(sg_layout *lo, int32_t nparts, double *loss,
                            cudaStream_t st);
 // simt.cu
+// One 32 x 32 tile of h^T: rows i0 .. i0 + 31 (features), columns b0 ..
+// b0 + 31 (samples; zero past B, up to ldB), by 256 threads (tx = thread
+// mod 32, ty = thread / 32) through a padded shared tile.  Every thread of the
+// block calls it.
+__device__ __forceinline__ void transpose_h_tile(const uint16_t *__restrict__ h, int B, int H, int ldB,
+                                                 uint16_t *__restrict__ hT, int i0, int b0, int tx, int ty,
+                                                 uint16_t (*tile)[34])
+{
+    for (int r = ty; r < 32; r += 8) {
+        const int b = b0 + r, i = i0 + tx;
+        tile[r][tx] = (b < B && i < H) ? h[(int64_t)b * H + i] : (uint16_t)0;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+        const int i = i0 + r, b = b0 + tx;
+        if (i < H && b < ldB)
+            hT[(int64_t)i * ldB + b] = tile[tx][r];
+    }
+}
+
+// The step's preparation in three fewer launches than the transpose plus
+// sg_pos_prepare: one kernel runs the positive rows and the transpose of h
+// side by side, then the group scan and the bucketing.
+sg_status sg_step_prepare(sg_layout *lo, const uint16_t *h, int32_t B, const int32_t *rowptr,
+                          const int32_t *labels, int64_t nnz, cudaStream_t st);
 sg_status simt_transpose_h(sg_layout *lo, const uint16_t *h, int32_t B,
                            cudaStream_t st);
 // dZ_lo (optional): second bf16 plane with dZ - bf16(dZ), so that hi + lo

@@ -20,18 +20,7 @@ __global__ void k_transpose_h(const uint16_t *__restrict__ h, int B, int H,
                               int ldB, uint16_t *__restrict__ hT)
 {
     __shared__ uint16_t tile[32][34];
-    const int i0 = blockIdx.x * 32, b0 = blockIdx.y * 32;
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    for (int r = ty; r < 32; r += 8) {
-        int b = b0 + r, i = i0 + tx;
-        tile[r][tx] = (b < B && i < H) ? h[(int64_t)b * H + i] : (uint16_t)0;
-    }
-    __syncthreads();
-    for (int r = ty; r < 32; r += 8) {
-        int i = i0 + r, b = b0 + tx;
-        if (i < H && b < ldB)
-            hT[(int64_t)i * ldB + b] = tile[tx][r];
-    }
+    transpose_h_tile(h, B, H, ldB, hT, blockIdx.x * 32, blockIdx.y * 32, threadIdx.x, threadIdx.y, tile);
 }
 
 __device__ __forceinline__ void block_sum_to(double v, double *dst)

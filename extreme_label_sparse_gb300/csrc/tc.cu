@@ -1136,6 +1136,10 @@ struct FWArgs {
     float lr, mu;
     const int32_t *gptr, *gent;
     double *loss_part;
+    // the step's loss: the CTA that takes the last ticket sums the partials
+    // in block order (no separate launch); the ticket starts at zero
+    double *loss;
+    uint32_t *ticket;
     int32_t *status;
     int64_t K, L;
     int32_t B, G, F, MT, FT, nk, S, zsw, nzc, nslot, Bp, ldB;
@@ -1511,6 +1515,27 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
                 }
             }
             epi_sum_to(lacc + (double)lf, c, a.loss_part + blockIdx.x, FIRST_EPI);
+            if (ew == 0 && a.loss) {
+                // the warp of the CTA that takes the last ticket sums the
+                // partials: lane l the partials l, l + 32, ..., then a fixed
+                // shuffle tree (one thread summing them serially at the end of
+                // the kernel cost 8-15 us)
+                uint32_t last = 0;
+                if (lane == 0) {
+                    __threadfence();  // this CTA's partial before its ticket
+                    last = atomicAdd(a.ticket, 1u) == gridDim.x - 1 ? 1u : 0u;
+                }
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    __threadfence();
+                    double sum = 0.0;
+                    for (unsigned i = lane; i < gridDim.x; i += 32)
+                        sum += __ldcg(a.loss_part + i);
+                    for (int o = 16; o > 0; o >>= 1)
+                        sum += __shfl_down_sync(0xffffffffu, sum, o);
+                    if (lane == 0)
+                        *a.loss = sum;
+                }
+            }
         } else {
             // dW_k^T accumulator [f lanes][hi j | lo j] -> dW rows k*G + j,
             // staged in shared memory as [j][f] and stored with one bulk copy.
@@ -2264,6 +2289,8 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.gptr = lo->gptr;
     a.gent = lo->gent;
     a.loss_part = lo->loss_part;
+    a.loss = loss;
+    a.ticket = lo->wmax + 1;
     a.status = lo->status;
     a.K = pair ? lo->K / 2 : lo->K * p.sub;
     a.sub_shift = log2_exact(p.sub);  // 0, 1 or 2
@@ -2302,10 +2329,11 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
-    SG_TRY_CUDA(cudaMemsetAsync(lo->wmax, 0, sizeof(uint32_t), st));
+    // max |W| and the loss ticket start at zero
+    SG_TRY_CUDA(cudaMemsetAsync(lo->wmax, 0, 2 * sizeof(uint32_t), st));
     SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, fw_threads(p.MT), smem, st>>>(tm_w, a));
     SG_TRY_CUDA(cudaGetLastError());
-    return sg_loss_finalize(lo, grid, loss, st);
+    return SG_OK;  // the kernel wrote the loss
 }
 
 sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
