@@ -609,7 +609,7 @@ sg_status step_impl(sg_layout *lo, const sg_bf16 *h, int32_t B, const sg_bf16 *W
         if (fused) {
             // the fused kernel leaves dZ as one fp16 plane and max |W| for dh
             // (and applies the optimiser step to dW in its epilogue)
-            TRY(tc_fwdw(lo, B, W, dZt, dW, sgd, loss, st));
+            TRY(tc_fwdw(lo, B, W, dZt, dW, sgd, loss, dh, st));
             return tc_dh(lo, nullptr, nullptr, dZt, true, B, W, dh, st);
         }
         TRY(tc_fwd(lo, B, W, nullptr, nullptr, nullptr, dZt, loss, st));

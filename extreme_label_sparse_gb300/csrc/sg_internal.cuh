@@ -46,8 +46,12 @@ struct sg_layout {
     // allocated on first use
     uint16_t *dZ_ws = nullptr;
     size_t dZ_ws_elems = 0;
-    // the step's max |W| as bf16 magnitude bits (scale of dh's fp16 operands)
+    // the step's max |W| as bf16 magnitude bits (scale of dh's fp16 operands),
+    // in two slots used by alternate fused launches (each launch clears the
+    // other slot for the next), then the fused kernel's loss ticket; zeroed
+    // once when allocated.  wmax_slot: the slot the last fused launch wrote.
     uint32_t *wmax = nullptr;
+    int32_t wmax_slot = 0;
 
     // scratch of sg_headtail_step when this layout is the tail (allocated on
     // first use): projected activations, both branches' dh, bf16 planes
@@ -244,8 +248,10 @@ struct sg_sgd {
     float lr, mu;
 };
 // with sgd, dW receives the updated weights instead of the gradient
+// dh_zero: the feature gradient the following tc_dh (fp16 workspace) adds
+// into, cleared by this kernel (B x H floats), or nullptr
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
-                  const sg_sgd *sgd, double *loss, cudaStream_t st);
+                  const sg_sgd *sgd, double *loss, float *dh_zero, cudaStream_t st);
 // the same update from a stored bf16 dW (in place: W_out holds dW on entry)
 sg_status sgd_update(sg_layout *lo, const uint16_t *W, uint16_t *W_out, const sg_sgd &sgd, cudaStream_t st);
 

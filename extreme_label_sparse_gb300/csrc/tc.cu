@@ -1128,7 +1128,10 @@ struct FWArgs {
     uint8_t *dZt;
     uint64_t tile_bytes;
     uint16_t *dW;     // dW, or the updated weights when `mom` is set
-    uint32_t *wmax;   // max |W| (bf16 magnitude bits) over the step, for dh
+    uint32_t *wmax;   // max |W| (bf16 magnitude bits) over the step, for dh (zero at entry)
+    uint32_t *wmax_next;  // the other slot, cleared by CTA 0 for the next launch
+    float *dh_zero;       // dh to clear (dh_n floats) for the dh kernel, or nullptr
+    int32_t dh_n;
     // momentum SGD in the dW epilogue (mom != nullptr): m <- mu m + dW,
     // W_out <- bf16(W - lr m), W_out written where dW would be
     const uint16_t *W;
@@ -1250,6 +1253,12 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
     tc_fence_after();
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
+    // the other max |W| slot for the next launch (read by no one until then),
+    // and this CTA's share of dh for the dh kernel that follows
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *a.wmax_next = 0u;
+    for (int i = blockIdx.x * NTHR + threadIdx.x; i < a.dh_n; i += gridDim.x * NTHR)
+        a.dh_zero[i] = 0.f;
 
     if (warp < NPW) {
         // ---------------------------------------------------------- producers
@@ -1532,8 +1541,10 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
                         sum += __ldcg(a.loss_part + i);
                     for (int o = 16; o > 0; o >>= 1)
                         sum += __shfl_down_sync(0xffffffffu, sum, o);
-                    if (lane == 0)
+                    if (lane == 0) {
                         *a.loss = sum;
+                        *a.ticket = 0u;  // for the next launch
+                    }
                 }
             }
         } else {
@@ -2253,7 +2264,7 @@ bool tc_fwdw_ok(const sg_layout *lo, int32_t B)
 }
 
 sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uint16_t *dW,
-                  const sg_sgd *sgd, double *loss, cudaStream_t st)
+                  const sg_sgd *sgd, double *loss, float *dh_zero, cudaStream_t st)
 {
     bool pair = false;
     const FWPlan p = fwdw_plan_of(lo, B, &pair);
@@ -2281,7 +2292,11 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     // one fp16 plane of a kernel group's tile (with pairs: of a layout group's)
     a.tile_bytes = tc_dz_tile_bytes(lo, B) / 2 / p.sub;
     a.dW = dW;
-    a.wmax = lo->wmax;
+    const int wslot = lo->wmax_slot ^ 1;  // the slot the previous launch cleared
+    a.wmax = lo->wmax + wslot;
+    a.wmax_next = lo->wmax + (wslot ^ 1);
+    a.dh_zero = dh_zero;
+    a.dh_n = dh_zero ? B * lo->H : 0;
     a.W = W;
     a.mom = sgd ? sgd->mom : nullptr;
     a.lr = sgd ? sgd->lr : 0.f;
@@ -2290,7 +2305,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     a.gent = lo->gent;
     a.loss_part = lo->loss_part;
     a.loss = loss;
-    a.ticket = lo->wmax + 1;
+    a.ticket = lo->wmax + 2;
     a.status = lo->status;
     a.K = pair ? lo->K / 2 : lo->K * p.sub;
     a.sub_shift = log2_exact(p.sub);  // 0, 1 or 2
@@ -2329,11 +2344,10 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
-    // max |W| and the loss ticket start at zero
-    SG_TRY_CUDA(cudaMemsetAsync(lo->wmax, 0, 2 * sizeof(uint32_t), st));
     SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, fw_threads(p.MT), smem, st>>>(tm_w, a));
     SG_TRY_CUDA(cudaGetLastError());
-    return SG_OK;  // the kernel wrote the loss
+    lo->wmax_slot = wslot;  // the slot the dh kernel reads
+    return SG_OK;           // the kernel wrote the loss
 }
 
 sg_status tc_dW(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const uint8_t *dZt,
@@ -2409,6 +2423,8 @@ sg_status tc_ensure_wmax(sg_layout *lo)
         sg_set_error("cudaMalloc of 16 bytes for the step's max |W| failed");
         return SG_ERR_OOM;
     }
+    SG_TRY_CUDA(cudaMemset(lo->wmax, 0, 16));
+    lo->wmax_slot = 0;
     return SG_OK;
 }
 
@@ -2449,7 +2465,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     DhArgs a;
     a.idx_s = lo->idx_s;
     a.W = W;
-    a.wmax = lo->wmax;
+    a.wmax = lo->wmax ? lo->wmax + lo->wmax_slot : nullptr;
     a.dZt = dZt;
     // one tile holds sub subgroups of gs labels (a whole group, or the fused
     // forward kernel's subgroup)
@@ -2513,7 +2529,8 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
-    SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
+    if (!dzt_f16)  // the fused kernel that wrote the fp16 workspace cleared dh
+        SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
     SG_LAUNCH(lo, SG_KIND_DH, st,
               kern<<<p.nbands * p.MT * parts, kDhThreads, smem, st>>>(tm_z, tm_zl, a));
     SG_TRY_CUDA(cudaGetLastError());
