@@ -1183,6 +1183,30 @@ struct CtlFW {
 // warps see the group once.  A group of 64 labels then needs the shared
 // memory of one tile instead of two, and runs as one group with N = 64 MMAs
 // instead of two subgroups of 32 with twice as many.
+// The loss ticket of the fused kernel, out of line (its SGD instance): the
+// warp of the CTA that takes the last ticket sums the partials, lane l the
+// partials l, l + 32, ..., then a fixed shuffle tree, and resets the ticket.
+static __device__ __noinline__ void fw_loss_ticket(const double *part, double *loss, uint32_t *ticket, int lane)
+{
+    uint32_t last = 0;
+    if (lane == 0) {
+        __threadfence();  // this CTA's partial before its ticket
+        last = atomicAdd(ticket, 1u) == gridDim.x - 1 ? 1u : 0u;
+    }
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+        __threadfence();
+        double sum = 0.0;
+        for (unsigned i = lane; i < gridDim.x; i += 32)
+            sum += __ldcg(part + i);
+        for (int o = 16; o > 0; o >>= 1)
+            sum += __shfl_down_sync(0xffffffffu, sum, o);
+        if (lane == 0) {
+            *loss = sum;
+            *ticket = 0u;  // for the next launch
+        }
+    }
+}
+
 template <int G_, int FK, int MT, bool SGD, bool PAIR = false, int TI = 1>
 __global__ void __launch_bounds__(fw_threads(MT), 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
@@ -1254,11 +1278,19 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
     const uint32_t tbase = c.tmem;
     volatile int *abort_flag = &c.abort_flag;
     // the other max |W| slot for the next launch (read by no one until then),
-    // and this CTA's share of dh for the dh kernel that follows
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-        *a.wmax_next = 0u;
-    for (int i = blockIdx.x * NTHR + threadIdx.x; i < a.dh_n; i += gridDim.x * NTHR)
-        a.dh_zero[i] = 0.f;
+    // and this CTA's share of dh for the dh kernel that follows: by every
+    // thread here, or (SGD) by the dW warps before their first group.  Where
+    // these few instructions and the loss ticket below sit in the code moved
+    // the SGD instance's time by up to 5 % either way (1.422 ms with this
+    // arrangement, 1.501 ms with the plain instance's), and the plain one's
+    // by 1 % the other way, so each keeps the arrangement it measured
+    // fastest with.
+    if (!SGD) {
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            *a.wmax_next = 0u;
+        for (int i = blockIdx.x * NTHR + threadIdx.x; i < a.dh_n; i += gridDim.x * NTHR)
+            a.dh_zero[i] = 0.f;
+    }
 
     if (warp < NPW) {
         // ---------------------------------------------------------- producers
@@ -1524,7 +1556,10 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
                 }
             }
             epi_sum_to(lacc + (double)lf, c, a.loss_part + blockIdx.x, FIRST_EPI);
-            if (ew == 0 && a.loss) {
+            if (SGD) {
+                if (ew == 0 && a.loss)
+                    fw_loss_ticket(a.loss_part, a.loss, a.ticket, lane);
+            } else if (ew == 0 && a.loss) {
                 // the warp of the CTA that takes the last ticket sums the
                 // partials: lane l the partials l, l + 32, ..., then a fixed
                 // shuffle tree (one thread summing them serially at the end of
@@ -1553,6 +1588,12 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
             // The team leaves together: every named barrier below is then
             // reached by all of its warps or by none.
             const int dw = ew - kFWBce;  // 0 .. kFWDw-1
+            if (SGD) {
+                if (blockIdx.x == 0 && dw == 0 && lane == 0)
+                    *a.wmax_next = 0u;
+                for (int i = blockIdx.x * (kFWDw * 32) + dw * 32 + lane; i < a.dh_n; i += gridDim.x * (kFWDw * 32))
+                    a.dh_zero[i] = 0.f;
+            }
             constexpr int wunits = ((FK + 7) / 8) * (G / CH);
             int it = 0;
             Ring rw;
