@@ -1097,21 +1097,20 @@ FWPlan plan_fwdw_g(const sg_layout *lo, int B, int Gv, bool stream = false)
     return p;
 }
 
-// With B > 128, groups of 32 or more labels stream their two sample tiles as
-// separate items (at B = 256, F = 128: 5 % faster than both tiles in one
-// stage at G = 32, and the only way G = 64 fits); groups of 16 keep both
-// tiles in one stage (streaming measured 3.5 % slower) unless they do not
-// fit.  Groups that fit neither way run as subgroups of half the labels
-// sharing the group's I_k: the kernel then sees K * sub groups of G / sub
-// labels, each with its own workspace tile.
+// With B > 128 a group's two sample tiles stream through the stages as
+// separate items (at B = 256, F = 128 the forward kernel measured 4-5 %
+// faster than with both tiles in one stage at G = 16 and 32, and it is the
+// only way G = 64 fits); both tiles in one stage remain the fallback.
+// Groups that fit neither way run as subgroups of half the labels sharing
+// the group's I_k: the kernel then sees K * sub groups of G / sub labels,
+// each with its own workspace tile.
 FWPlan plan_fwdw(const sg_layout *lo, int B)
 {
     // subgroups of G, G / 2 or G / 4 labels
     for (int gs = lo->G; gs >= 16 && lo->G % gs == 0 && 4 * gs >= lo->G; gs /= 2) {
-        const bool stream_first = gs >= 32;
-        FWPlan p = plan_fwdw_g(lo, B, gs, stream_first);
+        FWPlan p = plan_fwdw_g(lo, B, gs, true);
         if (!p.ok)
-            p = plan_fwdw_g(lo, B, gs, !stream_first);
+            p = plan_fwdw_g(lo, B, gs);
         if (p.ok) {
             p.gs = gs;
             p.sub = lo->G / gs;
@@ -2263,8 +2262,8 @@ FWPlan plan_fwdw_pair(const sg_layout *lo, int B)
 using FwdwKernel = void (*)(CUtensorMap, FWArgs);
 
 // The instance for a plan (nullptr: none).  Only the instances some plan
-// reaches are built: with B > 128 subgroups of 32 and 64 labels always
-// stream their sample tiles, and G = 64, F = 256 runs as subgroups of 32.
+// reaches are built: with B > 128 every group streams its sample tiles, and
+// G = 64, F = 256 runs as subgroups of 32.
 FwdwKernel fwdw_kernel(const FWPlan &p, int F, bool pair, bool sgd)
 {
     FwdwKernel kern = nullptr;
@@ -2277,10 +2276,10 @@ FwdwKernel fwdw_kernel(const FWPlan &p, int F, bool pair, bool sgd)
 #define SG_FW_PAIR(GG, KK)                                               \
     if (pair && p.gs == GG && F == KK * 16)                             \
         kern = sgd ? k_tc_fwdw<GG, KK, 1, true, true> : k_tc_fwdw<GG, KK, 1, false, true>;
-    SG_FW_PICK(16, 4, 1) SG_FW_PICK(16, 4, 2) SG_FW_PICK(16, 8, 1) SG_FW_PICK(16, 8, 2) SG_FW_PICK(16, 16, 1)
+    SG_FW_PICK(16, 4, 1) SG_FW_PICK(16, 8, 1) SG_FW_PICK(16, 16, 1)
     SG_FW_PICK(32, 4, 1) SG_FW_PICK(32, 8, 1) SG_FW_PICK(32, 16, 1)
     SG_FW_PICK(64, 4, 1) SG_FW_PICK(64, 8, 1)
-    SG_FW_STREAM(16, 16) SG_FW_STREAM(32, 4) SG_FW_STREAM(32, 8) SG_FW_STREAM(32, 16) SG_FW_STREAM(64, 4)
+    SG_FW_STREAM(16, 4) SG_FW_STREAM(16, 8) SG_FW_STREAM(16, 16) SG_FW_STREAM(32, 4) SG_FW_STREAM(32, 8) SG_FW_STREAM(32, 16) SG_FW_STREAM(64, 4)
     SG_FW_STREAM(64, 8)
     SG_FW_PAIR(32, 4) SG_FW_PAIR(32, 8) SG_FW_PAIR(32, 16) SG_FW_PAIR(64, 4) SG_FW_PAIR(64, 8) SG_FW_PAIR(64, 16)
 #undef SG_FW_PICK

@@ -52,8 +52,8 @@
  *   256), at F = 256 for every G up to 128 and at G = 256 with F = 64 or
  *   128.  dh runs on them for every such G and F.  A phase outside that runs
  *   on CUDA cores (SG_ENGINE_TC makes it an error instead).  With B > 128 the
- *   fused kernel takes a group's two sample tiles one after the other where
- *   both do not fit it together; groups that still do not fit run there as
+ *   fused kernel takes a group's two sample tiles one after the other;
+ *   groups that still do not fit run there as
  *   subgroups of G/2 or G/4 labels sharing I_k, and groups of more than 64
  *   labels enter dh as subgroups of at most 64.  Every other G
  *   (including G = 1, per-label fixed fan-in) runs on the CUDA-core engine.
