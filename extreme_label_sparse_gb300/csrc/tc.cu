@@ -98,7 +98,9 @@ constexpr int kDhMaxBuf = 3;  // scattered-W buffers in shared memory (one per b
 // 14 % faster than two at B = 256; two at G = 32), else one group (one group
 // per unit measured 4-40 % slower than two at G <= 32)
 __host__ __device__ constexpr int dh_units(int G) { return G <= 16 ? 4 : G <= 32 ? 2 : 1; }
-constexpr int kDhThreads = 32 * (2 + kDhBuilders);
+// threads of the dh kernel with `iss` MMA-issuing warps: one load warp, the
+// issuers, the builders
+__host__ __device__ constexpr int dh_threads(int iss) { return 32 * (1 + iss + kDhBuilders); }
 
 // ------------------------------------------------------------------ plans
 struct FwdPlan {
@@ -1693,7 +1695,6 @@ struct DhArgs {
     uint32_t z_bytes, w_bytes, i_bytes, stage_bytes, ws_bytes, tmem_cols;
 };
 
-constexpr int kDhFirstEpi = 2;  // warp 0: loads, warp 1: MMA, then the builders
 
 struct CtlDh {
     Ctl c;                                           // stages, drain
@@ -1774,12 +1775,14 @@ __device__ __forceinline__ void read_w_pair(const uint32_t *Wp, int F2, float do
     }
 }
 
-template <int NPASS, int NKS, int BWT, bool F16>
-__global__ void __launch_bounds__(kDhThreads, 1)
+template <int NPASS, int NKS, int BWT, bool F16, int ISS = 1>
+__global__ void __launch_bounds__(dh_threads(ISS), 1)
     k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
             const DhArgs a)
 {
     static_assert(!F16 || NPASS == 1, "the fp16 dZ workspace has one plane");
+    static_assert(ISS == 1 || ISS == 2, "one or two MMA-issuing warps");
+    constexpr int FIRST_B = 1 + ISS;  // warp 0: loads, warps 1 .. ISS: MMA, then the builders
     constexpr int G = NKS * 16;
     constexpr int RB = 2 * G;         // bytes of one Ws row (one dh column)
     constexpr int BW = BWT * 128;     // dh columns of the band
@@ -1809,10 +1812,10 @@ __global__ void __launch_bounds__(kDhThreads, 1)
     // stages: full = loads landed; empty = the MMAs (and builders) are done
     // with them.  wfull/wempty: Ws buffer written / consumed.
     if (threadIdx.x == 0) {
-        setup_ctl(c, S, 0, 1, 1);
+        setup_ctl(c, S, 0, 1, ISS);  // every issuer releases stages and buffers
         for (int i = 0; i < NB && i < kDhMaxBuf; ++i) {
             mbar_init(bar_addr(cd.wfull[i]), kDhBuilders / NB);  // one arrival per warp of its team
-            mbar_init(bar_addr(cd.wempty[i]), 1);
+            mbar_init(bar_addr(cd.wempty[i]), ISS);
         }
         fence_mbar_init();
     }
@@ -1869,18 +1872,28 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             __syncwarp();
         }
         drain_loads(c, it, S);
-    } else if (warp == 1) {
+    } else if (warp <= ISS) {
         // ---------------------------------------------------------- MMA issue
-        // descriptors: everything but the start address is fixed, and within a
-        // unit the start addresses differ by compile-time offsets
+        // One warp issues an N = 256 and an N = 128 MMA per K step (a band of
+        // 384 columns), or, with ISS = 2, two warps each one MMA over half of
+        // the band's columns into their half of the accumulator: one thread
+        // issues a tcgen05.mma about every 100 cycles (N <= 128) to 128 (N =
+        // 256), which sets the pace where the builders have little to do.
+        // Descriptors: everything but the start address is fixed, and within
+        // a unit the start addresses differ by compile-time offsets.
         constexpr int ZSW = 2 * G >= 128 ? 128 : 2 * G;  // dZ row bytes (= a.zsw)
         constexpr uint32_t ZCH = 128u * ZSW;             // one plane of one group
         constexpr uint32_t ZB = NPASS * ZCH;             // one group's dZ (= a.z_bytes)
+        constexpr int NH = BW / ISS;                     // columns of this warp's accumulator
+        constexpr int NA = ISS == 1 ? N0 : NH, NB1 = ISS == 1 ? N1 : 0;
+        const int mh = warp - 1;
+        const uint32_t dcol = tbase + (uint32_t)(mh * NH);
+        const uint32_t boff = (uint32_t)(mh * NH * RB);
         const uint64_t adesc0 = sdesc(0, 16, 8 * ZSW, layout_for_swizzle(ZSW));
         const uint64_t bdesc0 = sdesc(0, 16, 8 * RB, layout_for_swizzle(RB));
-        constexpr uint32_t id0 = F16 ? idesc_f16(128, N0, 0, 0) : idesc_bf16(128, N0, 0, 0);
-        constexpr uint32_t id1 = N1 == 0 ? 0u : F16 ? idesc_f16(128, N1 > 0 ? N1 : 16, 0, 0)
-                                                     : idesc_bf16(128, N1 > 0 ? N1 : 16, 0, 0);
+        constexpr uint32_t id0 = F16 ? idesc_f16(128, NA, 0, 0) : idesc_bf16(128, NA, 0, 0);
+        constexpr uint32_t id1 = NB1 == 0 ? 0u : F16 ? idesc_f16(128, NB1 > 0 ? NB1 : 16, 0, 0)
+                                                      : idesc_bf16(128, NB1 > 0 ? NB1 : 16, 0, 0);
         int it = 0, buf = 0;
         uint32_t wph = 0;
         Ring rs;
@@ -1898,7 +1911,7 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             if (lane == 0) {
                 // A: dZ (rows = samples), B: Ws rows (dh columns); 16 j per K step
                 const uint64_t au = adesc0 + (uint64_t)((stage0 + (uint32_t)s * a.stage_bytes + zoff) >> 4);
-                const uint64_t bu = bdesc0 + (uint64_t)((base + (uint32_t)buf * a.ws_bytes) >> 4);
+                const uint64_t bu = bdesc0 + (uint64_t)((base + (uint32_t)buf * a.ws_bytes + boff) >> 4);
 #pragma unroll
                 for (int g = 0; g < P; ++g) {
                     if (g < np) {
@@ -1908,9 +1921,9 @@ __global__ void __launch_bounds__(kDhThreads, 1)
                             const uint32_t acc = (it > 0 || g > 0 || ks2 > 0) ? 1u : 0u;
                             const uint64_t ad = au + ((g * ZB + (ks2 / NKS) * ZCH + ks * 32) >> 4);
                             const uint64_t bd = bu + ((g * BW * RB + ks * 32) >> 4);
-                            mma_bf16(tbase, ad, bd, id0, acc);
-                            if (N1 > 0)
-                                mma_bf16(tbase + (uint32_t)N0, ad, bd + ((N0 * RB) >> 4), id1, acc);
+                            mma_bf16(dcol, ad, bd, id0, acc);
+                            if (NB1 > 0)
+                                mma_bf16(dcol + (uint32_t)NA, ad, bd + ((NA * RB) >> 4), id1, acc);
                         }
                     }
                 }
@@ -1924,9 +1937,9 @@ __global__ void __launch_bounds__(kDhThreads, 1)
             }
         }
         if (lane == 0)
-            mma_commit(bar_addr(c.drain[0]));
+            mma_commit(bar_addr(c.drain[mh]));
         __syncwarp();
-        mbar_wait_drain(bar_addr(c.drain[0]), 0);  // no MMA in flight at the dealloc
+        mbar_wait_drain(bar_addr(c.drain[mh]), 0);  // no MMA in flight at the dealloc
     } else {
         // ---------------------------------------------------------- builders
         // NB = 2 teams of kDhBuilders / 2 warps take turns at the units (team
@@ -1951,9 +1964,9 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         constexpr int NSLOT = (P * HS * (256 / FP) + NT_MIN - 1) / NT_MIN;
         static_assert(NCW % NCWH == 0, "rows of whole spans");
         const int FW = F / FP;  // feature blocks per row of W_k
-        const int tb = threadIdx.x - kDhFirstEpi * 32;  // 0 .. kDhBuilders * 32 - 1
+        const int tb = threadIdx.x - FIRST_B * 32;  // 0 .. kDhBuilders * 32 - 1
         const int team = tb / NT, tt = tb - team * NT;
-        const int q = warp & 3, sub = (warp - kDhFirstEpi) / 4;
+        const int q = warp & 3, sub = (warp - FIRST_B) / 4;
         float down = 1.f, up = 1.f;  // 2^-s, 2^s (fp16 operands)
         if (F16) {
             const uint32_t m = __ldg(a.wmax);
@@ -2095,9 +2108,10 @@ __global__ void __launch_bounds__(kDhThreads, 1)
         // the accumulator (lanes = samples, columns = the band's dh columns)
         // holds this CTA's partial: add it in, transposed through shared memory
         // (free once every MMA is done) so that the atomics run along dh rows
-        if (mbar_wait(bar_addr(c.drain[0]), 0, abort_flag, a.status) && !*abort_flag && it > 0) {
+        if (mbar_wait(bar_addr(c.drain[0]), 0, abort_flag, a.status) &&
+            (ISS < 2 || mbar_wait(bar_addr(c.drain[1]), 0, abort_flag, a.status)) && !*abort_flag && it > 0) {
             tc_fence_after();
-            float *tr = reinterpret_cast<float *>(base_ptr) + (size_t)(warp - kDhFirstEpi) * 33 * 32;
+            float *tr = reinterpret_cast<float *>(base_ptr) + (size_t)(warp - FIRST_B) * 33 * 32;
             const uint32_t lane_off = (uint32_t)(q * 32) << 16;
             for (int cs = sub; cs < BWT; cs += kDhBuilders / 4) {
                 for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -2561,6 +2575,13 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     SG_DH_PICK(1, 2, 1, true) SG_DH_PICK(1, 2, 2, true) SG_DH_PICK(1, 2, 3, true)
     SG_DH_PICK(1, 4, 1, true) SG_DH_PICK(1, 4, 2, true) SG_DH_PICK(1, 4, 3, true)
 #undef SG_DH_PICK
+    // two MMA-issuing warps where a unit's builders have little to do: the
+    // fp16 workspace at G = 32 with F <= 64 and 384-column bands (the LF-8.6M
+    // shape: dh 3 % faster; at F = 128 the second issuer measured 2-3 %
+    // slower)
+    const int iss = (dzt_f16 && lo->F <= 64 && nks == 2 && p.bwt == 3) ? 2 : 1;
+    if (iss == 2)
+        kern = k_tc_dh<1, 2, 3, true, 2>;
     if (!kern) {
         sg_set_error("tc_dh: no kernel for G = %d (subgroups of %d), band of %d columns", lo->G, p.gs, p.band_w);
         return SG_ERR_UNSUPPORTED;
@@ -2572,7 +2593,7 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
     if (!dzt_f16)  // the fused kernel that wrote the fp16 workspace cleared dh
         SG_TRY_CUDA(cudaMemsetAsync(dh, 0, sizeof(float) * B * lo->H, st));
     SG_LAUNCH(lo, SG_KIND_DH, st,
-              kern<<<p.nbands * p.MT * parts, kDhThreads, smem, st>>>(tm_z, tm_zl, a));
+              kern<<<p.nbands * p.MT * parts, dh_threads(iss), smem, st>>>(tm_z, tm_zl, a));
     SG_TRY_CUDA(cudaGetLastError());
     return SG_OK;
 }
