@@ -1959,9 +1959,12 @@ __global__ void __launch_bounds__(dh_threads(ISS), 1)
         const int NT = kDhBuilders * 32 / NB;  // threads of a team
         constexpr int NT_MIN = kDhBuilders * 32 / 2;
         constexpr int FP = G == 16 ? 2 : 1;                    // features per slot
-        constexpr int NCWH = FP == 2 ? 2 : G == 64 ? 4 : NCW;  // 16-byte units of a span
+        // G = 64: half rows; G = 32: whole rows, or half rows in the F <= 64
+        // instance (ISS = 2), whose F = 64 features left half the team idle
+        constexpr int NCWH = FP == 2 ? 2 : G == 64 ? 4 : ISS == 2 ? 2 : NCW;  // 16-byte units of a span
         constexpr int HS = NCW / NCWH;                         // spans per Ws row
-        constexpr int NSLOT = (P * HS * (256 / FP) + NT_MIN - 1) / NT_MIN;
+        constexpr int FMAX = ISS == 2 ? 64 : 256;  // the host takes ISS = 2 only for F <= 64
+        constexpr int NSLOT = (P * HS * (FMAX / FP) + NT_MIN - 1) / NT_MIN;
         static_assert(NCW % NCWH == 0, "rows of whole spans");
         const int FW = F / FP;  // feature blocks per row of W_k
         const int tb = threadIdx.x - FIRST_B * 32;  // 0 .. kDhBuilders * 32 - 1
