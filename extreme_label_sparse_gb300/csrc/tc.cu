@@ -377,18 +377,20 @@ __device__ __forceinline__ void drain_loads(Ctl &c, int issued, int S)
         mbar_wait_drain(bar_addr(c.full[i % S]), (uint32_t)(i / S) & 1u);
 }
 
-// sum of one double per thread over the epilogue threads (warps first_epi ..)
-__device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst, int first_epi)
+// sum of one double per thread over the nwarps (<= kEpiWarps) epilogue warps
+// first_epi ..; every thread of those warps calls it
+__device__ __forceinline__ void epi_sum_to(double v, Ctl &c, double *dst, int first_epi,
+                                           int nwarps = kEpiWarps)
 {
     for (int o = 16; o > 0; o >>= 1)
         v += __shfl_down_sync(0xffffffffu, v, o);
     const int ew = threadIdx.x / 32 - first_epi;
     if ((threadIdx.x & 31) == 0)
         c.red[ew] = v;
-    named_bar(1, kEpiWarps * 32);
+    named_bar(1, nwarps * 32);
     if (ew == 0 && (threadIdx.x & 31) == 0) {
         double s = 0.0;
-        for (int i = 0; i < kEpiWarps; ++i)
+        for (int i = 0; i < nwarps; ++i)
             s += c.red[i];
         *dst = s;
     }
@@ -1013,7 +1015,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // dh's fp16 scale.
 // Warps: the producers, one forward MMA warp, one dW MMA warp, eight BCE
 // warps and four dW warps.
-constexpr int kFWBce = 8;  // BCE warps: two per TMEM lane quarter
+// BCE warps, a multiple of the four TMEM lane quarters: eight in the plain
+// instance; four in the momentum-SGD one, whose dW warps (the update's loads
+// and stores of m and W) set its pace and gain the issue slots (SGD step
+// 1.886 -> 1.800 ms at 3M; the plain instance measured 16 % slower with four)
+__host__ __device__ constexpr int fw_bce(bool sgd) { return sgd ? 4 : 8; }
 constexpr int kFWDw = 4;   // dW store warps: one per lane quarter
 // Producer warps: four where a stage holds one 128-sample tile (eight
 // measured up to 4 % slower there: each producer warp's per-group costs of
@@ -1021,7 +1027,10 @@ constexpr int kFWDw = 4;   // dW store warps: one per lane quarter
 // rest), eight where it holds two (four: 2.4 % slower; twice the gather per
 // group).
 __host__ __device__ constexpr int fw_prod(int MT) { return MT > 1 ? 8 : 4; }
-__host__ __device__ constexpr int fw_threads(int MT) { return 32 * (fw_prod(MT) + 2 + kFWBce + kFWDw); }
+__host__ __device__ constexpr int fw_threads(int MT, bool sgd)
+{
+    return 32 * (fw_prod(MT) + 2 + fw_bce(sgd) + kFWDw);
+}
 // dynamic shared memory the fused plan may use (the opt-in maximum is 227 KB)
 constexpr int kFWBudget = 224 * 1024;
 
@@ -1209,10 +1218,12 @@ static __device__ __noinline__ void fw_loss_ticket(const double *part, double *l
 }
 
 template <int G_, int FK, int MT, bool SGD, bool PAIR = false, int TI = 1>
-__global__ void __launch_bounds__(fw_threads(MT), 1)
+__global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
 {
-    constexpr int NPW = fw_prod(MT), NTHR = fw_threads(MT), FIRST_EPI = NPW + 2;
+    constexpr int NPW = fw_prod(MT), NTHR = fw_threads(MT, SGD), FIRST_EPI = NPW + 2;
+    constexpr int NBCE = fw_bce(SGD), kBcePerQ = NBCE / 4;
+    static_assert(NBCE % 4 == 0 && NBCE <= kEpiWarps, "whole lane quarters");
     static_assert(!PAIR || MT == 1, "pairs share one 128-row sample tile");
     // compile-time group width: column chunk of the epilogue (with pairs,
     // half a layout group's columns, so that both BCE warps of a lane quarter
@@ -1251,12 +1262,12 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
         setup_ctl(c, S, 0, NPW * 32 + 1, NPW + 1);
         for (int i = 0; i < NS && i < 4; ++i) {
             mbar_init(bar_addr(c.tfull[i]), 1);
-            mbar_init(bar_addr(c.tempty[i]), kFWBce * 32);
+            mbar_init(bar_addr(c.tempty[i]), NBCE * 32);
             mbar_init(bar_addr(cf.wfull[i]), 1);
             mbar_init(bar_addr(cf.wempty[i]), kFWDw * 32);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(cf.dzfull[i]), kFWBce * 32);
+            mbar_init(bar_addr(cf.dzfull[i]), NBCE * 32);
             // freed by the dW MMA (commit)
             mbar_init(bar_addr(cf.dzempty[i]), 1);
             mbar_init(bar_addr(cf.wdrain[i]), 1);
@@ -1448,12 +1459,12 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
-        const int ew = warp - FIRST_EPI;  // BCE warps 0 .. kFWBce-1, then the dW warps
+        const int ew = warp - FIRST_EPI;  // BCE warps 0 .. NBCE-1, then the dW warps
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-        if (ew < kFWBce) {
+        if (ew < NBCE) {
             double lacc = 0.0;  // folded in from lf every 32 groups (fp64 is slow on this part)
             float lf = 0.f;
-            const int sub = ew / 4;  // two warps per lane quarter split the column units
+            const int sub = ew / 4;  // the kBcePerQ warps of a lane quarter split the column units
             // Z_k -> BCE -> dZ_k (workspace tile and shared memory for the dW MMA)
             constexpr int zunits = MT * (G / CH);
             // positive-list bounds of the group, loaded one group ahead (with
@@ -1507,7 +1518,9 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
                     const int ga = grp ? e1 : e0, gb = grp ? e2 : e1;
                     const int64_t kl = 2 * k + grp;
                     const int bz = q * 32 + lane, b = bz & 63;
-                    const int cl = sub * CH, c0 = grp * GL + cl;
+#pragma unroll
+                    for (int hc = sub; hc < 2; hc += kBcePerQ) {  // the two CH-column halves
+                    const int cl = hc * CH, c0 = grp * GL + cl;
                     float v[CH];
                     tmem_ld_chunk<CH>(tbase + lane_off + (uint32_t)(zs * a.zcols + c0), v);
                     if (b < a.B) {
@@ -1520,9 +1533,10 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
                     }
                     store_dz_tile<CH>(zs_smem, bz, c0, v, ZSW, NZC, 128);
                     store_dz_tile_f16<CH>(a.dZt + (size_t)kl * a.tile_bytes, b, cl, v, ZSW_L, 128);
+                    }
                 } else {
 #pragma unroll
-                for (int u = sub; u < zunits; u += 2) {
+                for (int u = sub; u < zunits; u += kBcePerQ) {
                     const int t = u / (G / CH), c0 = (u % (G / CH)) * CH;
                     const int b = t * 128 + q * 32 + lane;  // row of the item's tiles
                     const int bg = TI > 1 ? itm.ti * 128 + b : b;  // sample
@@ -1556,7 +1570,7 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
                     lf = 0.f;
                 }
             }
-            epi_sum_to(lacc + (double)lf, c, a.loss_part + blockIdx.x, FIRST_EPI);
+            epi_sum_to(lacc + (double)lf, c, a.loss_part + blockIdx.x, FIRST_EPI, NBCE);
             if (SGD) {
                 if (ew == 0 && a.loss)
                     fw_loss_ticket(a.loss_part, a.loss, a.ticket, lane);
@@ -1588,7 +1602,7 @@ __global__ void __launch_bounds__(fw_threads(MT), 1)
             // staged in shared memory as [j][f] and stored with one bulk copy.
             // The team leaves together: every named barrier below is then
             // reached by all of its warps or by none.
-            const int dw = ew - kFWBce;  // 0 .. kFWDw-1
+            const int dw = ew - NBCE;  // 0 .. kFWDw-1
             if (SGD) {
                 if (blockIdx.x == 0 && dw == 0 && lane == 0)
                     *a.wmax_next = 0u;
@@ -2401,7 +2415,7 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
-    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, fw_threads(p.MT), smem, st>>>(tm_w, a));
+    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, fw_threads(p.MT, sgd != nullptr), smem, st>>>(tm_w, a));
     SG_TRY_CUDA(cudaGetLastError());
     lo->wmax_slot = wslot;  // the slot the dh kernel reads
     return SG_OK;           // the kernel wrote the loss
