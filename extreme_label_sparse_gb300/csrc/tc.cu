@@ -1020,7 +1020,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // and stores of m and W) set its pace and gain the issue slots (SGD step
 // 1.886 -> 1.800 ms at 3M; the plain instance measured 16 % slower with four)
 __host__ __device__ constexpr int fw_bce(bool sgd) { return sgd ? 4 : 8; }
-constexpr int kFWDw = 4;   // dW store warps: one per lane quarter
+// dW store warps, a multiple of the four TMEM lane quarters: four, or eight
+// in the momentum-SGD instance, where they carry the update (two per lane
+// quarter on alternate column units: SGD step 1.798 -> 1.677 ms at 3M)
+__host__ __device__ constexpr int fw_dw(bool sgd) { return sgd ? 8 : 4; }
 // Producer warps: four where a stage holds one 128-sample tile (eight
 // measured up to 4 % slower there: each producer warp's per-group costs of
 // waits, index loads, the max |W| pass and arrivals took issue slots from the
@@ -1029,7 +1032,7 @@ constexpr int kFWDw = 4;   // dW store warps: one per lane quarter
 __host__ __device__ constexpr int fw_prod(int MT) { return MT > 1 ? 8 : 4; }
 __host__ __device__ constexpr int fw_threads(int MT, bool sgd)
 {
-    return 32 * (fw_prod(MT) + 2 + fw_bce(sgd) + kFWDw);
+    return 32 * (fw_prod(MT) + 2 + fw_bce(sgd) + fw_dw(sgd));
 }
 // dynamic shared memory the fused plan may use (the opt-in maximum is 227 KB)
 constexpr int kFWBudget = 224 * 1024;
@@ -1223,6 +1226,7 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
 {
     constexpr int NPW = fw_prod(MT), NTHR = fw_threads(MT, SGD), FIRST_EPI = NPW + 2;
     constexpr int NBCE = fw_bce(SGD), kBcePerQ = NBCE / 4;
+    constexpr int NDW = fw_dw(SGD), kDwPerQ = NDW / 4;
     static_assert(NBCE % 4 == 0 && NBCE <= kEpiWarps, "whole lane quarters");
     static_assert(!PAIR || MT == 1, "pairs share one 128-row sample tile");
     // compile-time group width: column chunk of the epilogue (with pairs,
@@ -1264,7 +1268,7 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
             mbar_init(bar_addr(c.tfull[i]), 1);
             mbar_init(bar_addr(c.tempty[i]), NBCE * 32);
             mbar_init(bar_addr(cf.wfull[i]), 1);
-            mbar_init(bar_addr(cf.wempty[i]), kFWDw * 32);
+            mbar_init(bar_addr(cf.wempty[i]), NDW * 32);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(cf.dzfull[i]), NBCE * 32);
@@ -1602,11 +1606,12 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
             // staged in shared memory as [j][f] and stored with one bulk copy.
             // The team leaves together: every named barrier below is then
             // reached by all of its warps or by none.
-            const int dw = ew - NBCE;  // 0 .. kFWDw-1
+            const int dw = ew - NBCE;  // 0 .. NDW-1
+            const int dsub = dw / 4;   // the kDwPerQ warps of a lane quarter split the column units
             if (SGD) {
                 if (blockIdx.x == 0 && dw == 0 && lane == 0)
                     *a.wmax_next = 0u;
-                for (int i = blockIdx.x * (kFWDw * 32) + dw * 32 + lane; i < a.dh_n; i += gridDim.x * (kFWDw * 32))
+                for (int i = blockIdx.x * (NDW * 32) + dw * 32 + lane; i < a.dh_n; i += gridDim.x * (NDW * 32))
                     a.dh_zero[i] = 0.f;
             }
             constexpr int wunits = ((FK + 7) / 8) * (G / CH);
@@ -1624,6 +1629,8 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
                     for (int r = lane; r < G; r += 32) {
 #pragma unroll
                         for (int tf = 0; tf < (FK + 7) / 8; ++tf) {
+                            if ((tf * (G / CH) + r / CH) % kDwPerQ != dsub)
+                                continue;  // another warp's column unit
                             const int64_t e = (k * G + r) * (int64_t)F + tf * 128 + q * 32;
                             prefetch_l2(a.mom + e);
                             prefetch_l2(a.W + e);
@@ -1631,7 +1638,7 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
                     }
                 }
                 FW_TRACE(1, it);
-                if (named_bar_any(2, kFWDw * 32,
+                if (named_bar_any(2, NDW * 32,
                                   !mbar_wait(bar_addr(cf.wfull[ws]), rw.ph, abort_flag, a.status)))
                     break;
                 FW_TRACE(2, it);
@@ -1639,9 +1646,9 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
                 // the staging buffer's store of two groups ago has read it
                 if (dw == 0 && lane == 0)
                     bulk_wait_read<1>();
-                named_bar(2, kFWDw * 32);
+                named_bar(2, NDW * 32);
 #pragma unroll 1
-                for (int u = 0; u < wunits; ++u) {
+                for (int u = dsub; u < wunits; u += kDwPerQ) {
                     const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
                     const int f = tf * 128 + q * 32 + lane;
                     const uint32_t col = tbase + lane_off + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G + c0);
@@ -1674,7 +1681,7 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
                 tc_fence_before();
                 mbar_arrive(bar_addr(cf.wempty[ws]));
                 fence_proxy_async();  // staged dW_k -> the bulk store (async proxy)
-                named_bar(2, kFWDw * 32);
+                named_bar(2, NDW * 32);
                 if (dw == 0 && lane == 0) {
                     bulk_store(a.dW + k * G * F, stg0 + (uint32_t)wb * a.stg_bytes, a.stg_bytes);
                     bulk_commit();
