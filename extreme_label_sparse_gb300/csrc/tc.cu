@@ -1027,12 +1027,17 @@ __host__ __device__ constexpr int fw_dw(bool sgd) { return sgd ? 8 : 4; }
 // Producer warps: four where a stage holds one 128-sample tile (eight
 // measured up to 4 % slower there: each producer warp's per-group costs of
 // waits, index loads, the max |W| pass and arrivals took issue slots from the
-// rest), eight where it holds two (four: 2.4 % slower; twice the gather per
-// group).
-__host__ __device__ constexpr int fw_prod(int MT) { return MT > 1 ? 8 : 4; }
-__host__ __device__ constexpr int fw_threads(int MT, bool sgd)
+// rest; two, 10 % slower), eight where it holds two (four: 2.4 % slower;
+// twice the gather per group); two in the momentum-SGD instance at F <= 128
+// (its update-bound dW warps gain the issue slots: SGD step 1.677 -> 1.590
+// ms at 3M).
+__host__ __device__ constexpr int fw_prod(int MT, int FK, bool sgd)
 {
-    return 32 * (fw_prod(MT) + 2 + fw_bce(sgd) + fw_dw(sgd));
+    return MT > 1 ? 8 : (sgd && FK <= 8) ? 2 : 4;
+}
+__host__ __device__ constexpr int fw_threads(int MT, bool sgd, int FK)
+{
+    return 32 * (fw_prod(MT, FK, sgd) + 2 + fw_bce(sgd) + fw_dw(sgd));
 }
 // dynamic shared memory the fused plan may use (the opt-in maximum is 227 KB)
 constexpr int kFWBudget = 224 * 1024;
@@ -1221,10 +1226,10 @@ static __device__ __noinline__ void fw_loss_ticket(const double *part, double *l
 }
 
 template <int G_, int FK, int MT, bool SGD, bool PAIR = false, int TI = 1>
-__global__ void __launch_bounds__(fw_threads(MT, SGD), 1)
+__global__ void __launch_bounds__(fw_threads(MT, SGD, FK), 1)
     k_tc_fwdw(const __grid_constant__ CUtensorMap tm_w, const FWArgs a)
 {
-    constexpr int NPW = fw_prod(MT), NTHR = fw_threads(MT, SGD), FIRST_EPI = NPW + 2;
+    constexpr int NPW = fw_prod(MT, FK, SGD), NTHR = fw_threads(MT, SGD, FK), FIRST_EPI = NPW + 2;
     constexpr int NBCE = fw_bce(SGD), kBcePerQ = NBCE / 4;
     constexpr int NDW = fw_dw(SGD), kDwPerQ = NDW / 4;
     static_assert(NBCE % 4 == 0 && NBCE <= kEpiWarps, "whole lane quarters");
@@ -2422,7 +2427,8 @@ sg_status tc_fwdw(sg_layout *lo, int32_t B, const uint16_t *W, uint8_t *dZt, uin
     rc = set_smem(kern, smem);
     if (rc != SG_OK)
         return rc;
-    SG_LAUNCH(lo, SG_KIND_FWD, st, kern<<<grid, fw_threads(p.MT, sgd != nullptr), smem, st>>>(tm_w, a));
+    SG_LAUNCH(lo, SG_KIND_FWD, st,
+              kern<<<grid, fw_threads(p.MT, sgd != nullptr, lo->F / 16), smem, st>>>(tm_w, a));
     SG_TRY_CUDA(cudaGetLastError());
     lo->wmax_slot = wslot;  // the slot the dh kernel reads
     return SG_OK;           // the kernel wrote the loss
