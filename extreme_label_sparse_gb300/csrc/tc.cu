@@ -1020,10 +1020,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // and stores of m and W) set its pace and gain the issue slots (SGD step
 // 1.886 -> 1.800 ms at 3M; the plain instance measured 16 % slower with four)
 __host__ __device__ constexpr int fw_bce(bool sgd) { return sgd ? 4 : 8; }
-// dW store warps, a multiple of the four TMEM lane quarters: four, or eight
-// in the momentum-SGD instance, where they carry the update (two per lane
-// quarter on alternate column units: SGD step 1.798 -> 1.677 ms at 3M)
-__host__ __device__ constexpr int fw_dw(bool sgd) { return sgd ? 8 : 4; }
+// dW store warps, a multiple of the four TMEM lane quarters: four, or
+// sixteen in the momentum-SGD instance, where they carry the update (four
+// per lane quarter on 8-column units; SGD step at 3M 1.798 ms with four,
+// 1.677 with eight, then 1.576 -> 1.551 ms from eight to sixteen)
+__host__ __device__ constexpr int fw_dw(bool sgd) { return sgd ? 16 : 4; }
 // Producer warps: four where a stage holds one 128-sample tile (eight
 // measured up to 4 % slower there: each producer warp's per-group costs of
 // waits, index loads, the max |W| pass and arrivals took issue slots from the
@@ -1619,7 +1620,10 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD, FK), 1)
                 for (int i = blockIdx.x * (NDW * 32) + dw * 32 + lane; i < a.dh_n; i += gridDim.x * (NDW * 32))
                     a.dh_zero[i] = 0.f;
             }
-            constexpr int wunits = ((FK + 7) / 8) * (G / CH);
+            // columns of a dW epilogue unit: CH, or 8 where four dW warps share
+            // a lane quarter
+            constexpr int CHW = kDwPerQ > 2 ? 8 : CH;
+            constexpr int wunits = ((FK + 7) / 8) * (G / CHW);
             int it = 0;
             Ring rw;
             for (int64_t k = blockIdx.x; k < a.K; k += gridDim.x, ++it, rw.next(NS)) {
@@ -1634,7 +1638,7 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD, FK), 1)
                     for (int r = lane; r < G; r += 32) {
 #pragma unroll
                         for (int tf = 0; tf < (FK + 7) / 8; ++tf) {
-                            if ((tf * (G / CH) + r / CH) % kDwPerQ != dsub)
+                            if ((tf * (G / CHW) + r / CHW) % kDwPerQ != dsub)
                                 continue;  // another warp's column unit
                             const int64_t e = (k * G + r) * (int64_t)F + tf * 128 + q * 32;
                             prefetch_l2(a.mom + e);
@@ -1654,31 +1658,31 @@ __global__ void __launch_bounds__(fw_threads(MT, SGD, FK), 1)
                 named_bar(2, NDW * 32);
 #pragma unroll 1
                 for (int u = dsub; u < wunits; u += kDwPerQ) {
-                    const int tf = u / (G / CH), c0 = (u % (G / CH)) * CH;
+                    const int tf = u / (G / CHW), c0 = (u % (G / CHW)) * CHW;
                     const int f = tf * 128 + q * 32 + lane;
                     const uint32_t col = tbase + lane_off + wbase + (uint32_t)(ws * a.wcols + tf * 2 * G + c0);
-                    float v[CH], w[CH];
-                    tmem_ld_chunk2<CH>(col, col + (uint32_t)G, v, w);
+                    float v[CHW], w[CHW];
+                    tmem_ld_chunk2<CHW>(col, col + (uint32_t)G, v, w);
                     if (SGD && f < F) {
                         // the optimiser step on dW while it is in registers
                         // (lanes run along f: coalesced rows of m and W)
                         const int64_t e0 = (k * G + c0) * (int64_t)F + f;
-                        float mv[CH];
-                        uint16_t wv[CH];
+                        float mv[CHW];
+                        uint16_t wv[CHW];
 #pragma unroll
-                        for (int i = 0; i < CH; ++i) {
+                        for (int i = 0; i < CHW; ++i) {
                             mv[i] = a.mom[e0 + (int64_t)i * F];
                             wv[i] = __ldg(a.W + e0 + (int64_t)i * F);
                         }
 #pragma unroll
-                        for (int i = 0; i < CH; ++i) {
+                        for (int i = 0; i < CHW; ++i) {
                             const float m = fmaf(a.mu, mv[i], v[i] + w[i]);
                             a.mom[e0 + (int64_t)i * F] = m;
                             stg[(c0 + i) * F + f] = bf16_rn(__uint_as_float((uint32_t)wv[i] << 16) - a.lr * m);
                         }
                     } else if (f < F) {
 #pragma unroll
-                        for (int i = 0; i < CH; ++i)
+                        for (int i = 0; i < CHW; ++i)
                             stg[(c0 + i) * F + f] = bf16_rn(v[i] + w[i]);
                     }
                 }
