@@ -1805,7 +1805,7 @@ __device__ __forceinline__ void read_w_pair(const uint32_t *Wp, int F2, float do
     }
 }
 
-template <int NPASS, int NKS, int BWT, bool F16, int ISS = 1>
+template <int NPASS, int NKS, int BWT, bool F16, int ISS = 1, int FMX = 256>
 __global__ void __launch_bounds__(dh_threads(ISS), 1)
     k_tc_dh(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_zl,
             const DhArgs a)
@@ -1990,11 +1990,10 @@ __global__ void __launch_bounds__(dh_threads(ISS), 1)
         constexpr int NT_MIN = kDhBuilders * 32 / 2;
         constexpr int FP = G == 16 ? 2 : 1;                    // features per slot
         // G = 64: half rows; G = 32: whole rows, or half rows in the F <= 64
-        // instance (ISS = 2), whose F = 64 features left half the team idle
-        constexpr int NCWH = FP == 2 ? 2 : G == 64 ? 4 : ISS == 2 ? 2 : NCW;  // 16-byte units of a span
+        // instance (FMX = 64), whose F = 64 features left half the team idle
+        constexpr int NCWH = FP == 2 ? 2 : G == 64 ? 4 : FMX <= 64 ? 2 : NCW;  // 16-byte units of a span
         constexpr int HS = NCW / NCWH;                         // spans per Ws row
-        constexpr int FMAX = ISS == 2 ? 64 : 256;  // the host takes ISS = 2 only for F <= 64
-        constexpr int NSLOT = (P * HS * (FMAX / FP) + NT_MIN - 1) / NT_MIN;
+        constexpr int NSLOT = (P * HS * (FMX / FP) + NT_MIN - 1) / NT_MIN;  // the host keeps F <= FMX
         static_assert(NCW % NCWH == 0, "rows of whole spans");
         const int FW = F / FP;  // feature blocks per row of W_k
         const int tb = threadIdx.x - FIRST_B * 32;  // 0 .. kDhBuilders * 32 - 1
@@ -2611,11 +2610,12 @@ sg_status tc_dh(sg_layout *lo, const uint16_t *dZ, const uint16_t *dZ_lo, const 
 #undef SG_DH_PICK
     // two MMA-issuing warps where a unit's builders have little to do: the
     // fp16 workspace at G = 32 with F <= 64 and 384-column bands (the LF-8.6M
-    // shape: dh 3 % faster; at F = 128 the second issuer measured 2-3 %
-    // slower)
+    // shape: dh 1.011 -> 0.944 ms together with the half-row builders of
+    // FMX = 64; at F = 128 the second issuer measured 1-3 % slower, also
+    // after the builders got cheaper)
     const int iss = (dzt_f16 && lo->F <= 64 && nks == 2 && p.bwt == 3) ? 2 : 1;
     if (iss == 2)
-        kern = k_tc_dh<1, 2, 3, true, 2>;
+        kern = k_tc_dh<1, 2, 3, true, 2, 64>;  // FMX = 64: rows in halves, slots for F <= 64
     if (!kern) {
         sg_set_error("tc_dh: no kernel for G = %d (subgroups of %d), band of %d columns", lo->G, p.gs, p.band_w);
         return SG_ERR_UNSUPPORTED;
